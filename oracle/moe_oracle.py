@@ -1,0 +1,389 @@
+"""CPU oracle for one Mixture-of-Experts layer, forward and backward, in float64.
+
+TEST INFRASTRUCTURE ONLY. The library never imports, links or runs this file;
+only the test suite, the smoke check and the benchmark's CPU-baseline / reference
+arm do. It shares no code with the CUDA path.
+
+Sources. The layer is the one described in the Mixture-of-Kittens articles:
+  [KC] "O MoK do Cursor alcanca aumento de desempenho de 2,37x no NVIDIA GB300 NVL72"
+       (kucoin.com), sections 01 (count, place, group the tokens of each expert),
+       02 (pull dispatch / push combine, minibatch, ring buffer, fused MXFP8
+       quantisation) and 03 (stages: Schedule, Dispatch, Expert FFN, Combine and
+       the final weighted fusion);
+  [NI] "Cursor abre codigo do Mixture-of-Kittens ..." (noticiai.com.br), sections
+       "O que e" (a single deterministic kernel) and "As tres decisoes de design"
+       (no token dropping, ring traversal, macrobatch interleave);
+  [DD] the deepdigest.ru digest of the same work (mirrored backward directions).
+The pages name the stages but print no formula. Where they are silent the
+oracle takes the plain reading of a softmax top-k MoE with SwiGLU experts:
+  logits = x W_r + bias;  p = softmax(logits);  top-k of p, ties to the lower
+  expert index;  w = p_sel / sum(p_sel);
+  y = sum_j w_j * W2_e(silu(x W1_e) * (x W3_e)),  silu(a) = a * sigmoid(a).
+
+Parity pins: every function here is pinned by tests/test_oracle_*.py against
+brute force, closed forms, special cases and finite differences (see each test).
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import numpy as np
+
+# --------------------------------------------------------------------------
+# number formats
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) -> float64 values (exact)."""
+    u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+# OCP MX FP8 E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits; no infinity;
+# S.1111.111 is NaN, so the largest finite magnitude is 1.75 * 2^8 = 448.
+E4M3_MAX = 448.0
+E4M3_EMAX = 8          # exponent of the largest normal binade
+E4M3_EMIN = -6         # exponent of the smallest normal binade
+E4M3_MBITS = 3
+
+
+def e4m3_round(v: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest E4M3 value (ties to even), saturating
+    finite values beyond 448 to +-448. Returns float64 holding E4M3 values."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    # binade exponent of each value, clamped to the subnormal binade
+    with np.errstate(divide="ignore"):
+        ex = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    ex = np.clip(ex, E4M3_EMIN, E4M3_EMAX)
+    quantum = np.exp2(ex - E4M3_MBITS)            # spacing of E4M3 values in that binade
+    q = np.round(a / quantum) * quantum           # np.round is half-to-even
+    q = np.minimum(q, E4M3_MAX)
+    return np.copysign(q, v)
+
+
+def e4m3_encode(q: np.ndarray) -> np.ndarray:
+    """Exact E4M3 values (float64) -> E4M3 bytes."""
+    q = np.asarray(q, dtype=np.float64)
+    sign = (np.signbit(q)).astype(np.uint8) << 7
+    a = np.abs(q)
+    code = np.zeros(a.shape, dtype=np.uint8)
+    nz = a > 0
+    with np.errstate(divide="ignore"):
+        ex = np.floor(np.log2(np.where(nz, a, 1.0))).astype(np.int64)
+    normal = nz & (ex >= E4M3_EMIN)
+    # normal: (1 + m/8) * 2^ex, biased exponent ex + 7
+    m_norm = np.round((a / np.exp2(ex.astype(np.float64)) - 1.0) * 8).astype(np.int64)
+    code = np.where(normal, ((ex + 7) << 3) | m_norm, code)
+    # subnormal: (m/8) * 2^-6
+    sub = nz & ~normal
+    m_sub = np.round(a / 2.0 ** (E4M3_EMIN - E4M3_MBITS)).astype(np.int64)
+    code = np.where(sub, m_sub, code)
+    return code.astype(np.uint8) | sign
+
+
+def e4m3_decode(code: np.ndarray) -> np.ndarray:
+    c = np.asarray(code, dtype=np.uint8).astype(np.int64)
+    s = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(e == 0, m / 8.0 * 2.0 ** E4M3_EMIN, (1 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where((c & 0x7F) == 0x7F, np.nan, val)
+    return s * val
+
+
+MX_BLOCK = 32
+
+
+def mx_scale_exponent(amax: np.ndarray) -> np.ndarray:
+    """Shared block exponent s: the smallest integer with amax <= 448 * 2^s, so
+    the block's largest element never saturates; clamped to [-127, 127];
+    an all-zero block gets s = -127 (E8M0 byte 0x00)."""
+    amax = np.asarray(amax, dtype=np.float64)
+    s = np.full(amax.shape, -127, dtype=np.int64)
+    nz = amax > 0
+    mant, ex = np.frexp(np.where(nz, amax, 1.0))   # amax = mant * 2^ex, mant in [0.5, 1)
+    # 448 = 0.875 * 2^9: amax <= 0.875 * 2^(9+s)  <=>  s >= ex - 9 (+1 if mant > 0.875)
+    cand = ex - 9 + (mant > 0.875)
+    s = np.where(nz, np.clip(cand, -127, 127), s)
+    return s
+
+
+def mx_quantize(v: np.ndarray, axis: int):
+    """MXFP8 quantisation: blocks of 32 consecutive elements along `axis`
+    (length must be a multiple of 32). Returns (e4m3 bytes, e8m0 bytes); the
+    scale tensor has the axis shortened 32-fold. [KC] section 02 places this
+    quantisation inside dispatch, the grouped GEMM and SwiGLU."""
+    v = np.moveaxis(np.asarray(v, dtype=np.float64), axis, -1)
+    n = v.shape[-1]
+    assert n % MX_BLOCK == 0, "MX blocks need a multiple of 32 elements"
+    blk = v.reshape(v.shape[:-1] + (n // MX_BLOCK, MX_BLOCK))
+    s = mx_scale_exponent(np.abs(blk).max(axis=-1))
+    q = e4m3_round(blk * np.exp2(-s.astype(np.float64))[..., None])
+    codes = e4m3_encode(q).reshape(v.shape)
+    scales = (s + 127).astype(np.uint8)
+    return np.moveaxis(codes, -1, axis), np.moveaxis(scales, -1, axis)
+
+
+def mx_dequantize(codes: np.ndarray, scales: np.ndarray, axis: int) -> np.ndarray:
+    c = np.moveaxis(codes, axis, -1)
+    s = np.moveaxis(scales, axis, -1).astype(np.float64) - 127.0
+    vals = e4m3_decode(c).reshape(c.shape[:-1] + (c.shape[-1] // MX_BLOCK, MX_BLOCK))
+    out = (vals * np.exp2(s)[..., None]).reshape(c.shape)
+    return np.moveaxis(out, -1, axis)
+
+
+def mx_roundtrip(v: np.ndarray, axis: int) -> np.ndarray:
+    """Quantise to MXFP8 along `axis` and return the represented values."""
+    c, s = mx_quantize(v, axis)
+    return mx_dequantize(c, s, axis)
+
+
+def mx_roundtrip_segments(v: np.ndarray, seg_starts, seg_ends) -> np.ndarray:
+    """MXFP8 along axis 0 (the token axis of sorted rows) where 32-row blocks
+    start at each segment start and never cross a segment end; a short last
+    block is padded with zero rows, which do not change its amax."""
+    out = np.zeros_like(np.asarray(v, dtype=np.float64))
+    for s0, s1 in zip(seg_starts, seg_ends):
+        n = s1 - s0
+        if n == 0:
+            continue
+        npad = -(-n // MX_BLOCK) * MX_BLOCK
+        blk = np.zeros((npad,) + v.shape[1:], dtype=np.float64)
+        blk[:n] = v[s0:s1]
+        out[s0:s1] = mx_roundtrip(blk, 0)[:n]
+    return out
+
+
+# --------------------------------------------------------------------------
+# router ([KC] section 01: the router picks each token's experts at every step)
+
+
+def router(x: np.ndarray, Wr: np.ndarray, bias: Optional[np.ndarray], k: int):
+    """Softmax over all E experts, top-k by descending probability with ties
+    going to the lower expert index, weights renormalised over the chosen k.
+    Returns dict(logits, probs, ids [T,k] int32, w [T,k])."""
+    logits = np.asarray(x, np.float64) @ np.asarray(Wr, np.float64)
+    if bias is not None:
+        logits = logits + np.asarray(bias, np.float64)[None, :]
+    z = logits - logits.max(axis=1, keepdims=True)
+    ez = np.exp(z)
+    p = ez / ez.sum(axis=1, keepdims=True)
+    order = np.argsort(-p, axis=1, kind="stable")   # stable: equal p keep index order
+    ids = order[:, :k].astype(np.int32)
+    psel = np.take_along_axis(p, ids, axis=1)
+    w = psel / psel.sum(axis=1, keepdims=True)
+    return {"logits": logits, "probs": p, "ids": ids, "w": w}
+
+
+def topk_margin(logits: np.ndarray, k: int) -> np.ndarray:
+    """Gap between the k-th and (k+1)-th largest logit of each token (inf if k=E).
+    Tokens with a tiny gap may legitimately select a different set on the GPU."""
+    E = logits.shape[1]
+    if k >= E:
+        return np.full(logits.shape[0], np.inf)
+    s = -np.sort(-logits, axis=1)
+    return s[:, k - 1] - s[:, k]
+
+
+# --------------------------------------------------------------------------
+# schedule ([KC] section 01: count each expert's tokens, decide where they go,
+# group the same expert's rows so the grouped GEMM gets ordered input;
+# [KC] section 02 / [NI] design decision 3: macrobatches of tokens cycle through
+# a fixed ring buffer)
+
+
+def num_macrobatches(T: int, macrobatch_tokens: int) -> int:
+    return max(1, -(-T // macrobatch_tokens)) if macrobatch_tokens > 0 else 1
+
+
+def schedule(ids: np.ndarray, E: int, macrobatch_tokens: int = 0):
+    """Stable sort of routed slots s = t*k + j by the key (m, e) with
+    m = t // macrobatch_tokens (m = 0 when macrobatch_tokens is 0).
+    Returns dict(counts [nM,E], offsets [nM,E+1] (absolute sorted positions),
+    sorted_to_slot [R], slot_to_sorted [R]) as int32."""
+    T, k = ids.shape
+    R = T * k
+    Mb = macrobatch_tokens if macrobatch_tokens > 0 else max(T, 1)
+    nM = num_macrobatches(T, macrobatch_tokens)
+    slot = np.arange(R, dtype=np.int64)
+    m = (slot // k) // Mb
+    key = m * E + ids.reshape(-1).astype(np.int64)
+    sorted_to_slot = np.argsort(key, kind="stable")
+    slot_to_sorted = np.empty(R, dtype=np.int64)
+    slot_to_sorted[sorted_to_slot] = np.arange(R)
+    counts = np.bincount(key, minlength=nM * E).reshape(nM, E)
+    flat = np.concatenate([[0], np.cumsum(counts.reshape(-1))])
+    offsets = np.empty((nM, E + 1), dtype=np.int64)
+    for mm in range(nM):
+        offsets[mm, :E] = flat[mm * E:(mm + 1) * E]
+        offsets[mm, E] = flat[(mm + 1) * E]
+    return {
+        "counts": counts.astype(np.int32),
+        "offsets": offsets.astype(np.int32),
+        "sorted_to_slot": sorted_to_slot.astype(np.int32),
+        "slot_to_sorted": slot_to_sorted.astype(np.int32),
+    }
+
+
+def expert_segments(sched):
+    """(expert, start, end) of every non-empty (macrobatch, expert) run of sorted rows."""
+    segs = []
+    off = sched["offsets"]
+    for mm in range(off.shape[0]):
+        for e in range(off.shape[1] - 1):
+            if off[mm, e + 1] > off[mm, e]:
+                segs.append((e, int(off[mm, e]), int(off[mm, e + 1])))
+    return segs
+
+
+# --------------------------------------------------------------------------
+# expert FFN and combine
+
+
+def silu(a):
+    return a / (1.0 + np.exp(-a))
+
+
+def sigmoid(a):
+    return 1.0 / (1.0 + np.exp(-a))
+
+
+def forward(x, Wr, bias, W1, W3, W2, k, *, precision="bf16", macrobatch_tokens=0, ids=None):
+    """One MoE layer forward over T tokens ([KC] section 03: Schedule, Dispatch,
+    Expert FFN, Combine, final weighted fusion).
+
+    x [T,H], Wr [H,E], W1/W3 [E,H,F], W2 [E,F,H] as float64 (or bf16 bits decoded
+    by the caller). `ids` overrides the router's choice (used where GPU and
+    oracle sit on a near-tie). precision "mxfp8" emulates MXFP8 operands of both
+    GEMMs: x and W1/W3 along H, h and W2 along F ([KC] section 02).
+    Returns a dict with out [T,H] and every saved intermediate."""
+    x = np.asarray(x, np.float64)
+    T, H = x.shape
+    E = Wr.shape[1]
+    r = router(x, Wr, bias, k)
+    if ids is not None:
+        r["ids"] = np.asarray(ids, np.int32)
+        psel = np.take_along_axis(r["probs"], r["ids"], axis=1)
+        r["w"] = psel / psel.sum(axis=1, keepdims=True)
+    sch = schedule(r["ids"], E, macrobatch_tokens)
+    R = T * k
+    tok = sch["sorted_to_slot"].astype(np.int64) // k          # token of each sorted row
+    Xs = x[tok]                                                 # dispatch: gather ([KC] section 02, pull)
+    F = W1.shape[2]
+    a = np.zeros((R, F)); b = np.zeros((R, F)); h = np.zeros((R, F)); Y = np.zeros((R, H))
+    mx = precision == "mxfp8"
+    for e, s0, s1 in expert_segments(sch):
+        Xe = Xs[s0:s1]
+        W1e, W3e, W2e = (np.asarray(W[e], np.float64) for W in (W1, W3, W2))
+        if mx:
+            Xe = mx_roundtrip(Xe, 1)
+            W1e = mx_roundtrip(W1e, 0)
+            W3e = mx_roundtrip(W3e, 0)
+            W2e = mx_roundtrip(W2e, 0)
+        a[s0:s1] = Xe @ W1e
+        b[s0:s1] = Xe @ W3e
+        h[s0:s1] = silu(a[s0:s1]) * b[s0:s1]
+        he = mx_roundtrip(h[s0:s1], 1) if mx else h[s0:s1]
+        Y[s0:s1] = he @ W2e
+    # combine: fixed j order per token ([NI] "O que e": deterministic)
+    out = np.zeros((T, H))
+    s2s = sch["slot_to_sorted"].reshape(T, k)
+    for j in range(k):
+        out += r["w"][:, j:j + 1] * Y[s2s[:, j]]
+    return {"out": out, **r, **sch, "Xs": Xs, "a": a, "b": b, "h": h, "Y": Y,
+            "tok": tok, "precision": precision}
+
+
+def backward(fwd, dout, x, Wr, W1, W3, W2):
+    """Gradients of sum(dout * out) with the top-k selection held fixed; the
+    router bias is a constant input. Mirrors the forward ([KC] section 02:
+    reverse-combine, then reverse-dispatch, [DD]).
+    Returns dict(dx [T,H], dWr [H,E], dW1, dW3 [E,H,F], dW2 [E,F,H], dw [T,k],
+    dlogits [T,E])."""
+    dout = np.asarray(dout, np.float64)
+    x = np.asarray(x, np.float64)
+    T, H = x.shape
+    E = Wr.shape[1]
+    k = fwd["ids"].shape[1]
+    F = W1.shape[2]
+    R = T * k
+    mx = fwd["precision"] == "mxfp8"
+    tok = fwd["tok"]
+    slot = fwd["sorted_to_slot"].astype(np.int64)
+    wrow = fwd["w"].reshape(-1)[slot]                 # weight of each sorted row
+    Gin = dout[tok]                                   # reverse combine: gather dout rows
+    a, b, h, Xs = fwd["a"], fwd["b"], fwd["h"], fwd["Xs"]
+    dX = np.zeros((R, H))
+    dwrow = np.zeros(R)
+    dW1 = np.zeros((E, H, F)); dW3 = np.zeros((E, H, F)); dW2 = np.zeros((E, F, H))
+    da_all = np.zeros((R, F)); db_all = np.zeros((R, F)); hw_all = np.zeros((R, F))
+    segs = expert_segments(fwd)
+    for e, s0, s1 in segs:
+        W1e, W3e, W2e = (np.asarray(W[e], np.float64) for W in (W1, W3, W2))
+        Ge = Gin[s0:s1]
+        if mx:
+            G = mx_roundtrip(Ge, 1) @ mx_roundtrip(W2e, 1).T     # K = H
+        else:
+            G = Ge @ W2e.T
+        ae, be, he = a[s0:s1], b[s0:s1], h[s0:s1]
+        dwrow[s0:s1] = np.sum(G * he, axis=1)
+        dh = wrow[s0:s1, None] * G
+        sg = sigmoid(ae)
+        da = dh * be * sg * (1.0 + ae * (1.0 - sg))
+        db = dh * ae * sg
+        da_all[s0:s1] = da; db_all[s0:s1] = db
+        hw_all[s0:s1] = wrow[s0:s1, None] * he
+        if mx:
+            dX[s0:s1] = (mx_roundtrip(da, 1) @ mx_roundtrip(W1e, 1).T
+                         + mx_roundtrip(db, 1) @ mx_roundtrip(W3e, 1).T)      # K = F
+        else:
+            dX[s0:s1] = da @ W1e.T + db @ W3e.T
+    # weight gradients: contraction over each expert's rows (token axis)
+    for e in range(E):
+        es = [(s0, s1) for ee, s0, s1 in segs if ee == e]
+        if not es:
+            continue
+        idx = np.concatenate([np.arange(s0, s1) for s0, s1 in es])
+        starts, ends = [], []
+        pos = 0
+        for s0, s1 in es:
+            starts.append(pos); pos += s1 - s0; ends.append(pos)
+        Xe, dae, dbe, hwe, Ge = Xs[idx], da_all[idx], db_all[idx], hw_all[idx], Gin[idx]
+        if mx:
+            q = lambda v: mx_roundtrip_segments(v, starts, ends)
+            Xe, dae, dbe, hwe, Ge = q(Xe), q(dae), q(dbe), q(hwe), q(Ge)
+        dW1[e] = Xe.T @ dae
+        dW3[e] = Xe.T @ dbe
+        dW2[e] = hwe.T @ Ge
+    # reverse dispatch: sum each token's k rows in fixed j order
+    dx = np.zeros((T, H))
+    s2s = fwd["slot_to_sorted"].reshape(T, k)
+    for j in range(k):
+        dx += dX[s2s[:, j]]
+    # router backward
+    dw = dwrow[fwd["slot_to_sorted"]].reshape(T, k)
+    p = fwd["probs"]
+    ids = fwd["ids"].astype(np.int64)
+    psel = np.take_along_axis(p, ids, axis=1)
+    S = psel.sum(axis=1, keepdims=True)
+    wsel = fwd["w"]
+    dpsel = (dw - np.sum(wsel * dw, axis=1, keepdims=True)) / S
+    dp = np.zeros_like(p)
+    np.put_along_axis(dp, ids, dpsel, axis=1)
+    dlogits = p * (dp - np.sum(p * dp, axis=1, keepdims=True))
+    dx += dlogits @ np.asarray(Wr, np.float64).T
+    dWr = x.T @ dlogits
+    return {"dx": dx, "dWr": dWr, "dW1": dW1, "dW3": dW3, "dW2": dW2, "dw": dw,
+            "dlogits": dlogits, "da": da_all, "db": db_all}
+
+
+def max_abs_rel(got: np.ndarray, ref: np.ndarray) -> float:
+    """max |got - ref| / max |ref| over a whole tensor (0 when both are zero)."""
+    got = np.asarray(got, np.float64); ref = np.asarray(ref, np.float64)
+    den = np.max(np.abs(ref)) if ref.size else 0.0
+    num = np.max(np.abs(got - ref)) if ref.size else 0.0
+    if den == 0.0:
+        return float(num)
+    return float(num / den)

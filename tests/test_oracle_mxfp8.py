@@ -1,0 +1,129 @@
+"""Pins of the oracle's MXFP8 quantiser: golden E4M3 codes from the OCP MX
+specification, an exhaustive nearest-value search over all 256 codes, closed
+forms for the shared scale, and the error bound of the emulated layer."""
+import os
+
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "e4m3_codes.txt")
+
+
+def load_golden():
+    rows = []
+    for line in open(GOLDEN):
+        line = line.split("#")[0].strip()
+        if line:
+            v, c = line.split()
+            rows.append((float(v), int(c, 16)))
+    return rows
+
+
+def test_e4m3_golden_codes():
+    for v, code in load_golden():
+        q = O.e4m3_round(np.array([v]))
+        assert O.e4m3_encode(q)[0] == code, (v, hex(code), hex(O.e4m3_encode(q)[0]))
+
+
+def e4m3_table():
+    """All finite E4M3 values, built from the bit-field definition."""
+    vals = {}
+    for c in range(256):
+        s = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 0xF, c & 7
+        if e == 0xF and m == 7:
+            continue
+        vals[c] = s * ((m / 8) * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+    return vals
+
+
+def test_e4m3_round_matches_exhaustive_nearest_even():
+    table = e4m3_table()
+    pos = sorted((v, c) for c, v in table.items() if v >= 0 and not (v == 0 and c == 0x80))
+    rng = np.random.default_rng(0)
+    samples = np.concatenate([
+        rng.uniform(0, 460, 3000), 2.0 ** rng.uniform(-12, 9, 3000),
+        np.array([v for v, _ in pos]),
+        np.array([(pos[i][0] + pos[i + 1][0]) / 2 for i in range(len(pos) - 1)]),  # exact ties
+    ])
+    for a in samples:
+        if a > 448:
+            want = 448.0
+        else:
+            best = min(pos, key=lambda vc: (abs(vc[0] - a), vc[1] & 1))   # nearest, tie -> even code
+            want = best[0]
+        got = O.e4m3_round(np.array([a]))[0]
+        assert got == want, (a, got, want)
+        assert O.e4m3_round(np.array([-a]))[0] == -want
+    for c, v in table.items():
+        if c == 0x80:
+            continue
+        assert O.e4m3_encode(np.array([v]))[0] == c
+        assert O.e4m3_decode(np.array([c], np.uint8))[0] == v
+
+
+def test_scale_exponent_closed_form():
+    # smallest s with amax <= 448 * 2^s
+    assert O.mx_scale_exponent(np.array([448.0]))[0] == 0
+    assert O.mx_scale_exponent(np.array([448.0 * (1 + 2 ** -20)]))[0] == 1
+    assert O.mx_scale_exponent(np.array([1.0]))[0] == -8          # 1 <= 448*2^-8 = 1.75
+    assert O.mx_scale_exponent(np.array([1.75]))[0] == -8
+    assert O.mx_scale_exponent(np.array([1.76]))[0] == -7
+    assert O.mx_scale_exponent(np.array([0.0]))[0] == -127
+    assert O.mx_scale_exponent(np.array([2.0 ** -140]))[0] == -127    # clamp
+    for a in 2.0 ** np.random.default_rng(1).uniform(-30, 30, 500):
+        s = O.mx_scale_exponent(np.array([a]))[0]
+        assert a <= 448 * 2.0 ** s and a > 448 * 2.0 ** (s - 1)
+
+
+def test_mx_block_properties():
+    rng = np.random.default_rng(2)
+    v = rng.standard_normal((6, 128)) * 2.0 ** rng.integers(-10, 10, (6, 1))
+    codes, scales = O.mx_quantize(v, 1)
+    assert codes.shape == (6, 128) and scales.shape == (6, 4)
+    deq = O.mx_dequantize(codes, scales, 1)
+    blk = np.abs(v).reshape(6, 4, 32)
+    # the block maximum maps to a finite code <= 448 (never saturates)
+    q = O.e4m3_decode(codes).reshape(6, 4, 32)
+    assert np.abs(q).max() <= 448 and np.isfinite(q).all()
+    # normal-range elements carry at most half an E4M3 ulp: relative error <= 2^-4
+    big = blk >= blk.max(axis=2, keepdims=True) * 2.0 ** -6
+    rel = np.abs(deq.reshape(6, 4, 32) - v.reshape(6, 4, 32)) / np.where(big, blk, 1)
+    assert rel[big].max() <= 2.0 ** -4
+    # a block of powers of two is exact
+    p2 = 2.0 ** rng.integers(-5, 5, (2, 64)).astype(float) * rng.choice([-1, 1], (2, 64))
+    np.testing.assert_array_equal(O.mx_roundtrip(p2, 1), p2)
+    # an all-zero block -> scale byte 0, code 0
+    c0, s0 = O.mx_quantize(np.zeros((1, 32)), 1)
+    assert (c0 == 0).all() and (s0 == 0).all()
+    # quantisation follows the requested axis
+    cT, sT = O.mx_quantize(v.T, 0)
+    np.testing.assert_array_equal(cT, codes.T)
+    np.testing.assert_array_equal(sT, scales.T)
+
+
+def test_segmented_token_blocks_do_not_cross_segments():
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal((50, 32))
+    v[20:30] *= 1000.0            # a loud segment must not coarsen its neighbours
+    got = O.mx_roundtrip_segments(v, [0, 20, 30], [20, 30, 50])
+    np.testing.assert_array_equal(got[0:20], O.mx_roundtrip(np.vstack([v[0:20], np.zeros((12, 32))]), 0)[:20])
+    np.testing.assert_array_equal(got[30:50], O.mx_roundtrip(np.vstack([v[30:50], np.zeros((12, 32))]), 0)[:20])
+    assert O.max_abs_rel(got[0:20], v[0:20]) < 2.0 ** -3
+
+
+def test_mxfp8_layer_within_format_error_of_exact():
+    from tests.test_oracle_ffn_grad import rand_layer
+    x, Wr, W1, W3, W2 = rand_layer(9, 40, 64, 4, 64, wstd=0.1)
+    f64 = O.forward(x, Wr, None, W1, W3, W2, 2)
+    fmx = O.forward(x, Wr, None, W1, W3, W2, 2, precision="mxfp8")
+    err = O.max_abs_rel(fmx["out"], f64["out"])
+    assert 1e-4 < err < 0.1
+    dout = np.random.default_rng(1).standard_normal(x.shape)
+    g64 = O.backward(f64, dout, x, Wr, W1, W3, W2)
+    gmx = O.backward(fmx, dout, x, Wr, W1, W3, W2)
+    for key in ("dx", "dW1", "dW3", "dW2", "dWr"):
+        e = O.max_abs_rel(gmx[key], g64[key])
+        assert 1e-5 < e < 0.15, (key, e)
