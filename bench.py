@@ -1,0 +1,336 @@
+"""Benchmark of the MoE layer (forward + backward) on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole layer over one batch of synthetic tokens:
+router, schedule, dispatch, GEMM1+SwiGLU, GEMM2, combine, then the backward
+(reverse combine, dgrad GEMMs with the SwiGLU backward, reverse dispatch,
+router backward, weight-gradient GEMMs). The default workload is the balanced
+BF16 shape T=4096, H=2048, E=32, k=4, F=1024 (workloads.py).
+
+Prints ONE JSON line (rank 0). `value` is whole-job tokens/s of fwd+bwd with
+inputs resident in HBM; L2 is flushed (256 MiB write) between timed steps and
+each step is timed with its own CUDA events on the launch stream. Under
+torchrun every rank runs an independent replica (weak scaling; the layer has
+no cross-GPU exchange) and the time is the max over ranks.
+
+--impl reference times the CPU float64 oracle (the only other implementation
+of this layer) on bounded token samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as WL  # noqa: E402
+
+METRIC = "MoE layer tokens/s fwd & fwd+bwd on 1 GB300; grouped-GEMM % of TC peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def oracle_step(w, inp, ntok):
+    """fwd+bwd of the oracle on the first ntok tokens (all weights)."""
+    from oracle import moe_oracle as O
+    o = {k: (O.bf16_to_f64(v) if k != "bias" and v is not None else v) for k, v in inp.items()}
+    x, dout = o["x"][:ntok], o["dout"][:ntok]
+    t0 = time.perf_counter()
+    f = O.forward(x, o["Wr"], o["bias"], o["W1"], o["W3"], o["W2"], w.k, precision=w.precision)
+    O.backward(f, dout, x, o["Wr"], o["W1"], o["W3"], o["W2"])
+    return time.perf_counter() - t0
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, inp, target_s=15.0):
+    t_small = oracle_step(w, inp, 256)
+    per_tok = t_small / 256
+    ntok = int(min(w.T, max(256, target_s / max(per_tok, 1e-9))))
+    ntok = max(256, ntok // 256 * 256)
+    t = oracle_step(w, inp, ntok)
+    return {"value": ntok / t, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"fwd+bwd of the first {ntok} of {w.T} tokens of {w.name}, all weights, float64 numpy "
+                      f"(BLAS threads = host cores), {t:.1f} s"}
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    inp = WL.make_inputs(w)
+    ntok = 256
+    for _ in range(args.warmup):
+        oracle_step(w, inp, ntok)
+    times = [oracle_step(w, inp, ntok) for _ in range(args.steps)]
+    tot = sum(times)
+    value = ntok * args.steps / tot
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "E": w.E, "k": w.k,
+                   "precision": w.precision, "sample_tokens_per_step": ntok},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                         "sample": f"fwd+bwd of the first {ntok} of {w.T} tokens per step, all weights"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def start_clocks(local_rank):
+    f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+    try:
+        p = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                              "-lms", "200", "-i", str(local_rank)], stdout=f, stderr=subprocess.DEVNULL)
+    except Exception:
+        p = None
+    return p, f.name
+
+
+def stop_clocks(p, path):
+    if p is None:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    p.terminate()
+    try:
+        p.wait(5)
+    except Exception:
+        p.kill()
+    rows = []
+    for line in open(path):
+        parts = [s.strip() for s in line.split(",")]
+        if len(parts) >= 9:
+            rows.append(parts)
+    os.unlink(path)
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+    sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+    smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+            "reasons": reasons, "samples": len(rows)}
+
+
+def gemm_flops(w, name):
+    R, H, F = w.R, w.H, w.F
+    return {"grouped_gemm_fwd1_swiglu": 4 * R * H * F, "grouped_gemm_fwd2": 2 * R * H * F,
+            "grouped_gemm_bwd2_swiglu": 2 * R * H * F, "grouped_gemm_bwd1": 4 * R * H * F,
+            "grouped_gemm_wgrad2": 2 * R * H * F, "grouped_gemm_wgrad13": 4 * R * H * F}.get(name)
+
+
+def run_ours(args, w):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from mixture_experts_layer_sum_gb300 import build_ext
+    build_ext.build()
+    import mixture_experts_layer_sum_gb300.moe as M
+    from mixture_experts_layer_sum_gb300.layer import MoeLayer
+
+    inp = WL.make_inputs(w.with_(seed=w.seed + rank))
+    dev = torch.device("cuda", local)
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    d = {k: to_dev(v) for k, v in inp.items() if k != "bias" and v is not None}
+    bias = torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None
+    layer = MoeLayer(w.T, w.H, w.F, w.E, w.k, w.precision, device=dev, ring_bytes=w.ring_bytes)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
+    ids = torch.empty(w.T, w.k, dtype=torch.int32, device=dev)
+    wts = torch.empty(w.T, w.k, dtype=torch.float32, device=dev)
+    dx = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
+    dWr = torch.empty(w.H, w.E, dtype=torch.float32, device=dev)
+    dW1 = torch.empty(w.E, w.H, w.F, dtype=torch.float32, device=dev)
+    dW3 = torch.empty_like(dW1)
+    dW2 = torch.empty(w.E, w.F, w.H, dtype=torch.float32, device=dev)
+
+    def fwd():
+        layer.forward(d["x"], d["Wr"], bias, d["W1"], d["W3"], d["W2"], out, ids, wts, stream=stream)
+
+    def step():
+        fwd()
+        layer.backward(d["dout"], d["x"], d["Wr"], d["W1"], d["W3"], d["W2"], dx, dWr, dW1, dW3, dW2,
+                       stream=stream)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def timed(fn, k):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+        with torch.cuda.stream(stream):
+            for a, b in evs:
+                flush.fill_(1)                # evict L2 between timed steps (untimed)
+                a.record(stream)
+                fn()
+                b.record(stream)
+        stream.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    layer.status(stream)
+    barrier()
+    clk_p, clk_path = start_clocks(local)
+    total_ms = timed(step, args.steps)
+    clocks = stop_clocks(clk_p, clk_path)
+    barrier()
+    fwd_ms = timed(fwd, args.steps)
+    layer.status(stream)
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms, fwd_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, fwd_ms = t.tolist()
+
+    # per-kernel breakdown: the same steps with events around every launch
+    M.moe_profile_begin()
+    prof_ms = timed(step, args.steps)
+    kernels = M.moe_profile_end()
+    launches = sum(n for _, n, _ in kernels)
+
+    # end to end through the public API with host buffers: H2D of x and dout,
+    # fwd+bwd, D2H of out and dx, every step
+    hx = torch.empty(w.T, w.H, dtype=torch.bfloat16, pin_memory=True)
+    hd = torch.empty_like(hx, pin_memory=True)
+    hx.copy_(d["x"].cpu())
+    hd.copy_(d["dout"].cpu())
+    hout = torch.empty_like(hx, pin_memory=True)
+    hdx = torch.empty_like(hx, pin_memory=True)
+    xin = torch.empty_like(d["x"])
+    din = torch.empty_like(d["dout"])
+
+    def e2e_step():
+        xin.copy_(hx, non_blocking=True)
+        din.copy_(hd, non_blocking=True)
+        layer.forward(xin, d["Wr"], bias, d["W1"], d["W3"], d["W2"], out, ids, wts, stream=stream)
+        layer.backward(din, xin, d["Wr"], d["W1"], d["W3"], d["W2"], dx, dWr, dW1, dW3, dW2, stream=stream)
+        hout.copy_(out, non_blocking=True)
+        hdx.copy_(dx, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+    stream.synchronize()
+    e2e_ms = timed(e2e_step, args.steps)
+    layer.status(stream)
+
+    if rank != 0:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    peaks, peak_src = load_peaks()
+    # dominant kernel: largest share of the profiled step
+    kt = sorted(kernels, key=lambda r: -r[2])
+    name, n, ms = kt[0]
+    per_launch_ms = ms / n
+    fl = gemm_flops(w, name)
+    roof = None
+    if fl is not None:
+        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+        ach = fl / (per_launch_ms * 1e-3) / 1e12
+        roof = {"kernel": name, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": None,
+                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside the step loop)"}
+    gemm_ms = sum(ms_ for nm, _, ms_ in kernels if nm.startswith("grouped_gemm"))
+    gemm_fl = sum(gemm_flops(w, nm) * n_ for nm, n_, _ in kernels if nm.startswith("grouped_gemm"))
+    value = ws * w.T * args.steps / (total_ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.precision == "bf16" else "mxfp8",
+        "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "E": w.E, "k": w.k,
+                   "precision": w.precision, "step": "forward+backward",
+                   "l2": "flushed (256 MiB write) between timed steps",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "fwd": {"value": ws * w.T * args.steps / (fwd_ms * 1e-3), "unit": "tokens/s",
+                "ms_per_step": fwd_ms / args.steps},
+        "roofline": roof,
+        "grouped_gemm": {"tflops": gemm_fl / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None,
+                         "frac_of_peak": (gemm_fl / (gemm_ms * 1e-3) / 1e12) /
+                         peaks.get("bf16_tflops_sustained", 1700.0) if gemm_ms else None,
+                         "share_of_step": gemm_ms / prof_ms if prof_ms else None},
+        "kernels": [{"name": nm, "launches": n_, "ms_per_step": ms_ / args.steps,
+                     "share": ms_ / prof_ms} for nm, n_, ms_ in kt],
+        "gpu_launches": launches,
+        "e2e": {"value": ws * w.T * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * w.T * w.H * 2, "d2h_bytes_per_step": 2 * w.T * w.H * 2},
+        "clocks": clocks,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=WL.BALANCED.name, choices=sorted(WL.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3 or args.impl == "reference" or args.steps < 3, "need >= 3 warm-up steps"
+    w = WL.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

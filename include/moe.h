@@ -1,0 +1,222 @@
+/*
+ * moe.h - C ABI of a single-GPU Mixture-of-Experts layer for GB300 (sm_103a).
+ *
+ * One MoE layer, forward and backward, over one GPU's tokens:
+ *   router (softmax over E experts, top-k, ties to the lower expert index,
+ *   weights renormalised over the k chosen) -> schedule (per-expert counts,
+ *   exclusive offsets, stable expert-sorted permutation) -> pull dispatch
+ *   (gather of token rows into expert-grouped rows, optionally quantised to
+ *   MXFP8 inside the gather) -> expert FFN y = W2 (silu(x W1) * (x W3)) as
+ *   grouped GEMMs -> combine (top-k weighted sum in fixed slot order), and the
+ *   mirrored backward.
+ *
+ * The stages are the ones the Mixture-of-Kittens articles name:
+ *   "O MoK do Cursor alcanca aumento de desempenho de 2,37x no NVIDIA GB300
+ *   NVL72" (kucoin.com), section 01 (count tokens per expert, decide where they
+ *   go, group each expert's rows for the grouped GEMM), section 02 (pull
+ *   dispatch and push combine, reverse-combine and reverse-dispatch in the
+ *   backward, minibatches of at least two SM waves, a fixed-size ring token
+ *   buffer advanced by GPU-side state, MXFP8 quantisation fused into dispatch,
+ *   grouped GEMM and SwiGLU) and section 03 (Schedule, Dispatch, Expert FFN,
+ *   Combine, final weighted fusion); "Cursor abre codigo do Mixture-of-Kittens"
+ *   (noticiai.com.br), "O que e" (one deterministic kernel) and "As tres
+ *   decisoes de design" (no token dropping; macrobatch interleave).
+ * The pages give no formulas; the router and SwiGLU forms above are the plain
+ * reading of a softmax top-k SwiGLU MoE.
+ *
+ * Conventions for every call below
+ *   - All tensor arguments are DEVICE pointers owned by the caller. The library
+ *     never allocates or frees device memory; scratch comes from the caller's
+ *     workspace, and the forward->backward context from the caller's `saved`
+ *     buffer, both sized by the query functions.
+ *   - Layouts are dense row-major: x, out, dout, dx [T,H] bf16; W_r [H,E] bf16;
+ *     bias [E] fp32; W1, W3 [E,H,F] bf16; W2 [E,F,H] bf16; topk ids [T,k]
+ *     int32; topk weights [T,k] fp32; weight gradients fp32 in the shape of
+ *     their weight. bf16 is IEEE bfloat16 stored as 16-bit words.
+ *   - Every call is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns without synchronising the host. Inputs are never
+ *     written.
+ *   - Host-detected errors (null pointer, unsupported size, workspace too
+ *     small, misalignment) return a non-zero status and launch nothing.
+ *     A failed kernel launch returns MOE_ERR_CUDA. Errors detected on the
+ *     device (a bounded wait that ran out, an index check that failed) are
+ *     written to a status word inside the workspace; moe_query_status reads it.
+ *   - Tensor pointers must be 16-byte aligned. The workspace and saved
+ *     buffers may start anywhere: the library uses them from the next
+ *     1024-byte boundary on, and the size queries include that slack.
+ *   - Calls sharing one workspace must not overlap in time (same stream, or
+ *     ordered by events).
+ *   - Thread safety: no global state besides a thread-local error string.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef struct CUstream_st *moe_stream_t;   /* same type as cudaStream_t */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
+    MOE_ERR_UNSUPPORTED = 2,   /* shape outside the supported envelope */
+    MOE_ERR_WORKSPACE = 3,     /* workspace or saved buffer too small */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+    MOE_ERR_TIMEOUT = 5,       /* a bounded device wait ran out (device status) */
+    MOE_ERR_INTERNAL = 6       /* a device-side consistency check failed */
+} moe_status_t;
+
+typedef enum {
+    MOE_PRECISION_BF16 = 0,    /* bf16 operands, fp32 accumulation */
+    MOE_PRECISION_MXFP8 = 1    /* e4m3 operands, one e8m0 scale per 32 along K */
+} moe_precision_t;
+
+/* Layer shape and run options. Zero-initialise, then set the shape.
+ *   T tokens, H hidden size, F expert FFN width, E experts, k experts per token.
+ *   Supported: 1 <= k <= E <= 64, H and F multiples of 256, T >= 0.
+ *   minibatch_rows: routed rows per grouped-GEMM step of the ring pipeline;
+ *     0 = smallest multiple of 128 giving at least two full waves of GEMM1
+ *     tiles on the device's SMs (article section 02: "at least two full SM
+ *     waves per expert grouped GEMM").
+ *   ring_bytes: size of the ring token buffer (dispatched rows, FFN hidden
+ *     rows and expert outputs of the macrobatches in flight); 0 = large enough
+ *     for all routed rows, i.e. one macrobatch.
+ *   macrobatch_tokens: tokens per macrobatch; 0 = derived from ring_bytes.
+ *   timeout_ms: budget of every device-side wait; 0 = 2000 ms.
+ *   num_sms: SM count used for planning; 0 = query the current device. */
+typedef struct {
+    int T, H, F, E, k;
+    int precision;
+    int minibatch_rows;
+    int macrobatch_tokens;
+    size_t ring_bytes;
+    unsigned timeout_ms;
+    int num_sms;
+} moe_config_t;
+
+/* Derived execution plan (host-only; no device access when cfg->num_sms > 0). */
+typedef struct {
+    int num_sms;             /* SMs the plan was made for */
+    int minibatch_rows;      /* rows per grouped-GEMM step */
+    int macrobatch_tokens;   /* tokens per macrobatch */
+    int num_macrobatches;    /* ceil(T / macrobatch_tokens) */
+    int rows_padded_max;     /* upper bound of padded expert-sorted rows */
+    int ring_rows;           /* rows held by the ring (all halves) */
+    size_t ring_bytes;       /* bytes the ring occupies in the workspace */
+    size_t workspace_bytes;  /* = moe_workspace_size(cfg) */
+    size_t saved_bytes;      /* = moe_saved_size(cfg) */
+    size_t qweights_bytes;   /* = moe_qweights_size(cfg) */
+} moe_plan_t;
+
+/* Library ABI version (MOE_ABI_VERSION of the build). */
+int moe_abi_version(void);
+
+/* Fills *plan for cfg. Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for a
+ * shape the library does not run. */
+moe_status_t moe_plan(const moe_config_t *cfg, moe_plan_t *plan);
+
+/* Bytes of scratch memory needed by moe_schedule / moe_forward / moe_backward
+ * (0 when cfg is invalid). Content is not preserved between calls. */
+size_t moe_workspace_size(const moe_config_t *cfg);
+
+/* Bytes of the forward->backward context written by moe_forward and read by
+ * moe_backward (router ids/weights/probabilities, schedule maps, the bf16
+ * FFN pre-activations a = x W1 and b = x W3 of every routed row). */
+size_t moe_saved_size(const moe_config_t *cfg);
+
+/* Bytes of the MXFP8 weight copies made by moe_quantize_weights (0 for bf16). */
+size_t moe_qweights_size(const moe_config_t *cfg);
+
+/* Schedule only (article section 01: count, place, group).
+ * topk_ids [T,k] int32 in [0,E). With macrobatch m = t / Mb (Mb = the plan's
+ * macrobatch_tokens), the routed slots s = t*k + j are stably sorted by the key
+ * (m, expert):
+ *   counts [nM*E]          rows of (m, e)
+ *   offsets [nM*(E+1)]     absolute sorted position where (m, e) starts; the
+ *                          last entry of each macrobatch is where it ends
+ *   sorted_to_slot [T*k]   slot at each sorted position
+ *   slot_to_sorted [T*k]   inverse permutation
+ * All outputs are bit-exact and deterministic. Ids outside [0,E) make the
+ * device status MOE_ERR_INTERNAL (their slots are left out). */
+moe_status_t moe_schedule(const moe_config_t *cfg, const int32_t *topk_ids,
+                          int32_t *counts, int32_t *offsets,
+                          int32_t *sorted_to_slot, int32_t *slot_to_sorted,
+                          void *workspace, size_t workspace_bytes,
+                          moe_stream_t stream);
+
+/* MXFP8 copies of the bf16 master weights for the forward and backward
+ * GEMMs (quantised along each GEMM's contraction axis). Run once per weight
+ * update. Returns MOE_ERR_UNSUPPORTED for a bf16 config. */
+moe_status_t moe_quantize_weights(const moe_config_t *cfg, const void *W1,
+                                  const void *W3, const void *W2,
+                                  void *qweights, size_t qweights_bytes,
+                                  moe_stream_t stream);
+
+/* Forward (article section 03: Schedule, Dispatch, Expert FFN, Combine and the
+ * final weighted fusion).
+ *   x [T,H] bf16, W_r [H,E] bf16, bias [E] fp32 or NULL, W1/W3 [E,H,F] bf16,
+ *   W2 [E,F,H] bf16, qweights: moe_quantize_weights output (MXFP8) or NULL.
+ *   out [T,H] bf16: out[t] = sum_j w[t,j] * y_j, summed in fp32 in slot order j
+ *     and rounded once; bit-reproducible run to run.
+ *   topk_ids [T,k] int32, topk_w [T,k] fp32: the router's choice (descending
+ *     probability) and renormalised weights.
+ *   saved: moe_saved_size bytes, consumed by moe_backward. */
+moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r,
+                         const float *bias, const void *W1, const void *W3,
+                         const void *W2, const void *qweights, void *out,
+                         int32_t *topk_ids, float *topk_w, void *saved,
+                         size_t saved_bytes, void *workspace,
+                         size_t workspace_bytes, moe_stream_t stream);
+
+/* Backward of sum(dout * out) with the top-k choice held fixed (article
+ * section 02: pull reverse-combine and push reverse-dispatch).
+ *   dout [T,H] bf16; x, W_r, W1, W3, W2, qweights and saved as given to the
+ *   matching moe_forward.
+ *   dx [T,H] bf16 (overwritten); dW_r [H,E], dW1/dW3 [E,H,F], dW2 [E,F,H] fp32:
+ *   overwritten when accumulate == 0, added to when accumulate != 0. */
+moe_status_t moe_backward(const moe_config_t *cfg, const void *dout,
+                          const void *x, const void *W_r, const void *W1,
+                          const void *W3, const void *W2, const void *qweights,
+                          const void *saved, void *dx, float *dW_r, float *dW1,
+                          float *dW3, float *dW2, int accumulate,
+                          void *workspace, size_t workspace_bytes,
+                          moe_stream_t stream);
+
+/* Synchronises `stream`, returns the device status word of `workspace`
+ * (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_INTERNAL) and clears it. */
+moe_status_t moe_query_status(void *workspace, moe_stream_t stream);
+
+/* Clears the device status word (enqueued on stream, no host sync). Call once
+ * on a fresh workspace before its first use. */
+moe_status_t moe_reset_status(void *workspace, moe_stream_t stream);
+
+/* Per-kernel timing of this host thread's calls (CUDA events recorded on the
+ * launch stream around every kernel the library launches). */
+typedef struct {
+    char name[32];        /* kernel name, e.g. "grouped_gemm_fwd1" */
+    int launches;         /* launches recorded since moe_profile_begin */
+    double total_ms;      /* sum of their event-measured durations */
+} moe_kernel_time_t;
+
+/* Starts recording (clears earlier records of this thread). */
+moe_status_t moe_profile_begin(void);
+
+/* Stops recording, waits for the recorded events, writes up to max_entries
+ * aggregated rows (one per kernel name, in first-launch order) and returns how
+ * many there are (negative moe_status_t on a CUDA error). */
+int moe_profile_end(moe_kernel_time_t *out, int max_entries);
+
+/* Message of the last error returned on this host thread. */
+const char *moe_last_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,466 @@
+// Persistent grouped GEMMs of the expert FFN on tcgen05 tensor cores.
+//
+// One kernel template serves the six contractions of the layer (article
+// "O MoK do Cursor ...", section 01: the grouped GEMM needs each expert's
+// tokens grouped; section 02: SwiGLU and the quantisation sit in the GEMM's
+// data path):
+//   FWD1  [a|b] = X_e [W1_e|W3_e]; epilogue stores bf16 a, b and h = silu(a)*b
+//   FWD2  Y = h_e W2_e
+//   BWD2  G = dY_e W2_e^T; epilogue: dw partials <G,h>, dh = w G, SwiGLU
+//         backward -> da, db, and hw = w*h for the W2 weight gradient
+//   BWD1  dX = da W1_e^T + db W3_e^T            (contraction over 2F)
+//   WG2   dW2_e = (w h)_e^T dY_e                (contraction over the expert's rows)
+//   WG13  [dW1_e|dW3_e] = X_e^T [da_e|db_e]      (contraction over the expert's rows)
+//
+// Structure (one CTA per SM, 192 threads):
+//   warp 0     TMA producer: 128B-swizzled tiles of A (128 x 64) and B
+//              (256 x 64) into a 4-stage shared-memory ring
+//   warp 1     TMEM allocator and single-thread tcgen05.mma issuer
+//              (M=128, N=256, K=16 per instruction); accumulators in TMEM,
+//              double buffered (2 x 256 columns)
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator, fused elementwise
+//              work, stores to global memory
+// Every mbarrier wait is bounded; when a wait gives up the status word is set
+// and all roles leave their loops, drain their in-flight copies/MMAs and free
+// TMEM before exiting.
+#include "grouped_gemm.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KiB
+constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KiB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t CHUNK_BYTES = 64 * 64 * 2;   // one 64x64 bf16 box, 8 KiB
+
+template <int OP>
+struct OpTraits;
+template <> struct OpTraits<OP_FWD1> { static constexpr bool grouped_k = false, a_mn = false, b_mn = true; };
+template <> struct OpTraits<OP_FWD2> { static constexpr bool grouped_k = false, a_mn = false, b_mn = true; };
+template <> struct OpTraits<OP_BWD2> { static constexpr bool grouped_k = false, a_mn = false, b_mn = false; };
+template <> struct OpTraits<OP_BWD1> { static constexpr bool grouped_k = false, a_mn = false, b_mn = false; };
+template <> struct OpTraits<OP_WG2> { static constexpr bool grouped_k = true, a_mn = true, b_mn = true; };
+template <> struct OpTraits<OP_WG13> { static constexpr bool grouped_k = true, a_mn = true, b_mn = true; };
+
+struct TileInfo {
+    int e, mt, nt;
+    int g0;      // grouped-M: first global padded row of the tile
+    int nk;      // number of BK blocks
+};
+
+struct SmemCtl {
+    uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+    uint32_t tmem_base;
+    int nt;                       // tiles along N
+    int mt_per_group;             // grouped-K: tiles along M (fixed)
+    int prefix[kMaxExperts + 1];  // grouped-M: tile prefix over experts; grouped-K: unused
+    int krows[kMaxExperts];       // grouped-K: padded rows of each expert (all macrobatches)
+    int seg_start[kMaxExperts];   // grouped-M: first padded row of (m, e)
+};
+
+template <int OP>
+__device__ __forceinline__ int num_tiles(const SmemCtl &c, const GemmArgs &g) {
+    if constexpr (OpTraits<OP>::grouped_k) return g.E * c.mt_per_group * c.nt;
+    else return c.prefix[g.E] * c.nt;
+}
+
+template <int OP>
+__device__ __forceinline__ TileInfo decode_tile(const SmemCtl &c, const GemmArgs &g, int t) {
+    TileInfo ti;
+    ti.nt = t % c.nt;
+    int q = t / c.nt;
+    if constexpr (OpTraits<OP>::grouped_k) {
+        ti.mt = q % c.mt_per_group;
+        ti.e = q / c.mt_per_group;
+        ti.g0 = 0;
+        ti.nk = c.krows[ti.e] / BK;
+    } else {
+        int e = 0;
+        while (c.prefix[e + 1] <= q) ++e;   // E <= 64
+        ti.e = e;
+        ti.mt = q - c.prefix[e];
+        ti.g0 = c.seg_start[e] + ti.mt * BM;
+        ti.nk = g.K / BK;
+    }
+    return ti;
+}
+
+// grouped-K ops: the padded row at position kb*BK of expert e's rows, walking
+// the (macrobatch, e) runs in macrobatch order.
+__device__ __forceinline__ int grouped_k_row(const GemmArgs &g, int e, int kb) {
+    int r = kb * BK;
+    for (int mm = 0; mm < g.nM; ++mm) {
+        int s0 = g.offp[mm * g.E + e], s1 = g.offp[mm * g.E + e + 1];
+        if (r < s1 - s0) return s0 + r;
+        r -= s1 - s0;
+    }
+    return 0;   // unreachable for kb < nk
+}
+
+template <int OP>
+__device__ void producer_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tiles, uint64_t *full,
+                              uint64_t *empty, const WaitCtl &ctl) {
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued[STAGES] = {0, 0, 0, 0};
+    uint32_t last_phase[STAGES] = {0, 0, 0, 0};
+    bool ok = true;
+    const int total = num_tiles<OP>(c, g);
+    const int a_shift = g.a_ring ? (g.ring_base - g.offp[g.m * g.E]) : 0;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        TileInfo ti = decode_tile<OP>(c, g, t);
+        for (int kb = 0; kb < ti.nk; ++kb) {
+            if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, ctl)) { ok = false; break; }
+            uint32_t bar = smem_u32(&full[stage]);
+            uint32_t sA = smem_u32(tiles + stage * STAGE_BYTES);
+            uint32_t sB = sA + A_BYTES;
+            mbar_arrive_expect_tx(bar, STAGE_BYTES);
+            if constexpr (OP == OP_FWD1) {
+                int ar = ti.g0 + a_shift, br = ti.e * g.H + kb * BK, n0 = ti.nt * 128;
+                tma_load_2d(sA, &g.a0, bar, kb * BK, ar);
+                tma_load_2d(sB, &g.b0, bar, n0, br);
+                tma_load_2d(sB + CHUNK_BYTES, &g.b0, bar, n0 + 64, br);
+                tma_load_2d(sB + 2 * CHUNK_BYTES, &g.b1, bar, n0, br);
+                tma_load_2d(sB + 3 * CHUNK_BYTES, &g.b1, bar, n0 + 64, br);
+            } else if constexpr (OP == OP_FWD2) {
+                int ar = ti.g0 + a_shift, br = ti.e * g.F + kb * BK, n0 = ti.nt * BN;
+                tma_load_2d(sA, &g.a0, bar, kb * BK, ar);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * CHUNK_BYTES, &g.b0, bar, n0 + 64 * j, br);
+            } else if constexpr (OP == OP_BWD2) {
+                tma_load_2d(sA, &g.a0, bar, kb * BK, ti.g0 + a_shift);
+                tma_load_2d(sB, &g.b0, bar, kb * BK, ti.e * g.F + ti.nt * BN);
+            } else if constexpr (OP == OP_BWD1) {
+                const int kf = g.F / BK;
+                const bool second = kb >= kf;
+                const int kk = second ? kb - kf : kb;
+                tma_load_2d(sA, second ? &g.a1 : &g.a0, bar, kk * BK, ti.g0 + a_shift);
+                tma_load_2d(sB, second ? &g.b1 : &g.b0, bar, kk * BK, ti.e * g.H + ti.nt * BN);
+            } else if constexpr (OP == OP_WG2) {
+                int row = grouped_k_row(g, ti.e, kb);
+                int m0 = ti.mt * BM, n0 = ti.nt * BN;
+                tma_load_2d(sA, &g.a0, bar, m0, row);
+                tma_load_2d(sA + CHUNK_BYTES, &g.a0, bar, m0 + 64, row);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * CHUNK_BYTES, &g.b0, bar, n0 + 64 * j, row);
+            } else if constexpr (OP == OP_WG13) {
+                int row = grouped_k_row(g, ti.e, kb);
+                int m0 = ti.mt * BM, n0 = ti.nt * 128;
+                tma_load_2d(sA, &g.a0, bar, m0, row);
+                tma_load_2d(sA + CHUNK_BYTES, &g.a0, bar, m0 + 64, row);
+                tma_load_2d(sB, &g.b0, bar, n0, row);
+                tma_load_2d(sB + CHUNK_BYTES, &g.b0, bar, n0 + 64, row);
+                tma_load_2d(sB + 2 * CHUNK_BYTES, &g.b1, bar, n0, row);
+                tma_load_2d(sB + 3 * CHUNK_BYTES, &g.b1, bar, n0 + 64, row);
+            }
+            issued[stage] = 1;
+            last_phase[stage] = phase;
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+    }
+    if (!ok) {
+        // leave no bulk copy in flight: wait (bounded, regardless of the
+        // status word) for the last copy issued into every stage
+        for (int s = 0; s < STAGES; ++s) {
+            if (!issued[s]) continue;
+            uint32_t bar = smem_u32(&full[s]);
+            uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar, last_phase[s]) && globaltimer_ns() - t0 < ctl.budget_ns) {}
+        }
+    }
+}
+
+template <int OP>
+__device__ void mma_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tiles, uint64_t *full,
+                         uint64_t *empty, uint64_t *tfull, uint64_t *tempty, uint64_t *drain,
+                         uint32_t tmem, const WaitCtl &ctl) {
+    constexpr bool AMN = OpTraits<OP>::a_mn, BMN = OpTraits<OP>::b_mn;
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, AMN, BMN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const int total = num_tiles<OP>(c, g);
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        TileInfo ti = decode_tile<OP>(c, g, t);
+        if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1, ctl)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < ti.nk; ++kb) {
+            if (!mbar_wait(smem_u32(&full[stage]), phase, ctl)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sA = smem_u32(tiles + stage * STAGE_BYTES);
+            const uint32_t sB = sA + A_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+                uint64_t ad = AMN ? sdesc_sw128(sA + kk * 2048, 8192, 1024) : sdesc_sw128(sA + kk * 32, 16, 1024);
+                uint64_t bd = BMN ? sdesc_sw128(sB + kk * 2048, 8192, 1024) : sdesc_sw128(sB + kk * 32, 16, 1024);
+                mma_bf16_ss(d, ad, bd, idesc, (kb | kk) != 0);
+            }
+            mma_commit(smem_u32(&empty[stage]));
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&tfull[acc]));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+    }
+    // all MMAs issued by this thread must be complete before TMEM is freed
+    mma_commit(smem_u32(drain));
+    uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(smem_u32(drain), 0) && globaltimer_ns() - t0 < ctl.budget_ns) {}
+}
+
+__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
+__device__ __forceinline__ float sigmoid_f(float a) { return 1.0f / (1.0f + __expf(-a)); }
+
+template <int OP>
+__device__ void epilogue_loop(const GemmArgs &g, const SmemCtl &c, uint64_t *tfull, uint64_t *tempty,
+                              uint32_t tmem, const WaitCtl &ctl) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int quarter = warp & 3;             // TMEM lanes this warp may read
+    const int r = quarter * 32 + lane;        // accumulator row of this thread
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const int total = num_tiles<OP>(c, g);
+    const int ring_shift = g.ring_base - g.offp[g.m * g.E];
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        TileInfo ti = decode_tile<OP>(c, g, t);
+        if (!mbar_wait(smem_u32(&tfull[acc]), acc_phase, ctl)) break;
+        tc_fence_after();
+        const uint32_t tbase = tmem + lane_base + acc * BN;
+        if constexpr (OP == OP_FWD1) {
+            const int grow = ti.g0 + r;
+            const size_t F = g.F;
+            bf16 *pa = g.o0 + grow * F + ti.nt * 128;
+            bf16 *pb = g.o1 + grow * F + ti.nt * 128;
+            bf16 *ph = g.o2 + (size_t)(grow + ring_shift) * F + ti.nt * 128;
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t va[32], vb[32];
+                tmem_ld_32x32b_x32(tbase + cc * 32, va);
+                tmem_ld_32x32b_x32(tbase + 128 + cc * 32, vb);
+                tmem_ld_wait();
+                uint32_t oa[16], ob[16], oh[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    oa[i] = pack_bf16x2(__uint_as_float(va[2 * i]), __uint_as_float(va[2 * i + 1]));
+                    ob[i] = pack_bf16x2(__uint_as_float(vb[2 * i]), __uint_as_float(vb[2 * i + 1]));
+                    // h from the bf16-rounded a and b, so the backward recomputes it exactly
+                    float a0 = bf16lo(oa[i]), a1 = bf16hi(oa[i]);
+                    float b0 = bf16lo(ob[i]), b1 = bf16hi(ob[i]);
+                    oh[i] = pack_bf16x2(silu_f(a0) * b0, silu_f(a1) * b1);
+                }
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    st_v4(pa + cc * 32 + v * 8, make_uint4(oa[4 * v], oa[4 * v + 1], oa[4 * v + 2], oa[4 * v + 3]));
+                    st_v4(pb + cc * 32 + v * 8, make_uint4(ob[4 * v], ob[4 * v + 1], ob[4 * v + 2], ob[4 * v + 3]));
+                    st_v4(ph + cc * 32 + v * 8, make_uint4(oh[4 * v], oh[4 * v + 1], oh[4 * v + 2], oh[4 * v + 3]));
+                }
+            }
+        } else if constexpr (OP == OP_FWD2 || OP == OP_BWD1) {
+            const int grow = ti.g0 + r;
+            const size_t orow = (OP == OP_FWD2 && g.o_ring) ? (size_t)(grow + ring_shift) : (size_t)grow;
+            bf16 *py = g.o0 + orow * g.H + ti.nt * BN;
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tbase + cc * 32, v);
+                tmem_ld_wait();
+                uint32_t o[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    st_v4(py + cc * 32 + q * 8, make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]));
+            }
+        } else if constexpr (OP == OP_BWD2) {
+            const int grow = ti.g0 + r;
+            const size_t F = g.F;
+            const int slot = g.row_slot[grow];
+            const float w = slot >= 0 ? g.wslot[slot] : 0.0f;
+            const bf16 *pa = g.in0 + grow * F + ti.nt * BN;
+            const bf16 *pb = g.in1 + grow * F + ti.nt * BN;
+            bf16 *pda = g.o0 + grow * F + ti.nt * BN;
+            bf16 *pdb = g.o1 + grow * F + ti.nt * BN;
+            bf16 *phw = g.o2 + grow * F + ti.nt * BN;
+            float dwp = 0.0f;
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tbase + cc * 32, v);
+                uint32_t ra[16], rb[16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 x = ld_v4(pa + cc * 32 + q * 8);
+                    uint4 y = ld_v4(pb + cc * 32 + q * 8);
+                    ra[4 * q] = x.x; ra[4 * q + 1] = x.y; ra[4 * q + 2] = x.z; ra[4 * q + 3] = x.w;
+                    rb[4 * q] = y.x; rb[4 * q + 1] = y.y; rb[4 * q + 2] = y.z; rb[4 * q + 3] = y.w;
+                }
+                tmem_ld_wait();
+                uint32_t oda[16], odb[16], ohw[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float da2[2], db2[2], hw2[2];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        float a = h2 ? bf16hi(ra[i]) : bf16lo(ra[i]);
+                        float b = h2 ? bf16hi(rb[i]) : bf16lo(rb[i]);
+                        float G = __uint_as_float(v[2 * i + h2]);
+                        float sg = sigmoid_f(a);
+                        float sl = a * sg;
+                        float hval = __bfloat162float(__float2bfloat16_rn(sl * b));   // h as the forward stored it
+                        dwp = fmaf(G, hval, dwp);
+                        float dh = w * G;
+                        da2[h2] = dh * b * sg * (1.0f + a * (1.0f - sg));
+                        db2[h2] = dh * sl;
+                        hw2[h2] = w * hval;
+                    }
+                    oda[i] = pack_bf16x2(da2[0], da2[1]);
+                    odb[i] = pack_bf16x2(db2[0], db2[1]);
+                    ohw[i] = pack_bf16x2(hw2[0], hw2[1]);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    st_v4(pda + cc * 32 + q * 8, make_uint4(oda[4 * q], oda[4 * q + 1], oda[4 * q + 2], oda[4 * q + 3]));
+                    st_v4(pdb + cc * 32 + q * 8, make_uint4(odb[4 * q], odb[4 * q + 1], odb[4 * q + 2], odb[4 * q + 3]));
+                    st_v4(phw + cc * 32 + q * 8, make_uint4(ohw[4 * q], ohw[4 * q + 1], ohw[4 * q + 2], ohw[4 * q + 3]));
+                }
+            }
+            g.of0[(size_t)grow * (g.F / BN) + ti.nt] = dwp;
+        } else {   // OP_WG2, OP_WG13: fp32 weight gradients
+            const bool empty_k = ti.nk == 0;
+            const int row = ti.mt * BM + r;
+            float *dst0, *dst1 = nullptr;
+            int ncol0;
+            if constexpr (OP == OP_WG2) {   // dW2[e][f][h]
+                dst0 = g.of0 + ((size_t)ti.e * g.F + row) * g.H + ti.nt * BN;
+                ncol0 = BN;
+            } else {                        // dW1/dW3[e][h][f]
+                dst0 = g.of0 + ((size_t)ti.e * g.H + row) * g.F + ti.nt * 128;
+                dst1 = g.of1 + ((size_t)ti.e * g.H + row) * g.F + ti.nt * 128;
+                ncol0 = 128;
+            }
+#pragma unroll 1
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                uint32_t v[32];
+                if (!empty_k) {
+                    tmem_ld_32x32b_x32(tbase + cc * 32, v);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0u;
+                }
+                float *dst = (cc * 32 < ncol0) ? dst0 + cc * 32 : dst1 + (cc * 32 - ncol0);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float4 o = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                           __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                    float4 *p = reinterpret_cast<float4 *>(dst + q * 4);
+                    if (g.accumulate) {
+                        float4 old = *p;
+                        o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+                    }
+                    *p = o;
+                }
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&tempty[acc]));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+    }
+}
+
+template <int OP>
+__global__ void __launch_bounds__(192, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs g) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    SmemCtl &c = *reinterpret_cast<SmemCtl *>(tiles + STAGES * STAGE_BYTES);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    WaitCtl ctl{g.status, g.budget_ns};
+
+    if (threadIdx.x == 0) {
+        if constexpr (OpTraits<OP>::grouped_k) {
+            c.nt = (OP == OP_WG13) ? g.N / 128 : g.N / BN;
+            c.mt_per_group = g.Mw / BM;
+            for (int e = 0; e < g.E; ++e) {
+                int rows = 0;
+                for (int mm = 0; mm < g.nM; ++mm) rows += g.offp[mm * g.E + e + 1] - g.offp[mm * g.E + e];
+                c.krows[e] = rows;
+            }
+        } else {
+            c.nt = (OP == OP_FWD1) ? g.N / 128 : g.N / BN;
+            c.prefix[0] = 0;
+            for (int e = 0; e < g.E; ++e) {
+                int s0 = g.offp[g.m * g.E + e], s1 = g.offp[g.m * g.E + e + 1];
+                c.seg_start[e] = s0;
+                c.prefix[e + 1] = c.prefix[e] + (s1 - s0) / BM;
+            }
+        }
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&c.full[s]), 1);
+            mbar_init(smem_u32(&c.empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&c.tfull[a]), 1);
+            mbar_init(smem_u32(&c.tempty[a]), 128);
+        }
+        mbar_init(smem_u32(&c.drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&g.a0);
+        tma_prefetch_map(&g.b0);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&c.tmem_base), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = c.tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) producer_loop<OP>(g, c, tiles, c.full, c.empty, ctl);
+    } else if (warp == 1) {
+        if (lane == 0) mma_loop<OP>(g, c, tiles, c.full, c.empty, c.tfull, c.tempty, &c.drain, tmem, ctl);
+    } else {
+        epilogue_loop<OP>(g, c, c.tfull, c.tempty, tmem, ctl);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+template <int OP>
+cudaError_t launch_op(const GemmArgs &g, int grid, cudaStream_t stream) {
+    constexpr size_t smem = STAGES * STAGE_BYTES + sizeof(SmemCtl) + 1024;
+    static_assert(smem <= 227 * 1024, "shared memory budget");
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    grouped_gemm_kernel<OP><<<grid, 192, smem, stream>>>(g);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream) {
+    switch (op) {
+        case OP_FWD1: return launch_op<OP_FWD1>(g, grid, stream);
+        case OP_FWD2: return launch_op<OP_FWD2>(g, grid, stream);
+        case OP_BWD2: return launch_op<OP_BWD2>(g, grid, stream);
+        case OP_BWD1: return launch_op<OP_BWD1>(g, grid, stream);
+        case OP_WG2: return launch_op<OP_WG2>(g, grid, stream);
+        case OP_WG13: return launch_op<OP_WG13>(g, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace moe

@@ -1,0 +1,34 @@
+// Arguments of the persistent tcgen05 grouped GEMM (grouped_gemm.cu).
+#pragma once
+#include "moe_common.cuh"
+
+namespace moe {
+
+enum GemmOp { OP_FWD1 = 0, OP_FWD2 = 1, OP_BWD2 = 2, OP_BWD1 = 3, OP_WG2 = 4, OP_WG13 = 5 };
+
+// Row spaces: "padded rows" are the expert-sorted routed rows where every
+// (macrobatch, expert) run starts at offp[m*E+e] and is padded with zero rows
+// to a multiple of 128. Ring buffers hold the rows of one macrobatch:
+// ring row = padded row - offp[m*E] + ring_base.
+struct GemmArgs {
+    CUtensorMap a0, a1, b0, b1;   // TMA maps (bf16, 128-byte swizzle, 64-element inner box)
+    const int *offp;              // [nM*E + 1] padded run starts
+    int E, nM, m;                 // experts, macrobatches, macrobatch of a grouped-M launch
+    int H, F;
+    int N, K, Mw;                 // output columns, contraction length (grouped-M), rows of dW (grouped-K)
+    int a_ring;                   // A rows are ring rows
+    int o_ring;                   // FWD2 output rows are ring rows
+    int ring_base;
+    bf16 *o0, *o1, *o2;           // bf16 outputs (see each op)
+    float *of0, *of1;             // fp32 outputs
+    const bf16 *in0, *in1;        // BWD2: saved a, b
+    const int *row_slot;          // BWD2: slot of each padded row (-1 = padding)
+    const float *wslot;           // BWD2: router weight of each slot
+    int accumulate;               // WG ops: add into the fp32 outputs
+    int *status;
+    unsigned long long budget_ns;
+};
+
+cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,626 @@
+// Host side of the C ABI declared in include/moe.h: argument checks, the
+// execution plan (minibatch, macrobatches, ring), carving of the caller's
+// workspace and saved buffers, TMA tensor maps, and the launch sequence of the
+// forward and backward passes. Nothing here allocates device memory.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "grouped_gemm.cuh"
+#include "route_kernels.cuh"
+
+using namespace moe;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status_t fail(moe_status_t s, const std::string &msg) {
+    g_last_error = msg;
+    return s;
+}
+
+// ---------------------------------------------------------------- profiling
+// Thread-local record of (kernel name, start event, end event) around every
+// launch while moe_profile_begin is active.
+struct ProfRec {
+    const char *name;
+    cudaEvent_t start, end;
+};
+struct Profiler {
+    bool on = false;
+    std::vector<ProfRec> recs;
+};
+thread_local Profiler g_prof;
+
+struct ProfScope {
+    ProfRec rec{};
+    cudaStream_t stream;
+    bool active;
+    ProfScope(const char *name, cudaStream_t s) : stream(s), active(g_prof.on) {
+        if (!active) return;
+        rec.name = name;
+        cudaEventCreate(&rec.start);
+        cudaEventCreate(&rec.end);
+        cudaEventRecord(rec.start, stream);
+    }
+    ~ProfScope() {
+        if (!active) return;
+        cudaEventRecord(rec.end, stream);
+        g_prof.recs.push_back(rec);
+    }
+};
+
+constexpr int kGemmBN1 = 256;   // GEMM1 tile: 128 rows x (128 a-columns + 128 b-columns)
+constexpr int kGemmBM = 128;
+
+// ---------------------------------------------------------------- planning
+
+int query_num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+moe_status_t check_shape(const moe_config_t *c) {
+    if (!c) return fail(MOE_ERR_INVALID_ARG, "config is NULL");
+    if (c->T < 0 || c->H <= 0 || c->F <= 0 || c->E <= 0 || c->k <= 0)
+        return fail(MOE_ERR_INVALID_ARG, "T must be >= 0 and H, F, E, k > 0");
+    if (c->E > kMaxExperts) return fail(MOE_ERR_UNSUPPORTED, "E > 64 experts is not supported");
+    if (c->k > c->E) return fail(MOE_ERR_INVALID_ARG, "k > E");
+    if (c->k > 32) return fail(MOE_ERR_UNSUPPORTED, "k > 32 is not supported");
+    if (c->H % 256 || c->F % 256) return fail(MOE_ERR_UNSUPPORTED, "H and F must be multiples of 256");
+    if (c->precision != MOE_PRECISION_BF16 && c->precision != MOE_PRECISION_MXFP8)
+        return fail(MOE_ERR_INVALID_ARG, "unknown precision");
+    if (c->minibatch_rows < 0 || c->macrobatch_tokens < 0) return fail(MOE_ERR_INVALID_ARG, "negative minibatch/macrobatch");
+    const long long R = (long long)c->T * c->k;
+    if (R > (1LL << 30) / 2) return fail(MOE_ERR_UNSUPPORTED, "T*k too large");
+    return MOE_OK;
+}
+
+size_t a1024(size_t v) { return align_up(v, 1024); }
+
+// Minimum minibatch: GEMM1 covers the 2F columns of [W1|W3] with tiles of
+// 128 rows x 256 columns, so r rows give (r/128)(2F/256) tiles; two full waves
+// on S SMs need r >= 2 S 128 256 / (2F).
+int minibatch_floor(int num_sms, int F) {
+    const long long num = 2LL * num_sms * kGemmBM * kGemmBN1;
+    const long long den = 2LL * F;
+    return (int)((num + den - 1) / den);
+}
+
+moe_status_t make_layout(const moe_config_t *c, Layout &L) {
+    moe_status_t st = check_shape(c);
+    if (st != MOE_OK) return st;
+    std::memset(&L, 0, sizeof(L));
+    L.T = c->T; L.H = c->H; L.F = c->F; L.E = c->E; L.k = c->k;
+    L.R = c->T * c->k;
+    L.precision = c->precision;
+    L.num_sms = c->num_sms > 0 ? c->num_sms : query_num_sms();
+    if (L.num_sms <= 0) return fail(MOE_ERR_CUDA, "could not query the SM count (no device?)");
+    const int floor_rows = minibatch_floor(L.num_sms, c->F);
+    L.minibatch_rows = c->minibatch_rows > 0 ? c->minibatch_rows : floor_rows;
+    const bool mx = c->precision == MOE_PRECISION_MXFP8;
+    const size_t xrow = mx ? (size_t)c->H + c->H / kMxBlock : 2 * (size_t)c->H;
+    const size_t hrow = mx ? (size_t)c->F + c->F / kMxBlock : 2 * (size_t)c->F;
+    const size_t yrow = 2 * (size_t)c->H;
+    const size_t ring_row_bytes = xrow + hrow + yrow;
+    const int pad = (kRowPad - 1) * c->E;
+    int Mb;
+    if (c->macrobatch_tokens > 0) {
+        Mb = c->macrobatch_tokens;
+    } else if (c->ring_bytes == 0) {
+        Mb = c->T > 0 ? c->T : 1;
+    } else {
+        // largest Mb whose two ring halves fit: 2 * (Mb*k + pad) * row_bytes <= ring_bytes
+        const long long rows_half = (long long)(c->ring_bytes / ring_row_bytes) / 2 - pad;
+        if (rows_half < c->k) return fail(MOE_ERR_UNSUPPORTED, "ring_bytes too small for one token per macrobatch");
+        Mb = (int)(rows_half / c->k);
+    }
+    if (c->T > 0 && Mb > c->T) Mb = c->T;
+    if (Mb <= 0) Mb = 1;
+    L.Mb = Mb;
+    L.nM = c->T > 0 ? ceil_div(c->T, Mb) : 1;
+    L.ring_halves = L.nM > 1 ? 2 : 1;
+    const long long rows_pad_max = (long long)L.R + (long long)L.nM * pad;
+    const long long half_rows = (long long)std::min<long long>((long long)Mb * c->k, L.R) + pad;
+    L.rows_pad_max = (int)align_up((size_t)std::max<long long>(rows_pad_max, kRowPad), kRowPad);
+    L.half_rows = L.nM > 1 ? (int)align_up((size_t)half_rows, kRowPad) : L.rows_pad_max;
+    L.chunks_per_mb = std::max(1, ceil_div(std::min(Mb, std::max(c->T, 1)) * c->k, kSchedChunk));
+    L.nchunks = c->T > 0 ? L.nM * L.chunks_per_mb : 0;
+    L.dwr_splits = std::max(1, std::min(16, ceil_div(std::max(c->T, 1), 512)));
+
+    const size_t R = L.R, T = L.T, E = L.E, H = L.H, F = L.F, nM = L.nM, rp = L.rows_pad_max;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = a1024(o + std::max<size_t>(bytes, 1)); return at; };
+    L.s_ids = take(4 * R);
+    L.s_w = take(4 * R);
+    L.s_probs = take(4 * T * E);
+    L.s_counts = take(4 * nM * E);
+    L.s_offsets = take(4 * nM * (E + 1));
+    L.s_offp = take(4 * (nM * E + 1));
+    L.s_s2sorted = take(4 * R);
+    L.s_sorted2s = take(4 * R);
+    L.s_slot_row = take(4 * R);
+    L.s_row_slot = take(4 * rp);
+    L.s_a = take(2 * rp * F);
+    L.s_b = take(2 * rp * F);
+    L.saved_bytes = o;
+
+    o = 0;
+    L.w_status = take(256);
+    L.w_chunk_counts = take(4 * std::max(L.nchunks, 1) * E);
+    L.w_chunk_base = take(4 * std::max(L.nchunks, 1) * E);
+    const size_t EP = (E + 7) / 8 * 8;
+    L.w_wrt = take(2 * EP * H);
+    L.w_offp = take(4 * (nM * E + 1));
+    const size_t region = o;
+    const size_t ring_rows = (size_t)L.half_rows * L.ring_halves;
+    // forward region: the ring
+    o = region;
+    L.w_ringX = take(ring_rows * (mx ? H : 2 * H));
+    L.w_ringXs = mx ? take(ring_rows * (H / kMxBlock)) : 0;
+    L.w_ringH = take(ring_rows * (mx ? F : 2 * F));
+    L.w_ringHs = mx ? take(ring_rows * (F / kMxBlock)) : 0;
+    L.w_ringY = take(ring_rows * 2 * H);
+    L.ring_bytes = o - region;
+    const size_t fwd_end = o;
+    // backward region
+    o = region;
+    L.w_Xs = take(rp * 2 * H);
+    L.w_Gin = take(rp * 2 * H);
+    L.w_da = take(rp * 2 * F);
+    L.w_db = take(rp * 2 * F);
+    L.w_hw = take(rp * 2 * F);
+    L.w_dXs = take(rp * 2 * H);
+    L.w_dwpart = take(4 * rp * (F / 256));
+    L.w_dlogits = take(4 * T * E);
+    L.w_dwr_part = take(4 * (size_t)L.dwr_splits * H * E);
+    const size_t bwd_end = o;
+    L.workspace_bytes = std::max(fwd_end, bwd_end);
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, cols] array; box = 64 columns (128 B,
+// the 128-byte swizzle span) x box_rows rows.
+bool make_map(CUtensorMap *m, const void *base, size_t rows, size_t cols, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || rows == 0) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Workspace and saved buffers may start anywhere: the library uses them from
+// the next 1024-byte boundary on (TMA tiles and the layout want that), and the
+// size queries include that slack.
+constexpr size_t kBaseSlack = 1024;
+void *align_base(void *p) {
+    return reinterpret_cast<void *>((reinterpret_cast<uintptr_t>(p) + kBaseSlack - 1) & ~uintptr_t(kBaseSlack - 1));
+}
+const void *align_base(const void *p) { return align_base(const_cast<void *>(p)); }
+bool fits(const void *base, size_t bytes, size_t need) {
+    const size_t lost = reinterpret_cast<uintptr_t>(align_base(base)) - reinterpret_cast<uintptr_t>(base);
+    return bytes >= lost && bytes - lost >= need;
+}
+
+template <class T>
+T *at(void *base, size_t off) { return reinterpret_cast<T *>(static_cast<char *>(base) + off); }
+template <class T>
+const T *at(const void *base, size_t off) { return reinterpret_cast<const T *>(static_cast<const char *>(base) + off); }
+
+moe_status_t cuda_check(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return MOE_OK;
+    return fail(MOE_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+unsigned long long budget_ns(const moe_config_t *c) {
+    return (unsigned long long)(c->timeout_ms ? c->timeout_ms : 2000u) * 1000000ull;
+}
+
+SchedArgs sched_args(const Layout &L, const int32_t *ids, void *ws, int32_t *counts, int32_t *offsets, int32_t *offp,
+                     int32_t *s2s, int32_t *s2sorted, int32_t *slot_row, int32_t *row_slot) {
+    SchedArgs a{};
+    a.ids = ids;
+    a.T = L.T; a.k = L.k; a.E = L.E; a.Mb = L.Mb; a.nM = L.nM;
+    a.chunks_per_mb = L.chunks_per_mb; a.nchunks = L.nchunks;
+    a.chunk_counts = at<int>(ws, L.w_chunk_counts);
+    a.chunk_base = at<int>(ws, L.w_chunk_base);
+    a.counts = counts; a.offsets = offsets; a.offp = offp;
+    a.sorted_to_slot = s2s; a.slot_to_sorted = s2sorted;
+    a.slot_row = slot_row; a.row_slot = row_slot;
+    a.status = at<int>(ws, L.w_status);
+    return a;
+}
+
+GemmArgs gemm_base(const Layout &L, void *ws, const int32_t *offp, const moe_config_t *c) {
+    GemmArgs g;
+    std::memset(&g, 0, sizeof(g));
+    g.offp = offp;
+    g.E = L.E; g.nM = L.nM; g.H = L.H; g.F = L.F;
+    g.status = at<int>(ws, L.w_status);
+    g.budget_ns = budget_ns(c);
+    return g;
+}
+
+}  // namespace
+
+// ======================================================================== ABI
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char *moe_last_error_string(void) { return g_last_error.c_str(); }
+
+moe_status_t moe_profile_begin(void) {
+    for (auto &r : g_prof.recs) {
+        cudaEventDestroy(r.start);
+        cudaEventDestroy(r.end);
+    }
+    g_prof.recs.clear();
+    g_prof.on = true;
+    return MOE_OK;
+}
+
+int moe_profile_end(moe_kernel_time_t *out, int max_entries) {
+    g_prof.on = false;
+    std::vector<moe_kernel_time_t> rows;
+    int rc = 0;
+    for (auto &r : g_prof.recs) {
+        float ms = 0.0f;
+        if (cudaEventSynchronize(r.end) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.end) != cudaSuccess)
+            rc = -(int)MOE_ERR_CUDA;
+        size_t i = 0;
+        for (; i < rows.size(); ++i)
+            if (std::strncmp(rows[i].name, r.name, sizeof(rows[i].name)) == 0) break;
+        if (i == rows.size()) {
+            moe_kernel_time_t t{};
+            std::strncpy(t.name, r.name, sizeof(t.name) - 1);
+            rows.push_back(t);
+        }
+        rows[i].launches += 1;
+        rows[i].total_ms += ms;
+        cudaEventDestroy(r.start);
+        cudaEventDestroy(r.end);
+    }
+    g_prof.recs.clear();
+    if (rc < 0) return fail(MOE_ERR_CUDA, "profiling events failed"), rc;
+    for (size_t i = 0; i < rows.size() && (int)i < max_entries; ++i) out[i] = rows[i];
+    return (int)rows.size();
+}
+
+moe_status_t moe_plan(const moe_config_t *cfg, moe_plan_t *plan) {
+    if (!plan) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+    Layout L;
+    moe_status_t st = make_layout(cfg, L);
+    if (st != MOE_OK) return st;
+    plan->num_sms = L.num_sms;
+    plan->minibatch_rows = L.minibatch_rows;
+    plan->macrobatch_tokens = L.Mb;
+    plan->num_macrobatches = L.nM;
+    plan->rows_padded_max = L.rows_pad_max;
+    plan->ring_rows = L.half_rows * L.ring_halves;
+    plan->ring_bytes = L.ring_bytes;
+    plan->workspace_bytes = L.workspace_bytes + kBaseSlack;
+    plan->saved_bytes = L.saved_bytes + kBaseSlack;
+    plan->qweights_bytes = 0;
+    return MOE_OK;
+}
+
+size_t moe_workspace_size(const moe_config_t *cfg) {
+    Layout L;
+    return make_layout(cfg, L) == MOE_OK ? L.workspace_bytes + kBaseSlack : 0;
+}
+
+size_t moe_saved_size(const moe_config_t *cfg) {
+    Layout L;
+    return make_layout(cfg, L) == MOE_OK ? L.saved_bytes + kBaseSlack : 0;
+}
+
+size_t moe_qweights_size(const moe_config_t *cfg) {
+    (void)cfg;
+    return 0;
+}
+
+moe_status_t moe_quantize_weights(const moe_config_t *cfg, const void *W1, const void *W3, const void *W2,
+                                  void *qweights, size_t qweights_bytes, moe_stream_t stream) {
+    (void)W1; (void)W3; (void)W2; (void)qweights; (void)qweights_bytes; (void)stream;
+    moe_status_t st = check_shape(cfg);
+    if (st != MOE_OK) return st;
+    return fail(MOE_ERR_UNSUPPORTED, "MXFP8 weight quantisation is not available in this build");
+}
+
+moe_status_t moe_reset_status(void *workspace, moe_stream_t stream) {
+    if (!workspace) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+    return cuda_check(cudaMemsetAsync(align_base(workspace), 0, 256, (cudaStream_t)stream), "cudaMemsetAsync(status)");
+}
+
+moe_status_t moe_query_status(void *workspace, moe_stream_t stream) {
+    if (!workspace) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+    moe_status_t st = cuda_check(cudaStreamSynchronize((cudaStream_t)stream), "cudaStreamSynchronize");
+    if (st != MOE_OK) return st;
+    int v = 0;
+    void *status = align_base(workspace);
+    st = cuda_check(cudaMemcpy(&v, status, sizeof(int), cudaMemcpyDeviceToHost), "cudaMemcpy(status)");
+    if (st != MOE_OK) return st;
+    st = cuda_check(cudaMemset(status, 0, sizeof(int)), "cudaMemset(status)");
+    if (st != MOE_OK) return st;
+    if (v == MOE_ERR_TIMEOUT) return fail(MOE_ERR_TIMEOUT, "a device-side wait ran out of time");
+    if (v != 0) return fail(MOE_ERR_INTERNAL, "a device-side check failed (status " + std::to_string(v) + ")");
+    return MOE_OK;
+}
+
+moe_status_t moe_schedule(const moe_config_t *cfg, const int32_t *topk_ids, int32_t *counts, int32_t *offsets,
+                          int32_t *sorted_to_slot, int32_t *slot_to_sorted, void *workspace, size_t workspace_bytes,
+                          moe_stream_t stream) {
+    Layout L;
+    moe_status_t st = make_layout(cfg, L);
+    if (st != MOE_OK) return st;
+    if (!counts || !offsets || !workspace || (L.R > 0 && (!topk_ids || !sorted_to_slot || !slot_to_sorted)))
+        return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
+    if (!fits(workspace, workspace_bytes, L.workspace_bytes)) return fail(MOE_ERR_WORKSPACE, "workspace too small");
+    workspace = align_base(workspace);
+    cudaStream_t s = (cudaStream_t)stream;
+    st = cuda_check(cudaMemsetAsync(at<int>(workspace, L.w_status), 0, 256, s), "status clear");
+    if (st != MOE_OK) return st;
+    int32_t *offp = at<int32_t>(workspace, L.w_offp);   // padded run starts (scratch)
+    SchedArgs a = sched_args(L, topk_ids, workspace, counts, offsets, offp, sorted_to_slot, slot_to_sorted, nullptr,
+                             nullptr);
+    {
+        ProfScope ps("schedule", s);
+        st = cuda_check(launch_schedule(a, s), "schedule launch");
+    }
+    return st;
+}
+
+moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r, const float *bias, const void *W1,
+                         const void *W3, const void *W2, const void *qweights, void *out, int32_t *topk_ids,
+                         float *topk_w, void *saved, size_t saved_bytes, void *workspace, size_t workspace_bytes,
+                         moe_stream_t stream) {
+    Layout L;
+    moe_status_t st = make_layout(cfg, L);
+    if (st != MOE_OK) return st;
+    if (cfg->precision == MOE_PRECISION_MXFP8 && !qweights)
+        return fail(MOE_ERR_INVALID_ARG, "MXFP8 forward needs qweights");
+    if (cfg->precision == MOE_PRECISION_MXFP8)
+        return fail(MOE_ERR_UNSUPPORTED, "MXFP8 forward is not available in this build");
+    if (!W_r || !W1 || !W3 || !W2 || !saved || !workspace || (L.T > 0 && (!x || !out || !topk_ids || !topk_w)))
+        return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
+    if (!fits(saved, saved_bytes, L.saved_bytes)) return fail(MOE_ERR_WORKSPACE, "saved buffer too small");
+    if (!fits(workspace, workspace_bytes, L.workspace_bytes)) return fail(MOE_ERR_WORKSPACE, "workspace too small");
+    saved = align_base(saved);
+    workspace = align_base(workspace);
+    const void *ptrs16[] = {x, W_r, W1, W3, W2, out};
+    for (const void *p : ptrs16)
+        if (p && !aligned(p, 16)) return fail(MOE_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    void *ws = workspace;
+    st = cuda_check(cudaMemsetAsync(at<int>(ws, L.w_status), 0, 256, s), "status clear");
+    if (st != MOE_OK) return st;
+
+    int32_t *s_ids = at<int32_t>(saved, L.s_ids);
+    float *s_w = at<float>(saved, L.s_w);
+    float *s_probs = at<float>(saved, L.s_probs);
+    int32_t *s_offp = at<int32_t>(saved, L.s_offp);
+    int32_t *s_slot_row = at<int32_t>(saved, L.s_slot_row);
+    int32_t *s_row_slot = at<int32_t>(saved, L.s_row_slot);
+    bf16 *s_a = at<bf16>(saved, L.s_a);
+    bf16 *s_b = at<bf16>(saved, L.s_b);
+
+    // 1. router
+    RouterArgs ra{};
+    ra.x = (const bf16 *)x; ra.Wr = (const bf16 *)W_r; ra.bias = bias;
+    ra.WrT = at<bf16>(ws, L.w_wrt);
+    ra.T = L.T; ra.H = L.H; ra.E = L.E; ra.k = L.k;
+    ra.probs = s_probs; ra.ids = topk_ids; ra.w = topk_w; ra.ids2 = s_ids; ra.w2 = s_w;
+    {
+        ProfScope ps("router_topk", s);
+        st = cuda_check(launch_router(ra, s), "router launch");
+    }
+    if (st != MOE_OK) return st;
+
+    // 2. schedule
+    SchedArgs sa = sched_args(L, s_ids, ws, at<int32_t>(saved, L.s_counts), at<int32_t>(saved, L.s_offsets), s_offp,
+                              at<int32_t>(saved, L.s_sorted2s), at<int32_t>(saved, L.s_s2sorted), s_slot_row,
+                              s_row_slot);
+    {
+        ProfScope ps("schedule", s);
+        st = cuda_check(launch_schedule(sa, s), "schedule launch");
+    }
+    if (st != MOE_OK) return st;
+
+    // 3. per macrobatch: dispatch -> GEMM1+SwiGLU -> GEMM2 -> combine
+    bf16 *ringX = at<bf16>(ws, L.w_ringX), *ringH = at<bf16>(ws, L.w_ringH), *ringY = at<bf16>(ws, L.w_ringY);
+    const size_t ring_rows = (size_t)L.half_rows * L.ring_halves;
+    GemmArgs g1 = gemm_base(L, ws, s_offp, cfg), g2 = gemm_base(L, ws, s_offp, cfg);
+    if (!make_map(&g1.a0, ringX, ring_rows, L.H, 128) || !make_map(&g1.b0, W1, (size_t)L.E * L.H, L.F, 64) ||
+        !make_map(&g1.b1, W3, (size_t)L.E * L.H, L.F, 64) || !make_map(&g2.a0, ringH, ring_rows, L.F, 128) ||
+        !make_map(&g2.b0, W2, (size_t)L.E * L.F, L.H, 64))
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    g1.N = L.F; g1.K = L.H; g1.a_ring = 1;
+    g1.o0 = s_a; g1.o1 = s_b; g1.o2 = ringH;
+    g2.N = L.H; g2.K = L.F; g2.a_ring = 1; g2.o_ring = 1;
+    g2.o0 = ringY;
+    for (int m = 0; m < L.nM; ++m) {
+        const int ring_base = (m % L.ring_halves) * L.half_rows;
+        DispatchArgs da{};
+        da.src = (const bf16 *)x; da.dst = ringX; da.row_slot = s_row_slot; da.offp = s_offp;
+        da.beg = m * L.E; da.end = (m + 1) * L.E; da.dst_row0 = ring_base; da.H = L.H; da.k = L.k;
+        {
+            ProfScope ps("dispatch", s);
+            st = cuda_check(launch_dispatch(da, L.half_rows, L.num_sms, s), "dispatch launch");
+        }
+        if (st != MOE_OK) return st;
+        g1.m = m; g1.ring_base = ring_base;
+        {
+            ProfScope ps("grouped_gemm_fwd1_swiglu", s);
+            st = cuda_check(launch_grouped_gemm(OP_FWD1, g1, L.num_sms, s), "GEMM1 launch");
+        }
+        if (st != MOE_OK) return st;
+        g2.m = m; g2.ring_base = ring_base;
+        {
+            ProfScope ps("grouped_gemm_fwd2", s);
+            st = cuda_check(launch_grouped_gemm(OP_FWD2, g2, L.num_sms, s), "GEMM2 launch");
+        }
+        if (st != MOE_OK) return st;
+        CombineArgs ca{};
+        ca.Y = ringY; ca.slot_row = s_slot_row; ca.offp = s_offp; ca.w = s_w; ca.out = (bf16 *)out;
+        ca.t0 = m * L.Mb; ca.t1 = std::min(L.T, (m + 1) * L.Mb); ca.k = L.k; ca.H = L.H; ca.E = L.E; ca.m = m;
+        ca.ring_base = ring_base;
+        {
+            ProfScope ps("combine", s);
+            st = cuda_check(launch_combine(ca, L.num_sms, s), "combine launch");
+        }
+        if (st != MOE_OK) return st;
+    }
+    return MOE_OK;
+}
+
+moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void *x, const void *W_r, const void *W1,
+                          const void *W3, const void *W2, const void *qweights, const void *saved, void *dx,
+                          float *dW_r, float *dW1, float *dW3, float *dW2, int accumulate, void *workspace,
+                          size_t workspace_bytes, moe_stream_t stream) {
+    (void)qweights;
+    Layout L;
+    moe_status_t st = make_layout(cfg, L);
+    if (st != MOE_OK) return st;
+    if (cfg->precision == MOE_PRECISION_MXFP8)
+        return fail(MOE_ERR_UNSUPPORTED, "MXFP8 backward is not available in this build");
+    if (!W_r || !W1 || !W3 || !W2 || !saved || !workspace || !dW_r || !dW1 || !dW3 || !dW2 ||
+        (L.T > 0 && (!x || !dout || !dx)))
+        return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
+    if (!fits(workspace, workspace_bytes, L.workspace_bytes)) return fail(MOE_ERR_WORKSPACE, "workspace too small");
+    saved = align_base(saved);
+    workspace = align_base(workspace);
+    const void *ptrs16[] = {x, dout, W_r, W1, W3, W2, dx, dW_r, dW1, dW3, dW2};
+    for (const void *p : ptrs16)
+        if (p && !aligned(p, 16)) return fail(MOE_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    void *ws = workspace;
+
+    const int32_t *s_ids = at<int32_t>(saved, L.s_ids);
+    const float *s_w = at<float>(saved, L.s_w);
+    const float *s_probs = at<float>(saved, L.s_probs);
+    const int32_t *s_offp = at<int32_t>(saved, L.s_offp);
+    const int32_t *s_slot_row = at<int32_t>(saved, L.s_slot_row);
+    const int32_t *s_row_slot = at<int32_t>(saved, L.s_row_slot);
+    const bf16 *s_a = at<bf16>(saved, L.s_a);
+    const bf16 *s_b = at<bf16>(saved, L.s_b);
+    bf16 *Xs = at<bf16>(ws, L.w_Xs), *Gin = at<bf16>(ws, L.w_Gin), *dA = at<bf16>(ws, L.w_da),
+         *dB = at<bf16>(ws, L.w_db), *HW = at<bf16>(ws, L.w_hw), *dXs = at<bf16>(ws, L.w_dXs);
+    float *dwpart = at<float>(ws, L.w_dwpart), *dlogits = at<float>(ws, L.w_dlogits);
+    const size_t rp = L.rows_pad_max;
+
+    // 1. replay dispatch (X rows) and reverse combine (dout rows), all macrobatches
+    if (L.T > 0) {
+        DispatchArgs d1{};
+        d1.src = (const bf16 *)x; d1.dst = Xs; d1.row_slot = s_row_slot; d1.offp = s_offp;
+        d1.beg = 0; d1.end = L.nM * L.E; d1.dst_row0 = 0; d1.H = L.H; d1.k = L.k;
+        {
+            ProfScope ps("dispatch_replay", s);
+            st = cuda_check(launch_dispatch(d1, L.rows_pad_max, L.num_sms, s), "replay dispatch launch");
+        }
+        if (st != MOE_OK) return st;
+        DispatchArgs d2 = d1;
+        d2.src = (const bf16 *)dout; d2.dst = Gin;
+        {
+            ProfScope ps("reverse_combine", s);
+            st = cuda_check(launch_dispatch(d2, L.rows_pad_max, L.num_sms, s), "reverse combine launch");
+        }
+        if (st != MOE_OK) return st;
+    }
+    GemmArgs gb2 = gemm_base(L, ws, s_offp, cfg), gb1 = gemm_base(L, ws, s_offp, cfg);
+    GemmArgs gw2 = gemm_base(L, ws, s_offp, cfg), gw13 = gemm_base(L, ws, s_offp, cfg);
+    if (!make_map(&gb2.a0, Gin, rp, L.H, 128) || !make_map(&gb2.b0, W2, (size_t)L.E * L.F, L.H, 256) ||
+        !make_map(&gb1.a0, dA, rp, L.F, 128) || !make_map(&gb1.a1, dB, rp, L.F, 128) ||
+        !make_map(&gb1.b0, W1, (size_t)L.E * L.H, L.F, 256) || !make_map(&gb1.b1, W3, (size_t)L.E * L.H, L.F, 256) ||
+        !make_map(&gw2.a0, HW, rp, L.F, 64) || !make_map(&gw2.b0, Gin, rp, L.H, 64) ||
+        !make_map(&gw13.a0, Xs, rp, L.H, 64) || !make_map(&gw13.b0, dA, rp, L.F, 64) ||
+        !make_map(&gw13.b1, dB, rp, L.F, 64))
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    // 2. GEMM2 dgrad + SwiGLU backward, per macrobatch (global rows)
+    gb2.N = L.F; gb2.K = L.H;
+    gb2.in0 = s_a; gb2.in1 = s_b; gb2.o0 = dA; gb2.o1 = dB; gb2.o2 = HW; gb2.of0 = dwpart;
+    gb2.row_slot = s_row_slot; gb2.wslot = s_w;
+    gb1.N = L.H; gb1.K = 2 * L.F; gb1.o0 = dXs;
+    if (L.T > 0) {
+        for (int m = 0; m < L.nM; ++m) {
+            gb2.m = m;
+            {
+                ProfScope ps("grouped_gemm_bwd2_swiglu", s);
+                st = cuda_check(launch_grouped_gemm(OP_BWD2, gb2, L.num_sms, s), "GEMM2 dgrad launch");
+            }
+            if (st != MOE_OK) return st;
+        }
+        for (int m = 0; m < L.nM; ++m) {
+            gb1.m = m;
+            {
+                ProfScope ps("grouped_gemm_bwd1", s);
+                st = cuda_check(launch_grouped_gemm(OP_BWD1, gb1, L.num_sms, s), "GEMM1 dgrad launch");
+            }
+            if (st != MOE_OK) return st;
+        }
+    }
+    // 3. router backward, reverse dispatch, router weight gradient
+    RouterBwdArgs rb{};
+    rb.dw_part = dwpart; rb.nparts = L.F / 256; rb.slot_row = s_slot_row; rb.ids = s_ids; rb.w = s_w;
+    rb.probs = s_probs; rb.dlogits = dlogits; rb.T = L.T; rb.k = L.k; rb.E = L.E;
+    RevDispatchArgs rd{};
+    rd.dXs = dXs; rd.slot_row = s_slot_row; rd.dlogits = dlogits; rd.Wr = (const bf16 *)W_r; rd.dx = (bf16 *)dx;
+    rd.T = L.T; rd.k = L.k; rd.E = L.E; rd.H = L.H;
+    RouterWgradArgs rw{};
+    rw.x = (const bf16 *)x; rw.dlogits = dlogits; rw.part = at<float>(ws, L.w_dwr_part); rw.dWr = dW_r;
+    rw.T = L.T; rw.H = L.H; rw.E = L.E; rw.splits = L.dwr_splits; rw.accumulate = accumulate;
+    {
+        ProfScope ps("router_bwd", s);
+        st = cuda_check(launch_router_bwd(rb, rd, rw, s), "router backward launch");
+    }
+    if (st != MOE_OK) return st;
+    // 4. weight gradients (contraction over each expert's rows, all macrobatches)
+    gw2.Mw = L.F; gw2.N = L.H; gw2.of0 = dW2; gw2.accumulate = accumulate;
+    {
+        ProfScope ps("grouped_gemm_wgrad2", s);
+        st = cuda_check(launch_grouped_gemm(OP_WG2, gw2, L.num_sms, s), "dW2 launch");
+    }
+    if (st != MOE_OK) return st;
+    gw13.Mw = L.H; gw13.N = L.F; gw13.of0 = dW1; gw13.of1 = dW3; gw13.accumulate = accumulate;
+    {
+        ProfScope ps("grouped_gemm_wgrad13", s);
+        st = cuda_check(launch_grouped_gemm(OP_WG13, gw13, L.num_sms, s), "dW1/dW3 launch");
+    }
+    return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,623 @@
+// Router, schedule, dispatch, combine and the token-side backward kernels.
+//
+//   router_topk      logits = x W_r (+bias) in fp32 on tensor cores (mma.sync,
+//                    fixed-order reduction), softmax, top-k (descending, ties to
+//                    the lower expert index), renormalised weights
+//   schedule_*       per-(macrobatch, expert) counts with warp match/ballot
+//                    histograms, exclusive scans, stable scatter (article
+//                    "O MoK do Cursor ...", section 01: count, place, group)
+//   dispatch_rows    pull-style gather of token rows into expert-sorted rows
+//                    (section 02: the destination reads the rows it needs)
+//   combine          top-k weighted sum in fixed slot order (section 03:
+//                    combine and final weighted fusion; deterministic)
+//   router_bwd       dw -> dp -> dlogits through renormalisation and softmax
+//   reverse_dispatch dx = sum_j dX rows (fixed order) + dlogits W_r^T
+//   router_wgrad     dW_r = x^T dlogits with fixed-order split reduction
+#include "route_kernels.cuh"
+
+namespace moe {
+
+// ------------------------------------------------------------------ router
+
+// W_r [H,E] -> WrT [EP,H] (EP = E rounded up to 8, extra rows zero), so the
+// tensor-core B fragments are contiguous along H.
+__global__ void transpose_wr_kernel(const bf16 *__restrict__ Wr, bf16 *__restrict__ WrT, int H, int E, int EP) {
+    int h = blockIdx.x * blockDim.x + threadIdx.x;
+    if (h >= H) return;
+    for (int e = 0; e < EP; ++e) WrT[(size_t)e * H + h] = e < E ? Wr[(size_t)h * E + e] : f2bf(0.0f);
+}
+
+__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+constexpr int kRouterTokens = 32;   // tokens per block
+constexpr int kRouterWarps = 8;     // warps split H
+
+// Block: 32 tokens x all experts. Warp w covers H range [w*H/8, (w+1)*H/8).
+// The contraction order inside a warp is permuted (thread c of a quad loads 8
+// consecutive h with one 16-byte load and feeds them as its k-slots of two
+// m16n8k16 steps); A and B use the same permutation, so the sum is exact in
+// structure and fixed in order.
+template <int NT>
+__global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a) {
+    extern __shared__ float part[];   // [warps][32 tokens][EP]
+    const int EP = NT * 8;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int g = lane >> 2, c = lane & 3;
+    const int t0 = blockIdx.x * kRouterTokens;
+    const int hspan = a.H / kRouterWarps;
+    const int hbeg = warp * hspan;
+    float acc[2][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[mt][n][i] = 0.0f;
+    // the four token rows this thread feeds: mt*16 + g and mt*16 + g + 8
+    const bf16 *xrow[2][2];
+    bool valid[2][2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            int t = t0 + mt * 16 + g + hh * 8;
+            valid[mt][hh] = t < a.T;
+            xrow[mt][hh] = a.x + (size_t)(valid[mt][hh] ? t : 0) * a.H;
+        }
+    for (int h0 = hbeg; h0 < hbeg + hspan; h0 += 32) {
+        const int hc = h0 + 8 * c;
+        uint4 xv[2][2];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+                xv[mt][hh] = valid[mt][hh] ? ld_nc_v4(xrow[mt][hh] + hc) : make_uint4(0, 0, 0, 0);
+        uint4 wv[NT];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) wv[n] = ld_nc_v4(a.WrT + (size_t)(n * 8 + g) * a.H + hc);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            // step 0 uses h = hc+0..3, step 1 uses hc+4..7
+            uint32_t A0[4] = {xv[mt][0].x, xv[mt][1].x, xv[mt][0].y, xv[mt][1].y};
+            uint32_t A1[4] = {xv[mt][0].z, xv[mt][1].z, xv[mt][0].w, xv[mt][1].w};
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                mma_16816_bf16(acc[mt][n], A0, wv[n].x, wv[n].y);
+                mma_16816_bf16(acc[mt][n], A1, wv[n].z, wv[n].w);
+            }
+        }
+    }
+    // partial logits of this warp -> shared memory
+    float *my = part + (size_t)warp * kRouterTokens * EP;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            int row = mt * 16 + g, col = n * 8 + 2 * c;
+            my[row * EP + col] = acc[mt][n][0];
+            my[row * EP + col + 1] = acc[mt][n][1];
+            my[(row + 8) * EP + col] = acc[mt][n][2];
+            my[(row + 8) * EP + col + 1] = acc[mt][n][3];
+        }
+    __syncthreads();
+    // each warp finishes 4 tokens; lane owns experts lane and lane+32
+    for (int tt = warp * 4; tt < warp * 4 + 4; ++tt) {
+        const int t = t0 + tt;
+        if (t >= a.T) break;
+        float l[2];
+        bool ok[2];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            int e = lane + 32 * s;
+            ok[s] = e < a.E;
+            float v = 0.0f;
+            if (ok[s]) {
+                for (int w = 0; w < kRouterWarps; ++w) v += part[((size_t)w * kRouterTokens + tt) * EP + e];
+                if (a.bias) v += a.bias[e];
+            }
+            l[s] = ok[s] ? v : -INFINITY;
+        }
+        float mx = fmaxf(l[0], l[1]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float ex[2], sum = 0.0f;
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            ex[s] = ok[s] ? __expf(l[s] - mx) : 0.0f;
+            sum += ex[s];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        const float inv = 1.0f / sum;
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+            if (ok[s]) a.probs[(size_t)t * a.E + lane + 32 * s] = ex[s] * inv;
+        // top-k: k rounds of a warp argmax over logits (ties -> lower index)
+        bool taken[2] = {!ok[0], !ok[1]};
+        float psel_sum = 0.0f;
+        float my_p = 0.0f;
+        int my_e = -1;
+        for (int j = 0; j < a.k; ++j) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                int e = lane + 32 * s;
+                if (!taken[s] && (l[s] > bv || (l[s] == bv && e < bi))) { bv = l[s]; bi = e; }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+            }
+#pragma unroll
+            for (int s = 0; s < 2; ++s)
+                if (lane + 32 * s == bi) taken[s] = true;
+            float p = __expf(bv - mx) * inv;
+            psel_sum += p;
+            if (lane == j) { my_p = p; my_e = bi; }
+        }
+        if (lane < a.k) {
+            const size_t o = (size_t)t * a.k + lane;
+            const float w = my_p / psel_sum;
+            a.ids[o] = my_e;
+            a.w[o] = w;
+            if (a.ids2) { a.ids2[o] = my_e; a.w2[o] = w; }
+        }
+    }
+}
+
+cudaError_t launch_router(const RouterArgs &a, cudaStream_t s) {
+    const int EP = (a.E + 7) / 8 * 8;
+    const int blocks = ceil_div(a.T, kRouterTokens);
+    const size_t smem = (size_t)kRouterWarps * kRouterTokens * EP * sizeof(float);
+    transpose_wr_kernel<<<ceil_div(a.H, 256), 256, 0, s>>>(a.Wr, a.WrT, a.H, a.E, EP);
+    if (blocks == 0) return cudaGetLastError();
+#define MOE_ROUTER_CASE(NT)                                                                           \
+    case NT: {                                                                                       \
+        cudaError_t e = cudaFuncSetAttribute(router_topk_kernel<NT>,                                 \
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+        if (e != cudaSuccess) return e;                                                              \
+        router_topk_kernel<NT><<<blocks, 256, smem, s>>>(a);                                         \
+        break;                                                                                       \
+    }
+    switch (EP / 8) {
+        MOE_ROUTER_CASE(1)
+        MOE_ROUTER_CASE(2)
+        MOE_ROUTER_CASE(3)
+        MOE_ROUTER_CASE(4)
+        MOE_ROUTER_CASE(5)
+        MOE_ROUTER_CASE(6)
+        MOE_ROUTER_CASE(7)
+        MOE_ROUTER_CASE(8)
+        default: return cudaErrorInvalidValue;
+    }
+#undef MOE_ROUTER_CASE
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ schedule
+//
+// Slots s = t*k + j of macrobatch m occupy [m*Mb*k, min(T,(m+1)*Mb)*k). Chunk
+// c = m*chunks_per_mb + i covers slots [m*Mb*k + i*kSchedChunk, ...) of that
+// macrobatch only. Inside a chunk, warp w walks its own contiguous sub-range of
+// 256 slots in order; the rank of a slot among equal experts is its warp's
+// running count plus its rank inside the 32-slot group (match_any + popc).
+
+__device__ __forceinline__ void chunk_range(const SchedArgs &a, int c, int &m, int &s0, int &s1) {
+    m = c / a.chunks_per_mb;
+    const int i = c % a.chunks_per_mb;
+    const int mb_s0 = m * a.Mb * a.k;
+    const int mb_s1 = min(a.T, (m + 1) * a.Mb) * a.k;
+    s0 = mb_s0 + i * kSchedChunk;
+    s1 = min(mb_s1, s0 + kSchedChunk);
+}
+
+// Pass over one chunk; calls f(slot, expert, rank_within_chunk) per valid slot
+// after the per-warp bases are known. With FINAL=false it only counts.
+template <bool FINAL>
+__device__ void chunk_pass(const SchedArgs &a, int c, int *s_warp_cnt /* [warps][E] */, int *s_base /* [E] */) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    int m, s0, s1;
+    chunk_range(a, c, m, s0, s1);
+    const int per_warp = kSchedChunk / kSchedWarps;
+    const int w0 = s0 + warp * per_warp, w1 = min(s1, w0 + per_warp);
+    int *cnt = s_warp_cnt + warp * a.E;
+    for (int e = lane; e < a.E; e += 32) cnt[e] = 0;
+    __syncwarp();
+    // counting walk
+    for (int base = w0; base < w1; base += 32) {
+        const int s = base + lane;
+        int e = s < w1 ? a.ids[s] : -1;
+        if (e >= a.E || (e < 0 && s < w1)) { raise_status(a.status, kStatusInternal); e = -1; }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int leader = __ffs(peers) - 1;
+        if (e >= 0 && lane == leader) cnt[e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    if (!FINAL) return;
+    // exclusive scan over warps per expert (in place: cnt becomes the warp base)
+    if (threadIdx.x < a.E) {
+        const int e = threadIdx.x;
+        int run = s_base[e];
+        for (int w = 0; w < kSchedWarps; ++w) {
+            int v = s_warp_cnt[w * a.E + e];
+            s_warp_cnt[w * a.E + e] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    // scatter walk
+    for (int base = w0; base < w1; base += 32) {
+        const int s = base + lane;
+        int e = s < w1 ? a.ids[s] : -1;
+        if (e >= a.E) e = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int leader = __ffs(peers) - 1;
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (e >= 0) {
+            const int pos = cnt[e] + rank;                 // unpadded sorted position
+            const int me = m * a.E + e;
+            const int prow = pos - a.offsets[m * (a.E + 1) + e] + a.offp[me];
+            a.sorted_to_slot[pos] = s;
+            a.slot_to_sorted[s] = pos;
+            if (a.slot_row) {
+                a.slot_row[s] = prow;
+                a.row_slot[prow] = s;
+            }
+        }
+        __syncwarp();
+        if (e >= 0 && lane == leader) cnt[e] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+__global__ void __launch_bounds__(kSchedWarps * 32) schedule_count_kernel(SchedArgs a) {
+    __shared__ int s_cnt[kSchedWarps * kMaxExperts];
+    chunk_pass<false>(a, blockIdx.x, s_cnt, nullptr);
+    if (threadIdx.x < a.E) {
+        int v = 0;
+        for (int w = 0; w < kSchedWarps; ++w) v += s_cnt[w * a.E + threadIdx.x];
+        a.chunk_counts[blockIdx.x * a.E + threadIdx.x] = v;
+    }
+}
+
+// One block: per-(m,e) counts, unpadded and padded exclusive scans, chunk bases,
+// and -1 marks on padding rows.
+__global__ void __launch_bounds__(1024) schedule_scan_kernel(SchedArgs a) {
+    __shared__ int s_tot[1024];
+    const int n = a.nM * a.E;
+    // counts and chunk bases (relative to the (m,e) start)
+    for (int me = threadIdx.x; me < n; me += blockDim.x) {
+        const int m = me / a.E, e = me % a.E;
+        int run = 0;
+        for (int i = 0; i < a.chunks_per_mb; ++i) {
+            const int c = m * a.chunks_per_mb + i;
+            a.chunk_base[c * a.E + e] = run;
+            run += a.chunk_counts[c * a.E + e];
+        }
+        a.counts[me] = run;
+    }
+    __syncthreads();
+    // sequential-in-blocks exclusive scan over (m, e): each thread owns a
+    // contiguous range, then the range totals are scanned
+    const int per = ceil_div(max(n, 1), (int)blockDim.x);
+    const int b0 = threadIdx.x * per, b1 = min(n, b0 + per);
+    int tot = 0, totp = 0;
+    for (int i = b0; i < b1; ++i) {
+        tot += a.counts[i];
+        totp += (a.counts[i] + kRowPad - 1) / kRowPad * kRowPad;
+    }
+    // pack (unpadded, padded) totals: each fits in 32 bits separately; scan twice
+    s_tot[threadIdx.x] = tot;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int i = 0; i < (int)blockDim.x; ++i) { int v = s_tot[i]; s_tot[i] = run; run += v; }
+    }
+    __syncthreads();
+    int run = s_tot[threadIdx.x];
+    __syncthreads();
+    s_tot[threadIdx.x] = totp;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int r = 0;
+        for (int i = 0; i < (int)blockDim.x; ++i) { int v = s_tot[i]; s_tot[i] = r; r += v; }
+    }
+    __syncthreads();
+    int runp = s_tot[threadIdx.x];
+    for (int i = b0; i < b1; ++i) {
+        const int m = i / a.E, e = i % a.E;
+        a.offsets[m * (a.E + 1) + e] = run;
+        a.offp[i] = runp;
+        run += a.counts[i];
+        runp += (a.counts[i] + kRowPad - 1) / kRowPad * kRowPad;
+        if (e == a.E - 1) a.offsets[m * (a.E + 1) + a.E] = run;
+    }
+    if (threadIdx.x == blockDim.x - 1) a.offp[n] = runp;
+    if (n == 0 && threadIdx.x == 0) a.offp[0] = 0;
+    __syncthreads();
+    // chunk bases become absolute sorted positions
+    for (int me = threadIdx.x; me < n; me += blockDim.x) {
+        const int m = me / a.E, e = me % a.E;
+        const int start = a.offsets[m * (a.E + 1) + e];
+        for (int i = 0; i < a.chunks_per_mb; ++i) a.chunk_base[(m * a.chunks_per_mb + i) * a.E + e] += start;
+    }
+    // padding rows of every (m, e) run hold no slot
+    if (a.row_slot) {
+        for (int me = threadIdx.x; me < n; me += blockDim.x) {
+            const int r1 = a.offp[me + 1];
+            for (int r = a.offp[me] + a.counts[me]; r < r1; ++r) a.row_slot[r] = -1;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kSchedWarps * 32) schedule_scatter_kernel(SchedArgs a) {
+    __shared__ int s_cnt[kSchedWarps * kMaxExperts];
+    __shared__ int s_base[kMaxExperts];
+    if (threadIdx.x < a.E) s_base[threadIdx.x] = a.chunk_base[blockIdx.x * a.E + threadIdx.x];
+    __syncthreads();
+    chunk_pass<true>(a, blockIdx.x, s_cnt, s_base);
+}
+
+cudaError_t launch_schedule(const SchedArgs &a, cudaStream_t s) {
+    if (a.nchunks > 0) schedule_count_kernel<<<a.nchunks, kSchedWarps * 32, 0, s>>>(a);
+    schedule_scan_kernel<<<1, 1024, 0, s>>>(a);
+    if (a.nchunks > 0) schedule_scatter_kernel<<<a.nchunks, kSchedWarps * 32, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ dispatch
+
+// Warp per padded row r in [offp[beg], offp[end]): dst[dst_row0 + r - offp[beg]]
+// = src[row_slot[r] / k], zeros for padding rows. 16-byte loads and stores.
+__global__ void __launch_bounds__(256) dispatch_rows_kernel(DispatchArgs a) {
+    const int lane = threadIdx.x % 32;
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
+    const int nw = gridDim.x * blockDim.x / 32;
+    const int r0 = a.offp[a.beg], r1 = a.offp[a.end];
+    const int vecs = a.H / 8;
+    for (int r = r0 + gw; r < r1; r += nw) {
+        const int slot = a.row_slot[r];
+        bf16 *dst = a.dst + (size_t)(a.dst_row0 + r - r0) * a.H;
+        if (slot < 0) {
+            for (int v = lane; v < vecs; v += 32) st_v4(dst + v * 8, make_uint4(0, 0, 0, 0));
+        } else {
+            const bf16 *src = a.src + (size_t)(slot / a.k) * a.H;
+            int v = lane;
+            for (; v + 96 < vecs; v += 128) {
+                uint4 x0 = ld_nc_v4(src + v * 8), x1 = ld_nc_v4(src + (v + 32) * 8);
+                uint4 x2 = ld_nc_v4(src + (v + 64) * 8), x3 = ld_nc_v4(src + (v + 96) * 8);
+                st_v4(dst + v * 8, x0);
+                st_v4(dst + (v + 32) * 8, x1);
+                st_v4(dst + (v + 64) * 8, x2);
+                st_v4(dst + (v + 96) * 8, x3);
+            }
+            for (; v < vecs; v += 32) st_v4(dst + v * 8, ld_nc_v4(src + v * 8));
+        }
+    }
+}
+
+cudaError_t launch_dispatch(const DispatchArgs &a, int max_rows, int num_sms, cudaStream_t s) {
+    if (max_rows <= 0) return cudaSuccess;
+    int blocks = min(ceil_div(max_rows, 8), num_sms * 8);
+    dispatch_rows_kernel<<<blocks, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ combine
+
+// Warp per token t in [t0, t1): out[t] = bf16( sum_{j=0}^{k-1} w[t,j] * Y[row(t,j)] ),
+// fp32 accumulation in fixed j order.
+__global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
+    const int lane = threadIdx.x % 32;
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
+    const int nw = gridDim.x * blockDim.x / 32;
+    const int shift = a.ring_base - a.offp[a.m * a.E];
+    for (int t = a.t0 + gw; t < a.t1; t += nw) {
+        for (int v = lane; v < a.H / 8; v += 32) {
+            float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            for (int j0 = 0; j0 < a.k; j0 += 8) {
+                const int nj = min(8, a.k - j0);
+                int rows[8];
+                float ws[8];
+                uint4 y[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < nj) {
+                        rows[j] = a.slot_row[(size_t)t * a.k + j0 + j] + shift;
+                        ws[j] = a.w[(size_t)t * a.k + j0 + j];
+                    }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < nj) y[j] = ld_v4(a.Y + (size_t)rows[j] * a.H + v * 8);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < nj) {
+                        const uint32_t q[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            acc[2 * i] = fmaf(ws[j], bf16lo(q[i]), acc[2 * i]);
+                            acc[2 * i + 1] = fmaf(ws[j], bf16hi(q[i]), acc[2 * i + 1]);
+                        }
+                    }
+            }
+            st_v4(a.out + (size_t)t * a.H + v * 8,
+                  make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                             pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+        }
+    }
+}
+
+cudaError_t launch_combine(const CombineArgs &a, int num_sms, cudaStream_t s) {
+    const int n = a.t1 - a.t0;
+    if (n <= 0) return cudaSuccess;
+    int blocks = min(ceil_div(n, 8), num_sms * 8);
+    combine_kernel<<<blocks, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ backward
+
+// Warp per token: dw[t,j] = sum of the per-N-tile partials of row(t,j) (fixed
+// order); dp_j = (dw_j - sum_i w_i dw_i) / S on the chosen experts, 0 elsewhere;
+// dlogits = p * (dp - sum_l p_l dp_l).
+__global__ void __launch_bounds__(256) router_bwd_kernel(RouterBwdArgs a) {
+    const int lane = threadIdx.x % 32;
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
+    if (t >= a.T) return;
+    // lane j < k: dw and w of slot j
+    float dwj = 0.0f, wj = 0.0f, pj = 0.0f;
+    int ej = -1;
+    if (lane < a.k) {
+        const int s = t * a.k + lane;
+        const int row = a.slot_row[s];
+        for (int n = 0; n < a.nparts; ++n) dwj += a.dw_part[(size_t)row * a.nparts + n];
+        wj = a.w[s];
+        ej = a.ids[s];
+        pj = a.probs[(size_t)t * a.E + ej];
+    }
+    float swd = wj * dwj, S = pj;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        swd += __shfl_xor_sync(0xffffffffu, swd, o);
+        S += __shfl_xor_sync(0xffffffffu, S, o);
+    }
+    const float dpj = lane < a.k ? (dwj - swd) / S : 0.0f;
+    // scatter dp to experts: lane owns experts lane, lane+32
+    float dp[2] = {0.0f, 0.0f}, p[2] = {0.0f, 0.0f};
+    for (int j = 0; j < a.k; ++j) {
+        const int e = __shfl_sync(0xffffffffu, ej, j);
+        const float v = __shfl_sync(0xffffffffu, dpj, j);
+        if (e == lane) dp[0] = v;
+        if (e == lane + 32) dp[1] = v;
+    }
+    float spdp = 0.0f;
+#pragma unroll
+    for (int s2 = 0; s2 < 2; ++s2) {
+        const int e = lane + 32 * s2;
+        if (e < a.E) p[s2] = a.probs[(size_t)t * a.E + e];
+        spdp += p[s2] * dp[s2];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) spdp += __shfl_xor_sync(0xffffffffu, spdp, o);
+#pragma unroll
+    for (int s2 = 0; s2 < 2; ++s2) {
+        const int e = lane + 32 * s2;
+        if (e < a.E) a.dlogits[(size_t)t * a.E + e] = p[s2] * (dp[s2] - spdp);
+    }
+}
+
+// Block of 8 warps = 8 tokens; per 256-wide H chunk the block stages W_r rows
+// in shared memory. dx[t] = bf16( sum_j dXs[row(t,j)] (fixed j order)
+//                                 + sum_e dlogits[t,e] W_r[h,e] ).
+__global__ void __launch_bounds__(256) reverse_dispatch_kernel(RevDispatchArgs a) {
+    extern __shared__ float sm[];
+    float *s_dl = sm;                                 // [8][E]
+    bf16 *s_wrT = reinterpret_cast<bf16 *>(sm + 8 * kMaxExperts);   // [E][256]
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int t = blockIdx.x * 8 + warp;
+    const bool tv = t < a.T;
+    for (int e = lane; e < a.E; e += 32) s_dl[warp * a.E + e] = tv ? a.dlogits[(size_t)t * a.E + e] : 0.0f;
+    int rows[8];
+    for (int j = 0; j < a.k && j < 8; ++j) rows[j] = tv ? a.slot_row[(size_t)t * a.k + j] : 0;
+    for (int h0 = 0; h0 < a.H; h0 += 256) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < 256 * a.E; i += blockDim.x)
+            s_wrT[(i % a.E) * 256 + i / a.E] = a.Wr[(size_t)h0 * a.E + i];
+        __syncthreads();
+        if (!tv) continue;
+        const int hb = h0 + lane * 8;
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int j = 0; j < a.k; ++j) {
+            const int row = j < 8 ? rows[j] : a.slot_row[(size_t)t * a.k + j];
+            const uint4 v = ld_v4(a.dXs + (size_t)row * a.H + hb);
+            const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] += bf16lo(q[i]);
+                acc[2 * i + 1] += bf16hi(q[i]);
+            }
+        }
+        float racc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int e = 0; e < a.E; ++e) {
+            const float d = s_dl[warp * a.E + e];
+            const uint4 wv = *reinterpret_cast<const uint4 *>(s_wrT + e * 256 + lane * 8);
+            const uint32_t q[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                racc[2 * i] = fmaf(d, bf16lo(q[i]), racc[2 * i]);
+                racc[2 * i + 1] = fmaf(d, bf16hi(q[i]), racc[2 * i + 1]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += racc[i];
+        st_v4(a.dx + (size_t)t * a.H + hb,
+              make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                         pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+    }
+}
+
+// dW_r partials: block (h-chunk of 32, split sp) sums tokens [sp*Ts, (sp+1)*Ts)
+// in order; thread (h = lane, expert group = warp) holds E/8 accumulators.
+__global__ void __launch_bounds__(256) router_wgrad_part_kernel(RouterWgradArgs a) {
+    __shared__ float s_dl[64 * kMaxExperts];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int h = blockIdx.x * 32 + lane;
+    const int sp = blockIdx.y;
+    const int ts = ceil_div(a.T, a.splits);
+    const int tb = sp * ts, te = min(a.T, tb + ts);
+    const int epw = ceil_div(a.E, 8);
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int c0 = tb; c0 < te; c0 += 64) {
+        const int cn = min(64, te - c0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < cn * a.E; i += blockDim.x) s_dl[i] = a.dlogits[(size_t)c0 * a.E + i];
+        __syncthreads();
+        for (int tt = 0; tt < cn; ++tt) {
+            const float xv = bf2f(a.x[(size_t)(c0 + tt) * a.H + h]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = warp * epw + i;
+                if (i < epw && e < a.E) acc[i] = fmaf(xv, s_dl[tt * a.E + e], acc[i]);
+            }
+        }
+    }
+    for (int i = 0; i < epw; ++i) {
+        const int e = warp * epw + i;
+        if (e < a.E) a.part[((size_t)sp * a.H + h) * a.E + e] = acc[i];
+    }
+}
+
+__global__ void router_wgrad_reduce_kernel(RouterWgradArgs a) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= a.H * a.E) return;
+    float v = 0.0f;
+    for (int sp = 0; sp < a.splits; ++sp) v += a.part[(size_t)sp * a.H * a.E + i];
+    a.dWr[i] = a.accumulate ? a.dWr[i] + v : v;
+}
+
+cudaError_t launch_router_bwd(const RouterBwdArgs &rb, const RevDispatchArgs &rd, const RouterWgradArgs &rw,
+                              cudaStream_t s) {
+    if (rb.T > 0) router_bwd_kernel<<<ceil_div(rb.T, 8), 256, 0, s>>>(rb);
+    if (rd.T > 0) {
+        const size_t smem = 8 * kMaxExperts * sizeof(float) + 256 * (size_t)rd.E * sizeof(bf16);
+        cudaError_t e = cudaFuncSetAttribute(reverse_dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        reverse_dispatch_kernel<<<ceil_div(rd.T, 8), 256, smem, s>>>(rd);
+    }
+    dim3 grid(rw.H / 32, rw.splits);
+    router_wgrad_part_kernel<<<grid, 256, 0, s>>>(rw);
+    router_wgrad_reduce_kernel<<<ceil_div(rw.H * rw.E, 256), 256, 0, s>>>(rw);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,96 @@
+"""Helpers of the GPU parity tests: run the CUDA layer on seeded inputs and
+compare it with the float64 oracle on the same bf16 bytes."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import moe_oracle as O
+import workloads as WL
+
+FWD_TOL = 1e-2     # max-abs-relative, forward (BF16)
+BWD_TOL = 2e-2     # max-abs-relative, backward (BF16)
+NEAR_TIE = 1e-4    # logit gap below which GPU and oracle may pick different experts
+
+
+def bf16_dev(a: np.ndarray) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
+    return t.view(torch.bfloat16).cuda()
+
+
+def dev_to_np(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return O.bf16_to_f64(t.view(torch.int16).cpu().numpy().view(np.uint16))
+    return t.cpu().numpy()
+
+
+def device_inputs(inp):
+    d = {k: bf16_dev(v) for k, v in inp.items() if k != "bias" and v is not None}
+    d["bias"] = torch.from_numpy(inp["bias"]).cuda() if inp.get("bias") is not None else None
+    return d
+
+
+def oracle_inputs(inp):
+    o = {k: O.bf16_to_f64(v) for k, v in inp.items() if k != "bias" and v is not None}
+    o["bias"] = None if inp.get("bias") is None else inp["bias"].astype(np.float64)
+    return o
+
+
+def run_gpu(w: WL.Workload, inp, backward=True, accumulate_into=None, **layer_kw):
+    from mixture_experts_layer_sum_gb300.layer import MoeLayer
+    d = device_inputs(inp)
+    T = inp["x"].shape[0]
+    layer = MoeLayer(T, w.H, w.F, w.E, w.k, w.precision, **layer_kw)
+    out, ids, wts = layer.forward(d["x"], d["Wr"], d["bias"], d["W1"], d["W3"], d["W2"])
+    res = {"out": out, "ids": ids, "w": wts}
+    if backward:
+        kw = {}
+        if accumulate_into is not None:
+            kw = {k: v.clone() for k, v in accumulate_into.items()}
+        dx, dWr, dW1, dW3, dW2 = layer.backward(d["dout"], d["x"], d["Wr"], d["W1"], d["W3"], d["W2"],
+                                                accumulate=accumulate_into is not None, **kw)
+        res.update(dx=dx, dWr=dWr, dW1=dW1, dW3=dW3, dW2=dW2)
+    layer.status()
+    torch.cuda.synchronize()
+    res = {k: dev_to_np(v) for k, v in res.items()}
+    res["layer"] = layer
+    return res
+
+
+def reconcile_ids(gpu_ids, oracle_fwd, k):
+    """GPU ids must equal the oracle's except on near-tie tokens. Returns the ids
+    to feed the oracle (the GPU's), after checking every difference is a near tie."""
+    logits = oracle_fwd["logits"]
+    diff = np.nonzero((np.sort(gpu_ids, axis=1) != np.sort(oracle_fwd["ids"], axis=1)).any(axis=1))[0]
+    if len(diff):
+        srt = -np.sort(-logits[diff], axis=1)
+        gap = srt[:, k - 1] - srt[:, k]
+        assert (gap < NEAR_TIE * (1 + np.abs(srt[:, k - 1]))).all(), f"non-tie id mismatch at tokens {diff[:10]}"
+    same_set = np.setdiff1d(np.arange(gpu_ids.shape[0]), diff)
+    # on agreeing tokens the slot order (descending probability) must agree too,
+    # except where two chosen experts are themselves near-tied
+    bad = same_set[(gpu_ids[same_set] != oracle_fwd["ids"][same_set]).any(axis=1)]
+    for t in bad:
+        l = logits[t, gpu_ids[t]]
+        assert np.min(np.abs(np.diff(np.sort(l)))) < NEAR_TIE * (1 + np.abs(l).max()), t
+    return gpu_ids, len(diff)
+
+
+def check_layer(w, inp, gpu, backward=True, macrobatch_tokens=0):
+    oi = oracle_inputs(inp)
+    f = O.forward(oi["x"], oi["Wr"], oi["bias"], oi["W1"], oi["W3"], oi["W2"], w.k,
+                  precision=w.precision, macrobatch_tokens=macrobatch_tokens)
+    ids, nties = reconcile_ids(gpu["ids"].astype(np.int32), f, w.k)
+    if nties or (ids != f["ids"]).any():
+        f = O.forward(oi["x"], oi["Wr"], oi["bias"], oi["W1"], oi["W3"], oi["W2"], w.k,
+                      precision=w.precision, macrobatch_tokens=macrobatch_tokens, ids=ids)
+    errs = {"w": float(np.abs(gpu["w"] - f["w"]).max()) if f["w"].size else 0.0,
+            "out": O.max_abs_rel(gpu["out"], f["out"])}
+    assert errs["w"] < 1e-4, errs
+    assert errs["out"] < FWD_TOL, errs
+    if backward:
+        g = O.backward(f, oi["dout"], oi["x"], oi["Wr"], oi["W1"], oi["W3"], oi["W2"])
+        for key in ("dx", "dWr", "dW1", "dW3", "dW2"):
+            errs[key] = O.max_abs_rel(gpu[key], g[key])
+            assert errs[key] < BWD_TOL, (key, errs)
+    return errs

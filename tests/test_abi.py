@@ -1,0 +1,120 @@
+"""Host-only checks of the C-ABI library: it builds, loads, exports every
+function include/moe.h declares, plans sizes (the minibatch floor is pinned to
+the figure the pages print) and rejects bad arguments before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_layer_sum_gb300 import build_ext
+    build_ext.build()
+    import mixture_experts_layer_sum_gb300.moe as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(moe):
+    names = declared_functions()
+    assert len(names) >= 12
+    lib = ctypes.CDLL(moe.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(moe.EXPORTED)
+
+
+def test_abi_version(moe):
+    assert moe.moe_abi_version() == 1
+
+
+def test_minibatch_floor_matches_pages_golden(moe):
+    path = os.path.join(ROOT, "tests", "golden", "minibatch_floor.txt")
+    rows = [l.split() for l in open(path) if l.strip() and not l.startswith("#")]
+    for sms, H, F, want in rows:
+        cfg = moe.make_config(4096, int(H), int(F), 16, 8, num_sms=int(sms))
+        assert moe.moe_plan(cfg).minibatch_rows == int(want)
+
+
+def test_plan_sizes_and_ring(moe):
+    cfg = moe.make_config(16384, 7168, 2048, 16, 8, num_sms=152, ring_bytes=256 << 20)
+    p = moe.moe_plan(cfg)
+    assert p.num_macrobatches > 1
+    assert p.ring_bytes <= 256 << 20
+    assert p.macrobatch_tokens * p.num_macrobatches >= 16384
+    assert p.workspace_bytes == moe.moe_workspace_size(cfg)
+    assert p.saved_bytes == moe.moe_saved_size(cfg)
+    full = moe.make_config(16384, 7168, 2048, 16, 8, num_sms=152)
+    pf = moe.moe_plan(full)
+    assert pf.num_macrobatches == 1 and pf.macrobatch_tokens == 16384
+    # padded rows bound: every (macrobatch, expert) run padded to 128 rows
+    assert pf.rows_padded_max >= 16384 * 8 and pf.rows_padded_max % 128 == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=16, H=250, F=512, E=4, k=2), 2),    # H not a multiple of 256
+    (dict(T=16, H=256, F=500, E=4, k=2), 2),
+    (dict(T=16, H=256, F=512, E=65, k=2), 2),   # too many experts
+    (dict(T=16, H=256, F=512, E=4, k=5), 1),    # k > E
+    (dict(T=-1, H=256, F=512, E=4, k=2), 1),
+    (dict(T=16, H=256, F=512, E=4, k=0), 1),
+])
+def test_bad_shapes_rejected(moe, kw, status):
+    cfg = moe.make_config(num_sms=148, **kw)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_plan(cfg)
+    assert ei.value.status == status
+    assert moe.moe_workspace_size(cfg) == 0
+
+
+def test_null_pointers_rejected_without_gpu(moe):
+    cfg = moe.make_config(64, 256, 512, 8, 2, num_sms=148)
+    lib = moe.library()
+    st = lib.moe_forward(ctypes.byref(cfg), None, None, None, None, None, None, None, None, None, None,
+                         None, 0, None, 0, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    assert "null" in moe.moe_last_error_string()
+    st = lib.moe_backward(ctypes.byref(cfg), None, None, None, None, None, None, None, None, None, None,
+                          None, None, None, 0, None, 0, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    st = lib.moe_schedule(ctypes.byref(cfg), None, None, None, None, None, None, 0, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+
+
+def test_small_buffers_rejected_without_gpu(moe):
+    cfg = moe.make_config(64, 256, 512, 8, 2, num_sms=148)
+    lib = moe.library()
+    fake = 1 << 20   # never dereferenced: the size check fails first
+    ws = moe.moe_workspace_size(cfg)
+    st = lib.moe_forward(ctypes.byref(cfg), fake, fake, None, fake, fake, fake, None, fake, fake, fake,
+                         fake, moe.moe_saved_size(cfg) - 1025, fake, ws, None)
+    assert st == moe.MOE_ERR_WORKSPACE
+    st = lib.moe_forward(ctypes.byref(cfg), fake, fake, None, fake, fake, fake, None, fake, fake, fake,
+                         fake, moe.moe_saved_size(cfg), fake, ws - 1025, None)
+    assert st == moe.MOE_ERR_WORKSPACE
+    # an unaligned workspace base costs up to 1023 bytes of the slack
+    st = lib.moe_forward(ctypes.byref(cfg), fake, fake, None, fake, fake, fake, None, fake, fake, fake,
+                         fake, moe.moe_saved_size(cfg), fake + 1, ws - 2, None)
+    assert st == moe.MOE_ERR_WORKSPACE
+    st = lib.moe_forward(ctypes.byref(cfg), fake + 8, fake, None, fake, fake, fake, None, fake, fake, fake,
+                         fake, moe.moe_saved_size(cfg), fake, ws, None)
+    assert st == moe.MOE_ERR_INVALID_ARG      # misaligned x
+
+
+def test_library_does_not_reference_oracle():
+    pkg = os.path.join(ROOT, "mixture_experts_layer_sum_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in src.lower(), f
