@@ -148,6 +148,15 @@ def stop_clocks(p, path):
             "reasons": reasons, "samples": len(rows)}
 
 
+def kernel_bytes(w, name):
+    """Algorithmic HBM bytes per launch of the memory-bound kernels."""
+    T, H, R, E, k = w.T, w.H, w.R, w.E, w.k
+    return {"dispatch": T * H * 2 + R * H * 2, "dispatch_replay": T * H * 2 + R * H * 2,
+            "reverse_combine": T * H * 2 + R * H * 2, "combine": R * H * 2 + T * H * 2 + R * 8,
+            "router_topk": T * H * 2 + T * E * 4 + T * k * 8,
+            "router_bwd": R * H * 2 + T * H * 2 + T * H * 2 + T * E * 8}.get(name)
+
+
 def gemm_flops(w, name):
     R, H, F = w.R, w.H, w.F
     return {"grouped_gemm_fwd1_swiglu": 4 * R * H * F, "grouped_gemm_fwd2": 2 * R * H * F,
@@ -213,14 +222,13 @@ def run_ours(args, w):
         stream.synchronize()
         return sum(a.elapsed_time(b) for a, b in evs)
 
+    clk_p, clk_path = start_clocks(local)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step()
     layer.status(stream)
     barrier()
-    clk_p, clk_path = start_clocks(local)
     total_ms = timed(step, args.steps)
-    clocks = stop_clocks(clk_p, clk_path)
     barrier()
     fwd_ms = timed(fwd, args.steps)
     layer.status(stream)
@@ -260,6 +268,7 @@ def run_ours(args, w):
     stream.synchronize()
     e2e_ms = timed(e2e_step, args.steps)
     layer.status(stream)
+    clocks = stop_clocks(clk_p, clk_path)
 
     if rank != 0:
         if ws > 1:
@@ -278,8 +287,14 @@ def run_ours(args, w):
         peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
         ach = fl / (per_launch_ms * 1e-3) / 1e12
         roof = {"kernel": name, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                "frac": ach / peak, "traffic": None,
+                "frac": ach / peak, "traffic": None, "algorithmic_per_launch": fl,
                 "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside the step loop)"}
+    elif kernel_bytes(w, name) is not None:
+        peak = peaks.get("hbm_gbs")
+        ach = kernel_bytes(w, name) / (per_launch_ms * 1e-3) / 1e9
+        roof = {"kernel": name, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                "frac": ach / peak, "traffic": None, "algorithmic_per_launch": kernel_bytes(w, name),
+                "peak_source": f"{peak_src} hbm_gbs"}
     gemm_ms = sum(ms_ for nm, _, ms_ in kernels if nm.startswith("grouped_gemm"))
     gemm_fl = sum(gemm_flops(w, nm) * n_ for nm, n_, _ in kernels if nm.startswith("grouped_gemm"))
     value = ws * w.T * args.steps / (total_ms * 1e-3)
@@ -299,8 +314,11 @@ def run_ours(args, w):
                          "frac_of_peak": (gemm_fl / (gemm_ms * 1e-3) / 1e12) /
                          peaks.get("bf16_tflops_sustained", 1700.0) if gemm_ms else None,
                          "share_of_step": gemm_ms / prof_ms if prof_ms else None},
-        "kernels": [{"name": nm, "launches": n_, "ms_per_step": ms_ / args.steps,
-                     "share": ms_ / prof_ms} for nm, n_, ms_ in kt],
+        "kernels": [dict({"name": nm, "launches": n_, "ms_per_step": ms_ / args.steps,
+                          "share": ms_ / prof_ms},
+                         **({"tflops": gemm_flops(w, nm) * n_ / (ms_ * 1e-3) / 1e12} if gemm_flops(w, nm) else {}),
+                         **({"gbs": kernel_bytes(w, nm) * n_ / (ms_ * 1e-3) / 1e9} if kernel_bytes(w, nm) else {}))
+                    for nm, n_, ms_ in kt],
         "gpu_launches": launches,
         "e2e": {"value": ws * w.T * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * w.T * w.H * 2, "d2h_bytes_per_step": 2 * w.T * w.H * 2},
@@ -318,7 +336,7 @@ def run_ours(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=WL.BALANCED.name, choices=sorted(WL.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -12,7 +12,7 @@ namespace moe {
 
 constexpr int kMaxExperts = 64;
 constexpr int kRowPad = 128;          // each (macrobatch, expert) run of sorted rows is padded to this
-constexpr int kSchedChunk = 2048;     // routed slots per schedule block
+constexpr int kSchedChunk = 1024;     // routed slots per schedule block
 constexpr int kSchedWarps = 8;
 constexpr int kMxBlock = 32;          // MXFP8 block along the contraction axis
 

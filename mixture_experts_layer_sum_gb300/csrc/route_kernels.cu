@@ -292,8 +292,36 @@ __global__ void __launch_bounds__(kSchedWarps * 32) schedule_count_kernel(SchedA
 
 // One block: per-(m,e) counts, unpadded and padded exclusive scans, chunk bases,
 // and -1 marks on padding rows.
+// Exclusive scan of two values per thread across a 1024-thread block.
+__device__ void block_exclusive_scan2(int &a, int &b, int *s_w /* [64] */) {
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32, nw = blockDim.x / 32;
+    int ia = a, ib = b;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int ta = __shfl_up_sync(0xffffffffu, ia, o), tb = __shfl_up_sync(0xffffffffu, ib, o);
+        if (lane >= o) { ia += ta; ib += tb; }
+    }
+    if (lane == 31) { s_w[warp] = ia; s_w[32 + warp] = ib; }
+    __syncthreads();
+    if (warp == 0) {
+        const int va = lane < nw ? s_w[lane] : 0, vb = lane < nw ? s_w[32 + lane] : 0;
+        int xa = va, xb = vb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ta = __shfl_up_sync(0xffffffffu, xa, o), tb = __shfl_up_sync(0xffffffffu, xb, o);
+            if (lane >= o) { xa += ta; xb += tb; }
+        }
+        __syncwarp();
+        s_w[lane] = xa - va;
+        s_w[32 + lane] = xb - vb;
+    }
+    __syncthreads();
+    a = ia - a + s_w[warp];
+    b = ib - b + s_w[32 + warp];
+}
+
 __global__ void __launch_bounds__(1024) schedule_scan_kernel(SchedArgs a) {
-    __shared__ int s_tot[1024];
+    __shared__ int s_tot[64];
     const int n = a.nM * a.E;
     // counts and chunk bases (relative to the (m,e) start)
     for (int me = threadIdx.x; me < n; me += blockDim.x) {
@@ -301,14 +329,16 @@ __global__ void __launch_bounds__(1024) schedule_scan_kernel(SchedArgs a) {
         int run = 0;
         for (int i = 0; i < a.chunks_per_mb; ++i) {
             const int c = m * a.chunks_per_mb + i;
+            if (c >= a.nchunks) break;   // no slots (T = 0): no count block wrote this chunk
             a.chunk_base[c * a.E + e] = run;
             run += a.chunk_counts[c * a.E + e];
         }
         a.counts[me] = run;
     }
     __syncthreads();
-    // sequential-in-blocks exclusive scan over (m, e): each thread owns a
-    // contiguous range, then the range totals are scanned
+    // exclusive scans over (m, e) of the counts and of the 128-padded counts:
+    // each thread owns a contiguous range, the range totals go through a
+    // warp-shuffle block scan
     const int per = ceil_div(max(n, 1), (int)blockDim.x);
     const int b0 = threadIdx.x * per, b1 = min(n, b0 + per);
     int tot = 0, totp = 0;
@@ -316,24 +346,8 @@ __global__ void __launch_bounds__(1024) schedule_scan_kernel(SchedArgs a) {
         tot += a.counts[i];
         totp += (a.counts[i] + kRowPad - 1) / kRowPad * kRowPad;
     }
-    // pack (unpadded, padded) totals: each fits in 32 bits separately; scan twice
-    s_tot[threadIdx.x] = tot;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0;
-        for (int i = 0; i < (int)blockDim.x; ++i) { int v = s_tot[i]; s_tot[i] = run; run += v; }
-    }
-    __syncthreads();
-    int run = s_tot[threadIdx.x];
-    __syncthreads();
-    s_tot[threadIdx.x] = totp;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int r = 0;
-        for (int i = 0; i < (int)blockDim.x; ++i) { int v = s_tot[i]; s_tot[i] = r; r += v; }
-    }
-    __syncthreads();
-    int runp = s_tot[threadIdx.x];
+    int run = tot, runp = totp;
+    block_exclusive_scan2(run, runp, s_tot);
     for (int i = b0; i < b1; ++i) {
         const int m = i / a.E, e = i % a.E;
         a.offsets[m * (a.E + 1) + e] = run;
@@ -349,7 +363,8 @@ __global__ void __launch_bounds__(1024) schedule_scan_kernel(SchedArgs a) {
     for (int me = threadIdx.x; me < n; me += blockDim.x) {
         const int m = me / a.E, e = me % a.E;
         const int start = a.offsets[m * (a.E + 1) + e];
-        for (int i = 0; i < a.chunks_per_mb; ++i) a.chunk_base[(m * a.chunks_per_mb + i) * a.E + e] += start;
+        for (int i = 0; i < a.chunks_per_mb && m * a.chunks_per_mb + i < a.nchunks; ++i)
+            a.chunk_base[(m * a.chunks_per_mb + i) * a.E + e] += start;
     }
     // padding rows of every (m, e) run hold no slot
     if (a.row_slot) {
@@ -516,84 +531,149 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(RouterBwdArgs a) {
     }
 }
 
-// Block of 8 warps = 8 tokens; per 256-wide H chunk the block stages W_r rows
-// in shared memory. dx[t] = bf16( sum_j dXs[row(t,j)] (fixed j order)
-//                                 + sum_e dlogits[t,e] W_r[h,e] ).
-__global__ void __launch_bounds__(256) reverse_dispatch_kernel(RevDispatchArgs a) {
-    extern __shared__ float sm[];
-    float *s_dl = sm;                                 // [8][E]
-    bf16 *s_wrT = reinterpret_cast<bf16 *>(sm + 8 * kMaxExperts);   // [E][256]
+// Reverse dispatch (article section 02: push reverse-dispatch, here a local
+// gather-sum):
+//   dx[t] = bf16( sum_j dXs[row(t,j)]  (fixed j order)  +  sum_e dlogits[t,e] W_r[h,e] ).
+// Block: 16 tokens, 4 warps; warp w covers H range [w H/4, (w+1) H/4) in
+// 64-wide chunks. The router term runs on mma.sync with dlogits split into
+// bf16 hi + lo parts (about 16 significant bits), the result goes through a
+// shared tile so each lane then owns 32 contiguous h of one token for the
+// 16-byte gathers of the k expert rows.
+constexpr int kRdTokens = 16;
+__global__ void __launch_bounds__(128) reverse_dispatch_kernel(RevDispatchArgs a) {
+    __shared__ float s_acc[4][kRdTokens][64 + 4];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int t = blockIdx.x * 8 + warp;
-    const bool tv = t < a.T;
-    for (int e = lane; e < a.E; e += 32) s_dl[warp * a.E + e] = tv ? a.dlogits[(size_t)t * a.E + e] : 0.0f;
-    int rows[8];
-    for (int j = 0; j < a.k && j < 8; ++j) rows[j] = tv ? a.slot_row[(size_t)t * a.k + j] : 0;
-    for (int h0 = 0; h0 < a.H; h0 += 256) {
-        __syncthreads();
-        for (int i = threadIdx.x; i < 256 * a.E; i += blockDim.x)
-            s_wrT[(i % a.E) * 256 + i / a.E] = a.Wr[(size_t)h0 * a.E + i];
-        __syncthreads();
-        if (!tv) continue;
-        const int hb = h0 + lane * 8;
-        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int j = 0; j < a.k; ++j) {
-            const int row = j < 8 ? rows[j] : a.slot_row[(size_t)t * a.k + j];
-            const uint4 v = ld_v4(a.dXs + (size_t)row * a.H + hb);
-            const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+    const int g = lane >> 2, c = lane & 3;
+    const int t0 = blockIdx.x * kRdTokens;
+    const int KS = (a.E + 15) / 16;   // k16 steps over experts (<= 4)
+    // A fragments of dlogits (rows g, g+8; k-slots 2c, 2c+1, 2c+8, 2c+9)
+    uint32_t Ahi[4][4], Alo[4][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] += bf16lo(q[i]);
-                acc[2 * i + 1] += bf16hi(q[i]);
+    for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            Ahi[ks][r] = 0u;
+            Alo[ks][r] = 0u;
+            if (ks < KS) {
+                const int t = t0 + g + ((r & 1) ? 8 : 0);
+                const int e = ks * 16 + 2 * c + ((r & 2) ? 8 : 0);
+                float v0 = 0.0f, v1 = 0.0f;
+                if (t < a.T) {
+                    if (e < a.E) v0 = a.dlogits[(size_t)t * a.E + e];
+                    if (e + 1 < a.E) v1 = a.dlogits[(size_t)t * a.E + e + 1];
+                }
+                const uint32_t hi = pack_bf16x2(v0, v1);
+                Ahi[ks][r] = hi;
+                Alo[ks][r] = pack_bf16x2(v0 - bf16lo(hi), v1 - bf16hi(hi));
             }
         }
-        float racc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int e = 0; e < a.E; ++e) {
-            const float d = s_dl[warp * a.E + e];
-            const uint4 wv = *reinterpret_cast<const uint4 *>(s_wrT + e * 256 + lane * 8);
-            const uint32_t q[4] = {wv.x, wv.y, wv.z, wv.w};
+    const int my_t = t0 + (lane >> 1);
+    const int half = lane & 1;
+    const int hspan = a.H / 4;
+    for (int h0 = warp * hspan; h0 < (warp + 1) * hspan; h0 += 64) {
+        float acc[8][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                racc[2 * i] = fmaf(d, bf16lo(q[i]), racc[2 * i]);
-                racc[2 * i + 1] = fmaf(d, bf16hi(q[i]), racc[2 * i + 1]);
+        for (int nt = 0; nt < 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            if (ks >= KS) break;
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                const bf16 *wr = a.Wr + (size_t)(h0 + nt * 8 + g) * a.E;
+                const int e0 = ks * 16 + 2 * c, e1 = e0 + 8;
+                const float w00 = e0 < a.E ? bf2f(wr[e0]) : 0.0f, w01 = e0 + 1 < a.E ? bf2f(wr[e0 + 1]) : 0.0f;
+                const float w10 = e1 < a.E ? bf2f(wr[e1]) : 0.0f, w11 = e1 + 1 < a.E ? bf2f(wr[e1 + 1]) : 0.0f;
+                const uint32_t b0 = pack_bf16x2(w00, w01), b1 = pack_bf16x2(w10, w11);
+                mma_16816_bf16(acc[nt], Ahi[ks], b0, b1);
+                mma_16816_bf16(acc[nt], Alo[ks], b0, b1);
             }
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += racc[i];
-        st_v4(a.dx + (size_t)t * a.H + hb,
-              make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                         pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+        for (int nt = 0; nt < 8; ++nt) {
+            s_acc[warp][g][nt * 8 + 2 * c] = acc[nt][0];
+            s_acc[warp][g][nt * 8 + 2 * c + 1] = acc[nt][1];
+            s_acc[warp][g + 8][nt * 8 + 2 * c] = acc[nt][2];
+            s_acc[warp][g + 8][nt * 8 + 2 * c + 1] = acc[nt][3];
+        }
+        __syncwarp();
+        if (my_t < a.T) {
+            const int hb = h0 + half * 32;
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+            for (int j = 0; j < a.k; ++j) {
+                const int row = a.slot_row[(size_t)my_t * a.k + j];
+                const bf16 *src = a.dXs + (size_t)row * a.H + hb;
+                uint4 q[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) q[u] = ld_v4(src + u * 8);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t qq[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        v[u * 8 + 2 * i] += bf16lo(qq[i]);
+                        v[u * 8 + 2 * i + 1] += bf16hi(qq[i]);
+                    }
+                }
+            }
+            uint32_t o[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                o[i] = pack_bf16x2(v[2 * i] + s_acc[warp][lane >> 1][half * 32 + 2 * i],
+                                   v[2 * i + 1] + s_acc[warp][lane >> 1][half * 32 + 2 * i + 1]);
+            bf16 *dst = a.dx + (size_t)my_t * a.H + hb;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) st_v4(dst + u * 8, make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]));
+        }
+        __syncwarp();
     }
 }
 
-// dW_r partials: block (h-chunk of 32, split sp) sums tokens [sp*Ts, (sp+1)*Ts)
-// in order; thread (h = lane, expert group = warp) holds E/8 accumulators.
+// dW_r partials: block = (64 h, split sp); lane owns h pair (h0 + 2 lane, +1),
+// warp w owns experts [8w, 8w+8); tokens of the split in increasing order.
+constexpr int kWgTok = 64;
 __global__ void __launch_bounds__(256) router_wgrad_part_kernel(RouterWgradArgs a) {
-    __shared__ float s_dl[64 * kMaxExperts];
+    __shared__ __align__(16) float s_dl[kWgTok][kMaxExperts];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int h = blockIdx.x * 32 + lane;
+    const int h = blockIdx.x * 64 + 2 * lane;
     const int sp = blockIdx.y;
     const int ts = ceil_div(a.T, a.splits);
     const int tb = sp * ts, te = min(a.T, tb + ts);
-    const int epw = ceil_div(a.E, 8);
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int c0 = tb; c0 < te; c0 += 64) {
-        const int cn = min(64, te - c0);
-        __syncthreads();
-        for (int i = threadIdx.x; i < cn * a.E; i += blockDim.x) s_dl[i] = a.dlogits[(size_t)c0 * a.E + i];
-        __syncthreads();
-        for (int tt = 0; tt < cn; ++tt) {
-            const float xv = bf2f(a.x[(size_t)(c0 + tt) * a.H + h]);
+    const int e0 = warp * 8;
+    float acc[2][8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = warp * epw + i;
-                if (i < epw && e < a.E) acc[i] = fmaf(xv, s_dl[tt * a.E + e], acc[i]);
+    for (int i = 0; i < 8; ++i) acc[0][i] = acc[1][i] = 0.0f;
+    for (int c0 = tb; c0 < te; c0 += kWgTok) {
+        const int cn = min(kWgTok, te - c0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < kWgTok * kMaxExperts; i += blockDim.x) {
+            const int tt = i / kMaxExperts, e = i % kMaxExperts;
+            s_dl[tt][e] = (tt < cn && e < a.E) ? a.dlogits[(size_t)(c0 + tt) * a.E + e] : 0.0f;
+        }
+        __syncthreads();
+        if (e0 < a.E) {
+            for (int tt = 0; tt < cn; ++tt) {
+                const uint32_t xv = *reinterpret_cast<const uint32_t *>(a.x + (size_t)(c0 + tt) * a.H + h);
+                const float x0 = bf16lo(xv), x1 = bf16hi(xv);
+                const float4 d0 = *reinterpret_cast<const float4 *>(&s_dl[tt][e0]);
+                const float4 d1 = *reinterpret_cast<const float4 *>(&s_dl[tt][e0 + 4]);
+                const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    acc[0][i] = fmaf(x0, d[i], acc[0][i]);
+                    acc[1][i] = fmaf(x1, d[i], acc[1][i]);
+                }
             }
         }
     }
-    for (int i = 0; i < epw; ++i) {
-        const int e = warp * epw + i;
-        if (e < a.E) a.part[((size_t)sp * a.H + h) * a.E + e] = acc[i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = e0 + i;
+        if (e < a.E) {
+            a.part[((size_t)sp * a.H + h) * a.E + e] = acc[0][i];
+            a.part[((size_t)sp * a.H + h + 1) * a.E + e] = acc[1][i];
+        }
     }
 }
 
@@ -608,14 +688,9 @@ __global__ void router_wgrad_reduce_kernel(RouterWgradArgs a) {
 cudaError_t launch_router_bwd(const RouterBwdArgs &rb, const RevDispatchArgs &rd, const RouterWgradArgs &rw,
                               cudaStream_t s) {
     if (rb.T > 0) router_bwd_kernel<<<ceil_div(rb.T, 8), 256, 0, s>>>(rb);
-    if (rd.T > 0) {
-        const size_t smem = 8 * kMaxExperts * sizeof(float) + 256 * (size_t)rd.E * sizeof(bf16);
-        cudaError_t e = cudaFuncSetAttribute(reverse_dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        reverse_dispatch_kernel<<<ceil_div(rd.T, 8), 256, smem, s>>>(rd);
-    }
-    dim3 grid(rw.H / 32, rw.splits);
-    router_wgrad_part_kernel<<<grid, 256, 0, s>>>(rw);
+    if (rd.T > 0) reverse_dispatch_kernel<<<ceil_div(rd.T, kRdTokens), 128, 0, s>>>(rd);
+    dim3 grid(rw.H / 64, rw.splits);
+    router_wgrad_part_kernel<<<grid, 32 * ceil_div(rw.E, 8), 0, s>>>(rw);
     router_wgrad_reduce_kernel<<<ceil_div(rw.H * rw.E, 256), 256, 0, s>>>(rw);
     return cudaGetLastError();
 }
