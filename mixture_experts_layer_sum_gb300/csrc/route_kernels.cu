@@ -541,7 +541,9 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(RouterBwdArgs a) {
 // 16-byte gathers of the k expert rows.
 constexpr int kRdTokens = 16;
 __global__ void __launch_bounds__(128) reverse_dispatch_kernel(RevDispatchArgs a) {
-    __shared__ float s_acc[4][kRdTokens][64 + 4];
+    extern __shared__ __align__(16) uint8_t rd_smem[];
+    auto s_acc = reinterpret_cast<float (*)[kRdTokens][64 + 4]>(rd_smem);                    // [4][16][68]
+    auto s_wr = reinterpret_cast<bf16 (*)[64][64 + 8]>(rd_smem + 4 * kRdTokens * 68 * 4);    // [4][64][72]
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int g = lane >> 2, c = lane & 3;
     const int t0 = blockIdx.x * kRdTokens;
@@ -574,18 +576,24 @@ __global__ void __launch_bounds__(128) reverse_dispatch_kernel(RevDispatchArgs a
         float acc[8][4];
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+        // W_r rows h0..h0+63 (E values each, zero padded to 64) -> this warp's tile
+        __syncwarp();
+        for (int i = lane; i < 64 * 64; i += 32) {
+            const int hh = i / 64, e = i % 64;
+            s_wr[warp][hh][e] = e < a.E ? a.Wr[(size_t)(h0 + hh) * a.E + e] : f2bf(0.0f);
+        }
+        __syncwarp();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-            if (ks >= KS) break;
+            if (ks < KS) {
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                const bf16 *wr = a.Wr + (size_t)(h0 + nt * 8 + g) * a.E;
-                const int e0 = ks * 16 + 2 * c, e1 = e0 + 8;
-                const float w00 = e0 < a.E ? bf2f(wr[e0]) : 0.0f, w01 = e0 + 1 < a.E ? bf2f(wr[e0 + 1]) : 0.0f;
-                const float w10 = e1 < a.E ? bf2f(wr[e1]) : 0.0f, w11 = e1 + 1 < a.E ? bf2f(wr[e1 + 1]) : 0.0f;
-                const uint32_t b0 = pack_bf16x2(w00, w01), b1 = pack_bf16x2(w10, w11);
-                mma_16816_bf16(acc[nt], Ahi[ks], b0, b1);
-                mma_16816_bf16(acc[nt], Alo[ks], b0, b1);
+                for (int nt = 0; nt < 8; ++nt) {
+                    const bf16 *wr = &s_wr[warp][nt * 8 + g][ks * 16 + 2 * c];
+                    const uint32_t b0 = *reinterpret_cast<const uint32_t *>(wr);
+                    const uint32_t b1 = *reinterpret_cast<const uint32_t *>(wr + 8);
+                    mma_16816_bf16(acc[nt], Ahi[ks], b0, b1);
+                    mma_16816_bf16(acc[nt], Alo[ks], b0, b1);
+                }
             }
         }
 #pragma unroll
@@ -601,21 +609,30 @@ __global__ void __launch_bounds__(128) reverse_dispatch_kernel(RevDispatchArgs a
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-            for (int j = 0; j < a.k; ++j) {
-                const int row = a.slot_row[(size_t)my_t * a.k + j];
-                const bf16 *src = a.dXs + (size_t)row * a.H + hb;
-                uint4 q[4];
+            for (int j0 = 0; j0 < a.k; j0 += 4) {
+                const int nj = min(4, a.k - j0);
+                uint4 q[4][4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) q[u] = ld_v4(src + u * 8);
+                for (int jj = 0; jj < 4; ++jj)
+                    if (jj < nj) {
+                        const int row = a.slot_row[(size_t)my_t * a.k + j0 + jj];
+                        const bf16 *src = a.dXs + (size_t)row * a.H + hb;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t qq[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        v[u * 8 + 2 * i] += bf16lo(qq[i]);
-                        v[u * 8 + 2 * i + 1] += bf16hi(qq[i]);
+                        for (int u = 0; u < 4; ++u) q[jj][u] = ld_v4(src + u * 8);
                     }
-                }
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    if (jj < nj) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t qq[4] = {q[jj][u].x, q[jj][u].y, q[jj][u].z, q[jj][u].w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                v[u * 8 + 2 * i] += bf16lo(qq[i]);
+                                v[u * 8 + 2 * i + 1] += bf16hi(qq[i]);
+                            }
+                        }
+                    }
             }
             uint32_t o[16];
 #pragma unroll
@@ -632,11 +649,14 @@ __global__ void __launch_bounds__(128) reverse_dispatch_kernel(RevDispatchArgs a
 
 // dW_r partials: block = (64 h, split sp); lane owns h pair (h0 + 2 lane, +1),
 // warp w owns experts [8w, 8w+8); tokens of the split in increasing order.
+// Each 64-token chunk of x (64 x 64 bf16) and of dlogits is staged in shared
+// memory with independent 16-byte loads first.
 constexpr int kWgTok = 64;
 __global__ void __launch_bounds__(256) router_wgrad_part_kernel(RouterWgradArgs a) {
     __shared__ __align__(16) float s_dl[kWgTok][kMaxExperts];
+    __shared__ __align__(16) bf16 s_x[kWgTok][64];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int h = blockIdx.x * 64 + 2 * lane;
+    const int hb = blockIdx.x * 64;
     const int sp = blockIdx.y;
     const int ts = ceil_div(a.T, a.splits);
     const int tb = sp * ts, te = min(a.T, tb + ts);
@@ -647,14 +667,21 @@ __global__ void __launch_bounds__(256) router_wgrad_part_kernel(RouterWgradArgs 
     for (int c0 = tb; c0 < te; c0 += kWgTok) {
         const int cn = min(kWgTok, te - c0);
         __syncthreads();
+        for (int i = threadIdx.x; i < kWgTok * 8; i += blockDim.x) {   // 8 x 16 B per token row
+            const int tt = i / 8, v = i % 8;
+            uint4 q = make_uint4(0, 0, 0, 0);
+            if (tt < cn) q = ld_nc_v4(a.x + (size_t)(c0 + tt) * a.H + hb + v * 8);
+            *reinterpret_cast<uint4 *>(&s_x[tt][v * 8]) = q;
+        }
         for (int i = threadIdx.x; i < kWgTok * kMaxExperts; i += blockDim.x) {
             const int tt = i / kMaxExperts, e = i % kMaxExperts;
             s_dl[tt][e] = (tt < cn && e < a.E) ? a.dlogits[(size_t)(c0 + tt) * a.E + e] : 0.0f;
         }
         __syncthreads();
         if (e0 < a.E) {
+#pragma unroll 4
             for (int tt = 0; tt < cn; ++tt) {
-                const uint32_t xv = *reinterpret_cast<const uint32_t *>(a.x + (size_t)(c0 + tt) * a.H + h);
+                const uint32_t xv = *reinterpret_cast<const uint32_t *>(&s_x[tt][2 * lane]);
                 const float x0 = bf16lo(xv), x1 = bf16hi(xv);
                 const float4 d0 = *reinterpret_cast<const float4 *>(&s_dl[tt][e0]);
                 const float4 d1 = *reinterpret_cast<const float4 *>(&s_dl[tt][e0 + 4]);
@@ -667,6 +694,7 @@ __global__ void __launch_bounds__(256) router_wgrad_part_kernel(RouterWgradArgs 
             }
         }
     }
+    const int h = hb + 2 * lane;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int e = e0 + i;
@@ -688,7 +716,12 @@ __global__ void router_wgrad_reduce_kernel(RouterWgradArgs a) {
 cudaError_t launch_router_bwd(const RouterBwdArgs &rb, const RevDispatchArgs &rd, const RouterWgradArgs &rw,
                               cudaStream_t s) {
     if (rb.T > 0) router_bwd_kernel<<<ceil_div(rb.T, 8), 256, 0, s>>>(rb);
-    if (rd.T > 0) reverse_dispatch_kernel<<<ceil_div(rd.T, kRdTokens), 128, 0, s>>>(rd);
+    if (rd.T > 0) {
+        const int smem = 4 * kRdTokens * 68 * 4 + 4 * 64 * 72 * 2;
+        cudaError_t e = cudaFuncSetAttribute(reverse_dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        reverse_dispatch_kernel<<<ceil_div(rd.T, kRdTokens), 128, smem, s>>>(rd);
+    }
     dim3 grid(rw.H / 64, rw.splits);
     router_wgrad_part_kernel<<<grid, 32 * ceil_div(rw.E, 8), 0, s>>>(rw);
     router_wgrad_reduce_kernel<<<ceil_div(rw.H * rw.E, 256), 256, 0, s>>>(rw);
