@@ -150,6 +150,26 @@ moe_status_t moe_schedule(const moe_config_t *cfg, const int32_t *topk_ids,
                           void *workspace, size_t workspace_bytes,
                           moe_stream_t stream);
 
+/* moe_schedule for callers that cannot allocate device memory (a framework
+ * callback whose pool owns all device memory, a deployment that forbids
+ * allocation after start-up). Same arguments and results as moe_schedule,
+ * minus the workspace: the scratch lives in a 1 MiB device array of the
+ * library itself, reserved on every device that loads the library until the
+ * process exits. The pages have no counterpart of this entry point.
+ *   - Shapes whose schedule scratch (two histograms of (chunk, expert) counts
+ *     plus the padded offsets, 1024 routed slots per chunk) exceeds the array
+ *     return MOE_ERR_UNSUPPORTED.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls on a device share the array; calls that overlap on the GPU
+ *     race and give undefined results. Each call clears what must start at 0.
+ *   - Device-side id checks are not reported: pass ids in [0,E).
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine. */
+moe_status_t moe_schedule_static(const moe_config_t *cfg, const int32_t *topk_ids,
+                                 int32_t *counts, int32_t *offsets,
+                                 int32_t *sorted_to_slot, int32_t *slot_to_sorted,
+                                 moe_stream_t stream);
+
 /* MXFP8 copies of the bf16 master weights for the forward and backward
  * GEMMs (quantised along each GEMM's contraction axis). Run once per weight
  * update. Returns MOE_ERR_UNSUPPORTED for a bf16 config. */

@@ -277,6 +277,10 @@ GemmArgs gemm_base(const Layout &L, void *ws, const int32_t *offp, const moe_con
 
 }  // namespace
 
+namespace moe {
+void set_last_error(const char *msg) { g_last_error = msg; }
+}  // namespace moe
+
 // ======================================================================== ABI
 
 extern "C" {

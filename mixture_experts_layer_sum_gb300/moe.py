@@ -24,7 +24,7 @@ MOE_PRECISION_MXFP8 = 1
 
 EXPORTED = (
     "moe_abi_version", "moe_plan", "moe_workspace_size", "moe_saved_size", "moe_qweights_size",
-    "moe_schedule", "moe_quantize_weights", "moe_forward", "moe_backward", "moe_query_status",
+    "moe_schedule", "moe_schedule_static", "moe_quantize_weights", "moe_forward", "moe_backward", "moe_query_status",
     "moe_reset_status", "moe_last_error_string", "moe_profile_begin", "moe_profile_end",
 )
 
@@ -75,6 +75,7 @@ def _load():
         "moe_saved_size": ([cfgp], ctypes.c_size_t),
         "moe_qweights_size": ([cfgp], ctypes.c_size_t),
         "moe_schedule": ([cfgp, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
+        "moe_schedule_static": ([cfgp, P, P, P, P, P, P], ctypes.c_int),
         "moe_quantize_weights": ([cfgp, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
         "moe_forward": ([cfgp, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, ctypes.c_size_t, P],
                         ctypes.c_int),
@@ -161,6 +162,12 @@ def moe_schedule(cfg, topk_ids, counts, offsets, sorted_to_slot, slot_to_sorted,
     return _check(_lib.moe_schedule(ctypes.byref(cfg), _ptr(topk_ids), _ptr(counts), _ptr(offsets),
                                     _ptr(sorted_to_slot), _ptr(slot_to_sorted), _ptr(workspace),
                                     _nbytes(workspace), _stream(stream)))
+
+
+def moe_schedule_static(cfg, topk_ids, counts, offsets, sorted_to_slot, slot_to_sorted, stream=None):
+    """moe_schedule without a workspace (scratch in the library's static device array)."""
+    return _check(_lib.moe_schedule_static(ctypes.byref(cfg), _ptr(topk_ids), _ptr(counts), _ptr(offsets),
+                                           _ptr(sorted_to_slot), _ptr(slot_to_sorted), _stream(stream)))
 
 
 def moe_quantize_weights(cfg, W1, W3, W2, qweights, stream=None):
