@@ -42,6 +42,21 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
+def committed_traffic(name):
+    """DRAM bytes per launch of `name` from the committed ncu table, if the
+    kernel sources are unchanged since the capture; else None."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    csrc = os.path.join(ROOT, "mixture_experts_layer_sum_gb300", "csrc")
+    for f, sha in d.get("sources_sha1", {}).items():
+        if hashlib.sha1(open(os.path.join(csrc, f), "rb").read()).hexdigest() != sha:
+            return None
+    return d.get("traffic_bytes_per_launch", {}).get(name)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -113,6 +128,51 @@ def run_reference(args, w):
 
 
 # ------------------------------------------------------------------ GPU arm
+
+class NvmlClockSampler:
+    """Reads SM clock and clock-event reasons through NVML every 10 ms on a
+    background thread (read-only queries; no setting is changed)."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, pci_bus_id):
+        import ctypes
+        import threading
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        self.c = ctypes
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle for " + pci_bus_id)
+        mx = ctypes.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+        self.max_mhz = mx.value
+        self.fn_reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.samples = []
+        self.stop_evt = threading.Event()
+        self.t = threading.Thread(target=self.run, daemon=True)
+        self.t.start()
+
+    def run(self):
+        c = self.c
+        while not self.stop_evt.is_set():
+            mhz, rs = c.c_uint(), c.c_ulonglong()
+            self.lib.nvmlDeviceGetClockInfo(self.h, 1, c.byref(mhz))
+            self.fn_reasons(self.h, c.byref(rs))
+            self.samples.append((mhz.value, rs.value))
+            self.stop_evt.wait(0.01)
+
+    def stop(self):
+        self.stop_evt.set()
+        self.t.join()
+        self.lib.nvmlShutdown()
+        sm = [m for m, _ in self.samples]
+        reasons = sorted({name for _, r in self.samples for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(sm), "source": "NVML, 10 ms period, during the timed loops"}
+
 
 def start_clocks(local_rank):
     f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
@@ -222,7 +282,14 @@ def run_ours(args, w):
         stream.synchronize()
         return sum(a.elapsed_time(b) for a, b in evs)
 
-    clk_p, clk_path = start_clocks(local)
+    props = torch.cuda.get_device_properties(dev)
+    try:
+        bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+        sampler = NvmlClockSampler(bus)
+        clk_p = clk_path = None
+    except Exception:
+        sampler = None
+        clk_p, clk_path = start_clocks(local)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step()
@@ -268,7 +335,7 @@ def run_ours(args, w):
     stream.synchronize()
     e2e_ms = timed(e2e_step, args.steps)
     layer.status(stream)
-    clocks = stop_clocks(clk_p, clk_path)
+    clocks = sampler.stop() if sampler is not None else stop_clocks(clk_p, clk_path)
 
     if rank != 0:
         if ws > 1:
@@ -287,7 +354,8 @@ def run_ours(args, w):
         peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
         ach = fl / (per_launch_ms * 1e-3) / 1e12
         roof = {"kernel": name, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                "frac": ach / peak, "traffic": None, "algorithmic_per_launch": fl,
+                "frac": ach / peak, "traffic": committed_traffic(name) if w.name == WL.BALANCED.name else None,
+                "algorithmic_per_launch": fl,
                 "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside the step loop)"}
     elif kernel_bytes(w, name) is not None:
         peak = peaks.get("hbm_gbs")
