@@ -20,6 +20,14 @@
 //              double buffered (2 x 256 columns)
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator, fused elementwise
 //              work, stores to global memory
+// MXFP8 variant (FP8 = true): every operand is K-major E4M3 with E8M0 scale
+// atoms (moe_common.cuh); a stage holds 128 elements of K (A 128x128 B,
+// B 256x128 B) plus the 512-byte scale atoms of A and of both 128-row halves
+// of B (1-D bulk copies). The MMA thread moves the atoms into tensor memory
+// with tcgen05.cp.32x128b.warpx4 (4 columns per 128 rows) and issues
+// tcgen05.mma.kind::mxf8f6f4.block_scale.scale_vec::1X (K=32) with the scale
+// byte selected by k-block. The scale columns take TMEM columns 256..319, so
+// the fp32 accumulator is single-buffered in this variant.
 // Every mbarrier wait is bounded; when a wait gives up the status word is set
 // and all roles leave their loops, drain their in-flight copies/MMAs and free
 // TMEM before exiting.
@@ -30,10 +38,53 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KiB
+constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KiB (bf16 128x64, or e4m3 128x128)
 constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KiB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t CHUNK_BYTES = 64 * 64 * 2;   // one 64x64 bf16 box, 8 KiB
+constexpr uint32_t SF_BYTES = 3 * 512;          // scale atoms: A, B rows 0-127, B rows 128-255
+constexpr uint32_t STAGE_STRIDE_FP8 = 51200;    // 48 KiB of tiles + atoms, 1 KiB aligned
+constexpr int BK8 = 128;                        // K elements per stage, e4m3
+
+template <bool FP8> __host__ __device__ constexpr uint32_t stage_stride() { return FP8 ? STAGE_STRIDE_FP8 : STAGE_BYTES; }
+template <bool FP8> __host__ __device__ constexpr int bk_elems() { return FP8 ? BK8 : BK; }
+
+// D[tmem] (+)= A[smem] * B[smem], e4m3 x e4m3 with E8M0 block scales read from
+// tensor memory (scale_vec::1X: one scale per 32 elements of K).
+__device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// 32 rows x 16 bytes of shared memory -> 4 TMEM columns, replicated to the four lane quarters
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Instruction descriptor, kind::mxf8f6f4 block-scaled: e4m3 A/B, E8M0 scales, both K-major.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sf_id) {
+    return ((uint32_t)sf_id << 4)               // B scale byte
+           | ((uint32_t)(N >> 3) << 17)         // N / 8
+           | (1u << 23)                         // scale format: E8M0
+           | ((uint32_t)(M >> 4) << 24)         // M / 16
+           | ((uint32_t)sf_id << 29);           // A scale byte
+}
+
+// 1-D bulk copy global -> shared, completion counted on an mbarrier
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar) : "memory");
+}
+
+// byte offset of the scale atom that covers (row, k) of a matrix with K columns
+__device__ __forceinline__ size_t atom_at(int row, int k, int K) {
+    return ((size_t)(row >> 7) * (size_t)(K >> 7) + (size_t)(k >> 7)) * 512;
+}
 
 template <int OP>
 struct OpTraits;
@@ -66,7 +117,7 @@ __device__ __forceinline__ int num_tiles(const SmemCtl &c, const GemmArgs &g) {
     else return c.prefix[g.E] * c.nt;
 }
 
-template <int OP>
+template <int OP, bool FP8>
 __device__ __forceinline__ TileInfo decode_tile(const SmemCtl &c, const GemmArgs &g, int t) {
     TileInfo ti;
     ti.nt = t % c.nt;
@@ -75,22 +126,22 @@ __device__ __forceinline__ TileInfo decode_tile(const SmemCtl &c, const GemmArgs
         ti.mt = q % c.mt_per_group;
         ti.e = q / c.mt_per_group;
         ti.g0 = 0;
-        ti.nk = c.krows[ti.e] / BK;
+        ti.nk = c.krows[ti.e] / bk_elems<FP8>();
     } else {
         int e = 0;
         while (c.prefix[e + 1] <= q) ++e;   // E <= 64
         ti.e = e;
         ti.mt = q - c.prefix[e];
         ti.g0 = c.seg_start[e] + ti.mt * BM;
-        ti.nk = g.K / BK;
+        ti.nk = g.K / bk_elems<FP8>();
     }
     return ti;
 }
 
 // grouped-K ops: the padded row at position kb*BK of expert e's rows, walking
 // the (macrobatch, e) runs in macrobatch order.
-__device__ __forceinline__ int grouped_k_row(const GemmArgs &g, int e, int kb) {
-    int r = kb * BK;
+__device__ __forceinline__ int grouped_k_row(const GemmArgs &g, int e, int kb, int bk) {
+    int r = kb * bk;
     for (int mm = 0; mm < g.nM; ++mm) {
         int s0 = g.offp[mm * g.E + e], s1 = g.offp[mm * g.E + e + 1];
         if (r < s1 - s0) return s0 + r;
@@ -99,7 +150,7 @@ __device__ __forceinline__ int grouped_k_row(const GemmArgs &g, int e, int kb) {
     return 0;   // unreachable for kb < nk
 }
 
-template <int OP>
+template <int OP, bool FP8>
 __device__ void producer_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tiles, uint64_t *full,
                               uint64_t *empty, const WaitCtl &ctl) {
     int stage = 0;
@@ -110,50 +161,104 @@ __device__ void producer_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tile
     const int total = num_tiles<OP>(c, g);
     const int a_shift = g.a_ring ? (g.ring_base - g.offp[g.m * g.E]) : 0;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        TileInfo ti = decode_tile<OP>(c, g, t);
+        TileInfo ti = decode_tile<OP, FP8>(c, g, t);
         for (int kb = 0; kb < ti.nk; ++kb) {
             if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, ctl)) { ok = false; break; }
             uint32_t bar = smem_u32(&full[stage]);
-            uint32_t sA = smem_u32(tiles + stage * STAGE_BYTES);
+            uint32_t sA = smem_u32(tiles + stage * stage_stride<FP8>());
             uint32_t sB = sA + A_BYTES;
-            mbar_arrive_expect_tx(bar, STAGE_BYTES);
-            if constexpr (OP == OP_FWD1) {
-                int ar = ti.g0 + a_shift, br = ti.e * g.H + kb * BK, n0 = ti.nt * 128;
-                tma_load_2d(sA, &g.a0, bar, kb * BK, ar);
-                tma_load_2d(sB, &g.b0, bar, n0, br);
-                tma_load_2d(sB + CHUNK_BYTES, &g.b0, bar, n0 + 64, br);
-                tma_load_2d(sB + 2 * CHUNK_BYTES, &g.b1, bar, n0, br);
-                tma_load_2d(sB + 3 * CHUNK_BYTES, &g.b1, bar, n0 + 64, br);
-            } else if constexpr (OP == OP_FWD2) {
-                int ar = ti.g0 + a_shift, br = ti.e * g.F + kb * BK, n0 = ti.nt * BN;
-                tma_load_2d(sA, &g.a0, bar, kb * BK, ar);
+            if constexpr (!FP8) {
+                mbar_arrive_expect_tx(bar, STAGE_BYTES);
+                if constexpr (OP == OP_FWD1) {
+                    int ar = ti.g0 + a_shift, br = ti.e * g.H + kb * BK, n0 = ti.nt * 128;
+                    tma_load_2d(sA, &g.a0, bar, kb * BK, ar);
+                    tma_load_2d(sB, &g.b0, bar, n0, br);
+                    tma_load_2d(sB + CHUNK_BYTES, &g.b0, bar, n0 + 64, br);
+                    tma_load_2d(sB + 2 * CHUNK_BYTES, &g.b1, bar, n0, br);
+                    tma_load_2d(sB + 3 * CHUNK_BYTES, &g.b1, bar, n0 + 64, br);
+                } else if constexpr (OP == OP_FWD2) {
+                    int ar = ti.g0 + a_shift, br = ti.e * g.F + kb * BK, n0 = ti.nt * BN;
+                    tma_load_2d(sA, &g.a0, bar, kb * BK, ar);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * CHUNK_BYTES, &g.b0, bar, n0 + 64 * j, br);
-            } else if constexpr (OP == OP_BWD2) {
-                tma_load_2d(sA, &g.a0, bar, kb * BK, ti.g0 + a_shift);
-                tma_load_2d(sB, &g.b0, bar, kb * BK, ti.e * g.F + ti.nt * BN);
-            } else if constexpr (OP == OP_BWD1) {
-                const int kf = g.F / BK;
-                const bool second = kb >= kf;
-                const int kk = second ? kb - kf : kb;
-                tma_load_2d(sA, second ? &g.a1 : &g.a0, bar, kk * BK, ti.g0 + a_shift);
-                tma_load_2d(sB, second ? &g.b1 : &g.b0, bar, kk * BK, ti.e * g.H + ti.nt * BN);
-            } else if constexpr (OP == OP_WG2) {
-                int row = grouped_k_row(g, ti.e, kb);
-                int m0 = ti.mt * BM, n0 = ti.nt * BN;
-                tma_load_2d(sA, &g.a0, bar, m0, row);
-                tma_load_2d(sA + CHUNK_BYTES, &g.a0, bar, m0 + 64, row);
+                    for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * CHUNK_BYTES, &g.b0, bar, n0 + 64 * j, br);
+                } else if constexpr (OP == OP_BWD2) {
+                    tma_load_2d(sA, &g.a0, bar, kb * BK, ti.g0 + a_shift);
+                    tma_load_2d(sB, &g.b0, bar, kb * BK, ti.e * g.F + ti.nt * BN);
+                } else if constexpr (OP == OP_BWD1) {
+                    const int kf = g.F / BK;
+                    const bool second = kb >= kf;
+                    const int kk = second ? kb - kf : kb;
+                    tma_load_2d(sA, second ? &g.a1 : &g.a0, bar, kk * BK, ti.g0 + a_shift);
+                    tma_load_2d(sB, second ? &g.b1 : &g.b0, bar, kk * BK, ti.e * g.H + ti.nt * BN);
+                } else if constexpr (OP == OP_WG2) {
+                    int row = grouped_k_row(g, ti.e, kb, BK);
+                    int m0 = ti.mt * BM, n0 = ti.nt * BN;
+                    tma_load_2d(sA, &g.a0, bar, m0, row);
+                    tma_load_2d(sA + CHUNK_BYTES, &g.a0, bar, m0 + 64, row);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * CHUNK_BYTES, &g.b0, bar, n0 + 64 * j, row);
-            } else if constexpr (OP == OP_WG13) {
-                int row = grouped_k_row(g, ti.e, kb);
-                int m0 = ti.mt * BM, n0 = ti.nt * 128;
-                tma_load_2d(sA, &g.a0, bar, m0, row);
-                tma_load_2d(sA + CHUNK_BYTES, &g.a0, bar, m0 + 64, row);
-                tma_load_2d(sB, &g.b0, bar, n0, row);
-                tma_load_2d(sB + CHUNK_BYTES, &g.b0, bar, n0 + 64, row);
-                tma_load_2d(sB + 2 * CHUNK_BYTES, &g.b1, bar, n0, row);
-                tma_load_2d(sB + 3 * CHUNK_BYTES, &g.b1, bar, n0 + 64, row);
+                    for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * CHUNK_BYTES, &g.b0, bar, n0 + 64 * j, row);
+                } else if constexpr (OP == OP_WG13) {
+                    int row = grouped_k_row(g, ti.e, kb, BK);
+                    int m0 = ti.mt * BM, n0 = ti.nt * 128;
+                    tma_load_2d(sA, &g.a0, bar, m0, row);
+                    tma_load_2d(sA + CHUNK_BYTES, &g.a0, bar, m0 + 64, row);
+                    tma_load_2d(sB, &g.b0, bar, n0, row);
+                    tma_load_2d(sB + CHUNK_BYTES, &g.b0, bar, n0 + 64, row);
+                    tma_load_2d(sB + 2 * CHUNK_BYTES, &g.b1, bar, n0, row);
+                    tma_load_2d(sB + 3 * CHUNK_BYTES, &g.b1, bar, n0 + 64, row);
+                }
+            } else {
+                // e4m3 tiles (all K-major, 128 B of K per row) + three scale atoms
+                const uint32_t sSF = sB + B_BYTES;
+                const int KS = g.kstore;
+                mbar_arrive_expect_tx(bar, STAGE_BYTES + SF_BYTES);
+                if constexpr (OP == OP_FWD1) {
+                    const int ar = ti.g0 + a_shift, br = ti.e * g.F + ti.nt * 128, k0 = kb * BK8;
+                    tma_load_2d(sA, &g.a0, bar, k0, ar);
+                    tma_load_2d(sB, &g.b0, bar, k0, br);
+                    tma_load_2d(sB + 16384, &g.b1, bar, k0, br);
+                    bulk_load(sSF, g.sfa0 + atom_at(ar, k0, KS), 512, bar);
+                    bulk_load(sSF + 512, g.sfb0 + atom_at(br, k0, KS), 512, bar);
+                    bulk_load(sSF + 1024, g.sfb1 + atom_at(br, k0, KS), 512, bar);
+                } else if constexpr (OP == OP_FWD2 || OP == OP_BWD2) {
+                    const int ar = ti.g0 + a_shift, k0 = kb * BK8;
+                    const int br = OP == OP_FWD2 ? ti.e * g.H + ti.nt * BN : ti.e * g.F + ti.nt * BN;
+                    tma_load_2d(sA, &g.a0, bar, k0, ar);
+                    tma_load_2d(sB, &g.b0, bar, k0, br);
+                    bulk_load(sSF, g.sfa0 + atom_at(ar, k0, KS), 512, bar);
+                    bulk_load(sSF + 512, g.sfb0 + atom_at(br, k0, KS), 512, bar);
+                    bulk_load(sSF + 1024, g.sfb0 + atom_at(br + 128, k0, KS), 512, bar);
+                } else if constexpr (OP == OP_BWD1) {
+                    const int kf = g.F / BK8;
+                    const bool second = kb >= kf;
+                    const int k0 = (second ? kb - kf : kb) * BK8;
+                    const int ar = ti.g0 + a_shift, br = ti.e * g.H + ti.nt * BN;
+                    const uint8_t *sfa = second ? g.sfa1 : g.sfa0, *sfb = second ? g.sfb1 : g.sfb0;
+                    tma_load_2d(sA, second ? &g.a1 : &g.a0, bar, k0, ar);
+                    tma_load_2d(sB, second ? &g.b1 : &g.b0, bar, k0, br);
+                    bulk_load(sSF, sfa + atom_at(ar, k0, KS), 512, bar);
+                    bulk_load(sSF + 512, sfb + atom_at(br, k0, KS), 512, bar);
+                    bulk_load(sSF + 1024, sfb + atom_at(br + 128, k0, KS), 512, bar);
+                } else if constexpr (OP == OP_WG2) {
+                    // A = (w h)^T [F][rows], B = dY^T [H][rows], both quantised along rows
+                    const int row = grouped_k_row(g, ti.e, kb, BK8);
+                    const int m0 = ti.mt * BM, n0 = ti.nt * BN;
+                    tma_load_2d(sA, &g.a0, bar, row, m0);
+                    tma_load_2d(sB, &g.b0, bar, row, n0);
+                    bulk_load(sSF, g.sfa0 + atom_at(m0, row, KS), 512, bar);
+                    bulk_load(sSF + 512, g.sfb0 + atom_at(n0, row, KS), 512, bar);
+                    bulk_load(sSF + 1024, g.sfb0 + atom_at(n0 + 128, row, KS), 512, bar);
+                } else if constexpr (OP == OP_WG13) {
+                    // A = X^T [H][rows], B = [da^T | db^T] [F][rows]
+                    const int row = grouped_k_row(g, ti.e, kb, BK8);
+                    const int m0 = ti.mt * BM, n0 = ti.nt * 128;
+                    tma_load_2d(sA, &g.a0, bar, row, m0);
+                    tma_load_2d(sB, &g.b0, bar, row, n0);
+                    tma_load_2d(sB + 16384, &g.b1, bar, row, n0);
+                    bulk_load(sSF, g.sfa0 + atom_at(m0, row, KS), 512, bar);
+                    bulk_load(sSF + 512, g.sfb0 + atom_at(n0, row, KS), 512, bar);
+                    bulk_load(sSF + 1024, g.sfb1 + atom_at(n0, row, KS), 512, bar);
+                }
             }
             issued[stage] = 1;
             last_phase[stage] = phase;
@@ -172,11 +277,11 @@ __device__ void producer_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tile
     }
 }
 
-template <int OP>
+template <int OP, bool FP8>
 __device__ void mma_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tiles, uint64_t *full,
                          uint64_t *empty, uint64_t *tfull, uint64_t *tempty, uint64_t *drain,
                          uint32_t tmem, const WaitCtl &ctl) {
-    constexpr bool AMN = OpTraits<OP>::a_mn, BMN = OpTraits<OP>::b_mn;
+    constexpr bool AMN = OpTraits<OP>::a_mn && !FP8, BMN = OpTraits<OP>::b_mn && !FP8;
     constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, AMN, BMN);
     int stage = 0;
     uint32_t phase = 0;
@@ -184,7 +289,7 @@ __device__ void mma_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tiles, ui
     uint32_t acc_phase = 0;
     const int total = num_tiles<OP>(c, g);
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        TileInfo ti = decode_tile<OP>(c, g, t);
+        TileInfo ti = decode_tile<OP, FP8>(c, g, t);
         if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1, ctl)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * BN;
@@ -192,21 +297,41 @@ __device__ void mma_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tiles, ui
         for (int kb = 0; kb < ti.nk; ++kb) {
             if (!mbar_wait(smem_u32(&full[stage]), phase, ctl)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t sA = smem_u32(tiles + stage * STAGE_BYTES);
+            const uint32_t sA = smem_u32(tiles + stage * stage_stride<FP8>());
             const uint32_t sB = sA + A_BYTES;
+            if constexpr (!FP8) {
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-                uint64_t ad = AMN ? sdesc_sw128(sA + kk * 2048, 8192, 1024) : sdesc_sw128(sA + kk * 32, 16, 1024);
-                uint64_t bd = BMN ? sdesc_sw128(sB + kk * 2048, 8192, 1024) : sdesc_sw128(sB + kk * 32, 16, 1024);
-                mma_bf16_ss(d, ad, bd, idesc, (kb | kk) != 0);
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    uint64_t ad = AMN ? sdesc_sw128(sA + kk * 2048, 8192, 1024) : sdesc_sw128(sA + kk * 32, 16, 1024);
+                    uint64_t bd = BMN ? sdesc_sw128(sB + kk * 2048, 8192, 1024) : sdesc_sw128(sB + kk * 32, 16, 1024);
+                    mma_bf16_ss(d, ad, bd, idesc, (kb | kk) != 0);
+                }
+            } else {
+                // scale atoms of this stage -> TMEM: A at column 256 + 16 * stage (4 columns),
+                // B at +8 (8 columns: rows 0-127 then rows 128-255)
+                const uint32_t sSF = sB + B_BYTES;
+                const uint32_t t_sf = tmem + 256 + 16 * stage;
+                tmem_cp_32x128b_x4(t_sf, sdesc_plain(sSF, 0, 128));
+                tmem_cp_32x128b_x4(t_sf + 8, sdesc_plain(sSF + 512, 0, 128));
+                tmem_cp_32x128b_x4(t_sf + 12, sdesc_plain(sSF + 1024, 0, 128));
+#pragma unroll
+                for (int kk = 0; kk < BK8 / 32; ++kk) {
+                    const uint64_t ad = sdesc_sw128(sA + kk * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(sB + kk * 32, 16, 1024);
+                    mma_mxf8_ss(d, ad, bd, idesc_mxf8(BM, BN, kk), t_sf, t_sf + 8, (kb | kk) != 0);
+                }
             }
             mma_commit(smem_u32(&empty[stage]));
             if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
         mma_commit(smem_u32(&tfull[acc]));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+        if constexpr (FP8) {
+            acc_phase ^= 1;                 // single accumulator buffer
+        } else {
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
     }
     // all MMAs issued by this thread must be complete before TMEM is freed
     mma_commit(smem_u32(drain));
@@ -217,7 +342,7 @@ __device__ void mma_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tiles, ui
 __device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
 __device__ __forceinline__ float sigmoid_f(float a) { return 1.0f / (1.0f + __expf(-a)); }
 
-template <int OP>
+template <int OP, bool FP8>
 __device__ void epilogue_loop(const GemmArgs &g, const SmemCtl &c, uint64_t *tfull, uint64_t *tempty,
                               uint32_t tmem, const WaitCtl &ctl) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -229,7 +354,7 @@ __device__ void epilogue_loop(const GemmArgs &g, const SmemCtl &c, uint64_t *tfu
     const int total = num_tiles<OP>(c, g);
     const int ring_shift = g.ring_base - g.offp[g.m * g.E];
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        TileInfo ti = decode_tile<OP>(c, g, t);
+        TileInfo ti = decode_tile<OP, FP8>(c, g, t);
         if (!mbar_wait(smem_u32(&tfull[acc]), acc_phase, ctl)) break;
         tc_fence_after();
         const uint32_t tbase = tmem + lane_base + acc * BN;
@@ -238,7 +363,7 @@ __device__ void epilogue_loop(const GemmArgs &g, const SmemCtl &c, uint64_t *tfu
             const size_t F = g.F;
             bf16 *pa = g.o0 + grow * F + ti.nt * 128;
             bf16 *pb = g.o1 + grow * F + ti.nt * 128;
-            bf16 *ph = g.o2 + (size_t)(grow + ring_shift) * F + ti.nt * 128;
+            bf16 *ph = FP8 ? nullptr : g.o2 + (size_t)(grow + ring_shift) * F + ti.nt * 128;
 #pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t va[32], vb[32];
@@ -246,6 +371,7 @@ __device__ void epilogue_loop(const GemmArgs &g, const SmemCtl &c, uint64_t *tfu
                 tmem_ld_32x32b_x32(tbase + 128 + cc * 32, vb);
                 tmem_ld_wait();
                 uint32_t oa[16], ob[16], oh[16];
+                float hf[32];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     oa[i] = pack_bf16x2(__uint_as_float(va[2 * i]), __uint_as_float(va[2 * i + 1]));
@@ -253,13 +379,27 @@ __device__ void epilogue_loop(const GemmArgs &g, const SmemCtl &c, uint64_t *tfu
                     // h from the bf16-rounded a and b, so the backward recomputes it exactly
                     float a0 = bf16lo(oa[i]), a1 = bf16hi(oa[i]);
                     float b0 = bf16lo(ob[i]), b1 = bf16hi(ob[i]);
-                    oh[i] = pack_bf16x2(silu_f(a0) * b0, silu_f(a1) * b1);
+                    hf[2 * i] = silu_f(a0) * b0;
+                    hf[2 * i + 1] = silu_f(a1) * b1;
+                    oh[i] = pack_bf16x2(hf[2 * i], hf[2 * i + 1]);
                 }
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     st_v4(pa + cc * 32 + v * 8, make_uint4(oa[4 * v], oa[4 * v + 1], oa[4 * v + 2], oa[4 * v + 3]));
                     st_v4(pb + cc * 32 + v * 8, make_uint4(ob[4 * v], ob[4 * v + 1], ob[4 * v + 2], ob[4 * v + 3]));
-                    st_v4(ph + cc * 32 + v * 8, make_uint4(oh[4 * v], oh[4 * v + 1], oh[4 * v + 2], oh[4 * v + 3]));
+                    if constexpr (!FP8)
+                        st_v4(ph + cc * 32 + v * 8, make_uint4(oh[4 * v], oh[4 * v + 1], oh[4 * v + 2], oh[4 * v + 3]));
+                }
+                if constexpr (FP8) {
+                    // h quantised along F (blocks of 32) for GEMM2's A operand
+                    uint32_t q[8];
+                    const uint32_t sb = mx_quant32(hf, q);
+                    const size_t hrow = (size_t)(grow + ring_shift);
+                    const size_t col = (size_t)ti.nt * 128 + cc * 32;
+                    uint4 *dq = reinterpret_cast<uint4 *>(g.q0 + hrow * F + col);
+                    dq[0] = make_uint4(q[0], q[1], q[2], q[3]);
+                    dq[1] = make_uint4(q[4], q[5], q[6], q[7]);
+                    g.qs0[mx_sf_offset(hrow, col, F)] = (uint8_t)sb;
                 }
             }
         } else if constexpr (OP == OP_FWD2 || OP == OP_BWD1) {
@@ -303,9 +443,10 @@ __device__ void epilogue_loop(const GemmArgs &g, const SmemCtl &c, uint64_t *tfu
                 }
                 tmem_ld_wait();
                 uint32_t oda[16], odb[16], ohw[16];
+                float daf[32], dbf[32];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    float da2[2], db2[2], hw2[2];
+                    float hw2[2];
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         float a = h2 ? bf16hi(ra[i]) : bf16lo(ra[i]);
@@ -316,13 +457,28 @@ __device__ void epilogue_loop(const GemmArgs &g, const SmemCtl &c, uint64_t *tfu
                         float hval = __bfloat162float(__float2bfloat16_rn(sl * b));   // h as the forward stored it
                         dwp = fmaf(G, hval, dwp);
                         float dh = w * G;
-                        da2[h2] = dh * b * sg * (1.0f + a * (1.0f - sg));
-                        db2[h2] = dh * sl;
+                        daf[2 * i + h2] = dh * b * sg * (1.0f + a * (1.0f - sg));
+                        dbf[2 * i + h2] = dh * sl;
                         hw2[h2] = w * hval;
                     }
-                    oda[i] = pack_bf16x2(da2[0], da2[1]);
-                    odb[i] = pack_bf16x2(db2[0], db2[1]);
+                    oda[i] = pack_bf16x2(daf[2 * i], daf[2 * i + 1]);
+                    odb[i] = pack_bf16x2(dbf[2 * i], dbf[2 * i + 1]);
                     ohw[i] = pack_bf16x2(hw2[0], hw2[1]);
+                }
+                if constexpr (FP8) {
+                    // da, db quantised along F (blocks of 32) for the GEMM1 dgrad
+                    const size_t col = (size_t)ti.nt * BN + cc * 32;
+                    uint32_t q[8];
+                    uint32_t sb = mx_quant32(daf, q);
+                    uint4 *dq = reinterpret_cast<uint4 *>(g.q0 + (size_t)grow * F + col);
+                    dq[0] = make_uint4(q[0], q[1], q[2], q[3]);
+                    dq[1] = make_uint4(q[4], q[5], q[6], q[7]);
+                    g.qs0[mx_sf_offset(grow, col, F)] = (uint8_t)sb;
+                    sb = mx_quant32(dbf, q);
+                    dq = reinterpret_cast<uint4 *>(g.q1 + (size_t)grow * F + col);
+                    dq[0] = make_uint4(q[0], q[1], q[2], q[3]);
+                    dq[1] = make_uint4(q[4], q[5], q[6], q[7]);
+                    g.qs1[mx_sf_offset(grow, col, F)] = (uint8_t)sb;
                 }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -371,16 +527,20 @@ __device__ void epilogue_loop(const GemmArgs &g, const SmemCtl &c, uint64_t *tfu
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&tempty[acc]));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+        if constexpr (FP8) {
+            acc_phase ^= 1;
+        } else {
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
     }
 }
 
-template <int OP>
+template <int OP, bool FP8>
 __global__ void __launch_bounds__(192, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    SmemCtl &c = *reinterpret_cast<SmemCtl *>(tiles + STAGES * STAGE_BYTES);
+    SmemCtl &c = *reinterpret_cast<SmemCtl *>(tiles + STAGES * stage_stride<FP8>());
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     WaitCtl ctl{g.status, g.budget_ns};
 
@@ -427,11 +587,11 @@ __global__ void __launch_bounds__(192, 1) grouped_gemm_kernel(const __grid_const
     const uint32_t tmem = c.tmem_base;
 
     if (warp == 0) {
-        if (lane == 0) producer_loop<OP>(g, c, tiles, c.full, c.empty, ctl);
+        if (lane == 0) producer_loop<OP, FP8>(g, c, tiles, c.full, c.empty, ctl);
     } else if (warp == 1) {
-        if (lane == 0) mma_loop<OP>(g, c, tiles, c.full, c.empty, c.tfull, c.tempty, &c.drain, tmem, ctl);
+        if (lane == 0) mma_loop<OP, FP8>(g, c, tiles, c.full, c.empty, c.tfull, c.tempty, &c.drain, tmem, ctl);
     } else {
-        epilogue_loop<OP>(g, c, c.tfull, c.tempty, tmem, ctl);
+        epilogue_loop<OP, FP8>(g, c, c.tfull, c.tempty, tmem, ctl);
     }
     tc_fence_before();
     __syncthreads();
@@ -439,28 +599,34 @@ __global__ void __launch_bounds__(192, 1) grouped_gemm_kernel(const __grid_const
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <int OP>
+template <int OP, bool FP8>
 cudaError_t launch_op(const GemmArgs &g, int grid, cudaStream_t stream) {
-    constexpr size_t smem = STAGES * STAGE_BYTES + sizeof(SmemCtl) + 1024;
+    constexpr size_t smem = STAGES * stage_stride<FP8>() + sizeof(SmemCtl) + 1024;
     static_assert(smem <= 227 * 1024, "shared memory budget");
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t err =
+        cudaFuncSetAttribute(grouped_gemm_kernel<OP, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    grouped_gemm_kernel<OP><<<grid, 192, smem, stream>>>(g);
+    grouped_gemm_kernel<OP, FP8><<<grid, 192, smem, stream>>>(g);
     return cudaGetLastError();
+}
+
+template <bool FP8>
+cudaError_t launch_any(int op, const GemmArgs &g, int grid, cudaStream_t stream) {
+    switch (op) {
+        case OP_FWD1: return launch_op<OP_FWD1, FP8>(g, grid, stream);
+        case OP_FWD2: return launch_op<OP_FWD2, FP8>(g, grid, stream);
+        case OP_BWD2: return launch_op<OP_BWD2, FP8>(g, grid, stream);
+        case OP_BWD1: return launch_op<OP_BWD1, FP8>(g, grid, stream);
+        case OP_WG2: return launch_op<OP_WG2, FP8>(g, grid, stream);
+        case OP_WG13: return launch_op<OP_WG13, FP8>(g, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
 
-cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream) {
-    switch (op) {
-        case OP_FWD1: return launch_op<OP_FWD1>(g, grid, stream);
-        case OP_FWD2: return launch_op<OP_FWD2>(g, grid, stream);
-        case OP_BWD2: return launch_op<OP_BWD2>(g, grid, stream);
-        case OP_BWD1: return launch_op<OP_BWD1>(g, grid, stream);
-        case OP_WG2: return launch_op<OP_WG2>(g, grid, stream);
-        case OP_WG13: return launch_op<OP_WG13>(g, grid, stream);
-        default: return cudaErrorInvalidValue;
-    }
+cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream, bool fp8) {
+    return fp8 ? launch_any<true>(op, g, grid, stream) : launch_any<false>(op, g, grid, stream);
 }
 
 }  // namespace moe

@@ -25,10 +25,15 @@ struct GemmArgs {
     const int *row_slot;          // BWD2: slot of each padded row (-1 = padding)
     const float *wslot;           // BWD2: router weight of each slot
     int accumulate;               // WG ops: add into the fp32 outputs
+    // MXFP8 variant: scale atoms of A (a0, a1) and B (b0, b1) operands, the
+    // K extent of the stored operand matrices, and quantised epilogue outputs
+    const uint8_t *sfa0, *sfa1, *sfb0, *sfb1;
+    int kstore;
+    uint8_t *q0, *q1, *qs0, *qs1;  // FWD1: h codes/scales (ring); BWD2: da, db codes/scales
     int *status;
     unsigned long long budget_ns;
 };
 
-cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream);
+cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream, bool fp8 = false);
 
 }  // namespace moe

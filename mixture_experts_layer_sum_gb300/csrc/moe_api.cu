@@ -10,6 +10,7 @@
 
 #include "../../include/moe.h"
 #include "grouped_gemm.cuh"
+#include "mx_quant.cuh"
 #include "route_kernels.cuh"
 
 using namespace moe;
@@ -181,6 +182,17 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     L.w_dwpart = take(4 * rp * (F / 256));
     L.w_dlogits = take(4 * T * E);
     L.w_dwr_part = take(4 * (size_t)L.dwr_splits * H * E);
+    if (mx) {
+        const size_t qh = rp * H, qf = rp * F;
+        L.w_Ginq = take(qh); L.w_Ginq_s = take(qh / kMxBlock);
+        L.w_daq = take(qf); L.w_daq_s = take(qf / kMxBlock);
+        L.w_dbq = take(qf); L.w_dbq_s = take(qf / kMxBlock);
+        L.w_GinT = take(qh); L.w_GinT_s = take(qh / kMxBlock);
+        L.w_XsT = take(qh); L.w_XsT_s = take(qh / kMxBlock);
+        L.w_hwT = take(qf); L.w_hwT_s = take(qf / kMxBlock);
+        L.w_daT = take(qf); L.w_daT_s = take(qf / kMxBlock);
+        L.w_dbT = take(qf); L.w_dbT_s = take(qf / kMxBlock);
+    }
     const size_t bwd_end = o;
     L.workspace_bytes = std::max(fwd_end, bwd_end);
     return MOE_OK;
@@ -219,6 +231,43 @@ bool make_map(CUtensorMap *m, const void *base, size_t rows, size_t cols, int bo
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// 2-D map over a row-major [rows, cols] array of bytes (E4M3 codes); box = 128
+// columns (the 128-byte swizzle span) x box_rows rows.
+bool make_map_u8(CUtensorMap *m, const void *base, size_t rows, size_t cols, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || rows == 0) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// MXFP8 weight copies made by moe_quantize_weights, each K-major for one GEMM:
+//   w1t, w3t: W1^T, W3^T [E][F][H] along H (GEMM1)     w2t: W2^T [E][H][F] along F (GEMM2)
+//   w2q:      W2 [E][F][H] along H (GEMM2 dgrad)       w1q, w3q: W1, W3 [E][H][F] along F (GEMM1 dgrad)
+// Each is E*H*F bytes of E4M3 codes followed by E*H*F/32 bytes of scale atoms.
+struct QwLayout {
+    size_t codes[6], scales[6], bytes;
+};
+enum { QW_W1T = 0, QW_W3T, QW_W2T, QW_W2Q, QW_W1Q, QW_W3Q };
+QwLayout qw_layout(const moe_config_t *c) {
+    QwLayout q{};
+    const size_t n = (size_t)c->E * c->H * c->F;
+    size_t o = 0;
+    for (int i = 0; i < 6; ++i) {
+        q.codes[i] = o;
+        o = align_up(o + n, 1024);
+        q.scales[i] = o;
+        o = align_up(o + n / kMxBlock, 1024);
+    }
+    q.bytes = o;
+    return q;
 }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -355,16 +404,46 @@ size_t moe_saved_size(const moe_config_t *cfg) {
 }
 
 size_t moe_qweights_size(const moe_config_t *cfg) {
-    (void)cfg;
-    return 0;
+    if (check_shape(cfg) != MOE_OK || cfg->precision != MOE_PRECISION_MXFP8) return 0;
+    return qw_layout(cfg).bytes + kBaseSlack;
 }
 
 moe_status_t moe_quantize_weights(const moe_config_t *cfg, const void *W1, const void *W3, const void *W2,
                                   void *qweights, size_t qweights_bytes, moe_stream_t stream) {
-    (void)W1; (void)W3; (void)W2; (void)qweights; (void)qweights_bytes; (void)stream;
     moe_status_t st = check_shape(cfg);
     if (st != MOE_OK) return st;
-    return fail(MOE_ERR_UNSUPPORTED, "MXFP8 weight quantisation is not available in this build");
+    if (cfg->precision != MOE_PRECISION_MXFP8) return fail(MOE_ERR_UNSUPPORTED, "weight quantisation is for MXFP8 configs");
+    if (!W1 || !W3 || !W2 || !qweights) return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
+    const QwLayout q = qw_layout(cfg);
+    if (!fits(qweights, qweights_bytes, q.bytes)) return fail(MOE_ERR_WORKSPACE, "qweights buffer too small");
+    const void *ptrs16[] = {W1, W3, W2};
+    for (const void *p : ptrs16)
+        if (!aligned(p, 16)) return fail(MOE_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    uint8_t *qw = static_cast<uint8_t *>(align_base(qweights));
+    cudaStream_t s = (cudaStream_t)stream;
+    const int E = cfg->E, H = cfg->H, F = cfg->F;
+    int sms = cfg->num_sms > 0 ? cfg->num_sms : query_num_sms();
+    if (sms <= 0) return fail(MOE_ERR_CUDA, "could not query the SM count");
+    ProfScope ps("quantize_weights", s);
+    // transposed copies (contraction axis = rows of the stored weight)
+    const struct { const void *src; int idx, R, C; } tr[3] = {{W1, QW_W1T, H, F}, {W3, QW_W3T, H, F}, {W2, QW_W2T, F, H}};
+    for (const auto &t : tr) {
+        MxTransposeArgs a{};
+        a.src = (const bf16 *)t.src; a.codes = qw + q.codes[t.idx]; a.scales = qw + q.scales[t.idx];
+        a.R = t.R; a.C = t.C; a.r_limit_ptr = nullptr;
+        st = cuda_check(launch_mx_transpose(a, E, s), "weight transpose-quantise launch");
+        if (st != MOE_OK) return st;
+    }
+    // row-wise copies (contraction axis = columns of the stored weight)
+    const struct { const void *src; int idx, rows, C; } rw[3] = {{W2, QW_W2Q, E * F, H}, {W1, QW_W1Q, E * H, F}, {W3, QW_W3Q, E * H, F}};
+    for (const auto &t : rw) {
+        MxRowsArgs a{};
+        a.src = (const bf16 *)t.src; a.codes = qw + q.codes[t.idx]; a.scales = qw + q.scales[t.idx];
+        a.nrows = t.rows; a.C = t.C; a.k = 1;
+        st = cuda_check(launch_mx_rows(a, t.rows, sms, s), "weight quantise launch");
+        if (st != MOE_OK) return st;
+    }
+    return MOE_OK;
 }
 
 moe_status_t moe_reset_status(void *workspace, moe_stream_t stream) {
@@ -419,8 +498,6 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
     if (st != MOE_OK) return st;
     if (cfg->precision == MOE_PRECISION_MXFP8 && !qweights)
         return fail(MOE_ERR_INVALID_ARG, "MXFP8 forward needs qweights");
-    if (cfg->precision == MOE_PRECISION_MXFP8)
-        return fail(MOE_ERR_UNSUPPORTED, "MXFP8 forward is not available in this build");
     if (!W_r || !W1 || !W3 || !W2 || !saved || !workspace || (L.T > 0 && (!x || !out || !topk_ids || !topk_w)))
         return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
     if (!fits(saved, saved_bytes, L.saved_bytes)) return fail(MOE_ERR_WORKSPACE, "saved buffer too small");
@@ -467,37 +544,62 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
     if (st != MOE_OK) return st;
 
     // 3. per macrobatch: dispatch -> GEMM1+SwiGLU -> GEMM2 -> combine
+    const bool mx = cfg->precision == MOE_PRECISION_MXFP8;
     bf16 *ringX = at<bf16>(ws, L.w_ringX), *ringH = at<bf16>(ws, L.w_ringH), *ringY = at<bf16>(ws, L.w_ringY);
+    uint8_t *ringXq = at<uint8_t>(ws, L.w_ringX), *ringHq = at<uint8_t>(ws, L.w_ringH);
+    uint8_t *ringXs = mx ? at<uint8_t>(ws, L.w_ringXs) : nullptr, *ringHs = mx ? at<uint8_t>(ws, L.w_ringHs) : nullptr;
     const size_t ring_rows = (size_t)L.half_rows * L.ring_halves;
     GemmArgs g1 = gemm_base(L, ws, s_offp, cfg), g2 = gemm_base(L, ws, s_offp, cfg);
-    if (!make_map(&g1.a0, ringX, ring_rows, L.H, 128) || !make_map(&g1.b0, W1, (size_t)L.E * L.H, L.F, 64) ||
-        !make_map(&g1.b1, W3, (size_t)L.E * L.H, L.F, 64) || !make_map(&g2.a0, ringH, ring_rows, L.F, 128) ||
-        !make_map(&g2.b0, W2, (size_t)L.E * L.F, L.H, 64))
-        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    if (!mx) {
+        if (!make_map(&g1.a0, ringX, ring_rows, L.H, 128) || !make_map(&g1.b0, W1, (size_t)L.E * L.H, L.F, 64) ||
+            !make_map(&g1.b1, W3, (size_t)L.E * L.H, L.F, 64) || !make_map(&g2.a0, ringH, ring_rows, L.F, 128) ||
+            !make_map(&g2.b0, W2, (size_t)L.E * L.F, L.H, 64))
+            return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        g1.o2 = ringH;
+    } else {
+        const QwLayout q = qw_layout(cfg);
+        const uint8_t *qw = static_cast<const uint8_t *>(align_base(qweights));
+        const size_t EF = (size_t)L.E * L.F, EH = (size_t)L.E * L.H;
+        if (!make_map_u8(&g1.a0, ringXq, ring_rows, L.H, 128) || !make_map_u8(&g1.b0, qw + q.codes[QW_W1T], EF, L.H, 128) ||
+            !make_map_u8(&g1.b1, qw + q.codes[QW_W3T], EF, L.H, 128) ||
+            !make_map_u8(&g2.a0, ringHq, ring_rows, L.F, 128) || !make_map_u8(&g2.b0, qw + q.codes[QW_W2T], EH, L.F, 256))
+            return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        g1.sfa0 = ringXs; g1.sfb0 = qw + q.scales[QW_W1T]; g1.sfb1 = qw + q.scales[QW_W3T]; g1.kstore = L.H;
+        g1.q0 = ringHq; g1.qs0 = ringHs;
+        g2.sfa0 = ringHs; g2.sfb0 = qw + q.scales[QW_W2T]; g2.kstore = L.F;
+    }
     g1.N = L.F; g1.K = L.H; g1.a_ring = 1;
-    g1.o0 = s_a; g1.o1 = s_b; g1.o2 = ringH;
+    g1.o0 = s_a; g1.o1 = s_b;
     g2.N = L.H; g2.K = L.F; g2.a_ring = 1; g2.o_ring = 1;
     g2.o0 = ringY;
     for (int m = 0; m < L.nM; ++m) {
         const int ring_base = (m % L.ring_halves) * L.half_rows;
-        DispatchArgs da{};
-        da.src = (const bf16 *)x; da.dst = ringX; da.row_slot = s_row_slot; da.offp = s_offp;
-        da.beg = m * L.E; da.end = (m + 1) * L.E; da.dst_row0 = ring_base; da.H = L.H; da.k = L.k;
-        {
+        if (!mx) {
+            DispatchArgs da{};
+            da.src = (const bf16 *)x; da.dst = ringX; da.row_slot = s_row_slot; da.offp = s_offp;
+            da.beg = m * L.E; da.end = (m + 1) * L.E; da.dst_row0 = ring_base; da.H = L.H; da.k = L.k;
             ProfScope ps("dispatch", s);
             st = cuda_check(launch_dispatch(da, L.half_rows, L.num_sms, s), "dispatch launch");
+        } else {
+            // quantising dispatch: x rows gathered and written once, as MXFP8 along H
+            MxRowsArgs da{};
+            da.src = (const bf16 *)x; da.codes = ringXq; da.scales = ringXs; da.row_slot = s_row_slot;
+            da.offp = s_offp; da.beg = m * L.E; da.end = (m + 1) * L.E; da.dst_row0 = ring_base; da.C = L.H;
+            da.k = L.k;
+            ProfScope ps("dispatch_mxfp8", s);
+            st = cuda_check(launch_mx_rows(da, L.half_rows, L.num_sms, s), "dispatch launch");
         }
         if (st != MOE_OK) return st;
         g1.m = m; g1.ring_base = ring_base;
         {
             ProfScope ps("grouped_gemm_fwd1_swiglu", s);
-            st = cuda_check(launch_grouped_gemm(OP_FWD1, g1, L.num_sms, s), "GEMM1 launch");
+            st = cuda_check(launch_grouped_gemm(OP_FWD1, g1, L.num_sms, s, mx), "GEMM1 launch");
         }
         if (st != MOE_OK) return st;
         g2.m = m; g2.ring_base = ring_base;
         {
             ProfScope ps("grouped_gemm_fwd2", s);
-            st = cuda_check(launch_grouped_gemm(OP_FWD2, g2, L.num_sms, s), "GEMM2 launch");
+            st = cuda_check(launch_grouped_gemm(OP_FWD2, g2, L.num_sms, s, mx), "GEMM2 launch");
         }
         if (st != MOE_OK) return st;
         CombineArgs ca{};
@@ -517,12 +619,11 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
                           const void *W3, const void *W2, const void *qweights, const void *saved, void *dx,
                           float *dW_r, float *dW1, float *dW3, float *dW2, int accumulate, void *workspace,
                           size_t workspace_bytes, moe_stream_t stream) {
-    (void)qweights;
     Layout L;
     moe_status_t st = make_layout(cfg, L);
     if (st != MOE_OK) return st;
-    if (cfg->precision == MOE_PRECISION_MXFP8)
-        return fail(MOE_ERR_UNSUPPORTED, "MXFP8 backward is not available in this build");
+    const bool mx = cfg->precision == MOE_PRECISION_MXFP8;
+    if (mx && !qweights) return fail(MOE_ERR_INVALID_ARG, "MXFP8 backward needs qweights");
     if (!W_r || !W1 || !W3 || !W2 || !saved || !workspace || !dW_r || !dW1 || !dW3 || !dW2 ||
         (L.T > 0 && (!x || !dout || !dx)))
         return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
@@ -568,13 +669,55 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
     }
     GemmArgs gb2 = gemm_base(L, ws, s_offp, cfg), gb1 = gemm_base(L, ws, s_offp, cfg);
     GemmArgs gw2 = gemm_base(L, ws, s_offp, cfg), gw13 = gemm_base(L, ws, s_offp, cfg);
-    if (!make_map(&gb2.a0, Gin, rp, L.H, 128) || !make_map(&gb2.b0, W2, (size_t)L.E * L.F, L.H, 256) ||
-        !make_map(&gb1.a0, dA, rp, L.F, 128) || !make_map(&gb1.a1, dB, rp, L.F, 128) ||
-        !make_map(&gb1.b0, W1, (size_t)L.E * L.H, L.F, 256) || !make_map(&gb1.b1, W3, (size_t)L.E * L.H, L.F, 256) ||
-        !make_map(&gw2.a0, HW, rp, L.F, 64) || !make_map(&gw2.b0, Gin, rp, L.H, 64) ||
-        !make_map(&gw13.a0, Xs, rp, L.H, 64) || !make_map(&gw13.b0, dA, rp, L.F, 64) ||
-        !make_map(&gw13.b1, dB, rp, L.F, 64))
-        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    const size_t EF = (size_t)L.E * L.F, EH = (size_t)L.E * L.H;
+    if (!mx) {
+        if (!make_map(&gb2.a0, Gin, rp, L.H, 128) || !make_map(&gb2.b0, W2, EF, L.H, 256) ||
+            !make_map(&gb1.a0, dA, rp, L.F, 128) || !make_map(&gb1.a1, dB, rp, L.F, 128) ||
+            !make_map(&gb1.b0, W1, EH, L.F, 256) || !make_map(&gb1.b1, W3, EH, L.F, 256) ||
+            !make_map(&gw2.a0, HW, rp, L.F, 64) || !make_map(&gw2.b0, Gin, rp, L.H, 64) ||
+            !make_map(&gw13.a0, Xs, rp, L.H, 64) || !make_map(&gw13.b0, dA, rp, L.F, 64) ||
+            !make_map(&gw13.b1, dB, rp, L.F, 64))
+            return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    } else {
+        const QwLayout q = qw_layout(cfg);
+        const uint8_t *qw = static_cast<const uint8_t *>(align_base(qweights));
+        auto u8 = [&](size_t off) { return at<uint8_t>(ws, off); };
+        if (!make_map_u8(&gb2.a0, u8(L.w_Ginq), rp, L.H, 128) || !make_map_u8(&gb2.b0, qw + q.codes[QW_W2Q], EF, L.H, 256) ||
+            !make_map_u8(&gb1.a0, u8(L.w_daq), rp, L.F, 128) || !make_map_u8(&gb1.a1, u8(L.w_dbq), rp, L.F, 128) ||
+            !make_map_u8(&gb1.b0, qw + q.codes[QW_W1Q], EH, L.F, 256) ||
+            !make_map_u8(&gb1.b1, qw + q.codes[QW_W3Q], EH, L.F, 256) ||
+            !make_map_u8(&gw2.a0, u8(L.w_hwT), L.F, rp, 128) || !make_map_u8(&gw2.b0, u8(L.w_GinT), L.H, rp, 256) ||
+            !make_map_u8(&gw13.a0, u8(L.w_XsT), L.H, rp, 128) || !make_map_u8(&gw13.b0, u8(L.w_daT), L.F, rp, 128) ||
+            !make_map_u8(&gw13.b1, u8(L.w_dbT), L.F, rp, 128))
+            return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        gb2.sfa0 = u8(L.w_Ginq_s); gb2.sfb0 = qw + q.scales[QW_W2Q]; gb2.kstore = L.H;
+        gb2.q0 = u8(L.w_daq); gb2.qs0 = u8(L.w_daq_s); gb2.q1 = u8(L.w_dbq); gb2.qs1 = u8(L.w_dbq_s);
+        gb1.sfa0 = u8(L.w_daq_s); gb1.sfa1 = u8(L.w_dbq_s);
+        gb1.sfb0 = qw + q.scales[QW_W1Q]; gb1.sfb1 = qw + q.scales[QW_W3Q]; gb1.kstore = L.F;
+        gw2.sfa0 = u8(L.w_hwT_s); gw2.sfb0 = u8(L.w_GinT_s); gw2.kstore = (int)rp;
+        gw13.sfa0 = u8(L.w_XsT_s); gw13.sfb0 = u8(L.w_daT_s); gw13.sfb1 = u8(L.w_dbT_s); gw13.kstore = (int)rp;
+    }
+    // token-axis MXFP8 copies: bf16 [rows][C] -> [C][rows] quantised along rows
+    auto transpose_q = [&](const bf16 *src, size_t codes, size_t scales, int C, const char *name) {
+        MxTransposeArgs a{};
+        a.src = src; a.codes = at<uint8_t>(ws, codes); a.scales = at<uint8_t>(ws, scales);
+        a.R = (int)rp; a.C = C; a.r_limit_ptr = s_offp + L.nM * L.E;
+        ProfScope ps(name, s);
+        return cuda_check(launch_mx_transpose(a, 1, s), "token-axis quantise launch");
+    };
+    if (mx && L.T > 0) {
+        // dY rows along H for the GEMM2 dgrad; dY and X along the token axis for the weight gradients
+        MxRowsArgs a{};
+        a.src = Gin; a.codes = at<uint8_t>(ws, L.w_Ginq); a.scales = at<uint8_t>(ws, L.w_Ginq_s);
+        a.offp = s_offp; a.beg = 0; a.end = L.nM * L.E; a.dst_row0 = 0; a.C = L.H; a.k = 1;
+        {
+            ProfScope ps("quantize_dy_rows", s);
+            st = cuda_check(launch_mx_rows(a, L.rows_pad_max, L.num_sms, s), "dY quantise launch");
+        }
+        if (st != MOE_OK) return st;
+        if ((st = transpose_q(Gin, L.w_GinT, L.w_GinT_s, L.H, "quantize_dy_tokens")) != MOE_OK) return st;
+        if ((st = transpose_q(Xs, L.w_XsT, L.w_XsT_s, L.H, "quantize_x_tokens")) != MOE_OK) return st;
+    }
     // 2. GEMM2 dgrad + SwiGLU backward, per macrobatch (global rows)
     gb2.N = L.F; gb2.K = L.H;
     gb2.in0 = s_a; gb2.in1 = s_b; gb2.o0 = dA; gb2.o1 = dB; gb2.o2 = HW; gb2.of0 = dwpart;
@@ -585,15 +728,20 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
             gb2.m = m;
             {
                 ProfScope ps("grouped_gemm_bwd2_swiglu", s);
-                st = cuda_check(launch_grouped_gemm(OP_BWD2, gb2, L.num_sms, s), "GEMM2 dgrad launch");
+                st = cuda_check(launch_grouped_gemm(OP_BWD2, gb2, L.num_sms, s, mx), "GEMM2 dgrad launch");
             }
             if (st != MOE_OK) return st;
+        }
+        if (mx) {
+            if ((st = transpose_q(HW, L.w_hwT, L.w_hwT_s, L.F, "quantize_hw_tokens")) != MOE_OK) return st;
+            if ((st = transpose_q(dA, L.w_daT, L.w_daT_s, L.F, "quantize_da_tokens")) != MOE_OK) return st;
+            if ((st = transpose_q(dB, L.w_dbT, L.w_dbT_s, L.F, "quantize_db_tokens")) != MOE_OK) return st;
         }
         for (int m = 0; m < L.nM; ++m) {
             gb1.m = m;
             {
                 ProfScope ps("grouped_gemm_bwd1", s);
-                st = cuda_check(launch_grouped_gemm(OP_BWD1, gb1, L.num_sms, s), "GEMM1 dgrad launch");
+                st = cuda_check(launch_grouped_gemm(OP_BWD1, gb1, L.num_sms, s, mx), "GEMM1 dgrad launch");
             }
             if (st != MOE_OK) return st;
         }
@@ -617,13 +765,13 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
     gw2.Mw = L.F; gw2.N = L.H; gw2.of0 = dW2; gw2.accumulate = accumulate;
     {
         ProfScope ps("grouped_gemm_wgrad2", s);
-        st = cuda_check(launch_grouped_gemm(OP_WG2, gw2, L.num_sms, s), "dW2 launch");
+        st = cuda_check(launch_grouped_gemm(OP_WG2, gw2, L.num_sms, s, mx), "dW2 launch");
     }
     if (st != MOE_OK) return st;
     gw13.Mw = L.H; gw13.N = L.F; gw13.of0 = dW1; gw13.of1 = dW3; gw13.accumulate = accumulate;
     {
         ProfScope ps("grouped_gemm_wgrad13", s);
-        st = cuda_check(launch_grouped_gemm(OP_WG13, gw13, L.num_sms, s), "dW1/dW3 launch");
+        st = cuda_check(launch_grouped_gemm(OP_WG13, gw13, L.num_sms, s, mx), "dW1/dW3 launch");
     }
     return st;
 }

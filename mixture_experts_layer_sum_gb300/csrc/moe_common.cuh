@@ -47,6 +47,9 @@ struct Layout {
     size_t w_status, w_chunk_counts, w_chunk_base, w_wrt, w_offp;
     size_t w_ringX, w_ringXs, w_ringH, w_ringHs, w_ringY, ring_bytes;   // forward
     size_t w_Xs, w_Gin, w_da, w_db, w_hw, w_dXs, w_dwpart, w_dlogits, w_dwr_part;   // backward
+    // backward, MXFP8 only: quantised operands (codes, scale atoms)
+    size_t w_Ginq, w_Ginq_s, w_daq, w_daq_s, w_dbq, w_dbq_s;       // along H / F (row-wise)
+    size_t w_GinT, w_GinT_s, w_XsT, w_XsT_s, w_hwT, w_hwT_s, w_daT, w_daT_s, w_dbT, w_dbT_s;   // along rows
     size_t workspace_bytes;
 };
 
@@ -71,5 +74,54 @@ __device__ __forceinline__ uint4 ld_v4(const void *p) {
     return *reinterpret_cast<const uint4 *>(p);
 }
 __device__ __forceinline__ void st_v4(void *p, uint4 v) { *reinterpret_cast<uint4 *>(p) = v; }
+
+}  // namespace moe
+
+namespace moe {
+
+// ---------------------------------------------------------------- MXFP8
+// E4M3 element codes with one E8M0 scale byte per 32 consecutive elements of a
+// row along the contraction axis K. Scales are stored in 512-byte atoms that
+// cover 128 rows x 128 elements (4 blocks): atom (r/128, k/128) in row-major
+// order, byte (r%32)*16 + ((r/32)%4)*4 + (k/32)%4 inside it. This is the order
+// tcgen05.cp.32x128b.warpx4 moves into tensor memory for the block-scaled MMA.
+__host__ __device__ __forceinline__ size_t mx_sf_offset(size_t r, size_t k, size_t K) {
+    return ((r >> 7) * (K >> 7) + (k >> 7)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + ((k >> 5) & 3);
+}
+
+// Shared exponent of a block: the smallest s with amax <= 448 * 2^s (the
+// block's largest element never saturates), clamped to [-127, 127]; zero and
+// subnormal maxima give -127.
+__device__ __forceinline__ int mx_exponent(float amax) {
+    const uint32_t b = __float_as_uint(amax);
+    const int e = (int)((b >> 23) & 0xFF);
+    if (e == 0) return -127;
+    const int s = e - 127 - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    return s < -127 ? -127 : (s > 127 ? 127 : s);
+}
+
+// 2^-s for s in [-127, 126] (finite fp32 maxima give s <= 120)
+__device__ __forceinline__ float mx_inv_scale(int s) { return __uint_as_float((uint32_t)(127 - s) << 23); }
+
+// four floats -> four E4M3 bytes (round to nearest even, saturate finite), element 0 in the low byte
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float d) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(lo) : "f"(a), "f"(b));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(hi) : "f"(c), "f"(d));
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// Quantises 32 values held by one thread: 8 words of codes, returns the scale byte.
+__device__ __forceinline__ uint32_t mx_quant32(const float (&v)[32], uint32_t (&codes)[8]) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int s = mx_exponent(amax);
+    const float inv = mx_inv_scale(s);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        codes[i] = cvt_e4m3x4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+    return (uint32_t)(s + 127);
+}
 
 }  // namespace moe

@@ -1,0 +1,101 @@
+"""GPU parity of the MXFP8 path (run on a GB300).
+
+- moe_quantize_weights: E4M3 codes and E8M0 scales of all six weight copies
+  are bit-exact against the oracle's quantiser (same blocks, same rounding).
+- forward + backward against the oracle run with the same MXFP8 quantisation
+  emulated at the same points: max-abs-relative error below 6e-2."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as WL
+from oracle import moe_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from mixture_experts_layer_sum_gb300 import build_ext
+    build_ext.build()
+    assert torch.cuda.is_available()
+
+
+def G():
+    import tests.gpu_common as g
+    return g
+
+
+def atoms_to_rows(sf_bytes, rows, K):
+    """Scale atoms (512 B per 128 rows x 128 elements) -> [rows, K/32] scale bytes."""
+    r = np.arange(rows)[:, None]
+    kb = np.arange(K // 32)[None, :]
+    off = ((r // 128) * (K // 128) + (kb * 32) // 128) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + kb % 4
+    return sf_bytes[off]
+
+
+def test_quantize_weights_bit_exact():
+    w = WL.Workload("mx_small", T=64, H=256, E=4, k=2, F=512, precision="mxfp8")
+    inp = WL.make_inputs(w)
+    from mixture_experts_layer_sum_gb300.layer import MoeLayer
+    d = G().device_inputs(inp)
+    layer = MoeLayer(w.T, w.H, w.F, w.E, w.k, "mxfp8")
+    layer.quantize_weights(d["W1"], d["W3"], d["W2"])
+    layer.status()
+    qw = layer.qweights.cpu().numpy()
+    E, H, F = w.E, w.H, w.F
+    n = E * H * F
+    # layout: six (codes, scales) pairs, each region 1024-aligned, base aligned inside the buffer
+    ptr = layer.qweights.data_ptr()
+    start = (-ptr) % 1024
+    offs = []
+    o = 0
+    for _ in range(6):
+        c = o; o = -(-(o + n) // 1024) * 1024
+        s_ = o; o = -(-(o + n // 32) // 1024) * 1024
+        offs.append((start + c, start + s_))
+    W = {k: O.bf16_to_f64(inp[k]) for k in ("W1", "W3", "W2")}
+    cases = [("W1", True, H, F), ("W3", True, H, F), ("W2", True, F, H),
+             ("W2", False, F, H), ("W1", False, H, F), ("W3", False, H, F)]
+    for i, (name, transposed, R, C) in enumerate(cases):
+        codes = qw[offs[i][0]:offs[i][0] + n]
+        sf = qw[offs[i][1]:offs[i][1] + n // 32]
+        for e in range(E):
+            if transposed:      # stored [C][R], blocks along R
+                ref_c, ref_s = O.mx_quantize(W[name][e].T, 1)
+                got_c = codes[e * C * R:(e + 1) * C * R].reshape(C, R)
+                got_s = atoms_to_rows(sf[e * C * R // 32:(e + 1) * C * R // 32], C, R)
+            else:               # stored [R][C], blocks along C
+                ref_c, ref_s = O.mx_quantize(W[name][e], 1)
+                got_c = codes[e * R * C:(e + 1) * R * C].reshape(R, C)
+                got_s = atoms_to_rows(sf[e * R * C // 32:(e + 1) * R * C // 32], R, C)
+            np.testing.assert_array_equal(got_s, ref_s, err_msg=f"{name} scales e={e} transposed={transposed}")
+            np.testing.assert_array_equal(got_c, ref_c, err_msg=f"{name} codes e={e} transposed={transposed}")
+
+
+@pytest.mark.parametrize("T,macro", [(300, 0), (300, 100), (1, 0)])
+def test_mxfp8_fwd_bwd_small(T, macro):
+    w = WL.Workload("mx_small", T=T, H=512, E=8, k=2, F=512, precision="mxfp8", zipf_s=0.8)
+    inp = WL.make_inputs(w)
+    gpu = G().run_gpu(w, inp, macrobatch_tokens=macro)
+    errs = G().check_layer(w, inp, gpu, macrobatch_tokens=macro)
+    print("mxfp8 small", T, macro, errs)
+
+
+def test_mxfp8_workload_shape_reduced_tokens():
+    # H=7168, F=2048 (the pages' shape), E=16, k=8, Zipf(0.8) skew, first 256 tokens
+    w = WL.MXFP8
+    inp = WL.make_inputs(w, tokens=256)
+    w = w.with_(T=256)
+    gpu = G().run_gpu(w, inp)
+    errs = G().check_layer(w, inp, gpu)
+    print("mxfp8 7168x2048 T=256", errs)
+
+
+def test_mxfp8_deterministic():
+    w = WL.Workload("mx_small", T=200, H=512, E=8, k=2, F=512, precision="mxfp8")
+    inp = WL.make_inputs(w)
+    a = G().run_gpu(w, inp)
+    b = G().run_gpu(w, inp)
+    for key in ("out", "dx", "dWr", "dW1", "dW3", "dW2"):
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
