@@ -408,6 +408,34 @@ def run_ours(args, w):
                 "h2d_bytes_per_step": 2 * w.T * w.H * 2, "d2h_bytes_per_step": 2 * w.T * w.H * 2},
         "clocks": clocks,
     }
+    if args.minibatch_sweep and w.minibatch_rows:
+        sweep = []
+        del layer
+        torch.cuda.empty_cache()
+        for mbr in w.minibatch_rows:
+            lay = MoeLayer(w.T, w.H, w.F, w.E, w.k, w.precision, device=dev, ring_bytes=w.ring_bytes,
+                           minibatch_rows=mbr)
+            if w.precision == "mxfp8":
+                lay.quantize_weights(d["W1"], d["W3"], d["W2"], stream=stream)
+
+            def f1(lay=lay):
+                lay.forward(d["x"], d["Wr"], bias, d["W1"], d["W3"], d["W2"], out, ids, wts, stream=stream)
+
+            def s1(lay=lay):
+                f1()
+                lay.backward(d["dout"], d["x"], d["Wr"], d["W1"], d["W3"], d["W2"], dx, dWr, dW1, dW3, dW2,
+                             stream=stream)
+            with torch.cuda.stream(stream):
+                for _ in range(2):
+                    s1()
+            k = max(2, args.steps // 4)
+            fm, sm = timed(f1, k), timed(s1, k)
+            lay.status(stream)
+            sweep.append({"minibatch_rows": mbr, "fwd_ms": fm / k, "fwd_bwd_ms": sm / k,
+                          "macrobatches": lay.plan.num_macrobatches, "macrobatch_tokens": lay.plan.macrobatch_tokens})
+            del lay
+            torch.cuda.empty_cache()
+        line["minibatch_sweep"] = sweep
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp)
     print(json.dumps(line), flush=True)
@@ -425,6 +453,8 @@ def main():
     ap.add_argument("--workload", default=WL.BALANCED.name, choices=sorted(WL.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--minibatch-sweep", action="store_true",
+                    help="also time fwd and fwd+bwd for each minibatch size of the workload (ring workload)")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference" or args.steps < 3, "need >= 3 warm-up steps"
     w = WL.WORKLOADS[args.workload]

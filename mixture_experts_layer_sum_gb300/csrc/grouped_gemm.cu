@@ -12,7 +12,7 @@
 //   WG2   dW2_e = (w h)_e^T dY_e                (contraction over the expert's rows)
 //   WG13  [dW1_e|dW3_e] = X_e^T [da_e|db_e]      (contraction over the expert's rows)
 //
-// Structure (one CTA per SM, 192 threads):
+// Structure (one CTA per SM, 192 threads; 320 for GEMM1 with the fused dispatch):
 //   warp 0     TMA producer: 128B-swizzled tiles of A (128 x 64) and B
 //              (256 x 64) into a 4-stage shared-memory ring
 //   warp 1     TMEM allocator and single-thread tcgen05.mma issuer
@@ -20,6 +20,8 @@
 //              double buffered (2 x 256 columns)
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator, fused elementwise
 //              work, stores to global memory
+//   warps 6-9  (GEMM1 only) dispatch: gather/quantise token rows into the ring
+//              minibatch by minibatch, publish per-minibatch ready counters
 // MXFP8 variant (FP8 = true): every operand is K-major E4M3 with E8M0 scale
 // atoms (moe_common.cuh); a stage holds 128 elements of K (A 128x128 B,
 // B 256x128 B) plus the 512-byte scale atoms of A and of both 128-row halves
@@ -150,6 +152,66 @@ __device__ __forceinline__ int grouped_k_row(const GemmArgs &g, int e, int kb, i
     return 0;   // unreachable for kb < nk
 }
 
+// Fused dispatch (FWD1): the 4 gather warps of each CTA pull token rows of the
+// macrobatch into the ring (article "O MoK do Cursor ...", section 02: pull
+// dispatch; the ring token buffer is advanced by GPU-side state, minibatch by
+// minibatch, with no CPU in the loop). Rows of minibatch j are spread over all
+// CTAs; after its share of j a CTA adds 1 to ready[j] with release semantics.
+template <bool FP8>
+__device__ void gather_loop(const GemmArgs &g) {
+    const int gw = threadIdx.x / 32 - 6, lane = threadIdx.x % 32;
+    const int r0 = g.offp[g.m * g.E], r1 = g.offp[(g.m + 1) * g.E];
+    const int nmb = (r1 - r0 + g.mb_rows - 1) / g.mb_rows;
+    const int stride = gridDim.x * 4;
+    const int vecs = g.H / 8;
+    for (int j = 0; j < nmb; ++j) {
+        const int b0 = r0 + j * g.mb_rows, b1 = min(r1, b0 + g.mb_rows);
+        for (int r = b0 + blockIdx.x * 4 + gw; r < b1; r += stride) {
+            const int slot = g.row_slot[r];
+            const bf16 *src = slot >= 0 ? g.xsrc + (size_t)(slot / g.k) * g.H : nullptr;
+            const size_t drow = (size_t)(r - r0 + g.ring_base);
+            if constexpr (!FP8) {
+                bf16 *dst = g.ringx + drow * g.H;
+                for (int v = lane; v < vecs; v += 32)
+                    st_v4(dst + v * 8, src ? ld_nc_v4(src + v * 8) : make_uint4(0, 0, 0, 0));
+            } else {
+                uint8_t *dst = g.ringxq + drow * g.H;
+                for (int v = lane; v < vecs; v += 32) {
+                    float f[8];
+                    if (src) {
+                        const uint4 q = ld_nc_v4(src + v * 8);
+                        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) { f[2 * i] = bf16lo(w4[i]); f[2 * i + 1] = bf16hi(w4[i]); }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) f[i] = 0.0f;
+                    }
+                    float amax = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                    const int sx = mx_exponent(amax);
+                    const float inv = mx_inv_scale(sx);
+                    uint2 cq;
+                    cq.x = cvt_e4m3x4(f[0] * inv, f[1] * inv, f[2] * inv, f[3] * inv);
+                    cq.y = cvt_e4m3x4(f[4] * inv, f[5] * inv, f[6] * inv, f[7] * inv);
+                    *reinterpret_cast<uint2 *>(dst + v * 8) = cq;
+                    if ((lane & 3) == 0) g.ringxs[mx_sf_offset(drow, (size_t)v * 8, g.H)] = (uint8_t)(sx + 127);
+                }
+            }
+        }
+        // all 128 gather threads of this CTA are done with minibatch j
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (gw == 0 && lane == 0) {
+            __threadfence();
+            fence_proxy_async_global();
+            red_release_gpu_add(g.ready + j, 1);
+        }
+    }
+}
+
 template <int OP, bool FP8>
 __device__ void producer_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tiles, uint64_t *full,
                               uint64_t *empty, const WaitCtl &ctl) {
@@ -160,8 +222,20 @@ __device__ void producer_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tile
     bool ok = true;
     const int total = num_tiles<OP>(c, g);
     const int a_shift = g.a_ring ? (g.ring_base - g.offp[g.m * g.E]) : 0;
+    int ready_mb = -1;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         TileInfo ti = decode_tile<OP, FP8>(c, g, t);
+        if constexpr (OP == OP_FWD1) {
+            if (g.fused) {
+                // the tile's rows lie in one minibatch (minibatches are 128-row aligned)
+                const int j = (ti.g0 - g.offp[g.m * g.E]) / g.mb_rows;
+                if (j != ready_mb) {
+                    if (!flag_wait_geq(g.ready + j, (int)gridDim.x, ctl)) { ok = false; break; }
+                    fence_proxy_async_global();
+                    ready_mb = j;
+                }
+            }
+        }
         for (int kb = 0; kb < ti.nk; ++kb) {
             if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, ctl)) { ok = false; break; }
             uint32_t bar = smem_u32(&full[stage]);
@@ -537,7 +611,7 @@ __device__ void epilogue_loop(const GemmArgs &g, const SmemCtl &c, uint64_t *tfu
 }
 
 template <int OP, bool FP8>
-__global__ void __launch_bounds__(192, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs g) {
+__global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     SmemCtl &c = *reinterpret_cast<SmemCtl *>(tiles + STAGES * stage_stride<FP8>());
@@ -590,8 +664,10 @@ __global__ void __launch_bounds__(192, 1) grouped_gemm_kernel(const __grid_const
         if (lane == 0) producer_loop<OP, FP8>(g, c, tiles, c.full, c.empty, ctl);
     } else if (warp == 1) {
         if (lane == 0) mma_loop<OP, FP8>(g, c, tiles, c.full, c.empty, c.tfull, c.tempty, &c.drain, tmem, ctl);
-    } else {
+    } else if (warp < 6) {
         epilogue_loop<OP, FP8>(g, c, c.tfull, c.tempty, tmem, ctl);
+    } else {
+        if constexpr (OP == OP_FWD1) gather_loop<FP8>(g);
     }
     tc_fence_before();
     __syncthreads();
@@ -606,6 +682,12 @@ cudaError_t launch_op(const GemmArgs &g, int grid, cudaStream_t stream) {
     cudaError_t err =
         cudaFuncSetAttribute(grouped_gemm_kernel<OP, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
+    if (OP == OP_FWD1 && g.fused) {
+        // gather warps publish flags that other CTAs wait on: all CTAs must be resident
+        void *args[] = {const_cast<GemmArgs *>(&g)};
+        return cudaLaunchCooperativeKernel((const void *)grouped_gemm_kernel<OP, FP8>, dim3(grid), dim3(320), args,
+                                           smem, stream);
+    }
     grouped_gemm_kernel<OP, FP8><<<grid, 192, smem, stream>>>(g);
     return cudaGetLastError();
 }

@@ -160,6 +160,8 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     const size_t EP = (E + 7) / 8 * 8;
     L.w_wrt = take(2 * EP * H);
     L.w_offp = take(4 * (nM * E + 1));
+    L.mb_rows = (int)align_up((size_t)std::max(L.minibatch_rows, kRowPad), kRowPad);
+    L.w_ready = take(4 * ((size_t)L.half_rows / kRowPad + 1));   // per-minibatch ready counters
     const size_t region = o;
     const size_t ring_rows = (size_t)L.half_rows * L.ring_halves;
     // forward region: the ring
@@ -572,23 +574,16 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
     g1.o0 = s_a; g1.o1 = s_b;
     g2.N = L.H; g2.K = L.F; g2.a_ring = 1; g2.o_ring = 1;
     g2.o0 = ringY;
+    // the dispatch runs inside GEMM1: its gather warps fill the ring minibatch by
+    // minibatch and GEMM1 tiles start as soon as their minibatch is complete
+    int *ready = at<int>(ws, L.w_ready);
+    g1.fused = 1; g1.xsrc = (const bf16 *)x; g1.row_slot = s_row_slot; g1.k = L.k; g1.mb_rows = L.mb_rows;
+    g1.ready = ready;
+    if (!mx) g1.ringx = ringX;
+    else { g1.ringxq = ringXq; g1.ringxs = ringXs; }
     for (int m = 0; m < L.nM; ++m) {
         const int ring_base = (m % L.ring_halves) * L.half_rows;
-        if (!mx) {
-            DispatchArgs da{};
-            da.src = (const bf16 *)x; da.dst = ringX; da.row_slot = s_row_slot; da.offp = s_offp;
-            da.beg = m * L.E; da.end = (m + 1) * L.E; da.dst_row0 = ring_base; da.H = L.H; da.k = L.k;
-            ProfScope ps("dispatch", s);
-            st = cuda_check(launch_dispatch(da, L.half_rows, L.num_sms, s), "dispatch launch");
-        } else {
-            // quantising dispatch: x rows gathered and written once, as MXFP8 along H
-            MxRowsArgs da{};
-            da.src = (const bf16 *)x; da.codes = ringXq; da.scales = ringXs; da.row_slot = s_row_slot;
-            da.offp = s_offp; da.beg = m * L.E; da.end = (m + 1) * L.E; da.dst_row0 = ring_base; da.C = L.H;
-            da.k = L.k;
-            ProfScope ps("dispatch_mxfp8", s);
-            st = cuda_check(launch_mx_rows(da, L.half_rows, L.num_sms, s), "dispatch launch");
-        }
+        st = cuda_check(cudaMemsetAsync(ready, 0, 4 * ((size_t)L.half_rows / kRowPad + 1), s), "ready clear");
         if (st != MOE_OK) return st;
         g1.m = m; g1.ring_base = ring_base;
         {

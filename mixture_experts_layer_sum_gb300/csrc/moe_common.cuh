@@ -44,7 +44,8 @@ struct Layout {
     size_t s_ids, s_w, s_probs, s_counts, s_offsets, s_offp, s_s2sorted, s_sorted2s, s_slot_row,
         s_row_slot, s_a, s_b, saved_bytes;
     // workspace (header first, then a region shared by forward and backward)
-    size_t w_status, w_chunk_counts, w_chunk_base, w_wrt, w_offp;
+    size_t w_status, w_chunk_counts, w_chunk_base, w_wrt, w_offp, w_ready;
+    int mb_rows;            // minibatch rows used by the fused dispatch (multiple of 128)
     size_t w_ringX, w_ringXs, w_ringH, w_ringHs, w_ringY, ring_bytes;   // forward
     size_t w_Xs, w_Gin, w_da, w_db, w_hw, w_dXs, w_dwpart, w_dlogits, w_dwr_part;   // backward
     // backward, MXFP8 only: quantised operands (codes, scale atoms)

@@ -76,6 +76,36 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     }
 }
 
+// ---------------------------------------------------------------- flags between CTAs
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(int *p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// orders generic-proxy global writes/reads with later async-proxy (TMA) accesses
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Waits until *p >= target (acquire). Gives up like mbar_wait.
+__device__ __forceinline__ bool flag_wait_geq(const int *p, int target, const WaitCtl &ctl) {
+    if (ld_acquire_gpu(p) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(p) >= target) return true;
+        if ((i & 63u) == 0) {
+            if (ld_volatile(ctl.status) != 0) return false;
+            if (globaltimer_ns() - t0 > ctl.budget_ns) {
+                raise_status(ctl.status, 5);
+                return false;
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

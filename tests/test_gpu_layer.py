@@ -152,3 +152,14 @@ def test_skewed_full_size_sampled_tokens():
     # skew really is skewed
     counts = np.bincount(gpu["ids"].ravel(), minlength=w.E)
     assert counts.max() / counts.mean() > 4
+
+
+@pytest.mark.parametrize("mb", [128, 384, 1 << 20])
+def test_minibatch_sizes_bitwise_equal(mb):
+    # the fused dispatch publishes rows minibatch by minibatch; no row's arithmetic
+    # depends on the partition, so every minibatch size gives identical bytes
+    w = WL.TINY
+    inp = WL.make_inputs(w)
+    base = G().run_gpu(w, inp, backward=False)
+    other = G().run_gpu(w, inp, backward=False, minibatch_rows=mb, macrobatch_tokens=100)
+    np.testing.assert_array_equal(base["out"], other["out"])
