@@ -209,13 +209,14 @@ def stop_clocks(p, path):
 
 
 def kernel_bytes(w, name):
-    """Algorithmic HBM bytes per launch of the memory-bound kernels."""
+    """Algorithmic HBM bytes per step of the memory-bound kernels."""
     T, H, R, E, k = w.T, w.H, w.R, w.E, w.k
     return {"dispatch": T * H * 2 + R * H * 2, "dispatch_replay": T * H * 2 + R * H * 2,
             "dispatch_mxfp8": T * H * 2 + R * H * 33 // 32,
             "reverse_combine": T * H * 2 + R * H * 2, "combine": R * H * 2 + T * H * 2 + R * 8,
             "router_topk": T * H * 2 + T * E * 4 + T * k * 8,
-            "router_bwd": R * H * 2 + T * H * 2 + T * H * 2 + T * E * 8}.get(name)
+            "reverse_dispatch": R * H * 2 + T * H * 2 + T * E * 4,
+            "router_wgrad": T * H * 2 + T * E * 4}.get(name)
 
 
 def gemm_flops(w, name):
@@ -356,7 +357,11 @@ def run_ours(args, w):
     kt = sorted(kernels, key=lambda r: -r[2])
     name, n, ms = kt[0]
     per_launch_ms = ms / n
+    # gemm_flops / kernel_bytes are per step; a kernel may launch several times
+    # per step (one launch per macrobatch)
+    per_step = n / args.steps
     fl = gemm_flops(w, name)
+    fl = None if fl is None else fl / per_step
     roof = None
     if fl is not None:
         peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
@@ -370,12 +375,12 @@ def run_ours(args, w):
                                + (" x 2 (nominal fp8/bf16 ratio)" if w.precision == "mxfp8" else "")}
     elif kernel_bytes(w, name) is not None:
         peak = peaks.get("hbm_gbs")
-        ach = kernel_bytes(w, name) / (per_launch_ms * 1e-3) / 1e9
+        ach = kernel_bytes(w, name) / per_step / (per_launch_ms * 1e-3) / 1e9
         roof = {"kernel": name, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
-                "frac": ach / peak, "traffic": None, "algorithmic_per_launch": kernel_bytes(w, name),
+                "frac": ach / peak, "traffic": None, "algorithmic_per_launch": kernel_bytes(w, name) / per_step,
                 "peak_source": f"{peak_src} hbm_gbs"}
     gemm_ms = sum(ms_ for nm, _, ms_ in kernels if nm.startswith("grouped_gemm"))
-    gemm_fl = sum(gemm_flops(w, nm) * n_ for nm, n_, _ in kernels if nm.startswith("grouped_gemm"))
+    gemm_fl = sum(gemm_flops(w, nm) * args.steps for nm, n_, _ in kernels if nm.startswith("grouped_gemm"))
     value = ws * w.T * args.steps / (total_ms * 1e-3)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
@@ -400,8 +405,8 @@ def run_ours(args, w):
                          "share_of_step": gemm_ms / prof_ms if prof_ms else None},
         "kernels": [dict({"name": nm, "launches": n_, "ms_per_step": ms_ / args.steps,
                           "share": ms_ / prof_ms},
-                         **({"tflops": gemm_flops(w, nm) * n_ / (ms_ * 1e-3) / 1e12} if gemm_flops(w, nm) else {}),
-                         **({"gbs": kernel_bytes(w, nm) * n_ / (ms_ * 1e-3) / 1e9} if kernel_bytes(w, nm) else {}))
+                         **({"tflops": gemm_flops(w, nm) * args.steps / (ms_ * 1e-3) / 1e12} if gemm_flops(w, nm) else {}),
+                         **({"gbs": kernel_bytes(w, nm) * args.steps / (ms_ * 1e-3) / 1e9} if kernel_bytes(w, nm) else {}))
                     for nm, n_, ms_ in kt],
         "gpu_launches": launches,
         "e2e": {"value": ws * w.T * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",

@@ -140,18 +140,6 @@ __device__ __forceinline__ TileInfo decode_tile(const SmemCtl &c, const GemmArgs
     return ti;
 }
 
-// grouped-K ops: the padded row at position kb*BK of expert e's rows, walking
-// the (macrobatch, e) runs in macrobatch order.
-__device__ __forceinline__ int grouped_k_row(const GemmArgs &g, int e, int kb, int bk) {
-    int r = kb * bk;
-    for (int mm = 0; mm < g.nM; ++mm) {
-        int s0 = g.offp[mm * g.E + e], s1 = g.offp[mm * g.E + e + 1];
-        if (r < s1 - s0) return s0 + r;
-        r -= s1 - s0;
-    }
-    return 0;   // unreachable for kb < nk
-}
-
 // Fused dispatch (FWD1): the 4 gather warps of each CTA pull token rows of the
 // macrobatch into the ring (article "O MoK do Cursor ...", section 02: pull
 // dispatch; the ring token buffer is advanced by GPU-side state, minibatch by
@@ -172,14 +160,38 @@ __device__ void gather_loop(const GemmArgs &g) {
             const size_t drow = (size_t)(r - r0 + g.ring_base);
             if constexpr (!FP8) {
                 bf16 *dst = g.ringx + drow * g.H;
-                for (int v = lane; v < vecs; v += 32)
-                    st_v4(dst + v * 8, src ? ld_nc_v4(src + v * 8) : make_uint4(0, 0, 0, 0));
+                int v = lane;
+                for (; v + 96 < vecs; v += 128) {
+                    uint4 q[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) q[u] = src ? ld_nc_v4(src + (v + 32 * u) * 8) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) st_v4(dst + (v + 32 * u) * 8, q[u]);
+                }
+                for (; v < vecs; v += 32) st_v4(dst + v * 8, src ? ld_nc_v4(src + v * 8) : make_uint4(0, 0, 0, 0));
             } else {
                 uint8_t *dst = g.ringxq + drow * g.H;
-                for (int v = lane; v < vecs; v += 32) {
+                uint4 pre[4];   // the next four 16-byte loads are issued before the current ones are used
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int vv = lane + 32 * u;
+                    pre[u] = (src && vv < vecs) ? ld_nc_v4(src + vv * 8) : make_uint4(0, 0, 0, 0);
+                }
+                for (int v0 = lane; v0 < vecs; v0 += 128) {
+                  uint4 cur[4];
+#pragma unroll
+                  for (int u = 0; u < 4; ++u) {
+                      cur[u] = pre[u];
+                      const int vn = v0 + 128 + 32 * u;
+                      pre[u] = (src && vn < vecs) ? ld_nc_v4(src + vn * 8) : make_uint4(0, 0, 0, 0);
+                  }
+#pragma unroll
+                  for (int u = 0; u < 4; ++u) {
+                    const int v = v0 + 32 * u;
+                    if (v >= vecs) break;
                     float f[8];
                     if (src) {
-                        const uint4 q = ld_nc_v4(src + v * 8);
+                        const uint4 q = cur[u];
                         const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                         for (int i = 0; i < 4; ++i) { f[2 * i] = bf16lo(w4[i]); f[2 * i + 1] = bf16hi(w4[i]); }
@@ -199,6 +211,7 @@ __device__ void gather_loop(const GemmArgs &g) {
                     cq.y = cvt_e4m3x4(f[4] * inv, f[5] * inv, f[6] * inv, f[7] * inv);
                     *reinterpret_cast<uint2 *>(dst + v * 8) = cq;
                     if ((lane & 3) == 0) g.ringxs[mx_sf_offset(drow, (size_t)v * 8, g.H)] = (uint8_t)(sx + 127);
+                  }
                 }
             }
         }
@@ -236,7 +249,19 @@ __device__ void producer_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tile
                 }
             }
         }
+        // grouped-K ops walk expert e's runs in macrobatch order: (run, offset) advance with kb
+        int run_m = 0, run_off = 0;
         for (int kb = 0; kb < ti.nk; ++kb) {
+            int krow = 0;
+            if constexpr (OpTraits<OP>::grouped_k) {
+                for (;;) {
+                    const int s0 = g.offp[run_m * g.E + ti.e], s1 = g.offp[run_m * g.E + ti.e + 1];
+                    if (run_off < s1 - s0) { krow = s0 + run_off; break; }
+                    run_off = 0;
+                    ++run_m;
+                }
+                run_off += bk_elems<FP8>();
+            }
             if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, ctl)) { ok = false; break; }
             uint32_t bar = smem_u32(&full[stage]);
             uint32_t sA = smem_u32(tiles + stage * stage_stride<FP8>());
@@ -265,14 +290,14 @@ __device__ void producer_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tile
                     tma_load_2d(sA, second ? &g.a1 : &g.a0, bar, kk * BK, ti.g0 + a_shift);
                     tma_load_2d(sB, second ? &g.b1 : &g.b0, bar, kk * BK, ti.e * g.H + ti.nt * BN);
                 } else if constexpr (OP == OP_WG2) {
-                    int row = grouped_k_row(g, ti.e, kb, BK);
+                    const int row = krow;
                     int m0 = ti.mt * BM, n0 = ti.nt * BN;
                     tma_load_2d(sA, &g.a0, bar, m0, row);
                     tma_load_2d(sA + CHUNK_BYTES, &g.a0, bar, m0 + 64, row);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * CHUNK_BYTES, &g.b0, bar, n0 + 64 * j, row);
                 } else if constexpr (OP == OP_WG13) {
-                    int row = grouped_k_row(g, ti.e, kb, BK);
+                    const int row = krow;
                     int m0 = ti.mt * BM, n0 = ti.nt * 128;
                     tma_load_2d(sA, &g.a0, bar, m0, row);
                     tma_load_2d(sA + CHUNK_BYTES, &g.a0, bar, m0 + 64, row);
@@ -315,7 +340,7 @@ __device__ void producer_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tile
                     bulk_load(sSF + 1024, sfb + atom_at(br + 128, k0, KS), 512, bar);
                 } else if constexpr (OP == OP_WG2) {
                     // A = (w h)^T [F][rows], B = dY^T [H][rows], both quantised along rows
-                    const int row = grouped_k_row(g, ti.e, kb, BK8);
+                    const int row = krow;
                     const int m0 = ti.mt * BM, n0 = ti.nt * BN;
                     tma_load_2d(sA, &g.a0, bar, row, m0);
                     tma_load_2d(sB, &g.b0, bar, row, n0);
@@ -324,7 +349,7 @@ __device__ void producer_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tile
                     bulk_load(sSF + 1024, g.sfb0 + atom_at(n0 + 128, row, KS), 512, bar);
                 } else if constexpr (OP == OP_WG13) {
                     // A = X^T [H][rows], B = [da^T | db^T] [F][rows]
-                    const int row = grouped_k_row(g, ti.e, kb, BK8);
+                    const int row = krow;
                     const int m0 = ti.mt * BM, n0 = ti.nt * 128;
                     tma_load_2d(sA, &g.a0, bar, row, m0);
                     tma_load_2d(sB, &g.b0, bar, row, n0);

@@ -752,8 +752,18 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
     rw.x = (const bf16 *)x; rw.dlogits = dlogits; rw.part = at<float>(ws, L.w_dwr_part); rw.dWr = dW_r;
     rw.T = L.T; rw.H = L.H; rw.E = L.E; rw.splits = L.dwr_splits; rw.accumulate = accumulate;
     {
-        ProfScope ps("router_bwd", s);
-        st = cuda_check(launch_router_bwd(rb, rd, rw, s), "router backward launch");
+        ProfScope ps("router_bwd_dlogits", s);
+        st = cuda_check(launch_router_bwd_dlogits(rb, s), "router backward launch");
+    }
+    if (st != MOE_OK) return st;
+    {
+        ProfScope ps("reverse_dispatch", s);
+        st = cuda_check(launch_reverse_dispatch(rd, s), "reverse dispatch launch");
+    }
+    if (st != MOE_OK) return st;
+    {
+        ProfScope ps("router_wgrad", s);
+        st = cuda_check(launch_router_wgrad(rw, s), "router weight gradient launch");
     }
     if (st != MOE_OK) return st;
     // 4. weight gradients (contraction over each expert's rows, all macrobatches)

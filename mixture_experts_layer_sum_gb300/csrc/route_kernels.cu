@@ -713,15 +713,22 @@ __global__ void router_wgrad_reduce_kernel(RouterWgradArgs a) {
     a.dWr[i] = a.accumulate ? a.dWr[i] + v : v;
 }
 
-cudaError_t launch_router_bwd(const RouterBwdArgs &rb, const RevDispatchArgs &rd, const RouterWgradArgs &rw,
-                              cudaStream_t s) {
+cudaError_t launch_router_bwd_dlogits(const RouterBwdArgs &rb, cudaStream_t s) {
     if (rb.T > 0) router_bwd_kernel<<<ceil_div(rb.T, 8), 256, 0, s>>>(rb);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reverse_dispatch(const RevDispatchArgs &rd, cudaStream_t s) {
     if (rd.T > 0) {
         const int smem = 4 * kRdTokens * 68 * 4 + 4 * 64 * 72 * 2;
         cudaError_t e = cudaFuncSetAttribute(reverse_dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         reverse_dispatch_kernel<<<ceil_div(rd.T, kRdTokens), 128, smem, s>>>(rd);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_wgrad(const RouterWgradArgs &rw, cudaStream_t s) {
     dim3 grid(rw.H / 64, rw.splits);
     router_wgrad_part_kernel<<<grid, 32 * ceil_div(rw.E, 8), 0, s>>>(rw);
     router_wgrad_reduce_kernel<<<ceil_div(rw.H * rw.E, 256), 256, 0, s>>>(rw);

@@ -74,7 +74,8 @@ struct RouterWgradArgs {
     float *dWr;
     int T, H, E, splits, accumulate;
 };
-cudaError_t launch_router_bwd(const RouterBwdArgs &rb, const RevDispatchArgs &rd, const RouterWgradArgs &rw,
-                              cudaStream_t s);
+cudaError_t launch_router_bwd_dlogits(const RouterBwdArgs &rb, cudaStream_t s);
+cudaError_t launch_reverse_dispatch(const RevDispatchArgs &rd, cudaStream_t s);
+cudaError_t launch_router_wgrad(const RouterWgradArgs &rw, cudaStream_t s);
 
 }  // namespace moe
