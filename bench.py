@@ -458,11 +458,17 @@ def main():
     ap.add_argument("--workload", default=WL.BALANCED.name, choices=sorted(WL.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (small cases for ncu captures)")
+    ap.add_argument("--experts", type=int, default=0, help="override E, keeping k <= E (small cases for ncu captures)")
     ap.add_argument("--minibatch-sweep", action="store_true",
                     help="also time fwd and fwd+bwd for each minibatch size of the workload (ring workload)")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference" or args.steps < 3, "need >= 3 warm-up steps"
     w = WL.WORKLOADS[args.workload]
+    if args.tokens:
+        w = w.with_(T=args.tokens, name=f"{w.name}@T{args.tokens}")
+    if args.experts:
+        w = w.with_(E=args.experts, k=min(w.k, args.experts), name=f"{w.name}@E{args.experts}")
     if args.impl == "reference":
         run_reference(args, w)
     else:
