@@ -133,8 +133,8 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     L.half_rows = L.nM > 1 ? (int)align_up((size_t)half_rows, kRowPad) : L.rows_pad_max;
     L.chunks_per_mb = std::max(1, ceil_div(std::min(Mb, std::max(c->T, 1)) * c->k, kSchedChunk));
     L.nchunks = c->T > 0 ? L.nM * L.chunks_per_mb : 0;
-    // router-weight gradient: about two blocks per SM over (H/64) x splits
-    L.dwr_splits = std::max(1, std::min(ceil_div(2 * L.num_sms, c->H / 64), ceil_div(std::max(c->T, 1), 256)));
+    // router-weight gradient: about eight blocks per SM over (H/64) x splits
+    L.dwr_splits = std::max(1, std::min(ceil_div(8 * L.num_sms, c->H / 64), ceil_div(std::max(c->T, 1), 64)));
 
     const size_t R = L.R, T = L.T, E = L.E, H = L.H, F = L.F, nM = L.nM, rp = L.rows_pad_max;
     size_t o = 0;
@@ -645,7 +645,8 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
     const size_t rp = L.rows_pad_max;
 
     // 1. replay dispatch (X rows) and reverse combine (dout rows), all macrobatches
-    if (L.T > 0) {
+    //    (bf16 path; the MXFP8 path gathers straight into its quantised operands)
+    if (L.T > 0 && !mx) {
         DispatchArgs d1{};
         d1.src = (const bf16 *)x; d1.dst = Xs; d1.row_slot = s_row_slot; d1.offp = s_offp;
         d1.beg = 0; d1.end = L.nM * L.E; d1.dst_row0 = 0; d1.H = L.H; d1.k = L.k;
@@ -693,25 +694,32 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
         gw13.sfa0 = u8(L.w_XsT_s); gw13.sfb0 = u8(L.w_daT_s); gw13.sfb1 = u8(L.w_dbT_s); gw13.kstore = (int)rp;
     }
     // token-axis MXFP8 copies: bf16 [rows][C] -> [C][rows] quantised along rows
-    auto transpose_q = [&](const bf16 *src, size_t codes, size_t scales, int C, const char *name) {
+    auto transpose_q = [&](const bf16 *src, size_t codes, size_t scales, int C, const char *name,
+                           bool gather = false) {
         MxTransposeArgs a{};
         a.src = src; a.codes = at<uint8_t>(ws, codes); a.scales = at<uint8_t>(ws, scales);
         a.R = (int)rp; a.C = C; a.r_limit_ptr = s_offp + L.nM * L.E;
+        if (gather) { a.row_slot = s_row_slot; a.k = L.k; }
         ProfScope ps(name, s);
         return cuda_check(launch_mx_transpose(a, 1, s), "token-axis quantise launch");
     };
     if (mx && L.T > 0) {
         // dY rows along H for the GEMM2 dgrad; dY and X along the token axis for the weight gradients
+        // reverse combine fused with quantisation: dY rows gathered from dout as MXFP8 along H
         MxRowsArgs a{};
-        a.src = Gin; a.codes = at<uint8_t>(ws, L.w_Ginq); a.scales = at<uint8_t>(ws, L.w_Ginq_s);
-        a.offp = s_offp; a.beg = 0; a.end = L.nM * L.E; a.dst_row0 = 0; a.C = L.H; a.k = 1;
+        a.src = (const bf16 *)dout; a.codes = at<uint8_t>(ws, L.w_Ginq); a.scales = at<uint8_t>(ws, L.w_Ginq_s);
+        a.row_slot = s_row_slot; a.offp = s_offp; a.beg = 0; a.end = L.nM * L.E; a.dst_row0 = 0; a.C = L.H;
+        a.k = L.k;
         {
-            ProfScope ps("quantize_dy_rows", s);
+            ProfScope ps("reverse_combine_mxfp8", s);
             st = cuda_check(launch_mx_rows(a, L.rows_pad_max, L.num_sms, s), "dY quantise launch");
         }
         if (st != MOE_OK) return st;
-        if ((st = transpose_q(Gin, L.w_GinT, L.w_GinT_s, L.H, "quantize_dy_tokens")) != MOE_OK) return st;
-        if ((st = transpose_q(Xs, L.w_XsT, L.w_XsT_s, L.H, "quantize_x_tokens")) != MOE_OK) return st;
+        // token-axis copies gathered straight from dout and x (activation replay)
+        if ((st = transpose_q((const bf16 *)dout, L.w_GinT, L.w_GinT_s, L.H, "quantize_dy_tokens", true)) != MOE_OK)
+            return st;
+        if ((st = transpose_q((const bf16 *)x, L.w_XsT, L.w_XsT_s, L.H, "quantize_x_tokens", true)) != MOE_OK)
+            return st;
     }
     // 2. GEMM2 dgrad + SwiGLU backward, per macrobatch (global rows)
     gb2.N = L.F; gb2.K = L.H;

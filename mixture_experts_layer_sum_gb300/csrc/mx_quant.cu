@@ -82,7 +82,14 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(MxTransposeArgs a) {
     for (int i = threadIdx.x; i < 128 * 8; i += blockDim.x) {
         const int rr = i / 8, v = i % 8;
         uint4 q = make_uint4(0, 0, 0, 0);
-        if (rb0 + rr < r_limit) q = ld_nc_v4(src + (size_t)(rb0 + rr) * a.C + c0 + v * 8);
+        if (rb0 + rr < r_limit) {
+            if (a.row_slot) {
+                const int slot = a.row_slot[rb0 + rr];
+                if (slot >= 0) q = ld_nc_v4(src + (size_t)(slot / a.k) * a.C + c0 + v * 8);
+            } else {
+                q = ld_nc_v4(src + (size_t)(rb0 + rr) * a.C + c0 + v * 8);
+            }
+        }
         *reinterpret_cast<uint4 *>(&tile[rr][v * 8]) = q;
     }
     __syncthreads();

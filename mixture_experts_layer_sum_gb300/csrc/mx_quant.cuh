@@ -21,11 +21,16 @@ cudaError_t launch_mx_rows(const MxRowsArgs &a, int max_rows, int num_sms, cudaS
 // batch x bf16 [R][C] -> batch x E4M3 [C][R] + scale atoms (K = R).
 // R multiple of 128, C multiple of 64. Input rows >= *r_limit_ptr (if set) are
 // treated as zeros and their 128-row blocks skipped.
+// Gather mode (row_slot != null, batch 1): input row r is token row_slot[r] / k
+// of src (zeros when row_slot[r] < 0), so expert-sorted rows are quantised
+// along the token axis straight from the token-ordered tensor.
 struct MxTransposeArgs {
     const bf16 *src;
     uint8_t *codes, *scales;
     int R, C;
     const int32_t *r_limit_ptr;
+    const int32_t *row_slot;
+    int k;
 };
 cudaError_t launch_mx_transpose(const MxTransposeArgs &a, int batch, cudaStream_t s);
 

@@ -534,19 +534,19 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(RouterBwdArgs a) {
 // Reverse dispatch (article section 02: push reverse-dispatch, here a local
 // gather-sum):
 //   dx[t] = bf16( sum_j dXs[row(t,j)]  (fixed j order)  +  sum_e dlogits[t,e] W_r[h,e] ).
-// Block: 16 tokens, 4 warps; warp w covers H range [w H/4, (w+1) H/4) in
-// 64-wide chunks. The router term runs on mma.sync with dlogits split into
-// bf16 hi + lo parts (about 16 significant bits), the result goes through a
-// shared tile so each lane then owns 32 contiguous h of one token for the
-// 16-byte gathers of the k expert rows.
-constexpr int kRdTokens = 16;
+// Block: 64 tokens (4 warps x 16) x 256 h (four 64-wide chunks). Per chunk the
+// block stages W_r[h0..h0+63][0..E) once in shared memory; each warp computes
+// its 16 x 64 router term on mma.sync with dlogits split into bf16 hi + lo
+// parts (about 16 significant bits), parks it in a shared tile, and then each
+// lane owns 32 contiguous h of one token for the 16-byte gathers of the k rows.
+constexpr int kRdTokens = 64;
 __global__ void __launch_bounds__(128) reverse_dispatch_kernel(RevDispatchArgs a) {
-    extern __shared__ __align__(16) uint8_t rd_smem[];
-    auto s_acc = reinterpret_cast<float (*)[kRdTokens][64 + 4]>(rd_smem);                    // [4][16][68]
-    auto s_wr = reinterpret_cast<bf16 (*)[64][64 + 8]>(rd_smem + 4 * kRdTokens * 68 * 4);    // [4][64][72]
+    __shared__ float s_acc[4][16][64 + 4];
+    __shared__ __align__(16) bf16 s_wr[64][64 + 8];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int g = lane >> 2, c = lane & 3;
-    const int t0 = blockIdx.x * kRdTokens;
+    const int t0 = blockIdx.x * kRdTokens + warp * 16;
+    const int hb0 = blockIdx.y * 256;
     const int KS = (a.E + 15) / 16;   // k16 steps over experts (<= 4)
     // A fragments of dlogits (rows g, g+8; k-slots 2c, 2c+1, 2c+8, 2c+9)
     uint32_t Ahi[4][4], Alo[4][4];
@@ -571,24 +571,36 @@ __global__ void __launch_bounds__(128) reverse_dispatch_kernel(RevDispatchArgs a
         }
     const int my_t = t0 + (lane >> 1);
     const int half = lane & 1;
-    const int hspan = a.H / 4;
-    for (int h0 = warp * hspan; h0 < (warp + 1) * hspan; h0 += 64) {
+    int rows[32];
+    const int kk = a.k < 32 ? a.k : 32;
+    for (int j = 0; j < kk; ++j) rows[j] = my_t < a.T ? a.slot_row[(size_t)my_t * a.k + j] : 0;
+    for (int h0 = hb0; h0 < hb0 + 256; h0 += 64) {
+        // W_r rows h0..h0+63, E values each, zero padded to 64 experts
+        __syncthreads();
+        if ((a.E & 7) == 0) {
+            const int vrow = a.E / 8;   // 16-byte vectors per W_r row
+            for (int i = threadIdx.x; i < 64 * 8; i += blockDim.x) {
+                const int hh = i / 8, v = i % 8;
+                uint4 q = make_uint4(0, 0, 0, 0);
+                if (v < vrow) q = ld_nc_v4(a.Wr + (size_t)(h0 + hh) * a.E + v * 8);
+                *reinterpret_cast<uint4 *>(&s_wr[hh][v * 8]) = q;
+            }
+        } else {
+            for (int i = threadIdx.x; i < 64 * 64; i += blockDim.x) {
+                const int hh = i / 64, e = i % 64;
+                s_wr[hh][e] = e < a.E ? a.Wr[(size_t)(h0 + hh) * a.E + e] : f2bf(0.0f);
+            }
+        }
+        __syncthreads();
         float acc[8][4];
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
-        // W_r rows h0..h0+63 (E values each, zero padded to 64) -> this warp's tile
-        __syncwarp();
-        for (int i = lane; i < 64 * 64; i += 32) {
-            const int hh = i / 64, e = i % 64;
-            s_wr[warp][hh][e] = e < a.E ? a.Wr[(size_t)(h0 + hh) * a.E + e] : f2bf(0.0f);
-        }
-        __syncwarp();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
             if (ks < KS) {
 #pragma unroll
                 for (int nt = 0; nt < 8; ++nt) {
-                    const bf16 *wr = &s_wr[warp][nt * 8 + g][ks * 16 + 2 * c];
+                    const bf16 *wr = &s_wr[nt * 8 + g][ks * 16 + 2 * c];
                     const uint32_t b0 = *reinterpret_cast<const uint32_t *>(wr);
                     const uint32_t b1 = *reinterpret_cast<const uint32_t *>(wr + 8);
                     mma_16816_bf16(acc[nt], Ahi[ks], b0, b1);
@@ -615,7 +627,8 @@ __global__ void __launch_bounds__(128) reverse_dispatch_kernel(RevDispatchArgs a
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj)
                     if (jj < nj) {
-                        const int row = a.slot_row[(size_t)my_t * a.k + j0 + jj];
+                        const int j = j0 + jj;
+                        const int row = j < 32 ? rows[j] : a.slot_row[(size_t)my_t * a.k + j];
                         const bf16 *src = a.dXs + (size_t)row * a.H + hb;
 #pragma unroll
                         for (int u = 0; u < 4; ++u) q[jj][u] = ld_v4(src + u * 8);
@@ -649,11 +662,11 @@ __global__ void __launch_bounds__(128) reverse_dispatch_kernel(RevDispatchArgs a
 
 // dW_r partials: block = (64 h, split sp); lane owns h pair (h0 + 2 lane, +1),
 // warp w owns experts [8w, 8w+8); tokens of the split in increasing order.
-// Each 64-token chunk of x (64 x 64 bf16) and of dlogits is staged in shared
-// memory with independent 16-byte loads first.
+// Each 64-token chunk of x (64 x 64 bf16) and of dlogits (64 x E) is staged in
+// shared memory with independent vector loads first.
 constexpr int kWgTok = 64;
 __global__ void __launch_bounds__(256) router_wgrad_part_kernel(RouterWgradArgs a) {
-    __shared__ __align__(16) float s_dl[kWgTok][kMaxExperts];
+    __shared__ __align__(16) float s_dl[kWgTok * kMaxExperts + 8];
     __shared__ __align__(16) bf16 s_x[kWgTok][64];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int hb = blockIdx.x * 64;
@@ -673,9 +686,13 @@ __global__ void __launch_bounds__(256) router_wgrad_part_kernel(RouterWgradArgs 
             if (tt < cn) q = ld_nc_v4(a.x + (size_t)(c0 + tt) * a.H + hb + v * 8);
             *reinterpret_cast<uint4 *>(&s_x[tt][v * 8]) = q;
         }
-        for (int i = threadIdx.x; i < kWgTok * kMaxExperts; i += blockDim.x) {
-            const int tt = i / kMaxExperts, e = i % kMaxExperts;
-            s_dl[tt][e] = (tt < cn && e < a.E) ? a.dlogits[(size_t)(c0 + tt) * a.E + e] : 0.0f;
+        // dlogits rows of the chunk are contiguous: cn * E floats
+        const int n = cn * a.E;
+        if ((a.E & 3) == 0) {
+            const float4 *src = reinterpret_cast<const float4 *>(a.dlogits + (size_t)c0 * a.E);
+            for (int i = threadIdx.x; i < n / 4; i += blockDim.x) reinterpret_cast<float4 *>(s_dl)[i] = src[i];
+        } else {
+            for (int i = threadIdx.x; i < n; i += blockDim.x) s_dl[i] = a.dlogits[(size_t)c0 * a.E + i];
         }
         __syncthreads();
         if (e0 < a.E) {
@@ -683,13 +700,12 @@ __global__ void __launch_bounds__(256) router_wgrad_part_kernel(RouterWgradArgs 
             for (int tt = 0; tt < cn; ++tt) {
                 const uint32_t xv = *reinterpret_cast<const uint32_t *>(&s_x[tt][2 * lane]);
                 const float x0 = bf16lo(xv), x1 = bf16hi(xv);
-                const float4 d0 = *reinterpret_cast<const float4 *>(&s_dl[tt][e0]);
-                const float4 d1 = *reinterpret_cast<const float4 *>(&s_dl[tt][e0 + 4]);
-                const float d[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+                const float *dl = s_dl + tt * a.E + e0;   // experts past E read neighbours; never stored
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    acc[0][i] = fmaf(x0, d[i], acc[0][i]);
-                    acc[1][i] = fmaf(x1, d[i], acc[1][i]);
+                    const float d = dl[i];
+                    acc[0][i] = fmaf(x0, d, acc[0][i]);
+                    acc[1][i] = fmaf(x1, d, acc[1][i]);
                 }
             }
         }
@@ -720,10 +736,7 @@ cudaError_t launch_router_bwd_dlogits(const RouterBwdArgs &rb, cudaStream_t s) {
 
 cudaError_t launch_reverse_dispatch(const RevDispatchArgs &rd, cudaStream_t s) {
     if (rd.T > 0) {
-        const int smem = 4 * kRdTokens * 68 * 4 + 4 * 64 * 72 * 2;
-        cudaError_t e = cudaFuncSetAttribute(reverse_dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        reverse_dispatch_kernel<<<ceil_div(rd.T, kRdTokens), 128, smem, s>>>(rd);
+        reverse_dispatch_kernel<<<dim3(ceil_div(rd.T, kRdTokens), rd.H / 256), 128, 0, s>>>(rd);
     }
     return cudaGetLastError();
 }
