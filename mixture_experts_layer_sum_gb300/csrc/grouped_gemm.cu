@@ -103,24 +103,28 @@ struct TileInfo {
     int nk;      // number of BK blocks
 };
 
-struct SmemCtl {
-    uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+template <int NS>
+struct CtlT {
+    uint64_t full[NS], empty[NS], tfull[2], tempty[2], drain;
     uint32_t tmem_base;
     int nt;                       // tiles along N
     int mt_per_group;             // grouped-K: tiles along M (fixed)
     int prefix[kMaxExperts + 1];  // grouped-M: tile prefix over experts; grouped-K: unused
     int krows[kMaxExperts];       // grouped-K: padded rows of each expert (all macrobatches)
     int seg_start[kMaxExperts];   // grouped-M: first padded row of (m, e)
+    int seg_end[kMaxExperts];     // grouped-M: end of the padded run of (m, e)
 };
+using SmemCtl = CtlT<STAGES>;
 
-template <int OP>
-__device__ __forceinline__ int num_tiles(const SmemCtl &c, const GemmArgs &g) {
+// TM = rows of an M tile: 128 (one CTA) or 256 (a CTA pair, 128 rows each)
+template <int OP, class Ctl>
+__device__ __forceinline__ int num_tiles(const Ctl &c, const GemmArgs &g) {
     if constexpr (OpTraits<OP>::grouped_k) return g.E * c.mt_per_group * c.nt;
     else return c.prefix[g.E] * c.nt;
 }
 
-template <int OP, bool FP8>
-__device__ __forceinline__ TileInfo decode_tile(const SmemCtl &c, const GemmArgs &g, int t) {
+template <int OP, bool FP8, int TM = BM, class Ctl>
+__device__ __forceinline__ TileInfo decode_tile(const Ctl &c, const GemmArgs &g, int t) {
     TileInfo ti;
     ti.nt = t % c.nt;
     int q = t / c.nt;
@@ -134,10 +138,32 @@ __device__ __forceinline__ TileInfo decode_tile(const SmemCtl &c, const GemmArgs
         while (c.prefix[e + 1] <= q) ++e;   // E <= 64
         ti.e = e;
         ti.mt = q - c.prefix[e];
-        ti.g0 = c.seg_start[e] + ti.mt * BM;
+        ti.g0 = c.seg_start[e] + ti.mt * TM;
         ti.nk = g.K / bk_elems<FP8>();
     }
     return ti;
+}
+
+template <int OP, int TM, class Ctl>
+__device__ void init_tile_table(Ctl &c, const GemmArgs &g) {
+    if constexpr (OpTraits<OP>::grouped_k) {
+        c.nt = (OP == OP_WG13) ? g.N / 128 : g.N / BN;
+        c.mt_per_group = g.Mw / TM;
+        for (int e = 0; e < g.E; ++e) {
+            int rows = 0;
+            for (int mm = 0; mm < g.nM; ++mm) rows += g.offp[mm * g.E + e + 1] - g.offp[mm * g.E + e];
+            c.krows[e] = rows;
+        }
+    } else {
+        c.nt = (OP == OP_FWD1) ? g.N / 128 : g.N / BN;
+        c.prefix[0] = 0;
+        for (int e = 0; e < g.E; ++e) {
+            const int s0 = g.offp[g.m * g.E + e], s1 = g.offp[g.m * g.E + e + 1];
+            c.seg_start[e] = s0;
+            c.seg_end[e] = s1;
+            c.prefix[e + 1] = c.prefix[e] + (s1 - s0 + TM - 1) / TM;
+        }
+    }
 }
 
 // Fused dispatch (FWD1): the 4 gather warps of each CTA pull token rows of the
@@ -441,8 +467,11 @@ __device__ void mma_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tiles, ui
 __device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
 __device__ __forceinline__ float sigmoid_f(float a) { return 1.0f / (1.0f + __expf(-a)); }
 
-template <int OP, bool FP8>
-__device__ void epilogue_loop(const GemmArgs &g, const SmemCtl &c, uint64_t *tfull, uint64_t *tempty,
+// PAIR: the CTA pair computes a 256-row tile; this CTA's accumulator holds
+// rows [128 * rank, +128). A half beyond its expert's run (odd number of
+// 128-row tiles) is computed on whatever rows follow and not stored.
+template <int OP, bool FP8, bool PAIR = false, class Ctl>
+__device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *tfull, uint64_t *tempty,
                               uint32_t tmem, const WaitCtl &ctl) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int quarter = warp & 3;             // TMEM lanes this warp may read
@@ -452,12 +481,26 @@ __device__ void epilogue_loop(const GemmArgs &g, const SmemCtl &c, uint64_t *tfu
     uint32_t acc_phase = 0;
     const int total = num_tiles<OP>(c, g);
     const int ring_shift = g.ring_base - g.offp[g.m * g.E];
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        TileInfo ti = decode_tile<OP, FP8>(c, g, t);
+    const int rank = PAIR ? (int)cluster_ctarank() : 0;
+    const int t0 = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+    const int tstep = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
+    for (int t = t0; t < total; t += tstep) {
+        TileInfo ti = decode_tile<OP, FP8, PAIR ? 2 * BM : BM>(c, g, t);
+        bool phantom = false;
+        if constexpr (PAIR) {
+            if constexpr (OpTraits<OP>::grouped_k) {
+                ti.mt = ti.mt * 2 + rank;
+            } else {
+                ti.g0 += BM * rank;
+                phantom = ti.g0 >= c.seg_end[ti.e];
+            }
+        }
         if (!mbar_wait(smem_u32(&tfull[acc]), acc_phase, ctl)) break;
         tc_fence_after();
         const uint32_t tbase = tmem + lane_base + acc * BN;
-        if constexpr (OP == OP_FWD1) {
+        if (phantom) {
+            // nothing to store for rows past the expert's run
+        } else if constexpr (OP == OP_FWD1) {
             const int grow = ti.g0 + r;
             const size_t F = g.F;
             bf16 *pa = g.o0 + grow * F + ti.nt * 128;
@@ -625,7 +668,12 @@ __device__ void epilogue_loop(const GemmArgs &g, const SmemCtl &c, uint64_t *tfu
             }
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(&tempty[acc]));
+        if constexpr (PAIR) {
+            // the leader's MMA thread waits for both CTAs' epilogues
+            mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+        } else {
+            mbar_arrive(smem_u32(&tempty[acc]));
+        }
         if constexpr (FP8) {
             acc_phase ^= 1;
         } else {
@@ -644,23 +692,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
     WaitCtl ctl{g.status, g.budget_ns};
 
     if (threadIdx.x == 0) {
-        if constexpr (OpTraits<OP>::grouped_k) {
-            c.nt = (OP == OP_WG13) ? g.N / 128 : g.N / BN;
-            c.mt_per_group = g.Mw / BM;
-            for (int e = 0; e < g.E; ++e) {
-                int rows = 0;
-                for (int mm = 0; mm < g.nM; ++mm) rows += g.offp[mm * g.E + e + 1] - g.offp[mm * g.E + e];
-                c.krows[e] = rows;
-            }
-        } else {
-            c.nt = (OP == OP_FWD1) ? g.N / 128 : g.N / BN;
-            c.prefix[0] = 0;
-            for (int e = 0; e < g.E; ++e) {
-                int s0 = g.offp[g.m * g.E + e], s1 = g.offp[g.m * g.E + e + 1];
-                c.seg_start[e] = s0;
-                c.prefix[e + 1] = c.prefix[e] + (s1 - s0) / BM;
-            }
-        }
+        init_tile_table<OP, BM>(c, g);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&c.full[s]), 1);
             mbar_init(smem_u32(&c.empty[s]), 1);
@@ -700,6 +732,225 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// ======================================================================
+// CTA-pair (cta_group::2) variant, bf16: 256-row tiles, each CTA holds its
+// 128 rows of A and one 128-wide half of B (6 stages of 32 KB); the leader
+// CTA (rank 0) issues M=256 N=256 MMAs over both CTAs' shared memory, the
+// accumulator rows of each CTA land in its own TMEM. Full barriers live in
+// the leader (both producers arrive with their bytes); MMA commits arrive on
+// the empty / tmem-full barriers of both CTAs; both epilogues arrive on the
+// leader's tmem-empty barrier.
+constexpr int PSTAGES = 6;
+constexpr uint32_t P_A_BYTES = BM * BK * 2;            // 16 KiB
+constexpr uint32_t P_B_BYTES = 128 * BK * 2;           // 16 KiB: half of N = 256
+constexpr uint32_t P_STAGE = P_A_BYTES + P_B_BYTES;    // 32 KiB
+using PairCtl = CtlT<PSTAGES>;
+
+template <int OP>
+__device__ void pair_producer_loop(const GemmArgs &g, const PairCtl &c, uint8_t *tiles, const WaitCtl &ctl) {
+    const int rank = (int)cluster_ctarank();
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued[PSTAGES] = {0, 0, 0, 0, 0, 0};
+    uint32_t last_phase[PSTAGES] = {0, 0, 0, 0, 0, 0};
+    bool ok = true;
+    const int total = num_tiles<OP>(c, g);
+    const int a_shift = g.a_ring ? (g.ring_base - g.offp[g.m * g.E]) : 0;
+    int ready_mb = -1;
+    for (int t = blockIdx.x / 2; t < total && ok; t += gridDim.x / 2) {
+        TileInfo ti = decode_tile<OP, false, 2 * BM>(c, g, t);
+        const int row0 = ti.g0 + BM * rank;              // grouped-M: this CTA's 128 rows
+        const int m0 = (ti.mt * 2 + rank) * BM;          // grouped-K: this CTA's 128 rows of dW
+        if constexpr (OP == OP_FWD1) {
+            if (g.fused && row0 < c.seg_end[ti.e]) {
+                const int j = (row0 - g.offp[g.m * g.E]) / g.mb_rows;
+                if (j != ready_mb) {
+                    if (!flag_wait_geq(g.ready + j, (int)gridDim.x, ctl)) { ok = false; break; }
+                    fence_proxy_async_global();
+                    ready_mb = j;
+                }
+            }
+        }
+        int run_m = 0, run_off = 0;
+        for (int kb = 0; kb < ti.nk; ++kb) {
+            int krow = 0;
+            if constexpr (OpTraits<OP>::grouped_k) {
+                for (;;) {
+                    const int s0 = g.offp[run_m * g.E + ti.e], s1 = g.offp[run_m * g.E + ti.e + 1];
+                    if (run_off < s1 - s0) { krow = s0 + run_off; break; }
+                    run_off = 0;
+                    ++run_m;
+                }
+                run_off += BK;
+            }
+            if (!mbar_wait(smem_u32(&c.empty[stage]), phase ^ 1, ctl)) { ok = false; break; }
+            const uint32_t bar = mapa_shared(smem_u32(&c.full[stage]), 0);   // the leader's full barrier
+            const uint32_t sA = smem_u32(tiles + stage * P_STAGE);
+            const uint32_t sB = sA + P_A_BYTES;
+            mbar_arrive_expect_tx_cluster(bar, P_STAGE);
+            if constexpr (OP == OP_FWD1) {
+                const int br = ti.e * g.H + kb * BK, n0 = ti.nt * 128;
+                const CUtensorMap *bm = rank == 0 ? &g.b0 : &g.b1;   // W1 half, W3 half
+                tma_load_2d_pair(sA, &g.a0, bar, kb * BK, row0 + a_shift);
+                tma_load_2d_pair(sB, bm, bar, n0, br);
+                tma_load_2d_pair(sB + CHUNK_BYTES, bm, bar, n0 + 64, br);
+            } else if constexpr (OP == OP_FWD2) {
+                const int br = ti.e * g.F + kb * BK, n0 = ti.nt * BN + 128 * rank;
+                tma_load_2d_pair(sA, &g.a0, bar, kb * BK, row0 + a_shift);
+                tma_load_2d_pair(sB, &g.b0, bar, n0, br);
+                tma_load_2d_pair(sB + CHUNK_BYTES, &g.b0, bar, n0 + 64, br);
+            } else if constexpr (OP == OP_BWD2) {
+                tma_load_2d_pair(sA, &g.a0, bar, kb * BK, row0 + a_shift);
+                tma_load_2d_pair(sB, &g.b0, bar, kb * BK, ti.e * g.F + ti.nt * BN + 128 * rank);
+            } else if constexpr (OP == OP_BWD1) {
+                const int kf = g.F / BK;
+                const bool second = kb >= kf;
+                const int kk = second ? kb - kf : kb;
+                tma_load_2d_pair(sA, second ? &g.a1 : &g.a0, bar, kk * BK, row0 + a_shift);
+                tma_load_2d_pair(sB, second ? &g.b1 : &g.b0, bar, kk * BK, ti.e * g.H + ti.nt * BN + 128 * rank);
+            } else if constexpr (OP == OP_WG2) {
+                const int n0 = ti.nt * BN + 128 * rank;
+                tma_load_2d_pair(sA, &g.a0, bar, m0, krow);
+                tma_load_2d_pair(sA + CHUNK_BYTES, &g.a0, bar, m0 + 64, krow);
+                tma_load_2d_pair(sB, &g.b0, bar, n0, krow);
+                tma_load_2d_pair(sB + CHUNK_BYTES, &g.b0, bar, n0 + 64, krow);
+            } else if constexpr (OP == OP_WG13) {
+                const int n0 = ti.nt * 128;
+                const CUtensorMap *bm = rank == 0 ? &g.b0 : &g.b1;   // da half, db half
+                tma_load_2d_pair(sA, &g.a0, bar, m0, krow);
+                tma_load_2d_pair(sA + CHUNK_BYTES, &g.a0, bar, m0 + 64, krow);
+                tma_load_2d_pair(sB, bm, bar, n0, krow);
+                tma_load_2d_pair(sB + CHUNK_BYTES, bm, bar, n0 + 64, krow);
+            }
+            issued[stage] = 1;
+            last_phase[stage] = phase;
+            if (++stage == PSTAGES) { stage = 0; phase ^= 1; }
+        }
+    }
+    if (!ok && rank == 0) {
+        // the leader's full barriers count both CTAs' copies: wait (bounded) for the last phases
+        for (int s = 0; s < PSTAGES; ++s) {
+            if (!issued[s]) continue;
+            const uint32_t bar = smem_u32(&c.full[s]);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar, last_phase[s]) && globaltimer_ns() - t0 < ctl.budget_ns) {}
+        }
+    }
+}
+
+template <int OP>
+__device__ void pair_mma_loop(const GemmArgs &g, PairCtl &c, uint8_t *tiles, uint32_t tmem, const WaitCtl &ctl) {
+    constexpr bool AMN = OpTraits<OP>::a_mn, BMN = OpTraits<OP>::b_mn;
+    constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN, AMN, BMN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const int total = num_tiles<OP>(c, g);
+    for (int t = blockIdx.x / 2; t < total; t += gridDim.x / 2) {
+        TileInfo ti = decode_tile<OP, false, 2 * BM>(c, g, t);
+        if (!mbar_wait(smem_u32(&c.tempty[acc]), acc_phase ^ 1, ctl)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < ti.nk; ++kb) {
+            if (!mbar_wait(smem_u32(&c.full[stage]), phase, ctl)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sA = smem_u32(tiles + stage * P_STAGE);
+            const uint32_t sB = sA + P_A_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+                const uint64_t ad = AMN ? sdesc_sw128(sA + kk * 2048, 8192, 1024) : sdesc_sw128(sA + kk * 32, 16, 1024);
+                const uint64_t bd = BMN ? sdesc_sw128(sB + kk * 2048, 8192, 1024) : sdesc_sw128(sB + kk * 32, 16, 1024);
+                mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0);
+            }
+            mma_commit_pair_mc(smem_u32(&c.empty[stage]));   // frees the stage in both CTAs
+            if (++stage == PSTAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit_pair_mc(smem_u32(&c.tfull[acc]));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+    }
+    mma_commit_pair(smem_u32(&c.drain));
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(smem_u32(&c.drain), 0) && globaltimer_ns() - t0 < ctl.budget_ns) {}
+}
+
+template <int OP>
+__global__ void __launch_bounds__(320, 1) pair_gemm_kernel(const __grid_constant__ GemmArgs g) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    PairCtl &c = *reinterpret_cast<PairCtl *>(tiles + PSTAGES * P_STAGE);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    WaitCtl ctl{g.status, g.budget_ns};
+    if (threadIdx.x == 0) {
+        init_tile_table<OP, 2 * BM>(c, g);
+        for (int s = 0; s < PSTAGES; ++s) {
+            mbar_init(smem_u32(&c.full[s]), 2);      // one arrive.expect_tx per CTA of the pair
+            mbar_init(smem_u32(&c.empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&c.tfull[a]), 1);
+            mbar_init(smem_u32(&c.tempty[a]), 256);  // 128 epilogue threads of each CTA
+        }
+        mbar_init(smem_u32(&c.drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&g.a0);
+        tma_prefetch_map(&g.b0);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(&c.tmem_base), 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();      // the peer's barriers are initialised before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem = c.tmem_base;
+    if (warp == 0) {
+        if (lane == 0) pair_producer_loop<OP>(g, c, tiles, ctl);
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) pair_mma_loop<OP>(g, c, tiles, tmem, ctl);
+    } else if (warp < 6) {
+        epilogue_loop<OP, false, true>(g, c, c.tfull, c.tempty, tmem, ctl);
+    } else {
+        if constexpr (OP == OP_FWD1) gather_loop<false>(g);
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();      // the leader's MMAs are drained before the pair frees TMEM
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem, 512);
+}
+
+template <int OP>
+cudaError_t launch_pair(const GemmArgs &g, int grid, cudaStream_t stream) {
+    constexpr size_t smem = PSTAGES * P_STAGE + sizeof(PairCtl) + 1024;
+    static_assert(smem <= 227 * 1024, "shared memory budget");
+    cudaError_t err = cudaFuncSetAttribute(pair_gemm_kernel<OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    const bool fused = OP == OP_FWD1 && g.fused;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid / 2 * 2);
+    cfg.blockDim = dim3(fused ? 320 : 192);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;   // gather warps publish flags other CTAs wait on
+    attr[1].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = fused ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<OP>, g);
+}
+
 template <int OP, bool FP8>
 cudaError_t launch_op(const GemmArgs &g, int grid, cudaStream_t stream) {
     constexpr size_t smem = STAGES * stage_stride<FP8>() + sizeof(SmemCtl) + 1024;
@@ -732,7 +983,18 @@ cudaError_t launch_any(int op, const GemmArgs &g, int grid, cudaStream_t stream)
 
 }  // namespace
 
-cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream, bool fp8) {
+cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream, bool fp8, bool pair) {
+    if (pair && !fp8) {
+        switch (op) {
+            case OP_FWD1: return launch_pair<OP_FWD1>(g, grid, stream);
+            case OP_FWD2: return launch_pair<OP_FWD2>(g, grid, stream);
+            case OP_BWD2: return launch_pair<OP_BWD2>(g, grid, stream);
+            case OP_BWD1: return launch_pair<OP_BWD1>(g, grid, stream);
+            case OP_WG2: return launch_pair<OP_WG2>(g, grid, stream);
+            case OP_WG13: return launch_pair<OP_WG13>(g, grid, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     return fp8 ? launch_any<true>(op, g, grid, stream) : launch_any<false>(op, g, grid, stream);
 }
 

@@ -45,6 +45,9 @@ struct GemmArgs {
     unsigned long long budget_ns;
 };
 
-cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream, bool fp8 = false);
+// pair = true (bf16 only): CTA-pair variant with 256-row tiles (cta_group::2);
+// the B maps of the K-major ops then need 128-row boxes.
+cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream, bool fp8 = false,
+                                bool pair = false);
 
 }  // namespace moe

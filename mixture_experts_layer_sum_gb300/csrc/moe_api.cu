@@ -55,6 +55,8 @@ struct ProfScope {
     }
 };
 
+// bf16 grouped GEMMs run as CTA pairs (cta_group::2, 256-row tiles)
+constexpr bool kPairGemm = true;
 constexpr int kGemmBN1 = 256;   // GEMM1 tile: 128 rows x (128 a-columns + 128 b-columns)
 constexpr int kGemmBM = 128;
 
@@ -588,13 +590,13 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
         g1.m = m; g1.ring_base = ring_base;
         {
             ProfScope ps("grouped_gemm_fwd1_swiglu", s);
-            st = cuda_check(launch_grouped_gemm(OP_FWD1, g1, L.num_sms, s, mx), "GEMM1 launch");
+            st = cuda_check(launch_grouped_gemm(OP_FWD1, g1, L.num_sms, s, mx, kPairGemm && !mx), "GEMM1 launch");
         }
         if (st != MOE_OK) return st;
         g2.m = m; g2.ring_base = ring_base;
         {
             ProfScope ps("grouped_gemm_fwd2", s);
-            st = cuda_check(launch_grouped_gemm(OP_FWD2, g2, L.num_sms, s, mx), "GEMM2 launch");
+            st = cuda_check(launch_grouped_gemm(OP_FWD2, g2, L.num_sms, s, mx, kPairGemm && !mx), "GEMM2 launch");
         }
         if (st != MOE_OK) return st;
         CombineArgs ca{};
@@ -667,9 +669,10 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
     GemmArgs gw2 = gemm_base(L, ws, s_offp, cfg), gw13 = gemm_base(L, ws, s_offp, cfg);
     const size_t EF = (size_t)L.E * L.F, EH = (size_t)L.E * L.H;
     if (!mx) {
-        if (!make_map(&gb2.a0, Gin, rp, L.H, 128) || !make_map(&gb2.b0, W2, EF, L.H, 256) ||
+        const int kb_rows = kPairGemm ? 128 : 256;   // K-major B box: half of N per CTA of a pair
+        if (!make_map(&gb2.a0, Gin, rp, L.H, 128) || !make_map(&gb2.b0, W2, EF, L.H, kb_rows) ||
             !make_map(&gb1.a0, dA, rp, L.F, 128) || !make_map(&gb1.a1, dB, rp, L.F, 128) ||
-            !make_map(&gb1.b0, W1, EH, L.F, 256) || !make_map(&gb1.b1, W3, EH, L.F, 256) ||
+            !make_map(&gb1.b0, W1, EH, L.F, kb_rows) || !make_map(&gb1.b1, W3, EH, L.F, kb_rows) ||
             !make_map(&gw2.a0, HW, rp, L.F, 64) || !make_map(&gw2.b0, Gin, rp, L.H, 64) ||
             !make_map(&gw13.a0, Xs, rp, L.H, 64) || !make_map(&gw13.b0, dA, rp, L.F, 64) ||
             !make_map(&gw13.b1, dB, rp, L.F, 64))
@@ -731,7 +734,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
             gb2.m = m;
             {
                 ProfScope ps("grouped_gemm_bwd2_swiglu", s);
-                st = cuda_check(launch_grouped_gemm(OP_BWD2, gb2, L.num_sms, s, mx), "GEMM2 dgrad launch");
+                st = cuda_check(launch_grouped_gemm(OP_BWD2, gb2, L.num_sms, s, mx, kPairGemm && !mx), "GEMM2 dgrad launch");
             }
             if (st != MOE_OK) return st;
         }
@@ -744,7 +747,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
             gb1.m = m;
             {
                 ProfScope ps("grouped_gemm_bwd1", s);
-                st = cuda_check(launch_grouped_gemm(OP_BWD1, gb1, L.num_sms, s, mx), "GEMM1 dgrad launch");
+                st = cuda_check(launch_grouped_gemm(OP_BWD1, gb1, L.num_sms, s, mx, kPairGemm && !mx), "GEMM1 dgrad launch");
             }
             if (st != MOE_OK) return st;
         }
@@ -778,13 +781,13 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
     gw2.Mw = L.F; gw2.N = L.H; gw2.of0 = dW2; gw2.accumulate = accumulate;
     {
         ProfScope ps("grouped_gemm_wgrad2", s);
-        st = cuda_check(launch_grouped_gemm(OP_WG2, gw2, L.num_sms, s, mx), "dW2 launch");
+        st = cuda_check(launch_grouped_gemm(OP_WG2, gw2, L.num_sms, s, mx, kPairGemm && !mx), "dW2 launch");
     }
     if (st != MOE_OK) return st;
     gw13.Mw = L.H; gw13.N = L.F; gw13.of0 = dW1; gw13.of1 = dW3; gw13.accumulate = accumulate;
     {
         ProfScope ps("grouped_gemm_wgrad13", s);
-        st = cuda_check(launch_grouped_gemm(OP_WG13, gw13, L.num_sms, s, mx), "dW1/dW3 launch");
+        st = cuda_check(launch_grouped_gemm(OP_WG13, gw13, L.num_sms, s, mx, kPairGemm && !mx), "dW1/dW3 launch");
     }
     return st;
 }
