@@ -33,6 +33,8 @@
 // Every mbarrier wait is bounded; when a wait gives up the status word is set
 // and all roles leave their loops, drain their in-flight copies/MMAs and free
 // TMEM before exiting.
+#include <algorithm>
+
 #include "grouped_gemm.cuh"
 
 namespace moe {
@@ -935,7 +937,6 @@ cudaError_t launch_pair(const GemmArgs &g, int grid, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     const bool fused = OP == OP_FWD1 && g.fused;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(grid / 2 * 2);
     cfg.blockDim = dim3(fused ? 320 : 192);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -947,6 +948,19 @@ cudaError_t launch_pair(const GemmArgs &g, int grid, cudaStream_t stream) {
     attr[1].id = cudaLaunchAttributeCooperative;   // gather warps publish flags other CTAs wait on
     attr[1].val.cooperative = 1;
     cfg.attrs = attr;
+    // A persistent grid must be fully co-resident: with GPCs of an odd SM count
+    // not every SM can host half of a pair, so size the grid by the number of
+    // clusters that fit at once (queried once per kernel and block size).
+    static int max_clusters[2] = {0, 0};
+    int &mc = max_clusters[fused ? 1 : 0];
+    if (mc == 0) {
+        cfg.gridDim = dim3(grid / 2 * 2);
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel<OP>, &cfg) != cudaSuccess || n <= 0) n = grid / 2;
+        mc = n;
+    }
+    cfg.gridDim = dim3(2 * std::min(grid / 2, mc));
     cfg.numAttrs = fused ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<OP>, g);
 }
