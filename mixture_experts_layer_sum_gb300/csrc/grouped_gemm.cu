@@ -299,15 +299,13 @@ __device__ void producer_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tile
                 if constexpr (OP == OP_FWD1) {
                     int ar = ti.g0 + a_shift, br = ti.e * g.H + kb * BK, n0 = ti.nt * 128;
                     tma_load_2d(sA, &g.a0, bar, kb * BK, ar);
-                    tma_load_2d(sB, &g.b0, bar, n0, br);
-                    tma_load_2d(sB + CHUNK_BYTES, &g.b0, bar, n0 + 64, br);
-                    tma_load_2d(sB + 2 * CHUNK_BYTES, &g.b1, bar, n0, br);
-                    tma_load_2d(sB + 3 * CHUNK_BYTES, &g.b1, bar, n0 + 64, br);
+                    tma_load_3d(sB, &g.b0, bar, 0, br, n0 / 64);                  // 2 chunks of W1
+                    tma_load_3d(sB + 2 * CHUNK_BYTES, &g.b1, bar, 0, br, n0 / 64);   // 2 chunks of W3
                 } else if constexpr (OP == OP_FWD2) {
                     int ar = ti.g0 + a_shift, br = ti.e * g.F + kb * BK, n0 = ti.nt * BN;
                     tma_load_2d(sA, &g.a0, bar, kb * BK, ar);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * CHUNK_BYTES, &g.b0, bar, n0 + 64 * j, br);
+                    tma_load_3d(sB, &g.b0, bar, 0, br, n0 / 64);                  // 4 chunks
                 } else if constexpr (OP == OP_BWD2) {
                     tma_load_2d(sA, &g.a0, bar, kb * BK, ti.g0 + a_shift);
                     tma_load_2d(sB, &g.b0, bar, kb * BK, ti.e * g.F + ti.nt * BN);
@@ -320,19 +318,14 @@ __device__ void producer_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tile
                 } else if constexpr (OP == OP_WG2) {
                     const int row = krow;
                     int m0 = ti.mt * BM, n0 = ti.nt * BN;
-                    tma_load_2d(sA, &g.a0, bar, m0, row);
-                    tma_load_2d(sA + CHUNK_BYTES, &g.a0, bar, m0 + 64, row);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * CHUNK_BYTES, &g.b0, bar, n0 + 64 * j, row);
+                    tma_load_3d(sA, &g.a0, bar, 0, row, m0 / 64);                 // 2 chunks
+                    tma_load_3d(sB, &g.b0, bar, 0, row, n0 / 64);                 // 4 chunks
                 } else if constexpr (OP == OP_WG13) {
                     const int row = krow;
                     int m0 = ti.mt * BM, n0 = ti.nt * 128;
-                    tma_load_2d(sA, &g.a0, bar, m0, row);
-                    tma_load_2d(sA + CHUNK_BYTES, &g.a0, bar, m0 + 64, row);
-                    tma_load_2d(sB, &g.b0, bar, n0, row);
-                    tma_load_2d(sB + CHUNK_BYTES, &g.b0, bar, n0 + 64, row);
-                    tma_load_2d(sB + 2 * CHUNK_BYTES, &g.b1, bar, n0, row);
-                    tma_load_2d(sB + 3 * CHUNK_BYTES, &g.b1, bar, n0 + 64, row);
+                    tma_load_3d(sA, &g.a0, bar, 0, row, m0 / 64);                 // 2 chunks
+                    tma_load_3d(sB, &g.b0, bar, 0, row, n0 / 64);                 // 2 chunks of da
+                    tma_load_3d(sB + 2 * CHUNK_BYTES, &g.b1, bar, 0, row, n0 / 64);   // 2 chunks of db
                 }
             } else {
                 // e4m3 tiles (all K-major, 128 B of K per row) + three scale atoms
@@ -794,13 +787,11 @@ __device__ void pair_producer_loop(const GemmArgs &g, const PairCtl &c, uint8_t 
                 const int br = ti.e * g.H + kb * BK, n0 = ti.nt * 128;
                 const CUtensorMap *bm = rank == 0 ? &g.b0 : &g.b1;   // W1 half, W3 half
                 tma_load_2d_pair(sA, &g.a0, bar, kb * BK, row0 + a_shift);
-                tma_load_2d_pair(sB, bm, bar, n0, br);
-                tma_load_2d_pair(sB + CHUNK_BYTES, bm, bar, n0 + 64, br);
+                tma_load_3d_pair(sB, bm, bar, 0, br, n0 / 64);
             } else if constexpr (OP == OP_FWD2) {
                 const int br = ti.e * g.F + kb * BK, n0 = ti.nt * BN + 128 * rank;
                 tma_load_2d_pair(sA, &g.a0, bar, kb * BK, row0 + a_shift);
-                tma_load_2d_pair(sB, &g.b0, bar, n0, br);
-                tma_load_2d_pair(sB + CHUNK_BYTES, &g.b0, bar, n0 + 64, br);
+                tma_load_3d_pair(sB, &g.b0, bar, 0, br, n0 / 64);
             } else if constexpr (OP == OP_BWD2) {
                 tma_load_2d_pair(sA, &g.a0, bar, kb * BK, row0 + a_shift);
                 tma_load_2d_pair(sB, &g.b0, bar, kb * BK, ti.e * g.F + ti.nt * BN + 128 * rank);
@@ -812,17 +803,13 @@ __device__ void pair_producer_loop(const GemmArgs &g, const PairCtl &c, uint8_t 
                 tma_load_2d_pair(sB, second ? &g.b1 : &g.b0, bar, kk * BK, ti.e * g.H + ti.nt * BN + 128 * rank);
             } else if constexpr (OP == OP_WG2) {
                 const int n0 = ti.nt * BN + 128 * rank;
-                tma_load_2d_pair(sA, &g.a0, bar, m0, krow);
-                tma_load_2d_pair(sA + CHUNK_BYTES, &g.a0, bar, m0 + 64, krow);
-                tma_load_2d_pair(sB, &g.b0, bar, n0, krow);
-                tma_load_2d_pair(sB + CHUNK_BYTES, &g.b0, bar, n0 + 64, krow);
+                tma_load_3d_pair(sA, &g.a0, bar, 0, krow, m0 / 64);
+                tma_load_3d_pair(sB, &g.b0, bar, 0, krow, n0 / 64);
             } else if constexpr (OP == OP_WG13) {
                 const int n0 = ti.nt * 128;
                 const CUtensorMap *bm = rank == 0 ? &g.b0 : &g.b1;   // da half, db half
-                tma_load_2d_pair(sA, &g.a0, bar, m0, krow);
-                tma_load_2d_pair(sA + CHUNK_BYTES, &g.a0, bar, m0 + 64, krow);
-                tma_load_2d_pair(sB, bm, bar, n0, krow);
-                tma_load_2d_pair(sB + CHUNK_BYTES, bm, bar, n0 + 64, krow);
+                tma_load_3d_pair(sA, &g.a0, bar, 0, krow, m0 / 64);
+                tma_load_3d_pair(sB, bm, bar, 0, krow, n0 / 64);
             }
             issued[stage] = 1;
             last_phase[stage] = phase;
@@ -998,7 +985,7 @@ cudaError_t launch_any(int op, const GemmArgs &g, int grid, cudaStream_t stream)
 }  // namespace
 
 cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream, bool fp8, bool pair) {
-    if (pair && !fp8) {
+    if (pair && !fp8 && op != OP_BWD2) {   // BWD2: heavy epilogue, phantom halves; 1-CTA tiles
         switch (op) {
             case OP_FWD1: return launch_pair<OP_FWD1>(g, grid, stream);
             case OP_FWD2: return launch_pair<OP_FWD2>(g, grid, stream);

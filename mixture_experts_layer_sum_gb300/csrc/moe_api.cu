@@ -252,6 +252,23 @@ bool make_map_u8(CUtensorMap *m, const void *base, size_t rows, size_t cols, int
     return r == CUDA_SUCCESS;
 }
 
+// 3-D map of an MN-major bf16 operand stored row-major [rows (K), cols (M or N)]:
+// dims (64 columns, rows, cols / 64 chunks) with the chunk stride 128 B, box
+// (64, box_rows, chunks): one load lands `chunks` 64-column slabs of box_rows
+// rows one after another, the layout the MN-major UMMA descriptor expects.
+bool make_map_mn(CUtensorMap *m, const void *base, size_t rows, size_t cols, int box_rows, int chunks) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || rows == 0) return false;
+    cuuint64_t dims[3] = {64, rows, cols / 64};
+    cuuint64_t strides[2] = {cols * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)chunks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // MXFP8 weight copies made by moe_quantize_weights, each K-major for one GEMM:
 //   w1t, w3t: W1^T, W3^T [E][F][H] along H (GEMM1)     w2t: W2^T [E][H][F] along F (GEMM2)
 //   w2q:      W2 [E][F][H] along H (GEMM2 dgrad)       w1q, w3q: W1, W3 [E][H][F] along F (GEMM1 dgrad)
@@ -555,9 +572,10 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
     const size_t ring_rows = (size_t)L.half_rows * L.ring_halves;
     GemmArgs g1 = gemm_base(L, ws, s_offp, cfg), g2 = gemm_base(L, ws, s_offp, cfg);
     if (!mx) {
-        if (!make_map(&g1.a0, ringX, ring_rows, L.H, 128) || !make_map(&g1.b0, W1, (size_t)L.E * L.H, L.F, 64) ||
-            !make_map(&g1.b1, W3, (size_t)L.E * L.H, L.F, 64) || !make_map(&g2.a0, ringH, ring_rows, L.F, 128) ||
-            !make_map(&g2.b0, W2, (size_t)L.E * L.F, L.H, 64))
+        const int nb2 = kPairGemm ? 2 : 4;   // 64-column chunks of GEMM2's B per CTA
+        if (!make_map(&g1.a0, ringX, ring_rows, L.H, 128) || !make_map_mn(&g1.b0, W1, (size_t)L.E * L.H, L.F, 64, 2) ||
+            !make_map_mn(&g1.b1, W3, (size_t)L.E * L.H, L.F, 64, 2) || !make_map(&g2.a0, ringH, ring_rows, L.F, 128) ||
+            !make_map_mn(&g2.b0, W2, (size_t)L.E * L.F, L.H, 64, nb2))
             return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         g1.o2 = ringH;
     } else {
@@ -670,12 +688,13 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
     const size_t EF = (size_t)L.E * L.F, EH = (size_t)L.E * L.H;
     if (!mx) {
         const int kb_rows = kPairGemm ? 128 : 256;   // K-major B box: half of N per CTA of a pair
-        if (!make_map(&gb2.a0, Gin, rp, L.H, 128) || !make_map(&gb2.b0, W2, EF, L.H, kb_rows) ||
+        const int nbw = kPairGemm ? 2 : 4;           // 64-column chunks of dW2's B per CTA
+        if (!make_map(&gb2.a0, Gin, rp, L.H, 128) || !make_map(&gb2.b0, W2, EF, L.H, 256) ||
             !make_map(&gb1.a0, dA, rp, L.F, 128) || !make_map(&gb1.a1, dB, rp, L.F, 128) ||
             !make_map(&gb1.b0, W1, EH, L.F, kb_rows) || !make_map(&gb1.b1, W3, EH, L.F, kb_rows) ||
-            !make_map(&gw2.a0, HW, rp, L.F, 64) || !make_map(&gw2.b0, Gin, rp, L.H, 64) ||
-            !make_map(&gw13.a0, Xs, rp, L.H, 64) || !make_map(&gw13.b0, dA, rp, L.F, 64) ||
-            !make_map(&gw13.b1, dB, rp, L.F, 64))
+            !make_map_mn(&gw2.a0, HW, rp, L.F, 64, 2) || !make_map_mn(&gw2.b0, Gin, rp, L.H, 64, nbw) ||
+            !make_map_mn(&gw13.a0, Xs, rp, L.H, 64, 2) || !make_map_mn(&gw13.b0, dA, rp, L.F, 64, 2) ||
+            !make_map_mn(&gw13.b1, dB, rp, L.F, 64, 2))
             return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     } else {
         const QwLayout q = qw_layout(cfg);
