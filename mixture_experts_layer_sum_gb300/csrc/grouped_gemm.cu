@@ -467,7 +467,7 @@ __device__ __forceinline__ float sigmoid_f(float a) { return 1.0f / (1.0f + __ex
 // 128-row tiles) is computed on whatever rows follow and not stored.
 template <int OP, bool FP8, bool PAIR = false, class Ctl>
 __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *tfull, uint64_t *tempty,
-                              uint32_t tmem, const WaitCtl &ctl) {
+                              uint32_t tmem, const WaitCtl &ctl, uint8_t *staging = nullptr) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int quarter = warp & 3;             // TMEM lanes this warp may read
     const int r = quarter * 32 + lane;        // accumulator row of this thread
@@ -477,6 +477,7 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
     const int total = num_tiles<OP>(c, g);
     const int ring_shift = g.ring_base - g.offp[g.m * g.E];
     const int rank = PAIR ? (int)cluster_ctarank() : 0;
+    int store_chunks = 0;   // TMA stores issued by this warp (lane 0 tracks the bulk groups)
     const int t0 = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
     const int tstep = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
     for (int t = t0; t < total; t += tstep) {
@@ -648,6 +649,30 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = 0u;
                 }
+                if (staging != nullptr && g.tma_store && !g.accumulate) {
+                    // 32 rows x 32 fp32 of this warp -> 128B-swizzled staging buffer -> one TMA store.
+                    // Two buffers per warp: wait until the store issued two chunks ago has read its source.
+                    uint8_t *buf = staging + ((warp - 2) * 2 + (store_chunks & 1)) * 4096;
+                    if (store_chunks >= 2) {
+                        if (lane == 0) bulk_wait_group_read<1>();
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<uint4 *>(buf + lane * 128 + ((q ^ (lane & 7)) * 16)) =
+                            make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int row0 = (OP == OP_WG2 ? ti.e * g.F : ti.e * g.H) + ti.mt * BM + quarter * 32;
+                        const CUtensorMap *om = (cc * 32 < ncol0) ? &g.om0 : &g.om1;
+                        const int col0 = (OP == OP_WG2 ? ti.nt * BN : ti.nt * 128) + (cc * 32 < ncol0 ? cc * 32 : cc * 32 - ncol0);
+                        tma_store_2d(om, smem_u32(buf), col0, row0);
+                        bulk_commit_group();
+                    }
+                    ++store_chunks;
+                    continue;
+                }
                 float *dst = (cc * 32 < ncol0) ? dst0 + cc * 32 : dst1 + (cc * 32 - ncol0);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
@@ -676,6 +701,7 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
             if (acc == 0) acc_phase ^= 1;
         }
     }
+    if (store_chunks > 0 && lane == 0) bulk_wait_group_all();
 }
 
 template <int OP, bool FP8>
@@ -739,6 +765,7 @@ constexpr int PSTAGES = 6;
 constexpr uint32_t P_A_BYTES = BM * BK * 2;            // 16 KiB
 constexpr uint32_t P_B_BYTES = 128 * BK * 2;           // 16 KiB: half of N = 256
 constexpr uint32_t P_STAGE = P_A_BYTES + P_B_BYTES;    // 32 KiB
+constexpr uint32_t P_STAGING = 4 * 2 * 4096;          // epilogue staging for TMA stores
 using PairCtl = CtlT<PSTAGES>;
 
 template <int OP>
@@ -870,7 +897,8 @@ template <int OP>
 __global__ void __launch_bounds__(320, 1) pair_gemm_kernel(const __grid_constant__ GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    PairCtl &c = *reinterpret_cast<PairCtl *>(tiles + PSTAGES * P_STAGE);
+    uint8_t *staging = tiles + PSTAGES * P_STAGE;                       // 4 epilogue warps x 2 x 4 KB
+    PairCtl &c = *reinterpret_cast<PairCtl *>(staging + P_STAGING);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = cluster_ctarank();
     WaitCtl ctl{g.status, g.budget_ns};
@@ -905,7 +933,7 @@ __global__ void __launch_bounds__(320, 1) pair_gemm_kernel(const __grid_constant
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) pair_mma_loop<OP>(g, c, tiles, tmem, ctl);
     } else if (warp < 6) {
-        epilogue_loop<OP, false, true>(g, c, c.tfull, c.tempty, tmem, ctl);
+        epilogue_loop<OP, false, true>(g, c, c.tfull, c.tempty, tmem, ctl, staging);
     } else {
         if constexpr (OP == OP_FWD1) gather_loop<false>(g);
     }
@@ -918,7 +946,7 @@ __global__ void __launch_bounds__(320, 1) pair_gemm_kernel(const __grid_constant
 
 template <int OP>
 cudaError_t launch_pair(const GemmArgs &g, int grid, cudaStream_t stream) {
-    constexpr size_t smem = PSTAGES * P_STAGE + sizeof(PairCtl) + 1024;
+    constexpr size_t smem = PSTAGES * P_STAGE + P_STAGING + sizeof(PairCtl) + 1024;
     static_assert(smem <= 227 * 1024, "shared memory budget");
     cudaError_t err = cudaFuncSetAttribute(pair_gemm_kernel<OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;

@@ -269,6 +269,19 @@ bool make_map_mn(CUtensorMap *m, const void *base, size_t rows, size_t cols, int
     return r == CUDA_SUCCESS;
 }
 
+// fp32 [rows, cols] output map for TMA stores of 32 x 32 boxes (128-byte swizzle)
+bool make_map_f32_out(CUtensorMap *m, void *base, size_t rows, size_t cols) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || rows == 0) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // MXFP8 weight copies made by moe_quantize_weights, each K-major for one GEMM:
 //   w1t, w3t: W1^T, W3^T [E][F][H] along H (GEMM1)     w2t: W2^T [E][H][F] along F (GEMM2)
 //   w2q:      W2 [E][F][H] along H (GEMM2 dgrad)       w1q, w3q: W1, W3 [E][H][F] along F (GEMM1 dgrad)
@@ -798,6 +811,14 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
     if (st != MOE_OK) return st;
     // 4. weight gradients (contraction over each expert's rows, all macrobatches)
     gw2.Mw = L.F; gw2.N = L.H; gw2.of0 = dW2; gw2.accumulate = accumulate;
+    if (kPairGemm && !mx && !accumulate) {
+        // weight-gradient tiles leave through shared memory and TMA stores
+        if (!make_map_f32_out(&gw2.om0, dW2, EF, L.H) || !make_map_f32_out(&gw13.om0, dW1, EH, L.F) ||
+            !make_map_f32_out(&gw13.om1, dW3, EH, L.F))
+            return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        gw2.tma_store = 1;
+        gw13.tma_store = 1;
+    }
     {
         ProfScope ps("grouped_gemm_wgrad2", s);
         st = cuda_check(launch_grouped_gemm(OP_WG2, gw2, L.num_sms, s, mx, kPairGemm && !mx), "dW2 launch");
