@@ -51,6 +51,7 @@ constexpr uint32_t STAGE_STRIDE_FP8 = 51200;    // 48 KiB of tiles + atoms, 1 Ki
 constexpr int BK8 = 128;                        // K elements per stage, e4m3
 
 template <bool FP8> __host__ __device__ constexpr uint32_t stage_stride() { return FP8 ? STAGE_STRIDE_FP8 : STAGE_BYTES; }
+constexpr uint32_t P_STAGING_1 = 4 * 8192;   // epilogue staging of the 1-CTA bf16 kernel
 template <bool FP8> __host__ __device__ constexpr int bk_elems() { return FP8 ? BK8 : BK; }
 
 // D[tmem] (+)= A[smem] * B[smem], e4m3 x e4m3 with E8M0 block scales read from
@@ -462,6 +463,29 @@ __device__ void mma_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tiles, ui
 __device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
 __device__ __forceinline__ float sigmoid_f(float a) { return 1.0f / (1.0f + __expf(-a)); }
 
+// 32 rows (one per lane) x 32 bf16 of this warp -> a 2 KB staging buffer (plain
+// row-major, 64 B per row) -> one TMA store at (col0, row0) of map m. Four
+// buffers per warp rotate; a buffer is reused once the store issued four
+// stores earlier has read it.
+__device__ __forceinline__ void stage_store_bf16(uint8_t *warp_stage, int &nstores, const uint32_t (&w)[16],
+                                                 const CUtensorMap *m, int col0, int row0, int lane) {
+    uint8_t *buf = warp_stage + (nstores & 3) * 2048;
+    if (nstores >= 4) {
+        if (lane == 0) bulk_wait_group_read<3>();
+        __syncwarp();
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4 *>(buf + lane * 64 + q * 16) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(m, smem_u32(buf), col0, row0);
+        bulk_commit_group();
+    }
+    ++nstores;
+}
+
 // PAIR: the CTA pair computes a 256-row tile; this CTA's accumulator holds
 // rows [128 * rank, +128). A half beyond its expert's run (odd number of
 // 128-row tiles) is computed on whatever rows follow and not stored.
@@ -478,6 +502,8 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
     const int ring_shift = g.ring_base - g.offp[g.m * g.E];
     const int rank = PAIR ? (int)cluster_ctarank() : 0;
     int store_chunks = 0;   // TMA stores issued by this warp (lane 0 tracks the bulk groups)
+    const bool tma_bf16 = !FP8 && staging != nullptr && g.tma_store && OP != OP_WG2 && OP != OP_WG13;
+    uint8_t *warp_stage = staging ? staging + (warp - 2) * 8192 : nullptr;
     const int t0 = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
     const int tstep = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
     for (int t = t0; t < total; t += tstep) {
@@ -521,12 +547,19 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                     hf[2 * i + 1] = silu_f(a1) * b1;
                     oh[i] = pack_bf16x2(hf[2 * i], hf[2 * i + 1]);
                 }
+                if (tma_bf16) {
+                    const int row0 = ti.g0 + quarter * 32, col0 = ti.nt * 128 + cc * 32;
+                    stage_store_bf16(warp_stage, store_chunks, oa, &g.om0, col0, row0, lane);
+                    stage_store_bf16(warp_stage, store_chunks, ob, &g.om1, col0, row0, lane);
+                    stage_store_bf16(warp_stage, store_chunks, oh, &g.om2, col0, row0 + ring_shift, lane);
+                } else {
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    st_v4(pa + cc * 32 + v * 8, make_uint4(oa[4 * v], oa[4 * v + 1], oa[4 * v + 2], oa[4 * v + 3]));
-                    st_v4(pb + cc * 32 + v * 8, make_uint4(ob[4 * v], ob[4 * v + 1], ob[4 * v + 2], ob[4 * v + 3]));
-                    if constexpr (!FP8)
-                        st_v4(ph + cc * 32 + v * 8, make_uint4(oh[4 * v], oh[4 * v + 1], oh[4 * v + 2], oh[4 * v + 3]));
+                    for (int v = 0; v < 4; ++v) {
+                        st_v4(pa + cc * 32 + v * 8, make_uint4(oa[4 * v], oa[4 * v + 1], oa[4 * v + 2], oa[4 * v + 3]));
+                        st_v4(pb + cc * 32 + v * 8, make_uint4(ob[4 * v], ob[4 * v + 1], ob[4 * v + 2], ob[4 * v + 3]));
+                        if constexpr (!FP8)
+                            st_v4(ph + cc * 32 + v * 8, make_uint4(oh[4 * v], oh[4 * v + 1], oh[4 * v + 2], oh[4 * v + 3]));
+                    }
                 }
                 if constexpr (FP8) {
                     // h quantised along F (blocks of 32) for GEMM2's A operand
@@ -552,9 +585,14 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                 uint32_t o[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) o[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                if (tma_bf16) {
+                    const int row0 = (int)(orow - r) + quarter * 32;
+                    stage_store_bf16(warp_stage, store_chunks, o, &g.om0, ti.nt * BN + cc * 32, row0, lane);
+                } else {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    st_v4(py + cc * 32 + q * 8, make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]));
+                    for (int q = 0; q < 4; ++q)
+                        st_v4(py + cc * 32 + q * 8, make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]));
+                }
             }
         } else if constexpr (OP == OP_BWD2) {
             const int grow = ti.g0 + r;
@@ -618,6 +656,13 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                     dq[1] = make_uint4(q[4], q[5], q[6], q[7]);
                     g.qs1[mx_sf_offset(grow, col, F)] = (uint8_t)sb;
                 }
+                if (tma_bf16) {
+                    const int row0 = ti.g0 + quarter * 32, col0 = ti.nt * BN + cc * 32;
+                    stage_store_bf16(warp_stage, store_chunks, oda, &g.om0, col0, row0, lane);
+                    stage_store_bf16(warp_stage, store_chunks, odb, &g.om1, col0, row0, lane);
+                    stage_store_bf16(warp_stage, store_chunks, ohw, &g.om2, col0, row0, lane);
+                    continue;
+                }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     st_v4(pda + cc * 32 + q * 8, make_uint4(oda[4 * q], oda[4 * q + 1], oda[4 * q + 2], oda[4 * q + 3]));
@@ -652,7 +697,7 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                 if (staging != nullptr && g.tma_store && !g.accumulate) {
                     // 32 rows x 32 fp32 of this warp -> 128B-swizzled staging buffer -> one TMA store.
                     // Two buffers per warp: wait until the store issued two chunks ago has read its source.
-                    uint8_t *buf = staging + ((warp - 2) * 2 + (store_chunks & 1)) * 4096;
+                    uint8_t *buf = warp_stage + (store_chunks & 1) * 4096;
                     if (store_chunks >= 2) {
                         if (lane == 0) bulk_wait_group_read<1>();
                         __syncwarp();
@@ -708,7 +753,8 @@ template <int OP, bool FP8>
 __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    SmemCtl &c = *reinterpret_cast<SmemCtl *>(tiles + STAGES * stage_stride<FP8>());
+    uint8_t *staging = FP8 ? nullptr : tiles + STAGES * stage_stride<FP8>();   // bf16: 4 warps x 8 KB
+    SmemCtl &c = *reinterpret_cast<SmemCtl *>(tiles + STAGES * stage_stride<FP8>() + (FP8 ? 0 : P_STAGING_1));
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     WaitCtl ctl{g.status, g.budget_ns};
 
@@ -743,7 +789,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
     } else if (warp == 1) {
         if (lane == 0) mma_loop<OP, FP8>(g, c, tiles, c.full, c.empty, c.tfull, c.tempty, &c.drain, tmem, ctl);
     } else if (warp < 6) {
-        epilogue_loop<OP, FP8>(g, c, c.tfull, c.tempty, tmem, ctl);
+        epilogue_loop<OP, FP8>(g, c, c.tfull, c.tempty, tmem, ctl, staging);
     } else {
         if constexpr (OP == OP_FWD1) gather_loop<FP8>(g);
     }
@@ -982,7 +1028,7 @@ cudaError_t launch_pair(const GemmArgs &g, int grid, cudaStream_t stream) {
 
 template <int OP, bool FP8>
 cudaError_t launch_op(const GemmArgs &g, int grid, cudaStream_t stream) {
-    constexpr size_t smem = STAGES * stage_stride<FP8>() + sizeof(SmemCtl) + 1024;
+    constexpr size_t smem = STAGES * stage_stride<FP8>() + (FP8 ? 0 : P_STAGING_1) + sizeof(SmemCtl) + 1024;
     static_assert(smem <= 227 * 1024, "shared memory budget");
     cudaError_t err =
         cudaFuncSetAttribute(grouped_gemm_kernel<OP, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

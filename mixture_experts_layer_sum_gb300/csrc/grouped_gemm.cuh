@@ -12,8 +12,9 @@ enum GemmOp { OP_FWD1 = 0, OP_FWD2 = 1, OP_BWD2 = 2, OP_BWD1 = 3, OP_WG2 = 4, OP
 // ring row = padded row - offp[m*E] + ring_base.
 struct GemmArgs {
     CUtensorMap a0, a1, b0, b1;   // TMA maps (bf16, 128-byte swizzle, 64-element inner box)
-    CUtensorMap om0, om1;         // weight-gradient outputs (fp32, 32 x 32 boxes), CTA-pair kernel
-    int tma_store;                // 1: weight-gradient epilogue stores through shared memory + TMA
+    CUtensorMap om0, om1, om2;    // output maps for TMA stores: fp32 weight gradients (32 x 32,
+                                  // 128B swizzle) or bf16 row outputs (32 x 32, no swizzle)
+    int tma_store;                // 1: bf16 variants store epilogue tiles through shared memory + TMA
     const int *offp;              // [nM*E + 1] padded run starts
     int E, nM, m;                 // experts, macrobatches, macrobatch of a grouped-M launch
     int H, F;

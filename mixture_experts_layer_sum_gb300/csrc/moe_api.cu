@@ -282,6 +282,19 @@ bool make_map_f32_out(CUtensorMap *m, void *base, size_t rows, size_t cols) {
     return r == CUDA_SUCCESS;
 }
 
+// bf16 [rows, cols] output map for TMA stores of 32 x 32 boxes (no swizzle)
+bool make_map_bf16_out(CUtensorMap *m, void *base, size_t rows, size_t cols) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || rows == 0) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // MXFP8 weight copies made by moe_quantize_weights, each K-major for one GEMM:
 //   w1t, w3t: W1^T, W3^T [E][F][H] along H (GEMM1)     w2t: W2^T [E][H][F] along F (GEMM2)
 //   w2q:      W2 [E][F][H] along H (GEMM2 dgrad)       w1q, w3q: W1, W3 [E][H][F] along F (GEMM1 dgrad)
@@ -591,6 +604,12 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
             !make_map_mn(&g2.b0, W2, (size_t)L.E * L.F, L.H, 64, nb2))
             return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         g1.o2 = ringH;
+        // epilogue tiles leave through shared memory and TMA stores
+        if (!make_map_bf16_out(&g1.om0, s_a, L.rows_pad_max, L.F) || !make_map_bf16_out(&g1.om1, s_b, L.rows_pad_max, L.F) ||
+            !make_map_bf16_out(&g1.om2, ringH, ring_rows, L.F) || !make_map_bf16_out(&g2.om0, ringY, ring_rows, L.H))
+            return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        g1.tma_store = 1;
+        g2.tma_store = 1;
     } else {
         const QwLayout q = qw_layout(cfg);
         const uint8_t *qw = static_cast<const uint8_t *>(align_base(qweights));
@@ -709,6 +728,11 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
             !make_map_mn(&gw13.a0, Xs, rp, L.H, 64, 2) || !make_map_mn(&gw13.b0, dA, rp, L.F, 64, 2) ||
             !make_map_mn(&gw13.b1, dB, rp, L.F, 64, 2))
             return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        if (!make_map_bf16_out(&gb2.om0, dA, rp, L.F) || !make_map_bf16_out(&gb2.om1, dB, rp, L.F) ||
+            !make_map_bf16_out(&gb2.om2, HW, rp, L.F) || !make_map_bf16_out(&gb1.om0, dXs, rp, L.H))
+            return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        gb2.tma_store = 1;
+        gb1.tma_store = 1;
     } else {
         const QwLayout q = qw_layout(cfg);
         const uint8_t *qw = static_cast<const uint8_t *>(align_base(qweights));
