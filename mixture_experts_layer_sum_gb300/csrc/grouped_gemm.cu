@@ -21,7 +21,7 @@
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator, fused elementwise
 //              work, stores to global memory
 //   warps 6-9  (GEMM1 only) dispatch: gather/quantise token rows into the ring
-//              minibatch by minibatch, publish per-minibatch ready counters
+//              minibatch by minibatch, publish per-minibatch ready row counts
 // MXFP8 variant (FP8 = true): every operand is K-major E4M3 with E8M0 scale
 // atoms (moe_common.cuh); a stage holds 128 elements of K (A 128x128 B,
 // B 256x128 B) plus the 512-byte scale atoms of A and of both 128-row halves
@@ -169,21 +169,27 @@ __device__ void init_tile_table(Ctl &c, const GemmArgs &g) {
     }
 }
 
-// Fused dispatch (FWD1): the 4 gather warps of each CTA pull token rows of the
-// macrobatch into the ring (article "O MoK do Cursor ...", section 02: pull
-// dispatch; the ring token buffer is advanced by GPU-side state, minibatch by
-// minibatch, with no CPU in the loop). Rows of minibatch j are spread over all
-// CTAs; after its share of j a CTA adds 1 to ready[j] with release semantics.
+// Fused dispatch (FWD1): the gather warps pull token rows of the macrobatch into
+// the ring (article "O MoK do Cursor ...", section 02: pull dispatch; the ring
+// token buffer is advanced by GPU-side state, minibatch by minibatch, with no
+// CPU in the loop). A warp claims the next 4 rows from a global counter
+// (claims go in row order, so minibatches fill in order), gathers them and adds
+// 4 to ready[j] of their minibatch with release semantics. Any subset of running
+// CTAs can finish the gathering, so no CTA has to wait for another to start.
+constexpr int kGatherRows = 4;
 template <bool FP8>
 __device__ void gather_loop(const GemmArgs &g) {
-    const int gw = threadIdx.x / 32 - 6, lane = threadIdx.x % 32;
+    const int lane = threadIdx.x % 32;
     const int r0 = g.offp[g.m * g.E], r1 = g.offp[(g.m + 1) * g.E];
-    const int nmb = (r1 - r0 + g.mb_rows - 1) / g.mb_rows;
-    const int stride = gridDim.x * 4;
     const int vecs = g.H / 8;
-    for (int j = 0; j < nmb; ++j) {
-        const int b0 = r0 + j * g.mb_rows, b1 = min(r1, b0 + g.mb_rows);
-        for (int r = b0 + blockIdx.x * 4 + gw; r < b1; r += stride) {
+    int *claim = g.ready + g.ready_slots;    // row-chunk counter, after the ready counters
+    for (;;) {
+        int c = 0;
+        if (lane == 0) c = atomicAdd(claim, 1);
+        c = __shfl_sync(0xffffffffu, c, 0);
+        const int rb = r0 + c * kGatherRows;
+        if (rb >= r1) break;
+        for (int r = rb; r < rb + kGatherRows; ++r) {
             const int slot = g.row_slot[r];
             const bf16 *src = slot >= 0 ? g.xsrc + (size_t)(slot / g.k) * g.H : nullptr;
             const size_t drow = (size_t)(r - r0 + g.ring_base);
@@ -200,27 +206,10 @@ __device__ void gather_loop(const GemmArgs &g) {
                 for (; v < vecs; v += 32) st_v4(dst + v * 8, src ? ld_nc_v4(src + v * 8) : make_uint4(0, 0, 0, 0));
             } else {
                 uint8_t *dst = g.ringxq + drow * g.H;
-                uint4 pre[4];   // the next four 16-byte loads are issued before the current ones are used
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int vv = lane + 32 * u;
-                    pre[u] = (src && vv < vecs) ? ld_nc_v4(src + vv * 8) : make_uint4(0, 0, 0, 0);
-                }
-                for (int v0 = lane; v0 < vecs; v0 += 128) {
-                  uint4 cur[4];
-#pragma unroll
-                  for (int u = 0; u < 4; ++u) {
-                      cur[u] = pre[u];
-                      const int vn = v0 + 128 + 32 * u;
-                      pre[u] = (src && vn < vecs) ? ld_nc_v4(src + vn * 8) : make_uint4(0, 0, 0, 0);
-                  }
-#pragma unroll
-                  for (int u = 0; u < 4; ++u) {
-                    const int v = v0 + 32 * u;
-                    if (v >= vecs) break;
+                for (int v = lane; v < vecs; v += 32) {
                     float f[8];
                     if (src) {
-                        const uint4 q = cur[u];
+                        const uint4 q = ld_nc_v4(src + v * 8);
                         const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                         for (int i = 0; i < 4; ++i) { f[2 * i] = bf16lo(w4[i]); f[2 * i + 1] = bf16hi(w4[i]); }
@@ -240,16 +229,15 @@ __device__ void gather_loop(const GemmArgs &g) {
                     cq.y = cvt_e4m3x4(f[4] * inv, f[5] * inv, f[6] * inv, f[7] * inv);
                     *reinterpret_cast<uint2 *>(dst + v * 8) = cq;
                     if ((lane & 3) == 0) g.ringxs[mx_sf_offset(drow, (size_t)v * 8, g.H)] = (uint8_t)(sx + 127);
-                  }
                 }
             }
         }
-        // all 128 gather threads of this CTA are done with minibatch j
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (gw == 0 && lane == 0) {
+        // publish: this warp's 4 rows of minibatch j are in the ring
+        __syncwarp();
+        if (lane == 0) {
             __threadfence();
             fence_proxy_async_global();
-            red_release_gpu_add(g.ready + j, 1);
+            red_release_gpu_add(g.ready + (rb - r0) / g.mb_rows, kGatherRows);
         }
     }
 }
@@ -270,9 +258,11 @@ __device__ void producer_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tile
         if constexpr (OP == OP_FWD1) {
             if (g.fused) {
                 // the tile's rows lie in one minibatch (minibatches are 128-row aligned)
-                const int j = (ti.g0 - g.offp[g.m * g.E]) / g.mb_rows;
+                const int r0 = g.offp[g.m * g.E], nrows = g.offp[(g.m + 1) * g.E] - r0;
+                const int j = (ti.g0 - r0) / g.mb_rows;
                 if (j != ready_mb) {
-                    if (!flag_wait_geq(g.ready + j, (int)gridDim.x, ctl)) { ok = false; break; }
+                    const int need = min(g.mb_rows, nrows - j * g.mb_rows);
+                    if (!flag_wait_geq(g.ready + j, need, ctl)) { ok = false; break; }
                     fence_proxy_async_global();
                     ready_mb = j;
                 }
@@ -831,9 +821,11 @@ __device__ void pair_producer_loop(const GemmArgs &g, const PairCtl &c, uint8_t 
         const int m0 = (ti.mt * 2 + rank) * BM;          // grouped-K: this CTA's 128 rows of dW
         if constexpr (OP == OP_FWD1) {
             if (g.fused && row0 < c.seg_end[ti.e]) {
-                const int j = (row0 - g.offp[g.m * g.E]) / g.mb_rows;
+                const int r0 = g.offp[g.m * g.E], nrows = g.offp[(g.m + 1) * g.E] - r0;
+                const int j = (row0 - r0) / g.mb_rows;
                 if (j != ready_mb) {
-                    if (!flag_wait_geq(g.ready + j, (int)gridDim.x, ctl)) { ok = false; break; }
+                    const int need = min(g.mb_rows, nrows - j * g.mb_rows);
+                    if (!flag_wait_geq(g.ready + j, need, ctl)) { ok = false; break; }
                     fence_proxy_async_global();
                     ready_mb = j;
                 }
@@ -1001,28 +993,25 @@ cudaError_t launch_pair(const GemmArgs &g, int grid, cudaStream_t stream) {
     cfg.blockDim = dim3(fused ? 320 : 192);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeCooperative;   // gather warps publish flags other CTAs wait on
-    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
     // A persistent grid must be fully co-resident: with GPCs of an odd SM count
     // not every SM can host half of a pair, so size the grid by the number of
     // clusters that fit at once (queried once per kernel and block size).
     static int max_clusters[2] = {0, 0};
     int &mc = max_clusters[fused ? 1 : 0];
+    cfg.numAttrs = 1;
     if (mc == 0) {
         cfg.gridDim = dim3(grid / 2 * 2);
-        cfg.numAttrs = 1;
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel<OP>, &cfg) != cudaSuccess || n <= 0) n = grid / 2;
         mc = n;
     }
     cfg.gridDim = dim3(2 * std::min(grid / 2, mc));
-    cfg.numAttrs = fused ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<OP>, g);
 }
 
@@ -1033,13 +1022,7 @@ cudaError_t launch_op(const GemmArgs &g, int grid, cudaStream_t stream) {
     cudaError_t err =
         cudaFuncSetAttribute(grouped_gemm_kernel<OP, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    if (OP == OP_FWD1 && g.fused) {
-        // gather warps publish flags that other CTAs wait on: all CTAs must be resident
-        void *args[] = {const_cast<GemmArgs *>(&g)};
-        return cudaLaunchCooperativeKernel((const void *)grouped_gemm_kernel<OP, FP8>, dim3(grid), dim3(320), args,
-                                           smem, stream);
-    }
-    grouped_gemm_kernel<OP, FP8><<<grid, 192, smem, stream>>>(g);
+    grouped_gemm_kernel<OP, FP8><<<grid, (OP == OP_FWD1 && g.fused) ? 320 : 192, smem, stream>>>(g);
     return cudaGetLastError();
 }
 

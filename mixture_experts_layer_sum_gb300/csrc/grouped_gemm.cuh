@@ -34,15 +34,17 @@ struct GemmArgs {
     int kstore;
     uint8_t *q0, *q1, *qs0, *qs1;  // FWD1: h codes/scales (ring); BWD2: da, db codes/scales
     // FWD1 with the dispatch fused in (fused = 1): warps 6-9 of every CTA
-    // gather the macrobatch's token rows into the ring minibatch by minibatch
-    // (bf16, or MXFP8 along H) and publish ready[j] = number of CTAs done with
-    // minibatch j; the TMA producer acquires ready[j] == gridDim.x before it
-    // loads a tile of minibatch j. Needs a cooperative (co-resident) launch.
+    // claim 4-row chunks of the macrobatch from a counter, gather them into the
+    // ring (bf16, or MXFP8 along H) and add the rows to ready[j] of their
+    // minibatch; the TMA producer acquires ready[j] == rows of minibatch j
+    // before it loads a tile of it. ready[0..ready_slots) and the claim counter
+    // ready[ready_slots] are zeroed before every launch.
     int fused;
     const bf16 *xsrc;
     bf16 *ringx;
     uint8_t *ringxq, *ringxs;
     int *ready;
+    int ready_slots;
     int mb_rows, k;
     int *status;
     unsigned long long budget_ns;

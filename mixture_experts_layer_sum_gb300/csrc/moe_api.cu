@@ -163,7 +163,7 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     L.w_wrt = take(2 * EP * H);
     L.w_offp = take(4 * (nM * E + 1));
     L.mb_rows = (int)align_up((size_t)std::max(L.minibatch_rows, kRowPad), kRowPad);
-    L.w_ready = take(4 * ((size_t)L.half_rows / kRowPad + 1));   // per-minibatch ready counters
+    L.w_ready = take(4 * ((size_t)L.half_rows / kRowPad + 2));   // per-minibatch ready rows + claim counter
     const size_t region = o;
     const size_t ring_rows = (size_t)L.half_rows * L.ring_halves;
     // forward region: the ring
@@ -631,11 +631,12 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
     int *ready = at<int>(ws, L.w_ready);
     g1.fused = 1; g1.xsrc = (const bf16 *)x; g1.row_slot = s_row_slot; g1.k = L.k; g1.mb_rows = L.mb_rows;
     g1.ready = ready;
+    g1.ready_slots = L.half_rows / kRowPad + 1;
     if (!mx) g1.ringx = ringX;
     else { g1.ringxq = ringXq; g1.ringxs = ringXs; }
     for (int m = 0; m < L.nM; ++m) {
         const int ring_base = (m % L.ring_halves) * L.half_rows;
-        st = cuda_check(cudaMemsetAsync(ready, 0, 4 * ((size_t)L.half_rows / kRowPad + 1), s), "ready clear");
+        st = cuda_check(cudaMemsetAsync(ready, 0, 4 * ((size_t)L.half_rows / kRowPad + 2), s), "ready clear");
         if (st != MOE_OK) return st;
         g1.m = m; g1.ring_base = ring_base;
         {
