@@ -595,6 +595,14 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
             bf16 *pdb = g.o1 + grow * F + ti.nt * BN;
             bf16 *phw = g.o2 + grow * F + ti.nt * BN;
             float dwp = 0.0f;
+            // saved a, b of the next 32 columns are loaded one chunk ahead so their
+            // latency overlaps the current chunk's work
+            uint4 na[4], nb[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                na[q] = ld_nc_v4(pa + q * 8);
+                nb[q] = ld_nc_v4(pb + q * 8);
+            }
 #pragma unroll 1
             for (int cc = 0; cc < BN / 32; ++cc) {
                 uint32_t v[32];
@@ -602,10 +610,15 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                 uint32_t ra[16], rb[16];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    uint4 x = ld_v4(pa + cc * 32 + q * 8);
-                    uint4 y = ld_v4(pb + cc * 32 + q * 8);
-                    ra[4 * q] = x.x; ra[4 * q + 1] = x.y; ra[4 * q + 2] = x.z; ra[4 * q + 3] = x.w;
-                    rb[4 * q] = y.x; rb[4 * q + 1] = y.y; rb[4 * q + 2] = y.z; rb[4 * q + 3] = y.w;
+                    ra[4 * q] = na[q].x; ra[4 * q + 1] = na[q].y; ra[4 * q + 2] = na[q].z; ra[4 * q + 3] = na[q].w;
+                    rb[4 * q] = nb[q].x; rb[4 * q + 1] = nb[q].y; rb[4 * q + 2] = nb[q].z; rb[4 * q + 3] = nb[q].w;
+                }
+                if (cc + 1 < BN / 32) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        na[q] = ld_nc_v4(pa + (cc + 1) * 32 + q * 8);
+                        nb[q] = ld_nc_v4(pb + (cc + 1) * 32 + q * 8);
+                    }
                 }
                 tmem_ld_wait();
                 uint32_t oda[16], odb[16], ohw[16];
