@@ -189,46 +189,72 @@ __device__ void gather_loop(const GemmArgs &g) {
         c = __shfl_sync(0xffffffffu, c, 0);
         const int rb = r0 + c * kGatherRows;
         if (rb >= r1) break;
-        for (int r = rb; r < rb + kGatherRows; ++r) {
-            const int slot = g.row_slot[r];
-            const bf16 *src = slot >= 0 ? g.xsrc + (size_t)(slot / g.k) * g.H : nullptr;
-            const size_t drow = (size_t)(r - r0 + g.ring_base);
-            if constexpr (!FP8) {
-                bf16 *dst = g.ringx + drow * g.H;
-                int v = lane;
-                for (; v + 96 < vecs; v += 128) {
+        if constexpr (!FP8) {
+            // two rows at a time, 8 vectors of each per lane in flight (8 KB per warp)
+            for (int r = rb; r < rb + kGatherRows; r += 2) {
+                const bf16 *src[2];
+                bf16 *dst[2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int slot = g.row_slot[r + i];
+                    src[i] = slot >= 0 ? g.xsrc + (size_t)(slot / g.k) * g.H : nullptr;
+                    dst[i] = g.ringx + (size_t)(r + i - r0 + g.ring_base) * g.H;
+                }
+                for (int v0 = 0; v0 < vecs; v0 += 256) {
+                    uint4 q[2][8];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int v = v0 + lane + 32 * u;
+                            q[i][u] = (src[i] && v < vecs) ? ld_nc_v4(src[i] + v * 8) : make_uint4(0, 0, 0, 0);
+                        }
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int v = v0 + lane + 32 * u;
+                            if (v < vecs) st_v4(dst[i] + v * 8, q[i][u]);
+                        }
+                }
+            }
+        } else {
+            for (int r = rb; r < rb + kGatherRows; ++r) {
+                const int slot = g.row_slot[r];
+                const bf16 *src = slot >= 0 ? g.xsrc + (size_t)(slot / g.k) * g.H : nullptr;
+                const size_t drow = (size_t)(r - r0 + g.ring_base);
+                uint8_t *dst = g.ringxq + drow * g.H;
+                // 4 vectors per lane in flight; a quad of lanes holds one 32-element block
+                // (vecs is a multiple of 16, so a quad is valid or invalid as a whole)
+                for (int v0 = 0; v0 < vecs; v0 += 128) {
                     uint4 q[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) q[u] = src ? ld_nc_v4(src + (v + 32 * u) * 8) : make_uint4(0, 0, 0, 0);
+                    for (int u = 0; u < 4; ++u) {
+                        const int v = v0 + lane + 32 * u;
+                        q[u] = (src && v < vecs) ? ld_nc_v4(src + v * 8) : make_uint4(0, 0, 0, 0);
+                    }
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) st_v4(dst + (v + 32 * u) * 8, q[u]);
-                }
-                for (; v < vecs; v += 32) st_v4(dst + v * 8, src ? ld_nc_v4(src + v * 8) : make_uint4(0, 0, 0, 0));
-            } else {
-                uint8_t *dst = g.ringxq + drow * g.H;
-                for (int v = lane; v < vecs; v += 32) {
-                    float f[8];
-                    if (src) {
-                        const uint4 q = ld_nc_v4(src + v * 8);
-                        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+                    for (int u = 0; u < 4; ++u) {
+                        const int v = v0 + lane + 32 * u;
+                        const uint32_t w4[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+                        float f[8];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) { f[2 * i] = bf16lo(w4[i]); f[2 * i + 1] = bf16hi(w4[i]); }
-                    } else {
+                        float amax = 0.0f;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) f[i] = 0.0f;
+                        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                        const int sx = mx_exponent(amax);
+                        const float inv = mx_inv_scale(sx);
+                        uint2 cq;
+                        cq.x = cvt_e4m3x4(f[0] * inv, f[1] * inv, f[2] * inv, f[3] * inv);
+                        cq.y = cvt_e4m3x4(f[4] * inv, f[5] * inv, f[6] * inv, f[7] * inv);
+                        if (v < vecs) {
+                            *reinterpret_cast<uint2 *>(dst + v * 8) = cq;
+                            if ((lane & 3) == 0) g.ringxs[mx_sf_offset(drow, (size_t)v * 8, g.H)] = (uint8_t)(sx + 127);
+                        }
                     }
-                    float amax = 0.0f;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-                    const int sx = mx_exponent(amax);
-                    const float inv = mx_inv_scale(sx);
-                    uint2 cq;
-                    cq.x = cvt_e4m3x4(f[0] * inv, f[1] * inv, f[2] * inv, f[3] * inv);
-                    cq.y = cvt_e4m3x4(f[4] * inv, f[5] * inv, f[6] * inv, f[7] * inv);
-                    *reinterpret_cast<uint2 *>(dst + v * 8) = cq;
-                    if ((lane & 3) == 0) g.ringxs[mx_sf_offset(drow, (size_t)v * 8, g.H)] = (uint8_t)(sx + 127);
                 }
             }
         }
@@ -450,8 +476,13 @@ __device__ void mma_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tiles, ui
     while (!mbar_try_wait(smem_u32(drain), 0) && globaltimer_ns() - t0 < ctl.budget_ns) {}
 }
 
-__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
-__device__ __forceinline__ float sigmoid_f(float a) { return 1.0f / (1.0f + __expf(-a)); }
+// sigmoid with the approximate reciprocal (one MUFU op; an IEEE division here
+// expands to a branchy sequence that serialises the epilogue). silu = a * sigmoid(a)
+// is formed the same way in the forward and the backward epilogues, so the
+// backward recomputes the forward's h bit for bit. For a < -88, exp(-a) = inf and
+// the reciprocal gives 0, the limit.
+__device__ __forceinline__ float sigmoid_f(float a) { return __fdividef(1.0f, 1.0f + __expf(-a)); }
+__device__ __forceinline__ float silu_f(float a) { return a * sigmoid_f(a); }
 
 // 32 rows (one per lane) x 32 bf16 of this warp -> a 2 KB staging buffer (plain
 // row-major, 64 B per row) -> one TMA store at (col0, row0) of map m. Four
