@@ -136,7 +136,7 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     L.chunks_per_mb = std::max(1, ceil_div(std::min(Mb, std::max(c->T, 1)) * c->k, kSchedChunk));
     L.nchunks = c->T > 0 ? L.nM * L.chunks_per_mb : 0;
     // router-weight gradient: about eight blocks per SM over (H/64) x splits
-    L.dwr_splits = std::max(1, std::min(ceil_div(8 * L.num_sms, c->H / 64), ceil_div(std::max(c->T, 1), 64)));
+    L.dwr_splits = std::max(1, std::min(ceil_div(4 * L.num_sms, c->H / 64), ceil_div(std::max(c->T, 1), 64)));
 
     const size_t R = L.R, T = L.T, E = L.E, H = L.H, F = L.F, nM = L.nM, rp = L.rows_pad_max;
     size_t o = 0;

@@ -21,10 +21,12 @@ namespace moe {
 
 // W_r [H,E] -> WrT [EP,H] (EP = E rounded up to 8, extra rows zero), so the
 // tensor-core B fragments are contiguous along H.
+// One thread per output element (coalesced stores; the reads of W_r stride by E).
 __global__ void transpose_wr_kernel(const bf16 *__restrict__ Wr, bf16 *__restrict__ WrT, int H, int E, int EP) {
-    int h = blockIdx.x * blockDim.x + threadIdx.x;
-    if (h >= H) return;
-    for (int e = 0; e < EP; ++e) WrT[(size_t)e * H + h] = e < E ? Wr[(size_t)h * E + e] : f2bf(0.0f);
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= H * EP) return;
+    const int e = i / H, h = i % H;
+    WrT[i] = e < E ? Wr[(size_t)h * E + e] : f2bf(0.0f);
 }
 
 __device__ __forceinline__ void mma_16816_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -35,54 +37,56 @@ __device__ __forceinline__ void mma_16816_bf16(float (&d)[4], const uint32_t (&a
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-constexpr int kRouterTokens = 32;   // tokens per block
+constexpr int kRouterTokens = 16;   // tokens per block (one m16 tile)
+constexpr int kRouterMT = kRouterTokens / 16;
 constexpr int kRouterWarps = 8;     // warps split H
 
-// Block: 32 tokens x all experts. Warp w covers H range [w*H/8, (w+1)*H/8).
+// Block: 16 tokens x all experts. Warp w covers H range [w*H/8, (w+1)*H/8).
 // The contraction order inside a warp is permuted (thread c of a quad loads 8
 // consecutive h with one 16-byte load and feeds them as its k-slots of two
 // m16n8k16 steps); A and B use the same permutation, so the sum is exact in
 // structure and fixed in order.
 template <int NT>
 __global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a) {
-    extern __shared__ float part[];   // [warps][32 tokens][EP]
+    extern __shared__ float part[];   // [warps][kRouterTokens][EP]
     const int EP = NT * 8;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int g = lane >> 2, c = lane & 3;
     const int t0 = blockIdx.x * kRouterTokens;
     const int hspan = a.H / kRouterWarps;
     const int hbeg = warp * hspan;
-    float acc[2][NT][4];
+    float acc[kRouterMT][NT][4];
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int mt = 0; mt < kRouterMT; ++mt)
 #pragma unroll
         for (int n = 0; n < NT; ++n)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[mt][n][i] = 0.0f;
-    // the four token rows this thread feeds: mt*16 + g and mt*16 + g + 8
-    const bf16 *xrow[2][2];
-    bool valid[2][2];
+    // the token rows this thread feeds: mt*16 + g and mt*16 + g + 8
+    const bf16 *xrow[kRouterMT][2];
+    bool valid[kRouterMT][2];
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int mt = 0; mt < kRouterMT; ++mt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             int t = t0 + mt * 16 + g + hh * 8;
             valid[mt][hh] = t < a.T;
             xrow[mt][hh] = a.x + (size_t)(valid[mt][hh] ? t : 0) * a.H;
         }
-    for (int h0 = hbeg; h0 < hbeg + hspan; h0 += 32) {
+    // 32 h per step; the loads of step i+1 are issued before the MMAs of step i
+    auto load = [&](int h0, uint4 (&xv)[kRouterMT][2], uint4 (&wv)[NT]) {
         const int hc = h0 + 8 * c;
-        uint4 xv[2][2];
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+        for (int mt = 0; mt < kRouterMT; ++mt)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)
                 xv[mt][hh] = valid[mt][hh] ? ld_nc_v4(xrow[mt][hh] + hc) : make_uint4(0, 0, 0, 0);
-        uint4 wv[NT];
 #pragma unroll
         for (int n = 0; n < NT; ++n) wv[n] = ld_nc_v4(a.WrT + (size_t)(n * 8 + g) * a.H + hc);
+    };
+    auto step = [&](const uint4 (&xv)[kRouterMT][2], const uint4 (&wv)[NT]) {
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+        for (int mt = 0; mt < kRouterMT; ++mt) {
             // step 0 uses h = hc+0..3, step 1 uses hc+4..7
             uint32_t A0[4] = {xv[mt][0].x, xv[mt][1].x, xv[mt][0].y, xv[mt][1].y};
             uint32_t A1[4] = {xv[mt][0].z, xv[mt][1].z, xv[mt][0].w, xv[mt][1].w};
@@ -92,11 +96,23 @@ __global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a) {
                 mma_16816_bf16(acc[mt][n], A1, wv[n].z, wv[n].w);
             }
         }
+    };
+    const int hend = hbeg + hspan;   // hspan is a multiple of 32
+    uint4 xa[kRouterMT][2], wa[NT], xb[kRouterMT][2], wb[NT];
+    load(hbeg, xa, wa);
+    for (int h0 = hbeg; h0 < hend; h0 += 64) {
+        const bool second = h0 + 32 < hend;
+        if (second) load(h0 + 32, xb, wb);
+        step(xa, wa);
+        if (second) {
+            if (h0 + 64 < hend) load(h0 + 64, xa, wa);
+            step(xb, wb);
+        }
     }
     // partial logits of this warp -> shared memory
     float *my = part + (size_t)warp * kRouterTokens * EP;
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int mt = 0; mt < kRouterMT; ++mt)
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
             int row = mt * 16 + g, col = n * 8 + 2 * c;
@@ -106,8 +122,9 @@ __global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a) {
             my[(row + 8) * EP + col + 1] = acc[mt][n][3];
         }
     __syncthreads();
-    // each warp finishes 4 tokens; lane owns experts lane and lane+32
-    for (int tt = warp * 4; tt < warp * 4 + 4; ++tt) {
+    // each warp finishes kRouterTokens / kRouterWarps tokens; lane owns experts lane and lane+32
+    constexpr int kPerWarp = kRouterTokens / kRouterWarps;
+    for (int tt = warp * kPerWarp; tt < warp * kPerWarp + kPerWarp; ++tt) {
         const int t = t0 + tt;
         if (t >= a.T) break;
         float l[2];
@@ -178,7 +195,7 @@ cudaError_t launch_router(const RouterArgs &a, cudaStream_t s) {
     const int EP = (a.E + 7) / 8 * 8;
     const int blocks = ceil_div(a.T, kRouterTokens);
     const size_t smem = (size_t)kRouterWarps * kRouterTokens * EP * sizeof(float);
-    transpose_wr_kernel<<<ceil_div(a.H, 256), 256, 0, s>>>(a.Wr, a.WrT, a.H, a.E, EP);
+    transpose_wr_kernel<<<ceil_div(a.H * EP, 256), 256, 0, s>>>(a.Wr, a.WrT, a.H, a.E, EP);
     if (blocks == 0) return cudaGetLastError();
 #define MOE_ROUTER_CASE(NT)                                                                           \
     case NT: {                                                                                       \
@@ -323,15 +340,25 @@ __device__ void block_exclusive_scan2(int &a, int &b, int *s_w /* [64] */) {
 __global__ void __launch_bounds__(1024) schedule_scan_kernel(SchedArgs a) {
     __shared__ int s_tot[64];
     const int n = a.nM * a.E;
-    // counts and chunk bases (relative to the (m,e) start)
+    // counts and chunk bases (relative to the (m,e) start); the chunk counts are
+    // read eight at a time so their loads overlap
     for (int me = threadIdx.x; me < n; me += blockDim.x) {
         const int m = me / a.E, e = me % a.E;
         int run = 0;
-        for (int i = 0; i < a.chunks_per_mb; ++i) {
-            const int c = m * a.chunks_per_mb + i;
-            if (c >= a.nchunks) break;   // no slots (T = 0): no count block wrote this chunk
-            a.chunk_base[c * a.E + e] = run;
-            run += a.chunk_counts[c * a.E + e];
+        for (int i0 = 0; i0 < a.chunks_per_mb; i0 += 8) {
+            int v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int c = m * a.chunks_per_mb + i0 + u;
+                // no slots (T = 0): no count block wrote chunks past nchunks
+                v[u] = (i0 + u < a.chunks_per_mb && c < a.nchunks) ? __ldg(a.chunk_counts + c * a.E + e) : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int c = m * a.chunks_per_mb + i0 + u;
+                if (i0 + u < a.chunks_per_mb && c < a.nchunks) a.chunk_base[c * a.E + e] = run;
+                run += v[u];
+            }
         }
         a.counts[me] = run;
     }
@@ -407,16 +434,20 @@ __global__ void __launch_bounds__(256) dispatch_rows_kernel(DispatchArgs a) {
             for (int v = lane; v < vecs; v += 32) st_v4(dst + v * 8, make_uint4(0, 0, 0, 0));
         } else {
             const bf16 *src = a.src + (size_t)(slot / a.k) * a.H;
-            int v = lane;
-            for (; v + 96 < vecs; v += 128) {
-                uint4 x0 = ld_nc_v4(src + v * 8), x1 = ld_nc_v4(src + (v + 32) * 8);
-                uint4 x2 = ld_nc_v4(src + (v + 64) * 8), x3 = ld_nc_v4(src + (v + 96) * 8);
-                st_v4(dst + v * 8, x0);
-                st_v4(dst + (v + 32) * 8, x1);
-                st_v4(dst + (v + 64) * 8, x2);
-                st_v4(dst + (v + 96) * 8, x3);
+            // 8 vectors per lane in flight (4 KB per warp)
+            for (int v0 = 0; v0 < vecs; v0 += 256) {
+                uint4 xv[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int v = v0 + lane + 32 * u;
+                    xv[u] = v < vecs ? ld_nc_v4(src + v * 8) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int v = v0 + lane + 32 * u;
+                    if (v < vecs) st_v4(dst + v * 8, xv[u]);
+                }
             }
-            for (; v < vecs; v += 32) st_v4(dst + v * 8, ld_nc_v4(src + v * 8));
         }
     }
 }
@@ -437,37 +468,52 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
     const int nw = gridDim.x * blockDim.x / 32;
     const int shift = a.ring_base - a.offp[a.m * a.E];
+    const int vecs = a.H / 8;   // a multiple of 32
     for (int t = a.t0 + gw; t < a.t1; t += nw) {
-        for (int v = lane; v < a.H / 8; v += 32) {
-            float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            for (int j0 = 0; j0 < a.k; j0 += 8) {
-                const int nj = min(8, a.k - j0);
-                int rows[8];
-                float ws[8];
-                uint4 y[8];
+        // two vectors per lane, rows in batches of 4: 8 loads of 16 B per lane in flight
+        for (int v0 = lane; v0 < vecs; v0 += 64) {
+            const bool two = v0 + 32 < vecs;
+            float acc[2][8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
+            for (int p = 0; p < 2; ++p)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[p][i] = 0.0f;
+            for (int j0 = 0; j0 < a.k; j0 += 4) {
+                const int nj = min(4, a.k - j0);
+                int rows[4];
+                float ws[4];
+                uint4 y[2][4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
                     if (j < nj) {
                         rows[j] = a.slot_row[(size_t)t * a.k + j0 + j] + shift;
                         ws[j] = a.w[(size_t)t * a.k + j0 + j];
                     }
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (j < nj) y[j] = ld_v4(a.Y + (size_t)rows[j] * a.H + v * 8);
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
+                for (int j = 0; j < 4; ++j)
                     if (j < nj) {
-                        const uint32_t q[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            acc[2 * i] = fmaf(ws[j], bf16lo(q[i]), acc[2 * i]);
-                            acc[2 * i + 1] = fmaf(ws[j], bf16hi(q[i]), acc[2 * i + 1]);
-                        }
+                        y[0][j] = ld_v4(a.Y + (size_t)rows[j] * a.H + v0 * 8);
+                        if (two) y[1][j] = ld_v4(a.Y + (size_t)rows[j] * a.H + (v0 + 32) * 8);
                     }
+#pragma unroll
+                for (int p = 0; p < 2; ++p)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (j < nj && (p == 0 || two)) {
+                            const uint32_t q[4] = {y[p][j].x, y[p][j].y, y[p][j].z, y[p][j].w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                acc[p][2 * i] = fmaf(ws[j], bf16lo(q[i]), acc[p][2 * i]);
+                                acc[p][2 * i + 1] = fmaf(ws[j], bf16hi(q[i]), acc[p][2 * i + 1]);
+                            }
+                        }
             }
-            st_v4(a.out + (size_t)t * a.H + v * 8,
-                  make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                             pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+#pragma unroll
+            for (int p = 0; p < 2; ++p)
+                if (p == 0 || two)
+                    st_v4(a.out + (size_t)t * a.H + (v0 + 32 * p) * 8,
+                          make_uint4(pack_bf16x2(acc[p][0], acc[p][1]), pack_bf16x2(acc[p][2], acc[p][3]),
+                                     pack_bf16x2(acc[p][4], acc[p][5]), pack_bf16x2(acc[p][6], acc[p][7])));
         }
     }
 }
@@ -540,7 +586,7 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(RouterBwdArgs a) {
 // parts (about 16 significant bits), parks it in a shared tile, and then each
 // lane owns 32 contiguous h of one token for the 16-byte gathers of the k rows.
 constexpr int kRdTokens = 64;
-__global__ void __launch_bounds__(128) reverse_dispatch_kernel(RevDispatchArgs a) {
+__global__ void __launch_bounds__(128, 4) reverse_dispatch_kernel(RevDispatchArgs a) {
     __shared__ float s_acc[4][16][64 + 4];
     __shared__ __align__(16) bf16 s_wr[64][64 + 8];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -621,11 +667,11 @@ __global__ void __launch_bounds__(128) reverse_dispatch_kernel(RevDispatchArgs a
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-            for (int j0 = 0; j0 < a.k; j0 += 4) {
-                const int nj = min(4, a.k - j0);
-                uint4 q[4][4];
+            for (int j0 = 0; j0 < a.k; j0 += 2) {
+                const int nj = min(2, a.k - j0);
+                uint4 q[2][4];
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
+                for (int jj = 0; jj < 2; ++jj)
                     if (jj < nj) {
                         const int j = j0 + jj;
                         const int row = j < 32 ? rows[j] : a.slot_row[(size_t)my_t * a.k + j];
@@ -634,7 +680,7 @@ __global__ void __launch_bounds__(128) reverse_dispatch_kernel(RevDispatchArgs a
                         for (int u = 0; u < 4; ++u) q[jj][u] = ld_v4(src + u * 8);
                     }
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
+                for (int jj = 0; jj < 2; ++jj)
                     if (jj < nj) {
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
@@ -660,73 +706,141 @@ __global__ void __launch_bounds__(128) reverse_dispatch_kernel(RevDispatchArgs a
     }
 }
 
-// dW_r partials: block = (64 h, split sp); lane owns h pair (h0 + 2 lane, +1),
-// warp w owns experts [8w, 8w+8); tokens of the split in increasing order.
-// Each 64-token chunk of x (64 x 64 bf16) and of dlogits (64 x E) is staged in
-// shared memory with independent vector loads first.
+// dW_r partials on tensor cores: D[h][e] = sum_t x[t][h] dl[t][e] as m16n8k16
+// MMAs with M = h, N = e, K = tokens. x is bf16 (exact); dlogits (fp32) enter as
+// a bf16 high part plus a bf16 low part (about 16 significant bits), both
+// products accumulate in fp32. Block = 64 h (warp w owns h 16w..16w+15) x all
+// experts, tokens of split sp in chunks of 64 staged in shared memory: x as
+// [t][h] (A fragments by ldmatrix.trans), dlogits transposed as [e][t] hi and lo
+// (B fragments). The partial tile leaves through shared memory as [split][e][h].
 constexpr int kWgTok = 64;
-__global__ void __launch_bounds__(256) router_wgrad_part_kernel(RouterWgradArgs a) {
-    __shared__ __align__(16) float s_dl[kWgTok * kMaxExperts + 8];
-    __shared__ __align__(16) bf16 s_x[kWgTok][64];
+constexpr int kWgPad = 8;   // bf16 row padding: conflict-free fragment loads
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void *p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"((uint32_t)__cvta_generic_to_shared(p)));
+}
+__global__ void __launch_bounds__(128) router_wgrad_part_kernel(RouterWgradArgs a) {
+    __shared__ __align__(16) bf16 s_x[kWgTok][64 + kWgPad];
+    __shared__ __align__(16) bf16 s_hi[kMaxExperts][kWgTok + kWgPad];
+    __shared__ __align__(16) bf16 s_lo[kMaxExperts][kWgTok + kWgPad];
+    __shared__ __align__(16) float s_out[kMaxExperts][64 + 4];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int g = lane >> 2, c = lane & 3;
     const int hb = blockIdx.x * 64;
     const int sp = blockIdx.y;
     const int ts = ceil_div(a.T, a.splits);
     const int tb = sp * ts, te = min(a.T, tb + ts);
-    const int e0 = warp * 8;
-    float acc[2][8];
+    const int EP = (a.E + 7) / 8 * 8;
+    const int NT = EP / 8;
+    float acc[8][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[0][i] = acc[1][i] = 0.0f;
-    for (int c0 = tb; c0 < te; c0 += kWgTok) {
+    for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
+    // this lane's ldmatrix row: matrix q = lane / 8 covers h +8*(q&1), t +8*(q>>1)
+    const int lq = lane >> 3, li = lane & 7;
+    // the next chunk's x and dlogits are loaded into registers while this chunk
+    // computes: x as 4 vectors per thread, dlogits as rows of token pairs with
+    // lanes over experts (up to 64 -> 2 per lane, 8 pairs per warp)
+    uint4 xr[4];
+    float dr[8][2][2];   // [token pair][expert half][token of the pair]
+    auto fetch = [&](int c0) {
         const int cn = min(kWgTok, te - c0);
-        __syncthreads();
-        for (int i = threadIdx.x; i < kWgTok * 8; i += blockDim.x) {   // 8 x 16 B per token row
-            const int tt = i / 8, v = i % 8;
-            uint4 q = make_uint4(0, 0, 0, 0);
-            if (tt < cn) q = ld_nc_v4(a.x + (size_t)(c0 + tt) * a.H + hb + v * 8);
-            *reinterpret_cast<uint4 *>(&s_x[tt][v * 8]) = q;
-        }
-        // dlogits rows of the chunk are contiguous: cn * E floats
-        const int n = cn * a.E;
-        if ((a.E & 3) == 0) {
-            const float4 *src = reinterpret_cast<const float4 *>(a.dlogits + (size_t)c0 * a.E);
-            for (int i = threadIdx.x; i < n / 4; i += blockDim.x) reinterpret_cast<float4 *>(s_dl)[i] = src[i];
-        } else {
-            for (int i = threadIdx.x; i < n; i += blockDim.x) s_dl[i] = a.dlogits[(size_t)c0 * a.E + i];
-        }
-        __syncthreads();
-        if (e0 < a.E) {
-#pragma unroll 4
-            for (int tt = 0; tt < cn; ++tt) {
-                const uint32_t xv = *reinterpret_cast<const uint32_t *>(&s_x[tt][2 * lane]);
-                const float x0 = bf16lo(xv), x1 = bf16hi(xv);
-                const float *dl = s_dl + tt * a.E + e0;   // experts past E read neighbours; never stored
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float d = dl[i];
-                    acc[0][i] = fmaf(x0, d, acc[0][i]);
-                    acc[1][i] = fmaf(x1, d, acc[1][i]);
+        for (int u = 0; u < 4; ++u) {
+            const int i = threadIdx.x + 128 * u, tt = i >> 3, v = i & 7;
+            xr[u] = tt < cn ? ld_nc_v4(a.x + (size_t)(c0 + tt) * a.H + hb + v * 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int tt = 2 * (warp + 4 * u);
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2) {
+                const int e = lane + 32 * s2;
+#pragma unroll
+                for (int p = 0; p < 2; ++p)
+                    dr[u][s2][p] = (tt + p < cn && e < a.E) ? __ldg(a.dlogits + (size_t)(c0 + tt + p) * a.E + e) : 0.0f;
+            }
+        }
+    };
+    if (tb < te) fetch(tb);
+    for (int c0 = tb; c0 < te; c0 += kWgTok) {
+        __syncthreads();   // the previous chunk's fragments have been read
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = threadIdx.x + 128 * u;
+            *reinterpret_cast<uint4 *>(&s_x[i >> 3][(i & 7) * 8]) = xr[u];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int tt = 2 * (warp + 4 * u);
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2) {
+                const int e = lane + 32 * s2;
+                if (e < EP) {
+                    const uint32_t hi = pack_bf16x2(dr[u][s2][0], dr[u][s2][1]);
+                    *reinterpret_cast<uint32_t *>(&s_hi[e][tt]) = hi;
+                    *reinterpret_cast<uint32_t *>(&s_lo[e][tt]) =
+                        pack_bf16x2(dr[u][s2][0] - bf16lo(hi), dr[u][s2][1] - bf16hi(hi));
+                }
+            }
+        }
+        __syncthreads();
+        if (c0 + kWgTok < te) fetch(c0 + kWgTok);
+#pragma unroll
+        for (int ks = 0; ks < kWgTok / 16; ++ks) {
+            uint32_t A[4];
+            ldmatrix_x4_trans(A, &s_x[ks * 16 + li + 8 * (lq >> 1)][warp * 16 + 8 * (lq & 1)]);
+            // ldmatrix.trans hands out matrices in the order (h0-7,t0-7) (h8-15,t0-7) (h0-7,t8-15) (h8-15,t8-15):
+            // exactly the a0..a3 registers of the m16n8k16 A fragment
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+                if (n < NT) {
+                    const bf16 *ph = &s_hi[n * 8 + g][ks * 16 + 2 * c];
+                    const bf16 *pl = &s_lo[n * 8 + g][ks * 16 + 2 * c];
+                    mma_16816_bf16(acc[n], A, *reinterpret_cast<const uint32_t *>(ph),
+                                   *reinterpret_cast<const uint32_t *>(ph + 8));
+                    mma_16816_bf16(acc[n], A, *reinterpret_cast<const uint32_t *>(pl),
+                                   *reinterpret_cast<const uint32_t *>(pl + 8));
                 }
             }
         }
     }
-    const int h = hb + 2 * lane;
+    // D fragment: rows h = 16 warp + g (+8), columns e = 8n + 2c (+1)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int e = e0 + i;
-        if (e < a.E) {
-            a.part[((size_t)sp * a.H + h) * a.E + e] = acc[0][i];
-            a.part[((size_t)sp * a.H + h + 1) * a.E + e] = acc[1][i];
+    for (int n = 0; n < 8; ++n) {
+        if (n < NT) {
+            const int h = warp * 16 + g, e = n * 8 + 2 * c;
+            s_out[e][h] = acc[n][0];
+            s_out[e + 1][h] = acc[n][1];
+            s_out[e][h + 8] = acc[n][2];
+            s_out[e + 1][h + 8] = acc[n][3];
         }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < a.E * 16; i += blockDim.x) {   // 16 float4 per expert row of 64 h
+        const int e = i / 16, v = i % 16;
+        const float4 q = *reinterpret_cast<const float4 *>(&s_out[e][v * 4]);
+        *reinterpret_cast<float4 *>(a.part + ((size_t)sp * a.E + e) * a.H + hb + v * 4) = q;
     }
 }
 
+// dW_r[h][e] (+)= sum over splits in increasing order; thread per (e, h), h fastest,
+// eight split loads in flight at a time.
 __global__ void router_wgrad_reduce_kernel(RouterWgradArgs a) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= a.H * a.E) return;
+    const int e = i / a.H, h = i % a.H;
+    const size_t stride = (size_t)a.E * a.H;
     float v = 0.0f;
-    for (int sp = 0; sp < a.splits; ++sp) v += a.part[(size_t)sp * a.H * a.E + i];
-    a.dWr[i] = a.accumulate ? a.dWr[i] + v : v;
+    for (int sp0 = 0; sp0 < a.splits; sp0 += 8) {
+        float p[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) p[u] = sp0 + u < a.splits ? __ldg(a.part + (size_t)(sp0 + u) * stride + i) : 0.0f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v += p[u];
+    }
+    const size_t o = (size_t)h * a.E + e;
+    a.dWr[o] = a.accumulate ? a.dWr[o] + v : v;
 }
 
 cudaError_t launch_router_bwd_dlogits(const RouterBwdArgs &rb, cudaStream_t s) {
@@ -736,6 +850,7 @@ cudaError_t launch_router_bwd_dlogits(const RouterBwdArgs &rb, cudaStream_t s) {
 
 cudaError_t launch_reverse_dispatch(const RevDispatchArgs &rd, cudaStream_t s) {
     if (rd.T > 0) {
+        // 128 registers: four blocks per SM, so the usual grid fits in one wave
         reverse_dispatch_kernel<<<dim3(ceil_div(rd.T, kRdTokens), rd.H / 256), 128, 0, s>>>(rd);
     }
     return cudaGetLastError();
@@ -743,7 +858,7 @@ cudaError_t launch_reverse_dispatch(const RevDispatchArgs &rd, cudaStream_t s) {
 
 cudaError_t launch_router_wgrad(const RouterWgradArgs &rw, cudaStream_t s) {
     dim3 grid(rw.H / 64, rw.splits);
-    router_wgrad_part_kernel<<<grid, 32 * ceil_div(rw.E, 8), 0, s>>>(rw);
+    router_wgrad_part_kernel<<<grid, 128, 0, s>>>(rw);
     router_wgrad_reduce_kernel<<<ceil_div(rw.H * rw.E, 256), 256, 0, s>>>(rw);
     return cudaGetLastError();
 }

@@ -70,7 +70,7 @@ struct RevDispatchArgs {
 struct RouterWgradArgs {
     const bf16 *x;
     const float *dlogits;
-    float *part;            // [splits, H, E]
+    float *part;            // [splits, E, H]
     float *dWr;
     int T, H, E, splits, accumulate;
 };
