@@ -485,14 +485,15 @@ __device__ __forceinline__ float sigmoid_f(float a) { return __fdividef(1.0f, 1.
 __device__ __forceinline__ float silu_f(float a) { return a * sigmoid_f(a); }
 
 // 32 rows (one per lane) x 32 bf16 of this warp -> a 2 KB staging buffer (plain
-// row-major, 64 B per row) -> one TMA store at (col0, row0) of map m. Four
-// buffers per warp rotate; a buffer is reused once the store issued four
+// row-major, 64 B per row) -> one TMA store at (col0, row0) of map m. NBUF
+// buffers per warp rotate; a buffer is reused once the store issued NBUF
 // stores earlier has read it.
+template <int NBUF = 4>
 __device__ __forceinline__ void stage_store_bf16(uint8_t *warp_stage, int &nstores, const uint32_t (&w)[16],
                                                  const CUtensorMap *m, int col0, int row0, int lane) {
-    uint8_t *buf = warp_stage + (nstores & 3) * 2048;
-    if (nstores >= 4) {
-        if (lane == 0) bulk_wait_group_read<3>();
+    uint8_t *buf = warp_stage + (nstores % NBUF) * 2048;
+    if (nstores >= NBUF) {
+        if (lane == 0) bulk_wait_group_read<NBUF - 1>();
         __syncwarp();
     }
 #pragma unroll
@@ -510,10 +511,17 @@ __device__ __forceinline__ void stage_store_bf16(uint8_t *warp_stage, int &nstor
 // PAIR: the CTA pair computes a 256-row tile; this CTA's accumulator holds
 // rows [128 * rank, +128). A half beyond its expert's run (odd number of
 // 128-row tiles) is computed on whatever rows follow and not stored.
-template <int OP, bool FP8, bool PAIR = false, class Ctl>
+// EW = epilogue warps (warps 2 .. 2+EW): with 8, two warps read each TMEM lane
+// quarter and split the tile's columns (GEMM2 dgrad: its SwiGLU backward is
+// latency-bound with one warp per SM sub-partition). Each warp owns
+// 32 KB / EW of staging.
+template <int OP, bool FP8, bool PAIR = false, int EW = 4, class Ctl>
 __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *tfull, uint64_t *tempty,
                               uint32_t tmem, const WaitCtl &ctl, uint8_t *staging = nullptr) {
+    static_assert(EW == 4 || EW == 8, "epilogue warps");
+    constexpr int NBUF = EW == 8 ? 2 : 4;     // 2 KB staging buffers per warp
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int half = EW == 8 ? (warp - 2) / 4 : 0;   // column half of the tile this warp takes
     const int quarter = warp & 3;             // TMEM lanes this warp may read
     const int r = quarter * 32 + lane;        // accumulator row of this thread
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
@@ -524,7 +532,7 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
     const int rank = PAIR ? (int)cluster_ctarank() : 0;
     int store_chunks = 0;   // TMA stores issued by this warp (lane 0 tracks the bulk groups)
     const bool tma_bf16 = !FP8 && staging != nullptr && g.tma_store && OP != OP_WG2 && OP != OP_WG13;
-    uint8_t *warp_stage = staging ? staging + (warp - 2) * 8192 : nullptr;
+    uint8_t *warp_stage = staging ? staging + (warp - 2) * (NBUF * 2048) : nullptr;
     const int t0 = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
     const int tstep = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
     for (int t = t0; t < total; t += tstep) {
@@ -570,9 +578,9 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                 }
                 if (tma_bf16) {
                     const int row0 = ti.g0 + quarter * 32, col0 = ti.nt * 128 + cc * 32;
-                    stage_store_bf16(warp_stage, store_chunks, oa, &g.om0, col0, row0, lane);
-                    stage_store_bf16(warp_stage, store_chunks, ob, &g.om1, col0, row0, lane);
-                    stage_store_bf16(warp_stage, store_chunks, oh, &g.om2, col0, row0 + ring_shift, lane);
+                    stage_store_bf16<NBUF>(warp_stage, store_chunks, oa, &g.om0, col0, row0, lane);
+                    stage_store_bf16<NBUF>(warp_stage, store_chunks, ob, &g.om1, col0, row0, lane);
+                    stage_store_bf16<NBUF>(warp_stage, store_chunks, oh, &g.om2, col0, row0 + ring_shift, lane);
                 } else {
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
@@ -608,7 +616,7 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                 for (int i = 0; i < 16; ++i) o[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
                 if (tma_bf16) {
                     const int row0 = (int)(orow - r) + quarter * 32;
-                    stage_store_bf16(warp_stage, store_chunks, o, &g.om0, ti.nt * BN + cc * 32, row0, lane);
+                    stage_store_bf16<NBUF>(warp_stage, store_chunks, o, &g.om0, ti.nt * BN + cc * 32, row0, lane);
                 } else {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
@@ -626,16 +634,18 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
             bf16 *pdb = g.o1 + grow * F + ti.nt * BN;
             bf16 *phw = g.o2 + grow * F + ti.nt * BN;
             float dwp = 0.0f;
+            constexpr int NCH = BN / 32 / (EW / 4);   // 32-column chunks of this warp
+            const int cc0 = half * NCH, cc1 = cc0 + NCH;
             // saved a, b of the next 32 columns are loaded one chunk ahead so their
             // latency overlaps the current chunk's work
             uint4 na[4], nb[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                na[q] = ld_nc_v4(pa + q * 8);
-                nb[q] = ld_nc_v4(pb + q * 8);
+                na[q] = ld_nc_v4(pa + cc0 * 32 + q * 8);
+                nb[q] = ld_nc_v4(pb + cc0 * 32 + q * 8);
             }
 #pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
+            for (int cc = cc0; cc < cc1; ++cc) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tbase + cc * 32, v);
                 uint32_t ra[16], rb[16];
@@ -644,7 +654,7 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                     ra[4 * q] = na[q].x; ra[4 * q + 1] = na[q].y; ra[4 * q + 2] = na[q].z; ra[4 * q + 3] = na[q].w;
                     rb[4 * q] = nb[q].x; rb[4 * q + 1] = nb[q].y; rb[4 * q + 2] = nb[q].z; rb[4 * q + 3] = nb[q].w;
                 }
-                if (cc + 1 < BN / 32) {
+                if (cc + 1 < cc1) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         na[q] = ld_nc_v4(pa + (cc + 1) * 32 + q * 8);
@@ -692,9 +702,9 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                 }
                 if (tma_bf16) {
                     const int row0 = ti.g0 + quarter * 32, col0 = ti.nt * BN + cc * 32;
-                    stage_store_bf16(warp_stage, store_chunks, oda, &g.om0, col0, row0, lane);
-                    stage_store_bf16(warp_stage, store_chunks, odb, &g.om1, col0, row0, lane);
-                    stage_store_bf16(warp_stage, store_chunks, ohw, &g.om2, col0, row0, lane);
+                    stage_store_bf16<NBUF>(warp_stage, store_chunks, oda, &g.om0, col0, row0, lane);
+                    stage_store_bf16<NBUF>(warp_stage, store_chunks, odb, &g.om1, col0, row0, lane);
+                    stage_store_bf16<NBUF>(warp_stage, store_chunks, ohw, &g.om2, col0, row0, lane);
                     continue;
                 }
 #pragma unroll
@@ -704,7 +714,14 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                     st_v4(phw + cc * 32 + q * 8, make_uint4(ohw[4 * q], ohw[4 * q + 1], ohw[4 * q + 2], ohw[4 * q + 3]));
                 }
             }
-            g.of0[(size_t)grow * (g.F / BN) + ti.nt] = dwp;
+            // dw partials: one per 128 columns of F, [row][F / 128]
+            float *dwo = g.of0 + (size_t)grow * (g.F / 128) + ti.nt * 2;
+            if (EW == 8) {
+                dwo[half] = dwp;
+            } else {
+                dwo[0] = dwp;
+                dwo[1] = 0.0f;
+            }
         } else {   // OP_WG2, OP_WG13: fp32 weight gradients
             const bool empty_k = ti.nk == 0;
             const int row = ti.mt * BM + r;
@@ -787,7 +804,7 @@ template <int OP, bool FP8>
 __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *staging = FP8 ? nullptr : tiles + STAGES * stage_stride<FP8>();   // bf16: 4 warps x 8 KB
+    uint8_t *staging = FP8 ? nullptr : tiles + STAGES * stage_stride<FP8>();   // bf16: 32 KB over the epilogue warps
     SmemCtl &c = *reinterpret_cast<SmemCtl *>(tiles + STAGES * stage_stride<FP8>() + (FP8 ? 0 : P_STAGING_1));
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     WaitCtl ctl{g.status, g.budget_ns};
@@ -800,7 +817,7 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&c.tfull[a]), 1);
-            mbar_init(smem_u32(&c.tempty[a]), 128);
+            mbar_init(smem_u32(&c.tempty[a]), OP == OP_BWD2 ? 256 : 128);   // epilogue threads
         }
         mbar_init(smem_u32(&c.drain), 1);
         fence_mbar_init();
@@ -822,6 +839,8 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         if (lane == 0) producer_loop<OP, FP8>(g, c, tiles, c.full, c.empty, ctl);
     } else if (warp == 1) {
         if (lane == 0) mma_loop<OP, FP8>(g, c, tiles, c.full, c.empty, c.tfull, c.tempty, &c.drain, tmem, ctl);
+    } else if constexpr (OP == OP_BWD2) {
+        epilogue_loop<OP, FP8, false, 8>(g, c, c.tfull, c.tempty, tmem, ctl, staging);   // warps 2-9
     } else if (warp < 6) {
         epilogue_loop<OP, FP8>(g, c, c.tfull, c.tempty, tmem, ctl, staging);
     } else {
@@ -1066,7 +1085,7 @@ cudaError_t launch_op(const GemmArgs &g, int grid, cudaStream_t stream) {
     cudaError_t err =
         cudaFuncSetAttribute(grouped_gemm_kernel<OP, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    grouped_gemm_kernel<OP, FP8><<<grid, (OP == OP_FWD1 && g.fused) ? 320 : 192, smem, stream>>>(g);
+    grouped_gemm_kernel<OP, FP8><<<grid, ((OP == OP_FWD1 && g.fused) || OP == OP_BWD2) ? 320 : 192, smem, stream>>>(g);
     return cudaGetLastError();
 }
 

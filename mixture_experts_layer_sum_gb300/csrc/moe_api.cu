@@ -183,7 +183,7 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     L.w_db = take(rp * 2 * F);
     L.w_hw = take(rp * 2 * F);
     L.w_dXs = take(rp * 2 * H);
-    L.w_dwpart = take(4 * rp * (F / 256));
+    L.w_dwpart = take(4 * rp * (F / 128));
     L.w_dlogits = take(4 * T * E);
     L.w_dwr_part = take(4 * (size_t)L.dwr_splits * H * E);
     if (mx) {
@@ -811,7 +811,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
     }
     // 3. router backward, reverse dispatch, router weight gradient
     RouterBwdArgs rb{};
-    rb.dw_part = dwpart; rb.nparts = L.F / 256; rb.slot_row = s_slot_row; rb.ids = s_ids; rb.w = s_w;
+    rb.dw_part = dwpart; rb.nparts = L.F / 128; rb.slot_row = s_slot_row; rb.ids = s_ids; rb.w = s_w;
     rb.probs = s_probs; rb.dlogits = dlogits; rb.T = L.T; rb.k = L.k; rb.E = L.E;
     RevDispatchArgs rd{};
     rd.dXs = dXs; rd.slot_row = s_slot_row; rd.dlogits = dlogits; rd.Wr = (const bf16 *)W_r; rd.dx = (bf16 *)dx;
