@@ -98,9 +98,14 @@ def cpu_baseline(w, inp, target_s=15.0):
     ntok = int(min(w.T, max(256, target_s / max(per_tok, 1e-9))))
     ntok = max(256, ntok // 256 * 256)
     t = oracle_step(w, inp, ntok)
-    return {"value": ntok / t, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"fwd+bwd of the first {ntok} of {w.T} tokens of {w.name}, all weights, float64 numpy "
-                      f"(BLAS threads = host cores), {t:.1f} s"}
+    # a workload smaller than the time budget is passed over again until about 10 s of CPU work
+    passes = 1
+    while t < 10.0 and passes < 16:
+        t += oracle_step(w, inp, ntok)
+        passes += 1
+    return {"value": ntok * passes / t, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"{passes} x fwd+bwd of the first {ntok} of {w.T} tokens of {w.name}, all weights, "
+                      f"float64 numpy (BLAS threads = host cores), {t:.1f} s"}
 
 
 def run_reference(args, w):
