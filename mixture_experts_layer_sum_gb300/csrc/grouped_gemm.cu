@@ -508,6 +508,29 @@ __device__ __forceinline__ void stage_store_bf16(uint8_t *warp_stage, int &nstor
     ++nstores;
 }
 
+// 32 rows (one per lane) x 32 bf16 of this warp -> a 2 KB staging buffer in the
+// blocked order of blk32_offset (conflict-free: lanes write consecutive 16 B) -> one
+// contiguous bulk copy to the block at dst. Shares the buffer rotation of stage_store_bf16.
+template <int NBUF = 4>
+__device__ __forceinline__ void stage_store_blk(uint8_t *warp_stage, int &nstores, const uint32_t (&w)[16],
+                                                bf16 *dst, int lane) {
+    uint8_t *buf = warp_stage + (nstores % NBUF) * 2048;
+    if (nstores >= NBUF) {
+        if (lane == 0) bulk_wait_group_read<NBUF - 1>();
+        __syncwarp();
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4 *>(buf + (q * 32 + lane) * 16) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+        bulk_store(dst, smem_u32(buf), 2048);
+        bulk_commit_group();
+    }
+    ++nstores;
+}
+
 // PAIR: the CTA pair computes a 256-row tile; this CTA's accumulator holds
 // rows [128 * rank, +128). A half beyond its expert's run (odd number of
 // 128-row tiles) is computed on whatever rows follow and not stored.
@@ -554,8 +577,7 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
         } else if constexpr (OP == OP_FWD1) {
             const int grow = ti.g0 + r;
             const size_t F = g.F;
-            bf16 *pa = g.o0 + grow * F + ti.nt * 128;
-            bf16 *pb = g.o1 + grow * F + ti.nt * 128;
+            const int brow = ti.g0 + quarter * 32;   // first row of this warp's 32-row blocks of a, b
             bf16 *ph = FP8 ? nullptr : g.o2 + (size_t)(grow + ring_shift) * F + ti.nt * 128;
 #pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
@@ -576,16 +598,17 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                     hf[2 * i + 1] = silu_f(a1) * b1;
                     oh[i] = pack_bf16x2(hf[2 * i], hf[2 * i + 1]);
                 }
+                const int col0 = ti.nt * 128 + cc * 32;
+                bf16 *ba = g.o0 + blk32_offset(brow, col0, g.F), *bb = g.o1 + blk32_offset(brow, col0, g.F);
                 if (tma_bf16) {
-                    const int row0 = ti.g0 + quarter * 32, col0 = ti.nt * 128 + cc * 32;
-                    stage_store_bf16<NBUF>(warp_stage, store_chunks, oa, &g.om0, col0, row0, lane);
-                    stage_store_bf16<NBUF>(warp_stage, store_chunks, ob, &g.om1, col0, row0, lane);
-                    stage_store_bf16<NBUF>(warp_stage, store_chunks, oh, &g.om2, col0, row0 + ring_shift, lane);
+                    stage_store_blk<NBUF>(warp_stage, store_chunks, oa, ba, lane);
+                    stage_store_blk<NBUF>(warp_stage, store_chunks, ob, bb, lane);
+                    stage_store_bf16<NBUF>(warp_stage, store_chunks, oh, &g.om2, col0, brow + ring_shift, lane);
                 } else {
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
-                        st_v4(pa + cc * 32 + v * 8, make_uint4(oa[4 * v], oa[4 * v + 1], oa[4 * v + 2], oa[4 * v + 3]));
-                        st_v4(pb + cc * 32 + v * 8, make_uint4(ob[4 * v], ob[4 * v + 1], ob[4 * v + 2], ob[4 * v + 3]));
+                        st_v4(ba + (v * 32 + lane) * 8, make_uint4(oa[4 * v], oa[4 * v + 1], oa[4 * v + 2], oa[4 * v + 3]));
+                        st_v4(bb + (v * 32 + lane) * 8, make_uint4(ob[4 * v], ob[4 * v + 1], ob[4 * v + 2], ob[4 * v + 3]));
                         if constexpr (!FP8)
                             st_v4(ph + cc * 32 + v * 8, make_uint4(oh[4 * v], oh[4 * v + 1], oh[4 * v + 2], oh[4 * v + 3]));
                     }
@@ -628,8 +651,11 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
             const size_t F = g.F;
             const int slot = g.row_slot[grow];
             const float w = slot >= 0 ? g.wslot[slot] : 0.0f;
-            const bf16 *pa = g.in0 + grow * F + ti.nt * BN;
-            const bf16 *pb = g.in1 + grow * F + ti.nt * BN;
+            // saved a, b in 32 x 32 blocks: this lane's 16-byte vector j of chunk cc is
+            // at blk32_offset(block row, column) + (j * 32 + lane) * 8 elements
+            const int brow = ti.g0 + quarter * 32;
+            auto pa_at = [&](int cc) { return g.in0 + blk32_offset(brow, ti.nt * BN + cc * 32, g.F) + lane * 8; };
+            auto pb_at = [&](int cc) { return g.in1 + blk32_offset(brow, ti.nt * BN + cc * 32, g.F) + lane * 8; };
             bf16 *pda = g.o0 + grow * F + ti.nt * BN;
             bf16 *pdb = g.o1 + grow * F + ti.nt * BN;
             bf16 *phw = g.o2 + grow * F + ti.nt * BN;
@@ -641,8 +667,8 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
             uint4 na[4], nb[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                na[q] = ld_nc_v4(pa + cc0 * 32 + q * 8);
-                nb[q] = ld_nc_v4(pb + cc0 * 32 + q * 8);
+                na[q] = ld_nc_v4(pa_at(cc0) + q * 256);
+                nb[q] = ld_nc_v4(pb_at(cc0) + q * 256);
             }
 #pragma unroll 1
             for (int cc = cc0; cc < cc1; ++cc) {
@@ -657,8 +683,8 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                 if (cc + 1 < cc1) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        na[q] = ld_nc_v4(pa + (cc + 1) * 32 + q * 8);
-                        nb[q] = ld_nc_v4(pb + (cc + 1) * 32 + q * 8);
+                        na[q] = ld_nc_v4(pa_at(cc + 1) + q * 256);
+                        nb[q] = ld_nc_v4(pb_at(cc + 1) + q * 256);
                     }
                 }
                 tmem_ld_wait();

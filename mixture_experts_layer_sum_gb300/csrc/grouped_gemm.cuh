@@ -24,7 +24,7 @@ struct GemmArgs {
     int ring_base;
     bf16 *o0, *o1, *o2;           // bf16 outputs (see each op)
     float *of0, *of1;             // fp32 outputs
-    const bf16 *in0, *in1;        // BWD2: saved a, b
+    const bf16 *in0, *in1;        // BWD2: saved a, b (2 KB blocks, blk32_offset); FWD1 writes o0, o1 so
     const int *row_slot;          // BWD2: slot of each padded row (-1 = padding)
     const float *wslot;           // BWD2: router weight of each slot
     int accumulate;               // WG ops: add into the fp32 outputs

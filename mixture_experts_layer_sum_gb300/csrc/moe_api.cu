@@ -605,8 +605,8 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
             return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         g1.o2 = ringH;
         // epilogue tiles leave through shared memory and TMA stores
-        if (!make_map_bf16_out(&g1.om0, s_a, L.rows_pad_max, L.F) || !make_map_bf16_out(&g1.om1, s_b, L.rows_pad_max, L.F) ||
-            !make_map_bf16_out(&g1.om2, ringH, ring_rows, L.F) || !make_map_bf16_out(&g2.om0, ringY, ring_rows, L.H))
+        // a, b leave in 2 KB blocks by contiguous bulk copies (blk32_offset); h and Y by tensor stores
+        if (!make_map_bf16_out(&g1.om2, ringH, ring_rows, L.F) || !make_map_bf16_out(&g2.om0, ringY, ring_rows, L.H))
             return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         g1.tma_store = 1;
         g2.tma_store = 1;

@@ -71,6 +71,15 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
                  : "l"(p));
     return r;
 }
+// Saved a, b (GEMM1 outputs read back by the GEMM2 dgrad epilogue) are stored in
+// 32 x 32 blocks of 2 KB: block (row / 32, col / 32) of a [rows][C] matrix starts at
+// element ((row / 32) * (C / 32) + col / 32) * 1024; inside it, element (r, c) sits at
+// ((c / 8) * 32 + r) * 8 + c % 8, so the 16-byte vector j of the 32 rows of a block is
+// 512 contiguous bytes and a warp (lane = row) reads or writes it in one instruction.
+__host__ __device__ __forceinline__ size_t blk32_offset(int row, int col, int C) {
+    return ((size_t)(row >> 5) * (size_t)(C >> 5) + (size_t)(col >> 5)) * 1024;
+}
+
 __device__ __forceinline__ uint4 ld_v4(const void *p) {
     return *reinterpret_cast<const uint4 *>(p);
 }

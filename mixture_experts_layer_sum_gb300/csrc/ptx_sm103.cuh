@@ -135,6 +135,12 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, uint32_t src,
                  "r"(src), "r"(c0), "r"(c1)
                  : "memory");
 }
+// contiguous shared -> global bulk copy (addresses 16-byte aligned, size a multiple of 16),
+// tracked by the same bulk groups as the tensor stores
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(reinterpret_cast<uint64_t>(dst)), "r"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // wait until at most N committed groups still read their shared-memory source
 template <int N>
