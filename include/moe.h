@@ -157,7 +157,7 @@ moe_status_t moe_schedule(const moe_config_t *cfg, const int32_t *topk_ids,
  * library itself, reserved on every device that loads the library until the
  * process exits. The pages have no counterpart of this entry point.
  *   - Shapes whose schedule scratch (two histograms of (chunk, expert) counts
- *     plus the padded offsets, 1024 routed slots per chunk) exceeds the array
+ *     plus the padded offsets, 256 routed slots per chunk) exceeds the array
  *     return MOE_ERR_UNSUPPORTED.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.

@@ -12,8 +12,8 @@ namespace moe {
 
 constexpr int kMaxExperts = 64;
 constexpr int kRowPad = 128;          // each (macrobatch, expert) run of sorted rows is padded to this
-constexpr int kSchedChunk = 1024;     // routed slots per schedule block
-constexpr int kSchedWarps = 32;      // one 32-slot group per warp: every id load of a chunk in flight at once
+constexpr int kSchedChunk = 256;      // routed slots per schedule block
+constexpr int kSchedWarps = 8;       // one 32-slot group per warp: every id load of a chunk in flight at once
 constexpr int kMxBlock = 32;          // MXFP8 block along the contraction axis
 
 // status codes written to the device status word (values of moe_status_t)

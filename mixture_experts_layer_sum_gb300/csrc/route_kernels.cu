@@ -337,6 +337,74 @@ __device__ void block_exclusive_scan2(int &a, int &b, int *s_w /* [64] */) {
     b = ib - b + s_w[32 + warp];
 }
 
+// Scan with every intermediate in shared memory (used when nchunks*E + 3*nM*E + 2
+// ints fit the dynamic allocation): one coalesced read of the chunk counts, no
+// global round trips between the phases.
+__global__ void __launch_bounds__(1024) schedule_scan_smem_kernel(SchedArgs a) {
+    extern __shared__ int sm[];
+    __shared__ int s_tot[64];
+    const int n = a.nM * a.E, ncc = a.nchunks * a.E;
+    int *s_cc = sm;                  // [nchunks*E]: counts, then bases relative to the (m, e) start
+    int *s_cnt = s_cc + ncc;         // [n]
+    int *s_off = s_cnt + n;          // [n + 1] exclusive scan of the counts
+    int *s_offp = s_off + n + 1;     // [n + 1] exclusive scan of the 128-padded counts
+    for (int i = threadIdx.x; i < ncc; i += blockDim.x) s_cc[i] = a.chunk_counts[i];
+    __syncthreads();
+    for (int me = threadIdx.x; me < n; me += blockDim.x) {
+        const int m = me / a.E, e = me % a.E;
+        int run = 0;
+        for (int i = 0; i < a.chunks_per_mb; ++i) {
+            const int c = m * a.chunks_per_mb + i;
+            if (c >= a.nchunks) break;   // no slots (T = 0)
+            const int v = s_cc[c * a.E + e];
+            s_cc[c * a.E + e] = run;
+            run += v;
+        }
+        s_cnt[me] = run;
+    }
+    __syncthreads();
+    const int per = ceil_div(max(n, 1), (int)blockDim.x);
+    const int b0 = threadIdx.x * per, b1 = min(n, b0 + per);
+    int tot = 0, totp = 0;
+    for (int i = b0; i < b1; ++i) {
+        tot += s_cnt[i];
+        totp += (s_cnt[i] + kRowPad - 1) / kRowPad * kRowPad;
+    }
+    int run = tot, runp = totp;
+    block_exclusive_scan2(run, runp, s_tot);
+    for (int i = b0; i < b1; ++i) {
+        s_off[i] = run;
+        s_offp[i] = runp;
+        run += s_cnt[i];
+        runp += (s_cnt[i] + kRowPad - 1) / kRowPad * kRowPad;
+    }
+    if (threadIdx.x == blockDim.x - 1) { s_off[n] = run; s_offp[n] = runp; }
+    if (n == 0 && threadIdx.x == 0) { s_off[0] = 0; s_offp[0] = 0; }
+    __syncthreads();
+    for (int me = threadIdx.x; me < n; me += blockDim.x) {
+        const int m = me / a.E, e = me % a.E;
+        a.counts[me] = s_cnt[me];
+        a.offsets[m * (a.E + 1) + e] = s_off[me];
+        if (e == a.E - 1) a.offsets[m * (a.E + 1) + a.E] = s_off[me] + s_cnt[me];
+        a.offp[me] = s_offp[me];
+    }
+    if (threadIdx.x == 0) a.offp[n] = s_offp[n];
+    for (int i = threadIdx.x; i < ncc; i += blockDim.x) {   // chunk bases -> absolute sorted positions
+        const int c = i / a.E, e = i % a.E;
+        a.chunk_base[i] = s_cc[i] + s_off[(c / a.chunks_per_mb) * a.E + e];
+    }
+    if (a.row_slot) {   // padding rows of every (m, e) run hold no slot: 128 candidates per run
+        for (int i = threadIdx.x; i < n * kRowPad; i += blockDim.x) {
+            const int me = i / kRowPad, r = s_offp[me] + s_cnt[me] + i % kRowPad;
+            if (r < s_offp[me + 1]) a.row_slot[r] = -1;
+        }
+    }
+}
+
+size_t schedule_scan_smem_bytes(const SchedArgs &a) {
+    return 4 * ((size_t)a.nchunks * a.E + 3 * (size_t)a.nM * a.E + 2);
+}
+
 __global__ void __launch_bounds__(1024) schedule_scan_kernel(SchedArgs a) {
     __shared__ int s_tot[64];
     const int n = a.nM * a.E;
@@ -412,7 +480,11 @@ __global__ void __launch_bounds__(kSchedWarps * 32) schedule_scatter_kernel(Sche
 
 cudaError_t launch_schedule(const SchedArgs &a, cudaStream_t s) {
     if (a.nchunks > 0) schedule_count_kernel<<<a.nchunks, kSchedWarps * 32, 0, s>>>(a);
-    schedule_scan_kernel<<<1, 1024, 0, s>>>(a);
+    const size_t scan_smem = schedule_scan_smem_bytes(a);
+    if (scan_smem <= 48 * 1024)
+        schedule_scan_smem_kernel<<<1, 1024, scan_smem, s>>>(a);
+    else
+        schedule_scan_kernel<<<1, 1024, 0, s>>>(a);
     if (a.nchunks > 0) schedule_scatter_kernel<<<a.nchunks, kSchedWarps * 32, 0, s>>>(a);
     return cudaGetLastError();
 }
