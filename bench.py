@@ -338,29 +338,66 @@ def run_ours(args, w):
     kernels = M.moe_profile_end()
     launches = sum(n for _, n, _ in kernels)
 
-    # end to end through the public API with host buffers: H2D of x and dout,
-    # fwd+bwd, D2H of out and dx, every step
+    # end to end through the public API with host buffers: every step copies its x and dout
+    # from pinned host memory to the device and reads its out and dx back. The copies run on
+    # their own streams and the device buffers are double-buffered, so step i+1's inputs
+    # arrive while step i computes, out leaves during the backward and dx during the next
+    # step (the usual input/output pipeline of a training or serving loop). The timed region
+    # runs from the first host-to-device copy to the end of the last device-to-host copy.
     hx = torch.empty(w.T, w.H, dtype=torch.bfloat16, pin_memory=True)
     hd = torch.empty_like(hx, pin_memory=True)
     hx.copy_(d["x"].cpu())
     hd.copy_(d["dout"].cpu())
-    hout = torch.empty_like(hx, pin_memory=True)
-    hdx = torch.empty_like(hx, pin_memory=True)
-    xin = torch.empty_like(d["x"])
-    din = torch.empty_like(d["dout"])
+    NB = 2
+    hout = [torch.empty_like(hx, pin_memory=True) for _ in range(NB)]
+    hdx = [torch.empty_like(hx, pin_memory=True) for _ in range(NB)]
+    xin = [torch.empty_like(d["x"]) for _ in range(NB)]
+    din = [torch.empty_like(d["dout"]) for _ in range(NB)]
+    outb = [torch.empty_like(out) for _ in range(NB)]
+    dxb = [torch.empty_like(dx) for _ in range(NB)]
+    h2d = torch.cuda.Stream(device=dev)
+    d2h = torch.cuda.Stream(device=dev)
 
-    def e2e_step():
-        xin.copy_(hx, non_blocking=True)
-        din.copy_(hd, non_blocking=True)
-        layer.forward(xin, d["Wr"], bias, d["W1"], d["W3"], d["W2"], out, ids, wts, stream=stream)
-        layer.backward(din, xin, d["Wr"], d["W1"], d["W3"], d["W2"], dx, dWr, dW1, dW3, dW2, stream=stream)
-        hout.copy_(out, non_blocking=True)
-        hdx.copy_(dx, non_blocking=True)
+    def e2e_run(k):
+        ev = lambda: torch.cuda.Event()
+        used = [None] * NB      # compute done with slot b (inputs free)
+        drained = [None] * NB   # outputs of slot b read back (output buffers free)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(h2d)
+        for i in range(k):
+            b = i % NB
+            with torch.cuda.stream(h2d):
+                if used[b] is not None:
+                    h2d.wait_event(used[b])
+                xin[b].copy_(hx, non_blocking=True)
+                ex = ev(); ex.record(h2d)
+                din[b].copy_(hd, non_blocking=True)
+                ed = ev(); ed.record(h2d)
+            stream.wait_event(ex)
+            if drained[b] is not None:
+                stream.wait_event(drained[b])
+            layer.forward(xin[b], d["Wr"], bias, d["W1"], d["W3"], d["W2"], outb[b], ids, wts, stream=stream)
+            ef = ev(); ef.record(stream)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(ef)
+                hout[b].copy_(outb[b], non_blocking=True)
+            stream.wait_event(ed)
+            layer.backward(din[b], xin[b], d["Wr"], d["W1"], d["W3"], d["W2"], dxb[b], dWr, dW1, dW3, dW2,
+                           stream=stream)
+            eb = ev(); eb.record(stream)
+            used[b] = eb
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(eb)
+                hdx[b].copy_(dxb[b], non_blocking=True)
+                dr = ev(); dr.record(d2h)
+            drained[b] = dr
+        d2h.wait_event(t0)
+        t1.record(d2h)
+        torch.cuda.synchronize(dev)
+        return t0.elapsed_time(t1)
 
-    with torch.cuda.stream(stream):
-        e2e_step()
-    stream.synchronize()
-    e2e_ms = timed(e2e_step, args.steps)
+    e2e_run(2)
+    e2e_ms = e2e_run(args.steps)
     layer.status(stream)
     clocks = sampler.stop() if sampler is not None else stop_clocks(clk_p, clk_path)
 
@@ -441,7 +478,8 @@ def run_ours(args, w):
                     for nm, n_, ms_ in kt],
         "gpu_launches": launches,
         "e2e": {"value": ws * w.T * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": 2 * w.T * w.H * 2, "d2h_bytes_per_step": 2 * w.T * w.H * 2},
+                "h2d_bytes_per_step": 2 * w.T * w.H * 2, "d2h_bytes_per_step": 2 * w.T * w.H * 2,
+                "pipelined": "copy streams, double-buffered inputs/outputs; no L2 flush (weights exceed L2)"},
         "clocks": clocks,
     }
     if args.minibatch_sweep and w.minibatch_rows:
