@@ -836,7 +836,6 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
     WaitCtl ctl{g.status, g.budget_ns};
 
     if (threadIdx.x == 0) {
-        init_tile_table<OP, BM>(c, g);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&c.full[s]), 1);
             mbar_init(smem_u32(&c.empty[s]), 1);
@@ -856,9 +855,12 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         tmem_alloc(smem_u32(&c.tmem_base), 512);
         tmem_relinquish();
     }
+    pdl_wait();   // barriers and TMEM are set up while the previous kernel finishes
+    if (threadIdx.x == 0) init_tile_table<OP, BM>(c, g);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_trigger();
     const uint32_t tmem = c.tmem_base;
 
     if (warp == 0) {
@@ -1030,7 +1032,6 @@ __global__ void __launch_bounds__(320, 1) pair_gemm_kernel(const __grid_constant
     const uint32_t rank = cluster_ctarank();
     WaitCtl ctl{g.status, g.budget_ns};
     if (threadIdx.x == 0) {
-        init_tile_table<OP, 2 * BM>(c, g);
         for (int s = 0; s < PSTAGES; ++s) {
             mbar_init(smem_u32(&c.full[s]), 2);      // one arrive.expect_tx per CTA of the pair
             mbar_init(smem_u32(&c.empty[s]), 1);
@@ -1050,10 +1051,13 @@ __global__ void __launch_bounds__(320, 1) pair_gemm_kernel(const __grid_constant
         tmem_alloc_pair(smem_u32(&c.tmem_base), 512);
         tmem_relinquish_pair();
     }
+    pdl_wait();   // barriers and TMEM are set up while the previous kernel finishes
+    if (threadIdx.x == 0) init_tile_table<OP, 2 * BM>(c, g);
     tc_fence_before();
     __syncthreads();
     cluster_sync();      // the peer's barriers are initialised before any remote arrive
     tc_fence_after();
+    pdl_trigger();
     const uint32_t tmem = c.tmem_base;
     if (warp == 0) {
         if (lane == 0) pair_producer_loop<OP>(g, c, tiles, ctl);
@@ -1082,11 +1086,13 @@ cudaError_t launch_pair(const GemmArgs &g, int grid, cudaStream_t stream) {
     cfg.blockDim = dim3(fused ? 320 : 192);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     // A persistent grid must be fully co-resident: with GPCs of an odd SM count
     // not every SM can host half of a pair, so size the grid by the number of
@@ -1101,6 +1107,7 @@ cudaError_t launch_pair(const GemmArgs &g, int grid, cudaStream_t stream) {
         mc = n;
     }
     cfg.gridDim = dim3(2 * std::min(grid / 2, mc));
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<OP>, g);
 }
 
@@ -1111,8 +1118,8 @@ cudaError_t launch_op(const GemmArgs &g, int grid, cudaStream_t stream) {
     cudaError_t err =
         cudaFuncSetAttribute(grouped_gemm_kernel<OP, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    grouped_gemm_kernel<OP, FP8><<<grid, ((OP == OP_FWD1 && g.fused) || OP == OP_BWD2) ? 320 : 192, smem, stream>>>(g);
-    return cudaGetLastError();
+    return launch_pdl(grouped_gemm_kernel<OP, FP8>, dim3(grid), dim3(((OP == OP_FWD1 && g.fused) || OP == OP_BWD2) ? 320 : 192),
+                      smem, stream, g);
 }
 
 template <bool FP8>

@@ -163,7 +163,8 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     L.w_wrt = take(2 * EP * H);
     L.w_offp = take(4 * (nM * E + 1));
     L.mb_rows = (int)align_up((size_t)std::max(L.minibatch_rows, kRowPad), kRowPad);
-    L.w_ready = take(4 * ((size_t)L.half_rows / kRowPad + 2));   // per-minibatch ready rows + claim counter
+    // per macrobatch: per-minibatch ready rows + the claim counter (zeroed by the schedule scan)
+    L.w_ready = take(4 * (size_t)L.nM * ((size_t)L.half_rows / kRowPad + 2));
     const size_t region = o;
     const size_t ring_rows = (size_t)L.half_rows * L.ring_halves;
     // forward region: the ring
@@ -584,6 +585,8 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
     SchedArgs sa = sched_args(L, s_ids, ws, at<int32_t>(saved, L.s_counts), at<int32_t>(saved, L.s_offsets), s_offp,
                               at<int32_t>(saved, L.s_sorted2s), at<int32_t>(saved, L.s_s2sorted), s_slot_row,
                               s_row_slot);
+    sa.ready = at<int>(ws, L.w_ready);   // GEMM1's per-minibatch counters of every macrobatch
+    sa.ready_n = L.nM * (L.half_rows / kRowPad + 2);
     {
         ProfScope ps("schedule", s);
         st = cuda_check(launch_schedule(sa, s), "schedule launch");
@@ -630,14 +633,13 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
     // minibatch and GEMM1 tiles start as soon as their minibatch is complete
     int *ready = at<int>(ws, L.w_ready);
     g1.fused = 1; g1.xsrc = (const bf16 *)x; g1.row_slot = s_row_slot; g1.k = L.k; g1.mb_rows = L.mb_rows;
-    g1.ready = ready;
+    const int ready_stride = L.half_rows / kRowPad + 2;
     g1.ready_slots = L.half_rows / kRowPad + 1;
     if (!mx) g1.ringx = ringX;
     else { g1.ringxq = ringXq; g1.ringxs = ringXs; }
     for (int m = 0; m < L.nM; ++m) {
         const int ring_base = (m % L.ring_halves) * L.half_rows;
-        st = cuda_check(cudaMemsetAsync(ready, 0, 4 * ((size_t)L.half_rows / kRowPad + 2), s), "ready clear");
-        if (st != MOE_OK) return st;
+        g1.ready = ready + (size_t)m * ready_stride;   // zeroed by the schedule scan
         g1.m = m; g1.ring_base = ring_base;
         {
             ProfScope ps("grouped_gemm_fwd1_swiglu", s);

@@ -1,6 +1,7 @@
 // Shared definitions of the MoE layer kernels: sizes, buffer layouts inside
 // the caller's workspace / saved buffers, and small device helpers.
 #pragma once
+#include <utility>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -80,6 +81,15 @@ __host__ __device__ __forceinline__ size_t blk32_offset(int row, int col, int C)
     return ((size_t)(row >> 5) * (size_t)(C >> 5) + (size_t)(col >> 5)) * 1024;
 }
 
+// Programmatic dependent launch: every kernel of the layer is launched with
+// programmatic stream serialisation, so it may start while its predecessor on the
+// stream finishes. pdl_wait() (every thread, before the first read of anything an
+// earlier kernel wrote) blocks until the predecessor grid has completed and its memory
+// is visible; pdl_trigger() lets the successor launch (it then waits in its own
+// pdl_wait). Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint4 ld_v4(const void *p) {
     return *reinterpret_cast<const uint4 *>(p);
 }
@@ -132,6 +142,23 @@ __device__ __forceinline__ uint32_t mx_quant32(const float (&v)[32], uint32_t (&
     for (int i = 0; i < 8; ++i)
         codes[i] = cvt_e4m3x4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
     return (uint32_t)(s + 127);
+}
+
+// Launch with programmatic stream serialisation (see pdl_wait / pdl_trigger).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace moe

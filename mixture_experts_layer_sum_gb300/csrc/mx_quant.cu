@@ -19,6 +19,8 @@ namespace moe {
 // Warp per destination row; lane handles 8 consecutive elements (one 16-byte
 // load), a quad of lanes forms one 32-element block.
 __global__ void __launch_bounds__(256) mx_rows_kernel(MxRowsArgs a) {
+    pdl_wait();      // predecessor's outputs visible
+    pdl_trigger();   // let the next kernel launch
     const int lane = threadIdx.x % 32;
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
     const int nw = gridDim.x * blockDim.x / 32;
@@ -65,7 +67,8 @@ __global__ void __launch_bounds__(256) mx_rows_kernel(MxRowsArgs a) {
 cudaError_t launch_mx_rows(const MxRowsArgs &a, int max_rows, int num_sms, cudaStream_t s) {
     if (max_rows <= 0) return cudaSuccess;
     const int blocks = min(ceil_div(max_rows, 8), num_sms * 8);
-    mx_rows_kernel<<<blocks, 256, 0, s>>>(a);
+    cudaError_t e = launch_pdl(mx_rows_kernel, dim3(blocks), dim3(256), 0, s, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -73,6 +76,8 @@ cudaError_t launch_mx_rows(const MxRowsArgs &a, int max_rows, int num_sms, cudaS
 // memory; thread (c, b) quantises input rows [32b, 32b+32) of column c into one
 // 32-byte run of output row c.
 __global__ void __launch_bounds__(256) mx_transpose_kernel(MxTransposeArgs a) {
+    pdl_wait();      // predecessor's outputs visible
+    pdl_trigger();   // let the next kernel launch
     __shared__ __align__(16) bf16 tile[128][64 + 8];
     const int c0 = blockIdx.x * 64, rb0 = blockIdx.y * 128;
     const size_t bi = blockIdx.z;
@@ -109,7 +114,8 @@ __global__ void __launch_bounds__(256) mx_transpose_kernel(MxTransposeArgs a) {
 cudaError_t launch_mx_transpose(const MxTransposeArgs &a, int batch, cudaStream_t s) {
     if (a.R <= 0 || batch <= 0) return cudaSuccess;
     dim3 grid(a.C / 64, ceil_div(a.R, 128), batch);
-    mx_transpose_kernel<<<grid, 256, 0, s>>>(a);
+    cudaError_t e = launch_pdl(mx_transpose_kernel, grid, dim3(256), 0, s, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

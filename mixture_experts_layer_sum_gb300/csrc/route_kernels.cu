@@ -23,6 +23,8 @@ namespace moe {
 // tensor-core B fragments are contiguous along H.
 // One thread per output element (coalesced stores; the reads of W_r stride by E).
 __global__ void transpose_wr_kernel(const bf16 *__restrict__ Wr, bf16 *__restrict__ WrT, int H, int E, int EP) {
+    pdl_wait();      // predecessor's outputs visible
+    pdl_trigger();   // let the next kernel launch
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= H * EP) return;
     const int e = i / H, h = i % H;
@@ -48,6 +50,8 @@ constexpr int kRouterWarps = 8;     // warps split H
 // structure and fixed in order.
 template <int NT>
 __global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a) {
+    pdl_wait();      // predecessor's outputs visible
+    pdl_trigger();   // let the next kernel launch
     extern __shared__ float part[];   // [warps][kRouterTokens][EP]
     const int EP = NT * 8;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -195,14 +199,16 @@ cudaError_t launch_router(const RouterArgs &a, cudaStream_t s) {
     const int EP = (a.E + 7) / 8 * 8;
     const int blocks = ceil_div(a.T, kRouterTokens);
     const size_t smem = (size_t)kRouterWarps * kRouterTokens * EP * sizeof(float);
-    transpose_wr_kernel<<<ceil_div(a.H * EP, 256), 256, 0, s>>>(a.Wr, a.WrT, a.H, a.E, EP);
+    cudaError_t le = launch_pdl(transpose_wr_kernel, dim3(ceil_div(a.H * EP, 256)), dim3(256), 0, s, a.Wr, a.WrT, a.H, a.E, EP);
+    if (le != cudaSuccess) return le;
     if (blocks == 0) return cudaGetLastError();
 #define MOE_ROUTER_CASE(NT)                                                                           \
     case NT: {                                                                                       \
         cudaError_t e = cudaFuncSetAttribute(router_topk_kernel<NT>,                                 \
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
         if (e != cudaSuccess) return e;                                                              \
-        router_topk_kernel<NT><<<blocks, 256, smem, s>>>(a);                                         \
+        e = launch_pdl(router_topk_kernel<NT>, dim3(blocks), dim3(256), smem, s, a);                 \
+        if (e != cudaSuccess) return e;                                                              \
         break;                                                                                       \
     }
     switch (EP / 8) {
@@ -298,6 +304,8 @@ __device__ void chunk_pass(const SchedArgs &a, int c, int *s_warp_cnt /* [warps]
 }
 
 __global__ void __launch_bounds__(kSchedWarps * 32) schedule_count_kernel(SchedArgs a) {
+    pdl_wait();      // predecessor's outputs visible
+    pdl_trigger();   // let the next kernel launch
     __shared__ int s_cnt[kSchedWarps * kMaxExperts];
     chunk_pass<false>(a, blockIdx.x, s_cnt, nullptr);
     if (threadIdx.x < a.E) {
@@ -341,6 +349,8 @@ __device__ void block_exclusive_scan2(int &a, int &b, int *s_w /* [64] */) {
 // ints fit the dynamic allocation): one coalesced read of the chunk counts, no
 // global round trips between the phases.
 __global__ void __launch_bounds__(1024) schedule_scan_smem_kernel(SchedArgs a) {
+    pdl_wait();      // predecessor's outputs visible
+    pdl_trigger();   // let the next kernel launch
     extern __shared__ int sm[];
     __shared__ int s_tot[64];
     const int n = a.nM * a.E, ncc = a.nchunks * a.E;
@@ -349,6 +359,8 @@ __global__ void __launch_bounds__(1024) schedule_scan_smem_kernel(SchedArgs a) {
     int *s_off = s_cnt + n;          // [n + 1] exclusive scan of the counts
     int *s_offp = s_off + n + 1;     // [n + 1] exclusive scan of the 128-padded counts
     for (int i = threadIdx.x; i < ncc; i += blockDim.x) s_cc[i] = a.chunk_counts[i];
+    if (a.ready)
+        for (int i = threadIdx.x; i < a.ready_n; i += blockDim.x) a.ready[i] = 0;
     __syncthreads();
     for (int me = threadIdx.x; me < n; me += blockDim.x) {
         const int m = me / a.E, e = me % a.E;
@@ -406,7 +418,11 @@ size_t schedule_scan_smem_bytes(const SchedArgs &a) {
 }
 
 __global__ void __launch_bounds__(1024) schedule_scan_kernel(SchedArgs a) {
+    pdl_wait();      // predecessor's outputs visible
+    pdl_trigger();   // let the next kernel launch
     __shared__ int s_tot[64];
+    if (a.ready)
+        for (int i = threadIdx.x; i < a.ready_n; i += blockDim.x) a.ready[i] = 0;
     const int n = a.nM * a.E;
     // counts and chunk bases (relative to the (m,e) start); the chunk counts are
     // read eight at a time so their loads overlap
@@ -471,6 +487,8 @@ __global__ void __launch_bounds__(1024) schedule_scan_kernel(SchedArgs a) {
 }
 
 __global__ void __launch_bounds__(kSchedWarps * 32) schedule_scatter_kernel(SchedArgs a) {
+    pdl_wait();      // predecessor's outputs visible
+    pdl_trigger();   // let the next kernel launch
     __shared__ int s_cnt[kSchedWarps * kMaxExperts];
     __shared__ int s_base[kMaxExperts];
     if (threadIdx.x < a.E) s_base[threadIdx.x] = a.chunk_base[blockIdx.x * a.E + threadIdx.x];
@@ -479,13 +497,17 @@ __global__ void __launch_bounds__(kSchedWarps * 32) schedule_scatter_kernel(Sche
 }
 
 cudaError_t launch_schedule(const SchedArgs &a, cudaStream_t s) {
-    if (a.nchunks > 0) schedule_count_kernel<<<a.nchunks, kSchedWarps * 32, 0, s>>>(a);
+    cudaError_t e = cudaSuccess;
+    if (a.nchunks > 0 && (e = launch_pdl(schedule_count_kernel, dim3(a.nchunks), dim3(kSchedWarps * 32), 0, s, a)) != cudaSuccess)
+        return e;
     const size_t scan_smem = schedule_scan_smem_bytes(a);
     if (scan_smem <= 48 * 1024)
-        schedule_scan_smem_kernel<<<1, 1024, scan_smem, s>>>(a);
+        e = launch_pdl(schedule_scan_smem_kernel, dim3(1), dim3(1024), scan_smem, s, a);
     else
-        schedule_scan_kernel<<<1, 1024, 0, s>>>(a);
-    if (a.nchunks > 0) schedule_scatter_kernel<<<a.nchunks, kSchedWarps * 32, 0, s>>>(a);
+        e = launch_pdl(schedule_scan_kernel, dim3(1), dim3(1024), 0, s, a);
+    if (e != cudaSuccess) return e;
+    if (a.nchunks > 0 && (e = launch_pdl(schedule_scatter_kernel, dim3(a.nchunks), dim3(kSchedWarps * 32), 0, s, a)) != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 
@@ -494,6 +516,8 @@ cudaError_t launch_schedule(const SchedArgs &a, cudaStream_t s) {
 // Warp per padded row r in [offp[beg], offp[end]): dst[dst_row0 + r - offp[beg]]
 // = src[row_slot[r] / k], zeros for padding rows. 16-byte loads and stores.
 __global__ void __launch_bounds__(256) dispatch_rows_kernel(DispatchArgs a) {
+    pdl_wait();      // predecessor's outputs visible
+    pdl_trigger();   // let the next kernel launch
     const int lane = threadIdx.x % 32;
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
     const int nw = gridDim.x * blockDim.x / 32;
@@ -527,7 +551,8 @@ __global__ void __launch_bounds__(256) dispatch_rows_kernel(DispatchArgs a) {
 cudaError_t launch_dispatch(const DispatchArgs &a, int max_rows, int num_sms, cudaStream_t s) {
     if (max_rows <= 0) return cudaSuccess;
     int blocks = min(ceil_div(max_rows, 8), num_sms * 8);
-    dispatch_rows_kernel<<<blocks, 256, 0, s>>>(a);
+    cudaError_t e = launch_pdl(dispatch_rows_kernel, dim3(blocks), dim3(256), 0, s, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -536,6 +561,8 @@ cudaError_t launch_dispatch(const DispatchArgs &a, int max_rows, int num_sms, cu
 // Warp per token t in [t0, t1): out[t] = bf16( sum_{j=0}^{k-1} w[t,j] * Y[row(t,j)] ),
 // fp32 accumulation in fixed j order.
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
+    pdl_wait();      // predecessor's outputs visible
+    pdl_trigger();   // let the next kernel launch
     const int lane = threadIdx.x % 32;
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
     const int nw = gridDim.x * blockDim.x / 32;
@@ -594,7 +621,8 @@ cudaError_t launch_combine(const CombineArgs &a, int num_sms, cudaStream_t s) {
     const int n = a.t1 - a.t0;
     if (n <= 0) return cudaSuccess;
     int blocks = min(ceil_div(n, 8), num_sms * 8);
-    combine_kernel<<<blocks, 256, 0, s>>>(a);
+    cudaError_t e = launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, s, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -604,6 +632,8 @@ cudaError_t launch_combine(const CombineArgs &a, int num_sms, cudaStream_t s) {
 // order); dp_j = (dw_j - sum_i w_i dw_i) / S on the chosen experts, 0 elsewhere;
 // dlogits = p * (dp - sum_l p_l dp_l).
 __global__ void __launch_bounds__(256) router_bwd_kernel(RouterBwdArgs a) {
+    pdl_wait();      // predecessor's outputs visible
+    pdl_trigger();   // let the next kernel launch
     const int lane = threadIdx.x % 32;
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
     if (t >= a.T) return;
@@ -659,6 +689,8 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(RouterBwdArgs a) {
 // lane owns 32 contiguous h of one token for the 16-byte gathers of the k rows.
 constexpr int kRdTokens = 64;
 __global__ void __launch_bounds__(128, 4) reverse_dispatch_kernel(RevDispatchArgs a) {
+    pdl_wait();      // predecessor's outputs visible
+    pdl_trigger();   // let the next kernel launch
     __shared__ float s_acc[4][16][64 + 4];
     __shared__ __align__(16) bf16 s_wr[64][64 + 8];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -793,6 +825,8 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void *
                  : "r"((uint32_t)__cvta_generic_to_shared(p)));
 }
 __global__ void __launch_bounds__(128) router_wgrad_part_kernel(RouterWgradArgs a) {
+    pdl_wait();      // predecessor's outputs visible
+    pdl_trigger();   // let the next kernel launch
     __shared__ __align__(16) bf16 s_x[kWgTok][64 + kWgPad];
     __shared__ __align__(16) bf16 s_hi[kMaxExperts][kWgTok + kWgPad];
     __shared__ __align__(16) bf16 s_lo[kMaxExperts][kWgTok + kWgPad];
@@ -899,6 +933,8 @@ __global__ void __launch_bounds__(128) router_wgrad_part_kernel(RouterWgradArgs 
 // dW_r[h][e] (+)= sum over splits in increasing order; thread per (e, h), h fastest,
 // eight split loads in flight at a time.
 __global__ void router_wgrad_reduce_kernel(RouterWgradArgs a) {
+    pdl_wait();      // predecessor's outputs visible
+    pdl_trigger();   // let the next kernel launch
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= a.H * a.E) return;
     const int e = i / a.H, h = i % a.H;
@@ -916,22 +952,28 @@ __global__ void router_wgrad_reduce_kernel(RouterWgradArgs a) {
 }
 
 cudaError_t launch_router_bwd_dlogits(const RouterBwdArgs &rb, cudaStream_t s) {
-    if (rb.T > 0) router_bwd_kernel<<<ceil_div(rb.T, 8), 256, 0, s>>>(rb);
+    if (rb.T > 0) {
+        cudaError_t e = launch_pdl(router_bwd_kernel, dim3(ceil_div(rb.T, 8)), dim3(256), 0, s, rb);
+        if (e != cudaSuccess) return e;
+    }
     return cudaGetLastError();
 }
 
 cudaError_t launch_reverse_dispatch(const RevDispatchArgs &rd, cudaStream_t s) {
     if (rd.T > 0) {
         // 128 registers: four blocks per SM, so the usual grid fits in one wave
-        reverse_dispatch_kernel<<<dim3(ceil_div(rd.T, kRdTokens), rd.H / 256), 128, 0, s>>>(rd);
+        cudaError_t e = launch_pdl(reverse_dispatch_kernel, dim3(ceil_div(rd.T, kRdTokens), rd.H / 256), dim3(128), 0, s, rd);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_router_wgrad(const RouterWgradArgs &rw, cudaStream_t s) {
     dim3 grid(rw.H / 64, rw.splits);
-    router_wgrad_part_kernel<<<grid, 128, 0, s>>>(rw);
-    router_wgrad_reduce_kernel<<<ceil_div(rw.H * rw.E, 256), 256, 0, s>>>(rw);
+    cudaError_t e = launch_pdl(router_wgrad_part_kernel, grid, dim3(128), 0, s, rw);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(router_wgrad_reduce_kernel, dim3(ceil_div(rw.H * rw.E, 256)), dim3(256), 0, s, rw);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

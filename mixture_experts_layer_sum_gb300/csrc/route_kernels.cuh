@@ -28,6 +28,8 @@ struct SchedArgs {
     int32_t *sorted_to_slot, *slot_to_sorted;   // [T*k]
     int32_t *slot_row;      // optional [T*k] padded row of each slot
     int32_t *row_slot;      // optional [rows_pad_max] slot of each padded row
+    int *ready;             // optional [ready_n] GEMM1 minibatch counters, zeroed by the scan
+    int ready_n;
     int *status;
 };
 cudaError_t launch_schedule(const SchedArgs &a, cudaStream_t s);
