@@ -176,14 +176,21 @@ __device__ void init_tile_table(Ctl &c, const GemmArgs &g) {
 // (claims go in row order, so minibatches fill in order), gathers them and adds
 // 4 to ready[j] of their minibatch with release semantics. Any subset of running
 // CTAs can finish the gathering, so no CTA has to wait for another to start.
+// stop_bar (optional): the warp stops claiming once phase 0 of this mbarrier has
+// completed — the epilogue warps gather too until their CTA's first accumulator is ready.
 constexpr int kGatherRows = 4;
 template <bool FP8>
-__device__ void gather_loop(const GemmArgs &g) {
+__device__ void gather_loop(const GemmArgs &g, const uint64_t *stop_bar = nullptr) {
     const int lane = threadIdx.x % 32;
     const int r0 = g.offp[g.m * g.E], r1 = g.offp[(g.m + 1) * g.E];
     const int vecs = g.H / 8;
     int *claim = g.ready + g.ready_slots;    // row-chunk counter, after the ready counters
     for (;;) {
+        if (stop_bar) {
+            int done = 0;
+            if (lane == 0) done = mbar_try_wait(smem_u32(stop_bar), 0) ? 1 : 0;
+            if (__shfl_sync(0xffffffffu, done, 0)) break;
+        }
         int c = 0;
         if (lane == 0) c = atomicAdd(claim, 1);
         c = __shfl_sync(0xffffffffu, c, 0);
@@ -870,6 +877,9 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
     } else if constexpr (OP == OP_BWD2) {
         epilogue_loop<OP, FP8, false, 8>(g, c, c.tfull, c.tempty, tmem, ctl, staging);   // warps 2-9
     } else if (warp < 6) {
+        if constexpr (OP == OP_FWD1) {
+            if (g.fused) gather_loop<FP8>(g, &c.tfull[0]);   // until the first accumulator is ready
+        }
         epilogue_loop<OP, FP8>(g, c, c.tfull, c.tempty, tmem, ctl, staging);
     } else {
         if constexpr (OP == OP_FWD1) gather_loop<FP8>(g);
@@ -1064,6 +1074,9 @@ __global__ void __launch_bounds__(320, 1) pair_gemm_kernel(const __grid_constant
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) pair_mma_loop<OP>(g, c, tiles, tmem, ctl);
     } else if (warp < 6) {
+        if constexpr (OP == OP_FWD1) {
+            if (g.fused) gather_loop<false>(g, &c.tfull[0]);   // until the first accumulator is ready
+        }
         epilogue_loop<OP, false, true>(g, c, c.tfull, c.tempty, tmem, ctl, staging);
     } else {
         if constexpr (OP == OP_FWD1) gather_loop<false>(g);
