@@ -244,6 +244,25 @@ def gemm_bytes(w, name):
             "grouped_gemm_wgrad13": R * H * 2 + 2 * R * F * 2 + 2 * E * H * F * 4}.get(name)
 
 
+def layer_roofline(w, peaks, step_ms):
+    """Layer roofline time: the GEMMs' flops at the tensor peak plus the memory-bound stages'
+    algorithmic bytes at the HBM copy bandwidth, run back to back; frac = roofline / measured."""
+    tf = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    hbm = peaks.get("hbm_gbs")
+    if not tf or not hbm:
+        return None
+    if w.precision == "mxfp8":
+        tf = 2 * tf
+    gemm = ["grouped_gemm_fwd1_swiglu", "grouped_gemm_fwd2", "grouped_gemm_bwd2_swiglu", "grouped_gemm_bwd1",
+            "grouped_gemm_wgrad2", "grouped_gemm_wgrad13"]
+    mem = ["dispatch", "combine", "router_topk", "reverse_combine", "reverse_dispatch", "router_wgrad"]
+    t_gemm = sum(gemm_flops(w, n) for n in gemm) / (tf * 1e12)
+    t_mem = sum(kernel_bytes(w, n) for n in mem) / (hbm * 1e9)
+    t = (t_gemm + t_mem) * 1e3
+    return {"time_ms": t, "gemm_ms": t_gemm * 1e3, "hbm_ms": t_mem * 1e3, "frac": t / step_ms,
+            "note": "sum of GEMM flops / peak tensor rate and memory-stage algorithmic bytes / HBM copy bandwidth"}
+
+
 def run_ours(args, w):
     import torch
     ws, rank, local = dist_env()
@@ -474,8 +493,11 @@ def run_ours(args, w):
         "kernels": [dict({"name": nm, "launches": n_, "ms_per_step": ms_ / args.steps,
                           "share": ms_ / prof_ms},
                          **({"tflops": gemm_flops(w, nm) * args.steps / (ms_ * 1e-3) / 1e12} if gemm_flops(w, nm) else {}),
-                         **({"gbs": kernel_bytes(w, nm) * args.steps / (ms_ * 1e-3) / 1e9} if kernel_bytes(w, nm) else {}))
+                         **({"gbs": kernel_bytes(w, nm) * args.steps / (ms_ * 1e-3) / 1e9,
+                             "frac_of_hbm": kernel_bytes(w, nm) * args.steps / (ms_ * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+                            if kernel_bytes(w, nm) and peaks.get("hbm_gbs") else {}))
                     for nm, n_, ms_ in kt],
+        "layer_roofline": layer_roofline(w, peaks, total_ms / args.steps),
         "gpu_launches": launches,
         "e2e": {"value": ws * w.T * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * w.T * w.H * 2, "d2h_bytes_per_step": 2 * w.T * w.H * 2,
