@@ -1124,6 +1124,267 @@ cudaError_t launch_pair(const GemmArgs &g, int grid, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<OP>, g);
 }
 
+// ======================================================================
+// MXFP8 CTA-pair variant: 256-row tiles, block-scaled tcgen05.mma.cta_group::2.
+// Each CTA stages its 128 rows of A and one 128-row half of B (e4m3, 128 elements
+// of K per stage) plus three scale atoms: A's (its rows) and B's for BOTH halves,
+// because each CTA's tensor memory must hold SFB for all 256 columns. The atoms
+// are TMA loads of a [bytes / 128][128] view so that, like the tiles, they count
+// on the leader's full barrier. The leader's tcgen05.cp.cta_group::2 copies each
+// CTA's own atoms into its own tensor memory (SFA at column 256 + 16 stage, SFB at
+// +8 and +12); the accumulator is single-buffered (columns 0-255).
+constexpr int P8_STAGES = 6;
+constexpr uint32_t P8_TILE = 128 * 128;                        // 16 KiB: 128 rows x 128 B
+constexpr uint32_t P8_TX = 2 * P8_TILE + 3 * 512;              // bytes landing per CTA per stage
+constexpr uint32_t P8_STAGE = 34816;                           // 1 KiB aligned stage stride
+using Pair8Ctl = CtlT<P8_STAGES>;
+
+__device__ __forceinline__ int atom_row(int row, int k, int K) { return (int)(atom_at(row, k, K) / 128); }
+
+template <int OP>
+__device__ void pair8_producer_loop(const GemmArgs &g, const Pair8Ctl &c, uint8_t *tiles, const WaitCtl &ctl) {
+    const int rank = (int)cluster_ctarank();
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued[P8_STAGES] = {};
+    uint32_t last_phase[P8_STAGES] = {};
+    bool ok = true;
+    const int total = num_tiles<OP>(c, g);
+    const int a_shift = g.a_ring ? (g.ring_base - g.offp[g.m * g.E]) : 0;
+    const int KS = g.kstore;
+    int ready_mb = -1;
+    for (int t = blockIdx.x / 2; t < total && ok; t += gridDim.x / 2) {
+        TileInfo ti = decode_tile<OP, true, 2 * BM>(c, g, t);
+        const int row0 = ti.g0 + BM * rank;              // grouped-M: this CTA's 128 rows
+        const int m0 = (ti.mt * 2 + rank) * BM;          // grouped-K: this CTA's 128 rows of dW
+        if constexpr (OP == OP_FWD1) {
+            if (g.fused && row0 < c.seg_end[ti.e]) {
+                const int r0 = g.offp[g.m * g.E], nrows = g.offp[(g.m + 1) * g.E] - r0;
+                const int j = (row0 - r0) / g.mb_rows;
+                if (j != ready_mb) {
+                    const int need = min(g.mb_rows, nrows - j * g.mb_rows);
+                    if (!flag_wait_geq(g.ready + j, need, ctl)) { ok = false; break; }
+                    fence_proxy_async_global();
+                    ready_mb = j;
+                }
+            }
+        }
+        int run_m = 0, run_off = 0;
+        for (int kb = 0; kb < ti.nk; ++kb) {
+            int krow = 0;
+            if constexpr (OpTraits<OP>::grouped_k) {
+                for (;;) {
+                    const int s0 = g.offp[run_m * g.E + ti.e], s1 = g.offp[run_m * g.E + ti.e + 1];
+                    if (run_off < s1 - s0) { krow = s0 + run_off; break; }
+                    run_off = 0;
+                    ++run_m;
+                }
+                run_off += BK8;
+            }
+            if (!mbar_wait(smem_u32(&c.empty[stage]), phase ^ 1, ctl)) { ok = false; break; }
+            const uint32_t bar = mapa_shared(smem_u32(&c.full[stage]), 0);   // the leader's full barrier
+            const uint32_t sA = smem_u32(tiles + stage * P8_STAGE);
+            const uint32_t sB = sA + P8_TILE;
+            const uint32_t sSF = sB + P8_TILE;
+            mbar_arrive_expect_tx_cluster(bar, P8_TX);
+            if constexpr (OP == OP_FWD1) {
+                const int ar = row0 + a_shift, br = ti.e * g.F + ti.nt * 128, k0 = kb * BK8;
+                tma_load_2d_pair(sA, &g.a0, bar, k0, ar);
+                tma_load_2d_pair(sB, rank == 0 ? &g.b0 : &g.b1, bar, k0, br);   // W1^T half, W3^T half
+                tma_load_2d_pair(sSF, &g.msa0, bar, 0, atom_row(ar, k0, KS));
+                tma_load_2d_pair(sSF + 512, &g.msb0, bar, 0, atom_row(br, k0, KS));
+                tma_load_2d_pair(sSF + 1024, &g.msb1, bar, 0, atom_row(br, k0, KS));
+            } else if constexpr (OP == OP_FWD2 || OP == OP_BWD2) {
+                const int ar = row0 + a_shift, k0 = kb * BK8;
+                const int br = OP == OP_FWD2 ? ti.e * g.H + ti.nt * BN : ti.e * g.F + ti.nt * BN;
+                tma_load_2d_pair(sA, &g.a0, bar, k0, ar);
+                tma_load_2d_pair(sB, &g.b0, bar, k0, br + 128 * rank);
+                tma_load_2d_pair(sSF, &g.msa0, bar, 0, atom_row(ar, k0, KS));
+                tma_load_2d_pair(sSF + 512, &g.msb0, bar, 0, atom_row(br, k0, KS));
+                tma_load_2d_pair(sSF + 1024, &g.msb0, bar, 0, atom_row(br + 128, k0, KS));
+            } else if constexpr (OP == OP_BWD1) {
+                const int kf = g.F / BK8;
+                const bool second = kb >= kf;
+                const int k0 = (second ? kb - kf : kb) * BK8;
+                const int ar = row0 + a_shift, br = ti.e * g.H + ti.nt * BN;
+                const CUtensorMap *msb = second ? &g.msb1 : &g.msb0;
+                tma_load_2d_pair(sA, second ? &g.a1 : &g.a0, bar, k0, ar);
+                tma_load_2d_pair(sB, second ? &g.b1 : &g.b0, bar, k0, br + 128 * rank);
+                tma_load_2d_pair(sSF, second ? &g.msa1 : &g.msa0, bar, 0, atom_row(ar, k0, KS));
+                tma_load_2d_pair(sSF + 512, msb, bar, 0, atom_row(br, k0, KS));
+                tma_load_2d_pair(sSF + 1024, msb, bar, 0, atom_row(br + 128, k0, KS));
+            } else if constexpr (OP == OP_WG2) {
+                // A = (w h)^T [F][rows], B = dY^T [H][rows], both quantised along rows
+                const int n0 = ti.nt * BN;
+                tma_load_2d_pair(sA, &g.a0, bar, krow, m0);
+                tma_load_2d_pair(sB, &g.b0, bar, krow, n0 + 128 * rank);
+                tma_load_2d_pair(sSF, &g.msa0, bar, 0, atom_row(m0, krow, KS));
+                tma_load_2d_pair(sSF + 512, &g.msb0, bar, 0, atom_row(n0, krow, KS));
+                tma_load_2d_pair(sSF + 1024, &g.msb0, bar, 0, atom_row(n0 + 128, krow, KS));
+            } else if constexpr (OP == OP_WG13) {
+                // A = X^T [H][rows], B = [da^T | db^T] [F][rows]: rank 0 loads da, rank 1 db
+                const int n0 = ti.nt * 128;
+                tma_load_2d_pair(sA, &g.a0, bar, krow, m0);
+                tma_load_2d_pair(sB, rank == 0 ? &g.b0 : &g.b1, bar, krow, n0);
+                tma_load_2d_pair(sSF, &g.msa0, bar, 0, atom_row(m0, krow, KS));
+                tma_load_2d_pair(sSF + 512, &g.msb0, bar, 0, atom_row(n0, krow, KS));
+                tma_load_2d_pair(sSF + 1024, &g.msb1, bar, 0, atom_row(n0, krow, KS));
+            }
+            issued[stage] = 1;
+            last_phase[stage] = phase;
+            if (++stage == P8_STAGES) { stage = 0; phase ^= 1; }
+        }
+    }
+    if (!ok && rank == 0) {
+        for (int s = 0; s < P8_STAGES; ++s) {
+            if (!issued[s]) continue;
+            const uint32_t bar = smem_u32(&c.full[s]);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar, last_phase[s]) && globaltimer_ns() - t0 < ctl.budget_ns) {}
+        }
+    }
+}
+
+__device__ __forceinline__ void tmem_cp_pair_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+template <int OP>
+__device__ void pair8_mma_loop(const GemmArgs &g, Pair8Ctl &c, uint8_t *tiles, uint32_t tmem, const WaitCtl &ctl) {
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t acc_phase = 0;
+    const int total = num_tiles<OP>(c, g);
+    for (int t = blockIdx.x / 2; t < total; t += gridDim.x / 2) {
+        TileInfo ti = decode_tile<OP, true, 2 * BM>(c, g, t);
+        if (!mbar_wait(smem_u32(&c.tempty[0]), acc_phase ^ 1, ctl)) break;   // single accumulator
+        tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < ti.nk; ++kb) {
+            if (!mbar_wait(smem_u32(&c.full[stage]), phase, ctl)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sA = smem_u32(tiles + stage * P8_STAGE);
+            const uint32_t sB = sA + P8_TILE;
+            const uint32_t sSF = sB + P8_TILE;
+            const uint32_t t_sf = tmem + 256 + 16 * stage;
+            tmem_cp_pair_32x128b_x4(t_sf, sdesc_plain(sSF, 0, 128));
+            tmem_cp_pair_32x128b_x4(t_sf + 8, sdesc_plain(sSF + 512, 0, 128));
+            tmem_cp_pair_32x128b_x4(t_sf + 12, sdesc_plain(sSF + 1024, 0, 128));
+#pragma unroll
+            for (int kk = 0; kk < BK8 / 32; ++kk) {
+                const uint64_t ad = sdesc_sw128(sA + kk * 32, 16, 1024);
+                const uint64_t bd = sdesc_sw128(sB + kk * 32, 16, 1024);
+                mma_mxf8_pair(tmem, ad, bd, idesc_mxf8(2 * BM, BN, kk), t_sf, t_sf + 8, (kb | kk) != 0);
+            }
+            mma_commit_pair_mc(smem_u32(&c.empty[stage]));   // frees the stage in both CTAs
+            if (++stage == P8_STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit_pair_mc(smem_u32(&c.tfull[0]));
+        acc_phase ^= 1;
+    }
+    mma_commit_pair(smem_u32(&c.drain));
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(smem_u32(&c.drain), 0) && globaltimer_ns() - t0 < ctl.budget_ns) {}
+}
+
+template <int OP>
+__global__ void __launch_bounds__(320, 1) pair8_gemm_kernel(const __grid_constant__ GemmArgs g) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Pair8Ctl &c = *reinterpret_cast<Pair8Ctl *>(tiles + P8_STAGES * P8_STAGE);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    WaitCtl ctl{g.status, g.budget_ns};
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P8_STAGES; ++s) {
+            mbar_init(smem_u32(&c.full[s]), 2);      // one arrive.expect_tx per CTA of the pair
+            mbar_init(smem_u32(&c.empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&c.tfull[a]), 1);
+            mbar_init(smem_u32(&c.tempty[a]), 256);  // 128 epilogue threads of each CTA
+        }
+        mbar_init(smem_u32(&c.drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&g.a0);
+        tma_prefetch_map(&g.b0);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(&c.tmem_base), 512);
+        tmem_relinquish_pair();
+    }
+    pdl_wait();
+    if (threadIdx.x == 0) init_tile_table<OP, 2 * BM>(c, g);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();      // the peer's barriers are initialised before any remote arrive
+    tc_fence_after();
+    pdl_trigger();
+    const uint32_t tmem = c.tmem_base;
+    if (warp == 0) {
+        if (lane == 0) pair8_producer_loop<OP>(g, c, tiles, ctl);
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) pair8_mma_loop<OP>(g, c, tiles, tmem, ctl);
+    } else if (warp < 6) {
+        if constexpr (OP == OP_FWD1) {
+            if (g.fused) gather_loop<true>(g, &c.tfull[0]);   // until the first accumulator is ready
+        }
+        epilogue_loop<OP, true, true>(g, c, c.tfull, c.tempty, tmem, ctl, nullptr);
+    } else {
+        if constexpr (OP == OP_FWD1) gather_loop<true>(g);
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();      // the leader's MMAs are drained before the pair frees TMEM
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem, 512);
+}
+
+template <int OP>
+cudaError_t launch_pair8(const GemmArgs &g, int grid, cudaStream_t stream) {
+    constexpr size_t smem = P8_STAGES * P8_STAGE + sizeof(Pair8Ctl) + 1024;
+    static_assert(smem <= 227 * 1024, "shared memory budget");
+    cudaError_t err = cudaFuncSetAttribute(pair8_gemm_kernel<OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    const bool fused = OP == OP_FWD1 && g.fused;
+    cudaLaunchConfig_t cfg{};
+    cfg.blockDim = dim3(fused ? 320 : 192);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    static int max_clusters[2] = {0, 0};
+    int &mc = max_clusters[fused ? 1 : 0];
+    cfg.numAttrs = 1;
+    if (mc == 0) {
+        cfg.gridDim = dim3(grid / 2 * 2);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, pair8_gemm_kernel<OP>, &cfg) != cudaSuccess || n <= 0) n = grid / 2;
+        mc = n;
+    }
+    cfg.gridDim = dim3(2 * std::min(grid / 2, mc));
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, pair8_gemm_kernel<OP>, g);
+}
+
 template <int OP, bool FP8>
 cudaError_t launch_op(const GemmArgs &g, int grid, cudaStream_t stream) {
     constexpr size_t smem = STAGES * stage_stride<FP8>() + (FP8 ? 0 : P_STAGING_1) + sizeof(SmemCtl) + 1024;
@@ -1151,6 +1412,17 @@ cudaError_t launch_any(int op, const GemmArgs &g, int grid, cudaStream_t stream)
 }  // namespace
 
 cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream, bool fp8, bool pair) {
+    if (pair && fp8) {
+        switch (op) {
+            case OP_FWD1: return launch_pair8<OP_FWD1>(g, grid, stream);
+            case OP_FWD2: return launch_pair8<OP_FWD2>(g, grid, stream);
+            case OP_BWD2: return launch_pair8<OP_BWD2>(g, grid, stream);
+            case OP_BWD1: return launch_pair8<OP_BWD1>(g, grid, stream);
+            case OP_WG2: return launch_pair8<OP_WG2>(g, grid, stream);
+            case OP_WG13: return launch_pair8<OP_WG13>(g, grid, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     if (pair && !fp8 && op != OP_BWD2) {   // BWD2: heavy epilogue, phantom halves; 1-CTA tiles
         switch (op) {
             case OP_FWD1: return launch_pair<OP_FWD1>(g, grid, stream);

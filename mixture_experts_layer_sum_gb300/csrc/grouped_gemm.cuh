@@ -46,12 +46,16 @@ struct GemmArgs {
     int *ready;
     int ready_slots;
     int mb_rows, k;
+    // MXFP8 CTA-pair variant: the scale arrays viewed as [bytes / 128][128] bytes (no swizzle),
+    // so one 128 x 4 box is one 512-byte atom, loaded by TMA with completion on the pair
+    // leader's barrier: A atoms (msa0, msa1) and B atoms (msb0, msb1)
+    CUtensorMap msa0, msa1, msb0, msb1;
     int *status;
     unsigned long long budget_ns;
 };
 
-// pair = true (bf16 only): CTA-pair variant with 256-row tiles (cta_group::2);
-// the B maps of the K-major ops then need 128-row boxes.
+// pair = true: CTA-pair variant with 256-row tiles (cta_group::2); the B maps of the
+// K-major ops then need 128-row boxes (bf16 and MXFP8), MXFP8 also the atom maps above.
 cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream, bool fp8 = false,
                                 bool pair = false);
 

@@ -57,6 +57,10 @@ struct ProfScope {
 
 // bf16 grouped GEMMs run as CTA pairs (cta_group::2, 256-row tiles)
 constexpr bool kPairGemm = true;
+// MXFP8 CTA pairs (block-scaled cta_group::2); the GEMM2 dgrad keeps 1-CTA tiles with eight
+// epilogue warps (its quantising SwiGLU backward)
+constexpr bool kPairGemmFp8 = true;
+inline bool pair_fp8(int op) { return kPairGemmFp8 && op != OP_BWD2; }
 constexpr int kGemmBN1 = 256;   // GEMM1 tile: 128 rows x (128 a-columns + 128 b-columns)
 constexpr int kGemmBM = 128;
 
@@ -249,6 +253,21 @@ bool make_map_u8(CUtensorMap *m, const void *base, size_t rows, size_t cols, int
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// MXFP8 scale atoms of a [rows, K] operand stored as 512-byte atoms: the array viewed as
+// [bytes / 128][128] bytes, no swizzle; box 128 x 4 = one atom (row = byte offset / 128)
+bool make_map_atoms(CUtensorMap *m, const void *base, size_t bytes) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || bytes < 512) return false;
+    cuuint64_t dims[2] = {128, bytes / 128};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, 4};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -617,9 +636,15 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
         const QwLayout q = qw_layout(cfg);
         const uint8_t *qw = static_cast<const uint8_t *>(align_base(qweights));
         const size_t EF = (size_t)L.E * L.F, EH = (size_t)L.E * L.H;
+        const int kb2 = pair_fp8(OP_FWD2) ? 128 : 256;   // K-major B box: half of N per CTA of a pair
+        const size_t nw = (size_t)L.E * L.H * L.F / kMxBlock;   // scale bytes of one weight copy
         if (!make_map_u8(&g1.a0, ringXq, ring_rows, L.H, 128) || !make_map_u8(&g1.b0, qw + q.codes[QW_W1T], EF, L.H, 128) ||
             !make_map_u8(&g1.b1, qw + q.codes[QW_W3T], EF, L.H, 128) ||
-            !make_map_u8(&g2.a0, ringHq, ring_rows, L.F, 128) || !make_map_u8(&g2.b0, qw + q.codes[QW_W2T], EH, L.F, 256))
+            !make_map_u8(&g2.a0, ringHq, ring_rows, L.F, 128) || !make_map_u8(&g2.b0, qw + q.codes[QW_W2T], EH, L.F, kb2) ||
+            !make_map_atoms(&g1.msa0, ringXs, ring_rows * (L.H / kMxBlock)) ||
+            !make_map_atoms(&g1.msb0, qw + q.scales[QW_W1T], nw) || !make_map_atoms(&g1.msb1, qw + q.scales[QW_W3T], nw) ||
+            !make_map_atoms(&g2.msa0, ringHs, ring_rows * (L.F / kMxBlock)) ||
+            !make_map_atoms(&g2.msb0, qw + q.scales[QW_W2T], nw))
             return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         g1.sfa0 = ringXs; g1.sfb0 = qw + q.scales[QW_W1T]; g1.sfb1 = qw + q.scales[QW_W3T]; g1.kstore = L.H;
         g1.q0 = ringHq; g1.qs0 = ringHs;
@@ -643,13 +668,13 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
         g1.m = m; g1.ring_base = ring_base;
         {
             ProfScope ps("grouped_gemm_fwd1_swiglu", s);
-            st = cuda_check(launch_grouped_gemm(OP_FWD1, g1, L.num_sms, s, mx, kPairGemm && !mx), "GEMM1 launch");
+            st = cuda_check(launch_grouped_gemm(OP_FWD1, g1, L.num_sms, s, mx, mx ? pair_fp8(OP_FWD1) : kPairGemm), "GEMM1 launch");
         }
         if (st != MOE_OK) return st;
         g2.m = m; g2.ring_base = ring_base;
         {
             ProfScope ps("grouped_gemm_fwd2", s);
-            st = cuda_check(launch_grouped_gemm(OP_FWD2, g2, L.num_sms, s, mx, kPairGemm && !mx), "GEMM2 launch");
+            st = cuda_check(launch_grouped_gemm(OP_FWD2, g2, L.num_sms, s, mx, mx ? pair_fp8(OP_FWD2) : kPairGemm), "GEMM2 launch");
         }
         if (st != MOE_OK) return st;
         CombineArgs ca{};
@@ -740,13 +765,24 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
         const QwLayout q = qw_layout(cfg);
         const uint8_t *qw = static_cast<const uint8_t *>(align_base(qweights));
         auto u8 = [&](size_t off) { return at<uint8_t>(ws, off); };
-        if (!make_map_u8(&gb2.a0, u8(L.w_Ginq), rp, L.H, 128) || !make_map_u8(&gb2.b0, qw + q.codes[QW_W2Q], EF, L.H, 256) ||
+        // K-major B boxes: half of N per CTA of a pair (pair_fp8), the whole 256 otherwise
+        const int kbb2 = pair_fp8(OP_BWD2) ? 128 : 256, kbb1 = pair_fp8(OP_BWD1) ? 128 : 256;
+        const int kbw2 = pair_fp8(OP_WG2) ? 128 : 256;
+        const size_t nw = (size_t)L.E * L.H * L.F / kMxBlock;   // scale bytes of one weight copy
+        const size_t sh = rp * (L.H / kMxBlock), sf = rp * (L.F / kMxBlock);   // token-side scale bytes
+        if (!make_map_u8(&gb2.a0, u8(L.w_Ginq), rp, L.H, 128) || !make_map_u8(&gb2.b0, qw + q.codes[QW_W2Q], EF, L.H, kbb2) ||
             !make_map_u8(&gb1.a0, u8(L.w_daq), rp, L.F, 128) || !make_map_u8(&gb1.a1, u8(L.w_dbq), rp, L.F, 128) ||
-            !make_map_u8(&gb1.b0, qw + q.codes[QW_W1Q], EH, L.F, 256) ||
-            !make_map_u8(&gb1.b1, qw + q.codes[QW_W3Q], EH, L.F, 256) ||
-            !make_map_u8(&gw2.a0, u8(L.w_hwT), L.F, rp, 128) || !make_map_u8(&gw2.b0, u8(L.w_GinT), L.H, rp, 256) ||
+            !make_map_u8(&gb1.b0, qw + q.codes[QW_W1Q], EH, L.F, kbb1) ||
+            !make_map_u8(&gb1.b1, qw + q.codes[QW_W3Q], EH, L.F, kbb1) ||
+            !make_map_u8(&gw2.a0, u8(L.w_hwT), L.F, rp, 128) || !make_map_u8(&gw2.b0, u8(L.w_GinT), L.H, rp, kbw2) ||
             !make_map_u8(&gw13.a0, u8(L.w_XsT), L.H, rp, 128) || !make_map_u8(&gw13.b0, u8(L.w_daT), L.F, rp, 128) ||
-            !make_map_u8(&gw13.b1, u8(L.w_dbT), L.F, rp, 128))
+            !make_map_u8(&gw13.b1, u8(L.w_dbT), L.F, rp, 128) ||
+            !make_map_atoms(&gb2.msa0, u8(L.w_Ginq_s), sh) || !make_map_atoms(&gb2.msb0, qw + q.scales[QW_W2Q], nw) ||
+            !make_map_atoms(&gb1.msa0, u8(L.w_daq_s), sf) || !make_map_atoms(&gb1.msa1, u8(L.w_dbq_s), sf) ||
+            !make_map_atoms(&gb1.msb0, qw + q.scales[QW_W1Q], nw) || !make_map_atoms(&gb1.msb1, qw + q.scales[QW_W3Q], nw) ||
+            !make_map_atoms(&gw2.msa0, u8(L.w_hwT_s), sf) || !make_map_atoms(&gw2.msb0, u8(L.w_GinT_s), sh) ||
+            !make_map_atoms(&gw13.msa0, u8(L.w_XsT_s), sh) || !make_map_atoms(&gw13.msb0, u8(L.w_daT_s), sf) ||
+            !make_map_atoms(&gw13.msb1, u8(L.w_dbT_s), sf))
             return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         gb2.sfa0 = u8(L.w_Ginq_s); gb2.sfb0 = qw + q.scales[QW_W2Q]; gb2.kstore = L.H;
         gb2.q0 = u8(L.w_daq); gb2.qs0 = u8(L.w_daq_s); gb2.q1 = u8(L.w_dbq); gb2.qs1 = u8(L.w_dbq_s);
@@ -793,7 +829,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
             gb2.m = m;
             {
                 ProfScope ps("grouped_gemm_bwd2_swiglu", s);
-                st = cuda_check(launch_grouped_gemm(OP_BWD2, gb2, L.num_sms, s, mx, kPairGemm && !mx), "GEMM2 dgrad launch");
+                st = cuda_check(launch_grouped_gemm(OP_BWD2, gb2, L.num_sms, s, mx, mx ? pair_fp8(OP_BWD2) : kPairGemm), "GEMM2 dgrad launch");
             }
             if (st != MOE_OK) return st;
         }
@@ -806,7 +842,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
             gb1.m = m;
             {
                 ProfScope ps("grouped_gemm_bwd1", s);
-                st = cuda_check(launch_grouped_gemm(OP_BWD1, gb1, L.num_sms, s, mx, kPairGemm && !mx), "GEMM1 dgrad launch");
+                st = cuda_check(launch_grouped_gemm(OP_BWD1, gb1, L.num_sms, s, mx, mx ? pair_fp8(OP_BWD1) : kPairGemm), "GEMM1 dgrad launch");
             }
             if (st != MOE_OK) return st;
         }
@@ -848,13 +884,13 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
     }
     {
         ProfScope ps("grouped_gemm_wgrad2", s);
-        st = cuda_check(launch_grouped_gemm(OP_WG2, gw2, L.num_sms, s, mx, kPairGemm && !mx), "dW2 launch");
+        st = cuda_check(launch_grouped_gemm(OP_WG2, gw2, L.num_sms, s, mx, mx ? pair_fp8(OP_WG2) : kPairGemm), "dW2 launch");
     }
     if (st != MOE_OK) return st;
     gw13.Mw = L.H; gw13.N = L.F; gw13.of0 = dW1; gw13.of1 = dW3; gw13.accumulate = accumulate;
     {
         ProfScope ps("grouped_gemm_wgrad13", s);
-        st = cuda_check(launch_grouped_gemm(OP_WG13, gw13, L.num_sms, s, mx, kPairGemm && !mx), "dW1/dW3 launch");
+        st = cuda_check(launch_grouped_gemm(OP_WG13, gw13, L.num_sms, s, mx, mx ? pair_fp8(OP_WG13) : kPairGemm), "dW1/dW3 launch");
     }
     return st;
 }
