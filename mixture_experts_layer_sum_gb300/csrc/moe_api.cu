@@ -791,13 +791,19 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
         gw2.sfa0 = u8(L.w_hwT_s); gw2.sfb0 = u8(L.w_GinT_s); gw2.kstore = (int)rp;
         gw13.sfa0 = u8(L.w_XsT_s); gw13.sfb0 = u8(L.w_daT_s); gw13.sfb1 = u8(L.w_dbT_s); gw13.kstore = (int)rp;
     }
+    // a (macrobatch, expert) run holds each token of the macrobatch at most once, padded to kRowPad
+    const int seg_rows_max = (int)align_up((size_t)std::min(L.Mb, std::max(L.T, 1)), kRowPad);
     // token-axis MXFP8 copies: bf16 [rows][C] -> [C][rows] quantised along rows
     auto transpose_q = [&](const bf16 *src, size_t codes, size_t scales, int C, const char *name,
                            bool gather = false) {
         MxTransposeArgs a{};
         a.src = src; a.codes = at<uint8_t>(ws, codes); a.scales = at<uint8_t>(ws, scales);
         a.R = (int)rp; a.C = C; a.r_limit_ptr = s_offp + L.nM * L.E;
-        if (gather) { a.row_slot = s_row_slot; a.k = L.k; }
+        if (gather) {
+            // experts visited in step (see MxTransposeArgs) so each token row is read once from HBM
+            a.row_slot = s_row_slot; a.k = L.k;
+            a.offp = s_offp; a.ilv_E = L.E; a.ilv_nseg = L.nM * L.E; a.ilv_jb = seg_rows_max / kRowPad;
+        }
         ProfScope ps(name, s);
         return cuda_check(launch_mx_transpose(a, 1, s), "token-axis quantise launch");
     };
