@@ -127,7 +127,10 @@ size_t moe_workspace_size(const moe_config_t *cfg);
 
 /* Bytes of the forward->backward context written by moe_forward and read by
  * moe_backward (router ids/weights/probabilities, schedule maps, the bf16
- * FFN pre-activations a = x W1 and b = x W3 of every routed row). */
+ * FFN pre-activations a = x W1 and b = x W3 of every routed row; for bf16
+ * configs whose routed rows fit one macrobatch also the expert-sorted x rows
+ * the dispatch gathered, which the backward's dW1/dW3 then reads instead of
+ * gathering them again). */
 size_t moe_saved_size(const moe_config_t *cfg);
 
 /* Bytes of the MXFP8 weight copies made by moe_quantize_weights (0 for bf16). */

@@ -157,6 +157,10 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     L.s_row_slot = take(4 * rp);
     L.s_a = take(2 * rp * F);
     L.s_b = take(2 * rp * F);
+    // one macrobatch holds every routed row in global expert order, which is the
+    // order the dW1/dW3 GEMM reads X in: keep the forward's dispatched rows
+    L.keep_x = !mx && nM == 1;
+    L.s_xs = L.keep_x ? take(2 * rp * H) : 0;
     L.saved_bytes = o;
 
     o = 0;
@@ -173,7 +177,7 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     const size_t ring_rows = (size_t)L.half_rows * L.ring_halves;
     // forward region: the ring
     o = region;
-    L.w_ringX = take(ring_rows * (mx ? H : 2 * H));
+    L.w_ringX = take(L.keep_x ? 0 : ring_rows * (mx ? H : 2 * H));   // kept X rows: in saved
     L.w_ringXs = mx ? take(ring_rows * (H / kMxBlock)) : 0;
     L.w_ringH = take(ring_rows * (mx ? F : 2 * F));
     L.w_ringHs = mx ? take(ring_rows * (F / kMxBlock)) : 0;
@@ -614,7 +618,8 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
 
     // 3. per macrobatch: dispatch -> GEMM1+SwiGLU -> GEMM2 -> combine
     const bool mx = cfg->precision == MOE_PRECISION_MXFP8;
-    bf16 *ringX = at<bf16>(ws, L.w_ringX), *ringH = at<bf16>(ws, L.w_ringH), *ringY = at<bf16>(ws, L.w_ringY);
+    bf16 *ringX = L.keep_x ? at<bf16>(saved, L.s_xs) : at<bf16>(ws, L.w_ringX);
+    bf16 *ringH = at<bf16>(ws, L.w_ringH), *ringY = at<bf16>(ws, L.w_ringY);
     uint8_t *ringXq = at<uint8_t>(ws, L.w_ringX), *ringHq = at<uint8_t>(ws, L.w_ringH);
     uint8_t *ringXs = mx ? at<uint8_t>(ws, L.w_ringXs) : nullptr, *ringHs = mx ? at<uint8_t>(ws, L.w_ringHs) : nullptr;
     const size_t ring_rows = (size_t)L.half_rows * L.ring_halves;
@@ -719,18 +724,20 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
     const int32_t *s_row_slot = at<int32_t>(saved, L.s_row_slot);
     const bf16 *s_a = at<bf16>(saved, L.s_a);
     const bf16 *s_b = at<bf16>(saved, L.s_b);
-    bf16 *Xs = at<bf16>(ws, L.w_Xs), *Gin = at<bf16>(ws, L.w_Gin), *dA = at<bf16>(ws, L.w_da),
+    bf16 *Xs = L.keep_x ? const_cast<bf16 *>(at<bf16>(saved, L.s_xs)) : at<bf16>(ws, L.w_Xs);
+    bf16 *Gin = at<bf16>(ws, L.w_Gin), *dA = at<bf16>(ws, L.w_da),
          *dB = at<bf16>(ws, L.w_db), *HW = at<bf16>(ws, L.w_hw), *dXs = at<bf16>(ws, L.w_dXs);
     float *dwpart = at<float>(ws, L.w_dwpart), *dlogits = at<float>(ws, L.w_dlogits);
     const size_t rp = L.rows_pad_max;
 
-    // 1. replay dispatch (X rows) and reverse combine (dout rows), all macrobatches
-    //    (bf16 path; the MXFP8 path gathers straight into its quantised operands)
+    // 1. replay dispatch (X rows; not needed when the forward's rows were kept) and
+    //    reverse combine (dout rows), all macrobatches (bf16 path; the MXFP8 path
+    //    gathers straight into its quantised operands)
     if (L.T > 0 && !mx) {
         DispatchArgs d1{};
         d1.src = (const bf16 *)x; d1.dst = Xs; d1.row_slot = s_row_slot; d1.offp = s_offp;
         d1.beg = 0; d1.end = L.nM * L.E; d1.dst_row0 = 0; d1.H = L.H; d1.k = L.k;
-        {
+        if (!L.keep_x) {
             ProfScope ps("dispatch_replay", s);
             st = cuda_check(launch_dispatch(d1, L.rows_pad_max, L.num_sms, s), "replay dispatch launch");
         }

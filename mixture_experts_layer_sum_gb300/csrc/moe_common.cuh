@@ -43,7 +43,10 @@ struct Layout {
     int dwr_splits;         // token splits of the router-weight gradient
     // saved buffer
     size_t s_ids, s_w, s_probs, s_counts, s_offsets, s_offp, s_s2sorted, s_sorted2s, s_slot_row,
-        s_row_slot, s_a, s_b, saved_bytes;
+        s_row_slot, s_a, s_b, s_xs, saved_bytes;
+    // bf16 with one macrobatch: the forward's dispatched X rows live in the saved
+    // buffer (s_xs) and the backward's weight gradient reads them there (no replay)
+    bool keep_x;
     // workspace (header first, then a region shared by forward and backward)
     size_t w_status, w_chunk_counts, w_chunk_base, w_wrt, w_offp, w_ready;
     int mb_rows;            // minibatch rows used by the fused dispatch (multiple of 128)
