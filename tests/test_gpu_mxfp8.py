@@ -99,3 +99,43 @@ def test_mxfp8_deterministic():
     b = G().run_gpu(w, inp)
     for key in ("out", "dx", "dWr", "dW1", "dW3", "dW2"):
         np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+
+
+def _check_sampled_tokens(w, inp, gpu, n, seed):
+    # out and dx of a token depend only on that token's rows: its x and dout rows
+    # are quantised along H, its routed rows' h, da, db along F, and the weight
+    # copies are fixed, so the oracle (same quantisation emulated) runs on the sample
+    sample = np.sort(np.random.default_rng(seed).choice(w.T, n, replace=False))
+    sub = {k: (v[sample] if k in ("x", "dout") else v) for k, v in inp.items()}
+    oi = G().oracle_inputs(sub)
+    args = (oi["x"], oi["Wr"], oi["bias"], oi["W1"], oi["W3"], oi["W2"], w.k)
+    r = O.router(oi["x"], oi["Wr"], oi["bias"], w.k)   # ids checked against the router alone
+    ids, _ = G().reconcile_ids(gpu["ids"][sample].astype(np.int32), r, w.k)
+    f = O.forward(*args, precision="mxfp8", ids=ids)
+    errs = {"out": O.max_abs_rel(gpu["out"][sample], f["out"])}
+    g = O.backward(f, oi["dout"], oi["x"], oi["Wr"], oi["W1"], oi["W3"], oi["W2"])
+    errs["dx"] = O.max_abs_rel(gpu["dx"][sample], g["dx"])
+    assert errs["out"] < G().MX_TOL and errs["dx"] < G().MX_TOL, errs
+    return errs
+
+
+def test_mxfp8_full_size_sampled_tokens():
+    # the MXFP8 workload at full size (T=8192, H=7168, E=16, k=8, F=2048) in the
+    # launch configuration the bench times; forward and dx of sampled tokens
+    w = WL.MXFP8
+    inp = WL.make_inputs(w)
+    gpu = G().run_gpu(w, inp)
+    errs = _check_sampled_tokens(w, inp, gpu, 48, 3)
+    print("mxfp8 full size, sampled", errs)
+    assert np.isfinite(gpu["dW1"]).all() and np.isfinite(gpu["dW2"]).all()
+
+
+def test_ring_full_size_sampled_tokens():
+    # T=16384 through the 256 MiB ring: many macrobatches, both ring halves reused,
+    # minibatch at the wave rule; forward and dx of sampled tokens
+    w = WL.RING
+    inp = WL.make_inputs(w)
+    gpu = G().run_gpu(w, inp, ring_bytes=w.ring_bytes)
+    assert gpu["layer"].plan.num_macrobatches > 2
+    errs = _check_sampled_tokens(w, inp, gpu, 48, 4)
+    print("ring full size, sampled", gpu["layer"].plan.num_macrobatches, "macrobatches", errs)
