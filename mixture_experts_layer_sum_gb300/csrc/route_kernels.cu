@@ -568,9 +568,15 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     const int nw = gridDim.x * blockDim.x / 32;
     const int shift = a.ring_base - a.offp[a.m * a.E];
     const int vecs = a.H / 8;   // a multiple of 32
-    for (int t = a.t0 + gw; t < a.t1; t += nw) {
+    // work item = (token, 512 columns): a macrobatch with few tokens still spreads
+    // over every warp, and each item is one or two rounds of loads
+    const int nch = (vecs + 63) / 64;
+    const int items = (a.t1 - a.t0) * nch;
+    for (int it = gw; it < items; it += nw) {
+        const int t = a.t0 + it / nch;
         // two vectors per lane, rows in batches of 4: 8 loads of 16 B per lane in flight
-        for (int v0 = lane; v0 < vecs; v0 += 64) {
+        {
+            const int v0 = (it % nch) * 64 + lane;
             const bool two = v0 + 32 < vecs;
             float acc[2][8];
 #pragma unroll
@@ -620,7 +626,8 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
 cudaError_t launch_combine(const CombineArgs &a, int num_sms, cudaStream_t s) {
     const int n = a.t1 - a.t0;
     if (n <= 0) return cudaSuccess;
-    int blocks = min(ceil_div(n, 8), num_sms * 8);
+    const int items = n * ((a.H / 8 + 63) / 64);
+    int blocks = min(ceil_div(items, 8), num_sms * 8);
     cudaError_t e = launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, s, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
