@@ -215,13 +215,19 @@ def stop_clocks(p, path):
 
 def kernel_bytes(w, name):
     """Algorithmic HBM bytes per step of the memory-bound kernels."""
-    T, H, R, E, k = w.T, w.H, w.R, w.E, w.k
+    T, H, F, R, E, k = w.T, w.H, w.F, w.R, w.E, w.k
+    qh, qf = R * H * 33 // 32, R * F * 33 // 32   # one MXFP8 copy of R rows (codes + scales)
     return {"dispatch": T * H * 2 + R * H * 2, "dispatch_replay": T * H * 2 + R * H * 2,
-            "dispatch_mxfp8": T * H * 2 + R * H * 33 // 32,
+            "dispatch_mxfp8": T * H * 2 + qh,
             "reverse_combine": T * H * 2 + R * H * 2, "combine": R * H * 2 + T * H * 2 + R * 8,
             "router_topk": T * H * 2 + T * E * 4 + T * k * 8,
             "reverse_dispatch": R * H * 2 + T * H * 2 + T * E * 4,
-            "router_wgrad": T * H * 2 + T * E * 4}.get(name)
+            "router_wgrad": T * H * 2 + T * E * 4,
+            # MXFP8 backward: dout gathered once into dY along H and along the tokens; x along
+            # the tokens; h.w, da, db (bf16 rows) along the tokens
+            "quantize_dy": T * H * 2 + 2 * qh, "quantize_x_tokens": T * H * 2 + qh,
+            "quantize_hw_tokens": R * F * 2 + qf, "quantize_da_tokens": R * F * 2 + qf,
+            "quantize_db_tokens": R * F * 2 + qf}.get(name)
 
 
 def gemm_flops(w, name):
@@ -256,6 +262,10 @@ def layer_roofline(w, peaks, step_ms):
     gemm = ["grouped_gemm_fwd1_swiglu", "grouped_gemm_fwd2", "grouped_gemm_bwd2_swiglu", "grouped_gemm_bwd1",
             "grouped_gemm_wgrad2", "grouped_gemm_wgrad13"]
     mem = ["dispatch", "combine", "router_topk", "reverse_combine", "reverse_dispatch", "router_wgrad"]
+    if w.precision == "mxfp8":
+        mem = ["dispatch_mxfp8", "combine", "router_topk", "quantize_dy", "quantize_x_tokens",
+               "quantize_hw_tokens", "quantize_da_tokens", "quantize_db_tokens", "reverse_dispatch",
+               "router_wgrad"]
     t_gemm = sum(gemm_flops(w, n) for n in gemm) / (tf * 1e12)
     t_mem = sum(kernel_bytes(w, n) for n in mem) / (hbm * 1e9)
     t = (t_gemm + t_mem) * 1e3

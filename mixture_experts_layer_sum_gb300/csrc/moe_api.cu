@@ -802,9 +802,10 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
     const int seg_rows_max = (int)align_up((size_t)std::min(L.Mb, std::max(L.T, 1)), kRowPad);
     // token-axis MXFP8 copies: bf16 [rows][C] -> [C][rows] quantised along rows
     auto transpose_q = [&](const bf16 *src, size_t codes, size_t scales, int C, const char *name,
-                           bool gather = false) {
+                           bool gather = false, size_t rcodes = 0, size_t rscales = 0) {
         MxTransposeArgs a{};
         a.src = src; a.codes = at<uint8_t>(ws, codes); a.scales = at<uint8_t>(ws, scales);
+        if (rcodes) { a.rcodes = at<uint8_t>(ws, rcodes); a.rscales = at<uint8_t>(ws, rscales); }
         a.R = (int)rp; a.C = C; a.r_limit_ptr = s_offp + L.nM * L.E;
         if (gather) {
             // experts visited in step (see MxTransposeArgs) so each token row is read once from HBM
@@ -815,19 +816,11 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
         return cuda_check(launch_mx_transpose(a, 1, s), "token-axis quantise launch");
     };
     if (mx && L.T > 0) {
-        // dY rows along H for the GEMM2 dgrad; dY and X along the token axis for the weight gradients
-        // reverse combine fused with quantisation: dY rows gathered from dout as MXFP8 along H
-        MxRowsArgs a{};
-        a.src = (const bf16 *)dout; a.codes = at<uint8_t>(ws, L.w_Ginq); a.scales = at<uint8_t>(ws, L.w_Ginq_s);
-        a.row_slot = s_row_slot; a.offp = s_offp; a.beg = 0; a.end = L.nM * L.E; a.dst_row0 = 0; a.C = L.H;
-        a.k = L.k;
-        {
-            ProfScope ps("reverse_combine_mxfp8", s);
-            st = cuda_check(launch_mx_rows(a, L.rows_pad_max, L.num_sms, s), "dY quantise launch");
-        }
-        if (st != MOE_OK) return st;
-        // token-axis copies gathered straight from dout and x (activation replay)
-        if ((st = transpose_q((const bf16 *)dout, L.w_GinT, L.w_GinT_s, L.H, "quantize_dy_tokens", true)) != MOE_OK)
+        // dY rows gathered from dout (reverse combine) quantised along H for the GEMM2 dgrad and,
+        // from the same staged tiles, along the token axis for dW2; X along the token axis for
+        // dW1/dW3 (activation replay)
+        if ((st = transpose_q((const bf16 *)dout, L.w_GinT, L.w_GinT_s, L.H, "quantize_dy", true, L.w_Ginq,
+                              L.w_Ginq_s)) != MOE_OK)
             return st;
         if ((st = transpose_q((const bf16 *)x, L.w_XsT, L.w_XsT_s, L.H, "quantize_x_tokens", true)) != MOE_OK)
             return st;

@@ -268,6 +268,38 @@ __global__ void __launch_bounds__(128) mx_transpose_kernel(MxTransposeArgs a) {
         const int c = lane * 4 + i;
         atom[(c & 31) * 16 + ((c >> 5) & 3) * 4 + warp] = (uint8_t)(sx[i] + 127);
     }
+    if (a.rcodes && rb0 + t < r_limit) {
+        // row-wise copy: thread t quantises tile row t along C (four 32-column blocks)
+        // from the same staged tile; 16-byte shared loads at the 272-byte row stride
+        // hit distinct banks within each quarter warp
+        const size_t grow = (size_t)(rb0 + t);
+        uint8_t *rdst = a.rcodes + grow * a.C + c0;
+        uint32_t sw = 0;
+#pragma unroll 1
+        for (int b = 0; b < 4; ++b) {
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint4 q = *reinterpret_cast<const uint4 *>(&tile[t][b * 32 + j * 8]);
+                w[4 * j] = q.x; w[4 * j + 1] = q.y; w[4 * j + 2] = q.z; w[4 * j + 3] = q.w;
+            }
+            uint32_t m[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m[i] = absmax_bf16x2(w[2 * i], w[2 * i + 1]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) m[i] = absmax_bf16x2(m[2 * i], m[2 * i + 1]);
+            m[0] = absmax_bf16x2(absmax_bf16x2(m[0], m[1]), absmax_bf16x2(m[2], m[3]));
+            const int rs = mx_exponent_bf16(max(m[0] & 0x7fffu, (m[0] >> 16) & 0x7fffu));
+            const uint16_t rinv = mx_inv_bf16(rs);
+            uint32_t cw[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) cw[i] = e4m3x4_row(w[2 * i], w[2 * i + 1], rinv);
+            st_global_32B(rdst + b * 32, cw);
+            sw |= (uint32_t)(rs + 127) << (8 * b);
+        }
+        // the four blocks' scale bytes are adjacent in the atom row
+        *reinterpret_cast<uint32_t *>(a.rscales + mx_sf_offset(grow, (size_t)c0, a.C)) = sw;
+    }
     __syncthreads();
     if (t < 32) {
         uint8_t *sdst = a.scales + bi * ((size_t)a.C * a.R / kMxBlock) +
@@ -280,6 +312,7 @@ cudaError_t launch_mx_transpose(const MxTransposeArgs &a, int batch, cudaStream_
     if (a.R <= 0 || batch <= 0) return cudaSuccess;
     if (a.R % kMxtRows || a.C % kMxtCols) return cudaErrorInvalidValue;
     dim3 grid(a.C / kMxtCols, a.R / kMxtRows, batch);
+    if (a.rcodes && batch != 1) return cudaErrorInvalidValue;
     if (a.offp) {
         if (batch != 1 || a.ilv_E <= 0 || a.ilv_nseg % a.ilv_E) return cudaErrorInvalidValue;
         const long long nb = (long long)(a.C / kMxtCols) * a.ilv_nseg * a.ilv_jb;

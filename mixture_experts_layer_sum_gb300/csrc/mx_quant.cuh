@@ -30,6 +30,9 @@ cudaError_t launch_mx_rows(const MxRowsArgs &a, int max_rows, int num_sms, cudaS
 // before block j + 1 of any, so the copies of one token taken by different
 // experts are read close together in time and the source leaves HBM about once.
 // r_limit_ptr is unused.
+// Row-wise copy as well (rcodes != null, batch 1): the same input rows quantised
+// along C into rcodes [R][C] + scale atoms rscales (K = C), destination row =
+// input row; the fused form of an mx_rows pass over the same gathered rows.
 struct MxTransposeArgs {
     const bf16 *src;
     uint8_t *codes, *scales;
@@ -39,6 +42,7 @@ struct MxTransposeArgs {
     int k;
     const int32_t *offp;
     int ilv_E, ilv_nseg, ilv_jb;
+    uint8_t *rcodes, *rscales;
 };
 cudaError_t launch_mx_transpose(const MxTransposeArgs &a, int batch, cudaStream_t s);
 
