@@ -510,7 +510,7 @@ moe_status_t moe_quantize_weights(const moe_config_t *cfg, const void *W1, const
     for (const auto &t : rw) {
         MxRowsArgs a{};
         a.src = (const bf16 *)t.src; a.codes = qw + q.codes[t.idx]; a.scales = qw + q.scales[t.idx];
-        a.nrows = t.rows; a.C = t.C; a.k = 1;
+        a.nrows = t.rows; a.C = t.C;
         st = cuda_check(launch_mx_rows(a, t.rows, sms, s), "weight quantise launch");
         if (st != MOE_OK) return st;
     }

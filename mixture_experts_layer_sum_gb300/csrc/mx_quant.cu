@@ -1,17 +1,16 @@
 // MXFP8 quantisers (article "O MoK do Cursor ...", section 02: MXFP8 activation
 // quantisation fused into dispatch, grouped GEMM and SwiGLU, with no separate
-// quantisation pass over HBM for the dispatched rows).
+// quantisation pass over HBM for the dispatched rows; the forward's quantising
+// dispatch itself runs inside GEMM1).
 //
-//   mx_rows_kernel       bf16 rows -> E4M3 rows + E8M0 scales along the row.
-//                        Gather mode is the quantising dispatch: destination
-//                        row r takes token row_slot[r] / k of the source (zero
-//                        for padding rows), so x is read once and written once
-//                        in MXFP8. Identity mode quantises a matrix in place
-//                        order (weights along their K, gathered dY rows).
+//   mx_rows_kernel       bf16 rows -> E4M3 rows + E8M0 scales along the row
+//                        (weight copies along their stored rows).
 //   mx_transpose_kernel  bf16 [R][C] -> E4M3 [C][R] + scales along R: operands
 //                        whose contraction axis is the row axis (weights for the
 //                        other GEMM orientation, token-axis operands of the
-//                        weight gradients).
+//                        weight gradients, gathered straight from x and dout);
+//                        optionally also the row-wise copy of the same rows
+//                        (dY along H for the GEMM2 dgrad).
 #include "mx_quant.cuh"
 
 namespace moe {
@@ -96,18 +95,10 @@ __global__ void __launch_bounds__(kRowsWarps * 32) mx_rows_kernel(MxRowsArgs a) 
     const int lane = threadIdx.x % 32, wib = threadIdx.x / 32;
     uint4 *wb = stage[wib];
     const int gw = blockIdx.x * kRowsWarps + wib, nw = gridDim.x * kRowsWarps;
-    int r0 = 0, r1 = a.nrows;
-    if (a.offp) { r0 = a.offp[a.beg]; r1 = a.offp[a.end]; }
     const int nchunk = (a.C + 1023) / 1024;
-    for (int r = r0 + gw; r < r1; r += nw) {
-        const bf16 *src = nullptr;
-        if (a.row_slot) {
-            const int slot = a.row_slot[r];
-            if (slot >= 0) src = a.src + (size_t)(slot / a.k) * a.C;
-        } else {
-            src = a.src + (size_t)r * a.C;
-        }
-        const size_t drow = (size_t)(a.dst_row0 + r - r0);
+    for (int r = gw; r < a.nrows; r += nw) {
+        const bf16 *src = a.src + (size_t)r * a.C;
+        const size_t drow = (size_t)r;
         uint8_t *dst = a.codes + drow * a.C;
         uint4 q[4];
         auto load = [&](int ch) {
@@ -115,7 +106,7 @@ __global__ void __launch_bounds__(kRowsWarps * 32) mx_rows_kernel(MxRowsArgs a) 
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int v = lane + 32 * u;
-                q[u] = (src && v < nvec) ? ld_nc_v4(src + e0 + v * 8) : make_uint4(0, 0, 0, 0);
+                q[u] = v < nvec ? ld_nc_v4(src + e0 + v * 8) : make_uint4(0, 0, 0, 0);
             }
         };
         load(0);

@@ -4,17 +4,12 @@
 
 namespace moe {
 
-// bf16 rows [*, C] -> E4M3 rows [*, C] + E8M0 scale atoms (K = C).
-// Gather mode (row_slot != null): rows r in [offp[beg], offp[end]) take source
-// token row_slot[r] / k (zeros when row_slot[r] < 0). Identity mode
-// (row_slot == null): rows [0, nrows), or [offp[beg], offp[end]) when offp is set.
-// Destination row = dst_row0 + r - first row.
+// bf16 rows [nrows, C] -> E4M3 rows [nrows, C] + E8M0 scale atoms (K = C), in place
+// order: the weight copies whose contraction axis is the stored row.
 struct MxRowsArgs {
     const bf16 *src;
     uint8_t *codes, *scales;
-    const int32_t *row_slot, *offp;
-    int beg, end, nrows;
-    int dst_row0, C, k;
+    int nrows, C;
 };
 cudaError_t launch_mx_rows(const MxRowsArgs &a, int max_rows, int num_sms, cudaStream_t s);
 
