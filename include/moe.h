@@ -46,7 +46,9 @@
  *     1024-byte boundary on, and the size queries include that slack.
  *   - Calls sharing one workspace must not overlap in time (same stream, or
  *     ordered by events).
- *   - Thread safety: no global state besides a thread-local error string.
+ *   - Thread safety: calls from several host threads are safe when they use
+ *     distinct workspaces. State shared across calls: a thread-local error
+ *     string and per-device caches of kernel occupancy queries (atomics).
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H

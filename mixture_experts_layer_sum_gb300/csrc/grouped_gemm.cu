@@ -34,6 +34,7 @@
 // and all roles leave their loops, drain their in-flight copies/MMAs and free
 // TMEM before exiting.
 #include <algorithm>
+#include <atomic>
 
 #include "grouped_gemm.cuh"
 
@@ -1088,6 +1089,25 @@ __global__ void __launch_bounds__(320, 1) pair_gemm_kernel(const __grid_constant
     if (warp == 1) tmem_dealloc_pair(tmem, 512);
 }
 
+// Co-resident cluster count of one kernel configuration, queried once per device and
+// kept in an atomic so that first launches from several host threads do not race.
+constexpr int kMaxCachedDevices = 64;
+template <class Kernel>
+int cached_max_clusters(std::atomic<int> (&cache)[kMaxCachedDevices][2], int slot, Kernel kernel,
+                        cudaLaunchConfig_t cfg, int fallback) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    if (dev >= 0 && dev < kMaxCachedDevices) {
+        const int c = cache[dev][slot].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    cfg.numAttrs = 1;   // the cluster shape alone
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) n = fallback;
+    if (dev >= 0 && dev < kMaxCachedDevices) cache[dev][slot].store(n, std::memory_order_relaxed);
+    return n;
+}
+
 template <int OP>
 cudaError_t launch_pair(const GemmArgs &g, int grid, cudaStream_t stream) {
     constexpr size_t smem = PSTAGES * P_STAGE + P_STAGING + sizeof(PairCtl) + 1024;
@@ -1109,16 +1129,10 @@ cudaError_t launch_pair(const GemmArgs &g, int grid, cudaStream_t stream) {
     cfg.attrs = attr;
     // A persistent grid must be fully co-resident: with GPCs of an odd SM count
     // not every SM can host half of a pair, so size the grid by the number of
-    // clusters that fit at once (queried once per kernel and block size).
-    static int max_clusters[2] = {0, 0};
-    int &mc = max_clusters[fused ? 1 : 0];
-    cfg.numAttrs = 1;
-    if (mc == 0) {
-        cfg.gridDim = dim3(grid / 2 * 2);
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel<OP>, &cfg) != cudaSuccess || n <= 0) n = grid / 2;
-        mc = n;
-    }
+    // clusters that fit at once (queried once per device, kernel and block size).
+    static std::atomic<int> max_clusters[kMaxCachedDevices][2];
+    cfg.gridDim = dim3(grid / 2 * 2);
+    const int mc = cached_max_clusters(max_clusters, fused ? 1 : 0, pair_gemm_kernel<OP>, cfg, grid / 2);
     cfg.gridDim = dim3(2 * std::min(grid / 2, mc));
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<OP>, g);
@@ -1371,15 +1385,9 @@ cudaError_t launch_pair8(const GemmArgs &g, int grid, cudaStream_t stream) {
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    static int max_clusters[2] = {0, 0};
-    int &mc = max_clusters[fused ? 1 : 0];
-    cfg.numAttrs = 1;
-    if (mc == 0) {
-        cfg.gridDim = dim3(grid / 2 * 2);
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, pair8_gemm_kernel<OP>, &cfg) != cudaSuccess || n <= 0) n = grid / 2;
-        mc = n;
-    }
+    static std::atomic<int> max_clusters[kMaxCachedDevices][2];
+    cfg.gridDim = dim3(grid / 2 * 2);
+    const int mc = cached_max_clusters(max_clusters, fused ? 1 : 0, pair8_gemm_kernel<OP>, cfg, grid / 2);
     cfg.gridDim = dim3(2 * std::min(grid / 2, mc));
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, pair8_gemm_kernel<OP>, g);
