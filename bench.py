@@ -65,6 +65,23 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def max_over_ranks(values, device=None):
+    """Per-entry maximum over every rank of the default process group (the slowest
+    replica sets the job's time); the values themselves when running alone."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tokens_per_s(world_size, tokens_per_rank, steps, ms):
+    """Whole-job throughput: the tokens every replica processed over the slowest time."""
+    return world_size * tokens_per_rank * steps / (ms * 1e-3)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -352,14 +369,11 @@ def run_ours(args, w):
     if w.precision == "mxfp8":
         # weight quantisation runs once per weight update, outside the step; timed on its own
         w0_ms = timed(lambda: layer.quantize_weights(d["W1"], d["W3"], d["W2"], stream=stream), args.steps)
+        w0_ms, = max_over_ranks([w0_ms], device=dev)   # every rank has the same precision
     barrier()
     fwd_ms = timed(fwd, args.steps)
     layer.status(stream)
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms, fwd_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, fwd_ms = t.tolist()
+    total_ms, fwd_ms = max_over_ranks([total_ms, fwd_ms], device=dev)
 
     # per-kernel breakdown: the same steps with events around every launch
     M.moe_profile_begin()
@@ -427,6 +441,7 @@ def run_ours(args, w):
 
     e2e_run(2)
     e2e_ms = e2e_run(args.steps)
+    e2e_ms, = max_over_ranks([e2e_ms], device=dev)
     layer.status(stream)
     clocks = sampler.stop() if sampler is not None else stop_clocks(clk_p, clk_path)
 
@@ -478,7 +493,7 @@ def run_ours(args, w):
                 "peak_source": f"{peak_src} hbm_gbs"}
     gemm_ms = sum(ms_ for nm, _, ms_ in kernels if nm.startswith("grouped_gemm"))
     gemm_fl = sum(gemm_flops(w, nm) * args.steps for nm, n_, _ in kernels if nm.startswith("grouped_gemm"))
-    value = ws * w.T * args.steps / (total_ms * 1e-3)
+    value = job_tokens_per_s(ws, w.T, args.steps, total_ms)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -490,9 +505,9 @@ def run_ours(args, w):
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "w0": None if w0_ms is None else {
             "ms": w0_ms / args.steps,
-            "fwd_bwd_value_incl_w0": ws * w.T * args.steps / ((total_ms + w0_ms) * 1e-3),
+            "fwd_bwd_value_incl_w0": job_tokens_per_s(ws, w.T, args.steps, total_ms + w0_ms),
             "note": "MXFP8 weight copies, once per weight update; excluded from value"},
-        "fwd": {"value": ws * w.T * args.steps / (fwd_ms * 1e-3), "unit": "tokens/s",
+        "fwd": {"value": job_tokens_per_s(ws, w.T, args.steps, fwd_ms), "unit": "tokens/s",
                 "ms_per_step": fwd_ms / args.steps},
         "roofline": roof,
         "grouped_gemm": {"tflops": gemm_fl / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None,
@@ -509,7 +524,7 @@ def run_ours(args, w):
                     for nm, n_, ms_ in kt],
         "layer_roofline": layer_roofline(w, peaks, total_ms / args.steps),
         "gpu_launches": launches,
-        "e2e": {"value": ws * w.T * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(ws, w.T, args.steps, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * w.T * w.H * 2, "d2h_bytes_per_step": 2 * w.T * w.H * 2,
                 "pipelined": "copy streams, double-buffered inputs/outputs; no L2 flush (weights exceed L2)"},
         "clocks": clocks,
