@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 typedef struct CUstream_st *moe_stream_t;   /* same type as cudaStream_t */
 
@@ -91,7 +91,13 @@ typedef enum {
  *     for all routed rows, i.e. one macrobatch.
  *   macrobatch_tokens: tokens per macrobatch; 0 = derived from ring_bytes.
  *   timeout_ms: budget of every device-side wait; 0 = 2000 ms.
- *   num_sms: SM count used for planning; 0 = query the current device. */
+ *   num_sms: SM count used for planning; 0 = query the current device.
+ *   fault_mask: 0 in normal use; bits inject a failure from the host for tests
+ *     of failure detection (no GPU fault, trap or unbounded wait):
+ *     MOE_FAULT_GEMM1_READY: moe_forward sets GEMM1's first minibatch ready
+ *     counter so that it never reaches its target; GEMM1's bounded wait runs
+ *     out, the status word reports MOE_ERR_TIMEOUT, every other wait sees the
+ *     status and returns, and the outputs of that call are undefined. */
 typedef struct {
     int T, H, F, E, k;
     int precision;
@@ -100,7 +106,10 @@ typedef struct {
     size_t ring_bytes;
     unsigned timeout_ms;
     int num_sms;
+    unsigned fault_mask;
 } moe_config_t;
+
+#define MOE_FAULT_GEMM1_READY 1u
 
 /* Derived execution plan (host-only; no device access when cfg->num_sms > 0). */
 typedef struct {

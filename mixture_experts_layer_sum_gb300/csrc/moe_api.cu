@@ -615,6 +615,13 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
         st = cuda_check(launch_schedule(sa, s), "schedule launch");
     }
     if (st != MOE_OK) return st;
+    if ((cfg->fault_mask & MOE_FAULT_GEMM1_READY) && L.T > 0) {
+        // failure-detection tests: the first minibatch's ready count (zeroed by the schedule)
+        // becomes a large negative number that the gather's additions cannot lift to its
+        // target; the claim counter next to it is untouched, so every gather stays in bounds
+        st = cuda_check(cudaMemsetAsync(at<int>(ws, L.w_ready), 0x80, sizeof(int), s), "fault injection");
+        if (st != MOE_OK) return st;
+    }
 
     // 3. per macrobatch: dispatch -> GEMM1+SwiGLU -> GEMM2 -> combine
     const bool mx = cfg->precision == MOE_PRECISION_MXFP8;

@@ -19,6 +19,7 @@ MOE_ERR_WORKSPACE = 3
 MOE_ERR_CUDA = 4
 MOE_ERR_TIMEOUT = 5
 MOE_ERR_INTERNAL = 6
+MOE_FAULT_GEMM1_READY = 1   # config fault_mask bit (failure-detection tests)
 MOE_PRECISION_BF16 = 0
 MOE_PRECISION_MXFP8 = 1
 
@@ -39,7 +40,7 @@ class moe_config_t(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("F", ctypes.c_int), ("E", ctypes.c_int),
                 ("k", ctypes.c_int), ("precision", ctypes.c_int), ("minibatch_rows", ctypes.c_int),
                 ("macrobatch_tokens", ctypes.c_int), ("ring_bytes", ctypes.c_size_t),
-                ("timeout_ms", ctypes.c_uint), ("num_sms", ctypes.c_int)]
+                ("timeout_ms", ctypes.c_uint), ("num_sms", ctypes.c_int), ("fault_mask", ctypes.c_uint)]
 
 
 class moe_kernel_time_t(ctypes.Structure):
@@ -55,9 +56,10 @@ class moe_plan_t(ctypes.Structure):
 
 
 def make_config(T, H, F, E, k, precision="bf16", minibatch_rows=0, macrobatch_tokens=0, ring_bytes=0,
-                timeout_ms=0, num_sms=0) -> moe_config_t:
+                timeout_ms=0, num_sms=0, fault_mask=0) -> moe_config_t:
     p = {"bf16": MOE_PRECISION_BF16, "mxfp8": MOE_PRECISION_MXFP8}.get(precision, precision)
-    return moe_config_t(T, H, F, E, k, p, minibatch_rows, macrobatch_tokens, ring_bytes, timeout_ms, num_sms)
+    return moe_config_t(T, H, F, E, k, p, minibatch_rows, macrobatch_tokens, ring_bytes, timeout_ms, num_sms,
+                        fault_mask)
 
 
 def _load():

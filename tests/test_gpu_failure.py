@@ -1,0 +1,44 @@
+"""Failure detection on the GPU without a GPU fault (run on a GB300).
+
+A host-injected failure (config fault_mask MOE_FAULT_GEMM1_READY: the first
+minibatch's ready counter is set so that it never reaches its target) makes
+GEMM1's bounded wait run out. The device status word must report
+MOE_ERR_TIMEOUT, every kernel must return (each wait is bounded and gives up
+once the status word is set), the query clears the word, and the same CUDA
+context must then run the layer correctly."""
+import time
+
+import pytest
+import torch
+
+import workloads as WL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from mixture_experts_layer_sum_gb300 import build_ext
+    build_ext.build()
+    assert torch.cuda.is_available()
+
+
+def test_gemm1_wait_runs_out_and_context_survives():
+    import mixture_experts_layer_sum_gb300.moe as M
+    from mixture_experts_layer_sum_gb300.layer import MoeLayer
+    import tests.gpu_common as G
+    w = WL.TINY
+    inp = WL.make_inputs(w)
+    d = G.device_inputs(inp)
+    layer = MoeLayer(w.T, w.H, w.F, w.E, w.k, timeout_ms=100, fault_mask=M.MOE_FAULT_GEMM1_READY)
+    assert layer.plan.num_macrobatches == 1 and layer.plan.minibatch_rows >= w.T * w.k   # one minibatch
+    t0 = time.time()
+    layer.forward(d["x"], d["Wr"], d["bias"], d["W1"], d["W3"], d["W2"])
+    with pytest.raises(M.MoeError) as err:
+        layer.status()
+    assert err.value.status == M.MOE_ERR_TIMEOUT
+    assert time.time() - t0 < 30.0          # bounded: 100 ms per wait, then every role leaves
+    layer.status()                          # the query cleared the status word
+    # same process and CUDA context: a fresh layer still matches the oracle
+    gpu = G.run_gpu(w, inp)
+    G.check_layer(w, inp, gpu)
