@@ -61,6 +61,24 @@ def test_plan_sizes_and_ring(moe):
     assert pf.rows_padded_max >= 16384 * 8 and pf.rows_padded_max % 128 == 0
 
 
+def test_saved_keeps_dispatched_rows_only_for_one_bf16_macrobatch(moe):
+    # bf16 with one macrobatch: the forward's expert-sorted x rows [rows_padded_max, H] bf16 live in
+    # the saved context (the backward's dW1/dW3 reads them there); MXFP8 or several macrobatches
+    # keep the same context without them
+    a1024 = lambda v: -(-v // 1024) * 1024
+    T, H, F, E, k = 4096, 2048, 1024, 32, 4
+    bf = moe.make_config(T, H, F, E, k, num_sms=152)
+    mx = moe.make_config(T, H, F, E, k, "mxfp8", num_sms=152)
+    p = moe.moe_plan(bf)
+    assert p.num_macrobatches == 1
+    assert moe.moe_saved_size(bf) - moe.moe_saved_size(mx) == a1024(2 * p.rows_padded_max * H)
+    many = moe.make_config(T, H, F, E, k, macrobatch_tokens=1024, num_sms=152)
+    pm = moe.moe_plan(many)
+    assert pm.num_macrobatches == 4
+    many_mx = moe.make_config(T, H, F, E, k, "mxfp8", macrobatch_tokens=1024, num_sms=152)
+    assert moe.moe_saved_size(many) == moe.moe_saved_size(many_mx)
+
+
 @pytest.mark.parametrize("kw,status", [
     (dict(T=16, H=250, F=512, E=4, k=2), 2),    # H not a multiple of 256
     (dict(T=16, H=256, F=500, E=4, k=2), 2),
