@@ -42,3 +42,24 @@ def test_gemm1_wait_runs_out_and_context_survives():
     # same process and CUDA context: a fresh layer still matches the oracle
     gpu = G.run_gpu(w, inp)
     G.check_layer(w, inp, gpu)
+
+
+def test_schedule_reports_out_of_range_ids():
+    # expert ids outside [0, E) passed to moe_schedule: the schedule's own check skips their
+    # slots (no access depends on them) and reports MOE_ERR_INTERNAL; the valid slots are counted
+    import numpy as np
+    import mixture_experts_layer_sum_gb300.moe as M
+    from mixture_experts_layer_sum_gb300.layer import MoeLayer
+    T, E, k = 300, 8, 2
+    rng = np.random.default_rng(5)
+    ids = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    for t, j, v in [(3, 0, E), (17, 1, -1), (250, 0, E + 100)]:
+        ids[t, j] = v
+    layer = MoeLayer(T, 256, 256, E, k)
+    counts, _, _, _ = layer.schedule(torch.from_numpy(ids).cuda())
+    with pytest.raises(M.MoeError) as err:
+        layer.status()
+    assert err.value.status == M.MOE_ERR_INTERNAL
+    valid = ids[(ids >= 0) & (ids < E)]
+    np.testing.assert_array_equal(counts.cpu().numpy().reshape(-1), np.bincount(valid, minlength=E))
+    layer.status()                          # cleared by the query
