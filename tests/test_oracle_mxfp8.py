@@ -127,3 +127,46 @@ def test_mxfp8_layer_within_format_error_of_exact():
     for key in ("dx", "dW1", "dW3", "dW2", "dWr"):
         e = O.max_abs_rel(gmx[key], g64[key])
         assert 1e-5 < e < 0.15, (key, e)
+
+
+def _axis_structured(rng, shape, axis):
+    """Entries u * c with u in {0, +-1/4, +-1/2, +-1, +-2} and a power-of-two scale c that is
+    constant along `axis` (the contraction axis) but spans 2^0 .. 2^-20 along the other one:
+    MX blocks along `axis` hold one scale (exact in E4M3), blocks across it do not."""
+    u = rng.choice(np.array([0.0, 0.25, -0.25, 0.5, -0.5, 1.0, -1.0, 2.0, -2.0]), shape)
+    other = 1 - axis
+    c = 2.0 ** -rng.choice(np.array([0, 20]), shape[other])
+    return u * (c[None, :] if other == 1 else c[:, None])
+
+
+def test_mxfp8_forward_quantises_each_operand_along_its_contraction_axis():
+    # x along H, W1/W3 along H, h along F, W2 along F: with operands whose blocks are exact along
+    # their contraction axis (and inexact across it), the emulated MXFP8 forward must equal the
+    # float64 forward with only h rounded, blockwise along F, before GEMM2. A wrong axis for any
+    # operand, or a missing / extra quantisation point, breaks the equality.
+    rng = np.random.default_rng(11)
+    T, H, F, E, k = 64, 64, 64, 4, 2
+    x = _axis_structured(rng, (T, H), 1)
+    W1 = np.stack([_axis_structured(rng, (H, F), 0) for _ in range(E)])
+    W3 = np.stack([_axis_structured(rng, (H, F), 0) for _ in range(E)])
+    W2 = np.stack([_axis_structured(rng, (F, H), 0) for _ in range(E)])
+    Wr = rng.standard_normal((H, E)) * 0.3
+    # the structure is what makes the test sensitive
+    assert (O.mx_roundtrip(x, 1) == x).all() and (O.mx_roundtrip(x, 0) != x).any()
+    assert (O.mx_roundtrip(W1[0], 0) == W1[0]).all() and (O.mx_roundtrip(W1[0], 1) != W1[0]).any()
+    assert (O.mx_roundtrip(W2[0], 0) == W2[0]).all() and (O.mx_roundtrip(W2[0], 1) != W2[0]).any()
+    f64 = O.forward(x, Wr, None, W1, W3, W2, k)
+    fmx = O.forward(x, Wr, None, W1, W3, W2, k, precision="mxfp8")
+    np.testing.assert_array_equal(fmx["ids"], f64["ids"])
+    # exact operands: GEMM1's pre-activations are the float64 ones, element for element
+    np.testing.assert_array_equal(fmx["a"], f64["a"])
+    np.testing.assert_array_equal(fmx["b"], f64["b"])
+    h = f64["h"]
+    assert (O.mx_roundtrip(h, 1) != h).any()
+    Y = np.zeros((T * k, H))
+    for e, s0, s1 in O.expert_segments(f64):
+        Y[s0:s1] = O.mx_roundtrip(h[s0:s1], 1) @ W2[e]
+    s2s = f64["slot_to_sorted"].reshape(T, k)
+    want = sum(f64["w"][:, j:j + 1] * Y[s2s[:, j]] for j in range(k))
+    np.testing.assert_allclose(fmx["out"], want, rtol=1e-12, atol=1e-300)
+    assert O.max_abs_rel(fmx["out"], f64["out"]) > 1e-6      # h's rounding is visible
