@@ -170,3 +170,37 @@ def test_mxfp8_forward_quantises_each_operand_along_its_contraction_axis():
     want = sum(f64["w"][:, j:j + 1] * Y[s2s[:, j]] for j in range(k))
     np.testing.assert_allclose(fmx["out"], want, rtol=1e-12, atol=1e-300)
     assert O.max_abs_rel(fmx["out"], f64["out"]) > 1e-6      # h's rounding is visible
+
+
+def test_mxfp8_backward_dgrads_quantise_along_their_contraction_axes():
+    # The backward's MXFP8 points on the dx path: dY rows and W2 along H (GEMM2 dgrad, K = H), da,
+    # db and W1, W3 along F (GEMM1 dgrad, K = F). The forward is run in float64 and only the
+    # backward emulates MXFP8, so with dY, W2 exact along H and W1, W3 exact along F (each inexact
+    # across), da and db must equal the float64 ones exactly and dx must equal the float64
+    # composition with only da and db rounded blockwise along F.
+    rng = np.random.default_rng(13)
+    T, H, F, E, k = 64, 64, 64, 4, 2
+    x = rng.standard_normal((T, H))
+    W1 = np.stack([_axis_structured(rng, (H, F), 1) for _ in range(E)])
+    W3 = np.stack([_axis_structured(rng, (H, F), 1) for _ in range(E)])
+    W2 = np.stack([_axis_structured(rng, (F, H), 1) for _ in range(E)])
+    Wr = rng.standard_normal((H, E)) * 0.3
+    dout = _axis_structured(rng, (T, H), 1)
+    assert (O.mx_roundtrip(W1[0], 1) == W1[0]).all() and (O.mx_roundtrip(W1[0], 0) != W1[0]).any()
+    assert (O.mx_roundtrip(W2[0], 1) == W2[0]).all() and (O.mx_roundtrip(W2[0], 0) != W2[0]).any()
+    assert (O.mx_roundtrip(dout, 1) == dout).all() and (O.mx_roundtrip(dout, 0) != dout).any()
+    f64 = O.forward(x, Wr, None, W1, W3, W2, k)
+    g64 = O.backward(f64, dout, x, Wr, W1, W3, W2)
+    gmx = O.backward(dict(f64, precision="mxfp8"), dout, x, Wr, W1, W3, W2)
+    np.testing.assert_array_equal(gmx["da"], g64["da"])
+    np.testing.assert_array_equal(gmx["db"], g64["db"])
+    np.testing.assert_array_equal(gmx["dlogits"], g64["dlogits"])
+    da, db = g64["da"], g64["db"]
+    assert (O.mx_roundtrip(da, 1) != da).any()
+    dX = np.zeros((T * k, H))
+    for e, s0, s1 in O.expert_segments(f64):
+        dX[s0:s1] = O.mx_roundtrip(da[s0:s1], 1) @ W1[e].T + O.mx_roundtrip(db[s0:s1], 1) @ W3[e].T
+    s2s = f64["slot_to_sorted"].reshape(T, k)
+    want = sum(dX[s2s[:, j]] for j in range(k)) + g64["dlogits"] @ Wr.T
+    np.testing.assert_allclose(gmx["dx"], want, rtol=1e-12, atol=1e-300)
+    assert O.max_abs_rel(gmx["dx"], g64["dx"]) > 1e-6      # da, db rounding is visible
