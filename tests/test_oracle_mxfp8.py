@@ -204,3 +204,29 @@ def test_mxfp8_backward_dgrads_quantise_along_their_contraction_axes():
     want = sum(dX[s2s[:, j]] for j in range(k)) + g64["dlogits"] @ Wr.T
     np.testing.assert_allclose(gmx["dx"], want, rtol=1e-12, atol=1e-300)
     assert O.max_abs_rel(gmx["dx"], g64["dx"]) > 1e-6      # da, db rounding is visible
+
+
+def test_mxfp8_weight_gradient_quantises_along_the_token_axis():
+    # dW1 = X^T da contracts over each expert's rows: both operands are rounded in 32-row blocks
+    # along the token axis that start at the expert's run. With X exact along the tokens (inexact
+    # across) and the dgrad operands exact as above, dW1 must equal X^T times da rounded in those
+    # blocks, expert by expert.
+    rng = np.random.default_rng(17)
+    T, H, F, E, k = 64, 64, 64, 4, 2
+    x = _axis_structured(rng, (T, H), 0)
+    W1 = np.stack([_axis_structured(rng, (H, F), 1) for _ in range(E)])
+    W3 = np.stack([_axis_structured(rng, (H, F), 1) for _ in range(E)])
+    W2 = np.stack([_axis_structured(rng, (F, H), 1) for _ in range(E)])
+    Wr = rng.standard_normal((H, E)) * 0.3
+    dout = _axis_structured(rng, (T, H), 1)
+    f64 = O.forward(x, Wr, None, W1, W3, W2, k)
+    Xs = f64["Xs"]
+    assert (O.mx_roundtrip(Xs, 1) != Xs).any()                 # rows of Xs are not exact along H
+    g64 = O.backward(f64, dout, x, Wr, W1, W3, W2)
+    gmx = O.backward(dict(f64, precision="mxfp8"), dout, x, Wr, W1, W3, W2)
+    da = g64["da"]
+    want = np.zeros_like(g64["dW1"])
+    for e, s0, s1 in O.expert_segments(f64):                  # one run per expert (one macrobatch)
+        want[e] = Xs[s0:s1].T @ O.mx_roundtrip_segments(da[s0:s1], [0], [s1 - s0])
+    np.testing.assert_allclose(gmx["dW1"], want, rtol=1e-12, atol=1e-300)
+    assert O.max_abs_rel(gmx["dW1"], g64["dW1"]) > 1e-6
