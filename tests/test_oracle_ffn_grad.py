@@ -81,17 +81,23 @@ def test_linear_in_W2():
     np.testing.assert_allclose(f3, 2.0 * f1 - 3.0 * f2, rtol=1e-11, atol=1e-12)
 
 
-def loss(x, Wr, bias, W1, W3, W2, k, dout, ids):
-    return float(np.sum(dout * O.forward(x, Wr, bias, W1, W3, W2, k, ids=ids)["out"]))
+def loss(x, Wr, bias, W1, W3, W2, k, dout, ids, macro=0):
+    return float(np.sum(dout * O.forward(x, Wr, bias, W1, W3, W2, k, ids=ids, macrobatch_tokens=macro)["out"]))
 
 
-def test_gradients_match_central_differences():
-    T, H, E, F, k = 4, 8, 4, 16, 2
+@pytest.mark.parametrize("macro", [0, 3])
+def test_gradients_match_central_differences(macro):
+    # macro = 3 splits the 6 tokens into two macrobatches, so experts have one run of
+    # sorted rows in each and the weight gradients must contract over both runs
+    T, H, E, F, k = 6, 8, 4, 16, 2
     x, Wr, W1, W3, W2 = rand_layer(6, T, H, E, F, wstd=0.4, rstd=1.0)
     bias = np.array([0.3, -0.2, 0.1, 0.0])
     dout = np.random.default_rng(7).standard_normal((T, H))
-    f = O.forward(x, Wr, bias, W1, W3, W2, k)
+    f = O.forward(x, Wr, bias, W1, W3, W2, k, macrobatch_tokens=macro)
     assert O.topk_margin(f["logits"], k).min() > 1e-3      # selection stays fixed under perturbation
+    if macro:
+        runs = np.bincount([e for e, _, _ in O.expert_segments(f)], minlength=E)
+        assert runs.max() >= 2                              # some expert really has two runs
     g = O.backward(f, dout, x, Wr, W1, W3, W2)
     ids = f["ids"]
     eps = 1e-6
@@ -104,9 +110,9 @@ def test_gradients_match_central_differences():
             i = it.multi_index
             old = P[i]
             P[i] = old + eps
-            lp = loss(params["x"], params["Wr"], bias, params["W1"], params["W3"], params["W2"], k, dout, ids)
+            lp = loss(params["x"], params["Wr"], bias, params["W1"], params["W3"], params["W2"], k, dout, ids, macro)
             P[i] = old - eps
-            lm = loss(params["x"], params["Wr"], bias, params["W1"], params["W3"], params["W2"], k, dout, ids)
+            lm = loss(params["x"], params["Wr"], bias, params["W1"], params["W3"], params["W2"], k, dout, ids, macro)
             P[i] = old
             num[i] = (lp - lm) / (2 * eps)
         scale = max(np.abs(num).max(), 1e-3)

@@ -206,11 +206,28 @@ def test_mxfp8_backward_dgrads_quantise_along_their_contraction_axes():
     assert O.max_abs_rel(gmx["dx"], g64["dx"]) > 1e-6      # da, db rounding is visible
 
 
-def test_mxfp8_weight_gradient_quantises_along_the_token_axis():
+def _runs(fwd):
+    """Per expert, the (start, end) of its runs of sorted rows, in macrobatch order."""
+    runs = {}
+    for e, s0, s1 in O.expert_segments(fwd):
+        runs.setdefault(e, []).append((s0, s1))
+    return runs
+
+
+def _token_blocks(v, s0, s1):
+    """v's rows s0..s1 (one run) rounded in 32-row blocks along the token axis that start
+    at the run's first row."""
+    return O.mx_roundtrip_segments(v[s0:s1], [0], [s1 - s0])
+
+
+@pytest.mark.parametrize("macro", [0, 24])
+def test_mxfp8_weight_gradient_quantises_along_the_token_axis(macro):
     # dW1 = X^T da contracts over each expert's rows: both operands are rounded in 32-row blocks
-    # along the token axis that start at the expert's run. With X exact along the tokens (inexact
-    # across) and the dgrad operands exact as above, dW1 must equal X^T times da rounded in those
-    # blocks, expert by expert.
+    # along the token axis that start at each (macrobatch, expert) run and never cross it. With X
+    # exact along the tokens (inexact across) and the dgrad operands exact as above, dW1 must equal
+    # the sum over the expert's runs of X_run^T times da_run rounded in the run's own blocks.
+    # macro = 24 gives three macrobatches, so experts have several runs whose lengths are not
+    # multiples of 32: a block that starts anywhere but the run's first row changes the result.
     rng = np.random.default_rng(17)
     T, H, F, E, k = 64, 64, 64, 4, 2
     x = _axis_structured(rng, (T, H), 0)
@@ -219,14 +236,116 @@ def test_mxfp8_weight_gradient_quantises_along_the_token_axis():
     W2 = np.stack([_axis_structured(rng, (F, H), 1) for _ in range(E)])
     Wr = rng.standard_normal((H, E)) * 0.3
     dout = _axis_structured(rng, (T, H), 1)
-    f64 = O.forward(x, Wr, None, W1, W3, W2, k)
+    f64 = O.forward(x, Wr, None, W1, W3, W2, k, macrobatch_tokens=macro)
     Xs = f64["Xs"]
     assert (O.mx_roundtrip(Xs, 1) != Xs).any()                 # rows of Xs are not exact along H
     g64 = O.backward(f64, dout, x, Wr, W1, W3, W2)
     gmx = O.backward(dict(f64, precision="mxfp8"), dout, x, Wr, W1, W3, W2)
     da = g64["da"]
+    runs = _runs(f64)
+    if macro:
+        assert max(len(r) for r in runs.values()) >= 2
+        assert any((s1 - s0) % 32 for r in runs.values() for s0, s1 in r)
     want = np.zeros_like(g64["dW1"])
-    for e, s0, s1 in O.expert_segments(f64):                  # one run per expert (one macrobatch)
-        want[e] = Xs[s0:s1].T @ O.mx_roundtrip_segments(da[s0:s1], [0], [s1 - s0])
+    for e, rr in runs.items():
+        for s0, s1 in rr:
+            want[e] += Xs[s0:s1].T @ _token_blocks(da, s0, s1)
     np.testing.assert_allclose(gmx["dW1"], want, rtol=1e-12, atol=1e-300)
     assert O.max_abs_rel(gmx["dW1"], g64["dW1"]) > 1e-6
+
+
+def _sorted_row_weights(fwd):
+    return fwd["w"].reshape(-1)[fwd["sorted_to_slot"].astype(np.int64)]
+
+
+def test_mxfp8_dW2_rounds_hw_along_the_token_axis():
+    # dW2 = (w h)^T dY contracts over each expert's rows. With dout exact along the tokens (one
+    # power-of-two scale per column, inexact across the columns), the dY operand is unchanged by
+    # its token-axis rounding, so dW2 must equal the sum over runs of (w h)_run rounded in the
+    # run's 32-row blocks, transposed, times dY_run.
+    rng = np.random.default_rng(19)
+    T, H, F, E, k = 64, 64, 64, 4, 2
+    x = rng.standard_normal((T, H))
+    W1 = rng.standard_normal((E, H, F)) * 0.2
+    W3 = rng.standard_normal((E, H, F)) * 0.2
+    W2 = rng.standard_normal((E, F, H)) * 0.2
+    Wr = rng.standard_normal((H, E)) * 0.3
+    dout = _axis_structured(rng, (T, H), 0)
+    assert (O.mx_roundtrip(dout, 0) == dout).all() and (O.mx_roundtrip(dout, 1) != dout).any()
+    f64 = O.forward(x, Wr, None, W1, W3, W2, k, macrobatch_tokens=24)
+    g64 = O.backward(f64, dout, x, Wr, W1, W3, W2)
+    gmx = O.backward(dict(f64, precision="mxfp8"), dout, x, Wr, W1, W3, W2)
+    hw = _sorted_row_weights(f64)[:, None] * f64["h"]
+    Gin = dout[f64["tok"]]
+    want = np.zeros_like(g64["dW2"])
+    for e, rr in _runs(f64).items():
+        for s0, s1 in rr:
+            assert (_token_blocks(Gin, s0, s1) == Gin[s0:s1]).all()
+            want[e] += _token_blocks(hw, s0, s1).T @ Gin[s0:s1]
+    np.testing.assert_allclose(gmx["dW2"], want, rtol=1e-12, atol=1e-300)
+    assert O.max_abs_rel(gmx["dW2"], g64["dW2"]) > 1e-6      # the h.w rounding is visible
+
+
+def test_mxfp8_dW2_rounds_dy_along_the_token_axis():
+    # The other operand of dW2. A layer built so that h.w is exact along the tokens: k = 1
+    # (w = 1); x[t] = c_t e_0 + e_(1 + chosen expert) with c_t in {1, 2, 4}; W1 and W3 read only
+    # x[:, 0], with W1[e][0, :] = 64 so a = 64 c_t and sigmoid(a) rounds to exactly 1 in
+    # float64 (silu(a) = a); W3[e][0, f] a signed power of two; so h[t, f] = 64 c_t^2 W3[e][0, f]
+    # and every column of h within a run holds powers of two at most 16x apart (exact at one
+    # scale). The router reads only the one-hot part. dout is exact along H and inexact along the
+    # tokens, so dW2 must equal (w h)_run^T times dY_run rounded in the run's 32-row blocks.
+    rng = np.random.default_rng(23)
+    T, H, F, E, k = 96, 64, 64, 4, 1
+    c = rng.choice(np.array([1.0, 2.0, 4.0]), T)
+    chosen = rng.integers(0, E, T)
+    x = np.zeros((T, H))
+    x[:, 0] = c
+    x[np.arange(T), 1 + chosen] = 1.0
+    Wr = np.zeros((H, E))
+    Wr[1 + np.arange(E), np.arange(E)] = 10.0
+    W1 = np.zeros((E, H, F)); W3 = np.zeros((E, H, F))
+    W1[:, 0, :] = 64.0
+    W3[:, 0, :] = rng.choice(np.array([-1.0, 1.0]), (E, F)) * 2.0 ** rng.integers(-3, 4, (E, F))
+    W2 = rng.standard_normal((E, F, H)) * 0.2
+    dout = _axis_structured(rng, (T, H), 1)
+    assert (O.mx_roundtrip(dout, 1) == dout).all() and (O.mx_roundtrip(dout, 0) != dout).any()
+    f64 = O.forward(x, Wr, None, W1, W3, W2, k, macrobatch_tokens=40)
+    np.testing.assert_array_equal(f64["ids"][:, 0], chosen)
+    g64 = O.backward(f64, dout, x, Wr, W1, W3, W2)
+    gmx = O.backward(dict(f64, precision="mxfp8"), dout, x, Wr, W1, W3, W2)
+    hw = _sorted_row_weights(f64)[:, None] * f64["h"]
+    Gin = dout[f64["tok"]]
+    runs = _runs(f64)
+    assert max(len(r) for r in runs.values()) >= 2
+    want = np.zeros_like(g64["dW2"])
+    for e, rr in runs.items():
+        for s0, s1 in rr:
+            assert (_token_blocks(hw, s0, s1) == hw[s0:s1]).all()    # the structure holds
+            want[e] += hw[s0:s1].T @ _token_blocks(Gin, s0, s1)
+    np.testing.assert_allclose(gmx["dW2"], want, rtol=1e-12, atol=1e-300)
+    # the dY rounding is visible (the rows scaled by 2^-20 lose most of their bits)
+    assert O.max_abs_rel(gmx["dW2"], g64["dW2"]) > 1e-8
+
+
+def test_mxfp8_backward_rounds_dy_along_H():
+    # The GEMM2 dgrad reads dY quantised along H. With W2 exact along H, that is the only
+    # rounding before da, db and dlogits, so with a dout that is NOT exact along H the emulated
+    # backward must give exactly what the float64 backward gives for dout rounded along H first
+    # (and visibly not what it gives for the unrounded dout).
+    rng = np.random.default_rng(29)
+    T, H, F, E, k = 64, 64, 64, 4, 2
+    x = rng.standard_normal((T, H))
+    W1 = np.stack([_axis_structured(rng, (H, F), 1) for _ in range(E)])
+    W3 = np.stack([_axis_structured(rng, (H, F), 1) for _ in range(E)])
+    W2 = np.stack([_axis_structured(rng, (F, H), 1) for _ in range(E)])
+    Wr = rng.standard_normal((H, E)) * 0.3
+    dout = rng.standard_normal((T, H))
+    dq = O.mx_roundtrip(dout, 1)
+    assert (dq != dout).any()
+    f64 = O.forward(x, Wr, None, W1, W3, W2, k)
+    gq = O.backward(f64, dq, x, Wr, W1, W3, W2)
+    g64 = O.backward(f64, dout, x, Wr, W1, W3, W2)
+    gmx = O.backward(dict(f64, precision="mxfp8"), dout, x, Wr, W1, W3, W2)
+    for key in ("da", "db", "dlogits"):
+        np.testing.assert_array_equal(gmx[key], gq[key], err_msg=key)
+    assert O.max_abs_rel(g64["da"], gq["da"]) > 1e-6

@@ -27,8 +27,11 @@ def _pins(module, *names):
             if n == "test_schedule_matches_bruteforce":
                 for case in SCHED_CASES:
                     fn(*case)
-            elif n == "test_forward_equals_dense_masked":
+            elif n in ("test_forward_equals_dense_masked", "test_gradients_match_central_differences"):
                 for macro in (0, 3):
+                    fn(macro)
+            elif n == "test_mxfp8_weight_gradient_quantises_along_the_token_axis":
+                for macro in (0, 24):
                     fn(macro)
             else:
                 fn()
@@ -43,6 +46,9 @@ GRAD = _pins(FG, "test_gradients_match_central_differences")
 MXF = _pins(MX, "test_mxfp8_forward_quantises_each_operand_along_its_contraction_axis")
 MXB = _pins(MX, "test_mxfp8_backward_dgrads_quantise_along_their_contraction_axes")
 MXW = _pins(MX, "test_mxfp8_weight_gradient_quantises_along_the_token_axis")
+MXW2H = _pins(MX, "test_mxfp8_dW2_rounds_hw_along_the_token_axis")
+MXW2G = _pins(MX, "test_mxfp8_dW2_rounds_dy_along_the_token_axis")
+MXDY = _pins(MX, "test_mxfp8_backward_rounds_dy_along_H")
 
 # (what the mistake is, text in the oracle, its replacement, the pins that must notice it)
 MUTATIONS = [
@@ -83,6 +89,18 @@ MUTATIONS = [
      "Xe, dae, dbe, hwe, Ge = q(Xe), dae, q(dbe), q(hwe), q(Ge)", MXW),
     ("MXFP8: X along H for dW1", "Xe, dae, dbe, hwe, Ge = q(Xe), q(dae), q(dbe), q(hwe), q(Ge)",
      "Xe, dae, dbe, hwe, Ge = mx_roundtrip(Xe, 1), q(dae), q(dbe), q(hwe), q(Ge)", MXW),
+    ("weight gradients from each expert's first run only",
+     "idx = np.concatenate([np.arange(s0, s1) for s0, s1 in es])",
+     "idx = np.concatenate([np.arange(s0, s1) for s0, s1 in es[:1]])", GRAD),
+    ("MXFP8: h.w not rounded for dW2", "Xe, dae, dbe, hwe, Ge = q(Xe), q(dae), q(dbe), q(hwe), q(Ge)",
+     "Xe, dae, dbe, hwe, Ge = q(Xe), q(dae), q(dbe), hwe, q(Ge)", MXW2H),
+    ("MXFP8: dY not rounded for dW2", "Xe, dae, dbe, hwe, Ge = q(Xe), q(dae), q(dbe), q(hwe), q(Ge)",
+     "Xe, dae, dbe, hwe, Ge = q(Xe), q(dae), q(dbe), q(hwe), Ge", MXW2G),
+    ("MXFP8: token-axis blocks start at the expert's first run, not at each run",
+     "starts.append(pos); pos += s1 - s0; ends.append(pos)",
+     "starts.append(0); pos += s1 - s0; ends.append(pos)", MXW),
+    ("MXFP8: dY not rounded along H for the GEMM2 dgrad", "G = mx_roundtrip(Ge, 1) @ mx_roundtrip(W2e, 1).T",
+     "G = Ge @ mx_roundtrip(W2e, 1).T", MXDY),
 ]
 
 
