@@ -135,9 +135,16 @@ def mx_dequantize(codes: np.ndarray, scales: np.ndarray, axis: int) -> np.ndarra
 
 
 def mx_roundtrip(v: np.ndarray, axis: int) -> np.ndarray:
-    """Quantise to MXFP8 along `axis` and return the represented values."""
-    c, s = mx_quantize(v, axis)
-    return mx_dequantize(c, s, axis)
+    """Quantise to MXFP8 along `axis` and return the represented values: each
+    element rounded to E4M3 at its block's scale, times that scale (the codes
+    of mx_quantize decoded by mx_dequantize, without forming the bytes)."""
+    v = np.moveaxis(np.asarray(v, dtype=np.float64), axis, -1)
+    n = v.shape[-1]
+    assert n % MX_BLOCK == 0, "MX blocks need a multiple of 32 elements"
+    blk = v.reshape(v.shape[:-1] + (n // MX_BLOCK, MX_BLOCK))
+    scale = np.exp2(mx_scale_exponent(np.abs(blk).max(axis=-1)).astype(np.float64))[..., None]
+    out = (e4m3_round(blk / scale) * scale).reshape(v.shape)
+    return np.moveaxis(out, -1, axis)
 
 
 def mx_roundtrip_segments(v: np.ndarray, seg_starts, seg_ends) -> np.ndarray:
@@ -274,14 +281,23 @@ def forward(x, Wr, bias, W1, W3, W2, k, *, precision="bf16", macrobatch_tokens=0
     F = W1.shape[2]
     a = np.zeros((R, F)); b = np.zeros((R, F)); h = np.zeros((R, F)); Y = np.zeros((R, H))
     mx = precision == "mxfp8"
+    wq = {}   # MXFP8: each expert's weight copies, quantised once for all its runs
+
+    def weights(e):
+        if e not in wq:
+            W1e, W3e, W2e = (np.asarray(W[e], np.float64) for W in (W1, W3, W2))
+            if mx:
+                W1e = mx_roundtrip(W1e, 0)
+                W3e = mx_roundtrip(W3e, 0)
+                W2e = mx_roundtrip(W2e, 0)
+            wq[e] = (W1e, W3e, W2e)
+        return wq[e]
+
     for e, s0, s1 in expert_segments(sch):
         Xe = Xs[s0:s1]
-        W1e, W3e, W2e = (np.asarray(W[e], np.float64) for W in (W1, W3, W2))
+        W1e, W3e, W2e = weights(e)
         if mx:
             Xe = mx_roundtrip(Xe, 1)
-            W1e = mx_roundtrip(W1e, 0)
-            W3e = mx_roundtrip(W3e, 0)
-            W2e = mx_roundtrip(W2e, 0)
         a[s0:s1] = Xe @ W1e
         b[s0:s1] = Xe @ W3e
         h[s0:s1] = silu(a[s0:s1]) * b[s0:s1]
@@ -320,11 +336,23 @@ def backward(fwd, dout, x, Wr, W1, W3, W2):
     dW1 = np.zeros((E, H, F)); dW3 = np.zeros((E, H, F)); dW2 = np.zeros((E, F, H))
     da_all = np.zeros((R, F)); db_all = np.zeros((R, F)); hw_all = np.zeros((R, F))
     segs = expert_segments(fwd)
+    wq = {}   # MXFP8: each expert's dgrad weight copies, quantised once for all its runs
+
+    def weights(e):
+        if e not in wq:
+            W1e, W3e, W2e = (np.asarray(W[e], np.float64) for W in (W1, W3, W2))
+            if mx:
+                W1e = mx_roundtrip(W1e, 1)     # K = F
+                W3e = mx_roundtrip(W3e, 1)     # K = F
+                W2e = mx_roundtrip(W2e, 1)     # K = H
+            wq[e] = (W1e, W3e, W2e)
+        return wq[e]
+
     for e, s0, s1 in segs:
-        W1e, W3e, W2e = (np.asarray(W[e], np.float64) for W in (W1, W3, W2))
+        W1e, W3e, W2e = weights(e)
         Ge = Gin[s0:s1]
         if mx:
-            G = mx_roundtrip(Ge, 1) @ mx_roundtrip(W2e, 1).T     # K = H
+            G = mx_roundtrip(Ge, 1) @ W2e.T     # K = H
         else:
             G = Ge @ W2e.T
         ae, be, he = a[s0:s1], b[s0:s1], h[s0:s1]
@@ -336,8 +364,7 @@ def backward(fwd, dout, x, Wr, W1, W3, W2):
         da_all[s0:s1] = da; db_all[s0:s1] = db
         hw_all[s0:s1] = wrow[s0:s1, None] * he
         if mx:
-            dX[s0:s1] = (mx_roundtrip(da, 1) @ mx_roundtrip(W1e, 1).T
-                         + mx_roundtrip(db, 1) @ mx_roundtrip(W3e, 1).T)      # K = F
+            dX[s0:s1] = mx_roundtrip(da, 1) @ W1e.T + mx_roundtrip(db, 1) @ W3e.T      # K = F
         else:
             dX[s0:s1] = da @ W1e.T + db @ W3e.T
     # weight gradients: contraction over each expert's rows (token axis)

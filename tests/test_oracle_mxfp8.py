@@ -104,6 +104,18 @@ def test_mx_block_properties():
     np.testing.assert_array_equal(sT, scales.T)
 
 
+def test_roundtrip_equals_dequantised_codes():
+    # mx_roundtrip forms the represented values directly; they must be exactly what the
+    # bytes of mx_quantize decode to, over the whole exponent range, zeros and both axes
+    rng = np.random.default_rng(5)
+    v = rng.standard_normal((64, 256)) * 2.0 ** rng.integers(-135, 130, (64, 256))
+    v[3] = 0.0
+    v[5, :32] = 448.0 * 2.0 ** 7
+    for axis in (0, 1):
+        c, s = O.mx_quantize(v, axis)
+        np.testing.assert_array_equal(O.mx_roundtrip(v, axis), O.mx_dequantize(c, s, axis))
+
+
 def test_segmented_token_blocks_do_not_cross_segments():
     rng = np.random.default_rng(3)
     v = rng.standard_normal((50, 32))

@@ -49,6 +49,7 @@ MXW = _pins(MX, "test_mxfp8_weight_gradient_quantises_along_the_token_axis")
 MXW2H = _pins(MX, "test_mxfp8_dW2_rounds_hw_along_the_token_axis")
 MXW2G = _pins(MX, "test_mxfp8_dW2_rounds_dy_along_the_token_axis")
 MXDY = _pins(MX, "test_mxfp8_backward_rounds_dy_along_H")
+MXRT = _pins(MX, "test_roundtrip_equals_dequantised_codes")
 
 # (what the mistake is, text in the oracle, its replacement, the pins that must notice it)
 MUTATIONS = [
@@ -81,10 +82,10 @@ MUTATIONS = [
     ("MXFP8: W2 along H in the forward", "W2e = mx_roundtrip(W2e, 0)", "W2e = mx_roundtrip(W2e, 1)", MXF),
     ("MXFP8: h not rounded", "he = mx_roundtrip(h[s0:s1], 1) if mx else h[s0:s1]", "he = h[s0:s1]", MXF),
     ("MXFP8: x along the tokens", "Xe = mx_roundtrip(Xe, 1)", "Xe = mx_roundtrip(Xe.T.copy(), 1).T", MXF),
-    ("MXFP8: W2 along F in the dgrad", "mx_roundtrip(W2e, 1).T     # K = H", "mx_roundtrip(W2e, 0).T     # K = H", MXB),
-    ("MXFP8: da not rounded for dX", "dX[s0:s1] = (mx_roundtrip(da, 1) @", "dX[s0:s1] = (da @", MXB),
-    ("MXFP8: W3 along H in the dgrad", "mx_roundtrip(db, 1) @ mx_roundtrip(W3e, 1).T",
-     "mx_roundtrip(db, 1) @ mx_roundtrip(W3e, 0).T", MXB),
+    ("MXFP8: W2 along F in the dgrad", "W2e = mx_roundtrip(W2e, 1)     # K = H", "W2e = mx_roundtrip(W2e, 0)     # K = H", MXB),
+    ("MXFP8: da not rounded for dX", "dX[s0:s1] = mx_roundtrip(da, 1) @", "dX[s0:s1] = da @", MXB),
+    ("MXFP8: W3 along H in the dgrad", "W3e = mx_roundtrip(W3e, 1)     # K = F",
+     "W3e = mx_roundtrip(W3e, 0)     # K = F", MXB),
     ("MXFP8: da not rounded for dW1", "Xe, dae, dbe, hwe, Ge = q(Xe), q(dae), q(dbe), q(hwe), q(Ge)",
      "Xe, dae, dbe, hwe, Ge = q(Xe), dae, q(dbe), q(hwe), q(Ge)", MXW),
     ("MXFP8: X along H for dW1", "Xe, dae, dbe, hwe, Ge = q(Xe), q(dae), q(dbe), q(hwe), q(Ge)",
@@ -99,8 +100,10 @@ MUTATIONS = [
     ("MXFP8: token-axis blocks start at the expert's first run, not at each run",
      "starts.append(pos); pos += s1 - s0; ends.append(pos)",
      "starts.append(0); pos += s1 - s0; ends.append(pos)", MXW),
-    ("MXFP8: dY not rounded along H for the GEMM2 dgrad", "G = mx_roundtrip(Ge, 1) @ mx_roundtrip(W2e, 1).T",
-     "G = Ge @ mx_roundtrip(W2e, 1).T", MXDY),
+    ("MXFP8: dY not rounded along H for the GEMM2 dgrad", "G = mx_roundtrip(Ge, 1) @ W2e.T",
+     "G = Ge @ W2e.T", MXDY),
+    ("MXFP8: round trip without the block scale", "out = (e4m3_round(blk / scale) * scale).reshape(v.shape)",
+     "out = e4m3_round(blk).reshape(v.shape)", MXRT),
 ]
 
 
