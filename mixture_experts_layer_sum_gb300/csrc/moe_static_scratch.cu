@@ -6,10 +6,12 @@
 // certified deployments that forbid allocation after start-up, and drivers of
 // pre-planned memory where every buffer is fixed ahead of time. For them this
 // entry point keeps its scratch (schedule chunk histograms, chunk bases,
-// padded offsets and a status word) in one file-scope device array that the
-// CUDA module reserves when the library is loaded, on every device that loads
-// it, until the process exits. It computes exactly what moe_schedule computes,
-// with the same kernels.
+// padded offsets and a status word) in one file-scope device array. The array
+// belongs to this file's CUDA module; with lazy module loading (the default) the
+// module, and with it the array's 1 MiB, is loaded on a device by the first
+// call made there, and stays until the process exits. A pool that already owns
+// every free byte can make that first call fail, so make it at start-up. The
+// entry point computes exactly what moe_schedule computes, with the same kernels.
 //
 // Limits and rules:
 //   - Capacity: kStaticScratchInts 32-bit words (1 MiB). A configuration whose
@@ -18,12 +20,16 @@
 //     device address is looked up once per device with cudaGetSymbolAddress
 //     (with that device current) on the first call made on that device, so
 //     make that first call before any stream capture begins.
+//   - The looked-up addresses are cached per device number for the life of the
+//     process. A cudaDeviceReset, or a different context made current on the
+//     device, invalidates them: do neither between calls.
 //   - Every call on a device uses the same array and leaves its contents
 //     behind; each call clears the part that must start at zero. Calls whose
 //     executions overlap on the GPU (different streams without ordering) race
 //     on the array and give undefined results.
 //   - No cudaMalloc, cudaFree or allocating library routine is called.
 #include <mutex>
+#include <string>
 
 #include "../../include/moe.h"
 #include "route_kernels.cuh"
@@ -42,6 +48,7 @@ __device__ __align__(256) int g_static_scratch[kStaticScratchInts];
 
 std::mutex g_mu;
 int *g_dev_ptr[kMaxDevices] = {};
+thread_local std::string g_last_msg;
 
 moe_status_t fail(moe_status_t st, const char *msg) {
     moe::set_last_error(msg);
@@ -76,8 +83,16 @@ extern "C" moe_status_t moe_schedule_static(const moe_config_t *cfg, const int32
         std::lock_guard<std::mutex> lock(g_mu);
         if (!g_dev_ptr[dev]) {
             void *p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p)
-                return fail(MOE_ERR_CUDA, "moe_schedule_static: cudaGetSymbolAddress failed");
+            const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+            if (e != cudaSuccess || !p) {
+                // the failure (often an out-of-memory error while the module loads) stays
+                // recorded as the runtime's last error; clear it so that it is not reported
+                // again by the next launch check of this or another entry point
+                cudaGetLastError();
+                g_last_msg = std::string("moe_schedule_static: looking up the static scratch array failed: ") +
+                             cudaGetErrorString(e);
+                return fail(MOE_ERR_CUDA, g_last_msg.c_str());
+            }
             g_dev_ptr[dev] = static_cast<int *>(p);
         }
         base = g_dev_ptr[dev];

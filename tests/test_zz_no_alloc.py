@@ -63,8 +63,22 @@ def test_static_schedule_matches_workspace_schedule_twice(moe):
 
 
 def test_static_schedule_rejects_shapes_beyond_capacity(moe):
-    # 2^20 tokens x 8 slots -> 8192 chunks x 64 experts x 2 words > 1 MiB
-    cfg = moe.make_config(1 << 20, 256, 256, 64, 8)
-    st = moe.library().moe_schedule_static(ctypes.byref(cfg), 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, None)
+    # 65536 tokens x 8 slots in macrobatches of 32 tokens: 2048 macrobatches x 64 experts
+    # need about 393 k words of scratch, over the 262 k the 1 MiB array holds. Every buffer
+    # is real and sized for the call, so a regression in the capacity check shows up as a
+    # wrong status, not as a stray access.
+    T, E, k, Mb = 65536, 64, 8, 32
+    cfg = moe.make_config(T, 256, 256, E, k, macrobatch_tokens=Mb)
+    plan = moe.moe_plan(cfg)
+    assert plan.num_macrobatches == T // Mb
+    ids = torch.from_numpy(routed_ids(5, 64, E, k)).cuda().repeat(T // 64, 1).contiguous()
+    counts = torch.zeros(plan.num_macrobatches * E, dtype=torch.int32, device="cuda")
+    offsets = torch.zeros(plan.num_macrobatches * (E + 1), dtype=torch.int32, device="cuda")
+    s2s = torch.zeros(T * k, dtype=torch.int32, device="cuda")
+    s2r = torch.zeros(T * k, dtype=torch.int32, device="cuda")
+    st = moe.library().moe_schedule_static(ctypes.byref(cfg), ids.data_ptr(), counts.data_ptr(),
+                                           offsets.data_ptr(), s2s.data_ptr(), s2r.data_ptr(), None)
     assert st == moe.MOE_ERR_UNSUPPORTED
     assert "1 MiB" in moe.moe_last_error_string()
+    torch.cuda.synchronize()
+    assert int(counts.abs().sum()) == 0 and int(s2s.abs().sum()) == 0    # nothing ran
