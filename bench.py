@@ -5,8 +5,11 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ou
 A step is one pass of the whole layer over one batch of synthetic tokens:
 router, schedule, dispatch, GEMM1+SwiGLU, GEMM2, combine, then the backward
 (reverse combine, dgrad GEMMs with the SwiGLU backward, reverse dispatch,
-router backward, weight-gradient GEMMs). The default workload is the balanced
-BF16 shape T=4096, H=2048, E=32, k=4, F=1024 (workloads.py).
+router backward, weight-gradient GEMMs). The default workload is the largest
+one, the ring workload: T=16384 tokens, H=7168, E=16 experts, k=8, F=2048,
+MXFP8 operands, through a 256 MiB ring at the wave-rule minibatch
+(workloads.py). The balanced, skewed and MXFP8 workloads are measured after it
+and reported under "other_workloads" (--only-headline skips them).
 
 Prints ONE JSON line (rank 0). `value` is whole-job tokens/s of fwd+bwd with
 inputs resident in HBM; L2 is flushed (256 MiB write) between timed steps and
@@ -42,14 +45,16 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
-def committed_traffic(name):
-    """DRAM bytes per launch of `name` from the committed ncu table, if the
+def committed_traffic(name, workload):
+    """DRAM bytes per launch of kernel `name` on `workload` from the committed ncu table, if the
     kernel sources are unchanged since the capture; else None."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
+    if d.get("workload") != workload:
+        return None
     csrc = os.path.join(ROOT, "mixture_experts_layer_sum_gb300", "csrc")
     for f, sha in d.get("sources_sha1", {}).items():
         if hashlib.sha1(open(os.path.join(csrc, f), "rb").read()).hexdigest() != sha:
@@ -91,14 +96,21 @@ def dist_env():
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def oracle_step(w, inp, ntok):
-    """fwd+bwd of the oracle on the first ntok tokens (all weights)."""
+def oracle_inputs(inp):
     from oracle import moe_oracle as O
-    o = {k: (O.bf16_to_f64(v) if k != "bias" and v is not None else v) for k, v in inp.items()}
+    return {k: (O.bf16_to_f64(v) if k != "bias" and v is not None else v) for k, v in inp.items()}
+
+
+def oracle_step(w, o, ntok, caches):
+    """fwd+bwd of the oracle on the first ntok tokens (all weights). `caches` keep the weight
+    copies between steps: like the GPU's weight quantisation (once per weight update), the
+    oracle's is made by the first, untimed, call and left out of the timed steps."""
+    from oracle import moe_oracle as O
     x, dout = o["x"][:ntok], o["dout"][:ntok]
     t0 = time.perf_counter()
-    f = O.forward(x, o["Wr"], o["bias"], o["W1"], o["W3"], o["W2"], w.k, precision=w.precision)
-    O.backward(f, dout, x, o["Wr"], o["W1"], o["W3"], o["W2"])
+    f = O.forward(x, o["Wr"], o["bias"], o["W1"], o["W3"], o["W2"], w.k, precision=w.precision,
+                  weight_cache=caches[0])
+    O.backward(f, dout, x, o["Wr"], o["W1"], o["W3"], o["W2"], weight_cache=caches[1])
     return time.perf_counter() - t0
 
 
@@ -110,19 +122,23 @@ def cpu_threads():
 
 
 def cpu_baseline(w, inp, target_s=15.0):
-    t_small = oracle_step(w, inp, 256)
-    per_tok = t_small / 256
-    ntok = int(min(w.T, max(256, target_s / max(per_tok, 1e-9))))
-    ntok = max(256, ntok // 256 * 256)
-    t = oracle_step(w, inp, ntok)
+    o = oracle_inputs(inp)
+    caches = ({}, {})
+    oracle_step(w, o, 32, caches)                 # weight copies (W0), untimed
+    t_small = oracle_step(w, o, 128, caches)
+    per_tok = t_small / 128
+    ntok = int(min(w.T, max(128, target_s / max(per_tok, 1e-9))))
+    ntok = max(128, ntok // 128 * 128)
+    t = oracle_step(w, o, ntok, caches)
     # a workload smaller than the time budget is passed over again until about 10 s of CPU work
     passes = 1
     while t < 10.0 and passes < 16:
-        t += oracle_step(w, inp, ntok)
+        t += oracle_step(w, o, ntok, caches)
         passes += 1
     return {"value": ntok * passes / t, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"{passes} x fwd+bwd of the first {ntok} of {w.T} tokens of {w.name}, all weights, "
-                      f"float64 numpy (BLAS threads = host cores), {t:.1f} s"}
+            "sample": f"{passes} x fwd+bwd of the first {ntok} of {w.T} tokens of {w.name}, all weights "
+                      f"(their {w.precision} copies made once, untimed, as the GPU's W0), float64 numpy "
+                      f"(BLAS threads = host cores), {t:.1f} s"}
 
 
 def run_reference(args, w):
@@ -130,10 +146,12 @@ def run_reference(args, w):
     if rank != 0:
         return
     inp = WL.make_inputs(w)
-    ntok = 256
+    o = oracle_inputs(inp)
+    ntok = 128 if w.precision == "mxfp8" else 256
+    caches = ({}, {})
     for _ in range(args.warmup):
-        oracle_step(w, inp, ntok)
-    times = [oracle_step(w, inp, ntok) for _ in range(args.steps)]
+        oracle_step(w, o, ntok, caches)
+    times = [oracle_step(w, o, ntok, caches) for _ in range(args.steps)]
     tot = sum(times)
     value = ntok * args.steps / tot
     line = {
@@ -143,7 +161,8 @@ def run_reference(args, w):
         "config": {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "E": w.E, "k": w.k,
                    "precision": w.precision, "sample_tokens_per_step": ntok},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
-                         "sample": f"fwd+bwd of the first {ntok} of {w.T} tokens per step, all weights"},
+                         "sample": f"fwd+bwd of the first {ntok} of {w.T} tokens per step, all weights "
+                                   f"(weight copies made in the warm-up steps, as the GPU's W0)"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -256,7 +275,8 @@ def gemm_flops(w, name):
 
 def gemm_bytes(w, name):
     """Algorithmic HBM bytes per step of each grouped GEMM: operands read once, outputs written
-    once (R = routed rows; the ring round trip of the dispatched rows is not counted)."""
+    once (R = routed rows; the ring round trip of the dispatched rows is not counted). bf16
+    operands; MXFP8 operands carry H*33/32 (or F*33/32) bytes per row instead of 2*H."""
     T, H, F, E, R = w.T, w.H, w.F, w.E, w.R
     W = E * H * F * 2   # one bf16 weight matrix of all experts
     return {"grouped_gemm_fwd1_swiglu": T * H * 2 + 2 * W + 3 * R * F * 2,
@@ -267,126 +287,153 @@ def gemm_bytes(w, name):
             "grouped_gemm_wgrad13": R * H * 2 + 2 * R * F * 2 + 2 * E * H * F * 4}.get(name)
 
 
-def layer_roofline(w, peaks, step_ms):
+GEMMS = ["grouped_gemm_fwd1_swiglu", "grouped_gemm_fwd2", "grouped_gemm_bwd2_swiglu", "grouped_gemm_bwd1",
+         "grouped_gemm_wgrad2", "grouped_gemm_wgrad13"]
+
+
+def tensor_peak(w, peaks, peak_src, loop_s):
+    """Dense tensor peak for GEMMs timed inside a loop of loop_s seconds: the burst bf16 figure
+    for a loop shorter than a second, the sustained (seconds-long, power-capped) one otherwise;
+    MXFP8 takes 2x the bf16 figure (the nominal fp8 / bf16 ratio, 4.5 vs 2.25 PFLOP/s)."""
+    burst = loop_s < 1.0 or "bf16_tflops_sustained" not in peaks
+    tf = peaks["bf16_tflops"] if burst else peaks["bf16_tflops_sustained"]
+    src = f"{peak_src} {'bf16_tflops (burst' if burst else 'bf16_tflops_sustained (sustained'}; timed loop {loop_s:.2f} s)"
+    if w.precision == "mxfp8":
+        tf, src = 2 * tf, src + " x 2 (nominal fp8/bf16 ratio)"
+    return tf, src
+
+
+def layer_roofline(w, tf, hbm, step_ms):
     """Layer roofline time: the GEMMs' flops at the tensor peak plus the memory-bound stages'
     algorithmic bytes at the HBM copy bandwidth, run back to back; frac = roofline / measured."""
-    tf = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
-    hbm = peaks.get("hbm_gbs")
-    if not tf or not hbm:
-        return None
-    if w.precision == "mxfp8":
-        tf = 2 * tf
-    gemm = ["grouped_gemm_fwd1_swiglu", "grouped_gemm_fwd2", "grouped_gemm_bwd2_swiglu", "grouped_gemm_bwd1",
-            "grouped_gemm_wgrad2", "grouped_gemm_wgrad13"]
     mem = ["dispatch", "combine", "router_topk", "reverse_combine", "reverse_dispatch", "router_wgrad"]
     if w.precision == "mxfp8":
         mem = ["dispatch_mxfp8", "combine", "router_topk", "quantize_dy", "quantize_x_tokens",
                "quantize_hw_tokens", "quantize_da_tokens", "quantize_db_tokens", "reverse_dispatch",
                "router_wgrad"]
-    t_gemm = sum(gemm_flops(w, n) for n in gemm) / (tf * 1e12)
+    t_gemm = sum(gemm_flops(w, n) for n in GEMMS) / (tf * 1e12)
     t_mem = sum(kernel_bytes(w, n) for n in mem) / (hbm * 1e9)
     t = (t_gemm + t_mem) * 1e3
     return {"time_ms": t, "gemm_ms": t_gemm * 1e3, "hbm_ms": t_mem * 1e3, "frac": t / step_ms,
             "note": "sum of GEMM flops / peak tensor rate and memory-stage algorithmic bytes / HBM copy bandwidth"}
 
 
-def run_ours(args, w):
-    import torch
-    ws, rank, local = dist_env()
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    from mixture_experts_layer_sum_gb300 import build_ext
-    build_ext.build()
-    import mixture_experts_layer_sum_gb300.moe as M
-    from mixture_experts_layer_sum_gb300.layer import MoeLayer
+def rate_kernels(w, kernels, steps, prof_ms, peaks, peak_src, loop_s):
+    """Per-kernel rates of a profiled run, the dominant kernel's roofline and the grouped GEMMs'
+    fraction of the tensor peak. kernels: [(name, launches, total ms)] over `steps` steps."""
+    tf, tf_src = tensor_peak(w, peaks, peak_src, loop_s)
+    hbm = peaks.get("hbm_gbs")
+    kt = sorted(kernels, key=lambda r: -r[2])
+    rows = []
+    for nm, n_, ms_ in kt:
+        row = {"name": nm, "launches": n_, "ms_per_step": ms_ / steps, "share": ms_ / prof_ms}
+        if gemm_flops(w, nm):
+            row["tflops"] = gemm_flops(w, nm) * steps / (ms_ * 1e-3) / 1e12
+            row["frac_of_tensor_peak"] = row["tflops"] / tf
+        if kernel_bytes(w, nm) and hbm:
+            row["gbs"] = kernel_bytes(w, nm) * steps / (ms_ * 1e-3) / 1e9
+            row["frac_of_hbm"] = row["gbs"] / hbm
+        rows.append(row)
+    # dominant kernel: the largest share of the profiled step; a kernel may launch several
+    # times per step (once per macrobatch), so per-launch work = per-step work / launches per step
+    name, n, ms = kt[0]
+    per_launch_ms = ms / n
+    per_step = n / steps
+    roof = None
+    if gemm_flops(w, name):
+        fl = gemm_flops(w, name) / per_step
+        ach = fl / (per_launch_ms * 1e-3) / 1e12
+        roof = {"kernel": name, "bound": "tensor", "achieved": ach, "peak": tf, "unit": "TFLOP/s",
+                "frac": ach / tf, "traffic": committed_traffic(name, w.name), "algorithmic_per_launch": fl,
+                "peak_source": tf_src}
+        if w.precision == "bf16" and hbm:
+            gb = gemm_bytes(w, name) / per_step
+            roof["hbm_rating"] = {"algorithmic_bytes_per_launch": gb,
+                                  "achieved_gbs": gb / (per_launch_ms * 1e-3) / 1e9,
+                                  "frac_of_hbm": gb / (per_launch_ms * 1e-3) / 1e9 / hbm}
+    elif kernel_bytes(w, name) is not None and hbm:
+        gb = kernel_bytes(w, name) / per_step
+        ach = gb / (per_launch_ms * 1e-3) / 1e9
+        roof = {"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "traffic": committed_traffic(name, w.name), "algorithmic_per_launch": gb,
+                "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"}
+    gemm_ms = sum(ms_ for nm, _, ms_ in kernels if nm.startswith("grouped_gemm"))
+    gemm_fl = sum(gemm_flops(w, nm) * steps for nm, _, _ in kernels if gemm_flops(w, nm))
+    gg = None
+    if gemm_ms:
+        t = gemm_fl / (gemm_ms * 1e-3) / 1e12
+        gg = {"tflops": t, "frac_of_peak": t / tf, "peak": tf, "peak_source": tf_src,
+              "share_of_step": gemm_ms / prof_ms}
+    return rows, roof, gg, tf
 
-    inp = WL.make_inputs(w.with_(seed=w.seed + rank))
-    dev = torch.device("cuda", local)
 
-    def to_dev(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+class Gpu:
+    """The device-side pieces of one measured workload: inputs in HBM, the layer, its output buffers."""
 
-    d = {k: to_dev(v) for k, v in inp.items() if k != "bias" and v is not None}
-    bias = torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None
-    layer = MoeLayer(w.T, w.H, w.F, w.E, w.k, w.precision, device=dev, ring_bytes=w.ring_bytes)
-    stream = torch.cuda.Stream(device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    out = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
-    ids = torch.empty(w.T, w.k, dtype=torch.int32, device=dev)
-    wts = torch.empty(w.T, w.k, dtype=torch.float32, device=dev)
-    dx = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
-    dWr = torch.empty(w.H, w.E, dtype=torch.float32, device=dev)
-    dW1 = torch.empty(w.E, w.H, w.F, dtype=torch.float32, device=dev)
-    dW3 = torch.empty_like(dW1)
-    dW2 = torch.empty(w.E, w.F, w.H, dtype=torch.float32, device=dev)
+    def __init__(self, w, dev, rank, M, MoeLayer, torch):
+        self.w, self.dev, self.torch = w, dev, torch
+        self.inp = WL.make_inputs(w.with_(seed=w.seed + rank))
+        self.d = {k: self.to_dev(v) for k, v in self.inp.items() if k != "bias" and v is not None}
+        self.bias = torch.from_numpy(self.inp["bias"]).to(dev) if self.inp["bias"] is not None else None
+        self.layer = MoeLayer(w.T, w.H, w.F, w.E, w.k, w.precision, device=dev, ring_bytes=w.ring_bytes)
+        self.stream = torch.cuda.Stream(device=dev)
+        bf, f32 = torch.bfloat16, torch.float32
+        self.out = torch.empty(w.T, w.H, dtype=bf, device=dev)
+        self.ids = torch.empty(w.T, w.k, dtype=torch.int32, device=dev)
+        self.wts = torch.empty(w.T, w.k, dtype=f32, device=dev)
+        self.dx = torch.empty(w.T, w.H, dtype=bf, device=dev)
+        self.dWr = torch.empty(w.H, w.E, dtype=f32, device=dev)
+        self.dW1 = torch.empty(w.E, w.H, w.F, dtype=f32, device=dev)
+        self.dW3 = torch.empty_like(self.dW1)
+        self.dW2 = torch.empty(w.E, w.F, w.H, dtype=f32, device=dev)
+        if w.precision == "mxfp8":
+            self.quantize()
 
-    if w.precision == "mxfp8":
-        layer.quantize_weights(d["W1"], d["W3"], d["W2"], stream=stream)
+    def to_dev(self, a):
+        t = self.torch
+        return t.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(t.bfloat16).to(self.dev)
 
-    def fwd():
-        layer.forward(d["x"], d["Wr"], bias, d["W1"], d["W3"], d["W2"], out, ids, wts, stream=stream)
+    def quantize(self):
+        d = self.d
+        self.layer.quantize_weights(d["W1"], d["W3"], d["W2"], stream=self.stream)
 
-    def step():
-        fwd()
-        layer.backward(d["dout"], d["x"], d["Wr"], d["W1"], d["W3"], d["W2"], dx, dWr, dW1, dW3, dW2,
-                       stream=stream)
+    def fwd(self, layer=None, x=None, out=None):
+        d = self.d
+        (layer or self.layer).forward(d["x"] if x is None else x, d["Wr"], self.bias, d["W1"], d["W3"], d["W2"],
+                                      self.out if out is None else out, self.ids, self.wts, stream=self.stream)
 
-    def barrier():
-        torch.cuda.synchronize(dev)
-        if ws > 1:
-            import torch.distributed as dist
-            dist.barrier()
-        torch.cuda.synchronize(dev)
+    def bwd(self, layer=None, x=None, dout=None, dx=None):
+        d = self.d
+        (layer or self.layer).backward(d["dout"] if dout is None else dout, d["x"] if x is None else x, d["Wr"],
+                                       d["W1"], d["W3"], d["W2"], self.dx if dx is None else dx, self.dWr,
+                                       self.dW1, self.dW3, self.dW2, stream=self.stream)
 
-    def timed(fn, k):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
-        with torch.cuda.stream(stream):
-            for a, b in evs:
-                flush.fill_(1)                # evict L2 between timed steps (untimed)
-                a.record(stream)
-                fn()
-                b.record(stream)
-        stream.synchronize()
-        return sum(a.elapsed_time(b) for a, b in evs)
+    def step(self, layer=None):
+        self.fwd(layer)
+        self.bwd(layer)
 
-    props = torch.cuda.get_device_properties(dev)
-    try:
-        bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
-        sampler = NvmlClockSampler(bus)
-        clk_p = clk_path = None
-    except Exception:
-        sampler = None
-        clk_p, clk_path = start_clocks(local)
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
-    layer.status(stream)
-    barrier()
-    total_ms = timed(step, args.steps)
-    w0_ms = None
-    if w.precision == "mxfp8":
-        # weight quantisation runs once per weight update, outside the step; timed on its own
-        w0_ms = timed(lambda: layer.quantize_weights(d["W1"], d["W3"], d["W2"], stream=stream), args.steps)
-        w0_ms, = max_over_ranks([w0_ms], device=dev)   # every rank has the same precision
-    barrier()
-    fwd_ms = timed(fwd, args.steps)
-    layer.status(stream)
-    total_ms, fwd_ms = max_over_ranks([total_ms, fwd_ms], device=dev)
 
-    # per-kernel breakdown: the same steps with events around every launch
-    M.moe_profile_begin()
-    prof_ms = timed(step, args.steps)
-    kernels = M.moe_profile_end()
-    launches = sum(n for _, n, _ in kernels)
+def timed(g, flush, fn, k):
+    torch = g.torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+    with torch.cuda.stream(g.stream):
+        for a, b in evs:
+            flush.fill_(1)                # evict L2 between timed steps (untimed)
+            a.record(g.stream)
+            fn()
+            b.record(g.stream)
+    g.stream.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs)
 
-    # end to end through the public API with host buffers: every step copies its x and dout
-    # from pinned host memory to the device and reads its out and dx back. The copies run on
-    # their own streams and the device buffers are double-buffered, so step i+1's inputs
-    # arrive while step i computes, out leaves during the backward and dx during the next
-    # step (the usual input/output pipeline of a training or serving loop). The timed region
-    # runs from the first host-to-device copy to the end of the last device-to-host copy.
+
+def e2e_ms(g, steps):
+    """End to end through the public API with host buffers: every step copies its x and dout
+    from pinned host memory to the device and reads its out and dx back. The copies run on their
+    own streams and the device buffers are double-buffered, so step i+1's inputs arrive while
+    step i computes, out leaves during the backward and dx during the next step (the usual
+    input/output pipeline of a training or serving loop). The timed region runs from the first
+    host-to-device copy to the end of the last device-to-host copy."""
+    torch, dev, w, d = g.torch, g.dev, g.w, g.d
     hx = torch.empty(w.T, w.H, dtype=torch.bfloat16, pin_memory=True)
     hd = torch.empty_like(hx, pin_memory=True)
     hx.copy_(d["x"].cpu())
@@ -396,12 +443,13 @@ def run_ours(args, w):
     hdx = [torch.empty_like(hx, pin_memory=True) for _ in range(NB)]
     xin = [torch.empty_like(d["x"]) for _ in range(NB)]
     din = [torch.empty_like(d["dout"]) for _ in range(NB)]
-    outb = [torch.empty_like(out) for _ in range(NB)]
-    dxb = [torch.empty_like(dx) for _ in range(NB)]
+    outb = [torch.empty_like(g.out) for _ in range(NB)]
+    dxb = [torch.empty_like(g.dx) for _ in range(NB)]
     h2d = torch.cuda.Stream(device=dev)
     d2h = torch.cuda.Stream(device=dev)
+    stream = g.stream
 
-    def e2e_run(k):
+    def run(k):
         ev = lambda: torch.cuda.Event()
         used = [None] * NB      # compute done with slot b (inputs free)
         drained = [None] * NB   # outputs of slot b read back (output buffers free)
@@ -419,14 +467,13 @@ def run_ours(args, w):
             stream.wait_event(ex)
             if drained[b] is not None:
                 stream.wait_event(drained[b])
-            layer.forward(xin[b], d["Wr"], bias, d["W1"], d["W3"], d["W2"], outb[b], ids, wts, stream=stream)
+            g.fwd(x=xin[b], out=outb[b])
             ef = ev(); ef.record(stream)
             with torch.cuda.stream(d2h):
                 d2h.wait_event(ef)
                 hout[b].copy_(outb[b], non_blocking=True)
             stream.wait_event(ed)
-            layer.backward(din[b], xin[b], d["Wr"], d["W1"], d["W3"], d["W2"], dxb[b], dWr, dW1, dW3, dW2,
-                           stream=stream)
+            g.bwd(x=xin[b], dout=din[b], dx=dxb[b])
             eb = ev(); eb.record(stream)
             used[b] = eb
             with torch.cuda.stream(d2h):
@@ -439,10 +486,126 @@ def run_ours(args, w):
         torch.cuda.synchronize(dev)
         return t0.elapsed_time(t1)
 
-    e2e_run(2)
-    e2e_ms = e2e_run(args.steps)
-    e2e_ms, = max_over_ranks([e2e_ms], device=dev)
-    layer.status(stream)
+    run(2)
+    return run(steps)
+
+
+def run_ours(args, w):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from mixture_experts_layer_sum_gb300 import build_ext
+    build_ext.build()
+    import mixture_experts_layer_sum_gb300.moe as M
+    from mixture_experts_layer_sum_gb300.layer import MoeLayer
+    dev = torch.device("cuda", local)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    g = Gpu(w, dev, rank, M, MoeLayer, torch)
+    plan = (g.layer.plan.num_macrobatches, g.layer.plan.macrobatch_tokens, g.layer.plan.minibatch_rows)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    props = torch.cuda.get_device_properties(dev)
+    try:
+        bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+        sampler = NvmlClockSampler(bus)
+        clk_p = clk_path = None
+    except Exception:
+        sampler = None
+        clk_p, clk_path = start_clocks(local)
+    with torch.cuda.stream(g.stream):
+        for _ in range(args.warmup):
+            g.step()
+    g.layer.status(g.stream)
+    barrier()
+    total_ms = timed(g, flush, g.step, args.steps)
+    w0_ms = None
+    if w.precision == "mxfp8":
+        # weight quantisation runs once per weight update, outside the step; timed on its own
+        w0_ms = timed(g, flush, g.quantize, args.steps)
+        w0_ms, = max_over_ranks([w0_ms], device=dev)   # every rank has the same precision
+    barrier()
+    fwd_ms = timed(g, flush, g.fwd, args.steps)
+    g.layer.status(g.stream)
+    total_ms, fwd_ms = max_over_ranks([total_ms, fwd_ms], device=dev)
+
+    # per-kernel breakdown: the same steps with events around every launch
+    M.moe_profile_begin()
+    prof_ms = timed(g, flush, g.step, args.steps)
+    kernels = M.moe_profile_end()
+    launches = sum(n for _, n, _ in kernels)
+
+    e2e = e2e_ms(g, args.steps)
+    e2e, = max_over_ranks([e2e], device=dev)
+    g.layer.status(g.stream)
+
+    sweep = None
+    if args.minibatch_sweep and w.minibatch_rows:
+        sweep = []
+        for mbr in w.minibatch_rows:
+            lay = MoeLayer(w.T, w.H, w.F, w.E, w.k, w.precision, device=dev, ring_bytes=w.ring_bytes,
+                           minibatch_rows=mbr)
+            if w.precision == "mxfp8":
+                lay.quantize_weights(g.d["W1"], g.d["W3"], g.d["W2"], stream=g.stream)
+            with torch.cuda.stream(g.stream):
+                for _ in range(2):
+                    g.step(lay)
+            k = max(2, args.steps // 4)
+            fm = timed(g, flush, lambda: g.fwd(lay), k)
+            sm = timed(g, flush, lambda: g.step(lay), k)
+            lay.status(g.stream)
+            sweep.append({"minibatch_rows": mbr, "fwd_ms": fm / k, "fwd_bwd_ms": sm / k,
+                          "macrobatches": lay.plan.num_macrobatches, "macrobatch_tokens": lay.plan.macrobatch_tokens})
+            del lay
+            torch.cuda.empty_cache()
+
+    # the other workloads (single GPU): the same step, its forward and its per-kernel rates
+    others = []
+    if ws == 1 and not args.only_headline:
+        headline_inp = g.inp
+        del g
+        torch.cuda.empty_cache()
+        for name in OTHER_WORKLOADS:
+            if name == w.name:
+                continue
+            wo = WL.WORKLOADS[name]
+            go = Gpu(wo, dev, rank, M, MoeLayer, torch)
+            with torch.cuda.stream(go.stream):
+                for _ in range(args.warmup):
+                    go.step()
+            go.layer.status(go.stream)
+            t_step = timed(go, flush, go.step, args.steps)
+            t_fwd = timed(go, flush, go.fwd, args.steps)
+            M.moe_profile_begin()
+            t_prof = timed(go, flush, go.step, args.steps)
+            kern = M.moe_profile_end()
+            go.layer.status(go.stream)
+            rows, roof_o, gg_o, tf_o = rate_kernels(wo, kern, args.steps, t_prof, *load_peaks(), t_step * 1e-3)
+            others.append({
+                "workload": wo.name, "precision": wo.precision, "T": wo.T, "H": wo.H, "F": wo.F, "E": wo.E,
+                "k": wo.k, "fwd_bwd": {"value": wo.T * args.steps / (t_step * 1e-3), "unit": "tokens/s",
+                                       "ms_per_step": t_step / args.steps},
+                "fwd": {"value": wo.T * args.steps / (t_fwd * 1e-3), "unit": "tokens/s",
+                        "ms_per_step": t_fwd / args.steps},
+                "grouped_gemm": gg_o, "roofline": roof_o,
+                "layer_roofline": layer_roofline(wo, tf_o, load_peaks()[0]["hbm_gbs"], t_step / args.steps),
+                "gpu_launches": sum(n for _, n, _ in kern),
+                "kernels": [{k_: r[k_] for k_ in ("name", "launches", "ms_per_step", "share", "tflops",
+                                                  "frac_of_tensor_peak", "gbs", "frac_of_hbm") if k_ in r}
+                            for r in rows]})
+            del go
+            torch.cuda.empty_cache()
+        inp = headline_inp
+    else:
+        inp = g.inp
     clocks = sampler.stop() if sampler is not None else stop_clocks(clk_p, clk_path)
 
     if rank != 0:
@@ -452,47 +615,7 @@ def run_ours(args, w):
             dist.destroy_process_group()
         return
     peaks, peak_src = load_peaks()
-    # dominant kernel: largest share of the profiled step
-    kt = sorted(kernels, key=lambda r: -r[2])
-    name, n, ms = kt[0]
-    per_launch_ms = ms / n
-    # gemm_flops / kernel_bytes are per step; a kernel may launch several times
-    # per step (one launch per macrobatch)
-    per_step = n / args.steps
-    fl = gemm_flops(w, name)
-    fl = None if fl is None else fl / per_step
-    roof = None
-    if fl is not None:
-        peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
-        if w.precision == "mxfp8":
-            peak = 2 * peak     # fp8 dense = 2x bf16 (nominal 4.5 vs 2.25 PFLOP/s)
-        gb = gemm_bytes(w, name) / per_step
-        if w.precision == "mxfp8":
-            gb = None           # operand bytes differ per operand in MXFP8; rated on the tensor pipe
-        hbm = peaks.get("hbm_gbs")
-        traffic = committed_traffic(name) if w.name == WL.BALANCED.name else None
-        if gb is not None and hbm and gb / (hbm * 1e9) > fl / (peak * 1e12):
-            # the kernel's roofline is HBM: its algorithmic bytes take longer than its flops
-            ach = gb / (per_launch_ms * 1e-3) / 1e9
-            roof = {"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
-                    "frac": ach / hbm, "traffic": traffic, "algorithmic_per_launch": gb,
-                    "tensor_frac": fl / (per_launch_ms * 1e-3) / 1e12 / peak,
-                    "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"}
-        else:
-            ach = fl / (per_launch_ms * 1e-3) / 1e12
-            roof = {"kernel": name, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                    "frac": ach / peak, "traffic": traffic, "algorithmic_per_launch": fl,
-                    "algorithmic_bytes_per_launch": gb,
-                    "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside the step loop)"
-                                   + (" x 2 (nominal fp8/bf16 ratio)" if w.precision == "mxfp8" else "")}
-    elif kernel_bytes(w, name) is not None:
-        peak = peaks.get("hbm_gbs")
-        ach = kernel_bytes(w, name) / per_step / (per_launch_ms * 1e-3) / 1e9
-        roof = {"kernel": name, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
-                "frac": ach / peak, "traffic": None, "algorithmic_per_launch": kernel_bytes(w, name) / per_step,
-                "peak_source": f"{peak_src} hbm_gbs"}
-    gemm_ms = sum(ms_ for nm, _, ms_ in kernels if nm.startswith("grouped_gemm"))
-    gemm_fl = sum(gemm_flops(w, nm) * args.steps for nm, n_, _ in kernels if nm.startswith("grouped_gemm"))
+    rows, roof, gg, tf = rate_kernels(w, kernels, args.steps, prof_ms, peaks, peak_src, total_ms * 1e-3)
     value = job_tokens_per_s(ws, w.T, args.steps, total_ms)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
@@ -501,6 +624,8 @@ def run_ours(args, w):
         "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "E": w.E, "k": w.k,
                    "precision": w.precision, "step": "forward+backward",
+                   "ring_bytes": w.ring_bytes or None, "macrobatches": plan[0], "macrobatch_tokens": plan[1],
+                   "minibatch_rows": plan[2],
                    "l2": "flushed (256 MiB write) between timed steps",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "w0": None if w0_ms is None else {
@@ -510,53 +635,19 @@ def run_ours(args, w):
         "fwd": {"value": job_tokens_per_s(ws, w.T, args.steps, fwd_ms), "unit": "tokens/s",
                 "ms_per_step": fwd_ms / args.steps},
         "roofline": roof,
-        "grouped_gemm": {"tflops": gemm_fl / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None,
-                         "frac_of_peak": (gemm_fl / (gemm_ms * 1e-3) / 1e12) /
-                         (peaks.get("bf16_tflops_sustained", 1700.0) * (2 if w.precision == "mxfp8" else 1))
-                         if gemm_ms else None,
-                         "share_of_step": gemm_ms / prof_ms if prof_ms else None},
-        "kernels": [dict({"name": nm, "launches": n_, "ms_per_step": ms_ / args.steps,
-                          "share": ms_ / prof_ms},
-                         **({"tflops": gemm_flops(w, nm) * args.steps / (ms_ * 1e-3) / 1e12} if gemm_flops(w, nm) else {}),
-                         **({"gbs": kernel_bytes(w, nm) * args.steps / (ms_ * 1e-3) / 1e9,
-                             "frac_of_hbm": kernel_bytes(w, nm) * args.steps / (ms_ * 1e-3) / 1e9 / peaks["hbm_gbs"]}
-                            if kernel_bytes(w, nm) and peaks.get("hbm_gbs") else {}))
-                    for nm, n_, ms_ in kt],
-        "layer_roofline": layer_roofline(w, peaks, total_ms / args.steps),
+        "grouped_gemm": gg,
+        "kernels": rows,
+        "layer_roofline": layer_roofline(w, tf, peaks["hbm_gbs"], total_ms / args.steps),
         "gpu_launches": launches,
-        "e2e": {"value": job_tokens_per_s(ws, w.T, args.steps, e2e_ms), "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(ws, w.T, args.steps, e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * w.T * w.H * 2, "d2h_bytes_per_step": 2 * w.T * w.H * 2,
                 "pipelined": "copy streams, double-buffered inputs/outputs; no L2 flush (weights exceed L2)"},
         "clocks": clocks,
     }
-    if args.minibatch_sweep and w.minibatch_rows:
-        sweep = []
-        del layer
-        torch.cuda.empty_cache()
-        for mbr in w.minibatch_rows:
-            lay = MoeLayer(w.T, w.H, w.F, w.E, w.k, w.precision, device=dev, ring_bytes=w.ring_bytes,
-                           minibatch_rows=mbr)
-            if w.precision == "mxfp8":
-                lay.quantize_weights(d["W1"], d["W3"], d["W2"], stream=stream)
-
-            def f1(lay=lay):
-                lay.forward(d["x"], d["Wr"], bias, d["W1"], d["W3"], d["W2"], out, ids, wts, stream=stream)
-
-            def s1(lay=lay):
-                f1()
-                lay.backward(d["dout"], d["x"], d["Wr"], d["W1"], d["W3"], d["W2"], dx, dWr, dW1, dW3, dW2,
-                             stream=stream)
-            with torch.cuda.stream(stream):
-                for _ in range(2):
-                    s1()
-            k = max(2, args.steps // 4)
-            fm, sm = timed(f1, k), timed(s1, k)
-            lay.status(stream)
-            sweep.append({"minibatch_rows": mbr, "fwd_ms": fm / k, "fwd_bwd_ms": sm / k,
-                          "macrobatches": lay.plan.num_macrobatches, "macrobatch_tokens": lay.plan.macrobatch_tokens})
-            del lay
-            torch.cuda.empty_cache()
+    if sweep is not None:
         line["minibatch_sweep"] = sweep
+    if others:
+        line["other_workloads"] = others
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp)
     print(json.dumps(line), flush=True)
@@ -566,12 +657,16 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+OTHER_WORKLOADS = [WL.BALANCED.name, WL.SKEWED.name, WL.MXFP8.name]
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=WL.BALANCED.name, choices=sorted(WL.WORKLOADS))
+    ap.add_argument("--workload", default=WL.RING.name, choices=sorted(WL.WORKLOADS))
+    ap.add_argument("--only-headline", action="store_true", help="skip the other workloads")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0, help="override T (small cases for ncu captures)")

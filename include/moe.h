@@ -86,9 +86,10 @@ typedef enum {
  *     0 = smallest multiple of 128 giving at least two full waves of GEMM1
  *     tiles on the device's SMs (article section 02: "at least two full SM
  *     waves per expert grouped GEMM").
- *   ring_bytes: size of the ring token buffer (dispatched rows, FFN hidden
- *     rows and expert outputs of the macrobatches in flight); 0 = large enough
- *     for all routed rows, i.e. one macrobatch.
+ *   ring_bytes: size of the ring buffer that holds the rows of the macrobatch in
+ *     flight (MXFP8: dispatched x rows, FFN hidden rows and expert outputs; bf16:
+ *     hidden rows and expert outputs, the x rows going to the saved context);
+ *     0 = large enough for all routed rows, i.e. one macrobatch.
  *   macrobatch_tokens: tokens per macrobatch; 0 = derived from ring_bytes.
  *   timeout_ms: budget of every device-side wait; 0 = 2000 ms.
  *   num_sms: SM count used for planning; 0 = query the current device.
@@ -139,9 +140,8 @@ size_t moe_workspace_size(const moe_config_t *cfg);
 /* Bytes of the forward->backward context written by moe_forward and read by
  * moe_backward (router ids/weights/probabilities, schedule maps, the bf16
  * FFN pre-activations a = x W1 and b = x W3 of every routed row; for bf16
- * configs whose routed rows fit one macrobatch also the expert-sorted x rows
- * the dispatch gathered, which the backward's dW1/dW3 then reads instead of
- * gathering them again). */
+ * configs also the expert-sorted x rows the dispatch gathered, which GEMM1 and
+ * then the backward's dW1/dW3 read, so the backward never gathers them again). */
 size_t moe_saved_size(const moe_config_t *cfg);
 
 /* Bytes of the MXFP8 weight copies made by moe_quantize_weights (0 for bf16). */
@@ -168,13 +168,18 @@ moe_status_t moe_schedule(const moe_config_t *cfg, const int32_t *topk_ids,
  * callback whose pool owns all device memory, a deployment that forbids
  * allocation after start-up). Same arguments and results as moe_schedule,
  * minus the workspace: the scratch lives in a 1 MiB device array of the
- * library itself, reserved on every device that loads the library until the
- * process exits. The pages have no counterpart of this entry point.
+ * library itself. The pages have no counterpart of this entry point.
  *   - Shapes whose schedule scratch (two histograms of (chunk, expert) counts
  *     plus the padded offsets, 256 routed slots per chunk) exceeds the array
  *     return MOE_ERR_UNSUPPORTED.
- *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *   - The first call on a device loads the array's module there (reserving
+ *     its 1 MiB until the process exits; in a pool that owns every free byte
+ *     this can fail with MOE_ERR_CUDA) and looks up the array's device address
+ *     with that device current. Make that first call at start-up, before any
+ *     stream capture.
+ *   - The address is cached per device number for the life of the process:
+ *     do not call cudaDeviceReset, or make another context current on the
+ *     device, between calls.
  *   - All calls on a device share the array; calls that overlap on the GPU
  *     race and give undefined results. Each call clears what must start at 0.
  *   - Device-side id checks are not reported: pass ids in [0,E).
@@ -229,6 +234,49 @@ moe_status_t moe_query_status(void *workspace, moe_stream_t stream);
 /* Clears the device status word (enqueued on stream, no host sync). Call once
  * on a fresh workspace before its first use. */
 moe_status_t moe_reset_status(void *workspace, moe_stream_t stream);
+
+/* Intermediate buffers of the layer that moe_buffer_location can locate (a test
+ * and debugging aid: the parity tests read them to compare the quantised
+ * operands byte for byte with a reference quantiser). Rows are padded
+ * expert-sorted rows: every (macrobatch, expert) run starts at a multiple of
+ * 128 and is padded with zero rows; MOE_BUF_ROW_SLOT gives each row's routed
+ * slot t*k + j (-1 = padding), MOE_BUF_PADDED_OFFSETS the run starts.
+ * "_SCALES" buffers hold E8M0 scale bytes in 512-byte atoms (128 rows x 128
+ * elements of the contraction axis; atom (r/128, k/128) in row-major order,
+ * byte (r%32)*16 + ((r/32)%4)*4 + (k/32)%4 inside it).
+ *   saved buffer (written by moe_forward):
+ *     PADDED_OFFSETS int32 [nM*E+1]; ROW_SLOT int32 [rows]; A, B bf16 [rows][F]
+ *     in 32 x 32 blocks of 2 KB (block (r/32, c/32) row-major, element (r, c) at
+ *     ((c%32)/8*32 + r%32)*8 + c%8 inside it).
+ *   workspace, valid after moe_forward until the next call on the workspace
+ *   (the ring holds the last macrobatch; ring row = padded row - first padded
+ *   row of that macrobatch):
+ *     RING_X: dispatched x rows, bf16 [ring_rows][H] or E4M3 along H (+ _SCALES);
+ *     RING_H: h rows, bf16 [ring_rows][F] or E4M3 along F (+ _SCALES).
+ *   workspace, valid after moe_backward until the next call on the workspace:
+ *     DA, DB, HW: bf16 [rows][F] (dh.b.sigmoid'(a) terms, w.h);
+ *     MXFP8 only: DY_ROWS (dout rows, E4M3 along H), DA_ROWS, DB_ROWS (E4M3
+ *     along F), each [rows][K] + _SCALES; X_TOKENS, DY_TOKENS (E4M3 [H][rows]
+ *     along the rows) and HW_TOKENS, DA_TOKENS, DB_TOKENS ([F][rows]), + _SCALES. */
+typedef enum {
+    MOE_BUF_PADDED_OFFSETS = 0, MOE_BUF_ROW_SLOT, MOE_BUF_A, MOE_BUF_B,
+    MOE_BUF_RING_X, MOE_BUF_RING_X_SCALES, MOE_BUF_RING_H, MOE_BUF_RING_H_SCALES,
+    MOE_BUF_DA, MOE_BUF_DB, MOE_BUF_HW,
+    MOE_BUF_DY_ROWS, MOE_BUF_DY_ROWS_SCALES, MOE_BUF_DA_ROWS, MOE_BUF_DA_ROWS_SCALES,
+    MOE_BUF_DB_ROWS, MOE_BUF_DB_ROWS_SCALES,
+    MOE_BUF_X_TOKENS, MOE_BUF_X_TOKENS_SCALES, MOE_BUF_DY_TOKENS, MOE_BUF_DY_TOKENS_SCALES,
+    MOE_BUF_HW_TOKENS, MOE_BUF_HW_TOKENS_SCALES, MOE_BUF_DA_TOKENS, MOE_BUF_DA_TOKENS_SCALES,
+    MOE_BUF_DB_TOKENS, MOE_BUF_DB_TOKENS_SCALES,
+    MOE_BUF_COUNT
+} moe_buffer_t;
+
+/* Where buffer `which` (a moe_buffer_t) lives: *in_saved = 1 for the saved
+ * buffer, 0 for the workspace; *offset = bytes from the 1024-byte boundary at
+ * or after the buffer's start (the base the library uses); *bytes = its size.
+ * Host-only. MOE_ERR_UNSUPPORTED for a buffer the configuration does not have
+ * (the MXFP8-only ones in a bf16 configuration). */
+moe_status_t moe_buffer_location(const moe_config_t *cfg, int which, int *in_saved, size_t *offset,
+                                 size_t *bytes);
 
 /* Per-kernel timing of this host thread's calls (CUDA events recorded on the
  * launch stream around every kernel the library launches). */

@@ -1,0 +1,301 @@
+// Decode-shaped expert FFN on tcgen05 tensor cores: the forward of few tokens.
+//
+// With few tokens ("warp decode" in Cursor's earlier work, noticiai.com.br, "Por que a camada
+// MoE virou o gargalo") each expert holds a handful of routed rows and the layer's time is
+// the weights' trip from HBM: every byte of W1, W3 and W2 has to be read once and there is
+// little arithmetic to hide it behind. The row tiles of the grouped GEMMs (128 or 256 rows)
+// would be almost empty, so here the roles swap: the weights are the M operand (128 of their
+// columns per tile, MN-major, straight from the row-major weights) and the expert's routed
+// rows (at most 128, zero-padded) are N:
+//   GEMM1 item (expert e, 128 columns f of F): D_a[f][r] = sum_h W1[e][h][f] x[r][h], D_b
+//     likewise with W3; epilogue: a, b rounded to bf16 (saved for the backward, 32 x 32 blocks),
+//     h = silu(a) * b rounded to bf16 into the h rows;
+//   GEMM2 item (expert e, 128 columns of H): D_y[c][r] = sum_f W2[e][f][c] h[r][f]; epilogue:
+//     y rows in bf16 for the combine.
+// One persistent CTA per SM (192 threads): warp 0 claims work items from a device counter
+// (every GEMM1 item first, then every GEMM2 item; items of experts without rows are skipped)
+// and streams their operands by TMA through a 4-stage ring of 48 KB stages; warp 1 issues the
+// MMAs (M = 128, N = 128, K = 16) into a double-buffered TMEM accumulator (256 columns per
+// item); warps 2-5 run the epilogues. A GEMM2 item waits (bounded, acquire) until all F/128
+// GEMM1 items of its expert have published h (release), so GEMM2 tiles of early experts run
+// while GEMM1 tiles of late ones still stream, and no SM idles at a phase boundary. Items
+// are claimed in order and GEMM1 items wait on nothing, so every wait ends.
+#include "decode_ffn.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int DST = 4;                               // pipeline stages
+constexpr uint32_t DW_TILE = 2 * 64 * 64 * 2;        // 16 KB: 128 weight columns x 64 K rows, MN-major
+constexpr uint32_t DT_TILE = 128 * 64 * 2;           // 16 KB: 128 token rows x 64 K, K-major
+constexpr uint32_t DSTAGE = 2 * DW_TILE + DT_TILE;   // 48 KB: W1 (or W2), W3, token rows
+constexpr int QD = 4;                                // depth of the work-item queue in shared memory
+
+struct DecCtl {
+    uint64_t full[DST], empty[DST], tfull[2], tempty[2], qfull[QD], qempty[QD], drain;
+    uint32_t tmem_base;
+    int item[QD];
+};
+
+// element (row, col) of a [rows][C] matrix stored in 32 x 32 blocks (blk32_offset)
+__device__ __forceinline__ size_t blk32_elem(int row, int col, int C) {
+    return blk32_offset(row, col, C) + (size_t)((((col & 31) >> 3) * 32 + (row & 31)) * 8 + (col & 7));
+}
+
+__device__ __forceinline__ float sigmoid_d(float a) { return __fdividef(1.0f, 1.0f + __expf(-a)); }
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+struct Item {
+    bool gemm1;
+    int e, col0, nk;
+};
+
+__device__ __forceinline__ Item decode_item(const DecodeArgs &a, int id) {
+    const int nf = a.F / 128, n1 = a.E * nf;
+    Item it;
+    it.gemm1 = id < n1;
+    if (it.gemm1) {
+        it.e = id / nf;
+        it.col0 = (id - it.e * nf) * 128;
+        it.nk = a.H / 64;
+    } else {
+        const int nh = a.H / 128, q = id - n1;
+        it.e = q / nh;
+        it.col0 = (q - it.e * nh) * 128;
+        it.nk = a.F / 64;
+    }
+    return it;
+}
+
+__device__ void dec_producer(const DecodeArgs &a, DecCtl &c, uint8_t *tiles, const WaitCtl &ctl) {
+    const int total = a.E * (a.F / 128 + a.H / 128);
+    int stage = 0, slot = 0;
+    uint32_t phase = 0, qphase = 0;
+    uint32_t issued = 0, last_phase = 0;
+    bool ok = true;
+    for (;;) {
+        int id = -1;
+        if (ok) {
+            for (;;) {
+                id = atomicAdd(a.claim, 1);
+                if (id >= total) { id = -1; break; }
+                if (a.counts[decode_item(a, id).e] > 0) break;   // experts without rows have no work
+            }
+        }
+        if (!mbar_wait(smem_u32(&c.qempty[slot]), qphase ^ 1, ctl)) { ok = false; id = -1; }
+        c.item[slot] = id;
+        mbar_arrive(smem_u32(&c.qfull[slot]));
+        if (++slot == QD) { slot = 0; qphase ^= 1; }
+        if (id < 0) break;
+        const Item it = decode_item(a, id);
+        const int s0 = a.offp[it.e];
+        if (!it.gemm1) {
+            // h of this expert: every GEMM1 item of it has published its columns
+            if (!flag_wait_geq(a.hdone + it.e, a.F / 128, ctl)) { ok = false; continue; }
+            fence_proxy_async_global();
+        }
+        for (int kb = 0; kb < it.nk && ok; ++kb) {
+            if (!mbar_wait(smem_u32(&c.empty[stage]), phase ^ 1, ctl)) { ok = false; break; }
+            const uint32_t bar = smem_u32(&c.full[stage]);
+            const uint32_t sA = smem_u32(tiles + stage * DSTAGE);
+            const uint32_t sT = sA + 2 * DW_TILE;
+            if (it.gemm1) {
+                mbar_arrive_expect_tx(bar, DSTAGE);
+                tma_load_3d(sA, &a.w1, bar, 0, it.e * a.H + kb * 64, it.col0 / 64);
+                tma_load_3d(sA + DW_TILE, &a.w3, bar, 0, it.e * a.H + kb * 64, it.col0 / 64);
+                tma_load_2d(sT, &a.x, bar, kb * 64, s0);
+            } else {
+                mbar_arrive_expect_tx(bar, DW_TILE + DT_TILE);
+                tma_load_3d(sA, &a.w2, bar, 0, it.e * a.F + kb * 64, it.col0 / 64);
+                tma_load_2d(sT, &a.h, bar, kb * 64, s0);
+            }
+            issued |= 1u << stage;
+            last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+            if (++stage == DST) { stage = 0; phase ^= 1; }
+        }
+    }
+    if (!ok) {
+        // leave no bulk copy in flight: wait (bounded, regardless of the status word) for the
+        // last copy issued into every stage
+        for (int s = 0; s < DST; ++s) {
+            if (!((issued >> s) & 1u)) continue;
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(&c.full[s]), (last_phase >> s) & 1u) && globaltimer_ns() - t0 < ctl.budget_ns) {}
+        }
+    }
+}
+
+__device__ void dec_mma(const DecodeArgs &a, DecCtl &c, uint8_t *tiles, uint32_t tmem, const WaitCtl &ctl) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, true, false);   // A MN-major, B K-major
+    int stage = 0, slot = 0, acc = 0;
+    uint32_t phase = 0, qphase = 0, acc_phase = 0;
+    for (;;) {
+        if (!mbar_wait(smem_u32(&c.qfull[slot]), qphase, ctl)) break;
+        const int id = c.item[slot];
+        mbar_arrive(smem_u32(&c.qempty[slot]));
+        if (++slot == QD) { slot = 0; qphase ^= 1; }
+        if (id < 0) break;
+        const Item it = decode_item(a, id);
+        if (!mbar_wait(smem_u32(&c.tempty[acc]), acc_phase ^ 1, ctl)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * 256;
+        bool ok = true;
+        for (int kb = 0; kb < it.nk; ++kb) {
+            if (!mbar_wait(smem_u32(&c.full[stage]), phase, ctl)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sA = smem_u32(tiles + stage * DSTAGE);
+            const uint32_t sT = sA + 2 * DW_TILE;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bd = sdesc_sw128(sT + kk * 32, 16, 1024);
+                mma_bf16_ss(d, sdesc_sw128(sA + kk * 2048, 8192, 1024), bd, idesc, (kb | kk) != 0);
+                if (it.gemm1) mma_bf16_ss(d + 128, sdesc_sw128(sA + DW_TILE + kk * 2048, 8192, 1024), bd, idesc, (kb | kk) != 0);
+            }
+            mma_commit(smem_u32(&c.empty[stage]));
+            if (++stage == DST) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&c.tfull[acc]));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+    }
+    mma_commit(smem_u32(&c.drain));
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(smem_u32(&c.drain), 0) && globaltimer_ns() - t0 < ctl.budget_ns) {}
+}
+
+__device__ void dec_epilogue(const DecodeArgs &a, DecCtl &c, uint32_t tmem, const WaitCtl &ctl) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int quarter = warp & 3;                    // TMEM lanes this warp may read
+    const int col = quarter * 32 + lane;             // weight column of this thread within the tile
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    int slot = 0, acc = 0;
+    uint32_t qphase = 0, acc_phase = 0;
+    for (;;) {
+        if (!mbar_wait(smem_u32(&c.qfull[slot]), qphase, ctl)) break;
+        const int id = c.item[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&c.qempty[slot]));
+        if (++slot == QD) { slot = 0; qphase ^= 1; }
+        if (id < 0) break;
+        const Item it = decode_item(a, id);
+        if (!mbar_wait(smem_u32(&c.tfull[acc]), acc_phase, ctl)) break;
+        tc_fence_after();
+        const uint32_t tbase = tmem + lane_base + acc * 256;
+        const int s0 = a.offp[it.e];
+        if (it.gemm1) {
+            // every row of the expert's 128-row padded run: padding rows have x = 0, so their
+            // a, b and h are exactly 0 (the backward reads a, b of the whole run)
+            const int f = it.col0 + col;
+#pragma unroll 1
+            for (int rc = 0; rc < 4; ++rc) {
+                uint32_t va[32], vb[32];
+                tmem_ld_32x32b_x32(tbase + rc * 32, va);
+                tmem_ld_32x32b_x32(tbase + 128 + rc * 32, vb);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int row = s0 + rc * 32 + i;
+                    const bf16 ab = f2bf(__uint_as_float(va[i])), bb = f2bf(__uint_as_float(vb[i]));
+                    const float av = bf2f(ab), bv = bf2f(bb);
+                    a.a[blk32_elem(row, f, a.F)] = ab;
+                    a.b[blk32_elem(row, f, a.F)] = bb;
+                    a.hrows[(size_t)row * a.F + f] = f2bf(av * sigmoid_d(av) * bv);
+                }
+            }
+        } else {
+            const int c0 = it.col0 + col, nrows = a.counts[it.e];
+#pragma unroll 1
+            for (int rc = 0; rc < 4 && rc * 32 < nrows; ++rc) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tbase + rc * 32, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int r = rc * 32 + i;
+                    if (r < nrows) a.y[(size_t)(s0 + r) * a.H + c0] = f2bf(__uint_as_float(v[i]));
+                }
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&c.tempty[acc]));
+        if (it.gemm1) {
+            // publish: this item's h columns of expert e are in memory (generic stores, read by
+            // later TMA loads of other CTAs)
+            epi_bar();
+            if (warp == 2 && lane == 0) {
+                __threadfence();
+                fence_proxy_async_global();
+                red_release_gpu_add(a.hdone + it.e, 1);
+            }
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+    }
+}
+
+__global__ void __launch_bounds__(192, 1) decode_ffn_kernel(const __grid_constant__ DecodeArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    DecCtl &c = *reinterpret_cast<DecCtl *>(tiles + DST * DSTAGE);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    WaitCtl ctl{a.status, a.budget_ns};
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < DST; ++s) {
+            mbar_init(smem_u32(&c.full[s]), 1);
+            mbar_init(smem_u32(&c.empty[s]), 1);
+        }
+        for (int q = 0; q < QD; ++q) {
+            mbar_init(smem_u32(&c.qfull[q]), 1);
+            mbar_init(smem_u32(&c.qempty[q]), 1 + 4);   // the MMA thread and the four epilogue warps
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&c.tfull[i]), 1);
+            mbar_init(smem_u32(&c.tempty[i]), 128);
+        }
+        mbar_init(smem_u32(&c.drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&a.w1);
+        tma_prefetch_map(&a.w3);
+        tma_prefetch_map(&a.w2);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&c.tmem_base), 512);
+        tmem_relinquish();
+    }
+    pdl_wait();   // the dispatched rows, offsets and counters are in place
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_trigger();
+    const uint32_t tmem = c.tmem_base;
+    if (warp == 0) {
+        if (lane == 0) dec_producer(a, c, tiles, ctl);
+    } else if (warp == 1) {
+        if (lane == 0) dec_mma(a, c, tiles, tmem, ctl);
+    } else {
+        dec_epilogue(a, c, tmem, ctl);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_ffn(const DecodeArgs &a, int num_sms, cudaStream_t s) {
+    constexpr size_t smem = DST * DSTAGE + sizeof(DecCtl) + 1024;
+    static_assert(smem <= 227 * 1024, "shared memory budget");
+    cudaError_t err = cudaFuncSetAttribute(decode_ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(decode_ffn_kernel, dim3(num_sms), dim3(192), smem, s, a);
+    if (err != cudaSuccess) return err;
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -103,8 +103,9 @@ template <> struct OpTraits<OP_WG13> { static constexpr bool grouped_k = true, a
 
 struct TileInfo {
     int e, mt, nt;
-    int g0;      // grouped-M: first global padded row of the tile
-    int nk;      // number of BK blocks
+    int g0;       // grouped-M: first global padded row of the tile
+    int seg_end;  // grouped-M: end of the tile's (macrobatch, expert) run
+    int nk;       // number of BK blocks
 };
 
 template <int NS>
@@ -112,6 +113,7 @@ struct CtlT {
     uint64_t full[NS], empty[NS], tfull[2], tempty[2], drain;
     uint32_t tmem_base;
     int nt;                       // tiles along N
+    int list_tiles;               // grouped-M over all macrobatches: M tiles in the device list
     int mt_per_group;             // grouped-K: tiles along M (fixed)
     int prefix[kMaxExperts + 1];  // grouped-M: tile prefix over experts; grouped-K: unused
     int krows[kMaxExperts];       // grouped-K: padded rows of each expert (all macrobatches)
@@ -124,7 +126,7 @@ using SmemCtl = CtlT<STAGES>;
 template <int OP, class Ctl>
 __device__ __forceinline__ int num_tiles(const Ctl &c, const GemmArgs &g) {
     if constexpr (OpTraits<OP>::grouped_k) return g.E * c.mt_per_group * c.nt;
-    else return c.prefix[g.E] * c.nt;
+    else return (g.tiles ? c.list_tiles : c.prefix[g.E]) * c.nt;
 }
 
 template <int OP, bool FP8, int TM = BM, class Ctl>
@@ -136,13 +138,23 @@ __device__ __forceinline__ TileInfo decode_tile(const Ctl &c, const GemmArgs &g,
         ti.mt = q % c.mt_per_group;
         ti.e = q / c.mt_per_group;
         ti.g0 = 0;
+        ti.seg_end = 0;
         ti.nk = c.krows[ti.e] / bk_elems<FP8>();
     } else {
-        int e = 0;
-        while (c.prefix[e + 1] <= q) ++e;   // E <= 64
-        ti.e = e;
-        ti.mt = q - c.prefix[e];
-        ti.g0 = c.seg_start[e] + ti.mt * TM;
+        if (g.tiles) {
+            const int4 v = g.tiles[q];   // (first row, expert, run end, 0)
+            ti.e = v.y;
+            ti.mt = 0;
+            ti.g0 = v.x;
+            ti.seg_end = v.z;
+        } else {
+            int e = 0;
+            while (c.prefix[e + 1] <= q) ++e;   // E <= 64
+            ti.e = e;
+            ti.mt = q - c.prefix[e];
+            ti.g0 = c.seg_start[e] + ti.mt * TM;
+            ti.seg_end = c.seg_end[e];
+        }
         ti.nk = g.K / bk_elems<FP8>();
     }
     return ti;
@@ -160,6 +172,10 @@ __device__ void init_tile_table(Ctl &c, const GemmArgs &g) {
         }
     } else {
         c.nt = (OP == OP_FWD1) ? g.N / 128 : g.N / BN;
+        if (g.tiles) {
+            c.list_tiles = *g.tile_count;
+            return;
+        }
         c.prefix[0] = 0;
         for (int e = 0; e < g.E; ++e) {
             const int s0 = g.offp[g.m * g.E + e], s1 = g.offp[g.m * g.E + e + 1];
@@ -206,7 +222,7 @@ __device__ void gather_loop(const GemmArgs &g, const uint64_t *stop_bar = nullpt
                 for (int i = 0; i < 2; ++i) {
                     const int slot = g.row_slot[r + i];
                     src[i] = slot >= 0 ? g.xsrc + (size_t)(slot / g.k) * g.H : nullptr;
-                    dst[i] = g.ringx + (size_t)(r + i - r0 + g.ring_base) * g.H;
+                    dst[i] = g.ringx + (size_t)(g.x_global ? r + i : r + i - r0 + g.ring_base) * g.H;
                 }
                 for (int v0 = 0; v0 < vecs; v0 += 256) {
                     uint4 q[2][8];
@@ -281,8 +297,7 @@ __device__ void producer_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tile
                               uint64_t *empty, const WaitCtl &ctl) {
     int stage = 0;
     uint32_t phase = 0;
-    int issued[STAGES] = {0, 0, 0, 0};
-    uint32_t last_phase[STAGES] = {0, 0, 0, 0};
+    uint32_t issued = 0, last_phase = 0;   // per stage: a copy was issued / the phase of the last one
     bool ok = true;
     const int total = num_tiles<OP>(c, g);
     const int a_shift = g.a_ring ? (g.ring_base - g.offp[g.m * g.E]) : 0;
@@ -405,8 +420,8 @@ __device__ void producer_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tile
                     bulk_load(sSF + 1024, g.sfb1 + atom_at(n0, row, KS), 512, bar);
                 }
             }
-            issued[stage] = 1;
-            last_phase[stage] = phase;
+            issued |= 1u << stage;
+            last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
             if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
     }
@@ -414,10 +429,10 @@ __device__ void producer_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tile
         // leave no bulk copy in flight: wait (bounded, regardless of the
         // status word) for the last copy issued into every stage
         for (int s = 0; s < STAGES; ++s) {
-            if (!issued[s]) continue;
+            if (!((issued >> s) & 1u)) continue;
             uint32_t bar = smem_u32(&full[s]);
             uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(bar, last_phase[s]) && globaltimer_ns() - t0 < ctl.budget_ns) {}
+            while (!mbar_try_wait(bar, (last_phase >> s) & 1u) && globaltimer_ns() - t0 < ctl.budget_ns) {}
         }
     }
 }
@@ -492,10 +507,12 @@ __device__ void mma_loop(const GemmArgs &g, const SmemCtl &c, uint8_t *tiles, ui
 __device__ __forceinline__ float sigmoid_f(float a) { return __fdividef(1.0f, 1.0f + __expf(-a)); }
 __device__ __forceinline__ float silu_f(float a) { return a * sigmoid_f(a); }
 
-// 32 rows (one per lane) x 32 bf16 of this warp -> a 2 KB staging buffer (plain
-// row-major, 64 B per row) -> one TMA store at (col0, row0) of map m. NBUF
-// buffers per warp rotate; a buffer is reused once the store issued NBUF
-// stores earlier has read it.
+// 32 rows (one per lane) x 32 bf16 of this warp -> a 2 KB staging buffer (64 B per
+// row, 64-byte swizzle: 16-byte chunk g of row r sits at chunk g ^ ((r >> 1) & 3), the
+// order a CU_TENSOR_MAP_SWIZZLE_64B map reads) -> one TMA store at (col0, row0) of map m.
+// With the swizzle the eight lanes of a quarter warp write eight different 16-byte bank
+// groups (unswizzled, rows r and r + 2 share one: a 4-way conflict). NBUF buffers per
+// warp rotate; a buffer is reused once the store issued NBUF stores earlier has read it.
 template <int NBUF = 4>
 __device__ __forceinline__ void stage_store_bf16(uint8_t *warp_stage, int &nstores, const uint32_t (&w)[16],
                                                  const CUtensorMap *m, int col0, int row0, int lane) {
@@ -506,7 +523,8 @@ __device__ __forceinline__ void stage_store_bf16(uint8_t *warp_stage, int &nstor
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4 *>(buf + lane * 64 + q * 16) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        *reinterpret_cast<uint4 *>(buf + lane * 64 + ((q ^ ((lane >> 1) & 3)) * 16)) =
+            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
     fence_proxy_async_shared();
     __syncwarp();
     if (lane == 0) {
@@ -574,7 +592,7 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                 ti.mt = ti.mt * 2 + rank;
             } else {
                 ti.g0 += BM * rank;
-                phantom = ti.g0 >= c.seg_end[ti.e];
+                phantom = ti.g0 >= ti.seg_end;
             }
         }
         if (!mbar_wait(smem_u32(&tfull[acc]), acc_phase, ctl)) break;
@@ -834,6 +852,8 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
     if (store_chunks > 0 && lane == 0) bulk_wait_group_all();
 }
 
+// 320 threads: ten warps over the SM's four sub-partitions, three of them on one 16K-register
+// file, so at most 168 registers per thread.
 template <int OP, bool FP8>
 __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
@@ -911,8 +931,7 @@ __device__ void pair_producer_loop(const GemmArgs &g, const PairCtl &c, uint8_t 
     const int rank = (int)cluster_ctarank();
     int stage = 0;
     uint32_t phase = 0;
-    int issued[PSTAGES] = {0, 0, 0, 0, 0, 0};
-    uint32_t last_phase[PSTAGES] = {0, 0, 0, 0, 0, 0};
+    uint32_t issued = 0, last_phase = 0;   // per stage: a copy was issued / the phase of the last one
     bool ok = true;
     const int total = num_tiles<OP>(c, g);
     const int a_shift = g.a_ring ? (g.ring_base - g.offp[g.m * g.E]) : 0;
@@ -922,7 +941,7 @@ __device__ void pair_producer_loop(const GemmArgs &g, const PairCtl &c, uint8_t 
         const int row0 = ti.g0 + BM * rank;              // grouped-M: this CTA's 128 rows
         const int m0 = (ti.mt * 2 + rank) * BM;          // grouped-K: this CTA's 128 rows of dW
         if constexpr (OP == OP_FWD1) {
-            if (g.fused && row0 < c.seg_end[ti.e]) {
+            if (g.fused && row0 < ti.seg_end) {
                 const int r0 = g.offp[g.m * g.E], nrows = g.offp[(g.m + 1) * g.E] - r0;
                 const int j = (row0 - r0) / g.mb_rows;
                 if (j != ready_mb) {
@@ -978,18 +997,18 @@ __device__ void pair_producer_loop(const GemmArgs &g, const PairCtl &c, uint8_t 
                 tma_load_3d_pair(sA, &g.a0, bar, 0, krow, m0 / 64);
                 tma_load_3d_pair(sB, bm, bar, 0, krow, n0 / 64);
             }
-            issued[stage] = 1;
-            last_phase[stage] = phase;
+            issued |= 1u << stage;
+            last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
             if (++stage == PSTAGES) { stage = 0; phase ^= 1; }
         }
     }
     if (!ok && rank == 0) {
         // the leader's full barriers count both CTAs' copies: wait (bounded) for the last phases
         for (int s = 0; s < PSTAGES; ++s) {
-            if (!issued[s]) continue;
+            if (!((issued >> s) & 1u)) continue;
             const uint32_t bar = smem_u32(&c.full[s]);
             const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(bar, last_phase[s]) && globaltimer_ns() - t0 < ctl.budget_ns) {}
+            while (!mbar_try_wait(bar, (last_phase >> s) & 1u) && globaltimer_ns() - t0 < ctl.budget_ns) {}
         }
     }
 }
@@ -1160,8 +1179,7 @@ __device__ void pair8_producer_loop(const GemmArgs &g, const Pair8Ctl &c, uint8_
     const int rank = (int)cluster_ctarank();
     int stage = 0;
     uint32_t phase = 0;
-    int issued[P8_STAGES] = {};
-    uint32_t last_phase[P8_STAGES] = {};
+    uint32_t issued = 0, last_phase = 0;   // per stage: a copy was issued / the phase of the last one
     bool ok = true;
     const int total = num_tiles<OP>(c, g);
     const int a_shift = g.a_ring ? (g.ring_base - g.offp[g.m * g.E]) : 0;
@@ -1172,7 +1190,7 @@ __device__ void pair8_producer_loop(const GemmArgs &g, const Pair8Ctl &c, uint8_
         const int row0 = ti.g0 + BM * rank;              // grouped-M: this CTA's 128 rows
         const int m0 = (ti.mt * 2 + rank) * BM;          // grouped-K: this CTA's 128 rows of dW
         if constexpr (OP == OP_FWD1) {
-            if (g.fused && row0 < c.seg_end[ti.e]) {
+            if (g.fused && row0 < ti.seg_end) {
                 const int r0 = g.offp[g.m * g.E], nrows = g.offp[(g.m + 1) * g.E] - r0;
                 const int j = (row0 - r0) / g.mb_rows;
                 if (j != ready_mb) {
@@ -1244,17 +1262,17 @@ __device__ void pair8_producer_loop(const GemmArgs &g, const Pair8Ctl &c, uint8_
                 tma_load_2d_pair(sSF + 512, &g.msb0, bar, 0, atom_row(n0, krow, KS));
                 tma_load_2d_pair(sSF + 1024, &g.msb1, bar, 0, atom_row(n0, krow, KS));
             }
-            issued[stage] = 1;
-            last_phase[stage] = phase;
+            issued |= 1u << stage;
+            last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
             if (++stage == P8_STAGES) { stage = 0; phase ^= 1; }
         }
     }
     if (!ok && rank == 0) {
         for (int s = 0; s < P8_STAGES; ++s) {
-            if (!issued[s]) continue;
+            if (!((issued >> s) & 1u)) continue;
             const uint32_t bar = smem_u32(&c.full[s]);
             const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(bar, last_phase[s]) && globaltimer_ns() - t0 < ctl.budget_ns) {}
+            while (!mbar_try_wait(bar, (last_phase >> s) & 1u) && globaltimer_ns() - t0 < ctl.budget_ns) {}
         }
     }
 }
@@ -1417,7 +1435,46 @@ cudaError_t launch_any(int op, const GemmArgs &g, int grid, cudaStream_t stream)
     }
 }
 
+// One warp per list: warp 0 writes 128-row tiles, warp 1 256-row tiles. Runs are taken
+// 32 at a time in expert-major order (run i = expert i / nM, macrobatch i % nM); a warp
+// scan of their tile counts places each lane's tiles after those of the runs before it.
+__global__ void __launch_bounds__(64) tile_list_kernel(const int *offp, int E, int nM, int4 *list128,
+                                                        int4 *list256, int *counts) {
+    pdl_wait();
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+    const int TM = warp == 0 ? 128 : 256;
+    int4 *list = warp == 0 ? list128 : list256;
+    const int nseg = E * nM;
+    int base = 0;
+    for (int i0 = 0; i0 < nseg; i0 += 32) {
+        const int i = i0 + lane;
+        int s0 = 0, s1 = 0, e = 0;
+        if (i < nseg) {
+            e = i / nM;
+            const int m = i - e * nM;
+            s0 = offp[m * E + e];
+            s1 = offp[m * E + e + 1];
+        }
+        const int n = (s1 - s0 + TM - 1) / TM;
+        int incl = n;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += v;
+        }
+        const int start = base + incl - n;
+        for (int j = 0; j < n; ++j) list[start + j] = make_int4(s0 + j * TM, e, s1, 0);
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) counts[warp] = base;
+}
+
 }  // namespace
+
+cudaError_t launch_tile_lists(const int *offp, int E, int nM, int4 *list128, int4 *list256, int *counts,
+                              cudaStream_t stream) {
+    return launch_pdl(tile_list_kernel, dim3(1), dim3(64), 0, stream, offp, E, nM, list128, list256, counts);
+}
 
 cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream, bool fp8, bool pair) {
     if (pair && fp8) {

@@ -40,6 +40,7 @@ struct GemmArgs {
     // before it loads a tile of it. ready[0..ready_slots) and the claim counter
     // ready[ready_slots] are zeroed before every launch.
     int fused;
+    int x_global;                 // bf16: gathered rows go to their global padded row (saved context)
     const bf16 *xsrc;
     bf16 *ringx;
     uint8_t *ringxq, *ringxs;
@@ -50,6 +51,13 @@ struct GemmArgs {
     // so one 128 x 4 box is one 512-byte atom, loaded by TMA with completion on the pair
     // leader's barrier: A atoms (msa0, msa1) and B atoms (msb0, msb1)
     CUtensorMap msa0, msa1, msb0, msb1;
+    // grouped-M ops over every macrobatch in one launch (tiles != nullptr): the M tiles come
+    // from a list built on the device by launch_tile_lists, one int4 per tile (first padded
+    // row, expert, end of the tile's run, 0), in expert-major order (every run of expert 0,
+    // then of expert 1, ...) so that the CTAs running at one time share one expert's weights;
+    // *tile_count holds the list's length. m stays 0 (only the ring ops use it).
+    const int4 *tiles;
+    const int *tile_count;
     int *status;
     unsigned long long budget_ns;
 };
@@ -58,5 +66,12 @@ struct GemmArgs {
 // K-major ops then need 128-row boxes (bf16 and MXFP8), MXFP8 also the atom maps above.
 cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream, bool fp8 = false,
                                 bool pair = false);
+
+// Writes the M-tile lists of every (macrobatch, expert) run of padded rows, expert-major:
+// list128 with 128-row tiles (1-CTA kernels), list256 with 256-row tiles (CTA pairs; a
+// tile's second half may lie past its run). counts[0], counts[1] = their lengths. Each list
+// needs at most offp[nM*E] / 128 + nM*E entries.
+cudaError_t launch_tile_lists(const int *offp, int E, int nM, int4 *list128, int4 *list256, int *counts,
+                              cudaStream_t stream);
 
 }  // namespace moe

@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "../../include/moe.h"
+#include "decode_ffn.cuh"
 #include "grouped_gemm.cuh"
 #include "mx_quant.cuh"
 #include "route_kernels.cuh"
@@ -62,6 +63,8 @@ constexpr bool kPairGemm = true;
 constexpr bool kPairGemmFp8 = true;
 inline bool pair_fp8(int op) { return kPairGemmFp8 && op != OP_BWD2; }
 constexpr int kGemmBN1 = 256;   // GEMM1 tile: 128 rows x (128 a-columns + 128 b-columns)
+// bf16 forward of at most kDecodeMaxTokens tokens through the decode kernel
+constexpr bool kDecodePath = false;
 constexpr int kGemmBM = 128;
 
 // ---------------------------------------------------------------- planning
@@ -115,7 +118,10 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     const size_t xrow = mx ? (size_t)c->H + c->H / kMxBlock : 2 * (size_t)c->H;
     const size_t hrow = mx ? (size_t)c->F + c->F / kMxBlock : 2 * (size_t)c->F;
     const size_t yrow = 2 * (size_t)c->H;
-    const size_t ring_row_bytes = xrow + hrow + yrow;
+    // bf16: the fused dispatch writes the x rows straight into the saved context (the backward's
+    // dW1/dW3 reads them there), so the ring holds h and Y rows only; MXFP8: x rows quantised
+    // along H live in the ring (the weight gradient needs them along the tokens instead)
+    const size_t ring_row_bytes = (mx ? xrow : 0) + hrow + yrow;
     const int pad = (kRowPad - 1) * c->E;
     int Mb;
     if (c->macrobatch_tokens > 0) {
@@ -123,16 +129,21 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     } else if (c->ring_bytes == 0) {
         Mb = c->T > 0 ? c->T : 1;
     } else {
-        // largest Mb whose two ring halves fit: 2 * (Mb*k + pad) * row_bytes <= ring_bytes
-        const long long rows_half = (long long)(c->ring_bytes / ring_row_bytes) / 2 - pad;
-        if (rows_half < c->k) return fail(MOE_ERR_UNSUPPORTED, "ring_bytes too small for one token per macrobatch");
-        Mb = (int)(rows_half / c->k);
+        // largest Mb whose padded rows fit the ring: (Mb*k + pad) * row_bytes <= ring_bytes.
+        // One macrobatch at a time: every kernel waits for its predecessor on the stream to
+        // complete (programmatic launches included), so macrobatch m+1's dispatch never runs
+        // while macrobatch m's rows are still read, and a second ring half would buy no overlap.
+        // whole 128-row tiles of padded rows, with room for the 1 KiB alignment of each ring buffer
+        const size_t usable = c->ring_bytes > 8 * 1024 ? c->ring_bytes - 8 * 1024 : 0;
+        const long long rows = (long long)(usable / ring_row_bytes) / kRowPad * kRowPad - pad;
+        if (rows < c->k) return fail(MOE_ERR_UNSUPPORTED, "ring_bytes too small for one token per macrobatch");
+        Mb = (int)(rows / c->k);
     }
     if (c->T > 0 && Mb > c->T) Mb = c->T;
     if (Mb <= 0) Mb = 1;
     L.Mb = Mb;
     L.nM = c->T > 0 ? ceil_div(c->T, Mb) : 1;
-    L.ring_halves = L.nM > 1 ? 2 : 1;
+    L.ring_halves = 1;
     const long long rows_pad_max = (long long)L.R + (long long)L.nM * pad;
     const long long half_rows = (long long)std::min<long long>((long long)Mb * c->k, L.R) + pad;
     L.rows_pad_max = (int)align_up((size_t)std::max<long long>(rows_pad_max, kRowPad), kRowPad);
@@ -157,9 +168,9 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     L.s_row_slot = take(4 * rp);
     L.s_a = take(2 * rp * F);
     L.s_b = take(2 * rp * F);
-    // one macrobatch holds every routed row in global expert order, which is the
-    // order the dW1/dW3 GEMM reads X in: keep the forward's dispatched rows
-    L.keep_x = !mx && nM == 1;
+    // bf16: the dispatched x rows stay in the saved context at their global padded rows (the
+    // order the dW1/dW3 GEMM reads X in), so the backward never gathers them again
+    L.keep_x = !mx;
     L.s_xs = L.keep_x ? take(2 * rp * H) : 0;
     L.saved_bytes = o;
 
@@ -173,6 +184,14 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     L.mb_rows = (int)align_up((size_t)std::max(L.minibatch_rows, kRowPad), kRowPad);
     // per macrobatch: per-minibatch ready rows + the claim counter (zeroed by the schedule scan)
     L.w_ready = take(4 * (size_t)L.nM * ((size_t)L.half_rows / kRowPad + 2));
+    L.tile_list_max = L.rows_pad_max / kRowPad + L.nM * L.E;
+    L.w_tiles128 = take(16 * (size_t)L.tile_list_max);
+    L.w_tiles256 = take(16 * (size_t)L.tile_list_max);
+    L.w_tile_counts = take(2 * 4);
+    L.w_decode = take(4 * (1 + (size_t)L.E));
+    // few bf16 tokens in one macrobatch: every expert holds at most T <= 128 rows, and the
+    // forward streams each expert's weights once through the decode kernel
+    L.decode = kDecodePath && !mx && c->T > 0 && c->T <= kDecodeMaxTokens && L.nM == 1;
     const size_t region = o;
     const size_t ring_rows = (size_t)L.half_rows * L.ring_halves;
     // forward region: the ring
@@ -306,7 +325,8 @@ bool make_map_f32_out(CUtensorMap *m, void *base, size_t rows, size_t cols) {
     return r == CUDA_SUCCESS;
 }
 
-// bf16 [rows, cols] output map for TMA stores of 32 x 32 boxes (no swizzle)
+// bf16 [rows, cols] output map for TMA stores of 32 x 32 boxes (64 B rows, 64-byte swizzle:
+// the staging layout of the epilogues)
 bool make_map_bf16_out(CUtensorMap *m, void *base, size_t rows, size_t cols) {
     EncodeTiledFn enc = encode_fn();
     if (!enc || rows == 0) return false;
@@ -315,7 +335,7 @@ bool make_map_bf16_out(CUtensorMap *m, void *base, size_t rows, size_t cols) {
     cuuint32_t box[2] = {32, 32};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -461,6 +481,56 @@ moe_status_t moe_plan(const moe_config_t *cfg, moe_plan_t *plan) {
     plan->workspace_bytes = L.workspace_bytes + kBaseSlack;
     plan->saved_bytes = L.saved_bytes + kBaseSlack;
     plan->qweights_bytes = 0;
+    return MOE_OK;
+}
+
+moe_status_t moe_buffer_location(const moe_config_t *cfg, int which, int *in_saved, size_t *offset,
+                                 size_t *bytes) {
+    if (!in_saved || !offset || !bytes) return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
+    Layout L;
+    moe_status_t st = make_layout(cfg, L);
+    if (st != MOE_OK) return st;
+    const bool mx = L.precision == MOE_PRECISION_MXFP8;
+    const size_t rp = L.rows_pad_max, H = L.H, F = L.F;
+    const size_t ring_rows = (size_t)L.half_rows * L.ring_halves;
+    struct Loc { int saved; size_t off, bytes; bool mx_only; };
+    Loc loc{};
+    switch (which) {
+        case MOE_BUF_PADDED_OFFSETS: loc = {1, L.s_offp, 4 * ((size_t)L.nM * L.E + 1), false}; break;
+        case MOE_BUF_ROW_SLOT: loc = {1, L.s_row_slot, 4 * rp, false}; break;
+        case MOE_BUF_A: loc = {1, L.s_a, 2 * rp * F, false}; break;
+        case MOE_BUF_B: loc = {1, L.s_b, 2 * rp * F, false}; break;
+        case MOE_BUF_RING_X:
+            loc = L.keep_x ? Loc{1, L.s_xs, 2 * rp * H, false} : Loc{0, L.w_ringX, ring_rows * (mx ? H : 2 * H), false};
+            break;
+        case MOE_BUF_RING_X_SCALES: loc = {0, L.w_ringXs, ring_rows * H / kMxBlock, true}; break;
+        case MOE_BUF_RING_H: loc = {0, L.w_ringH, ring_rows * (mx ? F : 2 * F), false}; break;
+        case MOE_BUF_RING_H_SCALES: loc = {0, L.w_ringHs, ring_rows * F / kMxBlock, true}; break;
+        case MOE_BUF_DA: loc = {0, L.w_da, 2 * rp * F, false}; break;
+        case MOE_BUF_DB: loc = {0, L.w_db, 2 * rp * F, false}; break;
+        case MOE_BUF_HW: loc = {0, L.w_hw, 2 * rp * F, false}; break;
+        case MOE_BUF_DY_ROWS: loc = {0, L.w_Ginq, rp * H, true}; break;
+        case MOE_BUF_DY_ROWS_SCALES: loc = {0, L.w_Ginq_s, rp * H / kMxBlock, true}; break;
+        case MOE_BUF_DA_ROWS: loc = {0, L.w_daq, rp * F, true}; break;
+        case MOE_BUF_DA_ROWS_SCALES: loc = {0, L.w_daq_s, rp * F / kMxBlock, true}; break;
+        case MOE_BUF_DB_ROWS: loc = {0, L.w_dbq, rp * F, true}; break;
+        case MOE_BUF_DB_ROWS_SCALES: loc = {0, L.w_dbq_s, rp * F / kMxBlock, true}; break;
+        case MOE_BUF_X_TOKENS: loc = {0, L.w_XsT, rp * H, true}; break;
+        case MOE_BUF_X_TOKENS_SCALES: loc = {0, L.w_XsT_s, rp * H / kMxBlock, true}; break;
+        case MOE_BUF_DY_TOKENS: loc = {0, L.w_GinT, rp * H, true}; break;
+        case MOE_BUF_DY_TOKENS_SCALES: loc = {0, L.w_GinT_s, rp * H / kMxBlock, true}; break;
+        case MOE_BUF_HW_TOKENS: loc = {0, L.w_hwT, rp * F, true}; break;
+        case MOE_BUF_HW_TOKENS_SCALES: loc = {0, L.w_hwT_s, rp * F / kMxBlock, true}; break;
+        case MOE_BUF_DA_TOKENS: loc = {0, L.w_daT, rp * F, true}; break;
+        case MOE_BUF_DA_TOKENS_SCALES: loc = {0, L.w_daT_s, rp * F / kMxBlock, true}; break;
+        case MOE_BUF_DB_TOKENS: loc = {0, L.w_dbT, rp * F, true}; break;
+        case MOE_BUF_DB_TOKENS_SCALES: loc = {0, L.w_dbT_s, rp * F / kMxBlock, true}; break;
+        default: return fail(MOE_ERR_INVALID_ARG, "unknown buffer");
+    }
+    if (loc.mx_only && !mx) return fail(MOE_ERR_UNSUPPORTED, "buffer exists in MXFP8 configurations only");
+    *in_saved = loc.saved;
+    *offset = loc.off;
+    *bytes = loc.bytes;
     return MOE_OK;
 }
 
@@ -623,8 +693,48 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
         if (st != MOE_OK) return st;
     }
 
-    // 3. per macrobatch: dispatch -> GEMM1+SwiGLU -> GEMM2 -> combine
     const bool mx = cfg->precision == MOE_PRECISION_MXFP8;
+    if (L.decode) {
+        // 3'. few tokens: dispatch into the saved x rows -> decode FFN (both GEMMs, weights
+        // streamed once) -> combine
+        bf16 *xs = at<bf16>(saved, L.s_xs);
+        bf16 *ringH = at<bf16>(ws, L.w_ringH), *ringY = at<bf16>(ws, L.w_ringY);
+        const size_t rp = L.rows_pad_max;
+        DecodeArgs da;
+        std::memset(&da, 0, sizeof(da));
+        if (!make_map_mn(&da.w1, W1, (size_t)L.E * L.H, L.F, 64, 2) || !make_map_mn(&da.w3, W3, (size_t)L.E * L.H, L.F, 64, 2) ||
+            !make_map_mn(&da.w2, W2, (size_t)L.E * L.F, L.H, 64, 2) || !make_map(&da.x, xs, rp, L.H, 128) ||
+            !make_map(&da.h, ringH, rp, L.F, 128))
+            return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        da.offp = s_offp; da.counts = at<int32_t>(saved, L.s_counts);
+        da.a = s_a; da.b = s_b; da.hrows = ringH; da.y = ringY;
+        int *dc = at<int>(ws, L.w_decode);
+        da.claim = dc; da.hdone = dc + 1;
+        da.E = L.E; da.H = L.H; da.F = L.F;
+        da.status = at<int>(ws, L.w_status); da.budget_ns = budget_ns(cfg);
+        st = cuda_check(cudaMemsetAsync(dc, 0, 4 * (1 + (size_t)L.E), s), "decode counters clear");
+        if (st != MOE_OK) return st;
+        DispatchArgs d{};
+        d.src = (const bf16 *)x; d.dst = xs; d.row_slot = s_row_slot; d.offp = s_offp;
+        d.beg = 0; d.end = L.E; d.dst_row0 = 0; d.H = L.H; d.k = L.k;
+        {
+            ProfScope ps("dispatch", s);
+            st = cuda_check(launch_dispatch(d, L.rows_pad_max, L.num_sms, s), "dispatch launch");
+        }
+        if (st != MOE_OK) return st;
+        {
+            ProfScope ps("decode_ffn", s);
+            st = cuda_check(launch_decode_ffn(da, L.num_sms, s), "decode FFN launch");
+        }
+        if (st != MOE_OK) return st;
+        CombineArgs ca{};
+        ca.Y = ringY; ca.slot_row = s_slot_row; ca.offp = s_offp; ca.w = s_w; ca.out = (bf16 *)out;
+        ca.t0 = 0; ca.t1 = L.T; ca.k = L.k; ca.H = L.H; ca.E = L.E; ca.m = 0; ca.ring_base = 0;
+        ProfScope ps("combine", s);
+        return cuda_check(launch_combine(ca, L.num_sms, s), "combine launch");
+    }
+
+    // 3. per macrobatch: dispatch -> GEMM1+SwiGLU -> GEMM2 -> combine
     bf16 *ringX = L.keep_x ? at<bf16>(saved, L.s_xs) : at<bf16>(ws, L.w_ringX);
     bf16 *ringH = at<bf16>(ws, L.w_ringH), *ringY = at<bf16>(ws, L.w_ringY);
     uint8_t *ringXq = at<uint8_t>(ws, L.w_ringX), *ringHq = at<uint8_t>(ws, L.w_ringH);
@@ -633,7 +743,9 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
     GemmArgs g1 = gemm_base(L, ws, s_offp, cfg), g2 = gemm_base(L, ws, s_offp, cfg);
     if (!mx) {
         const int nb2 = kPairGemm ? 2 : 4;   // 64-column chunks of GEMM2's B per CTA
-        if (!make_map(&g1.a0, ringX, ring_rows, L.H, 128) || !make_map_mn(&g1.b0, W1, (size_t)L.E * L.H, L.F, 64, 2) ||
+        // kept x rows: GEMM1's A rows are global padded rows of the saved context
+        if (!make_map(&g1.a0, ringX, L.keep_x ? (size_t)L.rows_pad_max : ring_rows, L.H, 128) ||
+            !make_map_mn(&g1.b0, W1, (size_t)L.E * L.H, L.F, 64, 2) ||
             !make_map_mn(&g1.b1, W3, (size_t)L.E * L.H, L.F, 64, 2) || !make_map(&g2.a0, ringH, ring_rows, L.F, 128) ||
             !make_map_mn(&g2.b0, W2, (size_t)L.E * L.F, L.H, 64, nb2))
             return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
@@ -662,7 +774,8 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
         g1.q0 = ringHq; g1.qs0 = ringHs;
         g2.sfa0 = ringHs; g2.sfb0 = qw + q.scales[QW_W2T]; g2.kstore = L.F;
     }
-    g1.N = L.F; g1.K = L.H; g1.a_ring = 1;
+    g1.N = L.F; g1.K = L.H; g1.a_ring = L.keep_x ? 0 : 1;
+    g1.x_global = L.keep_x ? 1 : 0;
     g1.o0 = s_a; g1.o1 = s_b;
     g2.N = L.H; g2.K = L.F; g2.a_ring = 1; g2.o_ring = 1;
     g2.o0 = ringY;
@@ -837,8 +950,28 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
     gb2.in0 = s_a; gb2.in1 = s_b; gb2.o0 = dA; gb2.o1 = dB; gb2.o2 = HW; gb2.of0 = dwpart;
     gb2.row_slot = s_row_slot; gb2.wslot = s_w;
     gb1.N = L.H; gb1.K = 2 * L.F; gb1.o0 = dXs;
+    // With several macrobatches the dgrads still run as one launch each: their operands and
+    // outputs are full size, so the M tiles of every (macrobatch, expert) run come from a
+    // device-built list in expert-major order, and the CTAs running at one time share one
+    // expert's weights (read from HBM about once per dgrad instead of once per macrobatch).
+    const int dgrad_launches = L.nM > 1 ? 1 : L.nM;
+    if (L.nM > 1 && L.T > 0) {
+        int4 *l128 = at<int4>(ws, L.w_tiles128), *l256 = at<int4>(ws, L.w_tiles256);
+        int *cnt = at<int>(ws, L.w_tile_counts);
+        {
+            ProfScope ps("tile_lists", s);
+            st = cuda_check(launch_tile_lists(s_offp, L.E, L.nM, l128, l256, cnt, s), "tile list launch");
+        }
+        if (st != MOE_OK) return st;
+        // the GEMM2 dgrad runs 1-CTA tiles of 128 rows; the GEMM1 dgrad CTA pairs of 256
+        const bool pair1 = mx ? pair_fp8(OP_BWD1) : kPairGemm;
+        gb2.tiles = l128;
+        gb2.tile_count = cnt;
+        gb1.tiles = pair1 ? l256 : l128;
+        gb1.tile_count = pair1 ? cnt + 1 : cnt;
+    }
     if (L.T > 0) {
-        for (int m = 0; m < L.nM; ++m) {
+        for (int m = 0; m < dgrad_launches; ++m) {
             gb2.m = m;
             {
                 ProfScope ps("grouped_gemm_bwd2_swiglu", s);
@@ -851,7 +984,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
             if ((st = transpose_q(dA, L.w_daT, L.w_daT_s, L.F, "quantize_da_tokens")) != MOE_OK) return st;
             if ((st = transpose_q(dB, L.w_dbT, L.w_dbT_s, L.F, "quantize_db_tokens")) != MOE_OK) return st;
         }
-        for (int m = 0; m < L.nM; ++m) {
+        for (int m = 0; m < dgrad_launches; ++m) {
             gb1.m = m;
             {
                 ProfScope ps("grouped_gemm_bwd1", s);

@@ -35,7 +35,7 @@ struct Layout {
     int Mb, nM;             // macrobatch tokens / count
     int rows_pad_max;       // bound on padded sorted rows (all macrobatches)
     int half_rows;          // bound on padded rows of one macrobatch (one ring half)
-    int ring_halves;        // 1 or 2
+    int ring_halves;        // 1 (the ring holds one macrobatch)
     int nchunks;            // schedule blocks
     int chunks_per_mb;
     int minibatch_rows;
@@ -49,6 +49,10 @@ struct Layout {
     bool keep_x;
     // workspace (header first, then a region shared by forward and backward)
     size_t w_status, w_chunk_counts, w_chunk_base, w_wrt, w_offp, w_ready;
+    size_t w_tiles128, w_tiles256, w_tile_counts;   // backward M-tile lists (several macrobatches)
+    size_t w_decode;        // decode forward: work-item counter + per-expert h counters
+    bool decode;            // bf16 forward of few tokens through the decode kernel
+    int tile_list_max;                              // entries each list can hold
     int mb_rows;            // minibatch rows used by the fused dispatch (multiple of 128)
     size_t w_ringX, w_ringXs, w_ringH, w_ringHs, w_ringY, ring_bytes;   // forward
     size_t w_Xs, w_Gin, w_da, w_db, w_hw, w_dXs, w_dwpart, w_dlogits, w_dwr_part;   // backward

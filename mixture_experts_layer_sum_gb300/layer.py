@@ -66,6 +66,14 @@ class MoeLayer:
         _m.moe_schedule(self.cfg, topk_ids, counts, offsets, s2s, s2sorted, self.workspace, stream)
         return counts, offsets, s2s[:R], s2sorted[:R]
 
+    def buffer(self, name):
+        """A uint8 view of one intermediate buffer inside the saved buffer or the workspace
+        (moe_buffer_location; a test and debugging aid)."""
+        in_saved, off, nb = _m.moe_buffer_location(self.cfg, name)
+        base = self.saved if in_saved else self.workspace
+        start = (-base.data_ptr()) % 1024          # the library's 1024-byte-aligned base
+        return base[start + off:start + off + nb]
+
     def status(self, stream=None):
         """Synchronises and raises MoeError if a device-side check failed."""
         return _m.moe_query_status(self.workspace, stream)

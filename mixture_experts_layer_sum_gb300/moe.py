@@ -26,7 +26,15 @@ MOE_PRECISION_MXFP8 = 1
 EXPORTED = (
     "moe_abi_version", "moe_plan", "moe_workspace_size", "moe_saved_size", "moe_qweights_size",
     "moe_schedule", "moe_schedule_static", "moe_quantize_weights", "moe_forward", "moe_backward", "moe_query_status",
-    "moe_reset_status", "moe_last_error_string", "moe_profile_begin", "moe_profile_end",
+    "moe_reset_status", "moe_last_error_string", "moe_profile_begin", "moe_profile_end", "moe_buffer_location",
+)
+
+# moe_buffer_t (include/moe.h): intermediate buffers moe_buffer_location can locate
+BUFFERS = (
+    "PADDED_OFFSETS", "ROW_SLOT", "A", "B", "RING_X", "RING_X_SCALES", "RING_H", "RING_H_SCALES",
+    "DA", "DB", "HW", "DY_ROWS", "DY_ROWS_SCALES", "DA_ROWS", "DA_ROWS_SCALES", "DB_ROWS", "DB_ROWS_SCALES",
+    "X_TOKENS", "X_TOKENS_SCALES", "DY_TOKENS", "DY_TOKENS_SCALES", "HW_TOKENS", "HW_TOKENS_SCALES",
+    "DA_TOKENS", "DA_TOKENS_SCALES", "DB_TOKENS", "DB_TOKENS_SCALES",
 )
 
 
@@ -88,6 +96,8 @@ def _load():
         "moe_last_error_string": ([], ctypes.c_char_p),
         "moe_profile_begin": ([], ctypes.c_int),
         "moe_profile_end": ([ctypes.POINTER(moe_kernel_time_t), ctypes.c_int], ctypes.c_int),
+        "moe_buffer_location": ([cfgp, ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_size_t),
+                                 ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -211,3 +221,12 @@ def moe_profile_end(max_entries: int = 64):
     if n < 0:
         raise MoeError(-n, moe_last_error_string())
     return [(buf[i].name.decode(), buf[i].launches, buf[i].total_ms) for i in range(min(n, max_entries))]
+
+
+def moe_buffer_location(cfg, name):
+    """(in_saved, offset, bytes) of an intermediate buffer, by its moe_buffer_t name without the
+    MOE_BUF_ prefix (a test and debugging aid; see include/moe.h)."""
+    in_saved, off, nb = ctypes.c_int(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(_lib.moe_buffer_location(ctypes.byref(cfg), BUFFERS.index(name), ctypes.byref(in_saved),
+                                    ctypes.byref(off), ctypes.byref(nb)))
+    return bool(in_saved.value), off.value, nb.value

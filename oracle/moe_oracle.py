@@ -257,7 +257,7 @@ def sigmoid(a):
     return 1.0 / (1.0 + np.exp(-a))
 
 
-def forward(x, Wr, bias, W1, W3, W2, k, *, precision="bf16", macrobatch_tokens=0, ids=None):
+def forward(x, Wr, bias, W1, W3, W2, k, *, precision="bf16", macrobatch_tokens=0, ids=None, weight_cache=None):
     """One MoE layer forward over T tokens ([KC] section 03: Schedule, Dispatch,
     Expert FFN, Combine, final weighted fusion).
 
@@ -265,6 +265,9 @@ def forward(x, Wr, bias, W1, W3, W2, k, *, precision="bf16", macrobatch_tokens=0
     by the caller). `ids` overrides the router's choice (used where GPU and
     oracle sit on a near-tie). precision "mxfp8" emulates MXFP8 operands of both
     GEMMs: x and W1/W3 along H, h and W2 along F ([KC] section 02).
+    weight_cache: optional dict that keeps each expert's (quantised) weight copies
+    across calls with the same weights (the quantisation of the weights happens once
+    per weight update, not per step).
     Returns a dict with out [T,H] and every saved intermediate."""
     x = np.asarray(x, np.float64)
     T, H = x.shape
@@ -281,7 +284,7 @@ def forward(x, Wr, bias, W1, W3, W2, k, *, precision="bf16", macrobatch_tokens=0
     F = W1.shape[2]
     a = np.zeros((R, F)); b = np.zeros((R, F)); h = np.zeros((R, F)); Y = np.zeros((R, H))
     mx = precision == "mxfp8"
-    wq = {}   # MXFP8: each expert's weight copies, quantised once for all its runs
+    wq = {} if weight_cache is None else weight_cache   # each expert's weight copies, made once
 
     def weights(e):
         if e not in wq:
@@ -312,12 +315,12 @@ def forward(x, Wr, bias, W1, W3, W2, k, *, precision="bf16", macrobatch_tokens=0
             "tok": tok, "precision": precision}
 
 
-def backward(fwd, dout, x, Wr, W1, W3, W2):
+def backward(fwd, dout, x, Wr, W1, W3, W2, weight_cache=None):
     """Gradients of sum(dout * out) with the top-k selection held fixed; the
     router bias is a constant input. Mirrors the forward ([KC] section 02:
     reverse-combine, then reverse-dispatch, [DD]).
     Returns dict(dx [T,H], dWr [H,E], dW1, dW3 [E,H,F], dW2 [E,F,H], dw [T,k],
-    dlogits [T,E])."""
+    dlogits [T,E]). weight_cache: as in forward, for the dgrads' weight copies."""
     dout = np.asarray(dout, np.float64)
     x = np.asarray(x, np.float64)
     T, H = x.shape
@@ -336,7 +339,7 @@ def backward(fwd, dout, x, Wr, W1, W3, W2):
     dW1 = np.zeros((E, H, F)); dW3 = np.zeros((E, H, F)); dW2 = np.zeros((E, F, H))
     da_all = np.zeros((R, F)); db_all = np.zeros((R, F)); hw_all = np.zeros((R, F))
     segs = expert_segments(fwd)
-    wq = {}   # MXFP8: each expert's dgrad weight copies, quantised once for all its runs
+    wq = {} if weight_cache is None else weight_cache   # each expert's dgrad weight copies, made once
 
     def weights(e):
         if e not in wq:

@@ -61,22 +61,18 @@ def test_plan_sizes_and_ring(moe):
     assert pf.rows_padded_max >= 16384 * 8 and pf.rows_padded_max % 128 == 0
 
 
-def test_saved_keeps_dispatched_rows_only_for_one_bf16_macrobatch(moe):
-    # bf16 with one macrobatch: the forward's expert-sorted x rows [rows_padded_max, H] bf16 live in
-    # the saved context (the backward's dW1/dW3 reads them there); MXFP8 or several macrobatches
-    # keep the same context without them
+def test_saved_keeps_dispatched_rows_for_bf16(moe):
+    # bf16: the forward's expert-sorted x rows [rows_padded_max, H] bf16 live in the saved context
+    # for any number of macrobatches (GEMM1 reads them there, then the backward's dW1/dW3); MXFP8
+    # keeps the same context without them (its weight gradient needs x along the tokens)
     a1024 = lambda v: -(-v // 1024) * 1024
     T, H, F, E, k = 4096, 2048, 1024, 32, 4
-    bf = moe.make_config(T, H, F, E, k, num_sms=152)
-    mx = moe.make_config(T, H, F, E, k, "mxfp8", num_sms=152)
-    p = moe.moe_plan(bf)
-    assert p.num_macrobatches == 1
-    assert moe.moe_saved_size(bf) - moe.moe_saved_size(mx) == a1024(2 * p.rows_padded_max * H)
-    many = moe.make_config(T, H, F, E, k, macrobatch_tokens=1024, num_sms=152)
-    pm = moe.moe_plan(many)
-    assert pm.num_macrobatches == 4
-    many_mx = moe.make_config(T, H, F, E, k, "mxfp8", macrobatch_tokens=1024, num_sms=152)
-    assert moe.moe_saved_size(many) == moe.moe_saved_size(many_mx)
+    for Mb in (0, 1024):
+        bf = moe.make_config(T, H, F, E, k, macrobatch_tokens=Mb, num_sms=152)
+        mx = moe.make_config(T, H, F, E, k, "mxfp8", macrobatch_tokens=Mb, num_sms=152)
+        p = moe.moe_plan(bf)
+        assert p.num_macrobatches == (1 if Mb == 0 else 4)
+        assert moe.moe_saved_size(bf) - moe.moe_saved_size(mx) == a1024(2 * p.rows_padded_max * H)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -136,3 +132,42 @@ def test_library_does_not_reference_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in src.lower(), f
+
+
+def test_buffer_locations_lie_inside_their_buffers(moe):
+    for prec in ("bf16", "mxfp8"):
+        for Mb in (0, 700):
+            cfg = moe.make_config(3000, 512, 512, 16, 4, prec, macrobatch_tokens=Mb, num_sms=152)
+            p = moe.moe_plan(cfg)
+            for name in moe.BUFFERS:
+                if prec == "bf16" and (name.endswith("_SCALES") or name.endswith("_ROWS") or name.endswith("_TOKENS")):
+                    with pytest.raises(moe.MoeError) as e:
+                        moe.moe_buffer_location(cfg, name)
+                    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+                    continue
+                in_saved, off, nb = moe.moe_buffer_location(cfg, name)
+                limit = (p.saved_bytes if in_saved else p.workspace_bytes) - 1024
+                assert nb > 0 and off % 1024 == 0 and off + nb <= limit, (prec, name)
+    # an unknown buffer and null outputs are rejected
+    cfg = moe.make_config(64, 256, 256, 4, 2, num_sms=152)
+    i, o, n = ctypes.c_int(), ctypes.c_size_t(), ctypes.c_size_t()
+    lib = moe.library()
+    assert lib.moe_buffer_location(ctypes.byref(cfg), len(moe.BUFFERS), ctypes.byref(i), ctypes.byref(o),
+                                   ctypes.byref(n)) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_buffer_location(ctypes.byref(cfg), 0, None, None, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_ring_holds_one_macrobatch(moe):
+    # the macrobatch is the largest token count whose padded rows (MXFP8: dispatched x, h and
+    # expert output rows; bf16: h and Y, x going to the saved context), in whole 128-row tiles,
+    # fit the ring once (less 8 KiB for buffer alignment); a kernel never overlaps its
+    # predecessor on the stream, so one macrobatch is in flight at a time
+    H, F, E, k = 7168, 2048, 16, 8
+    pad = 127 * E
+    for prec, row in (("mxfp8", (H + H // 32) + (F + F // 32) + 2 * H), ("bf16", 2 * F + 2 * H)):
+        cfg = moe.make_config(16384, H, F, E, k, prec, ring_bytes=256 << 20, num_sms=152)
+        p = moe.moe_plan(cfg)
+        cap = ((256 << 20) - 8192) // row // 128 * 128
+        assert p.macrobatch_tokens * k + pad <= cap < (p.macrobatch_tokens + 1) * k + pad, prec
+        assert p.ring_bytes <= 256 << 20
+        assert p.num_macrobatches == -(-16384 // p.macrobatch_tokens)
