@@ -14,9 +14,10 @@
 //     y rows in bf16 for the combine.
 // One persistent CTA per SM (192 threads): warp 0 claims work items from a device counter
 // (every GEMM1 item first, then every GEMM2 item; items of experts without rows are skipped)
-// and streams their operands by TMA through a 4-stage ring of 48 KB stages; warp 1 issues the
-// MMAs (M = 128, N = 128, K = 16) into a double-buffered TMEM accumulator (256 columns per
-// item); warps 2-5 run the epilogues. A GEMM2 item waits (bounded, acquire) until all F/128
+// and streams their operands by TMA through a ring of 36-48 KB stages (32 KB of weights and
+// the expert's token rows in 32-row boxes; 4-6 stages, the more the fewer tokens); warp 1
+// issues the MMAs (M = 128, N = the expert's rows rounded up to 32, K = 16) into a
+// double-buffered TMEM accumulator (256 columns per item); warps 2-5 run the epilogues. A GEMM2 item waits (bounded, acquire) until all F/128
 // GEMM1 items of its expert have published h (release), so GEMM2 tiles of early experts run
 // while GEMM1 tiles of late ones still stream, and no SM idles at a phase boundary. Items
 // are claimed in order and GEMM1 items wait on nothing, so every wait ends.
@@ -26,14 +27,22 @@ namespace moe {
 
 namespace {
 
-constexpr int DST = 4;                               // pipeline stages
+constexpr int DST_MAX = 8;                           // pipeline stages (at most)
 constexpr uint32_t DW_TILE = 2 * 64 * 64 * 2;        // 16 KB: 128 weight columns x 64 K rows, MN-major
-constexpr uint32_t DT_TILE = 128 * 64 * 2;           // 16 KB: 128 token rows x 64 K, K-major
-constexpr uint32_t DSTAGE = 2 * DW_TILE + DT_TILE;   // 48 KB: W1 (or W2), W3, token rows
+constexpr uint32_t DT_BOX = 32 * 64 * 2;             // 4 KB: 32 token rows x 64 K, K-major
+constexpr uint32_t DSMEM = 216 * 1024;               // shared memory for the stages
 constexpr int QD = 4;                                // depth of the work-item queue in shared memory
 
+// Stage layout for a launch: W1 (or W2) tile, W3 tile, then nb boxes of 32 token rows, where
+// nb = ceil(T / 32) covers the most rows an expert can hold; fewer token rows per stage leave
+// room for more stages, i.e. more weight bytes in flight per SM.
+__host__ __device__ constexpr uint32_t dec_stage_bytes(int nb) { return 2 * DW_TILE + nb * DT_BOX; }
+__host__ __device__ constexpr int dec_stages(int nb) {
+    return (int)(DSMEM / dec_stage_bytes(nb)) < DST_MAX ? (int)(DSMEM / dec_stage_bytes(nb)) : DST_MAX;
+}
+
 struct DecCtl {
-    uint64_t full[DST], empty[DST], tfull[2], tempty[2], qfull[QD], qempty[QD], drain;
+    uint64_t full[DST_MAX], empty[DST_MAX], tfull[2], tempty[2], qfull[QD], qempty[QD], drain;
     uint32_t tmem_base;
     int item[QD];
 };
@@ -71,6 +80,8 @@ __device__ __forceinline__ Item decode_item(const DecodeArgs &a, int id) {
 
 __device__ void dec_producer(const DecodeArgs &a, DecCtl &c, uint8_t *tiles, const WaitCtl &ctl) {
     const int total = a.E * (a.F / 128 + a.H / 128);
+    const int DST = dec_stages(a.nb);
+    const uint32_t DSTAGE = dec_stage_bytes(a.nb);
     int stage = 0, slot = 0;
     uint32_t phase = 0, qphase = 0;
     uint32_t issued = 0, last_phase = 0;
@@ -91,6 +102,7 @@ __device__ void dec_producer(const DecodeArgs &a, DecCtl &c, uint8_t *tiles, con
         if (id < 0) break;
         const Item it = decode_item(a, id);
         const int s0 = a.offp[it.e];
+        const int nb = (a.counts[it.e] + 31) / 32;   // 32-row boxes holding the expert's rows
         if (!it.gemm1) {
             // h of this expert: every GEMM1 item of it has published its columns
             if (!flag_wait_geq(a.hdone + it.e, a.F / 128, ctl)) { ok = false; continue; }
@@ -102,14 +114,14 @@ __device__ void dec_producer(const DecodeArgs &a, DecCtl &c, uint8_t *tiles, con
             const uint32_t sA = smem_u32(tiles + stage * DSTAGE);
             const uint32_t sT = sA + 2 * DW_TILE;
             if (it.gemm1) {
-                mbar_arrive_expect_tx(bar, DSTAGE);
+                mbar_arrive_expect_tx(bar, 2 * DW_TILE + nb * DT_BOX);
                 tma_load_3d(sA, &a.w1, bar, 0, it.e * a.H + kb * 64, it.col0 / 64);
                 tma_load_3d(sA + DW_TILE, &a.w3, bar, 0, it.e * a.H + kb * 64, it.col0 / 64);
-                tma_load_2d(sT, &a.x, bar, kb * 64, s0);
+                for (int j = 0; j < nb; ++j) tma_load_2d(sT + j * DT_BOX, &a.x, bar, kb * 64, s0 + 32 * j);
             } else {
-                mbar_arrive_expect_tx(bar, DW_TILE + DT_TILE);
+                mbar_arrive_expect_tx(bar, DW_TILE + nb * DT_BOX);
                 tma_load_3d(sA, &a.w2, bar, 0, it.e * a.F + kb * 64, it.col0 / 64);
-                tma_load_2d(sT, &a.h, bar, kb * 64, s0);
+                for (int j = 0; j < nb; ++j) tma_load_2d(sT + j * DT_BOX, &a.h, bar, kb * 64, s0 + 32 * j);
             }
             issued |= 1u << stage;
             last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
@@ -128,7 +140,8 @@ __device__ void dec_producer(const DecodeArgs &a, DecCtl &c, uint8_t *tiles, con
 }
 
 __device__ void dec_mma(const DecodeArgs &a, DecCtl &c, uint8_t *tiles, uint32_t tmem, const WaitCtl &ctl) {
-    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, true, false);   // A MN-major, B K-major
+    const int DST = dec_stages(a.nb);
+    const uint32_t DSTAGE = dec_stage_bytes(a.nb);
     int stage = 0, slot = 0, acc = 0;
     uint32_t phase = 0, qphase = 0, acc_phase = 0;
     for (;;) {
@@ -138,6 +151,8 @@ __device__ void dec_mma(const DecodeArgs &a, DecCtl &c, uint8_t *tiles, uint32_t
         if (++slot == QD) { slot = 0; qphase ^= 1; }
         if (id < 0) break;
         const Item it = decode_item(a, id);
+        // N = the expert's rows rounded up to 32 (A MN-major weights, B K-major token rows)
+        const uint32_t idesc = idesc_bf16_f32(128, 32 * ((a.counts[it.e] + 31) / 32), true, false);
         if (!mbar_wait(smem_u32(&c.tempty[acc]), acc_phase ^ 1, ctl)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * 256;
@@ -185,16 +200,23 @@ __device__ void dec_epilogue(const DecodeArgs &a, DecCtl &c, uint32_t tmem, cons
         tc_fence_after();
         const uint32_t tbase = tmem + lane_base + acc * 256;
         const int s0 = a.offp[it.e];
+        const int nb = (a.counts[it.e] + 31) / 32;   // 32-row column blocks the MMA computed
         if (it.gemm1) {
             // every row of the expert's 128-row padded run: padding rows have x = 0, so their
-            // a, b and h are exactly 0 (the backward reads a, b of the whole run)
+            // a, b and h are exactly 0 (the backward reads a, b of the whole run); rows past the
+            // computed blocks are written as those zeros
             const int f = it.col0 + col;
 #pragma unroll 1
             for (int rc = 0; rc < 4; ++rc) {
                 uint32_t va[32], vb[32];
-                tmem_ld_32x32b_x32(tbase + rc * 32, va);
-                tmem_ld_32x32b_x32(tbase + 128 + rc * 32, vb);
-                tmem_ld_wait();
+                if (rc < nb) {
+                    tmem_ld_32x32b_x32(tbase + rc * 32, va);
+                    tmem_ld_32x32b_x32(tbase + 128 + rc * 32, vb);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) va[i] = vb[i] = 0u;
+                }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int row = s0 + rc * 32 + i;
@@ -239,11 +261,11 @@ __device__ void dec_epilogue(const DecodeArgs &a, DecCtl &c, uint32_t tmem, cons
 __global__ void __launch_bounds__(192, 1) decode_ffn_kernel(const __grid_constant__ DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    DecCtl &c = *reinterpret_cast<DecCtl *>(tiles + DST * DSTAGE);
+    DecCtl &c = *reinterpret_cast<DecCtl *>(tiles + DSMEM);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     WaitCtl ctl{a.status, a.budget_ns};
     if (threadIdx.x == 0) {
-        for (int s = 0; s < DST; ++s) {
+        for (int s = 0; s < dec_stages(a.nb); ++s) {
             mbar_init(smem_u32(&c.full[s]), 1);
             mbar_init(smem_u32(&c.empty[s]), 1);
         }
@@ -289,7 +311,7 @@ __global__ void __launch_bounds__(192, 1) decode_ffn_kernel(const __grid_constan
 }  // namespace
 
 cudaError_t launch_decode_ffn(const DecodeArgs &a, int num_sms, cudaStream_t s) {
-    constexpr size_t smem = DST * DSTAGE + sizeof(DecCtl) + 1024;
+    constexpr size_t smem = DSMEM + sizeof(DecCtl) + 1024;
     static_assert(smem <= 227 * 1024, "shared memory budget");
     cudaError_t err = cudaFuncSetAttribute(decode_ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;

@@ -12,8 +12,9 @@ constexpr int kDecodeMaxTokens = 128;
 struct DecodeArgs {
     CUtensorMap w1, w3;   // W1, W3 viewed MN-major: (64 columns, E*H rows, F/64 chunks), box (64, 64, 2)
     CUtensorMap w2;       // W2 viewed MN-major: (64 columns, E*F rows, H/64 chunks), box (64, 64, 2)
-    CUtensorMap x;        // dispatched x rows [rows][H] bf16, box (64, 128), 128-byte swizzle
-    CUtensorMap h;        // h rows [rows][F] bf16, box (64, 128), 128-byte swizzle
+    CUtensorMap x;        // dispatched x rows [rows][H] bf16, box (64, 32), 128-byte swizzle
+    CUtensorMap h;        // h rows [rows][F] bf16, box (64, 32), 128-byte swizzle
+    int nb;               // ceil(T / 32): 32-row boxes the largest expert can need (<= 4)
     const int *offp;      // [E + 1] padded run starts (one macrobatch)
     const int *counts;    // [E] routed rows of each expert
     bf16 *a, *b;          // saved a = x W1, b = x W3 of every padded row (32 x 32 blocks, blk32_offset)

@@ -64,7 +64,7 @@ constexpr bool kPairGemmFp8 = true;
 inline bool pair_fp8(int op) { return kPairGemmFp8 && op != OP_BWD2; }
 constexpr int kGemmBN1 = 256;   // GEMM1 tile: 128 rows x (128 a-columns + 128 b-columns)
 // bf16 forward of at most kDecodeMaxTokens tokens through the decode kernel
-constexpr bool kDecodePath = false;
+constexpr bool kDecodePath = true;
 constexpr int kGemmBM = 128;
 
 // ---------------------------------------------------------------- planning
@@ -703,14 +703,14 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
         DecodeArgs da;
         std::memset(&da, 0, sizeof(da));
         if (!make_map_mn(&da.w1, W1, (size_t)L.E * L.H, L.F, 64, 2) || !make_map_mn(&da.w3, W3, (size_t)L.E * L.H, L.F, 64, 2) ||
-            !make_map_mn(&da.w2, W2, (size_t)L.E * L.F, L.H, 64, 2) || !make_map(&da.x, xs, rp, L.H, 128) ||
-            !make_map(&da.h, ringH, rp, L.F, 128))
+            !make_map_mn(&da.w2, W2, (size_t)L.E * L.F, L.H, 64, 2) || !make_map(&da.x, xs, rp, L.H, 32) ||
+            !make_map(&da.h, ringH, rp, L.F, 32))
             return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         da.offp = s_offp; da.counts = at<int32_t>(saved, L.s_counts);
         da.a = s_a; da.b = s_b; da.hrows = ringH; da.y = ringY;
         int *dc = at<int>(ws, L.w_decode);
         da.claim = dc; da.hdone = dc + 1;
-        da.E = L.E; da.H = L.H; da.F = L.F;
+        da.E = L.E; da.H = L.H; da.F = L.F; da.nb = ceil_div(L.T, 32);
         da.status = at<int>(ws, L.w_status); da.budget_ns = budget_ns(cfg);
         st = cuda_check(cudaMemsetAsync(dc, 0, 4 * (1 + (size_t)L.E), s), "decode counters clear");
         if (st != MOE_OK) return st;
