@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 typedef struct CUstream_st *moe_stream_t;   /* same type as cudaStream_t */
 
@@ -98,7 +98,13 @@ typedef enum {
  *     MOE_FAULT_GEMM1_READY: moe_forward sets GEMM1's first minibatch ready
  *     counter so that it never reaches its target; GEMM1's bounded wait runs
  *     out, the status word reports MOE_ERR_TIMEOUT, every other wait sees the
- *     status and returns, and the outputs of that call are undefined. */
+ *     status and returns, and the outputs of that call are undefined.
+ *   forward_mode: MOE_FORWARD_PERSISTENT (0, default): after the router and the
+ *     schedule, one persistent launch runs the dispatch, both expert GEMMs and
+ *     the combine of every macrobatch, handing work on through device counters;
+ *     MOE_FORWARD_PER_STAGE: one launch per stage and macrobatch. Both give the
+ *     same bytes. (A bf16 forward of at most 128 tokens in one macrobatch runs
+ *     the decode kernel in either mode.) */
 typedef struct {
     int T, H, F, E, k;
     int precision;
@@ -108,7 +114,11 @@ typedef struct {
     unsigned timeout_ms;
     int num_sms;
     unsigned fault_mask;
+    int forward_mode;
 } moe_config_t;
+
+#define MOE_FORWARD_PERSISTENT 0
+#define MOE_FORWARD_PER_STAGE 1
 
 #define MOE_FAULT_GEMM1_READY 1u
 

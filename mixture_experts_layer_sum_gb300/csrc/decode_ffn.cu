@@ -54,8 +54,6 @@ __device__ __forceinline__ size_t blk32_elem(int row, int col, int C) {
 
 __device__ __forceinline__ float sigmoid_d(float a) { return __fdividef(1.0f, 1.0f + __expf(-a)); }
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
 struct Item {
     bool gemm1;
     int e, col0, nk;
@@ -104,8 +102,8 @@ __device__ void dec_producer(const DecodeArgs &a, DecCtl &c, uint8_t *tiles, con
         const int s0 = a.offp[it.e];
         const int nb = (a.counts[it.e] + 31) / 32;   // 32-row boxes holding the expert's rows
         if (!it.gemm1) {
-            // h of this expert: every GEMM1 item of it has published its columns
-            if (!flag_wait_geq(a.hdone + it.e, a.F / 128, ctl)) { ok = false; continue; }
+            // h of this expert: the four epilogue warps of every GEMM1 item of it have published
+            if (!flag_wait_geq(a.hdone + it.e, 4 * (a.F / 128), ctl)) { ok = false; continue; }
             fence_proxy_async_global();
         }
         for (int kb = 0; kb < it.nk && ok; ++kb) {
@@ -244,11 +242,12 @@ __device__ void dec_epilogue(const DecodeArgs &a, DecCtl &c, uint32_t tmem, cons
         tc_fence_before();
         mbar_arrive(smem_u32(&c.tempty[acc]));
         if (it.gemm1) {
-            // publish: this item's h columns of expert e are in memory (generic stores, read by
-            // later TMA loads of other CTAs)
-            epi_bar();
-            if (warp == 2 && lane == 0) {
-                __threadfence();
+            // publish: this warp's 32 h columns of expert e are in memory (generic stores, read
+            // by later TMA loads of other CTAs); one release per warp, so no barrier joins the
+            // warps and a warp that gave up on a wait cannot hold the others
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) {
                 fence_proxy_async_global();
                 red_release_gpu_add(a.hdone + it.e, 1);
             }

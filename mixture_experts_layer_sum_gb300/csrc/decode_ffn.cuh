@@ -21,7 +21,7 @@ struct DecodeArgs {
     bf16 *hrows;          // h rows [rows][F] (the same memory as map h)
     bf16 *y;              // expert outputs [rows][H]
     int *claim;           // work-item counter (zeroed before the launch)
-    int *hdone;           // [E] GEMM1 items finished per expert (zeroed before the launch)
+    int *hdone;           // [E] GEMM1 epilogue warps finished per expert, 4 per item (zeroed before the launch)
     int E, H, F;
     int *status;
     unsigned long long budget_ns;

@@ -37,6 +37,7 @@
 #include <atomic>
 
 #include "grouped_gemm.cuh"
+#include "combine_item.cuh"
 
 namespace moe {
 
@@ -196,12 +197,13 @@ __device__ void init_tile_table(Ctl &c, const GemmArgs &g) {
 // stop_bar (optional): the warp stops claiming once phase 0 of this mbarrier has
 // completed — the epilogue warps gather too until their CTA's first accumulator is ready.
 constexpr int kGatherRows = 4;
+// m: the macrobatch; ready: its per-minibatch ready counters (the claim counter follows them).
 template <bool FP8>
-__device__ void gather_loop(const GemmArgs &g, const uint64_t *stop_bar = nullptr) {
+__device__ void gather_loop(const GemmArgs &g, int m, int *ready, const uint64_t *stop_bar = nullptr) {
     const int lane = threadIdx.x % 32;
-    const int r0 = g.offp[g.m * g.E], r1 = g.offp[(g.m + 1) * g.E];
+    const int r0 = g.offp[m * g.E], r1 = g.offp[(m + 1) * g.E];
     const int vecs = g.H / 8;
-    int *claim = g.ready + g.ready_slots;    // row-chunk counter, after the ready counters
+    int *claim = ready + g.ready_slots;      // row-chunk counter, after the ready counters
     for (;;) {
         if (stop_bar) {
             int done = 0;
@@ -287,7 +289,7 @@ __device__ void gather_loop(const GemmArgs &g, const uint64_t *stop_bar = nullpt
         if (lane == 0) {
             __threadfence();
             fence_proxy_async_global();
-            red_release_gpu_add(g.ready + (rb - r0) / g.mb_rows, kGatherRows);
+            red_release_gpu_add(ready + (rb - r0) / g.mb_rows, kGatherRows);
         }
     }
 }
@@ -557,6 +559,93 @@ __device__ __forceinline__ void stage_store_blk(uint8_t *warp_stage, int &nstore
     ++nstores;
 }
 
+// Epilogue of one GEMM1 tile (this thread's accumulator row r): a, b rounded to bf16 and saved
+// in 32 x 32 blocks at the global padded rows, h = silu(a) * b from the rounded a, b into the ring
+// (bf16, or E4M3 along F with its scale bytes).
+template <bool FP8, int NBUF>
+__device__ __forceinline__ void epi_fwd1_tile(const GemmArgs &g, const TileInfo &ti, uint32_t tbase, int r,
+                                              int quarter, int lane, int ring_shift, bool tma_bf16,
+                                              uint8_t *warp_stage, int &store_chunks) {
+    const int grow = ti.g0 + r;
+    const size_t F = g.F;
+    const int brow = ti.g0 + quarter * 32;   // first row of this warp's 32-row blocks of a, b
+    bf16 *ph = FP8 ? nullptr : g.o2 + (size_t)(grow + ring_shift) * F + ti.nt * 128;
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+        uint32_t va[32], vb[32];
+        tmem_ld_32x32b_x32(tbase + cc * 32, va);
+        tmem_ld_32x32b_x32(tbase + 128 + cc * 32, vb);
+        tmem_ld_wait();
+        uint32_t oa[16], ob[16], oh[16];
+        float hf[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            oa[i] = pack_bf16x2(__uint_as_float(va[2 * i]), __uint_as_float(va[2 * i + 1]));
+            ob[i] = pack_bf16x2(__uint_as_float(vb[2 * i]), __uint_as_float(vb[2 * i + 1]));
+            // h from the bf16-rounded a and b, so the backward recomputes it exactly
+            float a0 = bf16lo(oa[i]), a1 = bf16hi(oa[i]);
+            float b0 = bf16lo(ob[i]), b1 = bf16hi(ob[i]);
+            hf[2 * i] = silu_f(a0) * b0;
+            hf[2 * i + 1] = silu_f(a1) * b1;
+            oh[i] = pack_bf16x2(hf[2 * i], hf[2 * i + 1]);
+        }
+        const int col0 = ti.nt * 128 + cc * 32;
+        bf16 *ba = g.o0 + blk32_offset(brow, col0, g.F), *bb = g.o1 + blk32_offset(brow, col0, g.F);
+        if (tma_bf16) {
+            stage_store_blk<NBUF>(warp_stage, store_chunks, oa, ba, lane);
+            stage_store_blk<NBUF>(warp_stage, store_chunks, ob, bb, lane);
+            stage_store_bf16<NBUF>(warp_stage, store_chunks, oh, &g.om2, col0, brow + ring_shift, lane);
+        } else {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                st_v4(ba + (v * 32 + lane) * 8, make_uint4(oa[4 * v], oa[4 * v + 1], oa[4 * v + 2], oa[4 * v + 3]));
+                st_v4(bb + (v * 32 + lane) * 8, make_uint4(ob[4 * v], ob[4 * v + 1], ob[4 * v + 2], ob[4 * v + 3]));
+                if constexpr (!FP8)
+                    st_v4(ph + cc * 32 + v * 8, make_uint4(oh[4 * v], oh[4 * v + 1], oh[4 * v + 2], oh[4 * v + 3]));
+            }
+        }
+        if constexpr (FP8) {
+            // h quantised along F (blocks of 32) for GEMM2's A operand
+            uint32_t q[8];
+            const uint32_t sb = mx_quant32(hf, q);
+            const size_t hrow = (size_t)(grow + ring_shift);
+            const size_t col = (size_t)ti.nt * 128 + cc * 32;
+            uint4 *dq = reinterpret_cast<uint4 *>(g.q0 + hrow * F + col);
+            dq[0] = make_uint4(q[0], q[1], q[2], q[3]);
+            dq[1] = make_uint4(q[4], q[5], q[6], q[7]);
+            g.qs0[mx_sf_offset(hrow, col, F)] = (uint8_t)sb;
+        }
+    }
+}
+
+// Epilogue of one GEMM2 or GEMM1-dgrad tile: the fp32 accumulator row rounded to bf16 (GEMM2:
+// Y into the ring rows; GEMM1 dgrad: dX rows).
+template <int OP, int NBUF>
+__device__ __forceinline__ void epi_rows_tile(const GemmArgs &g, const TileInfo &ti, uint32_t tbase, int r,
+                                              int quarter, int lane, int ring_shift, bool tma_bf16,
+                                              uint8_t *warp_stage, int &store_chunks) {
+    const int grow = ti.g0 + r;
+    const size_t orow = (OP == OP_FWD2 && g.o_ring) ? (size_t)(grow + ring_shift) : (size_t)grow;
+    bf16 *py = g.o0 + orow * g.H + ti.nt * BN;
+#pragma unroll 1
+    for (int cc = 0; cc < BN / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tbase + cc * 32, v);
+        tmem_ld_wait();
+        uint32_t o[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        if (tma_bf16) {
+            const int row0 = (int)(orow - r) + quarter * 32;
+            stage_store_bf16<NBUF>(warp_stage, store_chunks, o, &g.om0, ti.nt * BN + cc * 32, row0, lane);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                st_v4(py + cc * 32 + q * 8, make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]));
+        }
+    }
+}
+
 // PAIR: the CTA pair computes a 256-row tile; this CTA's accumulator holds
 // rows [128 * rank, +128). A half beyond its expert's run (odd number of
 // 128-row tiles) is computed on whatever rows follow and not stored.
@@ -601,77 +690,9 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
         if (phantom) {
             // nothing to store for rows past the expert's run
         } else if constexpr (OP == OP_FWD1) {
-            const int grow = ti.g0 + r;
-            const size_t F = g.F;
-            const int brow = ti.g0 + quarter * 32;   // first row of this warp's 32-row blocks of a, b
-            bf16 *ph = FP8 ? nullptr : g.o2 + (size_t)(grow + ring_shift) * F + ti.nt * 128;
-#pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t va[32], vb[32];
-                tmem_ld_32x32b_x32(tbase + cc * 32, va);
-                tmem_ld_32x32b_x32(tbase + 128 + cc * 32, vb);
-                tmem_ld_wait();
-                uint32_t oa[16], ob[16], oh[16];
-                float hf[32];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    oa[i] = pack_bf16x2(__uint_as_float(va[2 * i]), __uint_as_float(va[2 * i + 1]));
-                    ob[i] = pack_bf16x2(__uint_as_float(vb[2 * i]), __uint_as_float(vb[2 * i + 1]));
-                    // h from the bf16-rounded a and b, so the backward recomputes it exactly
-                    float a0 = bf16lo(oa[i]), a1 = bf16hi(oa[i]);
-                    float b0 = bf16lo(ob[i]), b1 = bf16hi(ob[i]);
-                    hf[2 * i] = silu_f(a0) * b0;
-                    hf[2 * i + 1] = silu_f(a1) * b1;
-                    oh[i] = pack_bf16x2(hf[2 * i], hf[2 * i + 1]);
-                }
-                const int col0 = ti.nt * 128 + cc * 32;
-                bf16 *ba = g.o0 + blk32_offset(brow, col0, g.F), *bb = g.o1 + blk32_offset(brow, col0, g.F);
-                if (tma_bf16) {
-                    stage_store_blk<NBUF>(warp_stage, store_chunks, oa, ba, lane);
-                    stage_store_blk<NBUF>(warp_stage, store_chunks, ob, bb, lane);
-                    stage_store_bf16<NBUF>(warp_stage, store_chunks, oh, &g.om2, col0, brow + ring_shift, lane);
-                } else {
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        st_v4(ba + (v * 32 + lane) * 8, make_uint4(oa[4 * v], oa[4 * v + 1], oa[4 * v + 2], oa[4 * v + 3]));
-                        st_v4(bb + (v * 32 + lane) * 8, make_uint4(ob[4 * v], ob[4 * v + 1], ob[4 * v + 2], ob[4 * v + 3]));
-                        if constexpr (!FP8)
-                            st_v4(ph + cc * 32 + v * 8, make_uint4(oh[4 * v], oh[4 * v + 1], oh[4 * v + 2], oh[4 * v + 3]));
-                    }
-                }
-                if constexpr (FP8) {
-                    // h quantised along F (blocks of 32) for GEMM2's A operand
-                    uint32_t q[8];
-                    const uint32_t sb = mx_quant32(hf, q);
-                    const size_t hrow = (size_t)(grow + ring_shift);
-                    const size_t col = (size_t)ti.nt * 128 + cc * 32;
-                    uint4 *dq = reinterpret_cast<uint4 *>(g.q0 + hrow * F + col);
-                    dq[0] = make_uint4(q[0], q[1], q[2], q[3]);
-                    dq[1] = make_uint4(q[4], q[5], q[6], q[7]);
-                    g.qs0[mx_sf_offset(hrow, col, F)] = (uint8_t)sb;
-                }
-            }
+            epi_fwd1_tile<FP8, NBUF>(g, ti, tbase, r, quarter, lane, ring_shift, tma_bf16, warp_stage, store_chunks);
         } else if constexpr (OP == OP_FWD2 || OP == OP_BWD1) {
-            const int grow = ti.g0 + r;
-            const size_t orow = (OP == OP_FWD2 && g.o_ring) ? (size_t)(grow + ring_shift) : (size_t)grow;
-            bf16 *py = g.o0 + orow * g.H + ti.nt * BN;
-#pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tbase + cc * 32, v);
-                tmem_ld_wait();
-                uint32_t o[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) o[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                if (tma_bf16) {
-                    const int row0 = (int)(orow - r) + quarter * 32;
-                    stage_store_bf16<NBUF>(warp_stage, store_chunks, o, &g.om0, ti.nt * BN + cc * 32, row0, lane);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        st_v4(py + cc * 32 + q * 8, make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]));
-                }
-            }
+            epi_rows_tile<OP, NBUF>(g, ti, tbase, r, quarter, lane, ring_shift, tma_bf16, warp_stage, store_chunks);
         } else if constexpr (OP == OP_BWD2) {
             const int grow = ti.g0 + r;
             const size_t F = g.F;
@@ -899,11 +920,11 @@ __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_const
         epilogue_loop<OP, FP8, false, 8>(g, c, c.tfull, c.tempty, tmem, ctl, staging);   // warps 2-9
     } else if (warp < 6) {
         if constexpr (OP == OP_FWD1) {
-            if (g.fused) gather_loop<FP8>(g, &c.tfull[0]);   // until the first accumulator is ready
+            if (g.fused) gather_loop<FP8>(g, g.m, g.ready, &c.tfull[0]);   // until the first accumulator is ready
         }
         epilogue_loop<OP, FP8>(g, c, c.tfull, c.tempty, tmem, ctl, staging);
     } else {
-        if constexpr (OP == OP_FWD1) gather_loop<FP8>(g);
+        if constexpr (OP == OP_FWD1) gather_loop<FP8>(g, g.m, g.ready);
     }
     tc_fence_before();
     __syncthreads();
@@ -1095,11 +1116,11 @@ __global__ void __launch_bounds__(320, 1) pair_gemm_kernel(const __grid_constant
         if (lane == 0 && rank == 0) pair_mma_loop<OP>(g, c, tiles, tmem, ctl);
     } else if (warp < 6) {
         if constexpr (OP == OP_FWD1) {
-            if (g.fused) gather_loop<false>(g, &c.tfull[0]);   // until the first accumulator is ready
+            if (g.fused) gather_loop<false>(g, g.m, g.ready, &c.tfull[0]);   // until the first accumulator is ready
         }
         epilogue_loop<OP, false, true>(g, c, c.tfull, c.tempty, tmem, ctl, staging);
     } else {
-        if constexpr (OP == OP_FWD1) gather_loop<false>(g);
+        if constexpr (OP == OP_FWD1) gather_loop<false>(g, g.m, g.ready);
     }
     tc_fence_before();
     __syncthreads();
@@ -1371,11 +1392,11 @@ __global__ void __launch_bounds__(320, 1) pair8_gemm_kernel(const __grid_constan
         if (lane == 0 && rank == 0) pair8_mma_loop<OP>(g, c, tiles, tmem, ctl);
     } else if (warp < 6) {
         if constexpr (OP == OP_FWD1) {
-            if (g.fused) gather_loop<true>(g, &c.tfull[0]);   // until the first accumulator is ready
+            if (g.fused) gather_loop<true>(g, g.m, g.ready, &c.tfull[0]);   // until the first accumulator is ready
         }
         epilogue_loop<OP, true, true>(g, c, c.tfull, c.tempty, tmem, ctl, nullptr);
     } else {
-        if constexpr (OP == OP_FWD1) gather_loop<true>(g);
+        if constexpr (OP == OP_FWD1) gather_loop<true>(g, g.m, g.ready);
     }
     tc_fence_before();
     __syncthreads();
@@ -1435,6 +1456,427 @@ cudaError_t launch_any(int op, const GemmArgs &g, int grid, cudaStream_t stream)
     }
 }
 
+// ======================================================================
+// Persistent forward (MegaArgs): one launch of CTA pairs runs the fused dispatch, GEMM1 +
+// SwiGLU, GEMM2 and the combine of every macrobatch (article "O MoK do Cursor ...", section 02:
+// one persistent kernel per layer whose roles hand work on through GPU-side counters, the ring
+// refilled as soon as its readers are done; noticiai.com.br, "O que e": one deterministic
+// kernel). Roles per CTA: warp 0 TMA producer, warp 1 MMA issuer (leader CTA), warps 2-5
+// epilogue, warps 6-9 dispatch gather and combine. The pairs walk one tile list in order
+// (GEMM1 tiles of macrobatch m, then its GEMM2 tiles, then macrobatch m + 1), so GEMM2 tiles
+// fill GEMM1's last wave and the next macrobatch's tiles fill GEMM2's. Hand-offs (every wait
+// bounded; each waits only on list items earlier than its own, so every wait ends):
+//   GEMM1 tile <- its minibatch's rows gathered (ready counters of the fused dispatch)
+//   GEMM2 tile <- h of its 128-row block stored by all F/128 GEMM1 n-tiles (hready; every
+//                 epilogue warp publishes its own 32 rows, so no barrier joins the warps)
+//   gather of m  <- every GEMM1 tile of m - 1 has loaded its x rows (ring x reused; MXFP8)
+//   h of m       <- every GEMM2 tile of m - 1 has loaded its h rows (ring h reused)
+//   combine of m <- every GEMM2 tile of m has stored its Y rows (the last macrobatch's combine
+//                   runs in the combine kernel after this launch, on every warp of the GPU)
+//   Y of m       <- the combine of m - 1 has read every Y row (ring Y reused)
+// Arithmetic and rounding are those of the one-launch-per-stage forward, so out is the same bytes.
+
+constexpr int MEGA_OP_GEMM1 = 0, MEGA_OP_GEMM2 = 1;
+
+struct MegaTile {
+    int op, e, nt, m, g0, seg_end;
+};
+__device__ __forceinline__ MegaTile mega_tile(const MegaArgs &a, int t) {
+    const int4 v = a.tiles[t];
+    MegaTile mt;
+    mt.g0 = v.x;
+    mt.e = v.y & 255;
+    mt.nt = (v.y >> 8) & 0xFFFF;
+    mt.op = v.y >> 24;
+    mt.seg_end = v.z;
+    mt.m = v.w;
+    return mt;
+}
+
+template <bool FP8>
+__device__ void mega_producer(const MegaArgs &a, const CtlT<FP8 ? P8_STAGES : PSTAGES> &c, uint8_t *tiles,
+                              int total, const WaitCtl &ctl) {
+    constexpr int NS = FP8 ? P8_STAGES : PSTAGES;
+    constexpr uint32_t SS = FP8 ? P8_STAGE : P_STAGE;
+    const GemmArgs &g1 = a.g1, &g2 = a.g2;
+    const int rank = (int)cluster_ctarank();
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, last_phase = 0;
+    bool ok = true;
+    int ready_m = -1, ready_j = -1;
+    for (int t = blockIdx.x / 2; t < total && ok; t += gridDim.x / 2) {
+        const MegaTile mt = mega_tile(a, t);
+        const int row0 = mt.g0 + BM * rank;          // this CTA's 128 rows
+        const bool rows = row0 < mt.seg_end;         // not a half past the run
+        const int r0m = g1.offp[mt.m * g1.E];        // first padded row of the macrobatch
+        const int hrow = row0 - r0m;                 // ring row (one macrobatch in the ring)
+        const int xrow = g1.a_ring ? hrow : row0;    // bf16 keeps x rows at their padded rows
+        if (mt.op == MEGA_OP_GEMM1) {
+            if (rows) {
+                const int j = hrow / g1.mb_rows;
+                if (mt.m != ready_m || j != ready_j) {
+                    const int need = min(g1.mb_rows, g1.offp[(mt.m + 1) * g1.E] - r0m - j * g1.mb_rows);
+                    if (!flag_wait_geq(g1.ready + (size_t)mt.m * a.ready_stride + j, need, ctl)) { ok = false; break; }
+                    fence_proxy_async_global();
+                    ready_m = mt.m;
+                    ready_j = j;
+                }
+            }
+        } else if (rows) {
+            // four epilogue warps publish each of the F/128 GEMM1 n-tiles of the block
+            if (!flag_wait_geq(a.hready + row0 / BM, 4 * (g1.F / 128), ctl)) { ok = false; break; }
+            fence_proxy_async_global();
+        }
+        const int nk = mt.op == MEGA_OP_GEMM1 ? g1.K / bk_elems<FP8>() : g2.K / bk_elems<FP8>();
+        for (int kb = 0; kb < nk; ++kb) {
+            if (!mbar_wait(smem_u32(&c.empty[stage]), phase ^ 1, ctl)) { ok = false; break; }
+            const uint32_t bar = mapa_shared(smem_u32(&c.full[stage]), 0);   // the leader's full barrier
+            const uint32_t sA = smem_u32(tiles + stage * SS);
+            if constexpr (!FP8) {
+                const uint32_t sB = sA + P_A_BYTES;
+                mbar_arrive_expect_tx_cluster(bar, P_STAGE);
+                if (mt.op == MEGA_OP_GEMM1) {
+                    tma_load_2d_pair(sA, &g1.a0, bar, kb * BK, xrow);
+                    tma_load_3d_pair(sB, rank == 0 ? &g1.b0 : &g1.b1, bar, 0, mt.e * g1.H + kb * BK, mt.nt * 2);
+                } else {
+                    tma_load_2d_pair(sA, &g2.a0, bar, kb * BK, hrow);
+                    tma_load_3d_pair(sB, &g2.b0, bar, 0, mt.e * g2.F + kb * BK, (mt.nt * BN + 128 * rank) / 64);
+                }
+            } else {
+                const uint32_t sB = sA + P8_TILE, sSF = sB + P8_TILE;
+                mbar_arrive_expect_tx_cluster(bar, P8_TX);
+                const int k0 = kb * BK8;
+                if (mt.op == MEGA_OP_GEMM1) {
+                    const int br = mt.e * g1.F + mt.nt * 128, KS = g1.kstore;
+                    tma_load_2d_pair(sA, &g1.a0, bar, k0, xrow);
+                    tma_load_2d_pair(sB, rank == 0 ? &g1.b0 : &g1.b1, bar, k0, br);   // W1^T half, W3^T half
+                    tma_load_2d_pair(sSF, &g1.msa0, bar, 0, atom_row(xrow, k0, KS));
+                    tma_load_2d_pair(sSF + 512, &g1.msb0, bar, 0, atom_row(br, k0, KS));
+                    tma_load_2d_pair(sSF + 1024, &g1.msb1, bar, 0, atom_row(br, k0, KS));
+                } else {
+                    const int br = mt.e * g2.H + mt.nt * BN, KS = g2.kstore;
+                    tma_load_2d_pair(sA, &g2.a0, bar, k0, hrow);
+                    tma_load_2d_pair(sB, &g2.b0, bar, k0, br + 128 * rank);
+                    tma_load_2d_pair(sSF, &g2.msa0, bar, 0, atom_row(hrow, k0, KS));
+                    tma_load_2d_pair(sSF + 512, &g2.msb0, bar, 0, atom_row(br, k0, KS));
+                    tma_load_2d_pair(sSF + 1024, &g2.msb0, bar, 0, atom_row(br + 128, k0, KS));
+                }
+            }
+            issued |= 1u << stage;
+            last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+            if (++stage == NS) { stage = 0; phase ^= 1; }
+        }
+    }
+    if (!ok && rank == 0) {
+        // the leader's full barriers count both CTAs' copies: wait (bounded) for the last phases
+        for (int s = 0; s < NS; ++s) {
+            if (!((issued >> s) & 1u)) continue;
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(&c.full[s]), (last_phase >> s) & 1u) && globaltimer_ns() - t0 < ctl.budget_ns) {}
+        }
+    }
+}
+
+template <bool FP8>
+__device__ void mega_mma(const MegaArgs &a, CtlT<FP8 ? P8_STAGES : PSTAGES> &c, uint8_t *tiles, uint32_t tmem,
+                         int total, const WaitCtl &ctl) {
+    constexpr int NS = FP8 ? P8_STAGES : PSTAGES;
+    constexpr uint32_t SS = FP8 ? P8_STAGE : P_STAGE;
+    constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN, false, true);
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    for (int t = blockIdx.x / 2; t < total; t += gridDim.x / 2) {
+        const MegaTile mt = mega_tile(a, t);
+        const int nk = mt.op == MEGA_OP_GEMM1 ? a.g1.K / bk_elems<FP8>() : a.g2.K / bk_elems<FP8>();
+        if (!mbar_wait(smem_u32(&c.tempty[acc]), acc_phase ^ 1, ctl)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+            if (!mbar_wait(smem_u32(&c.full[stage]), phase, ctl)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sA = smem_u32(tiles + stage * SS);
+            if constexpr (!FP8) {
+                const uint32_t sB = sA + P_A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    mma_bf16_pair(d, sdesc_sw128(sA + kk * 32, 16, 1024), sdesc_sw128(sB + kk * 2048, 8192, 1024), idesc,
+                                  (kb | kk) != 0);
+            } else {
+                const uint32_t sB = sA + P8_TILE, sSF = sB + P8_TILE;
+                const uint32_t t_sf = tmem + 256 + 16 * stage;
+                tmem_cp_pair_32x128b_x4(t_sf, sdesc_plain(sSF, 0, 128));
+                tmem_cp_pair_32x128b_x4(t_sf + 8, sdesc_plain(sSF + 512, 0, 128));
+                tmem_cp_pair_32x128b_x4(t_sf + 12, sdesc_plain(sSF + 1024, 0, 128));
+#pragma unroll
+                for (int kk = 0; kk < BK8 / 32; ++kk)
+                    mma_mxf8_pair(tmem, sdesc_sw128(sA + kk * 32, 16, 1024), sdesc_sw128(sB + kk * 32, 16, 1024),
+                                  idesc_mxf8(2 * BM, BN, kk), t_sf, t_sf + 8, (kb | kk) != 0);
+            }
+            mma_commit_pair_mc(smem_u32(&c.empty[stage]));   // frees the stage in both CTAs
+            if (++stage == NS) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        // every copy of this tile has landed: its source rows in the ring may be overwritten
+        fence_proxy_async_global();
+        red_release_gpu_add(a.cnt + (size_t)mt.m * MEGA_NCNT + (mt.op == MEGA_OP_GEMM1 ? MEGA_G1_READ : MEGA_G2_READ), 1);
+        mma_commit_pair_mc(smem_u32(&c.tfull[acc]));
+        if constexpr (FP8) {
+            acc_phase ^= 1;                 // single accumulator (scale atoms in TMEM columns 256+)
+        } else {
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+    }
+    mma_commit_pair(smem_u32(&c.drain));
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(smem_u32(&c.drain), 0) && globaltimer_ns() - t0 < ctl.budget_ns) {}
+}
+
+template <bool FP8>
+__device__ void mega_epilogue(const MegaArgs &a, CtlT<FP8 ? P8_STAGES : PSTAGES> &c, uint32_t tmem, int total,
+                              const WaitCtl &ctl, uint8_t *staging) {
+    constexpr int NBUF = 4;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int quarter = warp & 3, r = quarter * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const int rank = (int)cluster_ctarank();
+    const GemmArgs &g1 = a.g1, &g2 = a.g2;
+    int acc = 0, store_chunks = 0;
+    uint32_t acc_phase = 0;
+    uint8_t *warp_stage = staging ? staging + (warp - 2) * (NBUF * 2048) : nullptr;
+    int h_free = 0, y_free = 0;   // macrobatches whose ring h / Y rows may be written
+    // A tile's rows are published one tile late: after the next tile's stores are issued, lane
+    // 0 waits only for the older bulk groups, whose writes have had a tile's time to land. A
+    // pending publication is flushed before any wait that could block, so no wait of this
+    // warp ever depends on a publication it still holds.
+    int *pending = nullptr;
+    auto flush = [&]() {
+        if (pending == nullptr) return;
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+            bulk_wait_group_all();
+            fence_proxy_async_global();
+            __threadfence();
+            red_release_gpu_add(pending, 1);
+        }
+        __syncwarp();
+        pending = nullptr;
+    };
+    for (int t = blockIdx.x / 2; t < total; t += gridDim.x / 2) {
+        const MegaTile mt = mega_tile(a, t);
+        TileInfo ti;
+        ti.e = mt.e; ti.nt = mt.nt; ti.mt = 0; ti.nk = 0;
+        ti.g0 = mt.g0 + BM * rank;
+        ti.seg_end = mt.seg_end;
+        const bool rows = ti.g0 < ti.seg_end;
+        const int ring_shift = -g1.offp[mt.m * g1.E];
+        // the ring rows this tile writes must be done with by the previous macrobatch's readers
+        if (mt.op == MEGA_OP_GEMM1 && mt.m > h_free) {
+            flush();
+            const int p = mt.m - 1;
+            if (!flag_wait_geq(a.cnt + (size_t)p * MEGA_NCNT + MEGA_G2_READ, a.meta[p * 4 + 1], ctl)) break;
+            h_free = mt.m;
+        }
+        if (mt.op == MEGA_OP_GEMM2 && mt.m > y_free) {
+            flush();
+            const int p = mt.m - 1;
+            if (!flag_wait_geq(a.cnt + (size_t)p * MEGA_NCNT + MEGA_COMBINED, a.meta[p * 4 + 3], ctl)) break;
+            y_free = mt.m;
+        }
+        if (!mbar_try_wait(smem_u32(&c.tfull[acc]), acc_phase)) flush();   // about to wait: publish first
+        if (!mbar_wait(smem_u32(&c.tfull[acc]), acc_phase, ctl)) break;
+        tc_fence_after();
+        const uint32_t tbase = tmem + lane_base + acc * BN;
+        if (rows) {
+            if (mt.op == MEGA_OP_GEMM1)
+                epi_fwd1_tile<FP8, NBUF>(g1, ti, tbase, r, quarter, lane, ring_shift, !FP8 && g1.tma_store, warp_stage,
+                                         store_chunks);
+            else
+                epi_rows_tile<OP_FWD2, NBUF>(g2, ti, tbase, r, quarter, lane, ring_shift, !FP8 && g2.tma_store,
+                                             warp_stage, store_chunks);
+        }
+        tc_fence_before();
+        mbar_arrive_cluster(mapa_shared(smem_u32(&c.tempty[acc]), 0));   // the leader's MMA thread waits for both CTAs
+        // publish the previous tile's rows (its bulk groups are older than this tile's: wait for
+        // all but this tile's), then hold this tile's. Each warp publishes its own 32 rows (it
+        // writes no other), so no barrier joins the warps; the counters' targets count four per tile.
+        if (pending != nullptr) {
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) {
+                if (!rows) bulk_wait_group_all();
+                else if (FP8) bulk_wait_group_all();                                    // no bulk stores
+                else if (mt.op == MEGA_OP_GEMM1) bulk_wait_group<12>();                 // a, b, h x 4 chunks
+                else bulk_wait_group<BN / 32>();                                        // Y: 8 chunks
+                fence_proxy_async_global();
+                __threadfence();
+                red_release_gpu_add(pending, 1);
+            }
+            __syncwarp();
+            pending = nullptr;
+        }
+        if (rows)
+            pending = mt.op == MEGA_OP_GEMM1 ? a.hready + ti.g0 / BM : a.cnt + (size_t)mt.m * MEGA_NCNT + MEGA_Y_DONE;
+        if constexpr (FP8) {
+            acc_phase ^= 1;
+        } else {
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+    }
+    flush();
+    if (store_chunks > 0 && lane == 0) bulk_wait_group_all();
+}
+
+// warps 6-9: gather macrobatch m, then combine macrobatch m - 1 while later macrobatches run.
+// The last macrobatch's combine has nothing left to overlap with: the combine kernel that
+// follows this launch does it with every warp of the GPU.
+template <bool FP8>
+__device__ void mega_gather_combine(const MegaArgs &a, const WaitCtl &ctl) {
+    const GemmArgs &g1 = a.g1;
+    const int lane = threadIdx.x % 32;
+    const int gw = blockIdx.x * 4 + (threadIdx.x / 32 - 6), nw = gridDim.x * 4;
+    CombineArgs ca{};
+    ca.Y = a.g2.o0; ca.slot_row = a.slot_row; ca.offp = g1.offp; ca.w = a.w; ca.out = a.out;
+    ca.k = g1.k; ca.H = g1.H; ca.E = g1.E; ca.ring_base = 0;
+    const int nch = (g1.H / 8 + 63) / 64;
+    for (int m = 0; m < g1.nM; ++m) {
+        {
+            // ring x rows free: every GEMM1 tile of m - 1 has loaded its rows (bf16 keeps the
+            // x rows at their own padded rows in the saved context: nothing is reused)
+            if (m > 0 && g1.a_ring &&
+                !flag_wait_geq(a.cnt + (size_t)(m - 1) * MEGA_NCNT + MEGA_G1_READ, a.meta[(m - 1) * 4 + 0], ctl))
+                return;
+            gather_loop<FP8>(g1, m, g1.ready + (size_t)m * a.ready_stride);
+        }
+        if (m > 0 && m < g1.nM) {
+            const int p = m - 1;
+            if (!flag_wait_geq(a.cnt + (size_t)p * MEGA_NCNT + MEGA_Y_DONE, a.meta[p * 4 + 2], ctl)) return;
+            ca.t0 = p * a.Mb;
+            ca.t1 = min(a.T, ca.t0 + a.Mb);
+            ca.m = p;
+            const int shift = -g1.offp[p * g1.E];
+            const int items = a.meta[p * 4 + 3];
+            (void)gw; (void)nw;
+            for (;;) {
+                int it = 0;
+                if (lane == 0) it = atomicAdd(a.cnt + (size_t)p * MEGA_NCNT + MEGA_COMBINE_CLAIM, 1);
+                it = __shfl_sync(0xffffffffu, it, 0);
+                if (it >= items) break;
+                combine_item(ca, it, nch, shift, lane);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) red_release_gpu_add(a.cnt + (size_t)p * MEGA_NCNT + MEGA_COMBINED, 1);
+            }
+        }
+    }
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(320, 1) fwd_mega_kernel(const __grid_constant__ MegaArgs a) {
+    using Ctl = CtlT<FP8 ? P8_STAGES : PSTAGES>;
+    constexpr int NS = FP8 ? P8_STAGES : PSTAGES;
+    constexpr uint32_t SS = FP8 ? P8_STAGE : P_STAGE;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *staging = FP8 ? nullptr : tiles + NS * SS;
+    Ctl &c = *reinterpret_cast<Ctl *>(tiles + NS * SS + (FP8 ? 0 : P_STAGING));
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    WaitCtl ctl{a.g1.status, a.g1.budget_ns};
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(smem_u32(&c.full[s]), 2);      // one arrive.expect_tx per CTA of the pair
+            mbar_init(smem_u32(&c.empty[s]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&c.tfull[i]), 1);
+            mbar_init(smem_u32(&c.tempty[i]), 256);  // 128 epilogue threads of each CTA
+        }
+        mbar_init(smem_u32(&c.drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&a.g1.a0);
+        tma_prefetch_map(&a.g1.b0);
+        tma_prefetch_map(&a.g2.a0);
+        tma_prefetch_map(&a.g2.b0);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(&c.tmem_base), 512);
+        tmem_relinquish_pair();
+    }
+    pdl_wait();   // the schedule, the tile list and the zeroed counters are in place
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();      // the peer's barriers are initialised before any remote arrive
+    tc_fence_after();
+    pdl_trigger();
+    const uint32_t tmem = c.tmem_base;
+    const int total = *a.tile_count;
+    if (warp == 0) {
+        if (lane == 0) mega_producer<FP8>(a, c, tiles, total, ctl);
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) mega_mma<FP8>(a, c, tiles, tmem, total, ctl);
+    } else if (warp < 6) {
+        // the epilogue warps gather the first macrobatch too, until their first accumulator is ready
+        gather_loop<FP8>(a.g1, 0, a.g1.ready, &c.tfull[0]);
+        mega_epilogue<FP8>(a, c, tmem, total, ctl, staging);
+    } else {
+        mega_gather_combine<FP8>(a, ctl);
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();      // the leader's MMAs are drained before the pair frees TMEM
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem, 512);
+}
+
+// One block per macrobatch m, one thread per expert: the pair m-tiles of every earlier
+// macrobatch place m's entries; GEMM1 tiles (expert-major, m-tile, n-tile), then GEMM2 tiles.
+__global__ void __launch_bounds__(64) mega_list_kernel(const int *offp, int E, int nM, int nt1, int nt2, int T,
+                                                       int Mb, int nch, int4 *list, int *meta, int *count) {
+    pdl_wait();
+    __shared__ int s_n[64], s_before[64];
+    const int m = blockIdx.x, e = threadIdx.x;
+    int before = 0, s0 = 0, s1 = 0;
+    if (e < E) {
+        for (int mm = 0; mm < m; ++mm) before += (offp[mm * E + e + 1] - offp[mm * E + e] + 255) / 256;
+        s0 = offp[m * E + e];
+        s1 = offp[m * E + e + 1];
+    }
+    const int nmt = (s1 - s0 + 255) / 256;
+    s_n[e] = nmt;
+    s_before[e] = before;
+    __syncthreads();
+    int pref = 0, total_mt = 0, total_before = 0;
+    for (int i = 0; i < E; ++i) {
+        if (i < e) pref += s_n[i];
+        total_mt += s_n[i];
+        total_before += s_before[i];
+    }
+    const int base = total_before * (nt1 + nt2);
+    const int base2 = base + total_mt * nt1;
+    if (e < E) {
+        for (int mt = 0; mt < nmt; ++mt) {
+            for (int nt = 0; nt < nt1; ++nt)
+                list[base + (pref + mt) * nt1 + nt] = make_int4(s0 + 256 * mt, e | (nt << 8) | (MEGA_OP_GEMM1 << 24), s1, m);
+            for (int nt = 0; nt < nt2; ++nt)
+                list[base2 + (pref + mt) * nt2 + nt] = make_int4(s0 + 256 * mt, e | (nt << 8) | (MEGA_OP_GEMM2 << 24), s1, m);
+        }
+    }
+    if (e == 0) {
+        meta[m * 4 + 0] = total_mt * nt1;
+        meta[m * 4 + 1] = total_mt * nt2;
+        meta[m * 4 + 2] = (offp[(m + 1) * E] - offp[m * E]) / 128 * nt2 * 4;   // one per epilogue warp
+        const int t0 = m * Mb, t1 = min(T, t0 + Mb);
+        meta[m * 4 + 3] = (t1 - t0) * nch;
+        if (m == nM - 1) *count = base + total_mt * (nt1 + nt2);
+    }
+}
+
 // One warp per list: warp 0 writes 128-row tiles, warp 1 256-row tiles. Runs are taken
 // 32 at a time in expert-major order (run i = expert i / nM, macrobatch i % nM); a warp
 // scan of their tile counts places each lane's tiles after those of the runs before it.
@@ -1470,6 +1912,45 @@ __global__ void __launch_bounds__(64) tile_list_kernel(const int *offp, int E, i
 }
 
 }  // namespace
+
+cudaError_t launch_mega_list(const int *offp, int E, int nM, int F, int H, int T, int Mb, int4 *list, int *meta,
+                             int *count, cudaStream_t stream) {
+    return launch_pdl(mega_list_kernel, dim3(nM), dim3(64), 0, stream, offp, E, nM, F / 128, H / BN, T, Mb,
+                      (H / 8 + 63) / 64, list, meta, count);
+}
+
+template <bool FP8>
+cudaError_t launch_mega_t(const MegaArgs &a, int grid, cudaStream_t stream) {
+    constexpr size_t smem = FP8 ? P8_STAGES * P8_STAGE + sizeof(Pair8Ctl) + 1024
+                                : PSTAGES * P_STAGE + P_STAGING + sizeof(PairCtl) + 1024;
+    static_assert(smem <= 227 * 1024, "shared memory budget");
+    static_assert(sizeof(MegaArgs) <= 32764, "kernel parameter space");
+    cudaError_t err = cudaFuncSetAttribute(fwd_mega_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg{};
+    cfg.blockDim = dim3(320);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    // every CTA waits on others' progress: the grid must be fully co-resident
+    static std::atomic<int> max_clusters[kMaxCachedDevices][2];
+    cfg.gridDim = dim3(grid / 2 * 2);
+    const int mc = cached_max_clusters(max_clusters, 0, fwd_mega_kernel<FP8>, cfg, grid / 2);
+    cfg.gridDim = dim3(2 * std::min(grid / 2, mc));
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, fwd_mega_kernel<FP8>, a);
+}
+
+cudaError_t launch_fwd_mega(const MegaArgs &a, int grid, cudaStream_t stream, bool fp8) {
+    return fp8 ? launch_mega_t<true>(a, grid, stream) : launch_mega_t<false>(a, grid, stream);
+}
 
 cudaError_t launch_tile_lists(const int *offp, int E, int nM, int4 *list128, int4 *list256, int *counts,
                               cudaStream_t stream) {

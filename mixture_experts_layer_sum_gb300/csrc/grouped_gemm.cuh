@@ -67,6 +67,34 @@ struct GemmArgs {
 cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream, bool fp8 = false,
                                 bool pair = false);
 
+// Persistent forward over every macrobatch (one launch of CTA pairs): the fused dispatch
+// (gather warps), GEMM1 + SwiGLU and GEMM2 tiles, and the combine, handed on by device
+// counters. Tiles come from a device-built list, macrobatch by macrobatch: GEMM1 tiles of m
+// (expert, pair m-tile, n-tile), then GEMM2 tiles of m. One macrobatch is in the ring (h, Y
+// rows; x rows too in MXFP8), so a tile that writes ring rows of m waits until the readers of
+// m - 1 are done with them.
+enum MegaCounter { MEGA_G1_READ = 0, MEGA_G2_READ, MEGA_Y_DONE, MEGA_COMBINED, MEGA_COMBINE_CLAIM, MEGA_NCNT = 8 };
+struct MegaArgs {
+    GemmArgs g1, g2;              // GEMM1 (fused dispatch) and GEMM2 of the forward (their m is unused)
+    const int4 *tiles;            // (first padded row, expert | n-tile << 8 | op << 24, run end, macrobatch)
+    const int *tile_count;        // [0]: tiles in the list
+    const int *meta;              // [nM][4]: GEMM1 pair tiles, GEMM2 pair tiles, 4 x GEMM2 CTA tiles
+                                  //          with rows (one per epilogue warp), combine items
+    // hready: per 128-row block, one count per epilogue warp and GEMM1 n-tile (4 F / 128 when full)
+    int *cnt;                     // [nM][MEGA_NCNT] counters (zeroed before the launch)
+    int *hready;                  // [padded rows / 128]: GEMM1 n-tiles that stored h of the block
+    const int32_t *slot_row;      // combine: padded row of each slot
+    const float *w;               // combine: router weights [T, k]
+    bf16 *out;                    // [T, H]
+    int T, Mb, ready_stride;      // tokens, macrobatch tokens, ready ints per macrobatch
+};
+
+// Builds the persistent forward's tile list and per-macrobatch counts (one block per
+// macrobatch). Entries: at most (rows_pad_max / 256 + nM * E) * (F / 128 + H / 256).
+cudaError_t launch_mega_list(const int *offp, int E, int nM, int F, int H, int T, int Mb, int4 *list, int *meta,
+                             int *count, cudaStream_t stream);
+cudaError_t launch_fwd_mega(const MegaArgs &a, int grid, cudaStream_t stream, bool fp8);
+
 // Writes the M-tile lists of every (macrobatch, expert) run of padded rows, expert-major:
 // list128 with 128-row tiles (1-CTA kernels), list256 with 256-row tiles (CTA pairs; a
 // tile's second half may lie past its run). counts[0], counts[1] = their lengths. Each list

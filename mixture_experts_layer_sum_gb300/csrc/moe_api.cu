@@ -87,6 +87,8 @@ moe_status_t check_shape(const moe_config_t *c) {
     if (c->precision != MOE_PRECISION_BF16 && c->precision != MOE_PRECISION_MXFP8)
         return fail(MOE_ERR_INVALID_ARG, "unknown precision");
     if (c->minibatch_rows < 0 || c->macrobatch_tokens < 0) return fail(MOE_ERR_INVALID_ARG, "negative minibatch/macrobatch");
+    if (c->forward_mode != MOE_FORWARD_PERSISTENT && c->forward_mode != MOE_FORWARD_PER_STAGE)
+        return fail(MOE_ERR_INVALID_ARG, "unknown forward mode");
     const long long R = (long long)c->T * c->k;
     if (R > (1LL << 30) / 2) return fail(MOE_ERR_UNSUPPORTED, "T*k too large");
     return MOE_OK;
@@ -189,6 +191,16 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     L.w_tiles256 = take(16 * (size_t)L.tile_list_max);
     L.w_tile_counts = take(2 * 4);
     L.w_decode = take(4 * (1 + (size_t)L.E));
+    // persistent forward: tile list, per-macrobatch counts, counters zeroed per call (the
+    // per-macrobatch counters and the per-128-row-block h counters, one contiguous range)
+    L.mega_list_max = ((size_t)L.rows_pad_max / 256 + (size_t)L.nM * L.E) * ((size_t)L.F / 128 + (size_t)L.H / 256);
+    L.w_mega_list = take(16 * L.mega_list_max);
+    L.w_mega_meta = take(16 * (size_t)L.nM);
+    L.w_mega_count = take(4);
+    L.w_mega_cnt = o;
+    L.mega_zero_bytes = 4 * ((size_t)L.nM * MEGA_NCNT + (size_t)L.rows_pad_max / kRowPad);
+    L.w_mega_hready = L.w_mega_cnt + 4 * (size_t)L.nM * MEGA_NCNT;
+    take(L.mega_zero_bytes);
     // few bf16 tokens in one macrobatch: every expert holds at most T <= 128 rows, and the
     // forward streams each expert's weights once through the decode kernel
     L.decode = kDecodePath && !mx && c->T > 0 && c->T <= kDecodeMaxTokens && L.nM == 1;
@@ -734,7 +746,7 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
         return cuda_check(launch_combine(ca, L.num_sms, s), "combine launch");
     }
 
-    // 3. per macrobatch: dispatch -> GEMM1+SwiGLU -> GEMM2 -> combine
+    // 3. dispatch -> GEMM1+SwiGLU -> GEMM2 -> combine: one persistent launch, or per macrobatch
     bf16 *ringX = L.keep_x ? at<bf16>(saved, L.s_xs) : at<bf16>(ws, L.w_ringX);
     bf16 *ringH = at<bf16>(ws, L.w_ringH), *ringY = at<bf16>(ws, L.w_ringY);
     uint8_t *ringXq = at<uint8_t>(ws, L.w_ringX), *ringHq = at<uint8_t>(ws, L.w_ringH);
@@ -787,6 +799,38 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
     g1.ready_slots = L.half_rows / kRowPad + 1;
     if (!mx) g1.ringx = ringX;
     else { g1.ringxq = ringXq; g1.ringxs = ringXs; }
+    if (cfg->forward_mode == MOE_FORWARD_PERSISTENT && L.T > 0) {
+        MegaArgs ma;
+        std::memset(&ma, 0, sizeof(ma));
+        g1.ready = ready; g1.m = 0; g1.ring_base = 0;
+        g2.m = 0; g2.ring_base = 0;
+        ma.g1 = g1; ma.g2 = g2;
+        int4 *list = at<int4>(ws, L.w_mega_list);
+        int *meta = at<int>(ws, L.w_mega_meta), *count = at<int>(ws, L.w_mega_count);
+        ma.tiles = list; ma.tile_count = count; ma.meta = meta;
+        ma.cnt = at<int>(ws, L.w_mega_cnt); ma.hready = at<int>(ws, L.w_mega_hready);
+        ma.slot_row = s_slot_row; ma.w = s_w; ma.out = (bf16 *)out;
+        ma.T = L.T; ma.Mb = L.Mb; ma.ready_stride = ready_stride;
+        st = cuda_check(cudaMemsetAsync(ma.cnt, 0, L.mega_zero_bytes, s), "persistent forward counters clear");
+        if (st != MOE_OK) return st;
+        {
+            ProfScope ps("forward_tile_list", s);
+            st = cuda_check(launch_mega_list(s_offp, L.E, L.nM, L.F, L.H, L.T, L.Mb, list, meta, count, s),
+                            "tile list launch");
+        }
+        if (st != MOE_OK) return st;
+        {
+            ProfScope ps("forward_persistent", s);
+            st = cuda_check(launch_fwd_mega(ma, L.num_sms, s, mx), "persistent forward launch");
+        }
+        if (st != MOE_OK) return st;
+        // the last macrobatch's combine: nothing left to overlap with, so it gets the whole GPU
+        CombineArgs ca{};
+        ca.Y = ringY; ca.slot_row = s_slot_row; ca.offp = s_offp; ca.w = s_w; ca.out = (bf16 *)out;
+        ca.t0 = (L.nM - 1) * L.Mb; ca.t1 = L.T; ca.k = L.k; ca.H = L.H; ca.E = L.E; ca.m = L.nM - 1; ca.ring_base = 0;
+        ProfScope ps("combine", s);
+        return cuda_check(launch_combine(ca, L.num_sms, s), "combine launch");
+    }
     for (int m = 0; m < L.nM; ++m) {
         const int ring_base = (m % L.ring_halves) * L.half_rows;
         g1.ready = ready + (size_t)m * ready_stride;   // zeroed by the schedule scan

@@ -51,6 +51,8 @@ struct Layout {
     size_t w_status, w_chunk_counts, w_chunk_base, w_wrt, w_offp, w_ready;
     size_t w_tiles128, w_tiles256, w_tile_counts;   // backward M-tile lists (several macrobatches)
     size_t w_decode;        // decode forward: work-item counter + per-expert h counters
+    size_t w_mega_list, w_mega_meta, w_mega_count, w_mega_cnt, w_mega_hready;   // persistent forward
+    size_t mega_list_max, mega_zero_bytes;   // list entries; bytes of counters zeroed per call
     bool decode;            // bf16 forward of few tokens through the decode kernel
     int tile_list_max;                              // entries each list can hold
     int mb_rows;            // minibatch rows used by the fused dispatch (multiple of 128)

@@ -14,6 +14,7 @@
 //   reverse_dispatch dx = sum_j dX rows (fixed order) + dlogits W_r^T
 //   router_wgrad     dW_r = x^T dlogits with fixed-order split reduction
 #include "route_kernels.cuh"
+#include "combine_item.cuh"
 
 namespace moe {
 
@@ -573,53 +574,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     const int nch = (vecs + 63) / 64;
     const int items = (a.t1 - a.t0) * nch;
     for (int it = gw; it < items; it += nw) {
-        const int t = a.t0 + it / nch;
-        // two vectors per lane, rows in batches of 4: 8 loads of 16 B per lane in flight
-        {
-            const int v0 = (it % nch) * 64 + lane;
-            const bool two = v0 + 32 < vecs;
-            float acc[2][8];
-#pragma unroll
-            for (int p = 0; p < 2; ++p)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[p][i] = 0.0f;
-            for (int j0 = 0; j0 < a.k; j0 += 4) {
-                const int nj = min(4, a.k - j0);
-                int rows[4];
-                float ws[4];
-                uint4 y[2][4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (j < nj) {
-                        rows[j] = a.slot_row[(size_t)t * a.k + j0 + j] + shift;
-                        ws[j] = a.w[(size_t)t * a.k + j0 + j];
-                    }
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (j < nj) {
-                        y[0][j] = ld_v4(a.Y + (size_t)rows[j] * a.H + v0 * 8);
-                        if (two) y[1][j] = ld_v4(a.Y + (size_t)rows[j] * a.H + (v0 + 32) * 8);
-                    }
-#pragma unroll
-                for (int p = 0; p < 2; ++p)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (j < nj && (p == 0 || two)) {
-                            const uint32_t q[4] = {y[p][j].x, y[p][j].y, y[p][j].z, y[p][j].w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                acc[p][2 * i] = fmaf(ws[j], bf16lo(q[i]), acc[p][2 * i]);
-                                acc[p][2 * i + 1] = fmaf(ws[j], bf16hi(q[i]), acc[p][2 * i + 1]);
-                            }
-                        }
-            }
-#pragma unroll
-            for (int p = 0; p < 2; ++p)
-                if (p == 0 || two)
-                    st_v4(a.out + (size_t)t * a.H + (v0 + 32 * p) * 8,
-                          make_uint4(pack_bf16x2(acc[p][0], acc[p][1]), pack_bf16x2(acc[p][2], acc[p][3]),
-                                     pack_bf16x2(acc[p][4], acc[p][5]), pack_bf16x2(acc[p][6], acc[p][7])));
-        }
+        combine_item(a, it, nch, shift, lane);
     }
 }
 

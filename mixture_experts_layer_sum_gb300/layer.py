@@ -13,11 +13,11 @@ from . import moe as _m
 
 class MoeLayer:
     def __init__(self, T, H, F, E, k, precision="bf16", *, device="cuda", ring_bytes=0, macrobatch_tokens=0,
-                 minibatch_rows=0, timeout_ms=0, fault_mask=0):
+                 minibatch_rows=0, timeout_ms=0, fault_mask=0, forward_mode=0):
         self.shape = dict(T=T, H=H, F=F, E=E, k=k)
         self.device = torch.device(device)
         self.cfg = _m.make_config(T, H, F, E, k, precision, minibatch_rows, macrobatch_tokens, ring_bytes,
-                                  timeout_ms, 0, fault_mask)
+                                  timeout_ms, 0, fault_mask, forward_mode)
         self.plan = _m.moe_plan(self.cfg)
         self.workspace = torch.empty(self.plan.workspace_bytes, dtype=torch.uint8, device=self.device)
         self.saved = torch.empty(self.plan.saved_bytes, dtype=torch.uint8, device=self.device)

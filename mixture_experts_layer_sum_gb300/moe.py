@@ -22,6 +22,8 @@ MOE_ERR_INTERNAL = 6
 MOE_FAULT_GEMM1_READY = 1   # config fault_mask bit (failure-detection tests)
 MOE_PRECISION_BF16 = 0
 MOE_PRECISION_MXFP8 = 1
+MOE_FORWARD_PERSISTENT = 0
+MOE_FORWARD_PER_STAGE = 1
 
 EXPORTED = (
     "moe_abi_version", "moe_plan", "moe_workspace_size", "moe_saved_size", "moe_qweights_size",
@@ -48,7 +50,8 @@ class moe_config_t(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("F", ctypes.c_int), ("E", ctypes.c_int),
                 ("k", ctypes.c_int), ("precision", ctypes.c_int), ("minibatch_rows", ctypes.c_int),
                 ("macrobatch_tokens", ctypes.c_int), ("ring_bytes", ctypes.c_size_t),
-                ("timeout_ms", ctypes.c_uint), ("num_sms", ctypes.c_int), ("fault_mask", ctypes.c_uint)]
+                ("timeout_ms", ctypes.c_uint), ("num_sms", ctypes.c_int), ("fault_mask", ctypes.c_uint),
+                ("forward_mode", ctypes.c_int)]
 
 
 class moe_kernel_time_t(ctypes.Structure):
@@ -64,10 +67,10 @@ class moe_plan_t(ctypes.Structure):
 
 
 def make_config(T, H, F, E, k, precision="bf16", minibatch_rows=0, macrobatch_tokens=0, ring_bytes=0,
-                timeout_ms=0, num_sms=0, fault_mask=0) -> moe_config_t:
+                timeout_ms=0, num_sms=0, fault_mask=0, forward_mode=0) -> moe_config_t:
     p = {"bf16": MOE_PRECISION_BF16, "mxfp8": MOE_PRECISION_MXFP8}.get(precision, precision)
     return moe_config_t(T, H, F, E, k, p, minibatch_rows, macrobatch_tokens, ring_bytes, timeout_ms, num_sms,
-                        fault_mask)
+                        fault_mask, forward_mode)
 
 
 def _load():

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(moe):
 
 
 def test_abi_version(moe):
-    assert moe.moe_abi_version() == 2
+    assert moe.moe_abi_version() == 3
 
 
 def test_minibatch_floor_matches_pages_golden(moe):

@@ -23,14 +23,16 @@ def built():
     assert torch.cuda.is_available()
 
 
-def test_gemm1_wait_runs_out_and_context_survives():
+@pytest.mark.parametrize("mode", [0, 1])   # the persistent forward, one launch per stage
+def test_gemm1_wait_runs_out_and_context_survives(mode):
     import mixture_experts_layer_sum_gb300.moe as M
     from mixture_experts_layer_sum_gb300.layer import MoeLayer
     import tests.gpu_common as G
     w = WL.TINY
     inp = WL.make_inputs(w)
     d = G.device_inputs(inp)
-    layer = MoeLayer(w.T, w.H, w.F, w.E, w.k, timeout_ms=100, fault_mask=M.MOE_FAULT_GEMM1_READY)
+    layer = MoeLayer(w.T, w.H, w.F, w.E, w.k, timeout_ms=100, fault_mask=M.MOE_FAULT_GEMM1_READY,
+                     forward_mode=mode)
     assert layer.plan.num_macrobatches == 1 and layer.plan.minibatch_rows >= w.T * w.k   # one minibatch
     t0 = time.time()
     layer.forward(d["x"], d["Wr"], d["bias"], d["W1"], d["W3"], d["W2"])
