@@ -164,6 +164,89 @@ def mx_roundtrip_segments(v: np.ndarray, seg_starts, seg_ends) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
+# NVFP4 expert weights. [NI] "Por que a camada MoE virou o gargalo" names Cursor's
+# earlier NVFP4 kernels and its "warp decode" inference path and nothing more; the format
+# taken here is the plain NVFP4 one: E2M1 elements (1 sign, 2 exponent bits with bias 1,
+# 1 mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), one E4M3 scale per 16 consecutive
+# elements along the contraction axis, and one FP32 scale per weight matrix. Reading: that
+# matrix scale is the smallest power of two g with amax <= 448 * 6 * g (every block scale
+# then fits E4M3, and a dequantised value e2m1 * scale * g has at most 7 significant bits,
+# exact in bf16); a block scale is the E4M3 value nearest to amax_block / (6 g), and an
+# element is the E2M1 value nearest (ties to even) to v / (scale * g), saturating at 6; a
+# block whose scale rounds to 0 holds zeros.
+
+E2M1_MAX = 6.0
+NV_BLOCK = 16
+
+
+def e2m1_round(v: np.ndarray) -> np.ndarray:
+    """Nearest E2M1 value (ties to the even mantissa), saturating at +-6."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    # spacing of E2M1 values: 0.5 below 2 (the subnormal and first normal binades), 1 in
+    # [2, 4), 2 in [4, 8)
+    quantum = np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))
+    q = np.minimum(np.round(a / quantum) * quantum, E2M1_MAX)   # np.round: half to even
+    return np.copysign(q, v)
+
+
+E2M1_MAGNITUDES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])   # codes 0..7
+
+
+def e2m1_encode(q: np.ndarray) -> np.ndarray:
+    """Exact E2M1 values -> 4-bit codes: sign << 3 | exponent << 1 | mantissa, i.e. the
+    index of the magnitude in E2M1_MAGNITUDES plus 8 for a negative sign."""
+    q = np.asarray(q, dtype=np.float64)
+    a = np.abs(q)
+    idx = np.searchsorted(E2M1_MAGNITUDES, a)
+    assert (E2M1_MAGNITUDES[np.minimum(idx, 7)] == a).all(), "not an E2M1 value"
+    return (idx.astype(np.uint8) | (np.signbit(q).astype(np.uint8) << 3)).astype(np.uint8)
+
+
+def e2m1_decode(code: np.ndarray) -> np.ndarray:
+    c = np.asarray(code, dtype=np.uint8)
+    e, m = (c >> 1) & 3, c & 1
+    mag = np.where(e == 0, 0.5 * m, (1.0 + 0.5 * m) * np.exp2(e.astype(np.float64) - 1.0))
+    return np.where(c & 8, -mag, mag)
+
+
+def nv_matrix_scale(amax: float) -> float:
+    """Smallest power of two g with amax <= 448 * 6 * g (1 for an all-zero matrix)."""
+    if amax <= 0:
+        return 1.0
+    mant, ex = math.frexp(amax / (E4M3_MAX * E2M1_MAX))    # x = mant * 2^ex, mant in [0.5, 1)
+    return math.ldexp(1.0, ex - 1) if mant == 0.5 else math.ldexp(1.0, ex)
+
+
+def nv_quantize(v: np.ndarray, axis: int):
+    """NVFP4 quantisation of one matrix along `axis` (length a multiple of 16). Returns
+    (E2M1 codes, one per element, same shape; E4M3 scale bytes with the axis shortened
+    16-fold; the matrix scale g)."""
+    v = np.moveaxis(np.asarray(v, dtype=np.float64), axis, -1)
+    n = v.shape[-1]
+    assert n % NV_BLOCK == 0, "NVFP4 blocks need a multiple of 16 elements"
+    g = nv_matrix_scale(float(np.abs(v).max()) if v.size else 0.0)
+    blk = v.reshape(v.shape[:-1] + (n // NV_BLOCK, NV_BLOCK))
+    s = e4m3_round(np.abs(blk).max(axis=-1) / (E2M1_MAX * g))   # block scales, E4M3 values
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(s[..., None] > 0, e2m1_round(blk / (s[..., None] * g)), 0.0)
+    codes = e2m1_encode(q).reshape(v.shape)
+    return np.moveaxis(codes, -1, axis), np.moveaxis(e4m3_encode(s), -1, axis), g
+
+
+def nv_dequantize(codes: np.ndarray, scales: np.ndarray, g: float, axis: int) -> np.ndarray:
+    c = np.moveaxis(codes, axis, -1)
+    s = e4m3_decode(np.moveaxis(scales, axis, -1))
+    vals = e2m1_decode(c).reshape(c.shape[:-1] + (c.shape[-1] // NV_BLOCK, NV_BLOCK))
+    return np.moveaxis((vals * s[..., None] * g).reshape(c.shape), -1, axis)
+
+
+def nv_roundtrip(v: np.ndarray, axis: int) -> np.ndarray:
+    c, s, g = nv_quantize(v, axis)
+    return nv_dequantize(c, s, g, axis)
+
+
+# --------------------------------------------------------------------------
 # router ([KC] section 01: the router picks each token's experts at every step)
 
 
@@ -264,7 +347,9 @@ def forward(x, Wr, bias, W1, W3, W2, k, *, precision="bf16", macrobatch_tokens=0
     x [T,H], Wr [H,E], W1/W3 [E,H,F], W2 [E,F,H] as float64 (or bf16 bits decoded
     by the caller). `ids` overrides the router's choice (used where GPU and
     oracle sit on a near-tie). precision "mxfp8" emulates MXFP8 operands of both
-    GEMMs: x and W1/W3 along H, h and W2 along F ([KC] section 02).
+    GEMMs: x and W1/W3 along H, h and W2 along F ([KC] section 02); precision
+    "nvfp4" emulates NVFP4 expert weights (W1, W3 along H, W2 along F, one matrix
+    scale per expert and matrix) with the activations as in the bf16 layer.
     weight_cache: optional dict that keeps each expert's (quantised) weight copies
     across calls with the same weights (the quantisation of the weights happens once
     per weight update, not per step).
@@ -293,6 +378,10 @@ def forward(x, Wr, bias, W1, W3, W2, k, *, precision="bf16", macrobatch_tokens=0
                 W1e = mx_roundtrip(W1e, 0)
                 W3e = mx_roundtrip(W3e, 0)
                 W2e = mx_roundtrip(W2e, 0)
+            elif precision == "nvfp4":
+                W1e = nv_roundtrip(W1e, 0)
+                W3e = nv_roundtrip(W3e, 0)
+                W2e = nv_roundtrip(W2e, 0)
             wq[e] = (W1e, W3e, W2e)
         return wq[e]
 

@@ -13,6 +13,7 @@ import pytest
 
 from tests import test_oracle_ffn_grad as FG
 from tests import test_oracle_mxfp8 as MX
+from tests import test_oracle_nvfp4 as NV
 from tests import test_oracle_router_schedule as RS
 
 ORACLE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "moe_oracle.py")
@@ -50,6 +51,9 @@ MXW2H = _pins(MX, "test_mxfp8_dW2_rounds_hw_along_the_token_axis")
 MXW2G = _pins(MX, "test_mxfp8_dW2_rounds_dy_along_the_token_axis")
 MXDY = _pins(MX, "test_mxfp8_backward_rounds_dy_along_H")
 MXRT = _pins(MX, "test_roundtrip_equals_dequantised_codes")
+NVQ = _pins(NV, "test_e2m1_golden_codes", "test_e2m1_round_matches_exhaustive_nearest_even",
+            "test_matrix_scale_closed_form", "test_nv_block_properties")
+NVL = _pins(NV, "test_nvfp4_layer_quantises_each_weight_along_its_contraction_axis")
 
 # (what the mistake is, text in the oracle, its replacement, the pins that must notice it)
 MUTATIONS = [
@@ -102,6 +106,19 @@ MUTATIONS = [
      "starts.append(0); pos += s1 - s0; ends.append(pos)", MXW),
     ("MXFP8: dY not rounded along H for the GEMM2 dgrad", "G = mx_roundtrip(Ge, 1) @ W2e.T",
      "G = Ge @ W2e.T", MXDY),
+    ("NVFP4: E2M1 ties away from zero", "q = np.minimum(np.round(a / quantum) * quantum, E2M1_MAX)",
+     "q = np.minimum(np.floor(a / quantum + 0.5) * quantum, E2M1_MAX)", NVQ),
+    ("NVFP4: E2M1 spacing of 1 from 1.5 on", "quantum = np.where(a < 2.0, 0.5,", "quantum = np.where(a < 1.5, 0.5,", NVQ),
+    ("NVFP4: no saturation at 6", "q = np.minimum(np.round(a / quantum) * quantum, E2M1_MAX)",
+     "q = np.round(a / quantum) * quantum", NVQ),
+    ("NVFP4: matrix scale rounded down", "return math.ldexp(1.0, ex - 1) if mant == 0.5 else math.ldexp(1.0, ex)",
+     "return math.ldexp(1.0, ex - 1)", NVQ),
+    ("NVFP4: block scale without the matrix scale", "s = e4m3_round(np.abs(blk).max(axis=-1) / (E2M1_MAX * g))",
+     "s = e4m3_round(np.abs(blk).max(axis=-1) / E2M1_MAX)", NVQ),
+    ("NVFP4: blocks of 32", "NV_BLOCK = 16", "NV_BLOCK = 32", NVQ),
+    ("NVFP4: W1 along F", "W1e = nv_roundtrip(W1e, 0)", "W1e = nv_roundtrip(W1e, 1)", NVL),
+    ("NVFP4: W2 along H", "W2e = nv_roundtrip(W2e, 0)", "W2e = nv_roundtrip(W2e, 1)", NVL),
+    ("NVFP4: W3 not quantised", "W3e = nv_roundtrip(W3e, 0)", "W3e = W3e", NVL),
     ("MXFP8: round trip without the block scale", "out = (e4m3_round(blk / scale) * scale).reshape(v.shape)",
      "out = e4m3_round(blk).reshape(v.shape)", MXRT),
 ]
