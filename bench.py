@@ -253,7 +253,8 @@ def kernel_bytes(w, name):
     """Algorithmic HBM bytes per step of the memory-bound kernels."""
     T, H, F, R, E, k = w.T, w.H, w.F, w.R, w.E, w.k
     qh, qf = R * H * 33 // 32, R * F * 33 // 32   # one MXFP8 copy of R rows (codes + scales)
-    return {"dispatch": T * H * 2 + R * H * 2, "dispatch_replay": T * H * 2 + R * H * 2,
+    return {"decode_ffn": 3 * E * H * F * 2,   # every expert's weights streamed once (few tokens)
+            "dispatch": T * H * 2 + R * H * 2, "dispatch_replay": T * H * 2 + R * H * 2,
             "dispatch_mxfp8": T * H * 2 + qh,
             "reverse_combine": T * H * 2 + R * H * 2, "combine": R * H * 2 + T * H * 2 + R * 8,
             "router_topk": T * H * 2 + T * E * 4 + T * k * 8,
@@ -267,8 +268,10 @@ def kernel_bytes(w, name):
 
 
 def gemm_flops(w, name):
+    """GEMM flops per step; the persistent forward and the decode kernel run both expert GEMMs."""
     R, H, F = w.R, w.H, w.F
-    return {"grouped_gemm_fwd1_swiglu": 4 * R * H * F, "grouped_gemm_fwd2": 2 * R * H * F,
+    return {"forward_persistent": 6 * R * H * F, "decode_ffn": 6 * R * H * F,
+            "grouped_gemm_fwd1_swiglu": 4 * R * H * F, "grouped_gemm_fwd2": 2 * R * H * F,
             "grouped_gemm_bwd2_swiglu": 2 * R * H * F, "grouped_gemm_bwd1": 4 * R * H * F,
             "grouped_gemm_wgrad2": 2 * R * H * F, "grouped_gemm_wgrad13": 4 * R * H * F}.get(name)
 
@@ -289,6 +292,7 @@ def gemm_bytes(w, name):
 
 GEMMS = ["grouped_gemm_fwd1_swiglu", "grouped_gemm_fwd2", "grouped_gemm_bwd2_swiglu", "grouped_gemm_bwd1",
          "grouped_gemm_wgrad2", "grouped_gemm_wgrad13"]
+GEMM_KERNELS = ("grouped_gemm", "forward_persistent")   # kernels whose time is expert-GEMM time
 
 
 def tensor_peak(w, peaks, peak_src, loop_s):
@@ -327,7 +331,7 @@ def rate_kernels(w, kernels, steps, prof_ms, peaks, peak_src, loop_s):
     rows = []
     for nm, n_, ms_ in kt:
         row = {"name": nm, "launches": n_, "ms_per_step": ms_ / steps, "share": ms_ / prof_ms}
-        if gemm_flops(w, nm):
+        if gemm_flops(w, nm) and nm != "decode_ffn":
             row["tflops"] = gemm_flops(w, nm) * steps / (ms_ * 1e-3) / 1e12
             row["frac_of_tensor_peak"] = row["tflops"] / tf
         if kernel_bytes(w, nm) and hbm:
@@ -340,7 +344,7 @@ def rate_kernels(w, kernels, steps, prof_ms, peaks, peak_src, loop_s):
     per_launch_ms = ms / n
     per_step = n / steps
     roof = None
-    if gemm_flops(w, name):
+    if gemm_flops(w, name) and name != "decode_ffn":
         fl = gemm_flops(w, name) / per_step
         ach = fl / (per_launch_ms * 1e-3) / 1e12
         roof = {"kernel": name, "bound": "tensor", "achieved": ach, "peak": tf, "unit": "TFLOP/s",
@@ -357,8 +361,8 @@ def rate_kernels(w, kernels, steps, prof_ms, peaks, peak_src, loop_s):
         roof = {"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
                 "frac": ach / hbm, "traffic": committed_traffic(name, w.name), "algorithmic_per_launch": gb,
                 "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"}
-    gemm_ms = sum(ms_ for nm, _, ms_ in kernels if nm.startswith("grouped_gemm"))
-    gemm_fl = sum(gemm_flops(w, nm) * steps for nm, _, _ in kernels if gemm_flops(w, nm))
+    gemm_ms = sum(ms_ for nm, _, ms_ in kernels if nm.startswith(GEMM_KERNELS))
+    gemm_fl = sum(gemm_flops(w, nm) * steps for nm, _, _ in kernels if nm.startswith(GEMM_KERNELS))
     gg = None
     if gemm_ms:
         t = gemm_fl / (gemm_ms * 1e-3) / 1e12
@@ -386,7 +390,7 @@ class Gpu:
         self.dW1 = torch.empty(w.E, w.H, w.F, dtype=f32, device=dev)
         self.dW3 = torch.empty_like(self.dW1)
         self.dW2 = torch.empty(w.E, w.F, w.H, dtype=f32, device=dev)
-        if w.precision == "mxfp8":
+        if w.precision in ("mxfp8", "nvfp4"):
             self.quantize()
 
     def to_dev(self, a):
@@ -602,6 +606,34 @@ def run_ours(args, w):
                                                   "frac_of_tensor_peak", "gbs", "frac_of_hbm") if k_ in r}
                             for r in rows]})
             del go
+            torch.cuda.empty_cache()
+        # decode-sized forward (few tokens of the balanced shape), bf16 and NVFP4 weights: every
+        # expert's weights stream once, so the floor is their bytes at the HBM copy bandwidth
+        for prec in ("bf16", "nvfp4"):
+            wd = WL.BALANCED.with_(T=64, precision=prec, name=f"{WL.BALANCED.name}@T64/{prec}")
+            gd = Gpu(wd, dev, rank, M, MoeLayer, torch)
+            with torch.cuda.stream(gd.stream):
+                for _ in range(args.warmup):
+                    gd.fwd()
+            t_fwd = timed(gd, flush, gd.fwd, args.steps)
+            M.moe_profile_begin()
+            timed(gd, flush, gd.fwd, args.steps)
+            kern = M.moe_profile_end()
+            gd.layer.status(gd.stream)
+            hbm_d = load_peaks()[0]["hbm_gbs"]
+            wbytes = kernel_bytes(wd, "decode_ffn") * (1.0 if prec == "bf16" else (0.5 + 1 / 16) / 2)
+            floor_us = wbytes / (hbm_d * 1e9) * 1e6
+            dk = {nm: ms_ / args.steps * 1e3 for nm, _, ms_ in kern}
+            kname = "decode_ffn" if prec == "bf16" else "decode_ffn_nvfp4"
+            others.append({
+                "workload": wd.name, "precision": prec, "T": wd.T, "H": wd.H, "F": wd.F, "E": wd.E, "k": wd.k,
+                "fwd": {"value": wd.T * args.steps / (t_fwd * 1e-3), "unit": "tokens/s",
+                        "us_per_step": t_fwd / args.steps * 1e3},
+                "weight_bytes": wbytes, "weight_stream_floor_us": floor_us,
+                "fwd_over_floor": t_fwd / args.steps * 1e3 / floor_us,
+                kname: {"us": dk.get(kname), "frac_of_hbm": floor_us / dk[kname] if dk.get(kname) else None},
+                "kernels_us": dk})
+            del gd
             torch.cuda.empty_cache()
         inp = headline_inp
     else:

@@ -76,7 +76,12 @@ typedef enum {
 
 typedef enum {
     MOE_PRECISION_BF16 = 0,    /* bf16 operands, fp32 accumulation */
-    MOE_PRECISION_MXFP8 = 1    /* e4m3 operands, one e8m0 scale per 32 along K */
+    MOE_PRECISION_MXFP8 = 1,   /* e4m3 operands, one e8m0 scale per 32 along K */
+    MOE_PRECISION_NVFP4 = 2    /* NVFP4 expert weights (e2m1, one e4m3 scale per 16 along K,
+                                  a power-of-two fp32 scale per expert matrix), bf16
+                                  activations: the forward of at most 128 tokens in one
+                                  macrobatch (the decode kernel); moe_backward and larger
+                                  batches return MOE_ERR_UNSUPPORTED */
 } moe_precision_t;
 
 /* Layer shape and run options. Zero-initialise, then set the shape.
@@ -154,7 +159,7 @@ size_t moe_workspace_size(const moe_config_t *cfg);
  * then the backward's dW1/dW3 read, so the backward never gathers them again). */
 size_t moe_saved_size(const moe_config_t *cfg);
 
-/* Bytes of the MXFP8 weight copies made by moe_quantize_weights (0 for bf16). */
+/* Bytes of the MXFP8 or NVFP4 weight copies made by moe_quantize_weights (0 for bf16). */
 size_t moe_qweights_size(const moe_config_t *cfg);
 
 /* Schedule only (article section 01: count, place, group).
@@ -199,9 +204,10 @@ moe_status_t moe_schedule_static(const moe_config_t *cfg, const int32_t *topk_id
                                  int32_t *sorted_to_slot, int32_t *slot_to_sorted,
                                  moe_stream_t stream);
 
-/* MXFP8 copies of the bf16 master weights for the forward and backward
- * GEMMs (quantised along each GEMM's contraction axis). Run once per weight
- * update. Returns MOE_ERR_UNSUPPORTED for a bf16 config. */
+/* Quantised copies of the bf16 master weights, run once per weight update:
+ * MXFP8: one copy per forward and backward GEMM, each along its contraction
+ * axis; NVFP4: W1, W3 along H and W2 along F, in the tiles the decode kernel
+ * streams. Returns MOE_ERR_UNSUPPORTED for a bf16 config. */
 moe_status_t moe_quantize_weights(const moe_config_t *cfg, const void *W1,
                                   const void *W3, const void *W2,
                                   void *qweights, size_t qweights_bytes,

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
 SOURCES = ["moe_api.cu", "route_kernels.cu", "grouped_gemm.cu", "mx_quant.cu", "moe_static_scratch.cu",
-           "decode_ffn.cu"]
+           "decode_ffn.cu", "nvfp4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"] + ARCH
 

@@ -12,6 +12,7 @@
 #include "decode_ffn.cuh"
 #include "grouped_gemm.cuh"
 #include "mx_quant.cuh"
+#include "nvfp4.cuh"
 #include "route_kernels.cuh"
 
 using namespace moe;
@@ -84,7 +85,8 @@ moe_status_t check_shape(const moe_config_t *c) {
     if (c->k > c->E) return fail(MOE_ERR_INVALID_ARG, "k > E");
     if (c->k > 32) return fail(MOE_ERR_UNSUPPORTED, "k > 32 is not supported");
     if (c->H % 256 || c->F % 256) return fail(MOE_ERR_UNSUPPORTED, "H and F must be multiples of 256");
-    if (c->precision != MOE_PRECISION_BF16 && c->precision != MOE_PRECISION_MXFP8)
+    if (c->precision != MOE_PRECISION_BF16 && c->precision != MOE_PRECISION_MXFP8 &&
+        c->precision != MOE_PRECISION_NVFP4)
         return fail(MOE_ERR_INVALID_ARG, "unknown precision");
     if (c->minibatch_rows < 0 || c->macrobatch_tokens < 0) return fail(MOE_ERR_INVALID_ARG, "negative minibatch/macrobatch");
     if (c->forward_mode != MOE_FORWARD_PERSISTENT && c->forward_mode != MOE_FORWARD_PER_STAGE)
@@ -204,6 +206,8 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     // few bf16 tokens in one macrobatch: every expert holds at most T <= 128 rows, and the
     // forward streams each expert's weights once through the decode kernel
     L.decode = kDecodePath && !mx && c->T > 0 && c->T <= kDecodeMaxTokens && L.nM == 1;
+    if (c->precision == MOE_PRECISION_NVFP4 && c->T > 0 && !L.decode)
+        return fail(MOE_ERR_UNSUPPORTED, "NVFP4 weights run the forward of at most 128 tokens in one macrobatch");
     const size_t region = o;
     const size_t ring_rows = (size_t)L.half_rows * L.ring_halves;
     // forward region: the ring
@@ -557,7 +561,9 @@ size_t moe_saved_size(const moe_config_t *cfg) {
 }
 
 size_t moe_qweights_size(const moe_config_t *cfg) {
-    if (check_shape(cfg) != MOE_OK || cfg->precision != MOE_PRECISION_MXFP8) return 0;
+    if (check_shape(cfg) != MOE_OK) return 0;
+    if (cfg->precision == MOE_PRECISION_NVFP4) return nv_layout(cfg->E, cfg->H, cfg->F).bytes + kBaseSlack;
+    if (cfg->precision != MOE_PRECISION_MXFP8) return 0;
     return qw_layout(cfg).bytes + kBaseSlack;
 }
 
@@ -565,8 +571,22 @@ moe_status_t moe_quantize_weights(const moe_config_t *cfg, const void *W1, const
                                   void *qweights, size_t qweights_bytes, moe_stream_t stream) {
     moe_status_t st = check_shape(cfg);
     if (st != MOE_OK) return st;
-    if (cfg->precision != MOE_PRECISION_MXFP8) return fail(MOE_ERR_UNSUPPORTED, "weight quantisation is for MXFP8 configs");
+    if (cfg->precision == MOE_PRECISION_BF16) return fail(MOE_ERR_UNSUPPORTED, "weight quantisation is for MXFP8 and NVFP4 configs");
     if (!W1 || !W3 || !W2 || !qweights) return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
+    if (cfg->precision == MOE_PRECISION_NVFP4) {
+        const NvLayout nl = nv_layout(cfg->E, cfg->H, cfg->F);
+        if (!fits(qweights, qweights_bytes, nl.bytes)) return fail(MOE_ERR_WORKSPACE, "qweights buffer too small");
+        const void *ptrs[] = {W1, W3, W2};
+        for (const void *p : ptrs)
+            if (!aligned(p, 16)) return fail(MOE_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+        const int sms = cfg->num_sms > 0 ? cfg->num_sms : query_num_sms();
+        if (sms <= 0) return fail(MOE_ERR_CUDA, "could not query the SM count");
+        ProfScope ps("quantize_weights", (cudaStream_t)stream);
+        return cuda_check(launch_nv_quantize((const bf16 *)W1, (const bf16 *)W3, (const bf16 *)W2,
+                                             static_cast<uint8_t *>(align_base(qweights)), nl, cfg->E, cfg->H,
+                                             cfg->F, sms, (cudaStream_t)stream),
+                          "NVFP4 weight quantise launch");
+    }
     const QwLayout q = qw_layout(cfg);
     if (!fits(qweights, qweights_bytes, q.bytes)) return fail(MOE_ERR_WORKSPACE, "qweights buffer too small");
     const void *ptrs16[] = {W1, W3, W2};
@@ -649,8 +669,8 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
     Layout L;
     moe_status_t st = make_layout(cfg, L);
     if (st != MOE_OK) return st;
-    if (cfg->precision == MOE_PRECISION_MXFP8 && !qweights)
-        return fail(MOE_ERR_INVALID_ARG, "MXFP8 forward needs qweights");
+    if (cfg->precision != MOE_PRECISION_BF16 && !qweights)
+        return fail(MOE_ERR_INVALID_ARG, "MXFP8 and NVFP4 forwards need qweights");
     if (!W_r || !W1 || !W3 || !W2 || !saved || !workspace || (L.T > 0 && (!x || !out || !topk_ids || !topk_w)))
         return fail(MOE_ERR_INVALID_ARG, "null pointer argument");
     if (!fits(saved, saved_bytes, L.saved_bytes)) return fail(MOE_ERR_WORKSPACE, "saved buffer too small");
@@ -724,6 +744,13 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
         da.claim = dc; da.hdone = dc + 1;
         da.E = L.E; da.H = L.H; da.F = L.F; da.nb = ceil_div(L.T, 32);
         da.status = at<int>(ws, L.w_status); da.budget_ns = budget_ns(cfg);
+        const bool nv = cfg->precision == MOE_PRECISION_NVFP4;
+        if (nv) {
+            const NvLayout nl = nv_layout(L.E, L.H, L.F);
+            da.nvq = static_cast<const uint8_t *>(align_base(qweights));
+            for (int i = 0; i < 3; ++i) { da.nv_codes[i] = nl.m[i].codes; da.nv_scales[i] = nl.m[i].scales; }
+            da.nv_g = reinterpret_cast<const float *>(da.nvq + nl.gscale);
+        }
         st = cuda_check(cudaMemsetAsync(dc, 0, 4 * (1 + (size_t)L.E), s), "decode counters clear");
         if (st != MOE_OK) return st;
         DispatchArgs d{};
@@ -735,8 +762,9 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
         }
         if (st != MOE_OK) return st;
         {
-            ProfScope ps("decode_ffn", s);
-            st = cuda_check(launch_decode_ffn(da, L.num_sms, s), "decode FFN launch");
+            ProfScope ps(nv ? "decode_ffn_nvfp4" : "decode_ffn", s);
+            st = cuda_check(nv ? launch_decode_nv(da, L.num_sms, s) : launch_decode_ffn(da, L.num_sms, s),
+                            "decode FFN launch");
         }
         if (st != MOE_OK) return st;
         CombineArgs ca{};
@@ -867,6 +895,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
     moe_status_t st = make_layout(cfg, L);
     if (st != MOE_OK) return st;
     const bool mx = cfg->precision == MOE_PRECISION_MXFP8;
+    if (cfg->precision == MOE_PRECISION_NVFP4) return fail(MOE_ERR_UNSUPPORTED, "the NVFP4 layer runs the forward only");
     if (mx && !qweights) return fail(MOE_ERR_INVALID_ARG, "MXFP8 backward needs qweights");
     if (!W_r || !W1 || !W3 || !W2 || !saved || !workspace || !dW_r || !dW1 || !dW3 || !dW2 ||
         (L.T > 0 && (!x || !dout || !dx)))

@@ -22,12 +22,12 @@ class MoeLayer:
         self.workspace = torch.empty(self.plan.workspace_bytes, dtype=torch.uint8, device=self.device)
         self.saved = torch.empty(self.plan.saved_bytes, dtype=torch.uint8, device=self.device)
         self.qweights = None
-        if precision == "mxfp8":
+        if precision in ("mxfp8", "nvfp4"):
             self.qweights = torch.empty(_m.moe_qweights_size(self.cfg), dtype=torch.uint8, device=self.device)
         _m.moe_reset_status(self.workspace)
 
     def quantize_weights(self, W1, W3, W2, stream=None):
-        """MXFP8 copies of the bf16 weights (run once per weight update)."""
+        """MXFP8 or NVFP4 copies of the bf16 weights (run once per weight update)."""
         _m.moe_quantize_weights(self.cfg, W1, W3, W2, self.qweights, stream)
 
     def forward(self, x, Wr, bias, W1, W3, W2, out=None, topk_ids=None, topk_w=None, stream=None):

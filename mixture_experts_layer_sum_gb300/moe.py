@@ -22,6 +22,7 @@ MOE_ERR_INTERNAL = 6
 MOE_FAULT_GEMM1_READY = 1   # config fault_mask bit (failure-detection tests)
 MOE_PRECISION_BF16 = 0
 MOE_PRECISION_MXFP8 = 1
+MOE_PRECISION_NVFP4 = 2
 MOE_FORWARD_PERSISTENT = 0
 MOE_FORWARD_PER_STAGE = 1
 
@@ -68,7 +69,7 @@ class moe_plan_t(ctypes.Structure):
 
 def make_config(T, H, F, E, k, precision="bf16", minibatch_rows=0, macrobatch_tokens=0, ring_bytes=0,
                 timeout_ms=0, num_sms=0, fault_mask=0, forward_mode=0) -> moe_config_t:
-    p = {"bf16": MOE_PRECISION_BF16, "mxfp8": MOE_PRECISION_MXFP8}.get(precision, precision)
+    p = {"bf16": MOE_PRECISION_BF16, "mxfp8": MOE_PRECISION_MXFP8, "nvfp4": MOE_PRECISION_NVFP4}.get(precision, precision)
     return moe_config_t(T, H, F, E, k, p, minibatch_rows, macrobatch_tokens, ring_bytes, timeout_ms, num_sms,
                         fault_mask, forward_mode)
 

@@ -42,7 +42,7 @@ def run_gpu(w: WL.Workload, inp, backward=True, accumulate_into=None, **layer_kw
     d = device_inputs(inp)
     T = inp["x"].shape[0]
     layer = MoeLayer(T, w.H, w.F, w.E, w.k, w.precision, **layer_kw)
-    if w.precision == "mxfp8":
+    if w.precision in ("mxfp8", "nvfp4"):
         layer.quantize_weights(d["W1"], d["W3"], d["W2"])
     out, ids, wts = layer.forward(d["x"], d["Wr"], d["bias"], d["W1"], d["W3"], d["W2"])
     res = {"out": out, "ids": ids, "w": wts}
@@ -103,6 +103,7 @@ def check_layer(w, inp, gpu, backward=True, macrobatch_tokens=0):
                       precision=w.precision, macrobatch_tokens=macrobatch_tokens, ids=ids, weight_cache=wc[0])
     errs = {"w": float(np.abs(gpu["w"] - f["w"]).max()) if f["w"].size else 0.0,
             "out": O.max_abs_rel(gpu["out"], f["out"])}
+    # NVFP4: the weights are exact on both sides (the same quantisation); activations as in bf16
     ftol, btol = (MX_TOL, MX_TOL) if w.precision == "mxfp8" else (FWD_TOL, BWD_TOL)
     assert errs["w"] < 1e-4, errs
     assert errs["out"] < ftol, errs
