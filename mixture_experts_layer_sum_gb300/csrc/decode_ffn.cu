@@ -337,16 +337,23 @@ namespace moe {
 
 namespace {
 
-constexpr int NV_C = 8;                                  // compressed stages
+constexpr int NV_CMAX = 8;                               // compressed stages (at most)
 constexpr uint32_t NV_QTILE = 4096 + 512;                // codes + scales of one weight tile
-constexpr uint32_t NV_CSTAGE = 2 * NV_QTILE;             // W1 and W3 (GEMM1) or W2 (GEMM2)
 constexpr int NV_B = 3;                                  // expanded stages
-constexpr uint32_t NV_BSTAGE = 2 * DW_TILE + 4 * DT_BOX; // bf16 weight tiles (K-major) + 128 token rows
-static_assert(NV_B * NV_BSTAGE + NV_C * NV_CSTAGE <= DSMEM, "shared memory budget");
+constexpr uint32_t NV_BSTAGE = 2 * DW_TILE;              // bf16 weight tiles (K-major)
 constexpr int NV_CONV_THREADS = 128;
+// compressed stage: the expert's token rows (nb boxes of 32 rows, 1 KB aligned for the
+// 128-byte swizzle) then the compressed W1 and W3 (or W2) tiles
+__host__ __device__ constexpr uint32_t nv_cstage(int nb) { return nb * DT_BOX + 2 * NV_QTILE; }
+__host__ __device__ constexpr int nv_cstages(int nb) {
+    return (int)((DSMEM - NV_B * NV_BSTAGE) / nv_cstage(nb)) < NV_CMAX ? (int)((DSMEM - NV_B * NV_BSTAGE) / nv_cstage(nb))
+                                                                       : NV_CMAX;
+}
+static_assert(nv_cstage(4) % 1024 == 0 && nv_cstage(1) % 1024 == 0, "1 KB aligned stages");
 
 struct NvDecCtl {
-    uint64_t cfull[NV_C], cempty[NV_C], bfull[NV_B], bempty[NV_B], tfull[2], tempty[2], qfull[QD], qempty[QD], drain;
+    uint64_t cfull[NV_CMAX], cempty[NV_CMAX], bfull[NV_B], bempty[NV_B], tfull[2], tempty[2], qfull[QD], qempty[QD],
+        drain;
     uint32_t tmem_base;
     int item[QD];
 };
@@ -357,8 +364,13 @@ __device__ __forceinline__ size_t nv_tile(const DecodeArgs &a, int mat, int e, i
     return ((size_t)e * (N / 128) + col0 / 128) * (K / 64) + kb;
 }
 
+// Streams every stage's token rows and compressed weight tiles; a compressed stage is freed by
+// the MMA thread once the tensor cores have read its token rows (its weights were expanded
+// before that), so the token copies run as far ahead as the compressed ring is deep.
 __device__ void nv_producer(const DecodeArgs &a, NvDecCtl &c, uint8_t *cring, const WaitCtl &ctl) {
     const int total = a.E * (a.F / 128 + a.H / 128);
+    const int NC = nv_cstages(a.nb);
+    const uint32_t CS = nv_cstage(a.nb);
     int stage = 0, slot = 0;
     uint32_t phase = 0, qphase = 0, issued = 0, last_phase = 0;
     bool ok = true;
@@ -377,25 +389,34 @@ __device__ void nv_producer(const DecodeArgs &a, NvDecCtl &c, uint8_t *cring, co
         if (++slot == QD) { slot = 0; qphase ^= 1; }
         if (id < 0) break;
         const Item it = decode_item(a, id);
+        const int s0 = a.offp[it.e];
+        const int nb = (a.counts[it.e] + 31) / 32;
+        if (!it.gemm1) {
+            // h of this expert: the four epilogue warps of every GEMM1 item of it have published
+            if (!flag_wait_geq(a.hdone + it.e, 4 * (a.F / 128), ctl)) { ok = false; continue; }
+            fence_proxy_async_global();
+        }
         for (int kb = 0; kb < it.nk && ok; ++kb) {
             if (!mbar_wait(smem_u32(&c.cempty[stage]), phase ^ 1, ctl)) { ok = false; break; }
             const uint32_t bar = smem_u32(&c.cfull[stage]);
-            const uint32_t sC = smem_u32(cring + stage * NV_CSTAGE);
+            const uint32_t sC = smem_u32(cring + stage * CS);
             const int nmat = it.gemm1 ? 2 : 1;
-            mbar_arrive_expect_tx(bar, nmat * NV_QTILE);
+            mbar_arrive_expect_tx(bar, nb * DT_BOX + nmat * NV_QTILE);
+            for (int j = 0; j < nb; ++j) tma_load_2d(sC + j * DT_BOX, it.gemm1 ? &a.x : &a.h, bar, kb * 64, s0 + 32 * j);
+            const uint32_t sQ = sC + a.nb * DT_BOX;
             for (int i = 0; i < nmat; ++i) {
                 const int mat = it.gemm1 ? i : 2;
                 const size_t t = nv_tile(a, mat, it.e, it.col0, kb);
-                bulk_load_1d(sC + i * NV_QTILE, a.nvq + a.nv_codes[mat] + t * 4096, 4096, bar);
-                bulk_load_1d(sC + i * NV_QTILE + 4096, a.nvq + a.nv_scales[mat] + t * 512, 512, bar);
+                bulk_load_1d(sQ + i * NV_QTILE, a.nvq + a.nv_codes[mat] + t * 4096, 4096, bar);
+                bulk_load_1d(sQ + i * NV_QTILE + 4096, a.nvq + a.nv_scales[mat] + t * 512, 512, bar);
             }
             issued |= 1u << stage;
             last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-            if (++stage == NV_C) { stage = 0; phase ^= 1; }
+            if (++stage == NC) { stage = 0; phase ^= 1; }
         }
     }
     if (!ok) {
-        for (int s = 0; s < NV_C; ++s) {
+        for (int s = 0; s < NC; ++s) {
             if (!((issued >> s) & 1u)) continue;
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(smem_u32(&c.cfull[s]), (last_phase >> s) & 1u) && globaltimer_ns() - t0 < ctl.budget_ns) {}
@@ -433,6 +454,8 @@ __device__ __forceinline__ float nv_scale_value(uint32_t byte) {
 __device__ void nv_converter(const DecodeArgs &a, NvDecCtl &c, uint8_t *bring, uint8_t *cring, const WaitCtl &ctl) {
     const int t = threadIdx.x - 192;             // 0..127: the weight row (column of W) this thread expands
     const int lane = threadIdx.x % 32;
+    const int NC = nv_cstages(a.nb);
+    const uint32_t CS = nv_cstage(a.nb);
     int slot = 0, cs = 0, bs = 0;
     uint32_t qphase = 0, cphase = 0, bphase = 0;
     for (;;) {
@@ -443,54 +466,39 @@ __device__ void nv_converter(const DecodeArgs &a, NvDecCtl &c, uint8_t *bring, u
         if (++slot == QD) { slot = 0; qphase ^= 1; }
         if (id < 0) break;
         const Item it = decode_item(a, id);
-        const int s0 = a.offp[it.e];
-        const int nb = (a.counts[it.e] + 31) / 32;
-        bool tok_ok = true;
-        if (!it.gemm1 && t == 0) {
-            // h of this expert: the four epilogue warps of every GEMM1 item of it have published
-            tok_ok = flag_wait_geq(a.hdone + it.e, 4 * (a.F / 128), ctl);
-            fence_proxy_async_global();
-        }
         bool ok = true;
         for (int kb = 0; kb < it.nk; ++kb) {
             if (!mbar_wait(smem_u32(&c.cfull[cs]), cphase, ctl)) { ok = false; break; }
             if (!mbar_wait(smem_u32(&c.bempty[bs]), bphase ^ 1, ctl)) { ok = false; break; }
             uint8_t *sB = bring + bs * NV_BSTAGE;
-            const uint32_t bar = smem_u32(&c.bfull[bs]);
-            if (t == 0) {
-                // the expert's token rows (x for GEMM1, h for GEMM2); after a failed wait the
-                // stage completes without them (the status word already reports the failure)
-                mbar_arrive_expect_tx(bar, tok_ok ? nb * DT_BOX : 0);
-                if (tok_ok)
-                    for (int j = 0; j < nb; ++j)
-                        tma_load_2d(smem_u32(sB + 2 * DW_TILE + j * DT_BOX), it.gemm1 ? &a.x : &a.h, bar, kb * 64, s0 + 32 * j);
-            }
-            const uint8_t *sC = cring + cs * NV_CSTAGE;
+            const uint8_t *sQ = cring + cs * CS + a.nb * DT_BOX;
             const int nmat = it.gemm1 ? 2 : 1;
             for (int i = 0; i < nmat; ++i) {
-                const uint4 q0 = *reinterpret_cast<const uint4 *>(sC + i * NV_QTILE + t * 32);
-                const uint4 q1 = *reinterpret_cast<const uint4 *>(sC + i * NV_QTILE + t * 32 + 16);
-                const uint32_t sb = *reinterpret_cast<const uint32_t *>(sC + i * NV_QTILE + 4096 + t * 4);
+                const uint4 q0 = *reinterpret_cast<const uint4 *>(sQ + i * NV_QTILE + t * 32);
+                const uint4 q1 = *reinterpret_cast<const uint4 *>(sQ + i * NV_QTILE + t * 32 + 16);
+                const uint32_t sb = *reinterpret_cast<const uint32_t *>(sQ + i * NV_QTILE + 4096 + t * 4);
+                const float sc[4] = {nv_scale_value(sb & 0xFFu), nv_scale_value((sb >> 8) & 0xFFu),
+                                     nv_scale_value((sb >> 16) & 0xFFu), nv_scale_value(sb >> 24)};
                 const uint32_t w8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
                 uint8_t *row = sB + i * DW_TILE + t * 128;   // K-major, 128-byte swizzle
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const float sc = nv_scale_value((sb >> (8 * (ch / 2))) & 0xFFu);
-                    *reinterpret_cast<uint4 *>(row + ((ch ^ (t & 7)) * 16)) = nv_expand8(w8[ch], sc);
-                }
+                for (int ch = 0; ch < 8; ++ch)
+                    *reinterpret_cast<uint4 *>(row + ((ch ^ (t & 7)) * 16)) = nv_expand8(w8[ch], sc[ch / 2]);
             }
             fence_proxy_async_shared();   // generic shared-memory writes, read by the tensor cores
-            mbar_arrive(bar);
-            mbar_arrive(smem_u32(&c.cempty[cs]));
-            if (++cs == NV_C) { cs = 0; cphase ^= 1; }
+            mbar_arrive(smem_u32(&c.bfull[bs]));
+            if (++cs == NC) { cs = 0; cphase ^= 1; }
             if (++bs == NV_B) { bs = 0; bphase ^= 1; }
         }
         if (!ok) break;
     }
 }
 
-__device__ void nv_mma(const DecodeArgs &a, NvDecCtl &c, uint8_t *bring, uint32_t tmem, const WaitCtl &ctl) {
-    int bs = 0, slot = 0, acc = 0;
+__device__ void nv_mma(const DecodeArgs &a, NvDecCtl &c, uint8_t *bring, uint8_t *cring, uint32_t tmem,
+                       const WaitCtl &ctl) {
+    const int NC = nv_cstages(a.nb);
+    const uint32_t CS = nv_cstage(a.nb);
+    int bs = 0, cs = 0, slot = 0, acc = 0;
     uint32_t bphase = 0, qphase = 0, acc_phase = 0;
     for (;;) {
         if (!mbar_wait(smem_u32(&c.qfull[slot]), qphase, ctl)) break;
@@ -505,10 +513,11 @@ __device__ void nv_mma(const DecodeArgs &a, NvDecCtl &c, uint8_t *bring, uint32_
         const uint32_t d = tmem + acc * 256;
         bool ok = true;
         for (int kb = 0; kb < it.nk; ++kb) {
+            // the converters arrive only after they saw the compressed stage (token rows included) land
             if (!mbar_wait(smem_u32(&c.bfull[bs]), bphase, ctl)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sB = smem_u32(bring + bs * NV_BSTAGE);
-            const uint32_t sT = sB + 2 * DW_TILE;
+            const uint32_t sT = smem_u32(cring + cs * CS);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t bd = sdesc_sw128(sT + kk * 32, 16, 1024);
@@ -516,7 +525,9 @@ __device__ void nv_mma(const DecodeArgs &a, NvDecCtl &c, uint8_t *bring, uint32_
                 if (it.gemm1) mma_bf16_ss(d + 128, sdesc_sw128(sB + DW_TILE + kk * 32, 16, 1024), bd, idesc, (kb | kk) != 0);
             }
             mma_commit(smem_u32(&c.bempty[bs]));
+            mma_commit(smem_u32(&c.cempty[cs]));   // its token rows read: the compressed stage is free
             if (++bs == NV_B) { bs = 0; bphase ^= 1; }
+            if (++cs == NC) { cs = 0; } 
         }
         if (!ok) break;
         mma_commit(smem_u32(&c.tfull[acc]));
@@ -607,17 +618,17 @@ __device__ void nv_epilogue(const DecodeArgs &a, NvDecCtl &c, uint32_t tmem, con
 __global__ void __launch_bounds__(320, 1) decode_nv_kernel(const __grid_constant__ DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *bring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *cring = bring + NV_B * NV_BSTAGE;
+    uint8_t *cring = bring + NV_B * NV_BSTAGE;   // 1 KB aligned: the token boxes come first in a stage
     NvDecCtl &c = *reinterpret_cast<NvDecCtl *>(bring + DSMEM);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     WaitCtl ctl{a.status, a.budget_ns};
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NV_C; ++s) {
+        for (int s = 0; s < nv_cstages(a.nb); ++s) {
             mbar_init(smem_u32(&c.cfull[s]), 1);
-            mbar_init(smem_u32(&c.cempty[s]), NV_CONV_THREADS);
+            mbar_init(smem_u32(&c.cempty[s]), 1);                  // the MMA thread's commit
         }
         for (int s = 0; s < NV_B; ++s) {
-            mbar_init(smem_u32(&c.bfull[s]), NV_CONV_THREADS + 1);   // converters + the token copy
+            mbar_init(smem_u32(&c.bfull[s]), NV_CONV_THREADS);       // every converter thread
             mbar_init(smem_u32(&c.bempty[s]), 1);
         }
         for (int q = 0; q < QD; ++q) {
@@ -648,7 +659,7 @@ __global__ void __launch_bounds__(320, 1) decode_nv_kernel(const __grid_constant
     if (warp == 0) {
         if (lane == 0) nv_producer(a, c, cring, ctl);
     } else if (warp == 1) {
-        if (lane == 0) nv_mma(a, c, bring, tmem, ctl);
+        if (lane == 0) nv_mma(a, c, bring, cring, tmem, ctl);
     } else if (warp < 6) {
         nv_epilogue(a, c, tmem, ctl);
     } else {
