@@ -282,7 +282,8 @@ def gemm_bytes(w, name):
     operands; MXFP8 operands carry H*33/32 (or F*33/32) bytes per row instead of 2*H."""
     T, H, F, E, R = w.T, w.H, w.F, w.E, w.R
     W = E * H * F * 2   # one bf16 weight matrix of all experts
-    return {"grouped_gemm_fwd1_swiglu": T * H * 2 + 2 * W + 3 * R * F * 2,
+    return {"forward_persistent": T * H * 2 + 3 * W + 3 * R * F * 2 + R * H * 2,   # GEMM1 + GEMM2 operands
+            "grouped_gemm_fwd1_swiglu": T * H * 2 + 2 * W + 3 * R * F * 2,
             "grouped_gemm_fwd2": R * F * 2 + W + R * H * 2,
             "grouped_gemm_bwd2_swiglu": R * H * 2 + W + 2 * R * F * 2 + 3 * R * F * 2,
             "grouped_gemm_bwd1": 2 * R * F * 2 + 2 * W + R * H * 2,
@@ -350,7 +351,7 @@ def rate_kernels(w, kernels, steps, prof_ms, peaks, peak_src, loop_s):
         roof = {"kernel": name, "bound": "tensor", "achieved": ach, "peak": tf, "unit": "TFLOP/s",
                 "frac": ach / tf, "traffic": committed_traffic(name, w.name), "algorithmic_per_launch": fl,
                 "peak_source": tf_src}
-        if w.precision == "bf16" and hbm:
+        if w.precision == "bf16" and hbm and gemm_bytes(w, name) is not None:
             gb = gemm_bytes(w, name) / per_step
             roof["hbm_rating"] = {"algorithmic_bytes_per_launch": gb,
                                   "achieved_gbs": gb / (per_launch_ms * 1e-3) / 1e9,

@@ -657,7 +657,7 @@ template <int OP, bool FP8, bool PAIR = false, int EW = 4, class Ctl>
 __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *tfull, uint64_t *tempty,
                               uint32_t tmem, const WaitCtl &ctl, uint8_t *staging = nullptr) {
     static_assert(EW == 4 || EW == 8, "epilogue warps");
-    constexpr int NBUF = EW == 8 ? 2 : 4;     // 2 KB staging buffers per warp
+    constexpr int NBUF = (EW == 8 || FP8) ? 2 : 4;   // 2 KB staging buffers per warp (MXFP8 pairs: 16 KB in all)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int half = EW == 8 ? (warp - 2) / 4 : 0;   // column half of the tile this warp takes
     const int quarter = warp & 3;             // TMEM lanes this warp may read
@@ -669,7 +669,10 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
     const int ring_shift = g.ring_base - g.offp[g.m * g.E];
     const int rank = PAIR ? (int)cluster_ctarank() : 0;
     int store_chunks = 0;   // TMA stores issued by this warp (lane 0 tracks the bulk groups)
-    const bool tma_bf16 = !FP8 && staging != nullptr && g.tma_store && OP != OP_WG2 && OP != OP_WG13;
+    // bf16 row outputs leave through shared memory and TMA stores; in MXFP8 kernels only the
+    // GEMM2 / GEMM1-dgrad rows (the quantised outputs are stored from registers)
+    const bool tma_bf16 = staging != nullptr && g.tma_store && OP != OP_WG2 && OP != OP_WG13 &&
+                          (!FP8 || OP == OP_FWD2 || OP == OP_BWD1);
     uint8_t *warp_stage = staging ? staging + (warp - 2) * (NBUF * 2048) : nullptr;
     const int t0 = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
     const int tstep = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
@@ -1191,6 +1194,7 @@ constexpr int P8_STAGES = 6;
 constexpr uint32_t P8_TILE = 128 * 128;                        // 16 KiB: 128 rows x 128 B
 constexpr uint32_t P8_TX = 2 * P8_TILE + 3 * 512;              // bytes landing per CTA per stage
 constexpr uint32_t P8_STAGE = 34816;                           // 1 KiB aligned stage stride
+constexpr uint32_t P8_STAGING = 4 * 2 * 2048;                  // epilogue staging: 4 warps x 2 x 2 KB
 using Pair8Ctl = CtlT<P8_STAGES>;
 
 __device__ __forceinline__ int atom_row(int row, int k, int K) { return (int)(atom_at(row, k, K) / 128); }
@@ -1354,7 +1358,8 @@ template <int OP>
 __global__ void __launch_bounds__(320, 1) pair8_gemm_kernel(const __grid_constant__ GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Pair8Ctl &c = *reinterpret_cast<Pair8Ctl *>(tiles + P8_STAGES * P8_STAGE);
+    uint8_t *staging = tiles + P8_STAGES * P8_STAGE;                    // 4 epilogue warps x 2 x 2 KB
+    Pair8Ctl &c = *reinterpret_cast<Pair8Ctl *>(staging + P8_STAGING);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = cluster_ctarank();
     WaitCtl ctl{g.status, g.budget_ns};
@@ -1394,7 +1399,7 @@ __global__ void __launch_bounds__(320, 1) pair8_gemm_kernel(const __grid_constan
         if constexpr (OP == OP_FWD1) {
             if (g.fused) gather_loop<true>(g, g.m, g.ready, &c.tfull[0]);   // until the first accumulator is ready
         }
-        epilogue_loop<OP, true, true>(g, c, c.tfull, c.tempty, tmem, ctl, nullptr);
+        epilogue_loop<OP, true, true>(g, c, c.tfull, c.tempty, tmem, ctl, staging);
     } else {
         if constexpr (OP == OP_FWD1) gather_loop<true>(g, g.m, g.ready);
     }
@@ -1407,7 +1412,7 @@ __global__ void __launch_bounds__(320, 1) pair8_gemm_kernel(const __grid_constan
 
 template <int OP>
 cudaError_t launch_pair8(const GemmArgs &g, int grid, cudaStream_t stream) {
-    constexpr size_t smem = P8_STAGES * P8_STAGE + sizeof(Pair8Ctl) + 1024;
+    constexpr size_t smem = P8_STAGES * P8_STAGE + P8_STAGING + sizeof(Pair8Ctl) + 1024;
     static_assert(smem <= 227 * 1024, "shared memory budget");
     cudaError_t err = cudaFuncSetAttribute(pair8_gemm_kernel<OP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
@@ -1636,7 +1641,7 @@ __device__ void mega_mma(const MegaArgs &a, CtlT<FP8 ? P8_STAGES : PSTAGES> &c, 
 template <bool FP8>
 __device__ void mega_epilogue(const MegaArgs &a, CtlT<FP8 ? P8_STAGES : PSTAGES> &c, uint32_t tmem, int total,
                               const WaitCtl &ctl, uint8_t *staging) {
-    constexpr int NBUF = 4;
+    constexpr int NBUF = FP8 ? 2 : 4;   // 2 KB staging buffers per warp
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int quarter = warp & 3, r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
@@ -1694,7 +1699,7 @@ __device__ void mega_epilogue(const MegaArgs &a, CtlT<FP8 ? P8_STAGES : PSTAGES>
                 epi_fwd1_tile<FP8, NBUF>(g1, ti, tbase, r, quarter, lane, ring_shift, !FP8 && g1.tma_store, warp_stage,
                                          store_chunks);
             else
-                epi_rows_tile<OP_FWD2, NBUF>(g2, ti, tbase, r, quarter, lane, ring_shift, !FP8 && g2.tma_store,
+                epi_rows_tile<OP_FWD2, NBUF>(g2, ti, tbase, r, quarter, lane, ring_shift, g2.tma_store != 0,
                                              warp_stage, store_chunks);
         }
         tc_fence_before();
@@ -1707,7 +1712,7 @@ __device__ void mega_epilogue(const MegaArgs &a, CtlT<FP8 ? P8_STAGES : PSTAGES>
             __syncwarp();
             if (lane == 0) {
                 if (!rows) bulk_wait_group_all();
-                else if (FP8) bulk_wait_group_all();                                    // no bulk stores
+                else if (mt.op == MEGA_OP_GEMM1 && FP8) bulk_wait_group_all();          // no bulk stores
                 else if (mt.op == MEGA_OP_GEMM1) bulk_wait_group<12>();                 // a, b, h x 4 chunks
                 else bulk_wait_group<BN / 32>();                                        // Y: 8 chunks
                 fence_proxy_async_global();
@@ -1781,8 +1786,8 @@ __global__ void __launch_bounds__(320, 1) fwd_mega_kernel(const __grid_constant_
     constexpr uint32_t SS = FP8 ? P8_STAGE : P_STAGE;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *staging = FP8 ? nullptr : tiles + NS * SS;
-    Ctl &c = *reinterpret_cast<Ctl *>(tiles + NS * SS + (FP8 ? 0 : P_STAGING));
+    uint8_t *staging = tiles + NS * SS;
+    Ctl &c = *reinterpret_cast<Ctl *>(tiles + NS * SS + (FP8 ? P8_STAGING : P_STAGING));
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = cluster_ctarank();
     WaitCtl ctl{a.g1.status, a.g1.budget_ns};
@@ -1921,7 +1926,7 @@ cudaError_t launch_mega_list(const int *offp, int E, int nM, int F, int H, int T
 
 template <bool FP8>
 cudaError_t launch_mega_t(const MegaArgs &a, int grid, cudaStream_t stream) {
-    constexpr size_t smem = FP8 ? P8_STAGES * P8_STAGE + sizeof(Pair8Ctl) + 1024
+    constexpr size_t smem = FP8 ? P8_STAGES * P8_STAGE + P8_STAGING + sizeof(Pair8Ctl) + 1024
                                 : PSTAGES * P_STAGE + P_STAGING + sizeof(PairCtl) + 1024;
     static_assert(smem <= 227 * 1024, "shared memory budget");
     static_assert(sizeof(MegaArgs) <= 32764, "kernel parameter space");

@@ -810,6 +810,9 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
             !make_map_atoms(&g2.msa0, ringHs, ring_rows * (L.F / kMxBlock)) ||
             !make_map_atoms(&g2.msb0, qw + q.scales[QW_W2T], nw))
             return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        // Y rows leave through shared memory and TMA stores (64-byte swizzled 32 x 32 boxes)
+        if (!make_map_bf16_out(&g2.om0, ringY, ring_rows, L.H)) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        g2.tma_store = 1;
         g1.sfa0 = ringXs; g1.sfb0 = qw + q.scales[QW_W1T]; g1.sfb1 = qw + q.scales[QW_W3T]; g1.kstore = L.H;
         g1.q0 = ringHq; g1.qs0 = ringHs;
         g2.sfa0 = ringHs; g2.sfb0 = qw + q.scales[QW_W2T]; g2.kstore = L.F;
@@ -986,6 +989,8 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
             return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         gb2.sfa0 = u8(L.w_Ginq_s); gb2.sfb0 = qw + q.scales[QW_W2Q]; gb2.kstore = L.H;
         gb2.q0 = u8(L.w_daq); gb2.qs0 = u8(L.w_daq_s); gb2.q1 = u8(L.w_dbq); gb2.qs1 = u8(L.w_dbq_s);
+        if (!make_map_bf16_out(&gb1.om0, dXs, rp, L.H)) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        gb1.tma_store = 1;   // dX rows through shared memory and TMA stores
         gb1.sfa0 = u8(L.w_daq_s); gb1.sfa1 = u8(L.w_dbq_s);
         gb1.sfb0 = qw + q.scales[QW_W1Q]; gb1.sfb1 = qw + q.scales[QW_W3Q]; gb1.kstore = L.F;
         gw2.sfa0 = u8(L.w_hwT_s); gw2.sfb0 = u8(L.w_GinT_s); gw2.kstore = (int)rp;
