@@ -105,7 +105,8 @@ template <> struct OpTraits<OP_WG13> { static constexpr bool grouped_k = true, a
 struct TileInfo {
     int e, mt, nt;
     int g0;       // grouped-M: first global padded row of the tile
-    int seg_end;  // grouped-M: end of the tile's (macrobatch, expert) run
+    int g1;       // grouped-M CTA pairs: first row of the second CTA's 128 rows, -1 if none
+    int seg_end;  // grouped-M: end of the tile's (macrobatch, expert) run (pair lists: unused)
     int nk;       // number of BK blocks
 };
 
@@ -139,15 +140,22 @@ __device__ __forceinline__ TileInfo decode_tile(const Ctl &c, const GemmArgs &g,
         ti.mt = q % c.mt_per_group;
         ti.e = q / c.mt_per_group;
         ti.g0 = 0;
+        ti.g1 = -1;
         ti.seg_end = 0;
         ti.nk = c.krows[ti.e] / bk_elems<FP8>();
     } else {
         if (g.tiles) {
-            const int4 v = g.tiles[q];   // (first row, expert, run end, 0)
+            const int4 v = g.tiles[q];
             ti.e = v.y;
             ti.mt = 0;
             ti.g0 = v.x;
-            ti.seg_end = v.z;
+            if constexpr (TM == 2 * BM) {   // (CTA 0's rows, expert, CTA 1's rows or -1, 0)
+                ti.g1 = v.z;
+                ti.seg_end = 0x7fffffff;
+            } else {                        // (first row, expert, run end, 0)
+                ti.g1 = -1;
+                ti.seg_end = v.z;
+            }
         } else {
             int e = 0;
             while (c.prefix[e + 1] <= q) ++e;   // E <= 64
@@ -155,6 +163,7 @@ __device__ __forceinline__ TileInfo decode_tile(const Ctl &c, const GemmArgs &g,
             ti.mt = q - c.prefix[e];
             ti.g0 = c.seg_start[e] + ti.mt * TM;
             ti.seg_end = c.seg_end[e];
+            ti.g1 = (TM == 2 * BM && ti.g0 + BM < ti.seg_end) ? ti.g0 + BM : -1;
         }
         ti.nk = g.K / bk_elems<FP8>();
     }
@@ -682,9 +691,9 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
         if constexpr (PAIR) {
             if constexpr (OpTraits<OP>::grouped_k) {
                 ti.mt = ti.mt * 2 + rank;
-            } else {
-                ti.g0 += BM * rank;
-                phantom = ti.g0 >= ti.seg_end;
+            } else if (rank) {
+                phantom = ti.g1 < 0;   // no second chunk: nothing to store
+                ti.g0 = ti.g1;
             }
         }
         if (!mbar_wait(smem_u32(&tfull[acc]), acc_phase, ctl)) break;
@@ -962,10 +971,11 @@ __device__ void pair_producer_loop(const GemmArgs &g, const PairCtl &c, uint8_t 
     int ready_mb = -1;
     for (int t = blockIdx.x / 2; t < total && ok; t += gridDim.x / 2) {
         TileInfo ti = decode_tile<OP, false, 2 * BM>(c, g, t);
-        const int row0 = ti.g0 + BM * rank;              // grouped-M: this CTA's 128 rows
+        // grouped-M: this CTA's 128 rows (a second CTA without a chunk loads rows it discards)
+        const int row0 = rank ? (ti.g1 >= 0 ? ti.g1 : ti.g0 + BM) : ti.g0;
         const int m0 = (ti.mt * 2 + rank) * BM;          // grouped-K: this CTA's 128 rows of dW
         if constexpr (OP == OP_FWD1) {
-            if (g.fused && row0 < ti.seg_end) {
+            if (g.fused && (rank == 0 || ti.g1 >= 0)) {
                 const int r0 = g.offp[g.m * g.E], nrows = g.offp[(g.m + 1) * g.E] - r0;
                 const int j = (row0 - r0) / g.mb_rows;
                 if (j != ready_mb) {
@@ -1212,10 +1222,11 @@ __device__ void pair8_producer_loop(const GemmArgs &g, const Pair8Ctl &c, uint8_
     int ready_mb = -1;
     for (int t = blockIdx.x / 2; t < total && ok; t += gridDim.x / 2) {
         TileInfo ti = decode_tile<OP, true, 2 * BM>(c, g, t);
-        const int row0 = ti.g0 + BM * rank;              // grouped-M: this CTA's 128 rows
+        // grouped-M: this CTA's 128 rows (a second CTA without a chunk loads rows it discards)
+        const int row0 = rank ? (ti.g1 >= 0 ? ti.g1 : ti.g0 + BM) : ti.g0;
         const int m0 = (ti.mt * 2 + rank) * BM;          // grouped-K: this CTA's 128 rows of dW
         if constexpr (OP == OP_FWD1) {
-            if (g.fused && row0 < ti.seg_end) {
+            if (g.fused && (rank == 0 || ti.g1 >= 0)) {
                 const int r0 = g.offp[g.m * g.E], nrows = g.offp[(g.m + 1) * g.E] - r0;
                 const int j = (row0 - r0) / g.mb_rows;
                 if (j != ready_mb) {
@@ -1882,27 +1893,27 @@ __global__ void __launch_bounds__(64) mega_list_kernel(const int *offp, int E, i
     }
 }
 
-// One warp per list: warp 0 writes 128-row tiles, warp 1 256-row tiles. Runs are taken
-// 32 at a time in expert-major order (run i = expert i / nM, macrobatch i % nM); a warp
-// scan of their tile counts places each lane's tiles after those of the runs before it.
-__global__ void __launch_bounds__(64) tile_list_kernel(const int *offp, int E, int nM, int4 *list128,
+// One warp. The 128-row list: runs are taken 32 at a time in expert-major order (run i =
+// expert i / nM, macrobatch i % nM); a warp scan of their chunk counts places each lane's
+// chunks after those of the runs before it, and the first chunk of each expert is noted.
+// The pair list then takes each expert's chunks two at a time, in the same order.
+__global__ void __launch_bounds__(32) tile_list_kernel(const int *offp, int E, int nM, int4 *list128,
                                                         int4 *list256, int *counts) {
+    __shared__ int ebase[kMaxExperts + 1];   // first list128 entry of each expert
     pdl_wait();
-    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-    const int TM = warp == 0 ? 128 : 256;
-    int4 *list = warp == 0 ? list128 : list256;
+    const int lane = threadIdx.x;
     const int nseg = E * nM;
     int base = 0;
     for (int i0 = 0; i0 < nseg; i0 += 32) {
         const int i = i0 + lane;
-        int s0 = 0, s1 = 0, e = 0;
+        int s0 = 0, s1 = 0, e = 0, m = 0;
         if (i < nseg) {
             e = i / nM;
-            const int m = i - e * nM;
+            m = i - e * nM;
             s0 = offp[m * E + e];
             s1 = offp[m * E + e + 1];
         }
-        const int n = (s1 - s0 + TM - 1) / TM;
+        const int n = (s1 - s0 + BM - 1) / BM;
         int incl = n;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -1910,10 +1921,27 @@ __global__ void __launch_bounds__(64) tile_list_kernel(const int *offp, int E, i
             if (lane >= d) incl += v;
         }
         const int start = base + incl - n;
-        for (int j = 0; j < n; ++j) list[start + j] = make_int4(s0 + j * TM, e, s1, 0);
+        if (i < nseg && m == 0) ebase[e] = start;
+        for (int j = 0; j < n; ++j) list128[start + j] = make_int4(s0 + j * BM, e, s1, 0);
         base += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) counts[warp] = base;
+    if (lane == 0) {
+        ebase[E] = base;
+        counts[0] = base;
+    }
+    __syncwarp();
+    __threadfence_block();   // list128 and ebase of every lane, seen by every lane
+    __syncwarp();
+    int pbase = 0;
+    for (int e = 0; e < E; ++e) {
+        const int c0 = ebase[e], n = ebase[e + 1] - c0, pairs = (n + 1) / 2;
+        for (int p = lane; p < pairs; p += 32) {
+            const int r1 = 2 * p + 1 < n ? list128[c0 + 2 * p + 1].x : -1;
+            list256[pbase + p] = make_int4(list128[c0 + 2 * p].x, e, r1, 0);
+        }
+        pbase += pairs;
+    }
+    if (lane == 0) counts[1] = pbase;
 }
 
 }  // namespace
@@ -1959,7 +1987,7 @@ cudaError_t launch_fwd_mega(const MegaArgs &a, int grid, cudaStream_t stream, bo
 
 cudaError_t launch_tile_lists(const int *offp, int E, int nM, int4 *list128, int4 *list256, int *counts,
                               cudaStream_t stream) {
-    return launch_pdl(tile_list_kernel, dim3(1), dim3(64), 0, stream, offp, E, nM, list128, list256, counts);
+    return launch_pdl(tile_list_kernel, dim3(1), dim3(32), 0, stream, offp, E, nM, list128, list256, counts);
 }
 
 cudaError_t launch_grouped_gemm(int op, const GemmArgs &g, int grid, cudaStream_t stream, bool fp8, bool pair) {

@@ -52,10 +52,12 @@ struct GemmArgs {
     // leader's barrier: A atoms (msa0, msa1) and B atoms (msb0, msb1)
     CUtensorMap msa0, msa1, msb0, msb1;
     // grouped-M ops over every macrobatch in one launch (tiles != nullptr): the M tiles come
-    // from a list built on the device by launch_tile_lists, one int4 per tile (first padded
-    // row, expert, end of the tile's run, 0), in expert-major order (every run of expert 0,
-    // then of expert 1, ...) so that the CTAs running at one time share one expert's weights;
-    // *tile_count holds the list's length. m stays 0 (only the ring ops use it).
+    // from a list built on the device by launch_tile_lists, one int4 per tile, in expert-major
+    // order (every run of expert 0, then of expert 1, ...) so that the CTAs running at one time
+    // share one expert's weights; *tile_count holds the list's length. m stays 0 (only the ring
+    // ops use it). 1-CTA kernels read 128-row tiles (first padded row, expert, end of the run,
+    // 0), CTA pairs 256-row ones (first row of CTA 0's half, expert, first row of CTA 1's half
+    // or -1, 0): two 128-row chunks of one expert, possibly from different runs.
     const int4 *tiles;
     const int *tile_count;
     int *status;
@@ -96,9 +98,10 @@ cudaError_t launch_mega_list(const int *offp, int E, int nM, int F, int H, int T
 cudaError_t launch_fwd_mega(const MegaArgs &a, int grid, cudaStream_t stream, bool fp8);
 
 // Writes the M-tile lists of every (macrobatch, expert) run of padded rows, expert-major:
-// list128 with 128-row tiles (1-CTA kernels), list256 with 256-row tiles (CTA pairs; a
-// tile's second half may lie past its run). counts[0], counts[1] = their lengths. Each list
-// needs at most offp[nM*E] / 128 + nM*E entries.
+// list128 with the 128-row chunks of each run (1-CTA kernels), list256 with those chunks
+// taken two at a time per expert (CTA pairs; an expert's last pair may have one chunk).
+// counts[0], counts[1] = their lengths. Each list needs at most offp[nM*E] / 128 + nM*E
+// entries; E <= kMaxExperts.
 cudaError_t launch_tile_lists(const int *offp, int E, int nM, int4 *list128, int4 *list256, int *counts,
                               cudaStream_t stream);
 

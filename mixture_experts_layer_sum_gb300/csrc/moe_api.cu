@@ -60,7 +60,8 @@ struct ProfScope {
 // bf16 grouped GEMMs run as CTA pairs (cta_group::2, 256-row tiles)
 constexpr bool kPairGemm = true;
 // MXFP8 CTA pairs (block-scaled cta_group::2); the GEMM2 dgrad keeps 1-CTA tiles with eight
-// epilogue warps (its quantising SwiGLU backward)
+// epilogue warps (its quantising SwiGLU backward: CTA pairs with four or eight epilogue warps
+// measured slower)
 constexpr bool kPairGemmFp8 = true;
 inline bool pair_fp8(int op) { return kPairGemmFp8 && op != OP_BWD2; }
 constexpr int kGemmBN1 = 256;   // GEMM1 tile: 128 rows x (128 a-columns + 128 b-columns)
@@ -1041,10 +1042,11 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
             st = cuda_check(launch_tile_lists(s_offp, L.E, L.nM, l128, l256, cnt, s), "tile list launch");
         }
         if (st != MOE_OK) return st;
-        // the GEMM2 dgrad runs 1-CTA tiles of 128 rows; the GEMM1 dgrad CTA pairs of 256
-        const bool pair1 = mx ? pair_fp8(OP_BWD1) : kPairGemm;
-        gb2.tiles = l128;
-        gb2.tile_count = cnt;
+        // CTA pairs take 256-row tiles, 1-CTA kernels 128-row ones (the GEMM2 dgrad runs 1-CTA
+        // tiles in bf16 whatever kPairGemm says)
+        const bool pair2 = mx && pair_fp8(OP_BWD2), pair1 = mx ? pair_fp8(OP_BWD1) : kPairGemm;
+        gb2.tiles = pair2 ? l256 : l128;
+        gb2.tile_count = pair2 ? cnt + 1 : cnt;
         gb1.tiles = pair1 ? l256 : l128;
         gb1.tile_count = pair1 ? cnt + 1 : cnt;
     }
