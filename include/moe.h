@@ -91,10 +91,15 @@ typedef enum {
  *     0 = smallest multiple of 128 giving at least two full waves of GEMM1
  *     tiles on the device's SMs (article section 02: "at least two full SM
  *     waves per expert grouped GEMM").
- *   ring_bytes: size of the ring buffer that holds the rows of the macrobatch in
- *     flight (MXFP8: dispatched x rows, FFN hidden rows and expert outputs; bf16:
- *     hidden rows and expert outputs, the x rows going to the saved context);
- *     0 = large enough for all routed rows, i.e. one macrobatch.
+ *   ring_bytes: size of the token ring: the dispatched token rows of the
+ *     macrobatch in flight, padded to whole 128-row tiles per expert, in the
+ *     layer's compute format (MXFP8: E4M3 along H plus scales, H + H/32 bytes a
+ *     row, in the workspace; bf16: 2H bytes a row, written straight into the
+ *     saved context, which the backward reads). The macrobatch's FFN hidden rows
+ *     and expert outputs take workspace buffers of the same row count (article
+ *     section 02: a fixed-size ring of tokens, each slot reused once the experts
+ *     and the combine are done with it). 0 = large enough for all routed rows,
+ *     i.e. one macrobatch.
  *   macrobatch_tokens: tokens per macrobatch; 0 = derived from ring_bytes.
  *   timeout_ms: budget of every device-side wait; 0 = 2000 ms.
  *   num_sms: SM count used for planning; 0 = query the current device.
@@ -265,10 +270,12 @@ moe_status_t moe_reset_status(void *workspace, moe_stream_t stream);
  *     in 32 x 32 blocks of 2 KB (block (r/32, c/32) row-major, element (r, c) at
  *     ((c%32)/8*32 + r%32)*8 + c%8 inside it).
  *   workspace, valid after moe_forward until the next call on the workspace
- *   (the ring holds the last macrobatch; ring row = padded row - first padded
- *   row of that macrobatch):
- *     RING_X: dispatched x rows, bf16 [ring_rows][H] or E4M3 along H (+ _SCALES);
- *     RING_H: h rows, bf16 [ring_rows][F] or E4M3 along F (+ _SCALES).
+ *   (the last macrobatch's rows; ring row = padded row - first padded row of
+ *   that macrobatch):
+ *     RING_X: dispatched x rows, E4M3 along H [ring_rows][H] (+ _SCALES); bf16:
+ *       in saved, every macrobatch's rows at their padded rows [rows][H];
+ *     RING_H: h rows of the macrobatch, bf16 [ring_rows][F] or E4M3 along F
+ *       (+ _SCALES).
  *   workspace, valid after moe_backward until the next call on the workspace:
  *     DA, DB, HW: bf16 [rows][F] (dh.b.sigmoid'(a) terms, w.h);
  *     MXFP8 only: DY_ROWS (dout rows, E4M3 along H), DA_ROWS, DB_ROWS (E4M3

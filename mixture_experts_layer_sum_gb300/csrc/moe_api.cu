@@ -123,10 +123,14 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     const size_t xrow = mx ? (size_t)c->H + c->H / kMxBlock : 2 * (size_t)c->H;
     const size_t hrow = mx ? (size_t)c->F + c->F / kMxBlock : 2 * (size_t)c->F;
     const size_t yrow = 2 * (size_t)c->H;
-    // bf16: the fused dispatch writes the x rows straight into the saved context (the backward's
-    // dW1/dW3 reads them there), so the ring holds h and Y rows only; MXFP8: x rows quantised
-    // along H live in the ring (the weight gradient needs them along the tokens instead)
-    const size_t ring_row_bytes = (mx ? xrow : 0) + hrow + yrow;
+    // The ring holds the dispatched token rows of the macrobatch in flight, in the layer's
+    // compute format (article "O MoK do Cursor ...", section 02: a fixed-size token ring whose
+    // slots the dispatch fills and which are reused once the experts and the combine are done
+    // with them). MXFP8: E4M3 along H plus scales, in the workspace; bf16: the fused dispatch
+    // writes the rows straight into the saved context (the backward's dW1/dW3 reads them
+    // there), so the ring is a window of it. The macrobatch's FFN hidden rows and expert
+    // outputs live in buffers of the same row count.
+    const size_t ring_row_bytes = xrow;
     const int pad = (kRowPad - 1) * c->E;
     int Mb;
     if (c->macrobatch_tokens > 0) {
@@ -211,19 +215,19 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
         return fail(MOE_ERR_UNSUPPORTED, "NVFP4 weights run the forward of at most 128 tokens in one macrobatch");
     const size_t region = o;
     const size_t ring_rows = (size_t)L.half_rows * L.ring_halves;
-    // forward region: the ring
+    // forward region: the token ring (MXFP8), then the macrobatch's h and Y rows
     o = region;
     L.w_ringX = take(L.keep_x ? 0 : ring_rows * (mx ? H : 2 * H));   // kept X rows: in saved
     L.w_ringXs = mx ? take(ring_rows * (H / kMxBlock)) : 0;
+    L.ring_bytes = L.keep_x ? ring_rows * xrow : o - region;
     L.w_ringH = take(ring_rows * (mx ? F : 2 * F));
     L.w_ringHs = mx ? take(ring_rows * (F / kMxBlock)) : 0;
     L.w_ringY = take(ring_rows * 2 * H);
-    L.ring_bytes = o - region;
     const size_t fwd_end = o;
-    // backward region
+    // backward region (X rows: bf16 in saved, MXFP8 only along the tokens; dout rows: bf16 only,
+    // MXFP8 gathers them straight into its two quantised copies)
     o = region;
-    L.w_Xs = take(rp * 2 * H);
-    L.w_Gin = take(rp * 2 * H);
+    L.w_Gin = take(mx ? 0 : rp * 2 * H);
     L.w_da = take(rp * 2 * F);
     L.w_db = take(rp * 2 * F);
     L.w_hw = take(rp * 2 * F);
@@ -605,7 +609,7 @@ moe_status_t moe_quantize_weights(const moe_config_t *cfg, const void *W1, const
         MxTransposeArgs a{};
         a.src = (const bf16 *)t.src; a.codes = qw + q.codes[t.idx]; a.scales = qw + q.scales[t.idx];
         a.R = t.R; a.C = t.C; a.r_limit_ptr = nullptr;
-        st = cuda_check(launch_mx_transpose(a, E, s), "weight transpose-quantise launch");
+        st = cuda_check(launch_mx_transpose(a, E, sms, s), "weight transpose-quantise launch");
         if (st != MOE_OK) return st;
     }
     // row-wise copies (contraction axis = columns of the stored weight)
@@ -921,26 +925,20 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
     const int32_t *s_row_slot = at<int32_t>(saved, L.s_row_slot);
     const bf16 *s_a = at<bf16>(saved, L.s_a);
     const bf16 *s_b = at<bf16>(saved, L.s_b);
-    bf16 *Xs = L.keep_x ? const_cast<bf16 *>(at<bf16>(saved, L.s_xs)) : at<bf16>(ws, L.w_Xs);
+    // bf16: the X rows the forward's dispatch kept in saved (no replay); MXFP8 gathers X along
+    // the tokens from x instead (the dW1/dW3 operand is quantised along the other axis)
+    const bf16 *Xs = L.keep_x ? at<bf16>(saved, L.s_xs) : nullptr;
     bf16 *Gin = at<bf16>(ws, L.w_Gin), *dA = at<bf16>(ws, L.w_da),
          *dB = at<bf16>(ws, L.w_db), *HW = at<bf16>(ws, L.w_hw), *dXs = at<bf16>(ws, L.w_dXs);
     float *dwpart = at<float>(ws, L.w_dwpart), *dlogits = at<float>(ws, L.w_dlogits);
     const size_t rp = L.rows_pad_max;
 
-    // 1. replay dispatch (X rows; not needed when the forward's rows were kept) and
-    //    reverse combine (dout rows), all macrobatches (bf16 path; the MXFP8 path
-    //    gathers straight into its quantised operands)
+    // 1. reverse combine (dout rows), all macrobatches (bf16 path; the MXFP8 path gathers
+    //    straight into its quantised operands)
     if (L.T > 0 && !mx) {
-        DispatchArgs d1{};
-        d1.src = (const bf16 *)x; d1.dst = Xs; d1.row_slot = s_row_slot; d1.offp = s_offp;
-        d1.beg = 0; d1.end = L.nM * L.E; d1.dst_row0 = 0; d1.H = L.H; d1.k = L.k;
-        if (!L.keep_x) {
-            ProfScope ps("dispatch_replay", s);
-            st = cuda_check(launch_dispatch(d1, L.rows_pad_max, L.num_sms, s), "replay dispatch launch");
-        }
-        if (st != MOE_OK) return st;
-        DispatchArgs d2 = d1;
-        d2.src = (const bf16 *)dout; d2.dst = Gin;
+        DispatchArgs d2{};
+        d2.src = (const bf16 *)dout; d2.dst = Gin; d2.row_slot = s_row_slot; d2.offp = s_offp;
+        d2.beg = 0; d2.end = L.nM * L.E; d2.dst_row0 = 0; d2.H = L.H; d2.k = L.k;
         {
             ProfScope ps("reverse_combine", s);
             st = cuda_check(launch_dispatch(d2, L.rows_pad_max, L.num_sms, s), "reverse combine launch");
@@ -1012,7 +1010,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
             a.offp = s_offp; a.ilv_E = L.E; a.ilv_nseg = L.nM * L.E; a.ilv_jb = seg_rows_max / kRowPad;
         }
         ProfScope ps(name, s);
-        return cuda_check(launch_mx_transpose(a, 1, s), "token-axis quantise launch");
+        return cuda_check(launch_mx_transpose(a, 1, L.num_sms, s), "token-axis quantise launch");
     };
     if (mx && L.T > 0) {
         // dY rows gathered from dout (reverse combine) quantised along H for the GEMM2 dgrad and,

@@ -57,7 +57,7 @@ struct Layout {
     int tile_list_max;                              // entries each list can hold
     int mb_rows;            // minibatch rows used by the fused dispatch (multiple of 128)
     size_t w_ringX, w_ringXs, w_ringH, w_ringHs, w_ringY, ring_bytes;   // forward
-    size_t w_Xs, w_Gin, w_da, w_db, w_hw, w_dXs, w_dwpart, w_dlogits, w_dwr_part;   // backward
+    size_t w_Gin, w_da, w_db, w_hw, w_dXs, w_dwpart, w_dlogits, w_dwr_part;   // backward
     // backward, MXFP8 only: quantised operands (codes, scale atoms)
     size_t w_Ginq, w_Ginq_s, w_daq, w_daq_s, w_dbq, w_dbq_s;       // along H / F (row-wise)
     size_t w_GinT, w_GinT_s, w_XsT, w_XsT_s, w_hwT, w_hwT_s, w_daT, w_daT_s, w_dbT, w_dbT_s;   // along rows

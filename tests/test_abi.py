@@ -158,13 +158,13 @@ def test_buffer_locations_lie_inside_their_buffers(moe):
 
 
 def test_ring_holds_one_macrobatch(moe):
-    # the macrobatch is the largest token count whose padded rows (MXFP8: dispatched x, h and
-    # expert output rows; bf16: h and Y, x going to the saved context), in whole 128-row tiles,
-    # fit the ring once (less 8 KiB for buffer alignment); a kernel never overlaps its
-    # predecessor on the stream, so one macrobatch is in flight at a time
+    # the macrobatch is the largest token count whose padded rows of dispatched tokens (MXFP8:
+    # E4M3 along H plus scales; bf16: 2H bytes), in whole 128-row tiles, fit the ring once
+    # (less 8 KiB for buffer alignment); a kernel never overlaps its predecessor on the stream,
+    # so one macrobatch is in flight at a time
     H, F, E, k = 7168, 2048, 16, 8
     pad = 127 * E
-    for prec, row in (("mxfp8", (H + H // 32) + (F + F // 32) + 2 * H), ("bf16", 2 * F + 2 * H)):
+    for prec, row in (("mxfp8", H + H // 32), ("bf16", 2 * H)):
         cfg = moe.make_config(16384, H, F, E, k, prec, ring_bytes=256 << 20, num_sms=152)
         p = moe.moe_plan(cfg)
         cap = ((256 << 20) - 8192) // row // 128 * 128
