@@ -135,12 +135,14 @@ def bf16_rows(t: torch.Tensor, rows, cols) -> np.ndarray:
     return O.bf16_to_f64(u8(t)[:2 * rows * cols].view(np.uint16).reshape(rows, cols))
 
 
-def bf16_blocks(t: torch.Tensor, rows, cols) -> np.ndarray:
+def bf16_blocks(t: torch.Tensor, rows, cols, keep=None) -> np.ndarray:
     """bf16 [rows][cols] stored in 32 x 32 blocks of 2 KB (block (r/32, c/32) row-major; element
-    (r, c) at ((c % 32) / 8 * 32 + r % 32) * 8 + c % 8 inside it) -> float64 [rows, cols]."""
+    (r, c) at ((c % 32) / 8 * 32 + r % 32) * 8 + c % 8 inside it) -> float64 [keep, cols] (the
+    first keep rows, default all; rows past the written ones are never converted)."""
     v = u8(t)[:2 * rows * cols].view(np.uint16).reshape(rows // 32, cols // 32, 4, 32, 8)
     # axes: block row, block col, c/8 within block, r within block, c%8
-    return O.bf16_to_f64(v.transpose(0, 3, 1, 2, 4).reshape(rows, cols))
+    keep = rows if keep is None else keep
+    return O.bf16_to_f64(v.transpose(0, 3, 1, 2, 4).reshape(rows, cols)[:keep])
 
 
 def check_mx_decided(codes, scales, ref, axis, rel):

@@ -67,8 +67,8 @@ def test_mxfp8_activation_bytes_match_oracle_quantiser(T):
     np.testing.assert_array_equal(codes, rc, err_msg="x codes")
 
     # GEMM1's h along F, from the GPU's saved bf16 a, b
-    a = g.bf16_blocks(layer.buffer("A"), rp, F)[:end]
-    b = g.bf16_blocks(layer.buffer("B"), rp, F)[:end]
+    a = g.bf16_blocks(layer.buffer("A"), rp, F, end)
+    b = g.bf16_blocks(layer.buffer("B"), rp, F, end)
     h64 = O.silu(a) * b
     hc = g.u8(layer.buffer("RING_H"))[:end * F].reshape(end, F)
     hs = g.atoms_to_rows(g.u8(layer.buffer("RING_H_SCALES")), end, F)
