@@ -609,7 +609,7 @@ moe_status_t moe_quantize_weights(const moe_config_t *cfg, const void *W1, const
         MxTransposeArgs a{};
         a.src = (const bf16 *)t.src; a.codes = qw + q.codes[t.idx]; a.scales = qw + q.scales[t.idx];
         a.R = t.R; a.C = t.C; a.r_limit_ptr = nullptr;
-        st = cuda_check(launch_mx_transpose(a, E, sms, s), "weight transpose-quantise launch");
+        st = cuda_check(launch_mx_transpose(a, E, s), "weight transpose-quantise launch");
         if (st != MOE_OK) return st;
     }
     // row-wise copies (contraction axis = columns of the stored weight)
@@ -1010,7 +1010,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
             a.offp = s_offp; a.ilv_E = L.E; a.ilv_nseg = L.nM * L.E; a.ilv_jb = seg_rows_max / kRowPad;
         }
         ProfScope ps(name, s);
-        return cuda_check(launch_mx_transpose(a, 1, L.num_sms, s), "token-axis quantise launch");
+        return cuda_check(launch_mx_transpose(a, 1, s), "token-axis quantise launch");
     };
     if (mx && L.T > 0) {
         // dY rows gathered from dout (reverse combine) quantised along H for the GEMM2 dgrad and,
