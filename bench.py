@@ -495,6 +495,52 @@ def e2e_ms(g, steps):
     return run(steps)
 
 
+def decode_entries(args, dev, rank, M, MoeLayer, torch, flush):
+    """Decode-sized forward (64 tokens of the balanced shape), bf16 and NVFP4 weights: every
+    expert's weights stream once, so the floor is their bytes at the HBM copy bandwidth."""
+    out = []
+    for prec in ("bf16", "nvfp4"):
+        wd = WL.BALANCED.with_(T=64, precision=prec, name=f"{WL.BALANCED.name}@T64/{prec}")
+        gd = Gpu(wd, dev, rank, M, MoeLayer, torch)
+        with torch.cuda.stream(gd.stream):
+            for _ in range(args.warmup):
+                gd.fwd()
+        t_fwd = timed(gd, flush, gd.fwd, args.steps)
+        M.moe_profile_begin()
+        timed(gd, flush, gd.fwd, args.steps)
+        kern = M.moe_profile_end()
+        gd.layer.status(gd.stream)
+        hbm_d = load_peaks()[0]["hbm_gbs"]
+        wbytes = kernel_bytes(wd, "decode_ffn") * (1.0 if prec == "bf16" else (0.5 + 1 / 16) / 2)
+        floor_us = wbytes / (hbm_d * 1e9) * 1e6
+        dk = {nm: ms_ / args.steps * 1e3 for nm, _, ms_ in kern}
+        kname = "decode_ffn" if prec == "bf16" else "decode_ffn_nvfp4"
+        out.append({
+            "workload": wd.name, "precision": prec, "T": wd.T, "H": wd.H, "F": wd.F, "E": wd.E, "k": wd.k,
+            "fwd": {"value": wd.T * args.steps / (t_fwd * 1e-3), "unit": "tokens/s",
+                    "us_per_step": t_fwd / args.steps * 1e3},
+            "weight_bytes": wbytes, "weight_stream_floor_us": floor_us,
+            "fwd_over_floor": t_fwd / args.steps * 1e3 / floor_us,
+            kname: {"us": dk.get(kname), "frac_of_hbm": floor_us / dk[kname] if dk.get(kname) else None},
+            "kernels_us": dk})
+        del gd
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_decode_only(args):
+    """Only the decode entries (one GPU): a short command for profiling the decode kernels."""
+    import torch
+    torch.cuda.set_device(0)
+    from mixture_experts_layer_sum_gb300 import build_ext
+    build_ext.build()
+    import mixture_experts_layer_sum_gb300.moe as M
+    from mixture_experts_layer_sum_gb300.layer import MoeLayer
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    print(json.dumps({"decode": decode_entries(args, dev, 0, M, MoeLayer, torch, flush)}))
+
+
 def run_ours(args, w):
     import torch
     ws, rank, local = dist_env()
@@ -608,34 +654,7 @@ def run_ours(args, w):
                             for r in rows]})
             del go
             torch.cuda.empty_cache()
-        # decode-sized forward (few tokens of the balanced shape), bf16 and NVFP4 weights: every
-        # expert's weights stream once, so the floor is their bytes at the HBM copy bandwidth
-        for prec in ("bf16", "nvfp4"):
-            wd = WL.BALANCED.with_(T=64, precision=prec, name=f"{WL.BALANCED.name}@T64/{prec}")
-            gd = Gpu(wd, dev, rank, M, MoeLayer, torch)
-            with torch.cuda.stream(gd.stream):
-                for _ in range(args.warmup):
-                    gd.fwd()
-            t_fwd = timed(gd, flush, gd.fwd, args.steps)
-            M.moe_profile_begin()
-            timed(gd, flush, gd.fwd, args.steps)
-            kern = M.moe_profile_end()
-            gd.layer.status(gd.stream)
-            hbm_d = load_peaks()[0]["hbm_gbs"]
-            wbytes = kernel_bytes(wd, "decode_ffn") * (1.0 if prec == "bf16" else (0.5 + 1 / 16) / 2)
-            floor_us = wbytes / (hbm_d * 1e9) * 1e6
-            dk = {nm: ms_ / args.steps * 1e3 for nm, _, ms_ in kern}
-            kname = "decode_ffn" if prec == "bf16" else "decode_ffn_nvfp4"
-            others.append({
-                "workload": wd.name, "precision": prec, "T": wd.T, "H": wd.H, "F": wd.F, "E": wd.E, "k": wd.k,
-                "fwd": {"value": wd.T * args.steps / (t_fwd * 1e-3), "unit": "tokens/s",
-                        "us_per_step": t_fwd / args.steps * 1e3},
-                "weight_bytes": wbytes, "weight_stream_floor_us": floor_us,
-                "fwd_over_floor": t_fwd / args.steps * 1e3 / floor_us,
-                kname: {"us": dk.get(kname), "frac_of_hbm": floor_us / dk[kname] if dk.get(kname) else None},
-                "kernels_us": dk})
-            del gd
-            torch.cuda.empty_cache()
+        others += decode_entries(args, dev, rank, M, MoeLayer, torch, flush)
         inp = headline_inp
     else:
         inp = g.inp
@@ -704,6 +723,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0, help="override T (small cases for ncu captures)")
     ap.add_argument("--experts", type=int, default=0, help="override E, keeping k <= E (small cases for ncu captures)")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time only the 64-token decode forward (bf16 and NVFP4 weights) and print it")
     ap.add_argument("--minibatch-sweep", action="store_true",
                     help="also time fwd and fwd+bwd for each minibatch size of the workload (ring workload)")
     args = ap.parse_args()
@@ -713,7 +734,9 @@ def main():
         w = w.with_(T=args.tokens, name=f"{w.name}@T{args.tokens}")
     if args.experts:
         w = w.with_(E=args.experts, k=min(w.k, args.experts), name=f"{w.name}@E{args.experts}")
-    if args.impl == "reference":
+    if args.decode_only:
+        run_decode_only(args)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_ours(args, w)

@@ -65,7 +65,7 @@ def test_persistent_equals_per_stage_balanced_full_size():
 
 
 def test_persistent_equals_per_stage_ring_full_size():
-    # 15 macrobatches through the 256 MiB ring: every hand-off between macrobatches
+    # four macrobatches through the 256 MiB token ring: every hand-off between macrobatches
     w = WL.RING
     p = both_modes(w, WL.make_inputs(w), backward=False, ring_bytes=w.ring_bytes)
     assert p["layer"].plan.num_macrobatches > 2
