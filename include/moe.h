@@ -277,7 +277,8 @@ moe_status_t moe_reset_status(void *workspace, moe_stream_t stream);
  *     RING_H: h rows of the macrobatch, bf16 [ring_rows][F] or E4M3 along F
  *       (+ _SCALES).
  *   workspace, valid after moe_backward until the next call on the workspace:
- *     DA, DB, HW: bf16 [rows][F] (dh.b.sigmoid'(a) terms, w.h);
+ *     DA, DB, HW: bf16 [rows][F] (dh.b.sigmoid'(a) terms, w.h), bf16 configurations
+ *     only (MXFP8 quantises them straight into DA/DB/HW_TOKENS);
  *     MXFP8 only: DY_ROWS (dout rows, E4M3 along H), DA_ROWS, DB_ROWS (E4M3
  *     along F), each [rows][K] + _SCALES; X_TOKENS, DY_TOKENS (E4M3 [H][rows]
  *     along the rows) and HW_TOKENS, DA_TOKENS, DB_TOKENS ([F][rows]), + _SCALES. */

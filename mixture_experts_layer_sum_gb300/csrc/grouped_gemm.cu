@@ -54,6 +54,11 @@ constexpr int BK8 = 128;                        // K elements per stage, e4m3
 
 template <bool FP8> __host__ __device__ constexpr uint32_t stage_stride() { return FP8 ? STAGE_STRIDE_FP8 : STAGE_BYTES; }
 constexpr uint32_t P_STAGING_1 = 4 * 8192;   // epilogue staging of the 1-CTA bf16 kernel
+// epilogue staging of the 1-CTA kernels: bf16 TMA-store buffers; the MXFP8 GEMM2 dgrad's
+// token-axis transposition (eight warps x 2 KB); none otherwise
+template <int OP, bool FP8> __host__ __device__ constexpr uint32_t staging_bytes() {
+    return FP8 ? (OP == OP_BWD2 ? 8 * 2048 : 0) : P_STAGING_1;
+}
 template <bool FP8> __host__ __device__ constexpr int bk_elems() { return FP8 ? BK8 : BK; }
 
 // D[tmem] (+)= A[smem] * B[smem], e4m3 x e4m3 with E8M0 block scales read from
@@ -571,6 +576,34 @@ __device__ __forceinline__ void stage_store_blk(uint8_t *warp_stage, int &nstore
 // Epilogue of one GEMM1 tile (this thread's accumulator row r): a, b rounded to bf16 and saved
 // in 32 x 32 blocks at the global padded rows, h = silu(a) * b from the rounded a, b into the ring
 // (bf16, or E4M3 along F with its scale bytes).
+// One warp's 32 rows x 32 columns of bf16 values (lane = row, w = its 32 columns packed)
+// quantised along the rows: MXFP8 blocks of 32 padded rows (the token axis of a weight-gradient
+// operand [C][R]). The tile passes through a 2 KB staging buffer (16-byte chunks XOR-swizzled as
+// in stage_store_bf16, so both the row writes and the column reads are free of bank conflicts);
+// lane c then holds column col0 + c whole and writes its 32 codes as one sector and its scale
+// byte. The arithmetic is mx_quant32 on the bf16 values, the same bytes the standalone
+// token-axis quantiser makes from those values.
+__device__ __forceinline__ void token_axis_q32(uint8_t *stage, const uint32_t (&w)[16], uint8_t *codes,
+                                               uint8_t *scales, int col0, int row0, int R, int lane) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4 *>(stage + lane * 64 + ((q ^ ((lane >> 1) & 3)) * 16)) =
+            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    __syncwarp();
+    float v[32];
+    const int cq = lane >> 3, ce = (lane & 7) * 2;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+        const uint32_t b = *reinterpret_cast<const uint16_t *>(stage + r * 64 + ((cq ^ ((r >> 1) & 3)) * 16) + ce);
+        v[r] = __uint_as_float(b << 16);
+    }
+    __syncwarp();   // the buffer is free for the next tile
+    uint32_t cw[8];
+    const uint32_t sb = mx_quant32(v, cw);
+    st_global_32B(codes + (size_t)(col0 + lane) * R + row0, cw);
+    scales[mx_sf_offset((size_t)(col0 + lane), (size_t)row0, (size_t)R)] = (uint8_t)sb;
+}
+
 template <bool FP8, int NBUF>
 __device__ __forceinline__ void epi_fwd1_tile(const GemmArgs &g, const TileInfo &ti, uint32_t tbase, int r,
                                               int quarter, int lane, int ring_shift, bool tma_bf16,
@@ -682,7 +715,9 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
     // GEMM2 / GEMM1-dgrad rows (the quantised outputs are stored from registers)
     const bool tma_bf16 = staging != nullptr && g.tma_store && OP != OP_WG2 && OP != OP_WG13 &&
                           (!FP8 || OP == OP_FWD2 || OP == OP_BWD1);
-    uint8_t *warp_stage = staging ? staging + (warp - 2) * (NBUF * 2048) : nullptr;
+    // MXFP8 GEMM2 dgrad: one 2 KB buffer per warp for the token-axis transposition
+    constexpr uint32_t kWarpStage = (FP8 && OP == OP_BWD2) ? 2048 : NBUF * 2048;
+    uint8_t *warp_stage = staging ? staging + (warp - 2) * kWarpStage : nullptr;
     const int t0 = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
     const int tstep = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
     for (int t = t0; t < total; t += tstep) {
@@ -784,6 +819,13 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                     dq[0] = make_uint4(q[0], q[1], q[2], q[3]);
                     dq[1] = make_uint4(q[4], q[5], q[6], q[7]);
                     g.qs1[mx_sf_offset(grow, col, F)] = (uint8_t)sb;
+                    // the bf16 da, db and h.w quantised along the padded rows for dW1/dW3 and dW2
+                    // (a warp's 32 rows are one block: runs start at multiples of 128 rows)
+                    const int row0 = ti.g0 + quarter * 32, col0 = ti.nt * BN + cc * 32;
+                    token_axis_q32(warp_stage, oda, g.tq[0], g.tqs[0], col0, row0, g.tR, lane);
+                    token_axis_q32(warp_stage, odb, g.tq[1], g.tqs[1], col0, row0, g.tR, lane);
+                    token_axis_q32(warp_stage, ohw, g.tq[2], g.tqs[2], col0, row0, g.tR, lane);
+                    continue;
                 }
                 if (tma_bf16) {
                     const int row0 = ti.g0 + quarter * 32, col0 = ti.nt * BN + cc * 32;
@@ -891,8 +933,9 @@ template <int OP, bool FP8>
 __global__ void __launch_bounds__(320, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *staging = FP8 ? nullptr : tiles + STAGES * stage_stride<FP8>();   // bf16: 32 KB over the epilogue warps
-    SmemCtl &c = *reinterpret_cast<SmemCtl *>(tiles + STAGES * stage_stride<FP8>() + (FP8 ? 0 : P_STAGING_1));
+    // bf16: 32 KB over the epilogue warps; MXFP8 GEMM2 dgrad: 2 KB per epilogue warp
+    uint8_t *staging = staging_bytes<OP, FP8>() ? tiles + STAGES * stage_stride<FP8>() : nullptr;
+    SmemCtl &c = *reinterpret_cast<SmemCtl *>(tiles + STAGES * stage_stride<FP8>() + staging_bytes<OP, FP8>());
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     WaitCtl ctl{g.status, g.budget_ns};
 
@@ -1450,7 +1493,7 @@ cudaError_t launch_pair8(const GemmArgs &g, int grid, cudaStream_t stream) {
 
 template <int OP, bool FP8>
 cudaError_t launch_op(const GemmArgs &g, int grid, cudaStream_t stream) {
-    constexpr size_t smem = STAGES * stage_stride<FP8>() + (FP8 ? 0 : P_STAGING_1) + sizeof(SmemCtl) + 1024;
+    constexpr size_t smem = STAGES * stage_stride<FP8>() + staging_bytes<OP, FP8>() + sizeof(SmemCtl) + 1024;
     static_assert(smem <= 227 * 1024, "shared memory budget");
     cudaError_t err =
         cudaFuncSetAttribute(grouped_gemm_kernel<OP, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -33,6 +33,10 @@ struct GemmArgs {
     const uint8_t *sfa0, *sfa1, *sfb0, *sfb1;
     int kstore;
     uint8_t *q0, *q1, *qs0, *qs1;  // FWD1: h codes/scales (ring); BWD2: da, db codes/scales
+    // BWD2, MXFP8: da, db and h.w quantised along the padded rows ([F][tR] codes + scale atoms,
+    // 32-row blocks), the weight gradients' operands
+    uint8_t *tq[3], *tqs[3];
+    int tR;
     // FWD1 with the dispatch fused in (fused = 1): warps 6-9 of every CTA
     // claim 4-row chunks of the macrobatch from a counter, gather them into the
     // ring (bf16, or MXFP8 along H) and add the rows to ready[j] of their

@@ -228,9 +228,11 @@ moe_status_t make_layout(const moe_config_t *c, Layout &L) {
     // MXFP8 gathers them straight into its two quantised copies)
     o = region;
     L.w_Gin = take(mx ? 0 : rp * 2 * H);
-    L.w_da = take(rp * 2 * F);
-    L.w_db = take(rp * 2 * F);
-    L.w_hw = take(rp * 2 * F);
+    // bf16 da, db, h.w rows: the bf16 weight gradients' operands (MXFP8 writes them quantised
+    // along the rows straight from the GEMM2 dgrad epilogue instead)
+    L.w_da = take(mx ? 0 : rp * 2 * F);
+    L.w_db = take(mx ? 0 : rp * 2 * F);
+    L.w_hw = take(mx ? 0 : rp * 2 * F);
     L.w_dXs = take(rp * 2 * H);
     L.w_dwpart = take(4 * rp * (F / 128));
     L.w_dlogits = take(4 * T * E);
@@ -514,7 +516,7 @@ moe_status_t moe_buffer_location(const moe_config_t *cfg, int which, int *in_sav
     const bool mx = L.precision == MOE_PRECISION_MXFP8;
     const size_t rp = L.rows_pad_max, H = L.H, F = L.F;
     const size_t ring_rows = (size_t)L.half_rows * L.ring_halves;
-    struct Loc { int saved; size_t off, bytes; bool mx_only; };
+    struct Loc { int saved; size_t off, bytes; int only; };   // only: 1 MXFP8, 2 bf16 configurations
     Loc loc{};
     switch (which) {
         case MOE_BUF_PADDED_OFFSETS: loc = {1, L.s_offp, 4 * ((size_t)L.nM * L.E + 1), false}; break;
@@ -527,9 +529,9 @@ moe_status_t moe_buffer_location(const moe_config_t *cfg, int which, int *in_sav
         case MOE_BUF_RING_X_SCALES: loc = {0, L.w_ringXs, ring_rows * H / kMxBlock, true}; break;
         case MOE_BUF_RING_H: loc = {0, L.w_ringH, ring_rows * (mx ? F : 2 * F), false}; break;
         case MOE_BUF_RING_H_SCALES: loc = {0, L.w_ringHs, ring_rows * F / kMxBlock, true}; break;
-        case MOE_BUF_DA: loc = {0, L.w_da, 2 * rp * F, false}; break;
-        case MOE_BUF_DB: loc = {0, L.w_db, 2 * rp * F, false}; break;
-        case MOE_BUF_HW: loc = {0, L.w_hw, 2 * rp * F, false}; break;
+        case MOE_BUF_DA: loc = {0, L.w_da, 2 * rp * F, 2}; break;
+        case MOE_BUF_DB: loc = {0, L.w_db, 2 * rp * F, 2}; break;
+        case MOE_BUF_HW: loc = {0, L.w_hw, 2 * rp * F, 2}; break;
         case MOE_BUF_DY_ROWS: loc = {0, L.w_Ginq, rp * H, true}; break;
         case MOE_BUF_DY_ROWS_SCALES: loc = {0, L.w_Ginq_s, rp * H / kMxBlock, true}; break;
         case MOE_BUF_DA_ROWS: loc = {0, L.w_daq, rp * F, true}; break;
@@ -548,7 +550,8 @@ moe_status_t moe_buffer_location(const moe_config_t *cfg, int which, int *in_sav
         case MOE_BUF_DB_TOKENS_SCALES: loc = {0, L.w_dbT_s, rp * F / kMxBlock, true}; break;
         default: return fail(MOE_ERR_INVALID_ARG, "unknown buffer");
     }
-    if (loc.mx_only && !mx) return fail(MOE_ERR_UNSUPPORTED, "buffer exists in MXFP8 configurations only");
+    if (loc.only == 1 && !mx) return fail(MOE_ERR_UNSUPPORTED, "buffer exists in MXFP8 configurations only");
+    if (loc.only == 2 && mx) return fail(MOE_ERR_UNSUPPORTED, "buffer exists in bf16 configurations only");
     *in_saved = loc.saved;
     *offset = loc.off;
     *bytes = loc.bytes;
@@ -988,6 +991,8 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
             return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         gb2.sfa0 = u8(L.w_Ginq_s); gb2.sfb0 = qw + q.scales[QW_W2Q]; gb2.kstore = L.H;
         gb2.q0 = u8(L.w_daq); gb2.qs0 = u8(L.w_daq_s); gb2.q1 = u8(L.w_dbq); gb2.qs1 = u8(L.w_dbq_s);
+        gb2.tq[0] = u8(L.w_daT); gb2.tqs[0] = u8(L.w_daT_s); gb2.tq[1] = u8(L.w_dbT); gb2.tqs[1] = u8(L.w_dbT_s);
+        gb2.tq[2] = u8(L.w_hwT); gb2.tqs[2] = u8(L.w_hwT_s); gb2.tR = (int)rp;
         if (!make_map_bf16_out(&gb1.om0, dXs, rp, L.H)) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         gb1.tma_store = 1;   // dX rows through shared memory and TMA stores
         gb1.sfa0 = u8(L.w_daq_s); gb1.sfa1 = u8(L.w_dbq_s);
@@ -1056,11 +1061,6 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
                 st = cuda_check(launch_grouped_gemm(OP_BWD2, gb2, L.num_sms, s, mx, mx ? pair_fp8(OP_BWD2) : kPairGemm), "GEMM2 dgrad launch");
             }
             if (st != MOE_OK) return st;
-        }
-        if (mx) {
-            if ((st = transpose_q(HW, L.w_hwT, L.w_hwT_s, L.F, "quantize_hw_tokens")) != MOE_OK) return st;
-            if ((st = transpose_q(dA, L.w_daT, L.w_daT_s, L.F, "quantize_da_tokens")) != MOE_OK) return st;
-            if ((st = transpose_q(dB, L.w_dbT, L.w_dbT_s, L.F, "quantize_db_tokens")) != MOE_OK) return st;
         }
         for (int m = 0; m < dgrad_launches; ++m) {
             gb1.m = m;

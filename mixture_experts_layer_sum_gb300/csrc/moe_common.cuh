@@ -140,6 +140,13 @@ __device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float 
     return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
+// One 32-byte global store (a whole sector); p 32-byte aligned.
+__device__ __forceinline__ void st_global_32B(void *p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // Quantises 32 values held by one thread: 8 words of codes, returns the scale byte.
 __device__ __forceinline__ uint32_t mx_quant32(const float (&v)[32], uint32_t (&codes)[8]) {
     float amax = 0.0f;

@@ -67,13 +67,6 @@ __device__ __forceinline__ uint32_t e4m3x4_row(uint32_t w0, uint32_t w1, uint16_
     return d;
 }
 
-// One 32-byte global store (a whole sector); p 32-byte aligned.
-__device__ __forceinline__ void st_global_32B(void *p, const uint32_t (&w)[8]) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
-                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                 : "memory");
-}
-
 // ---------------------------------------------------------------- rows
 // Warp per destination row, in chunks of 1024 elements (32 blocks). The warp
 // loads a chunk with coalesced 16-byte vectors (the next chunk's loads go out

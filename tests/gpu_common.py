@@ -145,14 +145,21 @@ def bf16_blocks(t: torch.Tensor, rows, cols, keep=None) -> np.ndarray:
     return O.bf16_to_f64(v.transpose(0, 3, 1, 2, 4).reshape(rows, cols)[:keep])
 
 
-def check_mx_decided(codes, scales, ref, axis, rel):
+def bf16_round(v) -> np.ndarray:
+    """float64 -> bf16 values as float64, through fp32 (each step to nearest even; monotone)."""
+    return WL.bf16_bits_to_f32(WL.f32_to_bf16_bits(np.asarray(v, np.float32))).astype(np.float64)
+
+
+def check_mx_decided(codes, scales, ref, axis, rel, bf16_values=False):
     """MXFP8 bytes the GPU made from values that agree with the float64 `ref` to within `rel`
     of their block maximum (its own arithmetic differs in rounding only). Where the block
     maximum is farther than rel from a scale boundary, the scale byte must be the oracle
     quantiser's; at the GPU's scale, an element whose value cannot cross a rounding midpoint
     within that error must carry the oracle's code; an element that can must lie between the
-    roundings of the two ends of its error interval (rounding is monotone). Returns (undecided
-    scales, undecided codes) counts."""
+    roundings of the two ends of its error interval (rounding is monotone). bf16_values: the
+    GPU rounded its values to bf16 before quantising them, so the interval ends are rounded the
+    same way and the scale test allows the bf16 step too. Returns (undecided scales, undecided
+    codes) counts."""
     rc, rs = O.mx_quantize(ref, axis)
     mv = lambda a: np.moveaxis(np.asarray(a), axis, -1)
     refm, gc, gs, rsm = mv(ref), mv(codes), mv(scales).astype(np.int64), mv(rs).astype(np.int64)
@@ -161,15 +168,43 @@ def check_mx_decided(codes, scales, ref, axis, rel):
     amax = np.abs(blk).max(-1)
     s = rsm - 127
     hi, lo = 448.0 * np.exp2(s), 448.0 * np.exp2(s - 1)
-    near = (np.abs(amax - hi) <= rel * hi) | (np.abs(amax - lo) <= rel * lo)
+    rs_ = rel + (2.0 ** -8 if bf16_values else 0.0)
+    near = (np.abs(amax - hi) <= rs_ * hi) | (np.abs(amax - lo) <= rs_ * lo)
     near &= amax > 0
     assert (gs[~near] == rsm[~near]).all(), "scale bytes differ away from a scale boundary"
     gscale = np.exp2(gs.astype(np.float64) - 127)[..., None]
     scaled = blk / gscale
     dev = (rel * amax)[..., None] / gscale
-    q_lo, q_hi = O.e4m3_round(scaled - dev), O.e4m3_round(scaled + dev)
+    pre = bf16_round if bf16_values else (lambda a: a)
+    q_lo, q_hi = O.e4m3_round(pre(scaled - dev)), O.e4m3_round(pre(scaled + dev))
     got = O.e4m3_decode(gc.reshape(blk.shape))
     decided = q_lo == q_hi
     assert (got[decided] == q_lo[decided]).all(), "codes differ where the reference decides them"
     assert ((got >= q_lo) & (got <= q_hi)).all(), "a code lies outside the reference's interval"
     return int(near.sum()), int((~decided).sum())
+
+
+def check_mx_interval(codes, scales, lo, hi, axis):
+    """MXFP8 bytes of values known only to lie in [lo, hi] elementwise (lo <= hi, both float64,
+    every rounding the GPU applies before quantising already taken into the ends). Where every
+    value of the interval gives one scale byte, the GPU's must be it, and it must lie between
+    the bytes of the interval's smallest and largest block maxima; at the GPU's scale every code
+    must lie between the roundings of its interval's ends (rounding is monotone). Returns
+    (undecided scales, undecided codes) counts."""
+    mv = lambda a: np.moveaxis(np.asarray(a), axis, -1)
+    lo_m, hi_m, gc, gs = mv(lo), mv(hi), mv(codes), mv(scales).astype(np.int64)
+    n = lo_m.shape[-1]
+    shp = lo_m.shape[:-1] + (n // 32, 32)
+    lo_b, hi_b = lo_m.reshape(shp), hi_m.reshape(shp)
+    assert (lo_b <= hi_b).all()
+    same_sign = (lo_b > 0) | (hi_b < 0)
+    mag_lo = np.where(same_sign, np.minimum(np.abs(lo_b), np.abs(hi_b)), 0.0).max(-1)
+    mag_hi = np.maximum(np.abs(lo_b), np.abs(hi_b)).max(-1)
+    s_lo, s_hi = O.mx_scale_exponent(mag_lo), O.mx_scale_exponent(mag_hi)
+    gsx = gs - 127
+    assert ((gsx >= s_lo) & (gsx <= s_hi)).all(), "a scale byte lies outside its interval"
+    gscale = np.exp2(gsx.astype(np.float64))[..., None]
+    q_lo, q_hi = O.e4m3_round(lo_b / gscale), O.e4m3_round(hi_b / gscale)
+    got = O.e4m3_decode(gc.reshape(shp))
+    assert ((got >= q_lo) & (got <= q_hi)).all(), "a code lies outside its interval"
+    return int((s_lo != s_hi).sum()), int((q_lo != q_hi).sum())

@@ -84,17 +84,14 @@ def test_mxfp8_activation_bytes_match_oracle_quantiser(T):
     np.testing.assert_array_equal(g.atoms_to_rows(g.u8(layer.buffer("DY_ROWS_SCALES")), end, H), rs)
     np.testing.assert_array_equal(g.u8(layer.buffer("DY_ROWS"))[:end * H].reshape(end, H), rc)
 
-    # token-axis operands: x and dY gathered from the inputs, h.w, da, db from the bf16 rows the
-    # GEMM2 dgrad wrote; blocks of 32 rows start at every run (runs start at multiples of 128)
+    # token-axis operands x and dY, gathered from the inputs: blocks of 32 rows start at every
+    # run (runs start at multiples of 128)
     def tokens(name, C):
         c = g.u8(layer.buffer(name)).reshape(C, rp)[:, :end]
         s = g.atoms_to_rows(g.u8(layer.buffer(name + "_SCALES")), C, rp)[:, :end // 32]
         return c, s
 
-    for name, ref in (("X_TOKENS", Xpad), ("DY_TOKENS", Dpad),
-                      ("HW_TOKENS", g.bf16_rows(layer.buffer("HW"), end, F)),
-                      ("DA_TOKENS", g.bf16_rows(layer.buffer("DA"), end, F)),
-                      ("DB_TOKENS", g.bf16_rows(layer.buffer("DB"), end, F))):
+    for name, ref in (("X_TOKENS", Xpad), ("DY_TOKENS", Dpad)):
         c, s = tokens(name, ref.shape[1])
         rc, rs = O.mx_quantize(ref, 0)
         np.testing.assert_array_equal(s, rs.T, err_msg=name + " scales")
@@ -122,3 +119,18 @@ def test_mxfp8_activation_bytes_match_oracle_quantiser(T):
         # midpoint; at least 85 % of the codes are still decided and compared exactly
         und = g.check_mx_decided(c, s, ref, 1, rel=1e-4)
         assert und[1] < 0.15 * ref.size, (name, und)
+    # the same epilogue's da, db rounded to bf16 and quantised along the padded rows (blocks of
+    # 32 rows: a warp's rows), the dW1/dW3 operands
+    for name, ref in (("DA_TOKENS", da), ("DB_TOKENS", db)):
+        c, s = tokens(name, F)
+        und = g.check_mx_decided(c.T, s.T, ref, 0, rel=1e-4, bf16_values=True)
+        assert und[1] < 0.2 * ref.size, (name, und)
+    # and h.w, the dW2 operand: h = bf16(silu(a) b) recomputed from the saved a, b in fp32 (within
+    # 1e-5 of float64), w h rounded to bf16
+    dlt = 1e-5 * np.abs(h64)
+    wcol = wrow[:, None]
+    hw_lo = g.bf16_round(wcol * g.bf16_round(h64 - dlt))
+    hw_hi = g.bf16_round(wcol * g.bf16_round(h64 + dlt))
+    c, s = tokens("HW_TOKENS", F)
+    und = g.check_mx_interval(c.T, s.T, hw_lo, hw_hi, 0)
+    assert und[1] < 0.05 * hw_lo.size, ("HW_TOKENS", und)
