@@ -265,8 +265,15 @@ moe_status_t moe_reset_status(void *workspace, moe_stream_t stream);
  * "_SCALES" buffers hold E8M0 scale bytes in 512-byte atoms (128 rows x 128
  * elements of the contraction axis; atom (r/128, k/128) in row-major order,
  * byte (r%32)*16 + ((r/32)%4)*4 + (k/32)%4 inside it).
+ * Every kernel that follows ROW_SLOT or SLOT_ROW to a row checks the index
+ * against its range (a slot in [-1, T*k), a row inside the padded rows, in the
+ * combine inside the macrobatch's rows); an index outside it sets the device
+ * status to MOE_ERR_INTERNAL and the access is skipped, so a corrupted saved
+ * context is reported by moe_query_status instead of touching memory out of
+ * bounds.
  *   saved buffer (written by moe_forward):
- *     PADDED_OFFSETS int32 [nM*E+1]; ROW_SLOT int32 [rows]; A, B bf16 [rows][F]
+ *     PADDED_OFFSETS int32 [nM*E+1]; ROW_SLOT int32 [rows]; SLOT_ROW int32 [T*k]
+ *     (each routed slot's padded row); A, B bf16 [rows][F]
  *     in 32 x 32 blocks of 2 KB (block (r/32, c/32) row-major, element (r, c) at
  *     ((c%32)/8*32 + r%32)*8 + c%8 inside it).
  *   workspace, valid after moe_forward until the next call on the workspace
@@ -291,6 +298,7 @@ typedef enum {
     MOE_BUF_X_TOKENS, MOE_BUF_X_TOKENS_SCALES, MOE_BUF_DY_TOKENS, MOE_BUF_DY_TOKENS_SCALES,
     MOE_BUF_HW_TOKENS, MOE_BUF_HW_TOKENS_SCALES, MOE_BUF_DA_TOKENS, MOE_BUF_DA_TOKENS_SCALES,
     MOE_BUF_DB_TOKENS, MOE_BUF_DB_TOKENS_SCALES,
+    MOE_BUF_SLOT_ROW,
     MOE_BUF_COUNT
 } moe_buffer_t;
 

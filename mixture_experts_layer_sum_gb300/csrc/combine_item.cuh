@@ -8,9 +8,12 @@
 namespace moe {
 
 // it: item index within [t0, t1) x (H / 512 column chunks); nch = column chunks per token;
-// shift: ring row - padded row. Y is read with plain (coherent) loads: in the persistent
+// shift: ring row - padded row; [lo, hi): the padded rows of the macrobatch, the only rows
+// its slots may name (a slot row outside them raises MOE_ERR_INTERNAL and the slot is left
+// out, so no load leaves the ring). Y is read with plain (coherent) loads: in the persistent
 // forward it was written earlier in the same kernel.
-__device__ __forceinline__ void combine_item(const CombineArgs &a, int it, int nch, int shift, int lane) {
+__device__ __forceinline__ void combine_item(const CombineArgs &a, int it, int nch, int shift, int lo, int hi,
+                                             int lane) {
     const int vecs = a.H / 8;   // a multiple of 32
     const int t = a.t0 + it / nch;
     // two vectors per lane, rows in batches of 4: 8 loads of 16 B per lane in flight
@@ -26,17 +29,23 @@ __device__ __forceinline__ void combine_item(const CombineArgs &a, int it, int n
         int rows[4];
         float ws[4];
         uint4 y[2][4];
+        bool ok[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < 4; ++j) {
+            ok[j] = false;
             if (j < nj) {
-                rows[j] = a.slot_row[(size_t)t * a.k + j0 + j] + shift;
-                ws[j] = a.w[(size_t)t * a.k + j0 + j];
+                const int prow = a.slot_row[(size_t)t * a.k + j0 + j];
+                ok[j] = prow >= lo && prow < hi;
+                if (!ok[j] && lane == 0) raise_status(a.status, kStatusInternal);
+                rows[j] = ok[j] ? prow + shift : 0;
+                ws[j] = ok[j] ? a.w[(size_t)t * a.k + j0 + j] : 0.0f;
             }
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             if (j < nj) {
-                y[0][j] = ld_v4(a.Y + (size_t)rows[j] * a.H + v0 * 8);
-                if (two) y[1][j] = ld_v4(a.Y + (size_t)rows[j] * a.H + (v0 + 32) * 8);
+                y[0][j] = ok[j] ? ld_v4(a.Y + (size_t)rows[j] * a.H + v0 * 8) : make_uint4(0, 0, 0, 0);
+                if (two) y[1][j] = ok[j] ? ld_v4(a.Y + (size_t)rows[j] * a.H + (v0 + 32) * 8) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
         for (int p = 0; p < 2; ++p)

@@ -210,6 +210,15 @@ __device__ void init_tile_table(Ctl &c, const GemmArgs &g) {
 // CTAs can finish the gathering, so no CTA has to wait for another to start.
 // stop_bar (optional): the warp stops claiming once phase 0 of this mbarrier has
 // completed — the epilogue warps gather too until their CTA's first accumulator is ready.
+// A row's slot from row_slot, range-checked: one outside [-1, nslots) raises MOE_ERR_INTERNAL
+// (from lane 0 of the calling warp, or from each caller when lane is always 0) and the row is
+// taken as padding (-1), so no access follows it.
+__device__ __forceinline__ int checked_slot(const GemmArgs &g, int slot, int lane) {
+    if (slot >= -1 && slot < g.nslots) return slot;
+    if (lane == 0) raise_status(g.status, kStatusInternal);
+    return -1;
+}
+
 constexpr int kGatherRows = 4;
 // m: the macrobatch; ready: its per-minibatch ready counters (the claim counter follows them).
 template <bool FP8>
@@ -236,7 +245,7 @@ __device__ void gather_loop(const GemmArgs &g, int m, int *ready, const uint64_t
                 bf16 *dst[2];
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
-                    const int slot = g.row_slot[r + i];
+                    const int slot = checked_slot(g, g.row_slot[r + i], lane);
                     src[i] = slot >= 0 ? g.xsrc + (size_t)(slot / g.k) * g.H : nullptr;
                     dst[i] = g.ringx + (size_t)(g.x_global ? r + i : r + i - r0 + g.ring_base) * g.H;
                 }
@@ -260,7 +269,7 @@ __device__ void gather_loop(const GemmArgs &g, int m, int *ready, const uint64_t
             }
         } else {
             for (int r = rb; r < rb + kGatherRows; ++r) {
-                const int slot = g.row_slot[r];
+                const int slot = checked_slot(g, g.row_slot[r], lane);
                 const bf16 *src = slot >= 0 ? g.xsrc + (size_t)(slot / g.k) * g.H : nullptr;
                 const size_t drow = (size_t)(r - r0 + g.ring_base);
                 uint8_t *dst = g.ringxq + drow * g.H;
@@ -743,7 +752,7 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
         } else if constexpr (OP == OP_BWD2) {
             const int grow = ti.g0 + r;
             const size_t F = g.F;
-            const int slot = g.row_slot[grow];
+            const int slot = checked_slot(g, g.row_slot[grow], 0);
             const float w = slot >= 0 ? g.wslot[slot] : 0.0f;
             // saved a, b in 32 x 32 blocks: this lane's 16-byte vector j of chunk cc is
             // at blk32_offset(block row, column) + (j * 32 + lane) * 8 elements
@@ -1799,7 +1808,7 @@ __device__ void mega_gather_combine(const MegaArgs &a, const WaitCtl &ctl) {
     const int gw = blockIdx.x * 4 + (threadIdx.x / 32 - 6), nw = gridDim.x * 4;
     CombineArgs ca{};
     ca.Y = a.g2.o0; ca.slot_row = a.slot_row; ca.offp = g1.offp; ca.w = a.w; ca.out = a.out;
-    ca.k = g1.k; ca.H = g1.H; ca.E = g1.E; ca.ring_base = 0;
+    ca.k = g1.k; ca.H = g1.H; ca.E = g1.E; ca.ring_base = 0; ca.status = g1.status;
     const int nch = (g1.H / 8 + 63) / 64;
     for (int m = 0; m < g1.nM; ++m) {
         {
@@ -1816,7 +1825,8 @@ __device__ void mega_gather_combine(const MegaArgs &a, const WaitCtl &ctl) {
             ca.t0 = p * a.Mb;
             ca.t1 = min(a.T, ca.t0 + a.Mb);
             ca.m = p;
-            const int shift = -g1.offp[p * g1.E];
+            const int lo = g1.offp[p * g1.E], hi = g1.offp[(p + 1) * g1.E];
+            const int shift = -lo;
             const int items = a.meta[p * 4 + 3];
             (void)gw; (void)nw;
             for (;;) {
@@ -1824,7 +1834,7 @@ __device__ void mega_gather_combine(const MegaArgs &a, const WaitCtl &ctl) {
                 if (lane == 0) it = atomicAdd(a.cnt + (size_t)p * MEGA_NCNT + MEGA_COMBINE_CLAIM, 1);
                 it = __shfl_sync(0xffffffffu, it, 0);
                 if (it >= items) break;
-                combine_item(ca, it, nch, shift, lane);
+                combine_item(ca, it, nch, shift, lo, hi, lane);
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) red_release_gpu_add(a.cnt + (size_t)p * MEGA_NCNT + MEGA_COMBINED, 1);

@@ -37,6 +37,9 @@ struct GemmArgs {
     // 32-row blocks), the weight gradients' operands
     uint8_t *tq[3], *tqs[3];
     int tR;
+    // routed slots (T * k): a row's slot in row_slot lies in [-1, nslots); one outside raises
+    // MOE_ERR_INTERNAL in the status word and the row is treated as padding
+    int nslots;
     // FWD1 with the dispatch fused in (fused = 1): warps 6-9 of every CTA
     // claim 4-row chunks of the macrobatch from a counter, gather them into the
     // ring (bf16, or MXFP8 along H) and add the rows to ready[j] of their

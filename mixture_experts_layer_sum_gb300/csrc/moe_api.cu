@@ -435,6 +435,7 @@ GemmArgs gemm_base(const Layout &L, void *ws, const int32_t *offp, const moe_con
     g.E = L.E; g.nM = L.nM; g.H = L.H; g.F = L.F;
     g.status = at<int>(ws, L.w_status);
     g.budget_ns = budget_ns(c);
+    g.nslots = L.R;
     return g;
 }
 
@@ -521,6 +522,7 @@ moe_status_t moe_buffer_location(const moe_config_t *cfg, int which, int *in_sav
     switch (which) {
         case MOE_BUF_PADDED_OFFSETS: loc = {1, L.s_offp, 4 * ((size_t)L.nM * L.E + 1), false}; break;
         case MOE_BUF_ROW_SLOT: loc = {1, L.s_row_slot, 4 * rp, false}; break;
+        case MOE_BUF_SLOT_ROW: loc = {1, L.s_slot_row, 4 * (size_t)L.R, false}; break;
         case MOE_BUF_A: loc = {1, L.s_a, 2 * rp * F, false}; break;
         case MOE_BUF_B: loc = {1, L.s_b, 2 * rp * F, false}; break;
         case MOE_BUF_RING_X:
@@ -764,6 +766,7 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
         DispatchArgs d{};
         d.src = (const bf16 *)x; d.dst = xs; d.row_slot = s_row_slot; d.offp = s_offp;
         d.beg = 0; d.end = L.E; d.dst_row0 = 0; d.H = L.H; d.k = L.k;
+        d.nslots = L.R; d.status = at<int>(ws, L.w_status);
         {
             ProfScope ps("dispatch", s);
             st = cuda_check(launch_dispatch(d, L.rows_pad_max, L.num_sms, s), "dispatch launch");
@@ -778,6 +781,7 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
         CombineArgs ca{};
         ca.Y = ringY; ca.slot_row = s_slot_row; ca.offp = s_offp; ca.w = s_w; ca.out = (bf16 *)out;
         ca.t0 = 0; ca.t1 = L.T; ca.k = L.k; ca.H = L.H; ca.E = L.E; ca.m = 0; ca.ring_base = 0;
+        ca.status = at<int>(ws, L.w_status);
         ProfScope ps("combine", s);
         return cuda_check(launch_combine(ca, L.num_sms, s), "combine launch");
     }
@@ -867,6 +871,7 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
         CombineArgs ca{};
         ca.Y = ringY; ca.slot_row = s_slot_row; ca.offp = s_offp; ca.w = s_w; ca.out = (bf16 *)out;
         ca.t0 = (L.nM - 1) * L.Mb; ca.t1 = L.T; ca.k = L.k; ca.H = L.H; ca.E = L.E; ca.m = L.nM - 1; ca.ring_base = 0;
+        ca.status = at<int>(ws, L.w_status);
         ProfScope ps("combine", s);
         return cuda_check(launch_combine(ca, L.num_sms, s), "combine launch");
     }
@@ -889,6 +894,7 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
         ca.Y = ringY; ca.slot_row = s_slot_row; ca.offp = s_offp; ca.w = s_w; ca.out = (bf16 *)out;
         ca.t0 = m * L.Mb; ca.t1 = std::min(L.T, (m + 1) * L.Mb); ca.k = L.k; ca.H = L.H; ca.E = L.E; ca.m = m;
         ca.ring_base = ring_base;
+        ca.status = at<int>(ws, L.w_status);
         {
             ProfScope ps("combine", s);
             st = cuda_check(launch_combine(ca, L.num_sms, s), "combine launch");
@@ -942,6 +948,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
         DispatchArgs d2{};
         d2.src = (const bf16 *)dout; d2.dst = Gin; d2.row_slot = s_row_slot; d2.offp = s_offp;
         d2.beg = 0; d2.end = L.nM * L.E; d2.dst_row0 = 0; d2.H = L.H; d2.k = L.k;
+        d2.nslots = L.R; d2.status = at<int>(ws, L.w_status);
         {
             ProfScope ps("reverse_combine", s);
             st = cuda_check(launch_dispatch(d2, L.rows_pad_max, L.num_sms, s), "reverse combine launch");
@@ -1009,6 +1016,7 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
         a.src = src; a.codes = at<uint8_t>(ws, codes); a.scales = at<uint8_t>(ws, scales);
         if (rcodes) { a.rcodes = at<uint8_t>(ws, rcodes); a.rscales = at<uint8_t>(ws, rscales); }
         a.R = (int)rp; a.C = C; a.r_limit_ptr = s_offp + L.nM * L.E;
+        a.nslots = L.R; a.status = at<int>(ws, L.w_status);
         if (gather) {
             // experts visited in step (see MxTransposeArgs) so each token row is read once from HBM
             a.row_slot = s_row_slot; a.k = L.k;
@@ -1075,9 +1083,11 @@ moe_status_t moe_backward(const moe_config_t *cfg, const void *dout, const void 
     RouterBwdArgs rb{};
     rb.dw_part = dwpart; rb.nparts = L.F / 128; rb.slot_row = s_slot_row; rb.ids = s_ids; rb.w = s_w;
     rb.probs = s_probs; rb.dlogits = dlogits; rb.T = L.T; rb.k = L.k; rb.E = L.E;
+    rb.rows = L.rows_pad_max; rb.status = at<int>(ws, L.w_status);
     RevDispatchArgs rd{};
     rd.dXs = dXs; rd.slot_row = s_slot_row; rd.dlogits = dlogits; rd.Wr = (const bf16 *)W_r; rd.dx = (bf16 *)dx;
     rd.T = L.T; rd.k = L.k; rd.E = L.E; rd.H = L.H;
+    rd.rows = L.rows_pad_max; rd.status = at<int>(ws, L.w_status);
     RouterWgradArgs rw{};
     rw.x = (const bf16 *)x; rw.dlogits = dlogits; rw.part = at<float>(ws, L.w_dwr_part); rw.dWr = dW_r;
     rw.T = L.T; rw.H = L.H; rw.E = L.E; rw.splits = L.dwr_splits; rw.accumulate = accumulate;

@@ -186,7 +186,8 @@ __global__ void __launch_bounds__(128) mx_transpose_kernel(MxTransposeArgs a) {
         if (r < r_limit) {
             if (a.row_slot) {
                 const int slot = a.row_slot[r];
-                if (slot >= 0) tk = slot / a.k;
+                if (slot >= a.nslots || slot < -1) raise_status(a.status, kStatusInternal);
+                else if (slot >= 0) tk = slot / a.k;
             } else {
                 tk = r;
             }

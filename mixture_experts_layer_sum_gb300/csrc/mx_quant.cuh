@@ -38,6 +38,8 @@ struct MxTransposeArgs {
     const int32_t *offp;
     int ilv_E, ilv_nseg, ilv_jb;
     uint8_t *rcodes, *rscales;
+    int nslots;     // gather mode: a row's slot lies in [-1, nslots); one outside raises
+    int *status;    // MOE_ERR_INTERNAL here and the row is read as zeros
 };
 cudaError_t launch_mx_transpose(const MxTransposeArgs &a, int batch, cudaStream_t s);
 

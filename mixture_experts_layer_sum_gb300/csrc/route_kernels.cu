@@ -515,7 +515,8 @@ cudaError_t launch_schedule(const SchedArgs &a, cudaStream_t s) {
 // ------------------------------------------------------------------ dispatch
 
 // Warp per padded row r in [offp[beg], offp[end]): dst[dst_row0 + r - offp[beg]]
-// = src[row_slot[r] / k], zeros for padding rows. 16-byte loads and stores.
+// = src[row_slot[r] / k], zeros for padding rows. 16-byte loads and stores. A slot outside
+// [-1, nslots) raises MOE_ERR_INTERNAL and its row is written as zeros.
 __global__ void __launch_bounds__(256) dispatch_rows_kernel(DispatchArgs a) {
     pdl_wait();      // predecessor's outputs visible
     pdl_trigger();   // let the next kernel launch
@@ -525,7 +526,11 @@ __global__ void __launch_bounds__(256) dispatch_rows_kernel(DispatchArgs a) {
     const int r0 = a.offp[a.beg], r1 = a.offp[a.end];
     const int vecs = a.H / 8;
     for (int r = r0 + gw; r < r1; r += nw) {
-        const int slot = a.row_slot[r];
+        int slot = a.row_slot[r];
+        if (slot < -1 || slot >= a.nslots) {
+            if (lane == 0) raise_status(a.status, kStatusInternal);
+            slot = -1;
+        }
         bf16 *dst = a.dst + (size_t)(a.dst_row0 + r - r0) * a.H;
         if (slot < 0) {
             for (int v = lane; v < vecs; v += 32) st_v4(dst + v * 8, make_uint4(0, 0, 0, 0));
@@ -567,14 +572,15 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
     const int lane = threadIdx.x % 32;
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
     const int nw = gridDim.x * blockDim.x / 32;
-    const int shift = a.ring_base - a.offp[a.m * a.E];
+    const int lo = a.offp[a.m * a.E], hi = a.offp[(a.m + 1) * a.E];
+    const int shift = a.ring_base - lo;
     const int vecs = a.H / 8;   // a multiple of 32
     // work item = (token, 512 columns): a macrobatch with few tokens still spreads
     // over every warp, and each item is one or two rounds of loads
     const int nch = (vecs + 63) / 64;
     const int items = (a.t1 - a.t0) * nch;
     for (int it = gw; it < items; it += nw) {
-        combine_item(a, it, nch, shift, lane);
+        combine_item(a, it, nch, shift, lo, hi, lane);
     }
 }
 
@@ -605,7 +611,11 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(RouterBwdArgs a) {
     if (lane < a.k) {
         const int s = t * a.k + lane;
         const int row = a.slot_row[s];
-        for (int n = 0; n < a.nparts; ++n) dwj += a.dw_part[(size_t)row * a.nparts + n];
+        if (row >= 0 && row < a.rows) {
+            for (int n = 0; n < a.nparts; ++n) dwj += a.dw_part[(size_t)row * a.nparts + n];
+        } else {
+            raise_status(a.status, kStatusInternal);   // the slot's dw is left at 0
+        }
         wj = a.w[s];
         ej = a.ids[s];
         pj = a.probs[(size_t)t * a.E + ej];
@@ -685,7 +695,14 @@ __global__ void __launch_bounds__(128, 4) reverse_dispatch_kernel(RevDispatchArg
     const int half = lane & 1;
     int rows[32];
     const int kk = a.k < 32 ? a.k : 32;
-    for (int j = 0; j < kk; ++j) rows[j] = my_t < a.T ? a.slot_row[(size_t)my_t * a.k + j] : 0;
+    // a row outside [0, rows) raises MOE_ERR_INTERNAL and is skipped (-1)
+    auto checked_row = [&](int j) {
+        const int r = a.slot_row[(size_t)my_t * a.k + j];
+        if (r >= 0 && r < a.rows) return r;
+        raise_status(a.status, kStatusInternal);
+        return -1;
+    };
+    for (int j = 0; j < kk; ++j) rows[j] = my_t < a.T ? checked_row(j) : -1;
     for (int h0 = hb0; h0 < hb0 + 256; h0 += 64) {
         // W_r rows h0..h0+63, E values each, zero padded to 64 experts
         __syncthreads();
@@ -740,10 +757,10 @@ __global__ void __launch_bounds__(128, 4) reverse_dispatch_kernel(RevDispatchArg
                 for (int jj = 0; jj < 2; ++jj)
                     if (jj < nj) {
                         const int j = j0 + jj;
-                        const int row = j < 32 ? rows[j] : a.slot_row[(size_t)my_t * a.k + j];
-                        const bf16 *src = a.dXs + (size_t)row * a.H + hb;
+                        const int row = j < 32 ? rows[j] : checked_row(j);
+                        const bf16 *src = a.dXs + (size_t)(row < 0 ? 0 : row) * a.H + hb;
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) q[jj][u] = ld_v4(src + u * 8);
+                        for (int u = 0; u < 4; ++u) q[jj][u] = row < 0 ? make_uint4(0, 0, 0, 0) : ld_v4(src + u * 8);
                     }
 #pragma unroll
                 for (int jj = 0; jj < 2; ++jj)

@@ -41,6 +41,8 @@ struct DispatchArgs {
     int beg, end;           // rows [offp[beg], offp[end])
     int dst_row0;
     int H, k;
+    int nslots;             // T * k: a row's slot lies in [-1, nslots) (-1 = padding)
+    int *status;            // MOE_ERR_INTERNAL on an index outside its range (the row is zeroed)
 };
 cudaError_t launch_dispatch(const DispatchArgs &a, int max_rows, int num_sms, cudaStream_t s);
 
@@ -50,6 +52,7 @@ struct CombineArgs {
     const float *w;
     bf16 *out;
     int t0, t1, k, H, E, m, ring_base;
+    int *status;            // MOE_ERR_INTERNAL on a slot row outside macrobatch m (the slot is skipped)
 };
 cudaError_t launch_combine(const CombineArgs &a, int num_sms, cudaStream_t s);
 
@@ -60,6 +63,8 @@ struct RouterBwdArgs {
     const float *w, *probs;
     float *dlogits;         // [T, E]
     int T, k, E;
+    int rows;               // padded rows: a slot's row lies in [0, rows)
+    int *status;            // MOE_ERR_INTERNAL on a row outside it (the slot's dw is taken as 0)
 };
 struct RevDispatchArgs {
     const bf16 *dXs;        // [rows, H]
@@ -68,6 +73,8 @@ struct RevDispatchArgs {
     const bf16 *Wr;
     bf16 *dx;
     int T, k, E, H;
+    int rows;               // padded rows: a slot's row lies in [0, rows)
+    int *status;            // MOE_ERR_INTERNAL on a row outside it (the row is skipped)
 };
 struct RouterWgradArgs {
     const bf16 *x;

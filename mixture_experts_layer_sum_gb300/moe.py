@@ -37,7 +37,7 @@ BUFFERS = (
     "PADDED_OFFSETS", "ROW_SLOT", "A", "B", "RING_X", "RING_X_SCALES", "RING_H", "RING_H_SCALES",
     "DA", "DB", "HW", "DY_ROWS", "DY_ROWS_SCALES", "DA_ROWS", "DA_ROWS_SCALES", "DB_ROWS", "DB_ROWS_SCALES",
     "X_TOKENS", "X_TOKENS_SCALES", "DY_TOKENS", "DY_TOKENS_SCALES", "HW_TOKENS", "HW_TOKENS_SCALES",
-    "DA_TOKENS", "DA_TOKENS_SCALES", "DB_TOKENS", "DB_TOKENS_SCALES",
+    "DA_TOKENS", "DA_TOKENS_SCALES", "DB_TOKENS", "DB_TOKENS_SCALES", "SLOT_ROW",
 )
 
 

@@ -65,3 +65,46 @@ def test_schedule_reports_out_of_range_ids():
     valid = ids[(ids >= 0) & (ids < E)]
     np.testing.assert_array_equal(counts.cpu().numpy().reshape(-1), np.bincount(valid, minlength=E))
     layer.status()                          # cleared by the query
+
+
+@pytest.mark.parametrize("precision", ["bf16", "mxfp8"])
+@pytest.mark.parametrize("which,bad", [("ROW_SLOT", 1 << 30), ("ROW_SLOT", -7), ("SLOT_ROW", 1 << 30),
+                                       ("SLOT_ROW", -3)])
+def test_corrupted_saved_index_maps_are_reported(precision, which, bad):
+    # the forward's row<->slot maps in the saved context overwritten between forward and backward
+    # with indices outside their ranges: every backward kernel that follows them (the reverse
+    # combine gathers, the GEMM2 dgrad epilogue, the router backward, the reverse dispatch) checks
+    # the index, skips the access and reports MOE_ERR_INTERNAL; the same context then still runs
+    # the layer correctly
+    import numpy as np
+    import mixture_experts_layer_sum_gb300.moe as M
+    from mixture_experts_layer_sum_gb300.layer import MoeLayer
+    import tests.gpu_common as G
+    w = WL.TINY if precision == "bf16" else WL.Workload("mx_small", T=300, H=512, E=8, k=2, F=512,
+                                                            precision="mxfp8", zipf_s=0.8)
+    inp = WL.make_inputs(w)
+    d = G.device_inputs(inp)
+    layer = MoeLayer(w.T, w.H, w.F, w.E, w.k, w.precision)
+    if precision == "mxfp8":
+        layer.quantize_weights(d["W1"], d["W3"], d["W2"])
+    layer.forward(d["x"], d["Wr"], d["bias"], d["W1"], d["W3"], d["W2"])
+    layer.status()
+    torch.cuda.synchronize()
+    offp = layer.buffer("PADDED_OFFSETS").view(torch.int32).cpu().numpy()
+    m = layer.buffer(which).view(torch.int32)
+    if which == "ROW_SLOT":
+        e = int(np.nonzero(np.diff(offp[:w.E + 1]) > 0)[0][0])   # a run with rows
+        targets = [int(offp[e]), int(offp[e]) + 1]                 # its first two rows (real slots)
+    else:
+        targets = [0, w.T * w.k - 1]
+    for r in targets:
+        m[r] = bad
+    torch.cuda.synchronize()
+    layer.backward(d["dout"], d["x"], d["Wr"], d["W1"], d["W3"], d["W2"])
+    with pytest.raises(M.MoeError) as err:
+        layer.status()
+    assert err.value.status == M.MOE_ERR_INTERNAL
+    layer.status()                          # cleared by the query
+    del layer
+    gpu = G.run_gpu(w, inp)
+    G.check_layer(w, inp, gpu)
