@@ -818,15 +818,12 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                     // da, db quantised along F (blocks of 32) for the GEMM1 dgrad
                     const size_t col = (size_t)ti.nt * BN + cc * 32;
                     uint32_t q[8];
+                    // one sector per row (workspace buffers: 32-byte aligned)
                     uint32_t sb = mx_quant32(daf, q);
-                    uint4 *dq = reinterpret_cast<uint4 *>(g.q0 + (size_t)grow * F + col);
-                    dq[0] = make_uint4(q[0], q[1], q[2], q[3]);
-                    dq[1] = make_uint4(q[4], q[5], q[6], q[7]);
+                    st_global_32B(g.q0 + (size_t)grow * F + col, q);
                     g.qs0[mx_sf_offset(grow, col, F)] = (uint8_t)sb;
                     sb = mx_quant32(dbf, q);
-                    dq = reinterpret_cast<uint4 *>(g.q1 + (size_t)grow * F + col);
-                    dq[0] = make_uint4(q[0], q[1], q[2], q[3]);
-                    dq[1] = make_uint4(q[4], q[5], q[6], q[7]);
+                    st_global_32B(g.q1 + (size_t)grow * F + col, q);
                     g.qs1[mx_sf_offset(grow, col, F)] = (uint8_t)sb;
                     // the bf16 da, db and h.w quantised along the padded rows for dW1/dW3 and dW2
                     // (a warp's 32 rows are one block: runs start at multiples of 128 rows)
@@ -906,6 +903,17 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                     continue;
                 }
                 float *dst = (cc * 32 < ncol0) ? dst0 + cc * 32 : dst1 + (cc * 32 - ncol0);
+                if (!g.accumulate && (reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
+                    // whole 32-byte sectors: four 8-word stores of this row's 32 columns (the
+                    // caller's gradient may be only 16-byte aligned: then 16-byte stores below)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t w8[8] = {v[8 * q], v[8 * q + 1], v[8 * q + 2], v[8 * q + 3],
+                                                v[8 * q + 4], v[8 * q + 5], v[8 * q + 6], v[8 * q + 7]};
+                        st_global_32B(dst + q * 8, w8);
+                    }
+                    continue;
+                }
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     float4 o = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),

@@ -722,6 +722,15 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
                               s_row_slot);
     sa.ready = at<int>(ws, L.w_ready);   // GEMM1's per-minibatch counters of every macrobatch
     sa.ready_n = L.nM * (L.half_rows / kRowPad + 2);
+    // the counters of the kernel that follows: the decode kernel's claim and h counts, or the
+    // persistent forward's hand-off counters (zeroed by the scan: no memset in the chain)
+    if (L.decode) {
+        sa.zero[0] = at<int>(ws, L.w_decode);
+        sa.zero_n[0] = 1 + L.E;
+    } else if (cfg->forward_mode == MOE_FORWARD_PERSISTENT && L.T > 0) {
+        sa.zero[0] = at<int>(ws, L.w_mega_cnt);
+        sa.zero_n[0] = (int)(L.mega_zero_bytes / 4);
+    }
     {
         ProfScope ps("schedule", s);
         st = cuda_check(launch_schedule(sa, s), "schedule launch");
@@ -761,8 +770,6 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
             for (int i = 0; i < 3; ++i) { da.nv_codes[i] = nl.m[i].codes; da.nv_scales[i] = nl.m[i].scales; }
             da.nv_g = reinterpret_cast<const float *>(da.nvq + nl.gscale);
         }
-        st = cuda_check(cudaMemsetAsync(dc, 0, 4 * (1 + (size_t)L.E), s), "decode counters clear");
-        if (st != MOE_OK) return st;
         DispatchArgs d{};
         d.src = (const bf16 *)x; d.dst = xs; d.row_slot = s_row_slot; d.offp = s_offp;
         d.beg = 0; d.end = L.E; d.dst_row0 = 0; d.H = L.H; d.k = L.k;
@@ -854,8 +861,6 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
         ma.cnt = at<int>(ws, L.w_mega_cnt); ma.hready = at<int>(ws, L.w_mega_hready);
         ma.slot_row = s_slot_row; ma.w = s_w; ma.out = (bf16 *)out;
         ma.T = L.T; ma.Mb = L.Mb; ma.ready_stride = ready_stride;
-        st = cuda_check(cudaMemsetAsync(ma.cnt, 0, L.mega_zero_bytes, s), "persistent forward counters clear");
-        if (st != MOE_OK) return st;
         {
             ProfScope ps("forward_tile_list", s);
             st = cuda_check(launch_mega_list(s_offp, L.E, L.nM, L.F, L.H, L.T, L.Mb, list, meta, count, s),

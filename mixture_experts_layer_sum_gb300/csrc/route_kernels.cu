@@ -362,6 +362,9 @@ __global__ void __launch_bounds__(1024) schedule_scan_smem_kernel(SchedArgs a) {
     for (int i = threadIdx.x; i < ncc; i += blockDim.x) s_cc[i] = a.chunk_counts[i];
     if (a.ready)
         for (int i = threadIdx.x; i < a.ready_n; i += blockDim.x) a.ready[i] = 0;
+    for (int z = 0; z < 2; ++z)
+        if (a.zero[z])
+            for (int i = threadIdx.x; i < a.zero_n[z]; i += blockDim.x) a.zero[z][i] = 0;
     __syncthreads();
     for (int me = threadIdx.x; me < n; me += blockDim.x) {
         const int m = me / a.E, e = me % a.E;
@@ -424,6 +427,9 @@ __global__ void __launch_bounds__(1024) schedule_scan_kernel(SchedArgs a) {
     __shared__ int s_tot[64];
     if (a.ready)
         for (int i = threadIdx.x; i < a.ready_n; i += blockDim.x) a.ready[i] = 0;
+    for (int z = 0; z < 2; ++z)
+        if (a.zero[z])
+            for (int i = threadIdx.x; i < a.zero_n[z]; i += blockDim.x) a.zero[z][i] = 0;
     const int n = a.nM * a.E;
     // counts and chunk bases (relative to the (m,e) start); the chunk counts are
     // read eight at a time so their loads overlap

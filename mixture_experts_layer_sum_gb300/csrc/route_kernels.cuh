@@ -30,6 +30,10 @@ struct SchedArgs {
     int32_t *row_slot;      // optional [rows_pad_max] slot of each padded row
     int *ready;             // optional [ready_n] GEMM1 minibatch counters, zeroed by the scan
     int ready_n;
+    // optional further counter ranges the scan zeroes (the decode kernel's, the persistent
+    // forward's), so that no memset breaks the chain of programmatic launches
+    int *zero[2];
+    int zero_n[2];
     int *status;
 };
 cudaError_t launch_schedule(const SchedArgs &a, cudaStream_t s);
