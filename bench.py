@@ -249,10 +249,14 @@ def stop_clocks(p, path):
             "reasons": reasons, "samples": len(rows)}
 
 
-def kernel_bytes(w, name):
-    """Algorithmic HBM bytes per step of the memory-bound kernels."""
+def kernel_bytes(w, name, combine_tokens=None):
+    """Algorithmic HBM bytes per step of the memory-bound kernels. combine_tokens: tokens the
+    combine kernel itself handles (the persistent forward combines every macrobatch but the last
+    inside its own launch); None = all T."""
     T, H, F, R, E, k = w.T, w.H, w.F, w.R, w.E, w.k
     qh, qf = R * H * 33 // 32, R * F * 33 // 32   # one MXFP8 copy of R rows (codes + scales)
+    if name == "combine" and combine_tokens is not None:
+        T, R = combine_tokens, combine_tokens * k
     return {"decode_ffn": 3 * E * H * F * 2,   # every expert's weights streamed once (few tokens)
             "dispatch": T * H * 2 + R * H * 2, "dispatch_replay": T * H * 2 + R * H * 2,
             "dispatch_mxfp8": T * H * 2 + qh,
@@ -323,9 +327,16 @@ def layer_roofline(w, tf, hbm, step_ms):
             "note": "sum of GEMM flops / peak tensor rate and memory-stage algorithmic bytes / HBM copy bandwidth"}
 
 
-def rate_kernels(w, kernels, steps, prof_ms, peaks, peak_src, loop_s):
+def combine_tokens_of(w, plan):
+    """Tokens the combine kernel handles with the persistent forward: the last macrobatch's."""
+    nM, Mb = plan
+    return w.T - (nM - 1) * Mb
+
+
+def rate_kernels(w, kernels, steps, prof_ms, peaks, peak_src, loop_s, combine_tokens=None):
     """Per-kernel rates of a profiled run, the dominant kernel's roofline and the grouped GEMMs'
-    fraction of the tensor peak. kernels: [(name, launches, total ms)] over `steps` steps."""
+    fraction of the tensor peak. kernels: [(name, launches, total ms)] over `steps` steps.
+    combine_tokens: see kernel_bytes."""
     tf, tf_src = tensor_peak(w, peaks, peak_src, loop_s)
     hbm = peaks.get("hbm_gbs")
     kt = sorted(kernels, key=lambda r: -r[2])
@@ -336,7 +347,7 @@ def rate_kernels(w, kernels, steps, prof_ms, peaks, peak_src, loop_s):
             row["tflops"] = gemm_flops(w, nm) * steps / (ms_ * 1e-3) / 1e12
             row["frac_of_tensor_peak"] = row["tflops"] / tf
         if kernel_bytes(w, nm) and hbm:
-            row["gbs"] = kernel_bytes(w, nm) * steps / (ms_ * 1e-3) / 1e9
+            row["gbs"] = kernel_bytes(w, nm, combine_tokens) * steps / (ms_ * 1e-3) / 1e9
             row["frac_of_hbm"] = row["gbs"] / hbm
         rows.append(row)
     # dominant kernel: the largest share of the profiled step; a kernel may launch several
@@ -357,7 +368,7 @@ def rate_kernels(w, kernels, steps, prof_ms, peaks, peak_src, loop_s):
                                   "achieved_gbs": gb / (per_launch_ms * 1e-3) / 1e9,
                                   "frac_of_hbm": gb / (per_launch_ms * 1e-3) / 1e9 / hbm}
     elif kernel_bytes(w, name) is not None and hbm:
-        gb = kernel_bytes(w, name) / per_step
+        gb = kernel_bytes(w, name, combine_tokens) / per_step
         ach = gb / (per_launch_ms * 1e-3) / 1e9
         roof = {"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
                 "frac": ach / hbm, "traffic": committed_traffic(name, w.name), "algorithmic_per_launch": gb,
@@ -639,7 +650,9 @@ def run_ours(args, w):
             t_prof = timed(go, flush, go.step, args.steps)
             kern = M.moe_profile_end()
             go.layer.status(go.stream)
-            rows, roof_o, gg_o, tf_o = rate_kernels(wo, kern, args.steps, t_prof, *load_peaks(), t_step * 1e-3)
+            pl = go.layer.plan
+            rows, roof_o, gg_o, tf_o = rate_kernels(wo, kern, args.steps, t_prof, *load_peaks(), t_step * 1e-3,
+                                                    combine_tokens_of(wo, (pl.num_macrobatches, pl.macrobatch_tokens)))
             others.append({
                 "workload": wo.name, "precision": wo.precision, "T": wo.T, "H": wo.H, "F": wo.F, "E": wo.E,
                 "k": wo.k, "fwd_bwd": {"value": wo.T * args.steps / (t_step * 1e-3), "unit": "tokens/s",
@@ -667,7 +680,8 @@ def run_ours(args, w):
             dist.destroy_process_group()
         return
     peaks, peak_src = load_peaks()
-    rows, roof, gg, tf = rate_kernels(w, kernels, args.steps, prof_ms, peaks, peak_src, total_ms * 1e-3)
+    rows, roof, gg, tf = rate_kernels(w, kernels, args.steps, prof_ms, peaks, peak_src, total_ms * 1e-3,
+                                      combine_tokens_of(w, plan[:2]))
     value = job_tokens_per_s(ws, w.T, args.steps, total_ms)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
