@@ -661,9 +661,7 @@ __device__ __forceinline__ void epi_fwd1_tile(const GemmArgs &g, const TileInfo 
             const uint32_t sb = mx_quant32(hf, q);
             const size_t hrow = (size_t)(grow + ring_shift);
             const size_t col = (size_t)ti.nt * 128 + cc * 32;
-            uint4 *dq = reinterpret_cast<uint4 *>(g.q0 + hrow * F + col);
-            dq[0] = make_uint4(q[0], q[1], q[2], q[3]);
-            dq[1] = make_uint4(q[4], q[5], q[6], q[7]);
+            st_global_32B(g.q0 + hrow * F + col, q);   // one sector per row (the ring: 32-byte aligned)
             g.qs0[mx_sf_offset(hrow, col, F)] = (uint8_t)sb;
         }
     }
@@ -689,6 +687,12 @@ __device__ __forceinline__ void epi_rows_tile(const GemmArgs &g, const TileInfo 
         if (tma_bf16) {
             const int row0 = (int)(orow - r) + quarter * 32;
             stage_store_bf16<NBUF>(warp_stage, store_chunks, o, &g.om0, ti.nt * BN + cc * 32, row0, lane);
+        } else if ((reinterpret_cast<uintptr_t>(py) & 31) == 0) {
+            // straight from registers: two whole-sector stores per row chunk
+            const uint32_t w0[8] = {o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]};
+            const uint32_t w1[8] = {o[8], o[9], o[10], o[11], o[12], o[13], o[14], o[15]};
+            st_global_32B(py + cc * 32, w0);
+            st_global_32B(py + cc * 32 + 16, w1);
         } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -1770,7 +1774,9 @@ __device__ void mega_epilogue(const MegaArgs &a, CtlT<FP8 ? P8_STAGES : PSTAGES>
                 epi_fwd1_tile<FP8, NBUF>(g1, ti, tbase, r, quarter, lane, ring_shift, !FP8 && g1.tma_store, warp_stage,
                                          store_chunks);
             else
-                epi_rows_tile<OP_FWD2, NBUF>(g2, ti, tbase, r, quarter, lane, ring_shift, g2.tma_store != 0,
+                // MXFP8 Y rows straight from registers: the staged TMA store's chain (staging wait,
+                // proxy fence, warp sync) held up the single accumulator longer
+                epi_rows_tile<OP_FWD2, NBUF>(g2, ti, tbase, r, quarter, lane, ring_shift, !FP8 && g2.tma_store != 0,
                                              warp_stage, store_chunks);
         }
         tc_fence_before();
