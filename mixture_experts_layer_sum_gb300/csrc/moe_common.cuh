@@ -149,9 +149,15 @@ __device__ __forceinline__ void st_global_32B(void *p, const uint32_t (&w)[8]) {
 
 // Quantises 32 values held by one thread: 8 words of codes, returns the scale byte.
 __device__ __forceinline__ uint32_t mx_quant32(const float (&v)[32], uint32_t (&codes)[8]) {
-    float amax = 0.0f;
+    // block maximum as a pairwise tree (depth 5, not a chain of 32 dependent steps)
+    float m[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    for (int i = 0; i < 16; ++i) m[i] = fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1]));
+#pragma unroll
+    for (int n = 8; n >= 1; n /= 2)
+#pragma unroll
+        for (int i = 0; i < n; ++i) m[i] = fmaxf(m[i], m[i + n]);
+    const float amax = m[0];
     const int s = mx_exponent(amax);
     const float inv = mx_inv_scale(s);
 #pragma unroll
