@@ -766,7 +766,9 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
             bf16 *pda = g.o0 + grow * F + ti.nt * BN;
             bf16 *pdb = g.o1 + grow * F + ti.nt * BN;
             bf16 *phw = g.o2 + grow * F + ti.nt * BN;
-            float dwp = 0.0f;
+            // <G, h> over this warp's columns in four interleaved sums (column i % 4), added in a
+            // fixed order at the end: a chain a quarter as deep, the same result every run
+            float dwq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             constexpr int NCH = BN / 32 / (EW / 4);   // 32-column chunks of this warp
             const int cc0 = half * NCH, cc1 = cc0 + NCH;
             // saved a, b of the next 32 columns are loaded one chunk ahead so their
@@ -808,7 +810,7 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                         float sg = sigmoid_f(a);
                         float sl = a * sg;
                         float hval = __bfloat162float(__float2bfloat16_rn(sl * b));   // h as the forward stored it
-                        dwp = fmaf(G, hval, dwp);
+                        dwq[(2 * i + h2) & 3] = fmaf(G, hval, dwq[(2 * i + h2) & 3]);
                         float dh = w * G;
                         daf[2 * i + h2] = dh * b * sg * (1.0f + a * (1.0f - sg));
                         dbf[2 * i + h2] = dh * sl;
@@ -851,6 +853,7 @@ __device__ void epilogue_loop(const GemmArgs &g, const Ctl &c, const uint64_t *t
                     st_v4(phw + cc * 32 + q * 8, make_uint4(ohw[4 * q], ohw[4 * q + 1], ohw[4 * q + 2], ohw[4 * q + 3]));
                 }
             }
+            const float dwp = (dwq[0] + dwq[1]) + (dwq[2] + dwq[3]);
             // dw partials: one per 128 columns of F, [row][F / 128]
             float *dwo = g.of0 + (size_t)grow * (g.F / 128) + ti.nt * 2;
             if (EW == 8) {
