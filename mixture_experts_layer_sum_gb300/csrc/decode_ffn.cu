@@ -24,6 +24,7 @@
 #include <cuda_fp16.h>
 
 #include "decode_ffn.cuh"
+#include "nvfp4.cuh"
 
 namespace moe {
 
@@ -324,53 +325,90 @@ cudaError_t launch_decode_ffn(const DecodeArgs &a, int num_sms, cudaStream_t s) 
 }  // namespace moe
 
 // ======================================================================
-// NVFP4 expert weights (the format of nvfp4.cu): each weight tile (128 columns x 64 of K) is
-// 4 KB of E2M1 codes and 512 B of E4M3 block scales, so the forward streams about 4.5 bits per
-// weight instead of 16. Roles (320 threads): warp 0 claims items and streams the compressed
-// tiles by 1-D bulk copies through an 8-stage ring; warps 6-9 expand them to bf16 tiles in
-// shared memory (code -> f16 by cvt, times its block scale: exact in bf16, at most 7
-// significant bits), load the expert's token rows into the same stage and hand it to warp 1,
-// which issues the MMAs (now with K-major weights) into the double-buffered accumulator; warps
-// 2-5 run the epilogues, multiplying the fp32 accumulator by the power-of-two matrix scale
-// (exact) before the bf16 rounding. Hand-offs between items are the bf16 kernel's.
+// NVFP4 expert weights (the format of nvfp4.cu): every 128-column x 64-K weight tile is 4 KB of
+// E2M1 codes and 512 B of E4M3 block scales, so the forward streams 4.5 bits per weight instead
+// of 16. A stage covers 128 K: the expert's token rows (two 64-K halves of 32-row boxes, by TMA)
+// and the stage's weight tiles, one contiguous bulk copy (18 KB of W1 and W3, 9 KB of W2).
+// Roles (448 threads):
+//   warp 0 claims items and streams their stages through a ring of up to 8;
+//   warps 6-13 expand the codes to bf16 (code -> f16 by cvt, times its block scale: exact in
+//     bf16, at most 7 significant bits) straight into tensor memory, the MMA's A operand, one
+//     weight row per lane: two warps per lane quarter, one per 64-K half of the stage;
+//   warp 1 issues the MMAs (A = the expanded weights in tensor memory, B = the token rows in
+//     shared memory, K-major) into the accumulator;
+//   warps 2-5 run the epilogues, multiplying the fp32 accumulator by the power-of-two matrix
+//     scale (exact) before the bf16 rounding.
+// Tensor memory (512 columns): the accumulators first (two buffers of 2 x 64 columns while an
+// expert holds at most 64 rows, else one of 2 x 128), then two expanded stages of 128 columns
+// (64 per matrix) from column 256. Each weight element crosses into the tensor cores once, from
+// tensor memory, and shared memory carries only the compressed bytes and the few token rows.
+// Hand-offs between items are the bf16 kernel's.
 namespace moe {
 
 namespace {
 
 constexpr int NV_CMAX = 8;                               // compressed stages (at most)
-constexpr uint32_t NV_QTILE = 4096 + 512;                // codes + scales of one weight tile
-constexpr int NV_B = 3;                                  // expanded stages
-constexpr uint32_t NV_BSTAGE = 2 * DW_TILE;              // bf16 weight tiles (K-major)
-constexpr int NV_CONV_THREADS = 128;
-// compressed stage: the expert's token rows (nb boxes of 32 rows, 1 KB aligned for the
-// 128-byte swizzle) then the compressed W1 and W3 (or W2) tiles
-__host__ __device__ constexpr uint32_t nv_cstage(int nb) { return nb * DT_BOX + 2 * NV_QTILE; }
+constexpr int NV_AST = 2;                                // expanded stages in tensor memory
+constexpr uint32_t NV_ACOL0 = 256;                       // first tensor-memory column of the expanded stages
+constexpr uint32_t NV_ACOLS = 128;                       // columns of one expanded stage (64 per matrix)
+constexpr int NV_CONV_WARPS = 8;
+// compressed stage: the token boxes of K half 0, those of K half 1, then the weight tiles; every
+// part 1 KB aligned (32-row boxes of 4 KB; two or four tiles of 4.5 KB)
+__host__ __device__ constexpr uint32_t nv_tok_half(int nb) { return nb * DT_BOX; }
+__host__ __device__ constexpr uint32_t nv_cstage(int nb) { return 2 * nv_tok_half(nb) + 4 * kNvTile; }
 __host__ __device__ constexpr int nv_cstages(int nb) {
-    return (int)((DSMEM - NV_B * NV_BSTAGE) / nv_cstage(nb)) < NV_CMAX ? (int)((DSMEM - NV_B * NV_BSTAGE) / nv_cstage(nb))
-                                                                       : NV_CMAX;
+    return (int)(DSMEM / nv_cstage(nb)) < NV_CMAX ? (int)(DSMEM / nv_cstage(nb)) : NV_CMAX;
 }
-static_assert(nv_cstage(4) % 1024 == 0 && nv_cstage(1) % 1024 == 0, "1 KB aligned stages");
+static_assert(nv_cstage(1) % 1024 == 0 && (2 * kNvTile) % 1024 == 0, "1 KB aligned stages");
+static_assert(nv_cstages(4) >= 2, "at least two compressed stages for 128 tokens");
+// accumulator buffers, and the columns of one (the b accumulator of a GEMM1 item sits half
+// of them after its a): N = 32 * boxes <= 64 columns while nb <= 2, <= 128 above
+__host__ __device__ constexpr int nv_nacc(int nb) { return nb <= 2 ? 2 : 1; }
+__host__ __device__ constexpr uint32_t nv_acc_cols(int nb) { return nb <= 2 ? 128 : 256; }
+static_assert(2 * 128 <= NV_ACOL0 && 1 * 256 <= NV_ACOL0 && NV_ACOL0 + NV_AST * NV_ACOLS <= 512, "tensor memory plan");
+
+// 32 lanes x 32 consecutive 32-bit columns of tensor memory: thread i of the warp writes lane i
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem], bf16 inputs, fp32 accumulator, cta_group::1. A is K-major in
+// tensor memory: row m in lane m, K elements 2c and 2c + 1 in column c (low, high half).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 
 struct NvDecCtl {
-    uint64_t cfull[NV_CMAX], cempty[NV_CMAX], bfull[NV_B], bempty[NV_B], tfull[2], tempty[2], qfull[QD], qempty[QD],
-        drain;
+    uint64_t cfull[NV_CMAX], cempty[NV_CMAX], afull[NV_AST], aempty[NV_AST], tfull[2], tempty[2], qfull[QD],
+        qempty[QD], drain;
     uint32_t tmem_base;
     int item[QD];
 };
 
-// byte offset of the tile holding (column block, K block) of matrix mat of expert e
-__device__ __forceinline__ size_t nv_tile(const DecodeArgs &a, int mat, int e, int col0, int kb) {
-    const int K = mat == 2 ? a.F : a.H, N = mat == 2 ? a.H : a.F;
-    return ((size_t)e * (N / 128) + col0 / 128) * (K / 64) + kb;
-}
-
-// Streams every stage's token rows and compressed weight tiles; a compressed stage is freed by
-// the MMA thread once the tensor cores have read its token rows (its weights were expanded
-// before that), so the token copies run as far ahead as the compressed ring is deep.
+// Streams every stage's token rows and weight tiles; a compressed stage is freed by the MMA
+// thread once the tensor cores have read its token rows (its weights were expanded before).
 __device__ void nv_producer(const DecodeArgs &a, NvDecCtl &c, uint8_t *cring, const WaitCtl &ctl) {
     const int total = a.E * (a.F / 128 + a.H / 128);
     const int NC = nv_cstages(a.nb);
-    const uint32_t CS = nv_cstage(a.nb);
+    const uint32_t CS = nv_cstage(a.nb), TH = nv_tok_half(a.nb);
+    const int H = a.H, F = a.F;
+    const uint8_t *w13 = a.nvq + a.nv_w13, *w2 = a.nvq + a.nv_w2;
     int stage = 0, slot = 0;
     uint32_t phase = 0, qphase = 0, issued = 0, last_phase = 0;
     bool ok = true;
@@ -391,25 +429,26 @@ __device__ void nv_producer(const DecodeArgs &a, NvDecCtl &c, uint8_t *cring, co
         const Item it = decode_item(a, id);
         const int s0 = a.offp[it.e];
         const int nb = (a.counts[it.e] + 31) / 32;
+        // the item's operands in registers: the stage loop reads no kernel parameter
+        const CUtensorMap *tmap = it.gemm1 ? &a.x : &a.h;
+        const uint32_t wbytes = (it.gemm1 ? 4 : 2) * kNvTile;
+        const uint8_t *wsrc = it.gemm1 ? w13 + ((size_t)it.e * (F / 128) + it.col0 / 128) * (H / 128) * wbytes
+                                       : w2 + ((size_t)it.e * (H / 128) + it.col0 / 128) * (F / 128) * wbytes;
+        const uint32_t tx = 2 * nb * DT_BOX + wbytes;
+        const int ns = it.nk / 2;
         if (!it.gemm1) {
             // h of this expert: the four epilogue warps of every GEMM1 item of it have published
             if (!flag_wait_geq(a.hdone + it.e, 4 * (a.F / 128), ctl)) { ok = false; continue; }
             fence_proxy_async_global();
         }
-        for (int kb = 0; kb < it.nk && ok; ++kb) {
+        for (int ks = 0; ks < ns && ok; ++ks) {
             if (!mbar_wait(smem_u32(&c.cempty[stage]), phase ^ 1, ctl)) { ok = false; break; }
             const uint32_t bar = smem_u32(&c.cfull[stage]);
             const uint32_t sC = smem_u32(cring + stage * CS);
-            const int nmat = it.gemm1 ? 2 : 1;
-            mbar_arrive_expect_tx(bar, nb * DT_BOX + nmat * NV_QTILE);
-            for (int j = 0; j < nb; ++j) tma_load_2d(sC + j * DT_BOX, it.gemm1 ? &a.x : &a.h, bar, kb * 64, s0 + 32 * j);
-            const uint32_t sQ = sC + a.nb * DT_BOX;
-            for (int i = 0; i < nmat; ++i) {
-                const int mat = it.gemm1 ? i : 2;
-                const size_t t = nv_tile(a, mat, it.e, it.col0, kb);
-                bulk_load_1d(sQ + i * NV_QTILE, a.nvq + a.nv_codes[mat] + t * 4096, 4096, bar);
-                bulk_load_1d(sQ + i * NV_QTILE + 4096, a.nvq + a.nv_scales[mat] + t * 512, 512, bar);
-            }
+            mbar_arrive_expect_tx(bar, tx);
+            for (int hh = 0; hh < 2; ++hh)
+                for (int j = 0; j < nb; ++j) tma_load_2d(sC + hh * TH + j * DT_BOX, tmap, bar, (2 * ks + hh) * 64, s0 + 32 * j);
+            bulk_load_1d(sC + 2 * TH, wsrc + (size_t)ks * wbytes, wbytes, bar);
             issued |= 1u << stage;
             last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
             if (++stage == NC) { stage = 0; phase ^= 1; }
@@ -425,7 +464,8 @@ __device__ void nv_producer(const DecodeArgs &a, NvDecCtl &c, uint8_t *cring, co
 }
 
 // 8 E2M1 codes (one 32-bit word; element 2i in the low nibble of byte i) times their block
-// scale -> 8 bf16 (one 16-byte chunk); the matrix scale is applied to the accumulator
+// scale -> 8 bf16 packed in pairs (element 2i in the low half of word i); the matrix scale is
+// applied to the accumulator
 __device__ __forceinline__ uint4 nv_expand8(uint32_t codes, float scale) {
     uint32_t h[4];
     asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
@@ -451,13 +491,18 @@ __device__ __forceinline__ float nv_scale_value(uint32_t byte) {
     return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
 }
 
-__device__ void nv_converter(const DecodeArgs &a, NvDecCtl &c, uint8_t *bring, uint8_t *cring, const WaitCtl &ctl) {
-    const int t = threadIdx.x - 192;             // 0..127: the weight row (column of W) this thread expands
-    const int lane = threadIdx.x % 32;
+// Expands one 64-K half of every stage into tensor memory: lane = weight row (a column of W),
+// 32 columns of bf16 pairs per matrix.
+__device__ void nv_converter(const DecodeArgs &a, NvDecCtl &c, uint8_t *cring, uint32_t tmem, const WaitCtl &ctl) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int quarter = warp & 3;                    // the lane quarter this warp may access
+    const int half = (warp - 6) >> 2;                // warps 6-9: K half 0, warps 10-13: K half 1
+    const int t = quarter * 32 + lane;               // weight row = tensor-memory lane
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const int NC = nv_cstages(a.nb);
-    const uint32_t CS = nv_cstage(a.nb);
-    int slot = 0, cs = 0, bs = 0;
-    uint32_t qphase = 0, cphase = 0, bphase = 0;
+    const uint32_t CS = nv_cstage(a.nb), TH = nv_tok_half(a.nb);
+    int slot = 0, cs = 0, as = 0;
+    uint32_t qphase = 0, cphase = 0, aphase = 0;
     for (;;) {
         if (!mbar_wait(smem_u32(&c.qfull[slot]), qphase, ctl)) break;
         const int id = c.item[slot];
@@ -466,40 +511,50 @@ __device__ void nv_converter(const DecodeArgs &a, NvDecCtl &c, uint8_t *bring, u
         if (++slot == QD) { slot = 0; qphase ^= 1; }
         if (id < 0) break;
         const Item it = decode_item(a, id);
+        const int nmat = it.gemm1 ? 2 : 1;
         bool ok = true;
-        for (int kb = 0; kb < it.nk; ++kb) {
+        for (int ks = 0; ks < it.nk / 2; ++ks) {
             if (!mbar_wait(smem_u32(&c.cfull[cs]), cphase, ctl)) { ok = false; break; }
-            if (!mbar_wait(smem_u32(&c.bempty[bs]), bphase ^ 1, ctl)) { ok = false; break; }
-            uint8_t *sB = bring + bs * NV_BSTAGE;
-            const uint8_t *sQ = cring + cs * CS + a.nb * DT_BOX;
-            const int nmat = it.gemm1 ? 2 : 1;
+            if (!mbar_wait(smem_u32(&c.aempty[as]), aphase ^ 1, ctl)) { ok = false; break; }
+            tc_fence_after();
+            const uint8_t *sW = cring + cs * CS + 2 * TH;
             for (int i = 0; i < nmat; ++i) {
-                const uint4 q0 = *reinterpret_cast<const uint4 *>(sQ + i * NV_QTILE + t * 32);
-                const uint4 q1 = *reinterpret_cast<const uint4 *>(sQ + i * NV_QTILE + t * 32 + 16);
-                const uint32_t sb = *reinterpret_cast<const uint32_t *>(sQ + i * NV_QTILE + 4096 + t * 4);
+                const uint8_t *tile = sW + (i * 2 + half) * kNvTile;
+                const uint4 q0 = *reinterpret_cast<const uint4 *>(tile + t * 32);
+                const uint4 q1 = *reinterpret_cast<const uint4 *>(tile + t * 32 + 16);
+                const uint32_t sb = *reinterpret_cast<const uint32_t *>(tile + 4096 + t * 4);
                 const float sc[4] = {nv_scale_value(sb & 0xFFu), nv_scale_value((sb >> 8) & 0xFFu),
                                      nv_scale_value((sb >> 16) & 0xFFu), nv_scale_value(sb >> 24)};
                 const uint32_t w8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                uint8_t *row = sB + i * DW_TILE + t * 128;   // K-major, 128-byte swizzle
+                uint32_t r[32];
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                    *reinterpret_cast<uint4 *>(row + ((ch ^ (t & 7)) * 16)) = nv_expand8(w8[ch], sc[ch / 2]);
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint4 v = nv_expand8(w8[ch], sc[ch / 2]);
+                    r[4 * ch] = v.x;
+                    r[4 * ch + 1] = v.y;
+                    r[4 * ch + 2] = v.z;
+                    r[4 * ch + 3] = v.w;
+                }
+                tmem_st_32x32b_x32(tmem + lane_base + NV_ACOL0 + as * NV_ACOLS + i * 64 + half * 32, r);
             }
-            fence_proxy_async_shared();   // generic shared-memory writes, read by the tensor cores
-            mbar_arrive(smem_u32(&c.bfull[bs]));
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&c.afull[as]));
             if (++cs == NC) { cs = 0; cphase ^= 1; }
-            if (++bs == NV_B) { bs = 0; bphase ^= 1; }
+            if (++as == NV_AST) { as = 0; aphase ^= 1; }
         }
         if (!ok) break;
     }
 }
 
-__device__ void nv_mma(const DecodeArgs &a, NvDecCtl &c, uint8_t *bring, uint8_t *cring, uint32_t tmem,
-                       const WaitCtl &ctl) {
+__device__ void nv_mma(const DecodeArgs &a, NvDecCtl &c, uint8_t *cring, uint32_t tmem, const WaitCtl &ctl) {
     const int NC = nv_cstages(a.nb);
-    const uint32_t CS = nv_cstage(a.nb);
-    int bs = 0, cs = 0, slot = 0, acc = 0;
-    uint32_t bphase = 0, qphase = 0, acc_phase = 0;
+    const uint32_t CS = nv_cstage(a.nb), TH = nv_tok_half(a.nb);
+    const int nacc = nv_nacc(a.nb);
+    const uint32_t acols = nv_acc_cols(a.nb);
+    int as = 0, cs = 0, slot = 0, acc = 0;
+    uint32_t aphase = 0, qphase = 0, acc_phase = 0;
     for (;;) {
         if (!mbar_wait(smem_u32(&c.qfull[slot]), qphase, ctl)) break;
         const int id = c.item[slot];
@@ -507,45 +562,48 @@ __device__ void nv_mma(const DecodeArgs &a, NvDecCtl &c, uint8_t *bring, uint8_t
         if (++slot == QD) { slot = 0; qphase ^= 1; }
         if (id < 0) break;
         const Item it = decode_item(a, id);
-        const uint32_t idesc = idesc_bf16_f32(128, 32 * ((a.counts[it.e] + 31) / 32), false, false);   // both K-major
+        // M = 128 weight columns (A, K-major in tensor memory), N = the expert's rows rounded up
+        // to 32 (B, K-major token rows)
+        const uint32_t idesc = idesc_bf16_f32(128, 32 * ((a.counts[it.e] + 31) / 32), false, false);
         if (!mbar_wait(smem_u32(&c.tempty[acc]), acc_phase ^ 1, ctl)) break;
         tc_fence_after();
-        const uint32_t d = tmem + acc * 256;
+        const uint32_t d = tmem + acc * acols;
         bool ok = true;
-        for (int kb = 0; kb < it.nk; ++kb) {
+        for (int ks = 0; ks < it.nk / 2; ++ks) {
             // the converters arrive only after they saw the compressed stage (token rows included) land
-            if (!mbar_wait(smem_u32(&c.bfull[bs]), bphase, ctl)) { ok = false; break; }
+            if (!mbar_wait(smem_u32(&c.afull[as]), aphase, ctl)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t sB = smem_u32(bring + bs * NV_BSTAGE);
             const uint32_t sT = smem_u32(cring + cs * CS);
+            const uint32_t aw = tmem + NV_ACOL0 + as * NV_ACOLS;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bd = sdesc_sw128(sT + kk * 32, 16, 1024);
-                mma_bf16_ss(d, sdesc_sw128(sB + kk * 32, 16, 1024), bd, idesc, (kb | kk) != 0);
-                if (it.gemm1) mma_bf16_ss(d + 128, sdesc_sw128(sB + DW_TILE + kk * 32, 16, 1024), bd, idesc, (kb | kk) != 0);
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t bd = sdesc_sw128(sT + (kk >> 2) * TH + (kk & 3) * 32, 16, 1024);
+                mma_bf16_ts(d, aw + kk * 8, bd, idesc, (ks | kk) != 0);
+                if (it.gemm1) mma_bf16_ts(d + acols / 2, aw + 64 + kk * 8, bd, idesc, (ks | kk) != 0);
             }
-            mma_commit(smem_u32(&c.bempty[bs]));
+            mma_commit(smem_u32(&c.aempty[as]));
             mma_commit(smem_u32(&c.cempty[cs]));   // its token rows read: the compressed stage is free
-            if (++bs == NV_B) { bs = 0; bphase ^= 1; }
-            if (++cs == NC) { cs = 0; } 
+            if (++as == NV_AST) { as = 0; aphase ^= 1; }
+            if (++cs == NC) cs = 0;
         }
         if (!ok) break;
         mma_commit(smem_u32(&c.tfull[acc]));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+        if (++acc == nacc) { acc = 0; acc_phase ^= 1; }
     }
     mma_commit(smem_u32(&c.drain));
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(smem_u32(&c.drain), 0) && globaltimer_ns() - t0 < ctl.budget_ns) {}
 }
 
-// The bf16 decode epilogue with the matrix scales applied to the accumulator (16 columns at
-// a time: this kernel has 320 threads, so at most 168 registers each).
+// The decode epilogue with the matrix scales applied to the accumulator (16 columns at a time).
+// GEMM1 writes the h rows of the boxes the MMA computed, which are the rows GEMM2 reads.
 __device__ void nv_epilogue(const DecodeArgs &a, NvDecCtl &c, uint32_t tmem, const WaitCtl &ctl) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int quarter = warp & 3;
     const int col = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const int nacc = nv_nacc(a.nb);
+    const uint32_t acols = nv_acc_cols(a.nb);
     int slot = 0, acc = 0;
     uint32_t qphase = 0, acc_phase = 0;
     for (;;) {
@@ -558,30 +616,22 @@ __device__ void nv_epilogue(const DecodeArgs &a, NvDecCtl &c, uint32_t tmem, con
         const Item it = decode_item(a, id);
         if (!mbar_wait(smem_u32(&c.tfull[acc]), acc_phase, ctl)) break;
         tc_fence_after();
-        const uint32_t tbase = tmem + lane_base + acc * 256;
+        const uint32_t tbase = tmem + lane_base + acc * acols;
         const int s0 = a.offp[it.e];
         const int nb = (a.counts[it.e] + 31) / 32;
         if (it.gemm1) {
             const float g1 = a.nv_g[0 * a.E + it.e], g3 = a.nv_g[1 * a.E + it.e];
             const int f = it.col0 + col;
 #pragma unroll 1
-            for (int rc = 0; rc < 8; ++rc) {            // 16 rows at a time; rows past the blocks: zeros
+            for (int rc = 0; rc < 2 * nb; ++rc) {            // 16 rows at a time
                 uint32_t va[16], vb[16];
-                if (rc < 2 * nb) {
-                    tmem_ld_32x32b_x16(tbase + rc * 16, va);
-                    tmem_ld_32x32b_x16(tbase + 128 + rc * 16, vb);
-                    tmem_ld_wait();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) va[i] = vb[i] = 0u;
-                }
+                tmem_ld_32x32b_x16(tbase + rc * 16, va);
+                tmem_ld_32x32b_x16(tbase + acols / 2 + rc * 16, vb);
+                tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int row = s0 + rc * 16 + i;
-                    const bf16 ab = f2bf(__uint_as_float(va[i]) * g1), bb = f2bf(__uint_as_float(vb[i]) * g3);
-                    const float av = bf2f(ab), bv = bf2f(bb);
-                    a.a[blk32_elem(row, f, a.F)] = ab;
-                    a.b[blk32_elem(row, f, a.F)] = bb;
+                    const float av = bf2f(f2bf(__uint_as_float(va[i]) * g1)), bv = bf2f(f2bf(__uint_as_float(vb[i]) * g3));
                     a.hrows[(size_t)row * a.F + f] = f2bf(av * sigmoid_d(av) * bv);
                 }
             }
@@ -610,16 +660,14 @@ __device__ void nv_epilogue(const DecodeArgs &a, NvDecCtl &c, uint32_t tmem, con
                 red_release_gpu_add(a.hdone + it.e, 1);
             }
         }
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+        if (++acc == nacc) { acc = 0; acc_phase ^= 1; }
     }
 }
 
-__global__ void __launch_bounds__(320, 1) decode_nv_kernel(const __grid_constant__ DecodeArgs a) {
+__global__ void __launch_bounds__(448, 1) decode_nv_kernel(const __grid_constant__ DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *bring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *cring = bring + NV_B * NV_BSTAGE;   // 1 KB aligned: the token boxes come first in a stage
-    NvDecCtl &c = *reinterpret_cast<NvDecCtl *>(bring + DSMEM);
+    uint8_t *cring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    NvDecCtl &c = *reinterpret_cast<NvDecCtl *>(cring + DSMEM);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     WaitCtl ctl{a.status, a.budget_ns};
     if (threadIdx.x == 0) {
@@ -627,13 +675,13 @@ __global__ void __launch_bounds__(320, 1) decode_nv_kernel(const __grid_constant
             mbar_init(smem_u32(&c.cfull[s]), 1);
             mbar_init(smem_u32(&c.cempty[s]), 1);                  // the MMA thread's commit
         }
-        for (int s = 0; s < NV_B; ++s) {
-            mbar_init(smem_u32(&c.bfull[s]), NV_CONV_THREADS);       // every converter thread
-            mbar_init(smem_u32(&c.bempty[s]), 1);
+        for (int s = 0; s < NV_AST; ++s) {
+            mbar_init(smem_u32(&c.afull[s]), NV_CONV_WARPS);        // one lane of every converter warp
+            mbar_init(smem_u32(&c.aempty[s]), 1);
         }
         for (int q = 0; q < QD; ++q) {
             mbar_init(smem_u32(&c.qfull[q]), 1);
-            mbar_init(smem_u32(&c.qempty[q]), 1 + 4 + 4);   // MMA thread, epilogue and converter warps
+            mbar_init(smem_u32(&c.qempty[q]), 1 + 4 + NV_CONV_WARPS);   // MMA thread, epilogue and converter warps
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&c.tfull[i]), 1);
@@ -659,11 +707,11 @@ __global__ void __launch_bounds__(320, 1) decode_nv_kernel(const __grid_constant
     if (warp == 0) {
         if (lane == 0) nv_producer(a, c, cring, ctl);
     } else if (warp == 1) {
-        if (lane == 0) nv_mma(a, c, bring, cring, tmem, ctl);
+        if (lane == 0) nv_mma(a, c, cring, tmem, ctl);
     } else if (warp < 6) {
         nv_epilogue(a, c, tmem, ctl);
     } else {
-        nv_converter(a, c, bring, cring, ctl);
+        nv_converter(a, c, cring, tmem, ctl);
     }
     tc_fence_before();
     __syncthreads();
@@ -678,7 +726,7 @@ cudaError_t launch_decode_nv(const DecodeArgs &a, int num_sms, cudaStream_t s) {
     static_assert(smem <= 227 * 1024, "shared memory budget");
     cudaError_t err = cudaFuncSetAttribute(decode_nv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(decode_nv_kernel, dim3(num_sms), dim3(320), smem, s, a);
+    err = launch_pdl(decode_nv_kernel, dim3(num_sms), dim3(32 * (6 + NV_CONV_WARPS)), smem, s, a);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }

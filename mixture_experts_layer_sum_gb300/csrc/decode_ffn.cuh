@@ -25,15 +25,17 @@ struct DecodeArgs {
     int E, H, F;
     int *status;
     unsigned long long budget_ns;
-    // NVFP4 weights (launch_decode_nv): the nvfp4.cuh tiles of W1, W3, W2 and their matrix scales
+    // NVFP4 weights (launch_decode_nv): the nvfp4.cuh stages of W1 and W3 (offset nv_w13) and
+    // of W2 (nv_w2) inside nvq, and the matrix scales
     const uint8_t *nvq;
-    size_t nv_codes[3], nv_scales[3];
+    size_t nv_w13, nv_w2;
     const float *nv_g;    // [3][E]
 };
 
 cudaError_t launch_decode_ffn(const DecodeArgs &a, int num_sms, cudaStream_t s);
 // The same forward with NVFP4 expert weights (maps w1, w3, w2 unused): compressed tiles stream
-// from HBM and are expanded to bf16 in shared memory for the MMA.
+// from HBM and are expanded to bf16 in tensor memory, the MMA's A operand. Writes the h rows and
+// the expert outputs only (an NVFP4 layer has no backward, so a and b are not saved).
 cudaError_t launch_decode_nv(const DecodeArgs &a, int num_sms, cudaStream_t s);
 
 }  // namespace moe

@@ -767,7 +767,8 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const void *W_r
         if (nv) {
             const NvLayout nl = nv_layout(L.E, L.H, L.F);
             da.nvq = static_cast<const uint8_t *>(align_base(qweights));
-            for (int i = 0; i < 3; ++i) { da.nv_codes[i] = nl.m[i].codes; da.nv_scales[i] = nl.m[i].scales; }
+            da.nv_w13 = nl.w13;
+            da.nv_w2 = nl.w2;
             da.nv_g = reinterpret_cast<const float *>(da.nvq + nl.gscale);
         }
         DispatchArgs d{};

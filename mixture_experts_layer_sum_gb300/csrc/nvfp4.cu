@@ -13,17 +13,12 @@ namespace moe {
 
 NvLayout nv_layout(int E, int H, int F) {
     NvLayout L{};
-    const int K[3] = {H, H, F}, N[3] = {F, F, H};
+    const size_t tiles = (size_t)E * (H / 64) * (F / 128);   // tiles of W1 (or W3, or W2) over all experts
     size_t o = 0;
-    for (int i = 0; i < 3; ++i) {
-        const size_t n = (size_t)E * K[i] * N[i];
-        L.m[i].K = K[i];
-        L.m[i].N = N[i];
-        L.m[i].codes = o;
-        o = align_up(o + n / 2, 1024);
-        L.m[i].scales = o;
-        o = align_up(o + n / kNvBlock, 1024);
-    }
+    L.w13 = o;
+    o = align_up(o + 2 * tiles * kNvTile, 1024);
+    L.w2 = o;
+    o = align_up(o + tiles * kNvTile, 1024);
     L.gscale = o;
     o = align_up(o + 4 * 3 * (size_t)E, 1024);
     L.amax = o;
@@ -94,25 +89,25 @@ __device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
 
 // One block per (128-column x 64-K tile, expert, matrix). The tile is staged in shared memory
 // [64 K][128 columns]; thread t quantises column t % 128, K blocks 2 (t / 128) and 2 (t / 128) + 1.
-__global__ void __launch_bounds__(256) nv_quant_kernel(NvSrc src, uint8_t *base, NvLayout L, int E) {
+__global__ void __launch_bounds__(256) nv_quant_kernel(NvSrc src, uint8_t *base, NvLayout L, int E, int H, int F) {
     pdl_wait();
     pdl_trigger();
     __shared__ __align__(16) bf16 tile[64][128];
     const int mat = blockIdx.z, e = blockIdx.y;
-    const NvMatrix M = L.m[mat];
-    const int ktiles = M.K / 64;
+    const int K = mat < 2 ? H : F, N = mat < 2 ? F : H;
+    const int ktiles = K / 64;
     const int nt = blockIdx.x / ktiles, kt = blockIdx.x % ktiles;
-    const bf16 *w = src.w[mat] + (size_t)e * M.K * M.N;
+    const bf16 *w = src.w[mat] + (size_t)e * K * N;
     // 64 rows x 256 B, coalesced 16-byte loads
     for (int i = threadIdx.x; i < 64 * 16; i += blockDim.x) {
         const int r = i / 16, c = i % 16;
-        *reinterpret_cast<uint4 *>(&tile[r][c * 8]) = ld_nc_v4(w + (size_t)(kt * 64 + r) * M.N + nt * 128 + c * 8);
+        *reinterpret_cast<uint4 *>(&tile[r][c * 8]) = ld_nc_v4(w + (size_t)(kt * 64 + r) * N + nt * 128 + c * 8);
     }
     __syncthreads();
     const float amax = __uint_as_float(reinterpret_cast<const unsigned *>(base + L.amax)[mat * E + e]);
     const float g = nv_gscale(amax);
     const int col = threadIdx.x % 128, half = threadIdx.x / 128;
-    const size_t tile_id = ((size_t)e * (M.N / 128) + nt) * ktiles + kt;
+    uint8_t *t = base + nv_tile_offset(L, mat, e, nt, kt, H, F);
     uint32_t codes[4], sbytes = 0;
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
@@ -132,10 +127,8 @@ __global__ void __launch_bounds__(256) nv_quant_kernel(NvSrc src, uint8_t *base,
         codes[2 * b + 1] = sg > 0.0f ? e2m1x8(q[1]) : 0u;
         sbytes |= sb << (8 * b);
     }
-    uint8_t *cp = base + M.codes + tile_id * 4096 + col * 32 + half * 16;
-    *reinterpret_cast<uint4 *>(cp) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-    uint8_t *sp = base + M.scales + tile_id * 512 + col * 4 + half * 2;
-    *reinterpret_cast<uint16_t *>(sp) = (uint16_t)sbytes;
+    *reinterpret_cast<uint4 *>(t + col * 32 + half * 16) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+    *reinterpret_cast<uint16_t *>(t + 4096 + col * 4 + half * 2) = (uint16_t)sbytes;
     if (blockIdx.x == 0 && threadIdx.x == 0) reinterpret_cast<float *>(base + L.gscale)[mat * E + e] = g;
 }
 
@@ -151,7 +144,7 @@ cudaError_t launch_nv_quantize(const bf16 *W1, const bf16 *W3, const bf16 *W2, u
                    E, H, F);
     if (e != cudaSuccess) return e;
     // W1, W3 have (F/128)(H/64) tiles per expert, W2 (H/128)(F/64): the same count
-    e = launch_pdl(nv_quant_kernel, dim3((F / 128) * (H / 64), E, 3), dim3(256), 0, s, src, base, L, E);
+    e = launch_pdl(nv_quant_kernel, dim3((F / 128) * (H / 64), E, 3), dim3(256), 0, s, src, base, L, E, H, F);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -23,18 +23,28 @@ def G():
     return g
 
 
-def _matrices(E, H, F):
-    """(name, K, N) of the three quantised matrix sets and their byte offsets, in buffer order."""
+TILE = 4096 + 512   # one 128-column x 64-K tile: [128 rows][32 B] codes, then [128 rows][4 B] scales
+
+
+def _unpack(buf, E, H, F):
+    """(name, K, N, codes [E][N/128][K/64][128][32], scales [E][N/128][K/64][128][4]) of W1, W3, W2
+    and the byte offset of the matrix scales, read from the NVFP4 buffer: W1 and W3 interleaved
+    per 128-K stage ([E][F/128][H/128][W1 k, W1 k+64, W3 k, W3 k+64]), then W2
+    ([E][H/128][F/128][k, k+64]), each part 1 KB aligned."""
     a1024 = lambda v: -(-v // 1024) * 1024
-    out, o = [], 0
-    for name, K, N in (("W1", H, F), ("W3", H, F), ("W2", F, H)):
-        n = E * K * N
-        codes = o
-        o = a1024(o + n // 2)
-        scales = o
-        o = a1024(o + n // 16)
+    tiles = E * (H // 64) * (F // 128)
+    w13 = buf[:2 * tiles * TILE].reshape(E, F // 128, H // 128, 2, 2, TILE)
+    o = a1024(2 * tiles * TILE)
+    w2 = buf[o:o + tiles * TILE].reshape(E, H // 128, F // 64, TILE)
+    gs = a1024(o + tiles * TILE)
+    out = []
+    for name, K, N, t in (("W1", H, F, w13[:, :, :, 0].reshape(E, F // 128, H // 64, TILE)),
+                          ("W3", H, F, w13[:, :, :, 1].reshape(E, F // 128, H // 64, TILE)),
+                          ("W2", F, H, w2)):
+        codes = t[..., :4096].reshape(E, N // 128, K // 64, 128, 32)
+        scales = t[..., 4096:].reshape(E, N // 128, K // 64, 128, 4)
         out.append((name, K, N, codes, scales))
-    return out, o
+    return out, gs
 
 
 def test_nvfp4_weights_bit_exact():
@@ -47,15 +57,12 @@ def test_nvfp4_weights_bit_exact():
     layer.status()
     buf = layer.qweights.cpu().numpy()
     buf = buf[(-layer.qweights.data_ptr()) % 1024:]
-    mats, gs_off = _matrices(w.E, w.H, w.F)
+    mats, gs_off = _unpack(buf, w.E, w.H, w.F)
     g_all = buf[gs_off:gs_off + 12 * w.E].view(np.float32).reshape(3, w.E)
-    for mi, (name, K, N, co, so) in enumerate(mats):
+    for mi, (name, K, N, packed, sc) in enumerate(mats):
         W = O.bf16_to_f64(inp[name])
-        n = w.E * K * N
-        packed = buf[co:co + n // 2].reshape(w.E, N // 128, K // 64, 128, 32)
         nib = np.stack([packed & 15, packed >> 4], axis=-1).reshape(w.E, N // 128, K // 64, 128, 64)
         codes = nib.transpose(0, 2, 4, 1, 3).reshape(w.E, K, N)          # [e][k][n]
-        sc = buf[so:so + n // 16].reshape(w.E, N // 128, K // 64, 128, 4)
         scales = sc.transpose(0, 2, 4, 1, 3).reshape(w.E, K // 16, N)
         for e in range(w.E):
             rc, rs, rg = O.nv_quantize(W[e], 0)
