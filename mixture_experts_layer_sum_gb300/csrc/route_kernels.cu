@@ -48,8 +48,11 @@ constexpr int kRouterWarps = 8;     // warps split H
 // The contraction order inside a warp is permuted (thread c of a quad loads 8
 // consecutive h with one 16-byte load and feeds them as its k-slots of two
 // m16n8k16 steps); A and B use the same permutation, so the sum is exact in
-// structure and fixed in order.
-template <int NT>
+// structure and fixed in order. PF = 32-h steps loaded ahead of the MMAs: 1 when
+// the grid fills the GPU, deeper for the few blocks of a small batch, whose warps
+// would otherwise wait out one memory round trip per step. The MMAs run in the
+// same order either way, so the logits do not depend on PF.
+template <int NT, int PF>
 __global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a) {
     pdl_wait();      // predecessor's outputs visible
     pdl_trigger();   // let the next kernel launch
@@ -78,7 +81,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a) {
             valid[mt][hh] = t < a.T;
             xrow[mt][hh] = a.x + (size_t)(valid[mt][hh] ? t : 0) * a.H;
         }
-    // 32 h per step; the loads of step i+1 are issued before the MMAs of step i
+    // 32 h per step; the loads of step i+PF are issued right after the MMAs of step i
     auto load = [&](int h0, uint4 (&xv)[kRouterMT][2], uint4 (&wv)[NT]) {
         const int hc = h0 + 8 * c;
 #pragma unroll
@@ -102,16 +105,20 @@ __global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a) {
             }
         }
     };
-    const int hend = hbeg + hspan;   // hspan is a multiple of 32
-    uint4 xa[kRouterMT][2], wa[NT], xb[kRouterMT][2], wb[NT];
-    load(hbeg, xa, wa);
-    for (int h0 = hbeg; h0 < hend; h0 += 64) {
-        const bool second = h0 + 32 < hend;
-        if (second) load(h0 + 32, xb, wb);
-        step(xa, wa);
-        if (second) {
-            if (h0 + 64 < hend) load(h0 + 64, xa, wa);
-            step(xb, wb);
+    const int nsteps = hspan / 32;   // hspan is a multiple of 32
+    uint4 xv[PF + 1][kRouterMT][2], wv[PF + 1][NT];
+#pragma unroll
+    for (int j = 0; j < PF; ++j)
+        if (j < nsteps) load(hbeg + 32 * j, xv[j], wv[j]);
+    // PF + 1 slots, so the load for step i + PF never overwrites the operands of step i
+    for (int i0 = 0; i0 < nsteps; i0 += PF + 1) {
+#pragma unroll
+        for (int j = 0; j <= PF; ++j) {
+            const int i = i0 + j;
+            if (i < nsteps) {
+                if (i + PF < nsteps) load(hbeg + 32 * (i + PF), xv[(j + PF) % (PF + 1)], wv[(j + PF) % (PF + 1)]);
+                step(xv[j], wv[j]);
+            }
         }
     }
     // partial logits of this warp -> shared memory
@@ -203,12 +210,14 @@ cudaError_t launch_router(const RouterArgs &a, cudaStream_t s) {
     cudaError_t le = launch_pdl(transpose_wr_kernel, dim3(ceil_div(a.H * EP, 256)), dim3(256), 0, s, a.Wr, a.WrT, a.H, a.E, EP);
     if (le != cudaSuccess) return le;
     if (blocks == 0) return cudaGetLastError();
+    // a batch of up to 64 blocks (1024 tokens) leaves most SMs idle: load four steps ahead
+    const bool deep = blocks <= 64;
 #define MOE_ROUTER_CASE(NT)                                                                           \
     case NT: {                                                                                       \
-        cudaError_t e = cudaFuncSetAttribute(router_topk_kernel<NT>,                                 \
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+        auto *kern = deep ? router_topk_kernel<NT, 4> : router_topk_kernel<NT, 1>;                   \
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
         if (e != cudaSuccess) return e;                                                              \
-        e = launch_pdl(router_topk_kernel<NT>, dim3(blocks), dim3(256), smem, s, a);                 \
+        e = launch_pdl(kern, dim3(blocks), dim3(256), smem, s, a);                                   \
         if (e != cudaSuccess) return e;                                                              \
         break;                                                                                       \
     }

@@ -65,3 +65,13 @@ def test_decode_deterministic():
     b = G().run_gpu(w, inp)
     for key in ("out", "dx", "dWr", "dW1", "dW3", "dW2"):
         np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+
+
+@pytest.mark.parametrize("base", [WL.BALANCED, WL.SKEWED])
+def test_router_does_not_depend_on_batch_size(base):
+    # a batch of a few router blocks loads four steps ahead, a full one a single step; the MMAs
+    # run in the same order, so the first 64 tokens get bitwise the same ids and weights
+    small = G().run_gpu(base.with_(T=64), WL.make_inputs(base, tokens=64), backward=False)
+    full = G().run_gpu(base, WL.make_inputs(base), backward=False)
+    np.testing.assert_array_equal(small["ids"], full["ids"][:64])
+    np.testing.assert_array_equal(small["w"], full["w"][:64])
