@@ -512,8 +512,96 @@ __global__ void __launch_bounds__(kSchedWarps * 32) schedule_scatter_kernel(Sche
     chunk_pass<true>(a, blockIdx.x, s_cnt, s_base);
 }
 
+// The whole schedule in one block when every slot sits in one macrobatch of at most
+// kSchedSingleChunks chunks (a small batch, where three launches would cost more than the
+// work): the count pass of every chunk, the scans over the experts by one warp, then the
+// scatter pass of every chunk. The passes and the layout are those of the three kernels.
+constexpr int kSchedSingleChunks = 8;
+__global__ void __launch_bounds__(kSchedWarps * 32) schedule_single_kernel(SchedArgs a) {
+    pdl_wait();      // predecessor's outputs visible
+    pdl_trigger();   // let the next kernel launch
+    __shared__ int s_cnt[kSchedWarps * kMaxExperts];
+    __shared__ int s_cc[kSchedSingleChunks * kMaxExperts];   // chunk counts, then bases inside the expert's run
+    __shared__ int s_start[kMaxExperts], s_num[kMaxExperts], s_offp[kMaxExperts + 1], s_base[kMaxExperts];
+    const int E = a.E, warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (a.ready)
+        for (int i = threadIdx.x; i < a.ready_n; i += blockDim.x) a.ready[i] = 0;
+    for (int z = 0; z < 2; ++z)
+        if (a.zero[z])
+            for (int i = threadIdx.x; i < a.zero_n[z]; i += blockDim.x) a.zero[z][i] = 0;
+    for (int c = 0; c < a.nchunks; ++c) {
+        chunk_pass<false>(a, c, s_cnt, nullptr);   // ends at a block barrier
+        if (threadIdx.x < E) {
+            int v = 0;
+            for (int w = 0; w < kSchedWarps; ++w) v += s_cnt[w * E + threadIdx.x];
+            s_cc[c * E + threadIdx.x] = v;
+        }
+        __syncthreads();   // the next pass clears s_cnt
+    }
+    if (warp == 0) {
+        // expert e = lane + 32 s: its count, the chunk bases inside its run, and exclusive scans
+        // over the experts in index order (lanes for s = 0, then lanes for s = 1)
+        int cnt[2], pad[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int e = lane + 32 * q;
+            cnt[q] = 0;
+            if (e < E)
+                for (int c = 0; c < a.nchunks; ++c) {
+                    const int v = s_cc[c * E + e];
+                    s_cc[c * E + e] = cnt[q];
+                    cnt[q] += v;
+                }
+            pad[q] = (cnt[q] + kRowPad - 1) / kRowPad * kRowPad;
+        }
+        int off = 0, offp = 0;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            int x = cnt[q], y = pad[q];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int tx = __shfl_up_sync(0xffffffffu, x, o), ty = __shfl_up_sync(0xffffffffu, y, o);
+                if (lane >= o) { x += tx; y += ty; }
+            }
+            const int e = lane + 32 * q;
+            if (e < E) {
+                s_num[e] = cnt[q];
+                s_start[e] = off + x - cnt[q];
+                s_offp[e] = offp + y - pad[q];
+                a.counts[e] = cnt[q];
+                a.offsets[e] = s_start[e];
+                a.offp[e] = s_offp[e];
+            }
+            off += __shfl_sync(0xffffffffu, x, 31);
+            offp += __shfl_sync(0xffffffffu, y, 31);
+        }
+        if (lane == 0) {
+            a.offsets[E] = off;
+            a.offp[E] = offp;
+            s_offp[E] = offp;
+        }
+    }
+    __syncthreads();
+    if (a.row_slot) {   // padding rows of every expert's run hold no slot: 128 candidates per run
+        for (int i = threadIdx.x; i < E * kRowPad; i += blockDim.x) {
+            const int e = i / kRowPad, r = s_offp[e] + s_num[e] + i % kRowPad;
+            if (r < s_offp[e + 1]) a.row_slot[r] = -1;
+        }
+    }
+    for (int c = 0; c < a.nchunks; ++c) {
+        if (threadIdx.x < E) s_base[threadIdx.x] = s_start[threadIdx.x] + s_cc[c * E + threadIdx.x];
+        __syncthreads();
+        chunk_pass<true>(a, c, s_cnt, s_base);
+        __syncthreads();   // the next chunk rewrites s_base and s_cnt
+    }
+}
+
 cudaError_t launch_schedule(const SchedArgs &a, cudaStream_t s) {
     cudaError_t e = cudaSuccess;
+    if (a.nM == 1 && a.nchunks >= 1 && a.nchunks <= kSchedSingleChunks) {
+        if ((e = launch_pdl(schedule_single_kernel, dim3(1), dim3(kSchedWarps * 32), 0, s, a)) != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     if (a.nchunks > 0 && (e = launch_pdl(schedule_count_kernel, dim3(a.nchunks), dim3(kSchedWarps * 32), 0, s, a)) != cudaSuccess)
         return e;
     const size_t scan_smem = schedule_scan_smem_bytes(a);

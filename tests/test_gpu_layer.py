@@ -103,7 +103,9 @@ def test_determinism_bitwise():
 def test_schedule_bit_exact():
     from mixture_experts_layer_sum_gb300.layer import MoeLayer
     rng = np.random.default_rng(0)
-    for T, E, k, Mb in [(4096, 32, 4, 0), (1000, 64, 8, 300), (3, 8, 2, 0), (16384, 16, 8, 2000), (2049, 7, 3, 0)]:
+    # the last three fit one macrobatch of at most eight 256-slot chunks: the one-block schedule
+    for T, E, k, Mb in [(4096, 32, 4, 0), (1000, 64, 8, 300), (3, 8, 2, 0), (16384, 16, 8, 2000), (2049, 7, 3, 0),
+                        (64, 32, 4, 0), (100, 7, 3, 0), (256, 64, 8, 0)]:
         # skewed ids: each token picks k distinct experts, Zipf-weighted
         pr = (np.arange(1, E + 1) ** -1.2); pr /= pr.sum()
         ids = np.stack([rng.choice(E, size=k, replace=False, p=pr) for _ in range(T)]).astype(np.int32)
