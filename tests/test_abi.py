@@ -173,3 +173,16 @@ def test_ring_holds_one_macrobatch(moe):
         assert p.macrobatch_tokens * k + pad <= cap < (p.macrobatch_tokens + 1) * k + pad, prec
         assert p.ring_bytes <= 256 << 20
         assert p.num_macrobatches == -(-16384 // p.macrobatch_tokens)
+
+
+def test_nvfp4_weight_buffer_holds_the_stage_layout(moe):
+    # W1 and W3 interleaved per 128-K stage, then W2, then the matrix scales and the quantiser's
+    # maxima, each part 1 KB aligned; a tile (128 columns x 64 K) is 4096 code and 512 scale bytes
+    a1024 = lambda v: -(-v // 1024) * 1024
+    for E, H, F in [(32, 2048, 1024), (4, 256, 512), (64, 7168, 2048)]:
+        tiles = E * (H // 64) * (F // 128)
+        w2 = a1024(2 * tiles * 4608)
+        gscale = a1024(w2 + tiles * 4608)
+        end = a1024(a1024(gscale + 12 * E) + 12 * E)
+        size = moe.moe_qweights_size(moe.make_config(64, H, F, E, 4, "nvfp4"))
+        assert end <= size <= end + 1024, (E, H, F, size, end)
