@@ -339,9 +339,10 @@ cudaError_t launch_decode_ffn(const DecodeArgs &a, int num_sms, cudaStream_t s) 
 //   warps 2-5 run the epilogues, multiplying the fp32 accumulator by the power-of-two matrix
 //     scale (exact) before the bf16 rounding.
 // Tensor memory (512 columns): the accumulators first (two buffers of 2 x 64 columns for a batch
-// of at most 64 tokens, which no expert can exceed; else one of 2 x 128), then two expanded stages of 128 columns
-// (64 per matrix) from column 256. Each weight element crosses into the tensor cores once, from
-// tensor memory, and shared memory carries only the compressed bytes and the few token rows.
+// of at most 64 tokens, which no expert can exceed; else one of 2 x 128), then two expanded
+// stages of 128 columns (64 per matrix) from column 256. Each weight element crosses into the
+// tensor cores once, from tensor memory, and shared memory carries only the compressed bytes and
+// the few token rows.
 // Hand-offs between items are the bf16 kernel's.
 namespace moe {
 
